@@ -1,0 +1,323 @@
+"""Pins of the fp64 oracle: checks against what the pages and mathematics fix.
+
+Each ``check_*`` takes an oracle library handle and raises AssertionError when
+the oracle disagrees with the pinned fact.  ``tests/test_oracle_pins.py`` runs
+them against the real oracle; ``tests/test_oracle_mutations.py`` runs them
+against deliberately broken copies of the oracle (planted on the CPU) and
+requires every planted mistake to be caught by at least one check.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+
+import oracle
+from paged_kv_cache_95_gb300 import workloads as W
+from brute_force import dense_attention
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+TOL = 1e-12
+
+
+def _bits(x):
+    return W.bf16_bits_from_f32(np.asarray(x, dtype=np.float32))
+
+
+def _appended(wl, lib):
+    return oracle.kv_reshape_and_cache(wl.new_key, wl.new_value, wl.k_cache, wl.v_cache,
+                                       wl.slot_mapping, lib=lib)
+
+
+def _attn(wl, batch, kc, vc, lib, **kw):
+    return oracle.paged_attention(batch.q, batch.cu_q_lens, kc, vc, batch.block_tables,
+                                  batch.context_lens, wl.scale, n_q=wl.n_q, lib=lib, **kw)
+
+
+def _vs_brute(wl, batch, lib, tol=TOL):
+    kc, vc = _appended(wl, lib)
+    got = _attn(wl, batch, kc, vc, lib)
+    ref = dense_attention(batch.q, batch.cu_q_lens, batch.logical_k, batch.logical_v, wl.scale, wl.n_q)
+    err = np.max(np.abs(got - ref))
+    assert np.all(np.isfinite(got)), "oracle produced non-finite output"
+    assert err <= tol, f"oracle vs contiguous brute force: max abs err {err:.3e}"
+
+
+# ---- sizes and index rules ---------------------------------------------------
+
+def check_kv_sizes(lib):
+    with open(os.path.join(GOLDEN, "kv_sizes.json")) as f:
+        g = json.load(f)
+    per_token = []
+    for c in g["cases"]:
+        got = oracle.kv_bytes_per_token(c["layers"], c["n_kv"], c["head_dim"], c["dtype_size"], lib=lib)
+        assert got == c["bytes"], f"{c['what']}: {got} != {c['bytes']}"
+        per_token.append(got)
+    for p in g["products"]:
+        got = per_token[p["per_token_case"]] * p["tokens"]
+        assert got == p["bytes"], f"{p['what']}: {got} != {p['bytes']}"
+    for e in g["elements"]:
+        got = oracle.kv_bytes_per_token(1, e["n_kv"], e["head_dim"], 1, lib=lib)
+        assert got == e["elements"], f"{e['what']}: {got} != {e['elements']}"
+
+
+def check_kv_groups(lib):
+    with open(os.path.join(GOLDEN, "kv_groups.json")) as f:
+        g = json.load(f)
+    for grp, heads in g["groups"].items():
+        for h in heads:
+            assert oracle.kv_group(h, g["n_q"], g["n_kv"], lib=lib) == int(grp), (h, grp)
+    # MHA: identity; MQA: all heads read group 0.
+    for h in range(32):
+        assert oracle.kv_group(h, 32, 32, lib=lib) == h
+        assert oracle.kv_group(h, 32, 1, lib=lib) == 0
+
+
+def check_slot_rule(lib):
+    table = np.array([7, 3, 11], dtype=np.int32)
+    for pos, want in [(0, 7 * 16), (15, 7 * 16 + 15), (16, 3 * 16), (40, 11 * 16 + 8)]:
+        assert oracle.slot_of(table, pos, 16, lib=lib) == want, (pos, want)
+
+
+# ---- cache write ---------------------------------------------------------------
+
+def check_cache_write_roundtrip(lib):
+    """Write through slot_mapping, read back through the block table: bit-exact."""
+    wl, batch = W.make_custom(32, 8, [10, 17, 33, 48], q_lens=[1, 1, 16, 5], seed=3)
+    kc, vc = _appended(wl, lib)
+    rows = 0
+    for b in range(batch.num_seqs):
+        ctx, ql = int(batch.context_lens[b]), int(batch.q_lens[b])
+        for r in range(ql):
+            pos = ctx - ql + r
+            blk = batch.block_tables[b, pos // 16]
+            assert np.array_equal(kc[blk, :, pos % 16, :], wl.new_key[rows]), (b, r)
+            assert np.array_equal(vc[blk, :, pos % 16, :], wl.new_value[rows]), (b, r)
+            rows += 1
+    # Every slot the append did not target keeps its previous bits (NaN sentinels included).
+    touched = np.zeros(wl.num_blocks * 16, dtype=bool)
+    touched[wl.slot_mapping] = True
+    flat_old = wl.k_cache.transpose(0, 2, 1, 3).reshape(wl.num_blocks * 16, -1)
+    flat_new = kc.transpose(0, 2, 1, 3).reshape(wl.num_blocks * 16, -1)
+    assert np.array_equal(flat_old[~touched], flat_new[~touched])
+
+
+def check_cache_write_skips_padding(lib):
+    wl, _ = W.make_custom(8, 2, [5, 9], seed=4)
+    slots = wl.slot_mapping.copy()
+    slots[0] = -1  # padding token
+    kc, vc = oracle.kv_reshape_and_cache(wl.new_key, wl.new_value, wl.k_cache, wl.v_cache, slots, lib=lib)
+    blk, off = divmod(int(wl.slot_mapping[0]), 16)
+    assert np.array_equal(kc[blk, :, off], wl.k_cache[blk, :, off])  # untouched (NaN)
+    blk, off = divmod(int(wl.slot_mapping[1]), 16)
+    assert np.array_equal(kc[blk, :, off], wl.new_key[1])
+
+
+# ---- attention against the contiguous brute force ---------------------------
+
+def check_tiny_vs_brute(lib):
+    wl = W.make_workload("tiny", materialize_logical=True)
+    _vs_brute(wl, wl.decode, lib)
+
+
+def check_group_sizes_vs_brute(lib):
+    for n_q, n_kv in [(32, 32), (32, 16), (32, 8), (64, 8), (32, 2), (32, 1)]:
+        wl, batch = W.make_custom(n_q, n_kv, [1, 16, 17, 40], seed=n_q * 100 + n_kv)
+        _vs_brute(wl, batch, lib)
+
+
+def check_chunks_vs_brute(lib):
+    # Causal chunks over a cached prefix (c > 0), a chunk from position 0 (c = 0,
+    # i.e. a dense causal prefill) and decode rows, in one batch.
+    wl, batch = W.make_custom(32, 8, [48, 20, 37, 5], q_lens=[16, 20, 1, 5], seed=11)
+    _vs_brute(wl, batch, lib)
+
+
+def check_scaled_workloads_vs_brute(lib):
+    for name in ["llama3_8b_b64", "sweep_mqa", "mixed"]:
+        wl = W.make_workload(name, materialize_logical=True, batch_scale=0.05)
+        for batch in [wl.chunk, wl.decode]:
+            if batch is not None:
+                _vs_brute(wl, batch, lib, tol=1e-11)
+
+
+# ---- closed forms ----------------------------------------------------------------
+
+def check_single_key_returns_v(lib):
+    """ctx = 1: softmax over one key is 1, so the output is that V row, exactly."""
+    wl, batch = W.make_custom(32, 8, [1, 1, 1], seed=5)
+    kc, vc = _appended(wl, lib)
+    out = _attn(wl, batch, kc, vc, lib)
+    G = wl.n_q // wl.n_kv
+    for b in range(3):
+        v = W.f32_from_bf16_bits(wl.new_value[b]).astype(np.float64)  # [n_kv, d]
+        assert np.array_equal(out[b], np.repeat(v, G, axis=0)), b
+
+
+def check_constant_scores_give_mean(lib):
+    """q = 0 makes every score equal, so the output is the plain mean of V."""
+    wl, batch = W.make_custom(16, 4, [7, 33], seed=6)
+    batch.q[:] = 0
+    kc, vc = _appended(wl, lib)
+    out = _attn(wl, batch, kc, vc, lib)
+    G = wl.n_q // wl.n_kv
+    for b in range(2):
+        V = W.f32_from_bf16_bits(batch.logical_v[b]).astype(np.float64)
+        mean = np.repeat(V.mean(axis=0), G, axis=0)
+        assert np.max(np.abs(out[b] - mean)) <= TOL, b
+
+
+def check_two_keys_sigmoid(lib):
+    """Two keys: weights are (sigmoid(s1 - s2), sigmoid(s2 - s1)), s = scale q.k."""
+    d = 128
+    n_q, n_kv = 2, 1
+    q = np.zeros((1, n_q, d), np.float32)
+    q[0, 0, 0] = 1.0; q[0, 0, 1] = 0.5       # head 0
+    q[0, 1, 2] = -2.0                          # head 1
+    K = np.zeros((2, n_kv, d), np.float32)
+    K[0, 0, 0] = 3.0; K[0, 0, 2] = 1.0
+    K[1, 0, 1] = -4.0; K[1, 0, 2] = -0.5
+    V = np.zeros((2, n_kv, d), np.float32)
+    V[0, 0, :] = 1.5
+    V[1, 0, :] = -0.25
+    V[1, 0, 5] = 8.0
+    k_cache = np.full((2, n_kv, 16, d), W.BF16_NAN, np.uint16)
+    v_cache = k_cache.copy()
+    k_cache[1, :, 0:2] = _bits(K).transpose(1, 0, 2)
+    v_cache[1, :, 0:2] = _bits(V).transpose(1, 0, 2)
+    scale = float(np.float32(1 / math.sqrt(d)))
+    out = oracle.paged_attention(_bits(q), np.array([0, 1], np.int32), k_cache, v_cache,
+                                 np.array([[1]], np.int32), np.array([2], np.int32), scale, n_q=n_q, lib=lib)
+    # head 0: s = scale*(3, -2); head 1: s = scale*(-2, 1)
+    for h, (s1, s2) in enumerate([(3.0, -2.0), (-2.0, 1.0)]):
+        w1 = 1.0 / (1.0 + math.exp(-(s1 - s2) * scale))
+        w2 = 1.0 / (1.0 + math.exp(-(s2 - s1) * scale))
+        want = w1 * V[0, 0].astype(np.float64) + w2 * V[1, 0].astype(np.float64)
+        assert np.max(np.abs(out[0, h] - want)) <= TOL, h
+
+
+def check_linearity_in_v(lib):
+    """The weights sum to one and enter linearly.
+
+    V -> 2 V (exact in bf16) gives out -> 2 out, and a V whose visible rows all
+    equal one vector c gives out = c whatever the scores are.
+    """
+    wl, batch = W.make_custom(8, 2, [21, 40], seed=8)
+    kc, vc = _appended(wl, lib)
+    base = _attn(wl, batch, kc, vc, lib)
+    vc2 = W.bf16_bits_from_f32(W.f32_from_bf16_bits(vc) * np.float32(2.0))
+    out2 = _attn(wl, batch, kc, vc2, lib)
+    assert np.max(np.abs(out2 - 2.0 * base)) <= TOL
+    c = _bits(np.linspace(-3.0, 3.0, wl.head_dim, dtype=np.float32))
+    vc3 = vc.copy()
+    vc3[:] = c  # every slot of every block and head
+    out3 = _attn(wl, batch, kc, vc3, lib)
+    assert np.max(np.abs(out3 - W.f32_from_bf16_bits(c).astype(np.float64))) <= TOL
+
+
+# ---- invariances -----------------------------------------------------------------
+
+def check_repeat_interleave_equivalence(lib):
+    """GQA equals MHA on K/V repeated G times along the head axis (page 1, section 3.2)."""
+    wl, batch = W.make_custom(32, 8, [9, 30, 64], q_lens=[1, 4, 1], seed=9)
+    kc, vc = _appended(wl, lib)
+    gqa = _attn(wl, batch, kc, vc, lib)
+    G = wl.n_q // wl.n_kv
+    mha = oracle.paged_attention(batch.q, batch.cu_q_lens, np.repeat(kc, G, axis=1), np.repeat(vc, G, axis=1),
+                                 batch.block_tables, batch.context_lens, wl.scale, n_q=wl.n_q, lib=lib)
+    assert np.array_equal(gqa, mha)
+
+
+def check_block_permutation_invariance(lib):
+    """Relocating physical blocks (and remapping the table) leaves the output bit-identical."""
+    wl, batch = W.make_custom(32, 8, [40, 17, 64], q_lens=[1, 1, 8], seed=10)
+    kc, vc = _appended(wl, lib)
+    base = _attn(wl, batch, kc, vc, lib)
+    perm = np.random.default_rng(1).permutation(wl.num_blocks)  # new position of block i
+    kc2 = np.empty_like(kc); vc2 = np.empty_like(vc)
+    kc2[perm] = kc; vc2[perm] = vc
+    batch.block_tables = perm[batch.block_tables].astype(np.int32)
+    out = _attn(wl, batch, kc2, vc2, lib)
+    assert np.array_equal(base, out)
+
+
+def check_shared_prefix_invariance(lib):
+    """Sequences sharing prefix blocks give the same result as with private copies."""
+    wl, batch = W.make_custom(32, 8, [40, 70, 33], seed=12, shared_prefix=[0, 1, 2], shared_prefix_blocks=2)
+    kc, vc = _appended(wl, lib)
+    shared = _attn(wl, batch, kc, vc, lib)
+    # Give sequences 1 and 2 private copies of the two shared blocks.
+    tables = batch.block_tables.copy()
+    extra = []
+    nb = wl.num_blocks
+    for b in (1, 2):
+        for j in range(2):
+            extra.append(tables[b, j]); tables[b, j] = nb; nb += 1
+    kc2 = np.concatenate([kc, kc[extra]]); vc2 = np.concatenate([vc, vc[extra]])
+    batch.block_tables = tables
+    private = _attn(wl, batch, kc2, vc2, lib)
+    assert np.array_equal(shared, private)
+
+
+def check_chunk_last_row_equals_decode(lib):
+    """The last row of a causal chunk sees every key, exactly like a decode of that token."""
+    wl, batch = W.make_custom(32, 8, [50], q_lens=[12], seed=13)
+    kc, vc = _appended(wl, lib)
+    chunk = _attn(wl, batch, kc, vc, lib)
+    dec = oracle.paged_attention(batch.q[11:12], np.array([0, 1], np.int32), kc, vc, batch.block_tables,
+                                 batch.context_lens, wl.scale, n_q=wl.n_q, lib=lib)
+    assert np.array_equal(chunk[11], dec[0])
+
+
+def check_chunk_split_invariance(lib):
+    """One chunk of 24 equals two chunks of 12 (the second over the first's keys)."""
+    wl, batch = W.make_custom(32, 8, [40], q_lens=[24], seed=14)
+    kc, vc = _appended(wl, lib)
+    one = _attn(wl, batch, kc, vc, lib)
+    first = oracle.paged_attention(batch.q[:12], np.array([0, 12], np.int32), kc, vc, batch.block_tables,
+                                   np.array([28], np.int32), wl.scale, n_q=wl.n_q, lib=lib)
+    second = oracle.paged_attention(batch.q[12:], np.array([0, 12], np.int32), kc, vc, batch.block_tables,
+                                    np.array([40], np.int32), wl.scale, n_q=wl.n_q, lib=lib)
+    assert np.array_equal(one, np.concatenate([first, second]))
+
+
+# ---- Flash-Decoding split and log-sum-exp merge ---------------------------------
+
+def check_split_merge_identity(lib):
+    wl, batch = W.make_custom(32, 8, [1, 15, 16, 17, 100, 300], seed=15)
+    kc, vc = _appended(wl, lib)
+    ref = _attn(wl, batch, kc, vc, lib)
+    for part in [16, 32, 64, 256, 4096]:
+        m, l, o = oracle.decode_partials(batch.q, kc, vc, batch.block_tables, batch.context_lens,
+                                         wl.scale, part, lib=lib)
+        merged = oracle.lse_merge(m, l, o, lib=lib)
+        err = np.max(np.abs(merged - ref))
+        assert err <= TOL, (part, err)
+
+
+def check_lse(lib):
+    """The returned log-sum-exp equals log(sum_j exp(s_j)) from the brute-force scores."""
+    wl, batch = W.make_custom(8, 2, [19, 3], seed=16)
+    kc, vc = _appended(wl, lib)
+    _, lse = _attn(wl, batch, kc, vc, lib, return_lse=True)
+    for b in range(2):
+        K = W.f32_from_bf16_bits(batch.logical_k[b]).astype(np.float64)
+        Q = W.f32_from_bf16_bits(batch.q[b]).astype(np.float64)
+        for h in range(wl.n_q):
+            s = K[:, h // 4, :] @ Q[h] * wl.scale
+            assert abs(lse[b, h] - math.log(np.sum(np.exp(s)))) <= 1e-10
+
+
+ALL_CHECKS = [
+    check_kv_sizes, check_kv_groups, check_slot_rule,
+    check_cache_write_roundtrip, check_cache_write_skips_padding,
+    check_tiny_vs_brute, check_group_sizes_vs_brute, check_chunks_vs_brute,
+    check_scaled_workloads_vs_brute,
+    check_single_key_returns_v, check_constant_scores_give_mean, check_two_keys_sigmoid,
+    check_linearity_in_v,
+    check_repeat_interleave_equivalence, check_block_permutation_invariance,
+    check_shared_prefix_invariance, check_chunk_last_row_equals_decode, check_chunk_split_invariance,
+    check_split_merge_identity, check_lse,
+]
