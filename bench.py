@@ -1,0 +1,440 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged decode-attention hot path on GB300.
+
+One step = the whole decode path over one batch: append the step's new K/V
+through slot_mapping (kv_reshape_and_cache), then paged decode attention with
+split-KV partitions and their log-sum-exp merge (paged_attention_decode).
+The metric is KV-read throughput: the logical K+V bytes the attention reads
+(sum over sequences of ctx * n_kv * 128 * 2 * 2) per second, with sequences/s
+and tokens/s alongside.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME]
+
+Prints ONE JSON line (rank 0).  Under torchrun every rank runs its own batch
+(weak scaling, no collective on the data path); the time is the max over ranks.
+``--impl reference`` times the fp64 CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_cache_95_gb300 import workloads as W  # noqa: E402
+
+METRIC = "paged decode attn: KV-read HBM GB/s (% of GB300 peak); sequences/s"
+DEFAULT_WORKLOAD = "llama3_8b_b64"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---- distributed plumbing (host side only) ---------------------------------------
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(world_size, backend):
+    if world_size <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group(backend=backend)
+    return dist
+
+
+def max_over_ranks(value: float, dist, device=None) -> float:
+    """Max of a float over all ranks (identity without a process group)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# ---- clocks during the timed region -----------------------------------------------
+
+class ClockSampler:
+    """Samples nvidia-smi SM clocks and throttle reasons every 200 ms."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+        self.window = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        rows = []
+        for ts, line in self.samples:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((ts, float(parts[1]), float(parts[2]), parts))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        inside = [r for r in rows if self.window and self.window[0] - 0.25 <= r[0] <= self.window[1] + 0.25]
+        use = inside if inside else rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in use:
+            for name, flag in zip(names, r[3][5:9]):
+                if flag.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": sorted(reasons), "samples": len(use), "samples_in_timed_region": len(inside)}
+
+
+# ---- the oracle on host cores (reference arm and cpu_baseline) -----------------------
+
+def oracle_step(wl: W.Workload, batch: W.Batch):
+    import oracle  # test infrastructure: only this arm and the cpu_baseline leg call it
+    kc, vc = oracle.kv_reshape_and_cache(wl.new_key, wl.new_value, wl.k_cache, wl.v_cache, wl.slot_mapping)
+    return oracle.paged_attention(batch.q, batch.cu_q_lens, kc, vc, batch.block_tables, batch.context_lens,
+                                  wl.scale, n_q=wl.n_q)
+
+
+def subset_workload(wl: W.Workload, nseq: int):
+    """The first ``nseq`` sequences of the decode batch (their append tokens too)."""
+    b = wl.decode
+    sub = W.Batch(q=b.q[:nseq], cu_q_lens=b.cu_q_lens[:nseq + 1], block_tables=b.block_tables[:nseq],
+                  context_lens=b.context_lens[:nseq])
+    w2 = W.Workload(name=wl.name, n_q=wl.n_q, n_kv=wl.n_kv, head_dim=wl.head_dim, block_size=wl.block_size,
+                    num_blocks=wl.num_blocks, poison_block=wl.poison_block, k_cache=wl.k_cache, v_cache=wl.v_cache,
+                    new_key=wl.new_key[:nseq], new_value=wl.new_value[:nseq], slot_mapping=wl.slot_mapping[:nseq],
+                    scale=wl.scale, decode=sub)
+    return w2
+
+
+def time_oracle(wl: W.Workload, budget_s: float, min_reps: int = 1):
+    """Time the oracle on a bounded sample of the workload; returns (GB/s, seqs/s, desc, threads, reps)."""
+    import oracle
+    threads = oracle.num_threads()
+    nseq = wl.decode.num_seqs
+    # calibrate on a small sample, then size the sample to the budget
+    probe = subset_workload(wl, max(1, nseq // 16))
+    t0 = time.perf_counter()
+    oracle_step(probe, probe.decode)
+    tp = time.perf_counter() - t0
+    per_seq = tp / probe.decode.num_seqs
+    take = int(max(1, min(nseq, budget_s / max(per_seq, 1e-9))))
+    sample = subset_workload(wl, take)
+    reps, elapsed = 0, 0.0
+    while reps < min_reps or elapsed < 0.5 * budget_s:
+        t0 = time.perf_counter()
+        oracle_step(sample, sample.decode)
+        elapsed += time.perf_counter() - t0
+        reps += 1
+        if elapsed > budget_s:
+            break
+    per_step = elapsed / reps
+    kv = wl.kv_read_bytes(sample.decode)
+    desc = (f"{take} of {nseq} sequences of {wl.name} (append + decode attention, fp64 oracle), "
+            f"{reps} repetition(s), {per_step:.3f} s each")
+    return kv / per_step / 1e9, take / per_step, desc, threads, reps, per_step
+
+
+# ---- our arm ------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = init_dist(world, "nccl")
+    from paged_kv_cache_95_gb300 import build as B
+    B.build()
+    from paged_kv_cache_95_gb300 import pagedkv as P
+    P.load_library()
+
+    wl = W.shard_for_rank(args.workload, rank, world)
+    batch = wl.decode
+    dev = torch.device("cuda", local)
+
+    def up_bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    def up_i32(a):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+
+    k_cache, v_cache = up_bf16(wl.k_cache), up_bf16(wl.v_cache)
+    new_k, new_v, slots = up_bf16(wl.new_key), up_bf16(wl.new_value), up_i32(wl.slot_mapping)
+    q, tables, lens = up_bf16(batch.q), up_i32(batch.block_tables), up_i32(batch.context_lens)
+    out = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+    desc = P.cache_desc(k_cache)
+    ws_bytes = P.paged_attention_workspace_size(batch.num_seqs, wl.n_q, batch.max_blocks_per_seq, 0, desc)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    kv_bytes = wl.kv_read_bytes(batch)
+    pool_bytes = 2 * k_cache.numel() * 2
+
+    stream = torch.cuda.current_stream(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+
+    def step(i=None):
+        if i is not None:
+            ev[i][0].record(stream)
+        P.kv_reshape_and_cache(new_k, new_v, k_cache, v_cache, slots)
+        if i is not None:
+            ev[i][1].record(stream)
+        P.paged_attention_decode(out, q, k_cache, v_cache, tables, lens, wl.scale, workspace=ws)
+        if i is not None:
+            ev[i][2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(dist)
+    torch.cuda.synchronize(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        step(i)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    w1 = time.time()
+    barrier(dist)
+    clocks.mark(w0, w1)
+    time.sleep(0.3)
+    clocks.stop()
+
+    total_ms = start.elapsed_time(end)
+    decode_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    append_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    t_max = max_over_ranks(total_ms / 1e3, dist, device=dev)
+    ms_per_step = t_max / args.steps * 1e3
+    value = world * kv_bytes * args.steps / t_max / 1e9
+    st = int(ws[:4].view(torch.int32).item()) & 0xFFFFFFFF
+    if st:
+        raise RuntimeError(f"device status word set during the bench: {st:#x}")
+
+    # ---- end to end through the public API with host buffers ----
+    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+    h_in = [pin(x) for x in (q, new_k, new_v, slots, tables, lens)]
+    d_in = [torch.empty_like(x) for x in (q, new_k, new_v, slots, tables, lens)]
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    bi = sum(x.numel() * x.element_size() for x in h_in)
+    bo = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        for h, d in zip(h_in, d_in):
+            d.copy_(h, non_blocking=True)
+        P.kv_reshape_and_cache(d_in[1], d_in[2], k_cache, v_cache, d_in[3])
+        P.paged_attention_decode(out, d_in[0], k_cache, v_cache, d_in[4], d_in[5], wl.scale, workspace=ws)
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(dist)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_t = max_over_ranks(e0.elapsed_time(e1) / 1e3, dist, device=dev)
+    e2e_value = world * kv_bytes * args.steps / e2e_t / 1e9
+
+    launches_per_step = 1 + 1 + (1 if _decode_splits(batch, ws_bytes, wl) else 0)
+
+    if rank == 0:
+        peak, peak_src = measured_peaks()
+        achieved = kv_bytes / (decode_ms / 1e3) / 1e9
+        cpu = None
+        if world == 1:
+            gbs, sps, sdesc, threads, reps, per_step = time_oracle(wl, budget_s=args.cpu_budget)
+            cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sdesc}
+        line = {
+            "metric": METRIC,
+            "value": round(value, 2),
+            "unit": "GB/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic",
+            "impl": "ours",
+            "pct_of_hbm_peak": round(100.0 * value / world / peak, 2),
+            "sequences_per_s": round(world * batch.num_seqs * args.steps / t_max, 1),
+            "tokens_per_s": round(world * batch.num_seqs * args.steps / t_max, 1),
+            "config": _config(wl, batch, kv_bytes, pool_bytes, world),
+            "roofline": {"bound": "hbm", "kernel": "paged_attention_decode (decode + merge launches)",
+                         "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+                         if peak_src == "measured" else "fallback 6.8 TB/s",
+                         "traffic": _profiled_traffic(args.workload),
+                         "bytes_per_launch": kv_bytes, "avg_launch_ms": round(decode_ms, 5),
+                         "append_avg_ms": round(append_ms, 5)},
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": bi,
+                    "d2h_bytes_per_step": bo, "ms_per_step": round(e2e_t / args.steps * 1e3, 5)},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def _decode_splits(batch, ws_bytes, wl) -> bool:
+    return ws_bytes > 256 and batch.max_blocks_per_seq > 16
+
+
+def _config(wl, batch, kv_bytes, pool_bytes, world):
+    lens = batch.context_lens
+    return {"workload": wl.name, "batch_per_gpu": batch.num_seqs, "global_batch": batch.num_seqs * world,
+            "n_q": wl.n_q, "n_kv": wl.n_kv, "head_dim": wl.head_dim, "block_size": wl.block_size,
+            "context_min": int(lens.min()), "context_max": int(lens.max()), "context_mean": float(lens.mean()),
+            "kv_read_bytes_per_step": kv_bytes, "pool_bytes": pool_bytes, "out_dtype": "bf16",
+            "partition": "auto", "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": f"inputs larger than L2: {kv_bytes / 1e6:.0f} MB read per step vs 129 MB L2; no flush"}
+
+
+def _profiled_traffic(workload):
+    """dram read+write bytes per decode launch from the committed ncu summary, if any."""
+    path = os.path.join(ROOT, "profiles", f"decode_{workload}.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d.get("dram_bytes_per_launch")
+    except Exception:
+        return None
+
+
+# ---- reference arm (the oracle on host cores) -----------------------------------------
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if world > 1 and rank != 0:
+        return  # rank 0 alone runs the CPU reference
+    wl = W.make_workload(args.workload)
+    import oracle
+    threads = oracle.num_threads()
+    nseq = wl.decode.num_seqs
+    # size the per-step sample so that warmup + steps fit the budget
+    probe = subset_workload(wl, max(1, nseq // 16))
+    t0 = time.perf_counter()
+    oracle_step(probe, probe.decode)
+    per_seq = (time.perf_counter() - t0) / probe.decode.num_seqs
+    budget = args.ref_budget / max(1, args.steps + args.warmup)
+    take = int(max(1, min(nseq, budget / max(per_seq, 1e-9))))
+    sample = subset_workload(wl, take)
+    for _ in range(args.warmup):
+        oracle_step(sample, sample.decode)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_step(sample, sample.decode)
+        times.append(time.perf_counter() - t0)
+    t = sum(times)
+    kv = wl.kv_read_bytes(sample.decode)
+    value = kv * args.steps / t / 1e9
+    sdesc = f"{take} of {nseq} sequences of {wl.name} per step (append + decode attention, fp64 oracle)"
+    line = {
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "config": _config(wl, sample.decode, kv, 2 * wl.k_cache.nbytes, 1),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": sdesc},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "sequences_per_s": round(take * args.steps / t, 3),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=W.WORKLOAD_NAMES)
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--ref-budget", type=float, default=120.0, help="seconds of oracle time for --impl reference")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,226 @@
+/*
+ * pagedkv.h -- C ABI of the GB300 (sm_103a) paged KV-cache attention library.
+ *
+ * What it computes
+ * ----------------
+ * Scaled dot-product attention softmax(q K^T * scale + M) V for the decode
+ * phase (one new query row per sequence) and for causal prefill chunks (many
+ * query rows per sequence), over a PagedAttention KV cache: K and V live in
+ * fixed-size physical blocks of 16 tokens that each sequence reaches through
+ * its row of a block table, and new tokens' K/V are appended through a
+ * slot mapping.  Query head h reads KV head floor(h / G), G = n_q / n_kv
+ * (MHA: G = 1, GQA: 1 < G < n_q, MQA: n_kv = 1).
+ *
+ * Sources (page title, section):
+ *  - "注意力演进与推理流程" (attention evolution and inference, jerryiiii.gitbook.io):
+ *    section 1.1 (SDPA with causal mask M), section 3.1 (GQA group rule
+ *    g = floor(h / G)), 变革 1 (PagedAttention: fixed blocks, e.g. 16 tokens,
+ *    allocated on demand), 变革 3 (chunked prefill).
+ *  - vLLM concepts deep dive, section 1 (yyzxw.github.io): decode attention
+ *    Attention(q_t, K_<=t, V_<=t); attention kernels receive a block table and
+ *    a slot mapping instead of contiguous K/V pointers.
+ *  - "LLM 推理全过程的维度变化与核心公式" (research.frankk.site, LLM inference
+ *    walkthrough): section "Decode 阶段维度流转" (write K/V at cache_len, then
+ *    read the whole cache; decode needs no causal mask), section "KV Cache 的
+ *    形状与增长" (paged blocks change only the layout), section "工程优化怎么嵌进
+ *    公式" (Flash-Decoding: split cache_len, then a log-sum-exp reduction;
+ *    chunked prefill leaves the formula unchanged).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All data pointers are DEVICE pointers owned by the caller; the library
+ *    allocates nothing, keeps no pointer after it returns and has no global
+ *    state besides a per-device cache of SM counts and kernel attributes.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Every call only enqueues work on that stream and returns; it
+ *    never synchronises.  Ordering between calls is the caller's: append the
+ *    new tokens (kv_reshape_and_cache) before attending over them, on the
+ *    same stream.
+ *  - Layouts (all row-major, contiguous):
+ *      k_cache, v_cache : bf16 [num_blocks][num_kv_heads][block_size][head_dim]
+ *                         (one (block, head) tile of 16 x 128 bf16 is 4096
+ *                         contiguous bytes; base 16-byte aligned)
+ *      block_tables     : int32 [num_seqs][max_blocks_per_seq]; entries past
+ *                         ceil(context_len / block_size) are never read
+ *      context_lens     : int32 [num_seqs]; counts the tokens of this step
+ *      q                : bf16 [rows][num_q_heads][head_dim]
+ *      out              : out_dtype [rows][num_q_heads][head_dim]
+ *  - Supported shapes: head_dim 128, block_size 16, bf16 K/V/q,
+ *    num_q_heads % num_kv_heads == 0 with G <= 8 or G a multiple of 8.
+ *  - Return value: PKV_OK or a negative PKV_ERR_* code; no exception crosses
+ *    the ABI.  Argument errors are detected before anything is enqueued.
+ *  - Data that only the device sees (context lengths, block ids) is checked
+ *    by the kernels: a context length outside [1, max_blocks_per_seq *
+ *    block_size] or a block id outside [0, num_blocks) never causes an
+ *    out-of-bounds access; the offending block contributes nothing, a
+ *    length < 1 yields zero output rows, and a PKV_STATUS_* bit is ORed into
+ *    the 32-bit status word at byte 0 of the workspace.
+ *    The word is sticky: clear it (e.g. cudaMemsetAsync) to reset.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types. */
+typedef enum pkv_dtype {
+    PKV_DTYPE_BF16 = 0,    /* bfloat16 */
+    PKV_DTYPE_FLOAT32 = 1  /* IEEE binary32 */
+} pkv_dtype;
+
+/* Description of the physical block pool shared by K and V. */
+typedef struct pkv_cache_desc {
+    int32_t num_blocks;    /* physical blocks in the pool (>= 1) */
+    int32_t block_size;    /* tokens per block; must be 16 */
+    int32_t num_kv_heads;  /* KV heads n_kv (>= 1) */
+    int32_t head_dim;      /* per-head dimension; must be 128 */
+    int32_t dtype;         /* pkv_dtype of K/V; must be PKV_DTYPE_BF16 */
+} pkv_cache_desc;
+
+/* Return codes. */
+#define PKV_OK 0
+#define PKV_ERR_INVALID_ARG (-1)         /* null pointer, bad size, misaligned pointer, n_q % n_kv != 0 */
+#define PKV_ERR_UNSUPPORTED (-2)         /* head_dim, block_size, dtype or group size not supported */
+#define PKV_ERR_WORKSPACE_TOO_SMALL (-3) /* workspace_bytes below the *_workspace_size() answer */
+#define PKV_ERR_CUDA (-4)                /* a CUDA runtime call or launch failed */
+
+/* Bits ORed into the device status word (workspace byte 0). */
+#define PKV_STATUS_BAD_CONTEXT_LEN 0x1u /* context_len < 1 or > max_blocks_per_seq * block_size */
+#define PKV_STATUS_BAD_BLOCK_ID 0x2u    /* a needed block_tables entry outside [0, num_blocks) */
+#define PKV_STATUS_BAD_Q_LEN 0x4u       /* prefill: q_len < 0, > context_len or > max_q_len */
+#define PKV_STATUS_TIMEOUT 0x8u         /* a bounded wait inside a kernel gave up (output invalid) */
+
+/*
+ * kv_reshape_and_cache -- append new tokens' K and V to the paged pool.
+ *
+ * For each token t < num_tokens and KV head h:
+ *     slot = slot_mapping[t];  block = slot / block_size;  off = slot % block_size
+ *     k_cache[block][h][off][:] = key[t][h][:];   v_cache[block][h][off][:] = value[t][h][:]
+ * This is the write of the new token's K/V at position cache_len that precedes
+ * the read in a decode step ("LLM 推理全过程的维度变化与核心公式", section
+ * "Decode 阶段维度流转"), done through the slot mapping the vLLM concepts deep
+ * dive (section 1) describes.  The copy is bit-exact.
+ *
+ *   key, value   : bf16 [num_tokens][num_kv_heads][head_dim], device, 16-B aligned
+ *   k_cache, v_cache : the pool (layout above), written in place
+ *   slot_mapping : int32 [num_tokens], device.  slot < 0 marks a padding
+ *                  token and is skipped; slot >= num_blocks * block_size is
+ *                  skipped too (nothing is written out of bounds).  Two
+ *                  tokens with the same slot in one call race (undefined).
+ *   num_tokens   : >= 0 (0 enqueues nothing)
+ * Errors: PKV_ERR_INVALID_ARG / PKV_ERR_UNSUPPORTED / PKV_ERR_CUDA.
+ */
+PKV_API int kv_reshape_and_cache(const void *key, const void *value, void *k_cache, void *v_cache,
+                         const int32_t *slot_mapping, int32_t num_tokens,
+                         const pkv_cache_desc *cache, void *stream);
+
+/*
+ * paged_attention_workspace_size -- bytes of device workspace that
+ * paged_attention_decode needs for these sizes and this partition_size
+ * (0 = automatic; the answer then covers every automatic choice).  Needs no
+ * GPU.  Returns 0 for invalid arguments.
+ */
+PKV_API size_t paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq,
+                                      int32_t partition_size, const pkv_cache_desc *cache);
+
+/*
+ * paged_attention_decode -- decode-phase attention over the paged cache.
+ *
+ * For each sequence b (ctx = context_lens[b], which already counts the token
+ * appended this step) and query head h with KV head g = floor(h / G):
+ *     s_j    = scale * <q[b][h], K_b[j][g]>                     j = 0 .. ctx-1
+ *     out[b][h] = sum_j softmax(s)_j * V_b[j][g]
+ * where K_b[j] is row j % block_size of block block_tables[b][j / block_size]
+ * ("LLM 推理全过程的维度变化与核心公式", section "Decode 阶段维度流转": scores
+ * [B, n_q, 1, cache_len], GQA broadcast, no causal mask).
+ *
+ * Long contexts are split into partitions of `partition_size` tokens that are
+ * processed in parallel and then combined by a log-sum-exp merge
+ * (Flash-Decoding; same page, section "工程优化怎么嵌进公式").  The result
+ * does not depend on the partition size beyond float rounding.
+ *
+ *   out            : out_dtype [num_seqs][num_q_heads][head_dim], device
+ *   out_dtype      : PKV_DTYPE_FLOAT32 or PKV_DTYPE_BF16 (round to nearest even)
+ *   q              : bf16 [num_seqs][num_q_heads][head_dim], device
+ *   block_tables   : int32 [num_seqs][max_blocks_per_seq], device
+ *   context_lens   : int32 [num_seqs], device
+ *   num_seqs       : 1 .. 65535;  num_q_heads: multiple of cache->num_kv_heads
+ *   scale          : softmax scale (usually 1/sqrt(head_dim))
+ *   partition_size : tokens per partition, a positive multiple of 16, or 0
+ *                    for an automatic choice sized to the GPU's SM count
+ *   workspace      : device scratch, 256-B aligned, of at least
+ *                    paged_attention_workspace_size(num_seqs, num_q_heads,
+ *                    max_blocks_per_seq, partition_size, cache) bytes; holds
+ *                    the status word and the per-partition partials.  Its
+ *                    contents need no initialisation (except the status word,
+ *                    which is only ever ORed into).  Calls that share a
+ *                    workspace must not overlap in time (they race on it).
+ * Errors: PKV_ERR_INVALID_ARG / PKV_ERR_UNSUPPORTED /
+ *         PKV_ERR_WORKSPACE_TOO_SMALL / PKV_ERR_CUDA.
+ */
+PKV_API int paged_attention_decode(void *out, int32_t out_dtype, const void *q, const void *k_cache,
+                           const void *v_cache, const int32_t *block_tables,
+                           const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                           int32_t max_blocks_per_seq, float scale, int32_t partition_size,
+                           const pkv_cache_desc *cache, void *workspace, size_t workspace_bytes,
+                           void *stream);
+
+/*
+ * paged_attention_prefill_workspace_size -- bytes of workspace that
+ * paged_attention_prefill_chunk needs (the status word).  Needs no GPU.
+ */
+PKV_API size_t paged_attention_prefill_workspace_size(int32_t num_seqs, int32_t num_q_heads,
+                                              const pkv_cache_desc *cache);
+
+/*
+ * paged_attention_prefill_chunk -- causal attention of a chunk of new query
+ * rows per sequence over that sequence's paged cache.
+ *
+ * Sequence b owns query rows cu_q_lens[b] .. cu_q_lens[b+1]-1 (q_len rows);
+ * its context length ctx = context_lens[b] counts those q_len tokens, whose
+ * K/V must already be in the cache.  Row i (0-based within the chunk) sits at
+ * absolute position c + i with c = ctx - q_len and sees keys j <= c + i:
+ * the causal mask M_ij = 0 for j <= i, -inf otherwise ("注意力演进与推理流程",
+ * section 1.1) shifted by the cached prefix, which is what chunked prefill
+ * computes (same page, 变革 3; walkthrough page, Chunked Prefill: "formula
+ * unchanged").  With q_len = 1 a row is a decode row.
+ *
+ *   out        : out_dtype [cu_q_lens[num_seqs]][num_q_heads][head_dim], device
+ *   q          : bf16 [cu_q_lens[num_seqs]][num_q_heads][head_dim], device
+ *   cu_q_lens  : int32 [num_seqs + 1], device, non-decreasing, cu_q_lens[0] = 0
+ *   max_q_len  : host upper bound of every q_len (sizes the launch grid)
+ *   total_q_rows : host value of cu_q_lens[num_seqs] (bounds the q/out tensors)
+ *   workspace  : >= paged_attention_prefill_workspace_size() bytes (status word)
+ * Uses the 5th-generation tensor cores (tcgen05, accumulators in tensor memory).
+ * Errors: PKV_ERR_INVALID_ARG / PKV_ERR_UNSUPPORTED /
+ *         PKV_ERR_WORKSPACE_TOO_SMALL / PKV_ERR_CUDA.
+ */
+PKV_API int paged_attention_prefill_chunk(void *out, int32_t out_dtype, const void *q, const int32_t *cu_q_lens,
+                                  int32_t max_q_len, int32_t total_q_rows, const void *k_cache,
+                                  const void *v_cache, const int32_t *block_tables,
+                                  const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                  int32_t max_blocks_per_seq, float scale, const pkv_cache_desc *cache,
+                                  void *workspace, size_t workspace_bytes, void *stream);
+
+/* Human-readable name of a return code (static string, never NULL). */
+PKV_API const char *pagedkv_status_string(int status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+PKV_API int pagedkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

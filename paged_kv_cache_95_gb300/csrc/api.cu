@@ -1,0 +1,356 @@
+// api.cu -- the extern "C" entry points declared in include/pagedkv.h.
+//
+// Responsibilities: argument validation (before anything is enqueued), the
+// split-KV partition plan, workspace carving, TMA tensor-map encoding and the
+// kernel launches on the caller's stream.  No allocation, no synchronisation.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/pagedkv.h"
+#include "launch.h"
+
+namespace {
+
+using pkv::kBlockSize;
+using pkv::kHeadDim;
+
+constexpr int kMaxDevices = 64;
+constexpr int kMinPartBlocks = 16;      // automatic plans never go below 256 tokens per partition
+constexpr int kDefaultPartBlocks = 32;  // 512 tokens
+constexpr size_t kStatusBytes = 256;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// ---- per-device caches -----------------------------------------------------------
+std::atomic<int> g_sm_count[kMaxDevices];
+std::once_flag g_decode_prepared[kMaxDevices][8];
+std::once_flag g_prefill_prepared[kMaxDevices];
+cudaError_t g_decode_prep_err[kMaxDevices][8];
+cudaError_t g_prefill_prep_err[kMaxDevices];
+
+int current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    return dev;
+}
+
+int sm_count(int dev) {
+    if (dev < 0 || dev >= kMaxDevices) return 0;
+    int v = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    g_sm_count[dev].store(v, std::memory_order_relaxed);
+    return v;
+}
+
+// ---- tensor maps -------------------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// Pool tensor [num_blocks][n_kv][16][128] bf16 viewed as 4-D (dims inner->outer:
+// head_dim, slot, head, block); box = 64 dims x 16 slots, 128-byte swizzle.
+bool encode_pool_map(CUtensorMap *map, const void *base, int32_t num_blocks, int32_t n_kv) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(kBlockSize),
+                                static_cast<cuuint64_t>(n_kv), static_cast<cuuint64_t>(num_blocks)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(kHeadDim) * 2,
+                                   static_cast<cuuint64_t>(kHeadDim) * 2 * kBlockSize,
+                                   static_cast<cuuint64_t>(kHeadDim) * 2 * kBlockSize * n_kv};
+    const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(kBlockSize), 1, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Query tensor [rows][n_q][128] bf16 viewed as 3-D (head_dim, head, row); box =
+// 64 dims x G heads x (128 / G) rows, 128-byte swizzle: one box is 128 rows of
+// 128 bytes ordered (row, head).
+bool encode_q_map(CUtensorMap *map, const void *base, int32_t rows, int32_t n_q, int32_t group) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(n_q),
+                                static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim) * 2, static_cast<cuuint64_t>(kHeadDim) * 2 * n_q};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(128 / group)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ---- validation helpers -------------------------------------------------------------
+int check_cache(const pkv_cache_desc *c) {
+    if (!c) return PKV_ERR_INVALID_ARG;
+    if (c->num_blocks < 1 || c->num_kv_heads < 1) return PKV_ERR_INVALID_ARG;
+    if (c->block_size != kBlockSize || c->head_dim != kHeadDim || c->dtype != PKV_DTYPE_BF16)
+        return PKV_ERR_UNSUPPORTED;
+    // The pool's byte size must stay addressable by the kernels' 64-bit index math
+    // and by the 32-bit block coordinate of the tensor map.
+    return PKV_OK;
+}
+
+int check_group(int32_t n_q, int32_t n_kv) {
+    if (n_q < 1 || n_q % n_kv != 0) return PKV_ERR_INVALID_ARG;
+    const int32_t G = n_q / n_kv;
+    if (G > 8 && G % 8 != 0) return PKV_ERR_UNSUPPORTED;
+    return PKV_OK;
+}
+
+// ---- decode plan -----------------------------------------------------------------------
+struct DecodePlan {
+    int32_t part_blocks;
+    int32_t max_parts;
+    size_t off_m, off_l, off_o, total;
+};
+
+DecodePlan plan_decode(int32_t num_seqs, int32_t n_q, int32_t max_blocks, int32_t part_blocks) {
+    DecodePlan pl{};
+    pl.part_blocks = part_blocks >= max_blocks ? max_blocks : part_blocks;
+    pl.max_parts = (max_blocks + pl.part_blocks - 1) / pl.part_blocks;
+    pl.off_m = kStatusBytes;
+    if (pl.max_parts <= 1) {
+        pl.off_l = pl.off_o = pl.total = kStatusBytes;
+        return pl;
+    }
+    const size_t rows = static_cast<size_t>(num_seqs) * n_q * pl.max_parts;
+    pl.off_l = pl.off_m + align_up(rows * 4, 256);
+    pl.off_o = pl.off_l + align_up(rows * 4, 256);
+    pl.total = pl.off_o + align_up(rows * kHeadDim * 4, 256);
+    return pl;
+}
+
+int32_t auto_part_blocks(int32_t num_seqs, int32_t n_kv, int32_t head_splits, int32_t max_blocks, int sms) {
+    // Partitions of 512 tokens keep every CTA's stream short and uniform, which
+    // balances ragged batches; a context that fits one partition is not split.
+    // When few (sequence, head) units exist the partitions shrink (not below 256
+    // tokens) until the grid covers the GPU several times.
+    int32_t pb = kDefaultPartBlocks;
+    const int64_t units = static_cast<int64_t>(num_seqs) * n_kv * head_splits;
+    const int64_t want = static_cast<int64_t>(sms > 0 ? sms : 148) * 8;
+    while (pb > kMinPartBlocks && units * ((max_blocks + pb - 1) / pb) < want) pb /= 2;
+    return pb;
+}
+
+pkv::DecodeVariant decode_variant() {
+    static pkv::DecodeVariant v = [] {
+        pkv::DecodeVariant d{4, 3};
+        if (const char *e = std::getenv("PAGEDKV_DECODE_VARIANT")) {  // "warps,stages", for tuning sweeps
+            int w = 0, s = 0;
+            if (sscanf(e, "%d,%d", &w, &s) == 2 && pkv::decode_variant_supported({w, s})) d = {w, s};
+        }
+        return d;
+    }();
+    return v;
+}
+
+int variant_index(pkv::DecodeVariant v) { return (v.warps == 8 ? 4 : 0) + (v.stages - 1) % 4; }
+
+}  // namespace
+
+extern "C" {
+
+int pagedkv_version(void) { return 100; }
+
+const char *pagedkv_status_string(int status) {
+    switch (status) {
+    case PKV_OK: return "PKV_OK";
+    case PKV_ERR_INVALID_ARG: return "PKV_ERR_INVALID_ARG: invalid argument";
+    case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED: unsupported shape or type";
+    case PKV_ERR_WORKSPACE_TOO_SMALL: return "PKV_ERR_WORKSPACE_TOO_SMALL: workspace too small";
+    case PKV_ERR_CUDA: return "PKV_ERR_CUDA: CUDA runtime error";
+    default: return "unknown pagedkv status";
+    }
+}
+
+int kv_reshape_and_cache(const void *key, const void *value, void *k_cache, void *v_cache,
+                         const int32_t *slot_mapping, int32_t num_tokens, const pkv_cache_desc *cache,
+                         void *stream) {
+    if (int rc = check_cache(cache)) return rc;
+    if (num_tokens < 0) return PKV_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PKV_OK;
+    if (!key || !value || !k_cache || !v_cache || !slot_mapping) return PKV_ERR_INVALID_ARG;
+    if (!aligned(key, 16) || !aligned(value, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(slot_mapping, 4))
+        return PKV_ERR_INVALID_ARG;
+    const int dev = current_device();
+    if (dev < 0) return PKV_ERR_CUDA;
+    const cudaError_t e =
+        pkv::launch_kv_cache_write(key, value, k_cache, v_cache, slot_mapping, num_tokens, cache->num_kv_heads,
+                                   cache->num_blocks, sm_count(dev), static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+size_t paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq,
+                                      int32_t partition_size, const pkv_cache_desc *cache) {
+    if (check_cache(cache) != PKV_OK || num_seqs < 1 || max_blocks_per_seq < 1) return 0;
+    if (check_group(num_q_heads, cache->num_kv_heads) != PKV_OK) return 0;
+    if (partition_size < 0 || partition_size % kBlockSize != 0) return 0;
+    const int32_t pb = partition_size > 0 ? partition_size / kBlockSize : kMinPartBlocks;
+    return plan_decode(num_seqs, num_q_heads, max_blocks_per_seq, pb).total;
+}
+
+int paged_attention_decode(void *out, int32_t out_dtype, const void *q, const void *k_cache, const void *v_cache,
+                           const int32_t *block_tables, const int32_t *context_lens, int32_t num_seqs,
+                           int32_t num_q_heads, int32_t max_blocks_per_seq, float scale, int32_t partition_size,
+                           const pkv_cache_desc *cache, void *workspace, size_t workspace_bytes, void *stream) {
+    if (int rc = check_cache(cache)) return rc;
+    if (int rc = check_group(num_q_heads, cache->num_kv_heads)) return rc;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PKV_ERR_INVALID_ARG;
+    if (out_dtype != PKV_DTYPE_FLOAT32 && out_dtype != PKV_DTYPE_BF16) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs < 1 || num_seqs > 65535 || max_blocks_per_seq < 1) return PKV_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(max_blocks_per_seq) * kBlockSize > INT32_MAX) return PKV_ERR_INVALID_ARG;
+    if (partition_size < 0 || partition_size % kBlockSize != 0) return PKV_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 4) || !aligned(out, 4) ||
+        !aligned(block_tables, 4) || !aligned(context_lens, 4))
+        return PKV_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 256)) return PKV_ERR_INVALID_ARG;
+    // The documented contract: at least what paged_attention_workspace_size() answers.
+    if (workspace_bytes <
+        paged_attention_workspace_size(num_seqs, num_q_heads, max_blocks_per_seq, partition_size, cache))
+        return PKV_ERR_WORKSPACE_TOO_SMALL;
+
+    const int32_t n_kv = cache->num_kv_heads;
+    const int32_t G = num_q_heads / n_kv;
+    const int32_t hpc = G < 8 ? G : 8;
+    const int32_t head_splits = G / hpc;
+    if (static_cast<int64_t>(n_kv) * head_splits > 65535) return PKV_ERR_UNSUPPORTED;
+
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return PKV_ERR_CUDA;
+    const int sms = sm_count(dev);
+    const int32_t pb = partition_size > 0 ? partition_size / kBlockSize
+                                          : auto_part_blocks(num_seqs, n_kv, head_splits, max_blocks_per_seq, sms);
+    const DecodePlan pl = plan_decode(num_seqs, num_q_heads, max_blocks_per_seq, pb);
+    if (workspace_bytes < pl.total) return PKV_ERR_WORKSPACE_TOO_SMALL;  // cannot happen for auto plans
+
+    CUtensorMap kmap, vmap;
+    if (!encode_pool_map(&kmap, k_cache, cache->num_blocks, n_kv) ||
+        !encode_pool_map(&vmap, v_cache, cache->num_blocks, n_kv))
+        return PKV_ERR_CUDA;
+
+    const pkv::DecodeVariant var = decode_variant();
+    const int vi = variant_index(var);
+    std::call_once(g_decode_prepared[dev][vi], [&] { g_decode_prep_err[dev][vi] = pkv::decode_prepare_device(var); });
+    if (g_decode_prep_err[dev][vi] != cudaSuccess) return PKV_ERR_CUDA;
+
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    pkv::DecodeParams p{};
+    p.q = q;
+    p.out = out;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.status = reinterpret_cast<uint32_t *>(ws);
+    p.part_m = pl.max_parts > 1 ? reinterpret_cast<float *>(ws + pl.off_m) : nullptr;
+    p.part_l = pl.max_parts > 1 ? reinterpret_cast<float *>(ws + pl.off_l) : nullptr;
+    p.part_o = pl.max_parts > 1 ? reinterpret_cast<float *>(ws + pl.off_o) : nullptr;
+    p.num_seqs = num_seqs;
+    p.n_q = num_q_heads;
+    p.n_kv = n_kv;
+    p.group = G;
+    p.heads_per_cta = hpc;
+    p.head_splits = head_splits;
+    p.max_blocks = max_blocks_per_seq;
+    p.num_blocks = cache->num_blocks;
+    p.part_blocks = pl.part_blocks;
+    p.max_parts = pl.max_parts;
+    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    p.out_bf16 = out_dtype == PKV_DTYPE_BF16;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (pkv::launch_paged_decode(kmap, vmap, p, var, s) != cudaSuccess) return PKV_ERR_CUDA;
+    if (pl.max_parts > 1 && pkv::launch_lse_merge(p, s) != cudaSuccess) return PKV_ERR_CUDA;
+    return PKV_OK;
+}
+
+size_t paged_attention_prefill_workspace_size(int32_t num_seqs, int32_t num_q_heads, const pkv_cache_desc *cache) {
+    if (check_cache(cache) != PKV_OK || num_seqs < 1) return 0;
+    if (check_group(num_q_heads, cache->num_kv_heads) != PKV_OK) return 0;
+    return kStatusBytes;
+}
+
+int paged_attention_prefill_chunk(void *out, int32_t out_dtype, const void *q, const int32_t *cu_q_lens,
+                                  int32_t max_q_len, int32_t total_q_rows, const void *k_cache, const void *v_cache,
+                                  const int32_t *block_tables, const int32_t *context_lens, int32_t num_seqs,
+                                  int32_t num_q_heads, int32_t max_blocks_per_seq, float scale,
+                                  const pkv_cache_desc *cache, void *workspace, size_t workspace_bytes,
+                                  void *stream) {
+    if (int rc = check_cache(cache)) return rc;
+    if (num_q_heads < 1 || num_q_heads % cache->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+    const int32_t G = num_q_heads / cache->num_kv_heads;
+    // A 128-row MMA tile packs 128 / G query positions x the G heads of one KV group.
+    if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return PKV_ERR_UNSUPPORTED;
+    if (!out || !q || !cu_q_lens || !k_cache || !v_cache || !block_tables || !context_lens)
+        return PKV_ERR_INVALID_ARG;
+    if (out_dtype != PKV_DTYPE_FLOAT32 && out_dtype != PKV_DTYPE_BF16) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs < 1 || num_seqs > 65535 || max_blocks_per_seq < 1 || max_q_len < 0 || total_q_rows < 0)
+        return PKV_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(max_blocks_per_seq) * kBlockSize > INT32_MAX) return PKV_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 16) || !aligned(out, 4) ||
+        !aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(cu_q_lens, 4))
+        return PKV_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 256)) return PKV_ERR_INVALID_ARG;
+    if (workspace_bytes < kStatusBytes) return PKV_ERR_WORKSPACE_TOO_SMALL;
+    if (max_q_len == 0 || total_q_rows == 0) return PKV_OK;
+
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return PKV_ERR_CUDA;
+
+    CUtensorMap qmap, kmap, vmap;
+    if (!encode_q_map(&qmap, q, total_q_rows, num_q_heads, G) ||
+        !encode_pool_map(&kmap, k_cache, cache->num_blocks, cache->num_kv_heads) ||
+        !encode_pool_map(&vmap, v_cache, cache->num_blocks, cache->num_kv_heads))
+        return PKV_ERR_CUDA;
+    std::call_once(g_prefill_prepared[dev], [&] { g_prefill_prep_err[dev] = pkv::prefill_prepare_device(); });
+    if (g_prefill_prep_err[dev] != cudaSuccess) return PKV_ERR_CUDA;
+
+    pkv::PrefillParams p{};
+    p.out = out;
+    p.cu_q_lens = cu_q_lens;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.status = static_cast<uint32_t *>(workspace);
+    p.num_seqs = num_seqs;
+    p.n_q = num_q_heads;
+    p.n_kv = cache->num_kv_heads;
+    p.group = G;
+    p.rows_per_tile = 128 / G;
+    p.max_blocks = max_blocks_per_seq;
+    p.num_blocks = cache->num_blocks;
+    p.total_rows = total_q_rows;
+    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    p.out_bf16 = out_dtype == PKV_DTYPE_BF16;
+    if (pkv::launch_prefill_chunk(qmap, kmap, vmap, p, max_q_len, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    return PKV_OK;
+}
+
+}  // extern "C"

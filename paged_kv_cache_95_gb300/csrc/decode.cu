@@ -1,0 +1,385 @@
+// decode.cu -- K2: paged decode attention (one CTA per sequence x KV head x
+// partition, serving the whole GQA group), and K3: the log-sum-exp merge of the
+// partitions (Flash-Decoding).
+//
+// What is computed ("LLM 推理全过程的维度变化与核心公式", section "Decode 阶段
+// 维度流转"; "注意力演进与推理流程", section 3.1):
+//   s_j = scale * <q[b][h], K_b[j][g]>,   g = floor(h / G),  j < ctx_b
+//   out[b][h] = sum_j softmax(s)_j V_b[j][g]
+// with K_b[j] at row j % 16 of physical block block_tables[b][j / 16].
+//
+// Design (GB300, HBM bound: every K/V byte is read once per KV head):
+//  * One CTA serves all G query heads of a KV head (up to 8; larger groups are
+//    split over CTAs), so each 4 KB (block, head) tile of K and of V is fetched
+//    from HBM once.  A context is cut into partitions of `part_blocks` blocks
+//    that run as independent CTAs (grid = partitions x heads x sequences); the
+//    partials are combined by K3.
+//  * Inside a CTA each warp owns every NW-th block of the partition and runs
+//    its own pipeline: lane 0 issues TMA tensor copies (128-byte swizzle) of the
+//    block's K and V tiles into a ring of ST stages, completing on one mbarrier
+//    per stage; the warp consumes stage after stage with no CTA-wide barrier.
+//  * The group's dot products run on the tensor cores with warp-level MMA
+//    (m16n8k16, bf16 in, fp32 accumulate), in the transposed form
+//    S^T[16 keys x 8 heads] = K[16 x 128] Q^T[128 x 8] so that up to 8 heads fill
+//    the n = 8 side, and O^T[128 x 8] += V^T[128 x 16] P^T[16 x 8].  The softmax
+//    is the fp32 online softmax (running max m, running sum l, rescale of O when
+//    m rises) with max reductions by warp shuffles across the 8 lanes that share
+//    a head column; probabilities go from the S^T accumulator layout to the
+//    B-operand layout of the second MMA with one movmatrix transpose.
+//  * Keys at or past ctx (the tail of the last block) are masked by index, never
+//    by value, and their V rows are zeroed in registers, so stale or NaN bytes in
+//    unused slots cannot leak into the result.
+//  * At the end the warps' (m, l, O) are combined through shared memory; with a
+//    single partition the CTA writes out = O / l directly, otherwise it writes
+//    the unnormalised partial (m, l, O) to the workspace for K3.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace pkv {
+
+namespace {
+
+constexpr uint32_t kTileBytes = kBlockSize * kHeadDim * 2;  // 4096 B: one (block, head) tile
+constexpr uint32_t kBoxBytes = kTileBytes / 2;              // 2048 B: 16 rows x 64 dims (128-B rows)
+constexpr uint32_t kStageBytes = 2 * kTileBytes;            // K tile + V tile
+
+__device__ __forceinline__ void store_out(void *out, int32_t bf16, size_t idx, float v) {
+    if (bf16)
+        static_cast<__nv_bfloat16 *>(out)[idx] = __float2bfloat16_rn(v);
+    else
+        static_cast<float *>(out)[idx] = v;
+}
+
+template <int NW, int ST>
+__global__ void __launch_bounds__(NW * 32)
+    paged_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                        const DecodeParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem =
+        reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int part = blockIdx.x;
+    const int hs = blockIdx.y;
+    const int b = blockIdx.z;
+    const int g = hs / p.head_splits;
+    const int hpc = p.heads_per_cta;
+    const int h0 = g * p.group + (hs - g * p.head_splits) * hpc;
+
+    // ---- sequence extent (device data: checked, never trusted) ----
+    int ctx = __ldg(p.context_lens + b);
+    const int max_ctx = p.max_blocks * kBlockSize;
+    if (ctx < 1 || ctx > max_ctx) {
+        if (part == 0 && threadIdx.x == 0 && p.status) atomicOr(p.status, kStatusBadContextLen);
+        ctx = ctx < 1 ? 0 : max_ctx;
+    }
+    if (ctx == 0) {
+        if (part == 0)
+            for (int i = threadIdx.x; i < hpc * kHeadDim; i += NW * 32)
+                store_out(p.out, p.out_bf16, (static_cast<size_t>(b) * p.n_q + h0 + (i >> 7)) * kHeadDim + (i & 127),
+                          0.f);
+        return;
+    }
+    const int nblocks = (ctx + kBlockSize - 1) / kBlockSize;
+    const int nparts = (nblocks + p.part_blocks - 1) / p.part_blocks;
+    if (part >= nparts) return;
+    const int blk_begin = part * p.part_blocks;
+    const int nblk = min(p.part_blocks, nblocks - blk_begin);
+    const int nmine = nblk > warp ? (nblk - warp + NW - 1) / NW : 0;
+    const int32_t *table = p.block_tables + static_cast<size_t>(b) * p.max_blocks;
+
+    const uint32_t stage_base = smem_u32(smem) + warp * (ST * kStageBytes);
+    const uint32_t bar_base = smem_u32(smem) + NW * ST * kStageBytes + warp * ST * 8;
+
+    if (lane == 0) {
+        for (int s = 0; s < ST; ++s) mbar_init(bar_base + 8 * s, 1);
+        fence_mbar_init();
+        if (warp == 0) {
+            prefetch_tensormap(&kmap);
+            prefetch_tensormap(&vmap);
+        }
+    }
+    __syncwarp();
+
+    // Lane 0: start the copies of this warp's i-th block into stage i % ST.
+    auto issue = [&](int i) {
+        const int s = i % ST;
+        const int j = blk_begin + warp + NW * i;
+        int phys = __ldg(table + j);
+        if (static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_blocks)) phys = 0;  // masked below
+        const uint32_t bar = bar_base + 8 * s;
+        const uint32_t dst = stage_base + s * kStageBytes;
+        mbar_arrive_expect_tx(bar, kStageBytes);
+        tma_load_4d(dst, &kmap, bar, 0, 0, g, phys);
+        tma_load_4d(dst + kBoxBytes, &kmap, bar, 64, 0, g, phys);
+        tma_load_4d(dst + kTileBytes, &vmap, bar, 0, 0, g, phys);
+        tma_load_4d(dst + kTileBytes + kBoxBytes, &vmap, bar, 64, 0, g, phys);
+    };
+    if (lane == 0)
+        for (int i = 0; i < ST && i < nmine; ++i) issue(i);
+
+    // ---- Q^T as the B operand (16 dims x 8 heads per k-step), kept in registers ----
+    const int n = lane >> 2;  // head column of B / row group of C
+    const int q4 = lane & 3;
+    uint32_t bq[8][2];
+    {
+        const bool hv = n < hpc;
+        const uint32_t *qrow = reinterpret_cast<const uint32_t *>(static_cast<const __nv_bfloat16 *>(p.q) +
+                                                                  (static_cast<size_t>(b) * p.n_q + h0 + n) * kHeadDim);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            bq[kk][0] = hv ? __ldg(qrow + (16 * kk + 2 * q4) / 2) : 0u;
+            bq[kk][1] = hv ? __ldg(qrow + (16 * kk + 8 + 2 * q4) / 2) : 0u;
+        }
+    }
+
+    // Per-lane swizzled ldmatrix row offsets.  128-byte swizzle: 16-byte chunk c
+    // of row r lives at chunk c ^ (r & 7).
+    const int kkey = (lane & 7) | (((lane >> 3) & 1) << 3);  // K: matrices (keys 0-7 | 8-15) x (dims lo | hi)
+    const int khi = lane >> 4;
+    const int vkey = (lane & 7) | ((lane >> 4) << 3);        // V: matrices (dims lo | hi) x (keys 0-7 | 8-15)
+    const int vhi = (lane >> 3) & 1;
+
+    float m0 = -INFINITY, m1 = -INFINITY;  // running max of head columns 2*q4, 2*q4+1 (log2 domain)
+    float l0 = 0.f, l1 = 0.f;              // this lane's share of the running sums
+    float o[8][4];
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+
+    const float sl2 = p.scale_log2;
+    int consumed = 0;
+    bool timed_out = false;
+    for (int i = 0; i < nmine; ++i) {
+        const int s = i % ST;
+        const uint32_t bar = bar_base + 8 * s;
+        bool ok = mbar_wait(bar, (i / ST) & 1);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) {
+            timed_out = true;
+            break;
+        }
+        const int j = blk_begin + warp + NW * i;
+        const int phys = __ldg(table + j);
+        int valid = min(kBlockSize, ctx - j * kBlockSize);
+        if (static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_blocks)) {
+            valid = 0;
+            if (lane == 0 && p.status) atomicOr(p.status, kStatusBadBlockId);
+        }
+        const uint32_t kb = stage_base + s * kStageBytes;
+        const uint32_t vb = kb + kTileBytes;
+
+        // S^T = K Q^T  (rows: keys, columns: heads)
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const int chunk = 2 * kk + khi;
+            const uint32_t addr = kb + (chunk >> 3) * kBoxBytes + kkey * 128 + (((chunk & 7) ^ (lane & 7)) << 4);
+            uint32_t a[4];
+            ldmatrix_x4(a, addr);
+            mma_bf16_16816(c, a, bq[kk][0], bq[kk][1]);
+        }
+
+        // Online softmax in the log2 domain (scale * log2(e) folded into the scores).
+        const int key_a = n, key_b = n + 8;
+        const float s00 = key_a < valid ? c[0] * sl2 : -INFINITY;
+        const float s01 = key_a < valid ? c[1] * sl2 : -INFINITY;
+        const float s10 = key_b < valid ? c[2] * sl2 : -INFINITY;
+        const float s11 = key_b < valid ? c[3] * sl2 : -INFINITY;
+        float bm0 = fmaxf(s00, s10), bm1 = fmaxf(s01, s11);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
+            bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
+        }
+        const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+        const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
+        const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float al0 = fast_exp2(m0 - mu0), al1 = fast_exp2(m1 - mu1);
+        const float p00 = fast_exp2(s00 - mu0), p01 = fast_exp2(s01 - mu1);
+        const float p10 = fast_exp2(s10 - mu0), p11 = fast_exp2(s11 - mu1);
+        l0 = l0 * al0 + p00 + p10;
+        l1 = l1 * al1 + p01 + p11;
+        m0 = mn0;
+        m1 = mn1;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            o[mt][0] *= al0;
+            o[mt][1] *= al1;
+            o[mt][2] *= al0;
+            o[mt][3] *= al1;
+        }
+
+        // P (C layout: row key, col head) -> P^T in the B-operand layout.
+        const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p00, p01));  // keys 0-7
+        const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p10, p11));  // keys 8-15
+
+        // Zero V rows of keys >= valid (their P is 0, but 0 * NaN would not be).
+        uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;
+        if (valid < kBlockSize) {
+            const int ka = 2 * q4, kb2 = 2 * q4 + 8;
+            vm_lo = (ka < valid ? 0x0000ffffu : 0u) | (ka + 1 < valid ? 0xffff0000u : 0u);
+            vm_hi = (kb2 < valid ? 0x0000ffffu : 0u) | (kb2 + 1 < valid ? 0xffff0000u : 0u);
+        }
+
+        // O^T += V^T P^T  (rows: head dims, columns: heads)
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            const int chunk = 2 * mt + vhi;
+            const uint32_t addr = vb + (chunk >> 3) * kBoxBytes + vkey * 128 + (((chunk & 7) ^ (lane & 7)) << 4);
+            uint32_t a[4];
+            ldmatrix_x4_trans(a, addr);
+            a[0] &= vm_lo;
+            a[1] &= vm_lo;
+            a[2] &= vm_hi;
+            a[3] &= vm_hi;
+            mma_bf16_16816(o[mt], a, pb0, pb1);
+        }
+        consumed = i + 1;
+
+        __syncwarp();
+        if (lane == 0 && i + ST < nmine) {
+            fence_proxy_async_smem();
+            issue(i + ST);
+        }
+    }
+
+    if (timed_out) {
+        if (lane == 0 && p.status) atomicOr(p.status, kStatusTimeout);
+        // Let this warp's copies still in flight land before the CTA exits.
+        const int issued = min(nmine, consumed + ST);
+        for (int i = consumed; i < issued; ++i) mbar_wait(bar_base + 8 * (i % ST), (i / ST) & 1);
+    }
+
+    // Full row sums of this warp: add the shares of the 8 lanes of a head column.
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+
+    // ---- combine the warps of the CTA (shared memory reused after the pipeline) ----
+    __syncthreads();
+    float *red_o = reinterpret_cast<float *>(smem);  // [NW][8 heads][128]
+    float *red_m = red_o + NW * 8 * kHeadDim;        // [NW][8]
+    float *red_l = red_m + NW * 8;                   // [NW][8]
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+        const int d0 = 16 * mt + n;
+        red_o[(warp * 8 + 2 * q4) * kHeadDim + d0] = o[mt][0];
+        red_o[(warp * 8 + 2 * q4 + 1) * kHeadDim + d0] = o[mt][1];
+        red_o[(warp * 8 + 2 * q4) * kHeadDim + d0 + 8] = o[mt][2];
+        red_o[(warp * 8 + 2 * q4 + 1) * kHeadDim + d0 + 8] = o[mt][3];
+    }
+    if (lane < 4) {
+        red_m[warp * 8 + 2 * lane] = m0;
+        red_m[warp * 8 + 2 * lane + 1] = m1;
+        red_l[warp * 8 + 2 * lane] = l0;
+        red_l[warp * 8 + 2 * lane + 1] = l1;
+    }
+    __syncthreads();
+
+    for (int idx = threadIdx.x; idx < hpc * kHeadDim; idx += NW * 32) {
+        const int hh = idx >> 7, d = idx & 127;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, red_m[w * 8 + hh]);
+        const float Mu = M == -INFINITY ? 0.f : M;
+        float L = 0.f, O = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            const float f = fast_exp2(red_m[w * 8 + hh] - Mu);
+            L += f * red_l[w * 8 + hh];
+            O += f * red_o[(w * 8 + hh) * kHeadDim + d];
+        }
+        const size_t row = static_cast<size_t>(b) * p.n_q + h0 + hh;
+        if (nparts == 1) {
+            store_out(p.out, p.out_bf16, row * kHeadDim + d, L > 0.f ? O / L : 0.f);
+        } else {
+            const size_t pi = row * p.max_parts + part;
+            p.part_o[pi * kHeadDim + d] = O;
+            if (d == 0) {
+                p.part_m[pi] = M;
+                p.part_l[pi] = L;
+            }
+        }
+    }
+}
+
+// K3: out[b][h] = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p,  M = max_p m_p.
+__global__ void __launch_bounds__(kHeadDim) lse_merge_kernel(const DecodeParams p) {
+    const int h = blockIdx.x;
+    const int b = blockIdx.y;
+    const int d = threadIdx.x;
+    int ctx = __ldg(p.context_lens + b);
+    const int max_ctx = p.max_blocks * kBlockSize;
+    ctx = ctx < 1 ? 0 : (ctx > max_ctx ? max_ctx : ctx);
+    const int nparts = ((ctx + kBlockSize - 1) / kBlockSize + p.part_blocks - 1) / p.part_blocks;
+    if (nparts <= 1) return;  // written directly by K2
+    const size_t base = (static_cast<size_t>(b) * p.n_q + h) * p.max_parts;
+    float M = -INFINITY;
+    for (int i = 0; i < nparts; ++i) M = fmaxf(M, __ldg(p.part_m + base + i));
+    const float Mu = M == -INFINITY ? 0.f : M;
+    float L = 0.f, O = 0.f;
+    for (int i = 0; i < nparts; ++i) {
+        const float f = fast_exp2(__ldg(p.part_m + base + i) - Mu);
+        L += f * __ldg(p.part_l + base + i);
+        O += f * __ldg(p.part_o + (base + i) * kHeadDim + d);
+    }
+    store_out(p.out, p.out_bf16, (static_cast<size_t>(b) * p.n_q + h) * kHeadDim + d, L > 0.f ? O / L : 0.f);
+}
+
+template <int NW, int ST>
+cudaError_t launch_variant(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParams &p,
+                           cudaStream_t stream) {
+    const dim3 grid(p.max_parts, p.n_kv * p.head_splits, p.num_seqs);
+    paged_decode_kernel<NW, ST><<<grid, NW * 32, decode_smem_bytes({NW, ST}), stream>>>(kmap, vmap, p);
+    return cudaGetLastError();
+}
+
+template <int NW, int ST>
+cudaError_t prepare_variant() {
+    return cudaFuncSetAttribute(paged_decode_kernel<NW, ST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(decode_smem_bytes({NW, ST})));
+}
+
+}  // namespace
+
+size_t decode_smem_bytes(DecodeVariant v) {
+    // stage ring + mbarriers + 1 KB for aligning the base to the 1 KB swizzle period
+    return static_cast<size_t>(v.warps) * v.stages * kStageBytes + static_cast<size_t>(v.warps) * v.stages * 8 + 1024;
+}
+
+bool decode_variant_supported(DecodeVariant v) {
+    return (v.warps == 4 && (v.stages == 2 || v.stages == 3 || v.stages == 4)) || (v.warps == 8 && v.stages == 2);
+}
+
+cudaError_t decode_prepare_device(DecodeVariant v) {
+    if (v.warps == 4 && v.stages == 2) return prepare_variant<4, 2>();
+    if (v.warps == 4 && v.stages == 3) return prepare_variant<4, 3>();
+    if (v.warps == 4 && v.stages == 4) return prepare_variant<4, 4>();
+    if (v.warps == 8 && v.stages == 2) return prepare_variant<8, 2>();
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_paged_decode(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParams &p,
+                                DecodeVariant v, cudaStream_t stream) {
+    if (v.warps == 4 && v.stages == 2) return launch_variant<4, 2>(kmap, vmap, p, stream);
+    if (v.warps == 4 && v.stages == 3) return launch_variant<4, 3>(kmap, vmap, p, stream);
+    if (v.warps == 4 && v.stages == 4) return launch_variant<4, 4>(kmap, vmap, p, stream);
+    if (v.warps == 8 && v.stages == 2) return launch_variant<8, 2>(kmap, vmap, p, stream);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_lse_merge(const DecodeParams &p, cudaStream_t stream) {
+    const dim3 grid(p.n_q, p.num_seqs);
+    lse_merge_kernel<<<grid, kHeadDim, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace pkv

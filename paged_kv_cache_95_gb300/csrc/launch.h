@@ -1,0 +1,80 @@
+// launch.h -- internal interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace pkv {
+
+constexpr int kHeadDim = 128;
+constexpr int kBlockSize = 16;
+
+// Device status bits (mirror the PKV_STATUS_* values of the public header).
+constexpr uint32_t kStatusBadContextLen = 0x1u;
+constexpr uint32_t kStatusBadBlockId = 0x2u;
+constexpr uint32_t kStatusBadQLen = 0x4u;
+constexpr uint32_t kStatusTimeout = 0x8u;
+
+// ---- K1: cache write ----------------------------------------------------------
+cudaError_t launch_kv_cache_write(const void *key, const void *value, void *k_cache, void *v_cache,
+                                  const int32_t *slot_mapping, int32_t num_tokens, int32_t n_kv,
+                                  int32_t num_blocks, int sm_count, cudaStream_t stream);
+
+// ---- K2/K3: decode with optional split-KV and its log-sum-exp merge ------------
+struct DecodeParams {
+    const void *q;               // bf16 [num_seqs][n_q][128]
+    void *out;                   // [num_seqs][n_q][128], f32 or bf16
+    const int32_t *block_tables; // [num_seqs][max_blocks]
+    const int32_t *context_lens; // [num_seqs]
+    float *part_m;               // [num_seqs][n_q][max_parts]   (log2 domain, scale folded in)
+    float *part_l;               // [num_seqs][n_q][max_parts]
+    float *part_o;               // [num_seqs][n_q][max_parts][128] (unnormalised)
+    uint32_t *status;            // device status word or nullptr
+    int32_t num_seqs, n_q, n_kv;
+    int32_t group;               // G = n_q / n_kv
+    int32_t heads_per_cta;       // min(G, 8)
+    int32_t head_splits;         // G / heads_per_cta
+    int32_t max_blocks;          // block-table row length
+    int32_t num_blocks;          // pool size
+    int32_t part_blocks;         // blocks per partition
+    int32_t max_parts;           // partitions of the longest possible context
+    float scale_log2;            // scale * log2(e)
+    int32_t out_bf16;            // 1: bf16 output, 0: f32
+};
+
+struct DecodeVariant {
+    int warps;
+    int stages;
+};
+
+// Shared-memory bytes and supported variants of the decode kernel.
+size_t decode_smem_bytes(DecodeVariant v);
+bool decode_variant_supported(DecodeVariant v);
+cudaError_t decode_prepare_device(DecodeVariant v);  // sets the dynamic shared memory limit
+cudaError_t launch_paged_decode(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParams &p,
+                                DecodeVariant v, cudaStream_t stream);
+cudaError_t launch_lse_merge(const DecodeParams &p, cudaStream_t stream);
+
+// ---- K4: causal chunked prefill on tcgen05 ---------------------------------------
+struct PrefillParams {
+    void *out;                   // [total_rows][n_q][128]
+    const int32_t *cu_q_lens;    // [num_seqs + 1]
+    const int32_t *block_tables; // [num_seqs][max_blocks]
+    const int32_t *context_lens; // [num_seqs]
+    uint32_t *status;
+    int32_t num_seqs, n_q, n_kv, group;
+    int32_t rows_per_tile;       // query positions per 128-row tile (128 / G)
+    int32_t max_blocks, num_blocks;
+    int32_t total_rows;
+    float scale_log2;
+    int32_t out_bf16;
+};
+
+size_t prefill_smem_bytes();
+cudaError_t prefill_prepare_device();
+cudaError_t launch_prefill_chunk(const CUtensorMap &qmap, const CUtensorMap &kmap, const CUtensorMap &vmap,
+                                 const PrefillParams &p, int max_q_len, cudaStream_t stream);
+
+}  // namespace pkv

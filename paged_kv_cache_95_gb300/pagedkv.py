@@ -1,0 +1,239 @@
+"""ctypes binding of libpagedkv.so (the C ABI in include/pagedkv.h).
+
+Argument marshalling only: every function checks that the torch tensors it
+is given have the dtype, device, shape and contiguity the C ABI documents,
+then passes their device pointers, sizes and the current CUDA stream to the
+entry point of the same name.  All computation happens in the library's CUDA
+kernels; there is no fallback of any kind.  If the library is missing, the
+first call raises ``RuntimeError`` (build it with ``__graft_entry__.build()``
+or ``python -m paged_kv_cache_95_gb300.build``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+PKV_DTYPE_BF16 = 0
+PKV_DTYPE_FLOAT32 = 1
+
+PKV_OK = 0
+PKV_ERR_INVALID_ARG = -1
+PKV_ERR_UNSUPPORTED = -2
+PKV_ERR_WORKSPACE_TOO_SMALL = -3
+PKV_ERR_CUDA = -4
+
+PKV_STATUS_BAD_CONTEXT_LEN = 0x1
+PKV_STATUS_BAD_BLOCK_ID = 0x2
+PKV_STATUS_BAD_Q_LEN = 0x4
+PKV_STATUS_TIMEOUT = 0x8
+
+HEAD_DIM = 128
+BLOCK_SIZE = 16
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpagedkv.so")
+HEADER_PATH = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "pagedkv.h")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class CacheDesc(ctypes.Structure):
+    """Mirror of ``pkv_cache_desc``."""
+
+    _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        self.code = code
+        super().__init__(f"{fn} failed: {status_string(code)} ({code})")
+
+
+def load_library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libpagedkv.so and declare the C signatures."""
+    global _lib
+    if path is None:
+        with _lock:
+            if _lib is None:
+                if not os.path.exists(LIB_PATH):
+                    raise RuntimeError(f"{LIB_PATH} is missing: build the CUDA library first "
+                                       "(python -c 'import __graft_entry__ as g; g.build()')")
+                _lib = _declare(ctypes.CDLL(LIB_PATH))
+            return _lib
+    return _declare(ctypes.CDLL(path))
+
+
+def _declare(lib):
+    P, i32, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+    D = ctypes.POINTER(CacheDesc)
+    lib.kv_reshape_and_cache.argtypes = [P, P, P, P, P, i32, D, P]
+    lib.kv_reshape_and_cache.restype = ctypes.c_int
+    lib.paged_attention_workspace_size.argtypes = [i32, i32, i32, i32, D]
+    lib.paged_attention_workspace_size.restype = sz
+    lib.paged_attention_decode.argtypes = [P, i32, P, P, P, P, P, i32, i32, i32, f32, i32, D, P, sz, P]
+    lib.paged_attention_decode.restype = ctypes.c_int
+    lib.paged_attention_prefill_workspace_size.argtypes = [i32, i32, D]
+    lib.paged_attention_prefill_workspace_size.restype = sz
+    lib.paged_attention_prefill_chunk.argtypes = [P, i32, P, P, i32, i32, P, P, P, P, i32, i32, i32, f32, D, P, sz, P]
+    lib.paged_attention_prefill_chunk.restype = ctypes.c_int
+    lib.pagedkv_status_string.argtypes = [ctypes.c_int]
+    lib.pagedkv_status_string.restype = ctypes.c_char_p
+    lib.pagedkv_version.argtypes = []
+    lib.pagedkv_version.restype = ctypes.c_int
+    return lib
+
+
+def status_string(code: int) -> str:
+    try:
+        return load_library().pagedkv_status_string(int(code)).decode()
+    except RuntimeError:
+        return f"status {code}"
+
+
+def version() -> int:
+    return int(load_library().pagedkv_version())
+
+
+# ---- tensor marshalling ----------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t) -> int:
+    return int(t.data_ptr())
+
+
+def _stream(stream) -> int:
+    torch = _torch()
+    if stream is None:
+        return int(torch.cuda.current_stream().cuda_stream)
+    return int(stream.cuda_stream if hasattr(stream, "cuda_stream") else stream)
+
+
+def _need(cond: bool, msg: str):
+    if not cond:
+        raise ValueError(msg)
+
+
+def _check(t, name, dtype, ndim=None, last=None):
+    torch = _torch()
+    _need(isinstance(t, torch.Tensor), f"{name} must be a torch.Tensor")
+    _need(t.is_cuda, f"{name} must be a CUDA tensor")
+    _need(t.dtype == dtype, f"{name} must be {dtype}, got {t.dtype}")
+    _need(t.is_contiguous(), f"{name} must be contiguous")
+    if ndim is not None:
+        _need(t.dim() == ndim, f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    if last is not None:
+        _need(t.shape[-1] == last, f"{name} last dim must be {last}")
+
+
+def cache_desc(k_cache) -> CacheDesc:
+    """Descriptor of a pool tensor [num_blocks, n_kv, 16, 128] (bf16)."""
+    torch = _torch()
+    _check(k_cache, "k_cache", torch.bfloat16, ndim=4, last=HEAD_DIM)
+    nb, n_kv, bs, d = k_cache.shape
+    return CacheDesc(int(nb), int(bs), int(n_kv), int(d), PKV_DTYPE_BF16)
+
+
+def _out_dtype(out) -> int:
+    torch = _torch()
+    if out.dtype == torch.float32:
+        return PKV_DTYPE_FLOAT32
+    if out.dtype == torch.bfloat16:
+        return PKV_DTYPE_BF16
+    raise ValueError(f"out must be float32 or bfloat16, got {out.dtype}")
+
+
+def _raise(fn, rc):
+    if rc != PKV_OK:
+        raise PagedKVError(fn, rc)
+
+
+# ---- entry points (same names as the C ABI) ----------------------------------------
+
+def kv_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, stream=None) -> None:
+    torch = _torch()
+    desc = cache_desc(k_cache)
+    _check(v_cache, "v_cache", torch.bfloat16, ndim=4)
+    _need(tuple(v_cache.shape) == tuple(k_cache.shape), "v_cache shape must equal k_cache shape")
+    _check(key, "key", torch.bfloat16, ndim=3, last=HEAD_DIM)
+    _check(value, "value", torch.bfloat16, ndim=3, last=HEAD_DIM)
+    _check(slot_mapping, "slot_mapping", torch.int32, ndim=1)
+    T = slot_mapping.shape[0]
+    _need(tuple(key.shape) == (T, desc.num_kv_heads, HEAD_DIM), "key must be [num_tokens, n_kv, 128]")
+    _need(tuple(value.shape) == tuple(key.shape), "value shape must equal key shape")
+    rc = load_library().kv_reshape_and_cache(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache),
+                                             _ptr(slot_mapping), int(T), ctypes.byref(desc), _stream(stream))
+    _raise("kv_reshape_and_cache", rc)
+
+
+def paged_attention_workspace_size(num_seqs: int, num_q_heads: int, max_blocks_per_seq: int,
+                                   partition_size: int, cache: CacheDesc) -> int:
+    return int(load_library().paged_attention_workspace_size(num_seqs, num_q_heads, max_blocks_per_seq,
+                                                             partition_size, ctypes.byref(cache)))
+
+
+def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                           workspace=None, partition_size: int = 0, stream=None):
+    """Decode attention; ``workspace`` (uint8 CUDA tensor) is allocated if None."""
+    torch = _torch()
+    desc = cache_desc(k_cache)
+    _check(v_cache, "v_cache", torch.bfloat16, ndim=4)
+    _need(tuple(v_cache.shape) == tuple(k_cache.shape), "v_cache shape must equal k_cache shape")
+    _check(q, "q", torch.bfloat16, ndim=3, last=HEAD_DIM)
+    B, n_q, _ = q.shape
+    _check(out, "out", out.dtype, ndim=3)
+    _need(tuple(out.shape) == tuple(q.shape), "out must have q's shape")
+    _check(block_tables, "block_tables", torch.int32, ndim=2)
+    _check(context_lens, "context_lens", torch.int32, ndim=1)
+    _need(block_tables.shape[0] == B and context_lens.shape[0] == B, "one table row and length per sequence")
+    max_blocks = int(block_tables.shape[1])
+    if workspace is None:
+        nbytes = paged_attention_workspace_size(B, n_q, max_blocks, partition_size, desc)
+        _need(nbytes > 0, "invalid sizes for paged_attention_decode")
+        workspace = torch.zeros(nbytes, dtype=torch.uint8, device=q.device)  # status word starts clear
+    _check(workspace, "workspace", torch.uint8, ndim=1)
+    rc = load_library().paged_attention_decode(
+        _ptr(out), _out_dtype(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        int(B), int(n_q), max_blocks, float(scale), int(partition_size), ctypes.byref(desc), _ptr(workspace),
+        int(workspace.numel()), _stream(stream))
+    _raise("paged_attention_decode", rc)
+    return workspace
+
+
+def paged_attention_prefill_workspace_size(num_seqs: int, num_q_heads: int, cache: CacheDesc) -> int:
+    return int(load_library().paged_attention_prefill_workspace_size(num_seqs, num_q_heads, ctypes.byref(cache)))
+
+
+def paged_attention_prefill_chunk(out, q, cu_q_lens, max_q_len: int, k_cache, v_cache, block_tables, context_lens,
+                                  scale: float, workspace=None, stream=None):
+    """Causal chunked-prefill attention; ``workspace`` is allocated if None."""
+    torch = _torch()
+    desc = cache_desc(k_cache)
+    _check(v_cache, "v_cache", torch.bfloat16, ndim=4)
+    _need(tuple(v_cache.shape) == tuple(k_cache.shape), "v_cache shape must equal k_cache shape")
+    _check(q, "q", torch.bfloat16, ndim=3, last=HEAD_DIM)
+    rows, n_q, _ = q.shape
+    _check(out, "out", out.dtype, ndim=3)
+    _need(tuple(out.shape) == tuple(q.shape), "out must have q's shape")
+    _check(cu_q_lens, "cu_q_lens", torch.int32, ndim=1)
+    _check(block_tables, "block_tables", torch.int32, ndim=2)
+    _check(context_lens, "context_lens", torch.int32, ndim=1)
+    B = int(context_lens.shape[0])
+    _need(cu_q_lens.shape[0] == B + 1 and block_tables.shape[0] == B, "cu_q_lens is [B+1], block_tables [B, *]")
+    if workspace is None:
+        nbytes = paged_attention_prefill_workspace_size(B, n_q, desc)
+        _need(nbytes > 0, "invalid sizes for paged_attention_prefill_chunk")
+        workspace = torch.zeros(nbytes, dtype=torch.uint8, device=q.device)  # status word starts clear
+    _check(workspace, "workspace", torch.uint8, ndim=1)
+    rc = load_library().paged_attention_prefill_chunk(
+        _ptr(out), _out_dtype(out), _ptr(q), _ptr(cu_q_lens), int(max_q_len), int(rows), _ptr(k_cache),
+        _ptr(v_cache), _ptr(block_tables), _ptr(context_lens), B, int(n_q), int(block_tables.shape[1]),
+        float(scale), ctypes.byref(desc), _ptr(workspace), int(workspace.numel()), _stream(stream))
+    _raise("paged_attention_prefill_chunk", rc)
+    return workspace

@@ -26,3 +26,10 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def built_library():
+    """Build libpagedkv.so in-tree (no-op when up to date); needs nvcc, not a GPU."""
+    from paged_kv_cache_95_gb300 import build
+    return build.build()

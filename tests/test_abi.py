@@ -1,0 +1,134 @@
+"""The C-ABI library: it loads, exports every declared symbol, and validates
+its arguments on the host before anything reaches the GPU (CPU only: every
+call below returns from argument checking without a CUDA call)."""
+import ctypes
+import re
+
+import pytest
+
+from paged_kv_cache_95_gb300 import pagedkv as P
+
+FAKE = 0x100000  # never dereferenced: validation fails before any device access
+
+
+@pytest.fixture(scope="module")
+def lib(built_library):
+    return P.load_library()
+
+
+def declared_symbols():
+    text = open(P.HEADER_PATH).read()
+    return re.findall(r"PKV_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+
+
+def test_header_declares_the_boundary():
+    names = set(declared_symbols())
+    assert {"kv_reshape_and_cache", "paged_attention_decode", "paged_attention_prefill_chunk",
+            "paged_attention_workspace_size", "paged_attention_prefill_workspace_size",
+            "pagedkv_status_string", "pagedkv_version"} <= names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), f"libpagedkv.so does not export {name}"
+
+
+def test_status_strings_and_version(lib):
+    for code in (0, -1, -2, -3, -4):
+        assert lib.pagedkv_status_string(code)
+    assert b"unknown" in lib.pagedkv_status_string(12345)
+    assert lib.pagedkv_version() >= 100
+
+
+def desc(num_blocks=100, bs=16, n_kv=8, d=128, dtype=0):
+    return P.CacheDesc(num_blocks, bs, n_kv, d, dtype)
+
+
+def test_workspace_size_math(lib):
+    c = desc()
+    # 64 seqs, 32 heads, 256 blocks/seq, 512-token partitions -> 8 parts
+    rows = 64 * 32 * 8
+    want = 256 + 2 * ((rows * 4 + 255) // 256 * 256) + rows * 128 * 4
+    assert lib.paged_attention_workspace_size(64, 32, 256, 512, ctypes.byref(c)) == want
+    # a partition that covers the whole context needs only the status word
+    assert lib.paged_attention_workspace_size(64, 32, 256, 4096, ctypes.byref(c)) == 256
+    # automatic plans are covered by the smallest automatic partition (256 tokens)
+    assert lib.paged_attention_workspace_size(64, 32, 256, 0, ctypes.byref(c)) == \
+        lib.paged_attention_workspace_size(64, 32, 256, 256, ctypes.byref(c))
+    assert lib.paged_attention_workspace_size(64, 32, 256, 100, ctypes.byref(c)) == 0  # not a multiple of 16
+    assert lib.paged_attention_workspace_size(64, 30, 256, 0, ctypes.byref(c)) == 0    # 30 % 8 != 0
+    assert lib.paged_attention_prefill_workspace_size(4, 32, ctypes.byref(c)) == 256
+
+
+def _decode(lib, c, **kw):
+    a = dict(out=FAKE, out_dtype=1, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, cl=FAKE, B=4, nq=32, mb=8, scale=0.088,
+             part=0, ws=FAKE, wsb=1 << 20, stream=None)
+    a.update(kw)
+    return lib.paged_attention_decode(a["out"], a["out_dtype"], a["q"], a["k"], a["v"], a["bt"], a["cl"], a["B"],
+                                      a["nq"], a["mb"], a["scale"], a["part"], ctypes.byref(c), a["ws"], a["wsb"],
+                                      a["stream"])
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(out=None), P.PKV_ERR_INVALID_ARG),
+    (dict(q=None), P.PKV_ERR_INVALID_ARG),
+    (dict(bt=None), P.PKV_ERR_INVALID_ARG),
+    (dict(ws=None), P.PKV_ERR_INVALID_ARG),
+    (dict(B=0), P.PKV_ERR_INVALID_ARG),
+    (dict(B=70000), P.PKV_ERR_INVALID_ARG),
+    (dict(mb=0), P.PKV_ERR_INVALID_ARG),
+    (dict(nq=30), P.PKV_ERR_INVALID_ARG),             # 30 % 8
+    (dict(nq=96), P.PKV_ERR_UNSUPPORTED),             # G = 12
+    (dict(part=100), P.PKV_ERR_INVALID_ARG),          # not a multiple of 16
+    (dict(part=-16), P.PKV_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), P.PKV_ERR_INVALID_ARG),
+    (dict(out_dtype=7), P.PKV_ERR_UNSUPPORTED),
+    (dict(k=FAKE + 8), P.PKV_ERR_INVALID_ARG),        # pool not 16-byte aligned
+    (dict(ws=FAKE + 64), P.PKV_ERR_INVALID_ARG),      # workspace not 256-byte aligned
+    (dict(part=256, mb=64, wsb=1024), P.PKV_ERR_WORKSPACE_TOO_SMALL),
+    (dict(wsb=100), P.PKV_ERR_WORKSPACE_TOO_SMALL),
+])
+def test_decode_argument_errors(lib, kw, want):
+    assert _decode(lib, desc(), **kw) == want
+
+
+@pytest.mark.parametrize("c,want", [
+    (desc(bs=32), P.PKV_ERR_UNSUPPORTED),
+    (desc(d=64), P.PKV_ERR_UNSUPPORTED),
+    (desc(dtype=1), P.PKV_ERR_UNSUPPORTED),
+    (desc(num_blocks=0), P.PKV_ERR_INVALID_ARG),
+    (desc(n_kv=0), P.PKV_ERR_INVALID_ARG),
+])
+def test_cache_descriptor_errors(lib, c, want):
+    assert _decode(lib, c) == want
+    assert lib.kv_reshape_and_cache(FAKE, FAKE, FAKE, FAKE, FAKE, 4, ctypes.byref(c), None) == want
+
+
+def test_cache_write_argument_errors(lib):
+    c = desc()
+    assert lib.kv_reshape_and_cache(FAKE, FAKE, FAKE, FAKE, FAKE, -1, ctypes.byref(c), None) == P.PKV_ERR_INVALID_ARG
+    assert lib.kv_reshape_and_cache(None, FAKE, FAKE, FAKE, FAKE, 4, ctypes.byref(c), None) == P.PKV_ERR_INVALID_ARG
+    assert lib.kv_reshape_and_cache(FAKE + 4, FAKE, FAKE, FAKE, FAKE, 4, ctypes.byref(c), None) == \
+        P.PKV_ERR_INVALID_ARG
+    assert lib.kv_reshape_and_cache(FAKE, FAKE, FAKE, FAKE, FAKE, 4, None, None) == P.PKV_ERR_INVALID_ARG
+    # zero tokens: nothing to do, nothing enqueued
+    assert lib.kv_reshape_and_cache(None, None, None, None, None, 0, ctypes.byref(c), None) == P.PKV_OK
+
+
+def test_prefill_argument_errors(lib):
+    c = desc()
+
+    def call(**kw):
+        a = dict(out=FAKE, dt=1, q=FAKE, cu=FAKE, mq=512, rows=2048, k=FAKE, v=FAKE, bt=FAKE, cl=FAKE, B=4, nq=32,
+                 mb=96, scale=0.088, ws=FAKE, wsb=256)
+        a.update(kw)
+        return lib.paged_attention_prefill_chunk(a["out"], a["dt"], a["q"], a["cu"], a["mq"], a["rows"], a["k"],
+                                                 a["v"], a["bt"], a["cl"], a["B"], a["nq"], a["mb"], a["scale"],
+                                                 ctypes.byref(c), a["ws"], a["wsb"], None)
+    assert call(cu=None) == P.PKV_ERR_INVALID_ARG
+    assert call(nq=24) == P.PKV_ERR_UNSUPPORTED         # G = 3 does not tile 128 rows
+    assert call(mq=-1) == P.PKV_ERR_INVALID_ARG
+    assert call(q=FAKE + 4) == P.PKV_ERR_INVALID_ARG    # TMA needs a 16-byte aligned q
+    assert call(wsb=8) == P.PKV_ERR_WORKSPACE_TOO_SMALL
+    assert call(ws=None) == P.PKV_ERR_INVALID_ARG
+    assert call(mq=0) == P.PKV_OK                        # empty chunk: nothing enqueued
