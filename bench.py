@@ -226,15 +226,23 @@ def run_ours(args):
     new_k, new_v, slots = up_bf16(wl.new_key), up_bf16(wl.new_value), up_i32(wl.slot_mapping)
     q, tables, lens = up_bf16(batch.q), up_i32(batch.block_tables), up_i32(batch.context_lens)
     out = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+    chunk = wl.chunk  # causal prefill chunks of a mixed batch (None for decode-only workloads)
+    if chunk is not None:
+        cq, ccu, ctab, clen = (up_bf16(chunk.q), up_i32(chunk.cu_q_lens), up_i32(chunk.block_tables),
+                               up_i32(chunk.context_lens))
+        cout = torch.empty(cq.shape, dtype=torch.bfloat16, device=dev)
+        cws = torch.zeros(256, dtype=torch.uint8, device=dev)
+        cmax = int(chunk.q_lens.max())
+        chunk_flops = _chunk_flops(chunk, wl)
     desc = P.cache_desc(k_cache)
     ws_bytes = P.paged_attention_workspace_size(batch.num_seqs, wl.n_q, batch.max_blocks_per_seq, 0, desc)
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
     kv_bytes = wl.kv_read_bytes(batch)
+    chunk_kv_bytes = wl.kv_read_bytes(chunk) if chunk is not None else 0
     pool_bytes = 2 * k_cache.numel() * 2
 
     stream = torch.cuda.current_stream(dev)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(args.steps)]
 
     def step(i=None):
         if i is not None:
@@ -242,9 +250,14 @@ def run_ours(args):
         P.kv_reshape_and_cache(new_k, new_v, k_cache, v_cache, slots)
         if i is not None:
             ev[i][1].record(stream)
-        P.paged_attention_decode(out, q, k_cache, v_cache, tables, lens, wl.scale, workspace=ws)
+        if chunk is not None:
+            P.paged_attention_prefill_chunk(cout, cq, ccu, cmax, k_cache, v_cache, ctab, clen, wl.scale,
+                                            workspace=cws)
         if i is not None:
             ev[i][2].record(stream)
+        P.paged_attention_decode(out, q, k_cache, v_cache, tables, lens, wl.scale, workspace=ws)
+        if i is not None:
+            ev[i][3].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -269,11 +282,12 @@ def run_ours(args):
     clocks.stop()
 
     total_ms = start.elapsed_time(end)
-    decode_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    decode_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
+    prefill_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev) if chunk is not None else None
     append_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     t_max = max_over_ranks(total_ms / 1e3, dist, device=dev)
     ms_per_step = t_max / args.steps * 1e3
-    value = world * kv_bytes * args.steps / t_max / 1e9
+    value = world * (kv_bytes + chunk_kv_bytes) * args.steps / t_max / 1e9
     st = int(ws[:4].view(torch.int32).item()) & 0xFFFFFFFF
     if st:
         raise RuntimeError(f"device status word set during the bench: {st:#x}")
@@ -286,10 +300,20 @@ def run_ours(args):
     bi = sum(x.numel() * x.element_size() for x in h_in)
     bo = h_out.numel() * h_out.element_size()
 
+    c_in = [pin(x) for x in (cq, ccu, ctab, clen)] if chunk is not None else []
+    c_dev = [torch.empty_like(x) for x in (cq, ccu, ctab, clen)] if chunk is not None else []
+    hc_out = torch.empty(cout.shape, dtype=cout.dtype).pin_memory() if chunk is not None else None
+    bi += sum(x.numel() * x.element_size() for x in c_in)
+    bo += hc_out.numel() * hc_out.element_size() if chunk is not None else 0
+
     def e2e_step():
-        for h, d in zip(h_in, d_in):
+        for h, d in zip(h_in + c_in, d_in + c_dev):
             d.copy_(h, non_blocking=True)
         P.kv_reshape_and_cache(d_in[1], d_in[2], k_cache, v_cache, d_in[3])
+        if chunk is not None:
+            P.paged_attention_prefill_chunk(cout, c_dev[0], c_dev[1], cmax, k_cache, v_cache, c_dev[2], c_dev[3],
+                                            wl.scale, workspace=cws)
+            hc_out.copy_(cout, non_blocking=True)
         P.paged_attention_decode(out, d_in[0], k_cache, v_cache, d_in[4], d_in[5], wl.scale, workspace=ws)
         h_out.copy_(out, non_blocking=True)
 
@@ -304,9 +328,10 @@ def run_ours(args):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_t = max_over_ranks(e0.elapsed_time(e1) / 1e3, dist, device=dev)
-    e2e_value = world * kv_bytes * args.steps / e2e_t / 1e9
+    e2e_value = world * (kv_bytes + chunk_kv_bytes) * args.steps / e2e_t / 1e9
 
-    launches_per_step = 1 + 1 + (1 if _decode_splits(batch, ws_bytes, wl) else 0)
+    # kv_cache_write + (prefill chunk) + paged decode + split-KV merge (when a context is split)
+    launches_per_step = 2 + (1 if chunk is not None else 0) + (1 if ws_bytes > 256 else 0)
 
     if rank == 0:
         peak, peak_src = measured_peaks()
@@ -333,7 +358,7 @@ def run_ours(args):
             "sequences_per_s": round(world * batch.num_seqs * args.steps / t_max, 1),
             "tokens_per_s": round(world * batch.num_seqs * args.steps / t_max, 1),
             "config": _config(wl, batch, kv_bytes, pool_bytes, world),
-            "roofline": {"bound": "hbm", "kernel": "paged_attention_decode (decode + merge launches)",
+            "roofline": {"bound": "hbm", "kernel": "paged_attention_decode (decode kernel + split-KV merge kernel)",
                          "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                          if peak_src == "measured" else "fallback 6.8 TB/s",
@@ -343,6 +368,7 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": bi,
                     "d2h_bytes_per_step": bo, "ms_per_step": round(e2e_t / args.steps * 1e3, 5)},
+            "prefill": None if chunk is None else _prefill_report(chunk_flops, prefill_ms, chunk, wl),
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks.summary(),
         }
@@ -351,8 +377,30 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def _decode_splits(batch, ws_bytes, wl) -> bool:
-    return ws_bytes > 256 and batch.max_blocks_per_seq > 16
+def _chunk_flops(chunk, wl) -> int:
+    """Algorithmic flops of the causal chunks: 4 * n_q * d per visible (query, key) pair."""
+    pairs = 0
+    for ql, ctx in zip(chunk.q_lens.tolist(), chunk.context_lens.tolist()):
+        c = ctx - ql
+        pairs += sum(c + i + 1 for i in range(ql))
+    return 4 * wl.n_q * wl.head_dim * pairs
+
+
+def _bf16_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured burst bf16 (MEASURED_PEAKS.json bf16_tflops)"
+    except Exception:
+        return 1900.0, "fallback 1.9 PFLOP/s"
+
+
+def _prefill_report(flops, ms, chunk, wl):
+    peak, src = _bf16_peak()
+    tflops = flops / (ms / 1e3) / 1e12
+    return {"kernel": "prefill_chunk_kernel (tcgen05)", "algorithmic_flops": flops, "avg_launch_ms": round(ms, 5),
+            "tflops": round(tflops, 2), "peak_tflops": peak, "frac": round(tflops / peak, 4), "peak_source": src,
+            "rows": int(chunk.cu_q_lens[-1]), "kv_read_bytes": wl.kv_read_bytes(chunk)}
 
 
 def _config(wl, batch, kv_bytes, pool_bytes, world):

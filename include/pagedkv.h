@@ -162,10 +162,16 @@ PKV_API size_t paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_he
  *   workspace      : device scratch, 256-B aligned, of at least
  *                    paged_attention_workspace_size(num_seqs, num_q_heads,
  *                    max_blocks_per_seq, partition_size, cache) bytes; holds
- *                    the status word and the per-partition partials.  Its
- *                    contents need no initialisation (except the status word,
- *                    which is only ever ORed into).  Calls that share a
- *                    workspace must not overlap in time (they race on it).
+ *                    the status word, per-group arrival counters and the
+ *                    per-partition partials.  Zero-fill it once before its
+ *                    first use (e.g. cudaMemsetAsync); every call that
+ *                    completes leaves the counters at zero again, so the same
+ *                    workspace serves later calls without clearing (after a
+ *                    call that set PKV_STATUS_TIMEOUT, zero-fill it again).
+ *                    Calls that share a workspace must not overlap in time
+ *                    (they race on it).
+ * Enqueues the decode kernel and, when a context is split into partitions,
+ * the log-sum-exp merge kernel (both with programmatic dependent launch).
  * Errors: PKV_ERR_INVALID_ARG / PKV_ERR_UNSUPPORTED /
  *         PKV_ERR_WORKSPACE_TOO_SMALL / PKV_ERR_CUDA.
  */

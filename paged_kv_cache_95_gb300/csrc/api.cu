@@ -24,7 +24,7 @@ using pkv::kHeadDim;
 
 constexpr int kMaxDevices = 64;
 constexpr int kMinPartBlocks = 16;      // automatic plans never go below 256 tokens per partition
-constexpr int kDefaultPartBlocks = 32;  // 512 tokens
+constexpr int kDefaultPartBlocks = 64;  // 1024 tokens
 constexpr size_t kStatusBytes = 256;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -124,22 +124,27 @@ int check_group(int32_t n_q, int32_t n_kv) {
 }
 
 // ---- decode plan -----------------------------------------------------------------------
+// Workspace layout: [status word | arrival counters | part_m | part_l | part_o],
+// each region 256-byte aligned; only the status word when nothing is split.
 struct DecodePlan {
     int32_t part_blocks;
     int32_t max_parts;
-    size_t off_m, off_l, off_o, total;
+    size_t off_cnt, off_m, off_l, off_o, total;
 };
 
-DecodePlan plan_decode(int32_t num_seqs, int32_t n_q, int32_t max_blocks, int32_t part_blocks) {
+DecodePlan plan_decode(int32_t num_seqs, int32_t n_q, int32_t n_kv, int32_t max_blocks, int32_t part_blocks) {
     DecodePlan pl{};
     pl.part_blocks = part_blocks >= max_blocks ? max_blocks : part_blocks;
     pl.max_parts = (max_blocks + pl.part_blocks - 1) / pl.part_blocks;
-    pl.off_m = kStatusBytes;
+    pl.off_cnt = kStatusBytes;
     if (pl.max_parts <= 1) {
-        pl.off_l = pl.off_o = pl.total = kStatusBytes;
+        pl.off_m = pl.off_l = pl.off_o = pl.total = kStatusBytes;
         return pl;
     }
+    const int32_t G = n_q / n_kv;
+    const int32_t groups = n_kv * (G <= 8 ? 1 : G / 8);  // CTAs per sequence and partition
     const size_t rows = static_cast<size_t>(num_seqs) * n_q * pl.max_parts;
+    pl.off_m = pl.off_cnt + align_up(static_cast<size_t>(num_seqs) * groups * 4, 256);
     pl.off_l = pl.off_m + align_up(rows * 4, 256);
     pl.off_o = pl.off_l + align_up(rows * 4, 256);
     pl.total = pl.off_o + align_up(rows * kHeadDim * 4, 256);
@@ -147,20 +152,25 @@ DecodePlan plan_decode(int32_t num_seqs, int32_t n_q, int32_t max_blocks, int32_
 }
 
 int32_t auto_part_blocks(int32_t num_seqs, int32_t n_kv, int32_t head_splits, int32_t max_blocks, int sms) {
-    // Partitions of 512 tokens keep every CTA's stream short and uniform, which
-    // balances ragged batches; a context that fits one partition is not split.
-    // When few (sequence, head) units exist the partitions shrink (not below 256
-    // tokens) until the grid covers the GPU several times.
+    // Partitions of 1024 tokens (measured best on ragged 8B-shaped batches and
+    // 70B-shaped long contexts) keep CTAs uniform and the merge small; a context
+    // that fits one partition is not split.  When few (sequence, head) units
+    // exist the partitions shrink (not below 256 tokens) until the grid covers
+    // every SM at least twice.
+    if (const char *e = std::getenv("PAGEDKV_PART_BLOCKS")) {  // tuning sweeps
+        const int v = std::atoi(e);
+        if (v >= kMinPartBlocks) return v;
+    }
     int32_t pb = kDefaultPartBlocks;
     const int64_t units = static_cast<int64_t>(num_seqs) * n_kv * head_splits;
-    const int64_t want = static_cast<int64_t>(sms > 0 ? sms : 148) * 8;
+    const int64_t want = static_cast<int64_t>(sms > 0 ? sms : 148) * 2;
     while (pb > kMinPartBlocks && units * ((max_blocks + pb - 1) / pb) < want) pb /= 2;
     return pb;
 }
 
 pkv::DecodeVariant decode_variant() {
     static pkv::DecodeVariant v = [] {
-        pkv::DecodeVariant d{4, 3};
+        pkv::DecodeVariant d{4, 2};  // 4 warps x 2 stages: 64 KB, 3 CTAs per SM (measured best)
         if (const char *e = std::getenv("PAGEDKV_DECODE_VARIANT")) {  // "warps,stages", for tuning sweeps
             int w = 0, s = 0;
             if (sscanf(e, "%d,%d", &w, &s) == 2 && pkv::decode_variant_supported({w, s})) d = {w, s};
@@ -171,6 +181,18 @@ pkv::DecodeVariant decode_variant() {
 }
 
 int variant_index(pkv::DecodeVariant v) { return (v.warps == 8 ? 4 : 0) + (v.stages - 1) % 4; }
+
+// How split partitions are merged: by a separate merge kernel launched with
+// programmatic dependent launch (default, measured faster), or inside the
+// decode kernel by the last CTA of each group ("PAGEDKV_MERGE=fused", for
+// tuning sweeps).  Both compute the same log-sum-exp reduction.
+bool fused_merge() {
+    static const bool fused = [] {
+        const char *e = std::getenv("PAGEDKV_MERGE");
+        return e && std::strcmp(e, "fused") == 0;
+    }();
+    return fused;
+}
 
 }  // namespace
 
@@ -213,7 +235,7 @@ size_t paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads, int
     if (check_group(num_q_heads, cache->num_kv_heads) != PKV_OK) return 0;
     if (partition_size < 0 || partition_size % kBlockSize != 0) return 0;
     const int32_t pb = partition_size > 0 ? partition_size / kBlockSize : kMinPartBlocks;
-    return plan_decode(num_seqs, num_q_heads, max_blocks_per_seq, pb).total;
+    return plan_decode(num_seqs, num_q_heads, cache->num_kv_heads, max_blocks_per_seq, pb).total;
 }
 
 int paged_attention_decode(void *out, int32_t out_dtype, const void *q, const void *k_cache, const void *v_cache,
@@ -248,7 +270,7 @@ int paged_attention_decode(void *out, int32_t out_dtype, const void *q, const vo
     const int sms = sm_count(dev);
     const int32_t pb = partition_size > 0 ? partition_size / kBlockSize
                                           : auto_part_blocks(num_seqs, n_kv, head_splits, max_blocks_per_seq, sms);
-    const DecodePlan pl = plan_decode(num_seqs, num_q_heads, max_blocks_per_seq, pb);
+    const DecodePlan pl = plan_decode(num_seqs, num_q_heads, n_kv, max_blocks_per_seq, pb);
     if (workspace_bytes < pl.total) return PKV_ERR_WORKSPACE_TOO_SMALL;  // cannot happen for auto plans
 
     CUtensorMap kmap, vmap;
@@ -271,6 +293,7 @@ int paged_attention_decode(void *out, int32_t out_dtype, const void *q, const vo
     p.part_m = pl.max_parts > 1 ? reinterpret_cast<float *>(ws + pl.off_m) : nullptr;
     p.part_l = pl.max_parts > 1 ? reinterpret_cast<float *>(ws + pl.off_l) : nullptr;
     p.part_o = pl.max_parts > 1 ? reinterpret_cast<float *>(ws + pl.off_o) : nullptr;
+    p.counters = pl.max_parts > 1 ? reinterpret_cast<uint32_t *>(ws + pl.off_cnt) : nullptr;
     p.num_seqs = num_seqs;
     p.n_q = num_q_heads;
     p.n_kv = n_kv;
@@ -283,10 +306,10 @@ int paged_attention_decode(void *out, int32_t out_dtype, const void *q, const vo
     p.max_parts = pl.max_parts;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     p.out_bf16 = out_dtype == PKV_DTYPE_BF16;
+    p.fused_merge = fused_merge() ? 1 : 0;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (pkv::launch_paged_decode(kmap, vmap, p, var, s) != cudaSuccess) return PKV_ERR_CUDA;
-    if (pl.max_parts > 1 && pkv::launch_lse_merge(p, s) != cudaSuccess) return PKV_ERR_CUDA;
     return PKV_OK;
 }
 

@@ -12,6 +12,7 @@
 #include <cuda_runtime.h>
 
 #include "launch.h"
+#include "ptx.cuh"
 
 namespace pkv {
 
@@ -21,6 +22,8 @@ __global__ void __launch_bounds__(256)
 kv_cache_write_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ value, uint4 *__restrict__ k_cache,
                       uint4 *__restrict__ v_cache, const int32_t *__restrict__ slot_mapping, int64_t total_vec,
                       int32_t n_kv, int64_t num_slots) {
+    griddep_launch_dependents();
+    griddep_wait();  // the previous kernel on the stream may still read the pool
     constexpr int kVecPerRow = kHeadDim * 2 / 16;  // 16 vectors of 8 bf16 per (token, head) row
     const int64_t vec_per_tok = static_cast<int64_t>(n_kv) * kVecPerRow;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -52,11 +55,10 @@ cudaError_t launch_kv_cache_write(const void *key, const void *value, void *k_ca
     int64_t blocks = (total_vec + threads - 1) / threads;
     const int64_t cap = static_cast<int64_t>(sm_count > 0 ? sm_count : 1) * 8;
     if (blocks > cap) blocks = cap;
-    kv_cache_write_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-        static_cast<const uint4 *>(key), static_cast<const uint4 *>(value), static_cast<uint4 *>(k_cache),
-        static_cast<uint4 *>(v_cache), slot_mapping, total_vec, n_kv,
-        static_cast<int64_t>(num_blocks) * kBlockSize);
-    return cudaGetLastError();
+    return launch_pdl(kv_cache_write_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, stream,
+                      static_cast<const uint4 *>(key), static_cast<const uint4 *>(value),
+                      static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), slot_mapping, total_vec, n_kv,
+                      static_cast<int64_t>(num_blocks) * kBlockSize);
 }
 
 }  // namespace pkv

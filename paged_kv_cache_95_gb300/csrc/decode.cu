@@ -1,6 +1,7 @@
-// decode.cu -- K2: paged decode attention (one CTA per sequence x KV head x
-// partition, serving the whole GQA group), and K3: the log-sum-exp merge of the
-// partitions (Flash-Decoding).
+// decode.cu -- paged decode attention: one CTA per sequence x KV head x
+// partition serves the whole GQA group; the partitions of a split context are
+// combined by a log-sum-exp merge (Flash-Decoding) done by the last CTA of the
+// group to finish, so one launch computes the whole decode.
 //
 // What is computed ("LLM 推理全过程的维度变化与核心公式", section "Decode 阶段
 // 维度流转"; "注意力演进与推理流程", section 3.1):
@@ -12,8 +13,7 @@
 //  * One CTA serves all G query heads of a KV head (up to 8; larger groups are
 //    split over CTAs), so each 4 KB (block, head) tile of K and of V is fetched
 //    from HBM once.  A context is cut into partitions of `part_blocks` blocks
-//    that run as independent CTAs (grid = partitions x heads x sequences); the
-//    partials are combined by K3.
+//    that run as independent CTAs (grid = partitions x heads x sequences).
 //  * Inside a CTA each warp owns every NW-th block of the partition and runs
 //    its own pipeline: lane 0 issues TMA tensor copies (128-byte swizzle) of the
 //    block's K and V tiles into a ring of ST stages, completing on one mbarrier
@@ -25,13 +25,16 @@
 //    is the fp32 online softmax (running max m, running sum l, rescale of O when
 //    m rises) with max reductions by warp shuffles across the 8 lanes that share
 //    a head column; probabilities go from the S^T accumulator layout to the
-//    B-operand layout of the second MMA with one movmatrix transpose.
+//    B-operand layout of the second MMA with movmatrix transposes, as a bf16
+//    head plus a bf16 remainder so that rounding P to bf16 costs no accuracy.
 //  * Keys at or past ctx (the tail of the last block) are masked by index, never
 //    by value, and their V rows are zeroed in registers, so stale or NaN bytes in
 //    unused slots cannot leak into the result.
 //  * At the end the warps' (m, l, O) are combined through shared memory; with a
 //    single partition the CTA writes out = O / l directly, otherwise it writes
-//    the unnormalised partial (m, l, O) to the workspace for K3.
+//    the unnormalised partial (m, l, O) to the workspace and counts itself on
+//    the group's arrival counter; the CTA that arrives last merges all
+//    partitions and resets the counter to zero for the next call.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -72,6 +75,13 @@ __global__ void __launch_bounds__(NW * 32)
     const int hpc = p.heads_per_cta;
     const int h0 = g * p.group + (hs - g * p.head_splits) * hpc;
 
+    if (threadIdx.x == 0) {
+        prefetch_tensormap(&kmap);
+        prefetch_tensormap(&vmap);
+    }
+    griddep_launch_dependents();
+    griddep_wait();  // inputs written by the previous kernel on the stream (e.g. the KV append)
+
     // ---- sequence extent (device data: checked, never trusted) ----
     int ctx = __ldg(p.context_lens + b);
     const int max_ctx = p.max_blocks * kBlockSize;
@@ -100,10 +110,6 @@ __global__ void __launch_bounds__(NW * 32)
     if (lane == 0) {
         for (int s = 0; s < ST; ++s) mbar_init(bar_base + 8 * s, 1);
         fence_mbar_init();
-        if (warp == 0) {
-            prefetch_tensormap(&kmap);
-            prefetch_tensormap(&vmap);
-        }
     }
     __syncwarp();
 
@@ -215,9 +221,16 @@ __global__ void __launch_bounds__(NW * 32)
             o[mt][3] *= al1;
         }
 
-        // P (C layout: row key, col head) -> P^T in the B-operand layout.
-        const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p00, p01));  // keys 0-7
-        const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p10, p11));  // keys 8-15
+        // P (C layout: row key, col head) -> P^T in the B-operand layout.  P is
+        // split into a bf16 head and a bf16 remainder (P = hi + lo to ~2^-17), so
+        // the weights keep fp32-like precision through the bf16 MMA.
+        const uint32_t ph0 = pack_bf16x2(p00, p01), ph1 = pack_bf16x2(p10, p11);
+        const uint32_t pl0 = pack_bf16x2(p00 - __uint_as_float(ph0 << 16), p01 - __uint_as_float(ph0 & 0xffff0000u));
+        const uint32_t pl1 = pack_bf16x2(p10 - __uint_as_float(ph1 << 16), p11 - __uint_as_float(ph1 & 0xffff0000u));
+        const uint32_t pb0 = movmatrix_trans(ph0);  // keys 0-7
+        const uint32_t pb1 = movmatrix_trans(ph1);  // keys 8-15
+        const uint32_t pr0 = movmatrix_trans(pl0);
+        const uint32_t pr1 = movmatrix_trans(pl1);
 
         // Zero V rows of keys >= valid (their P is 0, but 0 * NaN would not be).
         uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;
@@ -239,6 +252,7 @@ __global__ void __launch_bounds__(NW * 32)
             a[2] &= vm_hi;
             a[3] &= vm_hi;
             mma_bf16_16816(o[mt], a, pb0, pb1);
+            mma_bf16_16816(o[mt], a, pr0, pr1);
         }
         consumed = i + 1;
 
@@ -309,37 +323,130 @@ __global__ void __launch_bounds__(NW * 32)
             }
         }
     }
+    if (nparts == 1 || !p.fused_merge) return;
+
+    // ---- split-KV: the last partition of this (sequence, head group) to finish merges ----
+    // out = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p,  M = max_p m_p
+    // (Flash-Decoding's log-sum-exp reduction, in the log2 domain of the scores).
+    // One acquire-release add per CTA publishes its partial (written by all
+    // threads before the barrier) and, for the last arrival, acquires the others'.
+    uint32_t *last_flag = reinterpret_cast<uint32_t *>(red_l + NW * 8);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const uint32_t prev = atom_add_acq_rel_gpu(p.counters + static_cast<size_t>(b) * gridDim.y + hs, 1u);
+        *last_flag = prev == static_cast<uint32_t>(nparts - 1);
+    }
+    __syncthreads();
+    if (*last_flag == 0) return;
+
+    // Warp w folds the partitions p = w, w + NW, ...; lane owns dims 4*lane .. 4*lane+3.
+    for (int hh = 0; hh < hpc; ++hh) {
+        const size_t base = (static_cast<size_t>(b) * p.n_q + h0 + hh) * p.max_parts;
+        float M = -INFINITY;
+        for (int i = lane; i < nparts; i += 32) M = fmaxf(M, __ldcg(p.part_m + base + i));
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        const float Mu = M == -INFINITY ? 0.f : M;
+        float L = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = warp; i < nparts; i += NW) {
+            const float f = fast_exp2(__ldcg(p.part_m + base + i) - Mu);
+            L += f * __ldcg(p.part_l + base + i);
+            const float4 v = __ldcg(reinterpret_cast<const float4 *>(p.part_o + (base + i) * kHeadDim) + lane);
+            acc.x += f * v.x;
+            acc.y += f * v.y;
+            acc.z += f * v.z;
+            acc.w += f * v.w;
+        }
+        reinterpret_cast<float4 *>(red_o + (warp * 8 + hh) * kHeadDim)[lane] = acc;
+        if (lane == 0) red_l[warp * 8 + hh] = L;
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < hpc * kHeadDim; idx += NW * 32) {
+        const int hh = idx >> 7, d = idx & 127;
+        float L = 0.f, O = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            L += red_l[w * 8 + hh];
+            O += red_o[(w * 8 + hh) * kHeadDim + d];
+        }
+        store_out(p.out, p.out_bf16, (static_cast<size_t>(b) * p.n_q + h0 + hh) * kHeadDim + d,
+                  L > 0.f ? O / L : 0.f);
+    }
+    if (threadIdx.x == 0) p.counters[static_cast<size_t>(b) * gridDim.y + hs] = 0u;  // ready for the next call
 }
 
-// K3: out[b][h] = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p,  M = max_p m_p.
-__global__ void __launch_bounds__(kHeadDim) lse_merge_kernel(const DecodeParams p) {
+}  // namespace
+
+namespace {
+
+// Standalone log-sum-exp merge of the partitions (one CTA per sequence and query
+// head), for decodes that do not merge inside the decode kernel.  8 warps fold
+// the partitions p = w, w + 8, ...; lane owns dims 4*lane .. 4*lane + 3.
+constexpr int kMergeWarps = 8;
+
+__global__ void __launch_bounds__(kMergeWarps * 32) lse_merge_kernel(const DecodeParams p) {
+    __shared__ float red_o[kMergeWarps][kHeadDim];
+    __shared__ float red_x[kMergeWarps];
+    __shared__ float red_l[kMergeWarps];
     const int h = blockIdx.x;
     const int b = blockIdx.y;
-    const int d = threadIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    griddep_launch_dependents();
+    griddep_wait();  // the decode grid's partials
     int ctx = __ldg(p.context_lens + b);
     const int max_ctx = p.max_blocks * kBlockSize;
     ctx = ctx < 1 ? 0 : (ctx > max_ctx ? max_ctx : ctx);
     const int nparts = ((ctx + kBlockSize - 1) / kBlockSize + p.part_blocks - 1) / p.part_blocks;
-    if (nparts <= 1) return;  // written directly by K2
+    if (nparts <= 1) return;  // written directly by the decode kernel
     const size_t base = (static_cast<size_t>(b) * p.n_q + h) * p.max_parts;
     float M = -INFINITY;
-    for (int i = 0; i < nparts; ++i) M = fmaxf(M, __ldg(p.part_m + base + i));
+    for (int i = threadIdx.x; i < nparts; i += kMergeWarps * 32) M = fmaxf(M, __ldcg(p.part_m + base + i));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    if (lane == 0) red_x[warp] = M;
+    __syncthreads();
+    M = red_x[0];
+#pragma unroll
+    for (int w = 1; w < kMergeWarps; ++w) M = fmaxf(M, red_x[w]);
     const float Mu = M == -INFINITY ? 0.f : M;
-    float L = 0.f, O = 0.f;
-    for (int i = 0; i < nparts; ++i) {
-        const float f = fast_exp2(__ldg(p.part_m + base + i) - Mu);
-        L += f * __ldg(p.part_l + base + i);
-        O += f * __ldg(p.part_o + (base + i) * kHeadDim + d);
+    float L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int i = warp; i < nparts; i += kMergeWarps) {
+        const float f = fast_exp2(__ldcg(p.part_m + base + i) - Mu);
+        L += f * __ldcg(p.part_l + base + i);
+        const float4 v = __ldcg(reinterpret_cast<const float4 *>(p.part_o + (base + i) * kHeadDim) + lane);
+        acc.x += f * v.x;
+        acc.y += f * v.y;
+        acc.z += f * v.z;
+        acc.w += f * v.w;
     }
-    store_out(p.out, p.out_bf16, (static_cast<size_t>(b) * p.n_q + h) * kHeadDim + d, L > 0.f ? O / L : 0.f);
+    reinterpret_cast<float4 *>(red_o[warp])[lane] = acc;
+    if (lane == 0) red_l[warp] = L;
+    __syncthreads();
+    if (threadIdx.x < kHeadDim) {
+        float Ls = 0.f, O = 0.f;
+#pragma unroll
+        for (int w = 0; w < kMergeWarps; ++w) {
+            Ls += red_l[w];
+            O += red_o[w][threadIdx.x];
+        }
+        store_out(p.out, p.out_bf16, (static_cast<size_t>(b) * p.n_q + h) * kHeadDim + threadIdx.x,
+                  Ls > 0.f ? O / Ls : 0.f);
+    }
 }
 
 template <int NW, int ST>
 cudaError_t launch_variant(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParams &p,
                            cudaStream_t stream) {
     const dim3 grid(p.max_parts, p.n_kv * p.head_splits, p.num_seqs);
-    paged_decode_kernel<NW, ST><<<grid, NW * 32, decode_smem_bytes({NW, ST}), stream>>>(kmap, vmap, p);
-    return cudaGetLastError();
+    cudaError_t e = launch_pdl(paged_decode_kernel<NW, ST>, grid, dim3(NW * 32), decode_smem_bytes({NW, ST}), stream,
+                               kmap, vmap, p);
+    if (e != cudaSuccess) return e;
+    if (p.max_parts > 1 && !p.fused_merge)
+        e = launch_pdl(lse_merge_kernel, dim3(p.n_q, p.num_seqs), dim3(kMergeWarps * 32), 0, stream, p);
+    return e;
 }
 
 template <int NW, int ST>
@@ -376,10 +483,5 @@ cudaError_t launch_paged_decode(const CUtensorMap &kmap, const CUtensorMap &vmap
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_lse_merge(const DecodeParams &p, cudaStream_t stream) {
-    const dim3 grid(p.n_q, p.num_seqs);
-    lse_merge_kernel<<<grid, kHeadDim, 0, stream>>>(p);
-    return cudaGetLastError();
-}
 
 }  // namespace pkv

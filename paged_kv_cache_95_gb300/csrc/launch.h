@@ -8,6 +8,24 @@
 
 namespace pkv {
 
+// Launch with programmatic stream serialisation: the kernel may start while the
+// previous kernel on the stream drains; every kernel here executes
+// griddepcontrol.wait before touching global memory, so stream order holds.
+template <typename Kernel, typename... Args>
+cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 constexpr int kHeadDim = 128;
 constexpr int kBlockSize = 16;
 
@@ -22,7 +40,7 @@ cudaError_t launch_kv_cache_write(const void *key, const void *value, void *k_ca
                                   const int32_t *slot_mapping, int32_t num_tokens, int32_t n_kv,
                                   int32_t num_blocks, int sm_count, cudaStream_t stream);
 
-// ---- K2/K3: decode with optional split-KV and its log-sum-exp merge ------------
+// ---- K2: decode with optional split-KV and its fused log-sum-exp merge ------------
 struct DecodeParams {
     const void *q;               // bf16 [num_seqs][n_q][128]
     void *out;                   // [num_seqs][n_q][128], f32 or bf16
@@ -31,7 +49,8 @@ struct DecodeParams {
     float *part_m;               // [num_seqs][n_q][max_parts]   (log2 domain, scale folded in)
     float *part_l;               // [num_seqs][n_q][max_parts]
     float *part_o;               // [num_seqs][n_q][max_parts][128] (unnormalised)
-    uint32_t *status;            // device status word or nullptr
+    uint32_t *counters;          // [num_seqs][n_kv * head_splits] arrivals; zero between calls
+    uint32_t *status;            // device status word
     int32_t num_seqs, n_q, n_kv;
     int32_t group;               // G = n_q / n_kv
     int32_t heads_per_cta;       // min(G, 8)
@@ -42,6 +61,7 @@ struct DecodeParams {
     int32_t max_parts;           // partitions of the longest possible context
     float scale_log2;            // scale * log2(e)
     int32_t out_bf16;            // 1: bf16 output, 0: f32
+    int32_t fused_merge;         // 1: last partition CTA merges; 0: a separate merge kernel runs
 };
 
 struct DecodeVariant {
@@ -53,9 +73,10 @@ struct DecodeVariant {
 size_t decode_smem_bytes(DecodeVariant v);
 bool decode_variant_supported(DecodeVariant v);
 cudaError_t decode_prepare_device(DecodeVariant v);  // sets the dynamic shared memory limit
+// Enqueues the decode kernel (and, when partitions are merged separately, the
+// merge kernel), both with programmatic dependent launch.
 cudaError_t launch_paged_decode(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParams &p,
                                 DecodeVariant v, cudaStream_t stream);
-cudaError_t launch_lse_merge(const DecodeParams &p, cudaStream_t stream);
 
 // ---- K4: causal chunked prefill on tcgen05 ---------------------------------------
 struct PrefillParams {

@@ -19,9 +19,11 @@
 //  * S = Q K^T (M=128, N=128, K=128) goes to tensor memory columns [0, 128).
 //    The 128 threads each own one tensor-memory lane (= one row): they load the
 //    row, apply the causal/length mask by index, update the running max and sum
-//    (fp32, log2 domain) and write P = 2^(s - m) as bf16 into shared memory in
-//    the K-major layout of the A operand.
-//  * O += P V (M=128, N=128 dims, K=128 keys) accumulates in tensor memory
+//    (fp32, log2 domain) and write P = 2^(s - m) into shared memory in the
+//    K-major layout of the A operand, as a bf16 head plus a bf16 remainder (the
+//    remainder goes into the K tile, which S = Q K^T no longer needs), so that
+//    P V = P_hi V + P_lo V keeps the weights to ~2^-17 relative.
+//  * O += P_hi V + P_lo V (M=128, N=128 dims, K=128 keys) accumulates in tensor memory
 //    columns [128, 256).  The running max used as the exponent reference is only
 //    raised when a row's max grows by more than 2^8, in which case the row's O
 //    is rescaled in tensor memory; P stays <= 256, safe in bf16/fp32.
@@ -92,6 +94,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int G = p.group;
     const int rpt = p.rows_per_tile;
 
+    if (tid == 0) {
+        prefetch_tensormap(&qmap);
+        prefetch_tensormap(&kmap);
+        prefetch_tensormap(&vmap);
+    }
+    griddep_launch_dependents();
+    griddep_wait();  // the KV append (or any producer of q) before us on the stream
+
     // ---- sequence extent (device data: checked) ----
     const int row0 = __ldg(p.cu_q_lens + b);
     const int q_len = __ldg(p.cu_q_lens + b + 1) - row0;
@@ -123,9 +133,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar_s, 1);
         mbar_init(bar_o, 1);
         fence_mbar_init();
-        prefetch_tensormap(&qmap);
-        prefetch_tensormap(&kmap);
-        prefetch_tensormap(&vmap);
     }
     if (warp == 0) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -248,20 +255,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const uint32_t prow = sbase + kOffP + (q >> 1) * kHalfTile + r * 128;
+            const uint32_t plow = kbase + (q >> 1) * kHalfTile + r * 128;  // remainder: into the spent K tile
 #pragma unroll
             for (int c8 = 0; c8 < 4; ++c8) {
-                uint32_t w[4];
+                uint32_t w[4], x[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float pa = fast_exp2(__uint_as_float(sr[q][8 * c8 + 2 * e]) - mu);
                     const float pb = fast_exp2(__uint_as_float(sr[q][8 * c8 + 2 * e + 1]) - mu);
                     rs += pa + pb;
                     w[e] = pack_bf16x2(pa, pb);
+                    x[e] = pack_bf16x2(pa - __uint_as_float(w[e] << 16), pb - __uint_as_float(w[e] & 0xffff0000u));
                 }
                 const int chunk = (q & 1) * 4 + c8;
-                const uint32_t addr = prow + ((chunk ^ (r & 7)) << 4);
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]),
-                             "r"(w[3])
+                const uint32_t sw = ((chunk ^ (r & 7)) << 4);
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + sw), "r"(w[0]), "r"(w[1]),
+                             "r"(w[2]), "r"(w[3])
+                             : "memory");
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(plow + sw), "r"(x[0]), "r"(x[1]),
+                             "r"(x[2]), "r"(x[3])
                              : "memory");
             }
         }
@@ -302,14 +314,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
         }
 
-        // ---- O += P V ----
+        // ---- O += P_hi V + P_lo V ----
         if (tid == 0) {
             tc_fence_after();
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
-                const uint64_t ad = sw128_desc(sbase + kOffP + (t >> 2) * kHalfTile + (t & 3) * 32, 16, 1024);
+                const uint32_t aoff = (t >> 2) * kHalfTile + (t & 3) * 32;
                 const uint64_t bd = sw128_desc(vbase + t * 2048, kHalfTile, 1024);
-                umma_bf16(tmem + 128, ad, bd, kIdescPV, (kt > 0 || t > 0) ? 1u : 0u);
+                umma_bf16(tmem + 128, sw128_desc(sbase + kOffP + aoff, 16, 1024), bd, kIdescPV,
+                          (kt > 0 || t > 0) ? 1u : 0u);
+                umma_bf16(tmem + 128, sw128_desc(kbase + aoff, 16, 1024), bd, kIdescPV, 1u);
             }
             umma_commit(bar_o);
         }
@@ -356,8 +370,7 @@ cudaError_t prefill_prepare_device() {
 cudaError_t launch_prefill_chunk(const CUtensorMap &qmap, const CUtensorMap &kmap, const CUtensorMap &vmap,
                                  const PrefillParams &p, int max_q_len, cudaStream_t stream) {
     const dim3 grid((max_q_len + p.rows_per_tile - 1) / p.rows_per_tile, p.n_kv, p.num_seqs);
-    prefill_chunk_kernel<<<grid, kThreads, kSmemBytes, stream>>>(qmap, kmap, vmap, p);
-    return cudaGetLastError();
+    return launch_pdl(prefill_chunk_kernel, grid, dim3(kThreads), kSmemBytes, stream, qmap, kmap, vmap, p);
 }
 
 }  // namespace pkv

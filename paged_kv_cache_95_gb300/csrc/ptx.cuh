@@ -61,6 +61,24 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     }
 }
 
+// ---- programmatic dependent launch ------------------------------------------
+// Every kernel waits for the grids it depends on before its first global
+// memory access, and lets its dependents launch early so their prologues
+// overlap its tail.  Both are no-ops for a launch without the PDL attribute.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// atomicAdd with acquire-release semantics at GPU scope: publishes the writes
+// that happen-before it (including other threads' writes ordered by a
+// preceding __syncthreads) and acquires the writes published by earlier adds.
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t *addr, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+    return old;
+}
+
 // ---- bulk tensor copies (TMA) -----------------------------------------------
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

@@ -89,6 +89,22 @@ def test_decode_partition_invariance(part):
     assert_close(out.cpu().numpy(), oracle_out("llama3_8b_b64", "decode"), what=f"partition {part}")
 
 
+def test_decode_repeated_calls_share_a_workspace():
+    """The split-KV arrival counters reset themselves: reusing one workspace for
+    many calls (with different partition sizes) gives bitwise-identical results."""
+    t = torch()
+    wl, _, _, _ = workload("llama3_8b_b64")
+    d = DevWorkload(wl)
+    d.append()
+    first, ws = d.decode(wl.decode, partition_size=256)
+    for part in (256, 512, 256, 0, 256):
+        again, _ = d.decode(wl.decode, partition_size=part, workspace=ws)
+        if part == 256:
+            assert t.equal(first, again)
+    assert status_word(ws) == 0
+    assert_close(first.cpu().numpy(), oracle_out("llama3_8b_b64", "decode"))
+
+
 def test_decode_bf16_output_is_rounded_f32():
     t = torch()
     wl, _, _, _ = workload("llama3_8b_b64")
