@@ -183,6 +183,58 @@ PKV_API int paged_attention_decode(void *out, int32_t out_dtype, const void *q, 
                            void *stream);
 
 /*
+ * Largest workspace that paged_attention_decode_static_scratch can stand in
+ * for: 16 MiB of device memory, held by every GPU that loads this library for
+ * as long as the process lives.
+ */
+#define PKV_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/*
+ * paged_attention_decode_static_scratch -- paged_attention_decode without a
+ * caller-provided workspace; it allocates nothing.  (The pages have no
+ * counterpart: this is a deployment convenience, not part of the method.)
+ *
+ * For callers that cannot allocate device memory at the point of the call:
+ * code running under a framework or allocator that owns all device memory
+ * (where a raw cudaMalloc would bypass its pool or its accounting), real-time
+ * or latency-critical loops where cudaMalloc/cudaFree would synchronise the
+ * device and stall, and callers such as plugins or other libraries that are
+ * handed only the input and output buffers.
+ *
+ * The split-KV scratch (status word, arrival counters and per-partition
+ * partials) lives in one file-scope device array of PKV_STATIC_SCRATCH_BYTES
+ * bytes instead of a workspace argument.  Everything else -- arguments,
+ * layouts, result and error codes -- is exactly paged_attention_decode's.
+ *
+ *   status : device pointer to one uint32 that receives this call's
+ *            PKV_STATUS_* bits (copied out of the scratch after the kernels),
+ *            or NULL to discard them.
+ * Limits and sharing:
+ *  - Sizes whose paged_attention_workspace_size(num_seqs, num_q_heads,
+ *    max_blocks_per_seq, partition_size, cache) exceeds
+ *    PKV_STATIC_SCRATCH_BYTES are rejected with PKV_ERR_WORKSPACE_TOO_SMALL
+ *    before anything is enqueued (use a larger partition_size, fewer
+ *    sequences per call, or paged_attention_decode with a workspace).
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current) and caches it; make
+ *    that first call outside any stream capture.
+ *  - Every call on a device shares the one array, which keeps the last
+ *    call's contents: each call clears the status word and counters it needs
+ *    (an asynchronous memset on `stream`) before its kernels run.  Calls
+ *    whose execution overlaps on the GPU (different streams without ordering
+ *    between them, or different host threads) race on the array and give
+ *    undefined results; serialise them.
+ * Errors: as paged_attention_decode; PKV_ERR_CUDA if the array's address
+ * cannot be obtained.
+ */
+PKV_API int paged_attention_decode_static_scratch(void *out, int32_t out_dtype, const void *q, const void *k_cache,
+                                                  const void *v_cache, const int32_t *block_tables,
+                                                  const int32_t *context_lens, int32_t num_seqs,
+                                                  int32_t num_q_heads, int32_t max_blocks_per_seq, float scale,
+                                                  int32_t partition_size, const pkv_cache_desc *cache,
+                                                  uint32_t *status, void *stream);
+
+/*
  * paged_attention_prefill_workspace_size -- bytes of workspace that
  * paged_attention_prefill_chunk needs (the status word).  Needs no GPU.
  */

@@ -376,4 +376,58 @@ int paged_attention_prefill_chunk(void *out, int32_t out_dtype, const void *q, c
     return PKV_OK;
 }
 
+// ---- decode without a caller workspace ------------------------------------------
+// The scratch that paged_attention_decode would take as its workspace, as one
+// file-scope device array.  Host code must not use the symbol itself as a
+// pointer (it names a host-side shadow); it uses the device address obtained
+// once per device with cudaGetSymbolAddress.
+static_assert(PKV_STATIC_SCRATCH_BYTES % 256 == 0, "scratch size must keep 256-byte alignment");
+static __device__ __align__(256) uint8_t g_decode_scratch[PKV_STATIC_SCRATCH_BYTES];
+
+namespace {
+std::once_flag g_scratch_once[kMaxDevices];
+void *g_scratch_addr[kMaxDevices];
+
+// Device address of g_decode_scratch on `dev` (which must be current); nullptr on failure.
+void *decode_scratch_address(int dev) {
+    std::call_once(g_scratch_once[dev], [dev] {
+        void *ptr = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&ptr, g_decode_scratch);
+        g_scratch_addr[dev] = e == cudaSuccess ? ptr : nullptr;
+    });
+    return g_scratch_addr[dev];
+}
+}  // namespace
+
+int paged_attention_decode_static_scratch(void *out, int32_t out_dtype, const void *q, const void *k_cache,
+                                          const void *v_cache, const int32_t *block_tables,
+                                          const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                          int32_t max_blocks_per_seq, float scale, int32_t partition_size,
+                                          const pkv_cache_desc *cache, uint32_t *status, void *stream) {
+    if (int rc = check_cache(cache)) return rc;
+    if (int rc = check_group(num_q_heads, cache->num_kv_heads)) return rc;
+    if (status && !aligned(status, 4)) return PKV_ERR_INVALID_ARG;
+    const size_t need =
+        paged_attention_workspace_size(num_seqs, num_q_heads, max_blocks_per_seq, partition_size, cache);
+    if (need == 0) return PKV_ERR_INVALID_ARG;
+    if (need > PKV_STATIC_SCRATCH_BYTES) return PKV_ERR_WORKSPACE_TOO_SMALL;
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return PKV_ERR_CUDA;
+    uint8_t *scratch = static_cast<uint8_t *>(decode_scratch_address(dev));
+    if (!scratch) return PKV_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // What must start at zero: the status word and the arrival counters, which
+    // follow it; the partials are always written before they are read.
+    const int32_t G = num_q_heads / cache->num_kv_heads;
+    const size_t counters = static_cast<size_t>(num_seqs) * cache->num_kv_heads * (G <= 8 ? 1 : G / 8) * 4;
+    if (cudaMemsetAsync(scratch, 0, kStatusBytes + align_up(counters, 256), s) != cudaSuccess) return PKV_ERR_CUDA;
+    const int rc = paged_attention_decode(out, out_dtype, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                                          num_q_heads, max_blocks_per_seq, scale, partition_size, cache, scratch,
+                                          PKV_STATIC_SCRATCH_BYTES, stream);
+    if (rc != PKV_OK) return rc;
+    if (status && cudaMemcpyAsync(status, scratch, sizeof(uint32_t), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    return PKV_OK;
+}
+
 }  // extern "C"

@@ -31,6 +31,7 @@ PKV_STATUS_TIMEOUT = 0x8
 
 HEAD_DIM = 128
 BLOCK_SIZE = 16
+STATIC_SCRATCH_BYTES = 16 * 1024 * 1024  # PKV_STATIC_SCRATCH_BYTES
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpagedkv.so")
 HEADER_PATH = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "pagedkv.h")
@@ -79,6 +80,8 @@ def _declare(lib):
     lib.paged_attention_prefill_workspace_size.restype = sz
     lib.paged_attention_prefill_chunk.argtypes = [P, i32, P, P, i32, i32, P, P, P, P, i32, i32, i32, f32, D, P, sz, P]
     lib.paged_attention_prefill_chunk.restype = ctypes.c_int
+    lib.paged_attention_decode_static_scratch.argtypes = [P, i32, P, P, P, P, P, i32, i32, i32, f32, i32, D, P, P]
+    lib.paged_attention_decode_static_scratch.restype = ctypes.c_int
     lib.pagedkv_status_string.argtypes = [ctypes.c_int]
     lib.pagedkv_status_string.restype = ctypes.c_char_p
     lib.pagedkv_version.argtypes = []
@@ -237,3 +240,28 @@ def paged_attention_prefill_chunk(out, q, cu_q_lens, max_q_len: int, k_cache, v_
         float(scale), ctypes.byref(desc), _ptr(workspace), int(workspace.numel()), _stream(stream))
     _raise("paged_attention_prefill_chunk", rc)
     return workspace
+
+
+def paged_attention_decode_static_scratch(out, q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                                          partition_size: int = 0, status=None, stream=None) -> None:
+    """Decode attention that allocates nothing: the split-KV scratch is the
+    library's fixed device array (STATIC_SCRATCH_BYTES), shared by all calls on
+    a device, so calls must not overlap on the GPU.  ``status`` is an optional
+    int32 CUDA tensor of one element that receives the call's status bits."""
+    torch = _torch()
+    desc = cache_desc(k_cache)
+    _check(v_cache, "v_cache", torch.bfloat16, ndim=4)
+    _need(tuple(v_cache.shape) == tuple(k_cache.shape), "v_cache shape must equal k_cache shape")
+    _check(q, "q", torch.bfloat16, ndim=3, last=HEAD_DIM)
+    B, n_q, _ = q.shape
+    _check(out, "out", out.dtype, ndim=3)
+    _need(tuple(out.shape) == tuple(q.shape), "out must have q's shape")
+    _check(block_tables, "block_tables", torch.int32, ndim=2)
+    _check(context_lens, "context_lens", torch.int32, ndim=1)
+    if status is not None:
+        _check(status, "status", torch.int32, ndim=1)
+    rc = load_library().paged_attention_decode_static_scratch(
+        _ptr(out), _out_dtype(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        int(B), int(n_q), int(block_tables.shape[1]), float(scale), int(partition_size), ctypes.byref(desc),
+        _ptr(status) if status is not None else None, _stream(stream))
+    _raise("paged_attention_decode_static_scratch", rc)
