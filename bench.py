@@ -413,12 +413,25 @@ def _config(wl, batch, kv_bytes, pool_bytes, world):
             "l2": f"inputs larger than L2: {kv_bytes / 1e6:.0f} MB read per step vs 129 MB L2; no flush"}
 
 
+def kernel_source_hash() -> str:
+    """Hash of the decode kernel's sources (a profile is stale once they change)."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in ("decode.cu", "ptx.cuh", "launch.h"):
+        with open(os.path.join(ROOT, "paged_kv_cache_95_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def _profiled_traffic(workload):
-    """dram read+write bytes per decode launch from the committed ncu summary, if any."""
+    """dram read+write bytes per decode launch from the committed ncu summary, or
+    None when there is none or the kernel sources changed since it was taken."""
     path = os.path.join(ROOT, "profiles", f"decode_{workload}.json")
     try:
         with open(path) as f:
             d = json.load(f)
+        if d.get("kernel_source_hash") != kernel_source_hash():
+            return None
         return d.get("dram_bytes_per_launch")
     except Exception:
         return None
