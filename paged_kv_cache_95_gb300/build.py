@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG_DIR, "csrc")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libpagedkv.so")
 SOURCES = ["api.cu", "cache_write.cu", "decode.cu", "prefill.cu"]
-HEADERS = ["launch.h", "ptx.cuh"]
+HEADERS = ["launch.h", "ptx.cuh", "decode_core.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -268,6 +268,7 @@ int paged_attention_decode(void *out, int32_t out_dtype, const void *q, const vo
     const int dev = current_device();
     if (dev < 0 || dev >= kMaxDevices) return PKV_ERR_CUDA;
     const int sms = sm_count(dev);
+
     const int32_t pb = partition_size > 0 ? partition_size / kBlockSize
                                           : auto_part_blocks(num_seqs, n_kv, head_splits, max_blocks_per_seq, sms);
     const DecodePlan pl = plan_decode(num_seqs, num_q_heads, n_kv, max_blocks_per_seq, pb);

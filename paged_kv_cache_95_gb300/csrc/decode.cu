@@ -40,23 +40,13 @@
 
 #include <cmath>
 
+#include "decode_core.cuh"
 #include "launch.h"
 #include "ptx.cuh"
 
 namespace pkv {
 
 namespace {
-
-constexpr uint32_t kTileBytes = kBlockSize * kHeadDim * 2;  // 4096 B: one (block, head) tile
-constexpr uint32_t kBoxBytes = kTileBytes / 2;              // 2048 B: 16 rows x 64 dims (128-B rows)
-constexpr uint32_t kStageBytes = 2 * kTileBytes;            // K tile + V tile
-
-__device__ __forceinline__ void store_out(void *out, int32_t bf16, size_t idx, float v) {
-    if (bf16)
-        static_cast<__nv_bfloat16 *>(out)[idx] = __float2bfloat16_rn(v);
-    else
-        static_cast<float *>(out)[idx] = v;
-}
 
 template <int NW, int ST>
 __global__ void __launch_bounds__(NW * 32)
@@ -119,13 +109,7 @@ __global__ void __launch_bounds__(NW * 32)
         const int j = blk_begin + warp + NW * i;
         int phys = __ldg(table + j);
         if (static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_blocks)) phys = 0;  // masked below
-        const uint32_t bar = bar_base + 8 * s;
-        const uint32_t dst = stage_base + s * kStageBytes;
-        mbar_arrive_expect_tx(bar, kStageBytes);
-        tma_load_4d(dst, &kmap, bar, 0, 0, g, phys);
-        tma_load_4d(dst + kBoxBytes, &kmap, bar, 64, 0, g, phys);
-        tma_load_4d(dst + kTileBytes, &vmap, bar, 0, 0, g, phys);
-        tma_load_4d(dst + kTileBytes + kBoxBytes, &vmap, bar, 64, 0, g, phys);
+        issue_block_copy(&kmap, &vmap, stage_base + s * kStageBytes, bar_base + 8 * s, g, phys);
     };
     if (lane == 0)
         for (int i = 0; i < ST && i < nmine; ++i) issue(i);
@@ -134,29 +118,10 @@ __global__ void __launch_bounds__(NW * 32)
     const int n = lane >> 2;  // head column of B / row group of C
     const int q4 = lane & 3;
     uint32_t bq[8][2];
-    {
-        const bool hv = n < hpc;
-        const uint32_t *qrow = reinterpret_cast<const uint32_t *>(static_cast<const __nv_bfloat16 *>(p.q) +
-                                                                  (static_cast<size_t>(b) * p.n_q + h0 + n) * kHeadDim);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-            bq[kk][0] = hv ? __ldg(qrow + (16 * kk + 2 * q4) / 2) : 0u;
-            bq[kk][1] = hv ? __ldg(qrow + (16 * kk + 8 + 2 * q4) / 2) : 0u;
-        }
-    }
+    load_q_frag(bq, p.q, static_cast<size_t>(b) * p.n_q + h0, hpc, lane);
 
-    // Per-lane swizzled ldmatrix row offsets.  128-byte swizzle: 16-byte chunk c
-    // of row r lives at chunk c ^ (r & 7).
-    const int kkey = (lane & 7) | (((lane >> 3) & 1) << 3);  // K: matrices (keys 0-7 | 8-15) x (dims lo | hi)
-    const int khi = lane >> 4;
-    const int vkey = (lane & 7) | ((lane >> 4) << 3);        // V: matrices (dims lo | hi) x (keys 0-7 | 8-15)
-    const int vhi = (lane >> 3) & 1;
-
-    float m0 = -INFINITY, m1 = -INFINITY;  // running max of head columns 2*q4, 2*q4+1 (log2 domain)
-    float l0 = 0.f, l1 = 0.f;              // this lane's share of the running sums
-    float o[8][4];
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    DecodeAcc acc;
+    acc.reset();
 
     const float sl2 = p.scale_log2;
     int consumed = 0;
@@ -178,82 +143,7 @@ __global__ void __launch_bounds__(NW * 32)
             if (lane == 0 && p.status) atomicOr(p.status, kStatusBadBlockId);
         }
         const uint32_t kb = stage_base + s * kStageBytes;
-        const uint32_t vb = kb + kTileBytes;
-
-        // S^T = K Q^T  (rows: keys, columns: heads)
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-            const int chunk = 2 * kk + khi;
-            const uint32_t addr = kb + (chunk >> 3) * kBoxBytes + kkey * 128 + (((chunk & 7) ^ (lane & 7)) << 4);
-            uint32_t a[4];
-            ldmatrix_x4(a, addr);
-            mma_bf16_16816(c, a, bq[kk][0], bq[kk][1]);
-        }
-
-        // Online softmax in the log2 domain (scale * log2(e) folded into the scores).
-        const int key_a = n, key_b = n + 8;
-        const float s00 = key_a < valid ? c[0] * sl2 : -INFINITY;
-        const float s01 = key_a < valid ? c[1] * sl2 : -INFINITY;
-        const float s10 = key_b < valid ? c[2] * sl2 : -INFINITY;
-        const float s11 = key_b < valid ? c[3] * sl2 : -INFINITY;
-        float bm0 = fmaxf(s00, s10), bm1 = fmaxf(s01, s11);
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
-            bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
-        }
-        const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
-        const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
-        const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
-        const float al0 = fast_exp2(m0 - mu0), al1 = fast_exp2(m1 - mu1);
-        const float p00 = fast_exp2(s00 - mu0), p01 = fast_exp2(s01 - mu1);
-        const float p10 = fast_exp2(s10 - mu0), p11 = fast_exp2(s11 - mu1);
-        l0 = l0 * al0 + p00 + p10;
-        l1 = l1 * al1 + p01 + p11;
-        m0 = mn0;
-        m1 = mn1;
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-            o[mt][0] *= al0;
-            o[mt][1] *= al1;
-            o[mt][2] *= al0;
-            o[mt][3] *= al1;
-        }
-
-        // P (C layout: row key, col head) -> P^T in the B-operand layout.  P is
-        // split into a bf16 head and a bf16 remainder (P = hi + lo to ~2^-17), so
-        // the weights keep fp32-like precision through the bf16 MMA.
-        const uint32_t ph0 = pack_bf16x2(p00, p01), ph1 = pack_bf16x2(p10, p11);
-        const uint32_t pl0 = pack_bf16x2(p00 - __uint_as_float(ph0 << 16), p01 - __uint_as_float(ph0 & 0xffff0000u));
-        const uint32_t pl1 = pack_bf16x2(p10 - __uint_as_float(ph1 << 16), p11 - __uint_as_float(ph1 & 0xffff0000u));
-        const uint32_t pb0 = movmatrix_trans(ph0);  // keys 0-7
-        const uint32_t pb1 = movmatrix_trans(ph1);  // keys 8-15
-        const uint32_t pr0 = movmatrix_trans(pl0);
-        const uint32_t pr1 = movmatrix_trans(pl1);
-
-        // Zero V rows of keys >= valid (their P is 0, but 0 * NaN would not be).
-        uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;
-        if (valid < kBlockSize) {
-            const int ka = 2 * q4, kb2 = 2 * q4 + 8;
-            vm_lo = (ka < valid ? 0x0000ffffu : 0u) | (ka + 1 < valid ? 0xffff0000u : 0u);
-            vm_hi = (kb2 < valid ? 0x0000ffffu : 0u) | (kb2 + 1 < valid ? 0xffff0000u : 0u);
-        }
-
-        // O^T += V^T P^T  (rows: head dims, columns: heads)
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-            const int chunk = 2 * mt + vhi;
-            const uint32_t addr = vb + (chunk >> 3) * kBoxBytes + vkey * 128 + (((chunk & 7) ^ (lane & 7)) << 4);
-            uint32_t a[4];
-            ldmatrix_x4_trans(a, addr);
-            a[0] &= vm_lo;
-            a[1] &= vm_lo;
-            a[2] &= vm_hi;
-            a[3] &= vm_hi;
-            mma_bf16_16816(o[mt], a, pb0, pb1);
-            mma_bf16_16816(o[mt], a, pr0, pr1);
-        }
+        decode_block(acc, bq, kb, kb + kTileBytes, valid, sl2, lane);
         consumed = i + 1;
 
         __syncwarp();
@@ -271,11 +161,7 @@ __global__ void __launch_bounds__(NW * 32)
     }
 
     // Full row sums of this warp: add the shares of the 8 lanes of a head column.
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-    }
+    acc.reduce_sums();
 
     // ---- combine the warps of the CTA (shared memory reused after the pipeline) ----
     __syncthreads();
@@ -285,16 +171,16 @@ __global__ void __launch_bounds__(NW * 32)
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
         const int d0 = 16 * mt + n;
-        red_o[(warp * 8 + 2 * q4) * kHeadDim + d0] = o[mt][0];
-        red_o[(warp * 8 + 2 * q4 + 1) * kHeadDim + d0] = o[mt][1];
-        red_o[(warp * 8 + 2 * q4) * kHeadDim + d0 + 8] = o[mt][2];
-        red_o[(warp * 8 + 2 * q4 + 1) * kHeadDim + d0 + 8] = o[mt][3];
+        red_o[(warp * 8 + 2 * q4) * kHeadDim + d0] = acc.o[mt][0];
+        red_o[(warp * 8 + 2 * q4 + 1) * kHeadDim + d0] = acc.o[mt][1];
+        red_o[(warp * 8 + 2 * q4) * kHeadDim + d0 + 8] = acc.o[mt][2];
+        red_o[(warp * 8 + 2 * q4 + 1) * kHeadDim + d0 + 8] = acc.o[mt][3];
     }
     if (lane < 4) {
-        red_m[warp * 8 + 2 * lane] = m0;
-        red_m[warp * 8 + 2 * lane + 1] = m1;
-        red_l[warp * 8 + 2 * lane] = l0;
-        red_l[warp * 8 + 2 * lane + 1] = l1;
+        red_m[warp * 8 + 2 * lane] = acc.m0;
+        red_m[warp * 8 + 2 * lane + 1] = acc.m1;
+        red_l[warp * 8 + 2 * lane] = acc.l0;
+        red_l[warp * 8 + 2 * lane + 1] = acc.l1;
     }
     __syncthreads();
 

@@ -133,6 +133,19 @@ def test_decode_edge_lengths_all_groups(n_q, n_kv):
         assert status_word(ws) == 0
 
 
+@pytest.mark.parametrize("n_q,n_kv,B,lo,hi", [(64, 8, 1000, 1, 300), (32, 32, 300, 1, 40), (32, 1, 700, 1, 2000),
+                                             (32, 8, 1025, 1, 600)])
+def test_decode_many_short_sequences(n_q, n_kv, B, lo, hi):
+    """Many short (and some long) sequences in one call, against the oracle."""
+    ctx = np.random.default_rng(B).integers(lo, hi, size=B, endpoint=True)
+    wl, batch = W.make_custom(n_q, n_kv, ctx.tolist(), seed=B, materialize_logical=False)
+    d = DevWorkload(wl)
+    d.append()
+    out, ws = d.decode(batch)
+    assert_close(out.cpu().numpy(), oracle_attention(wl, batch), what=f"B={B} G={n_q // n_kv}")
+    assert status_word(ws) == 0
+
+
 def test_decode_block_permutation_is_bitwise_invariant():
     t = torch()
     wl, batch = W.make_custom(32, 8, [700, 33, 1500, 16], seed=31, materialize_logical=False)

@@ -63,13 +63,14 @@ def _close(got, ref):
 @pytest.mark.gpu
 def test_static_scratch_matches_workspace_decode_on_consecutive_calls(lib):
     import torch
-    # Two different batches in a row (both split into several partitions), so
-    # the second call runs on scratch that still holds the first call's data.
+    # Different batches in a row (explicit and automatic partition sizes), so
+    # each call runs on scratch that still holds the previous call's data.
     cases = [
         W.make_custom(32, 8, [3000, 17, 1025, 2048, 700], seed=51, materialize_logical=False),
         W.make_custom(64, 8, [5000, 260, 4097], seed=52, materialize_logical=False),
+        W.make_custom(32, 8, [9000, 33, 4000], seed=53, materialize_logical=False),
     ]
-    for (wl, batch), part in zip(cases, (512, 256)):
+    for (wl, batch), part in zip(cases, (512, 256, 0)):
         kc, vc, q, tables, lens = _upload(wl, batch)
         ref = torch.empty(q.shape, dtype=torch.float32, device="cuda")
         P.paged_attention_decode(ref, q, kc, vc, tables, lens, wl.scale, partition_size=part)
