@@ -417,7 +417,7 @@ def kernel_source_hash() -> str:
     """Hash of the decode kernel's sources (a profile is stale once they change)."""
     import hashlib
     h = hashlib.sha256()
-    for name in ("decode.cu", "ptx.cuh", "launch.h"):
+    for name in ("decode.cu", "decode_core.cuh", "ptx.cuh", "launch.h"):
         with open(os.path.join(ROOT, "paged_kv_cache_95_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
