@@ -336,6 +336,7 @@ int paged_attention_prefill_chunk(void *out, int32_t out_dtype, const void *q, c
     if (out_dtype != PKV_DTYPE_FLOAT32 && out_dtype != PKV_DTYPE_BF16) return PKV_ERR_UNSUPPORTED;
     if (num_seqs < 1 || num_seqs > 65535 || max_blocks_per_seq < 1 || max_q_len < 0 || total_q_rows < 0)
         return PKV_ERR_INVALID_ARG;
+    if ((static_cast<int64_t>(max_q_len) + 127) / 128 * G > 65535) return PKV_ERR_UNSUPPORTED;  // grid z
     if (static_cast<int64_t>(max_blocks_per_seq) * kBlockSize > INT32_MAX) return PKV_ERR_INVALID_ARG;
     if (!std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
     if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 16) || !aligned(out, 4) ||

@@ -12,29 +12,43 @@
 //    the group (row r = position (r / G), head (r % G)), so every K/V tile is
 //    shared by the whole group.  Q is loaded once by TMA (128-byte swizzle).
 //  * Keys are walked in tiles of 128 (= 8 paged blocks of 16).  Each paged
-//    block's K and V tile (2 x 4 KB) is gathered with TMA from the block table
-//    into a 2-stage ring; the blocks' halves are placed so that every operand
-//    is one canonical 128-byte-swizzled UMMA layout: K as a K-major B operand,
-//    V as an MN-major B operand.
-//  * S = Q K^T (M=128, N=128, K=128) goes to tensor memory columns [0, 128).
-//    The 128 threads each own one tensor-memory lane (= one row): they load the
-//    row, apply the causal/length mask by index, update the running max and sum
-//    (fp32, log2 domain) and write P = 2^(s - m) into shared memory in the
-//    K-major layout of the A operand, as a bf16 head plus a bf16 remainder (the
-//    remainder goes into the K tile, which S = Q K^T no longer needs), so that
-//    P V = P_hi V + P_lo V keeps the weights to ~2^-17 relative.
-//  * O += P_hi V + P_lo V (M=128, N=128 dims, K=128 keys) accumulates in tensor memory
-//    columns [128, 256).  The running max used as the exponent reference is only
-//    raised when a row's max grows by more than 2^8, in which case the row's O
-//    is rescaled in tensor memory; P stays <= 256, safe in bf16/fp32.
+//    block's K and V tiles (4 KB each) are gathered with TMA from the block
+//    table into separate 3-deep K and V rings; the blocks' halves are placed so
+//    that every operand is one canonical 128-byte-swizzled UMMA layout: K as a
+//    K-major B operand, V as an MN-major B operand.
+//
+// Warp roles (warp specialisation, all hand-offs through mbarriers):
+//  * warp 8: TMA producer (lane 0 issues; lanes 0-7 read a tile's block-table
+//    entries in parallel).  Loads in the order the MMAs consume them
+//    -- K0, K1, V0, K2, V1, ... -- refilling a K slot as soon as the S MMA that
+//    read it completes and a V slot as soon as its P V MMAs complete.
+//  * warp 9 (one lane): MMA issuer; also owns the tensor-memory allocation.
+//    S(k) = Q K(k)^T (M=128, N=128, K=128) goes to tensor-memory buffer k % 2
+//    (columns [0,128) or [128,256)); O += P(k) V(k) accumulates in columns
+//    [256,384), with P(k) read from tensor memory as the A operand.  S(k+1) is
+//    issued before P(k) V(k), so the tensor core works while the softmax warps
+//    work; S(k+2) reuses buffer k % 2 once P(k) V(k) has completed.
+//  * warps 0-7 (256 threads): warps w and w+4 own tensor-memory lanes
+//    32*(w%4) .. +31 (= tile rows) and split the 128 columns: each thread holds
+//    one row's 64 scores of its half, applies the causal/length mask by index
+//    (skipped for fully visible 32-key chunks), and the two halves exchange
+//    their row maxima through shared memory (a 64-thread named barrier per
+//    pair).  Each updates the running max and its half of the running sum
+//    (fp32, log2 domain) and writes P = 2^(s - m) back over its half as
+//    [bf16 head | bf16 remainder] (P V = P_hi V + P_lo V keeps
+//    the weights to ~2^-17 relative).  P is thereby double-buffered with S, so
+//    the softmax of tile k+1 never waits for P(k) V(k); it waits for it only
+//    when it must rescale O.  The exponent reference is only raised when a
+//    row's max grows by more than 2^8, in which case the row's O is rescaled in
+//    tensor memory; P stays <= 256.
 //  * Epilogue: O / l from tensor memory to global memory.
 //  * Keys at or past the context length and keys of blocks with an invalid id
 //    are masked by index and their V rows are zeroed in shared memory, so stale
 //    or NaN bytes cannot reach the result.
 //
-// Every mbarrier wait is bounded; on a timeout the CTA records
-// PKV_STATUS_TIMEOUT, drains its outstanding copies and MMAs (bounded) and
-// frees its tensor memory before returning.
+// Every mbarrier wait is bounded; a role whose wait runs out raises a
+// CTA-wide abort flag, the others stop at their next wait, the CTA records
+// PKV_STATUS_TIMEOUT and frees its tensor memory before returning.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -47,16 +61,31 @@ namespace pkv {
 
 namespace {
 
-constexpr int kThreads = 128;
-constexpr uint32_t kHalfTile = 128 * 128;        // 16 KB: 128 rows x 64 bf16
-constexpr uint32_t kOpBytes = 2 * kHalfTile;     // 32 KB: a 128 x 128 bf16 operand (lo | hi halves)
+constexpr int kSoftmaxWarps = 8;  // warps 0-7: warps w and w+4 share lanes 32*(w%4).. and split the columns
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 10 * 32;
+
+constexpr uint32_t kHalfTile = 128 * 128;     // 16 KB: 128 rows x 64 bf16
+constexpr uint32_t kOpBytes = 2 * kHalfTile;  // 32 KB: a 128 x 128 bf16 operand (lo | hi halves)
 constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK0 = kOffQ + kOpBytes;    // stage s: K at kOffK0 + s * 2 * kOpBytes, V right after
-constexpr uint32_t kOffP = kOffK0 + 4 * kOpBytes;
-constexpr uint32_t kOffBar = kOffP + kOpBytes;   // mbarriers: q_full, kv_full[2], s_done, o_done
-constexpr uint32_t kOffTmem = kOffBar + 64;
-constexpr uint32_t kSmemBytes = kOffTmem + 16 + 1024;  // + alignment slack
-constexpr uint32_t kTmemCols = 256;              // S: [0,128), O: [128,256)
+constexpr int kStages = 3;                              // depth of the K and V rings
+constexpr uint32_t kOffK = kOffQ + kOpBytes;            // K ring: kStages x 32 KB
+constexpr uint32_t kOffV = kOffK + kStages * kOpBytes;  // V ring: kStages x 32 KB
+constexpr uint32_t kOffBar = kOffV + kStages * kOpBytes;
+constexpr uint32_t kNumBars = 1 + 4 * kStages + 6;  // q_full, k_full/k_empty/v_full/v_empty[kStages],
+                                                    // s_full[2], p_full[2], o_done[2]
+constexpr uint32_t kOffTmem = kOffBar + 8 * 24;
+constexpr uint32_t kOffAbort = kOffTmem + 8;
+constexpr uint32_t kOffXch = kOffAbort + 8;  // per-row partial maxima [2 tiles][2 halves][128]; after the
+                                             // last tile, per-row partial sums [2 halves][128]
+// The dynamic shared memory is declared 1024-byte aligned (the swizzle period of
+// the TMA/UMMA operands); the kernel checks it and refuses to run otherwise.
+constexpr uint32_t kSmemBytes = kOffXch + 2 * 2 * 128 * 4;
+constexpr uint32_t kTmemCols = 512;                     // S/P 0 [0,128), S/P 1 [128,256), O [256,384)
+constexpr uint32_t kTmemO = 256;
+static_assert(kSmemBytes <= 232448, "prefill shared memory exceeds the per-CTA limit");
+static_assert(kNumBars <= 24, "barrier area");
 
 // Instruction descriptor, kind::f16: D f32, A/B bf16, M = 128, N = 128.
 constexpr uint32_t kIdescBase = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
@@ -82,15 +111,16 @@ __device__ __forceinline__ void store_row(void *out, int32_t bf16, size_t base, 
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_chunk_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                          const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem =
-        reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_u32(smem);
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
-    const int tile = blockIdx.x;
-    const int g = blockIdx.y;
-    const int b = blockIdx.z;
+    const int lane = tid & 31;
+    // Grid (KV group, sequence, row tile), row tiles in reverse: later rows see
+    // more keys, so the longest CTAs start first and the last wave is short.
+    const int g = blockIdx.x;
+    const int b = blockIdx.y;
+    const int tile = gridDim.z - 1 - blockIdx.z;
     const int G = p.group;
     const int rpt = p.rows_per_tile;
 
@@ -101,6 +131,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     griddep_launch_dependents();
     griddep_wait();  // the KV append (or any producer of q) before us on the stream
+    if (sbase & 1023u) {  // operands need the 1 KB swizzle alignment
+        if (tid == 0 && p.status) atomicOr(p.status, kStatusTimeout);
+        return;
+    }
 
     // ---- sequence extent (device data: checked) ----
     const int row0 = __ldg(p.cu_q_lens + b);
@@ -116,25 +150,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int c = ctx - q_len;
     const int last_pos = c + i0 + rows_here - 1;
     const int n_keys = last_pos + 1;  // keys 0 .. last_pos
-    const int n_ktiles = (n_keys + 127) / 128;
+    const int n_tiles = (n_keys + 127) / 128;
     const int nblocks = (ctx + kBlockSize - 1) / kBlockSize;
     const int32_t *table = p.block_tables + static_cast<size_t>(b) * p.max_blocks;
 
     const uint32_t bar_q = sbase + kOffBar;
-    const uint32_t bar_kv0 = bar_q + 8;  // kv_full[0], kv_full[1]
-    const uint32_t bar_s = bar_q + 24;
-    const uint32_t bar_o = bar_q + 32;
+    // K/V ring slot kt % kStages (use number kt / kStages); S/P buffer kt % 2.
+    auto k_full = [&](int st) { return sbase + kOffBar + 8 * (1 + st); };
+    auto k_empty = [&](int st) { return sbase + kOffBar + 8 * (1 + kStages + st); };
+    auto v_full = [&](int st) { return sbase + kOffBar + 8 * (1 + 2 * kStages + st); };
+    auto v_empty = [&](int st) { return sbase + kOffBar + 8 * (1 + 3 * kStages + st); };
+    auto s_full = [&](int s) { return sbase + kOffBar + 8 * (1 + 4 * kStages + s); };
+    auto p_full = [&](int s) { return sbase + kOffBar + 8 * (3 + 4 * kStages + s); };
+    auto o_done = [&](int s) { return sbase + kOffBar + 8 * (5 + 4 * kStages + s); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffTmem);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + kOffAbort);
 
     if (tid == 0) {
         mbar_init(bar_q, 1);
-        mbar_init(bar_kv0, 1);
-        mbar_init(bar_kv0 + 8, 1);
-        mbar_init(bar_s, 1);
-        mbar_init(bar_o, 1);
+        for (int st = 0; st < kStages; ++st) {
+            mbar_init(k_full(st), 1);
+            mbar_init(k_empty(st), 1);
+            mbar_init(v_full(st), 1);
+            mbar_init(v_empty(st), 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(s_full(s), 1);
+            mbar_init(p_full(s), kSoftmaxWarps);
+            mbar_init(o_done(s), 1);
+        }
+        *abort_flag = 0u;
         fence_mbar_init();
     }
-    if (warp == 0) {
+    if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
@@ -142,220 +190,278 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t t_s = tmem + lane_off;        // this warp's S lanes
-    const uint32_t t_o = tmem + lane_off + 128;  // this warp's O lanes
 
-    // Thread 0 gathers key tile kt (8 paged blocks) into stage kt & 1.
-    auto issue_kv = [&](int kt) {
-        const int s = kt & 1;
-        const uint32_t kbase = sbase + kOffK0 + s * 2 * kOpBytes;
-        const uint32_t vbase = kbase + kOpBytes;
-        const uint32_t bar = bar_kv0 + 8 * s;
-        int nload = 0;
-        for (int t = 0; t < 8; ++t) nload += (kt * 8 + t < nblocks) ? 1 : 0;
-        mbar_arrive_expect_tx(bar, nload * 4 * 2048);
-        for (int t = 0; t < 8; ++t) {
-            const int jb = kt * 8 + t;
-            if (jb >= nblocks) break;
-            int phys = __ldg(table + jb);
-            if (static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_blocks)) phys = 0;  // masked below
-            tma_load_4d(kbase + t * 2048, &kmap, bar, 0, 0, g, phys);
-            tma_load_4d(kbase + kHalfTile + t * 2048, &kmap, bar, 64, 0, g, phys);
-            tma_load_4d(vbase + t * 2048, &vmap, bar, 0, 0, g, phys);
-            tma_load_4d(vbase + kHalfTile + t * 2048, &vmap, bar, 64, 0, g, phys);
-        }
+    // A bounded wait that gives up at once after another role gave up.
+    auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
+        if (*abort_flag) return false;
+        if (mbar_wait(bar, parity)) return true;
+        *abort_flag = 1u;
+        return false;
     };
 
-    if (tid == 0) {
-        mbar_arrive_expect_tx(bar_q, kOpBytes);
-        tma_load_3d(sbase + kOffQ, &qmap, bar_q, 0, g * G, row0 + i0);
-        tma_load_3d(sbase + kOffQ + kHalfTile, &qmap, bar_q, 64, g * G, row0 + i0);
-        issue_kv(0);
-        if (n_ktiles > 1) issue_kv(1);
-    }
-
-    // This thread's row of the tile.
-    const int r = tid;
-    const int ii = r / G;
-    const bool row_valid = ii < rows_here;
-    const int pos = c + i0 + (row_valid ? ii : 0);
-    const int limit = min(pos, ctx - 1);  // visible keys: j <= limit
-    const float sl2 = p.scale_log2;
-
-    float m_ref = -INFINITY;  // exponent reference (raised lazily)
-    float l = 0.f;
-    bool fail = !mbar_wait(bar_q, 0);
-    int kt = 0;
-    for (; kt < n_ktiles && !fail; ++kt) {
-        const int s = kt & 1;
-        const uint32_t kbase = sbase + kOffK0 + s * 2 * kOpBytes;
-        const uint32_t vbase = kbase + kOpBytes;
-        fail |= !mbar_wait(bar_kv0 + 8 * s, (kt >> 1) & 1);
-        if (__syncthreads_or(fail)) {
-            fail = true;
-            break;
-        }
-
-        // Which of this tile's blocks have an invalid id (their keys are masked).
-        uint32_t bad = 0;
-        for (int t = 0; t < 8; ++t) {
-            const int jb = kt * 8 + t;
-            if (jb < nblocks && static_cast<unsigned>(__ldg(table + jb)) >= static_cast<unsigned>(p.num_blocks))
-                bad |= 1u << t;
-        }
-        if (bad && tid == 0 && p.status) atomicOr(p.status, kStatusBadBlockId);
-
-        // ---- S = Q K^T ----
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t half = (kk >> 2) * kHalfTile, koff = (kk & 3) * 32;
-                const uint64_t ad = sw128_desc(sbase + kOffQ + half + koff, 16, 1024);
-                const uint64_t bd = sw128_desc(kbase + half + koff, 16, 1024);
-                umma_bf16(tmem, ad, bd, kIdescQK, kk > 0);
+    if (warp == kProducerWarp) {
+        // ---------------- TMA producer (lane 0 issues; lanes 0-7 read the block table) ----------------
+        // Physical block of key tile kt's t-th paged block, read by lane t (one parallel
+        // load per tile instead of eight dependent ones); lane 0 fetches it by shuffle.
+        auto tile_block = [&](int kt) -> int {
+            const int jb = kt * 8 + lane;
+            int mine = 0;
+            if (lane < 8 && jb < nblocks) {
+                mine = __ldg(table + jb);
+                if (static_cast<unsigned>(mine) >= static_cast<unsigned>(p.num_blocks)) mine = 0;  // masked
             }
-            umma_commit(bar_s);
-        }
-        fail |= !mbar_wait(bar_s, kt & 1);
-        tc_fence_after();
-
-        // ---- softmax on this thread's row ----
-        uint32_t sr[4][32];
+            return mine;
+        };
+        // Gather key tile kt's 8 blocks (K or V) into ring slot `dst`; lane t holds block t's id.
+        auto gather = [&](const CUtensorMap *map, uint32_t dst, uint32_t bar, int kt, int mine) {
+            const int nload = min(8, nblocks - kt * 8);
+            if (lane == 0) mbar_arrive_expect_tx(bar, nload * 2 * 2048);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) tmem_ld_32x32b_x32(t_s + 32 * q, sr[q]);
-        tmem_wait_ld();
-        const int key0 = kt * 128;
-        float mt = -INFINITY;
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-#pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                const int j = key0 + 32 * q + k;
-                const bool ok = j <= limit && !((bad >> ((32 * q + k) >> 4)) & 1u);
-                const float v = ok ? __uint_as_float(sr[q][k]) * sl2 : -INFINITY;
-                sr[q][k] = __float_as_uint(v);
-                mt = fmaxf(mt, v);
-            }
-        float alpha = 1.f;
-        if (mt > m_ref + 8.f || (m_ref == -INFINITY && mt != -INFINITY)) {
-            alpha = fast_exp2(m_ref - mt);  // 0 when m_ref = -inf
-            m_ref = mt;
-        }
-        const float mu = m_ref == -INFINITY ? 0.f : m_ref;
-        float rs = 0.f;
-
-        // The previous P V must be done before P is overwritten and O is rescaled.
-        if (kt > 0) fail |= !mbar_wait(bar_o, (kt - 1) & 1);
-        tc_fence_after();
-        if (tid == 0 && kt >= 1 && kt + 1 < n_ktiles) issue_kv(kt + 1);  // stage (kt+1)&1 is free now
-
-        // P as bf16, K-major 128-byte-swizzled rows: chunk c of row r at c ^ (r & 7).
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const uint32_t prow = sbase + kOffP + (q >> 1) * kHalfTile + r * 128;
-            const uint32_t plow = kbase + (q >> 1) * kHalfTile + r * 128;  // remainder: into the spent K tile
-#pragma unroll
-            for (int c8 = 0; c8 < 4; ++c8) {
-                uint32_t w[4], x[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float pa = fast_exp2(__uint_as_float(sr[q][8 * c8 + 2 * e]) - mu);
-                    const float pb = fast_exp2(__uint_as_float(sr[q][8 * c8 + 2 * e + 1]) - mu);
-                    rs += pa + pb;
-                    w[e] = pack_bf16x2(pa, pb);
-                    x[e] = pack_bf16x2(pa - __uint_as_float(w[e] << 16), pb - __uint_as_float(w[e] & 0xffff0000u));
+            for (int t = 0; t < 8; ++t) {
+                const int phys = __shfl_sync(0xffffffffu, mine, t);
+                if (lane == 0 && t < nload) {
+                    tma_load_4d(dst + t * 2048, map, bar, 0, 0, g, phys);
+                    tma_load_4d(dst + kHalfTile + t * 2048, map, bar, 64, 0, g, phys);
                 }
-                const int chunk = (q & 1) * 4 + c8;
-                const uint32_t sw = ((chunk ^ (r & 7)) << 4);
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + sw), "r"(w[0]), "r"(w[1]),
-                             "r"(w[2]), "r"(w[3])
-                             : "memory");
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(plow + sw), "r"(x[0]), "r"(x[1]),
-                             "r"(x[2]), "r"(x[3])
-                             : "memory");
             }
+        };
+        // All lanes walk the schedule (their waits agree through __all_sync); lane 0 issues.
+        auto load_k = [&](int kt, int mine) -> bool {
+            const int st = kt % kStages;
+            if (kt >= kStages && !__all_sync(0xffffffffu, wait(k_empty(st), ((kt / kStages) - 1) & 1))) return false;
+            gather(&kmap, sbase + kOffK + st * kOpBytes, k_full(st), kt, mine);
+            return true;
+        };
+        auto load_v = [&](int kt, int mine) -> bool {
+            const int st = kt % kStages;
+            if (kt >= kStages && !__all_sync(0xffffffffu, wait(v_empty(st), ((kt / kStages) - 1) & 1))) return false;
+            gather(&vmap, sbase + kOffV + st * kOpBytes, v_full(st), kt, mine);
+            return true;
+        };
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar_q, kOpBytes);
+            tma_load_3d(sbase + kOffQ, &qmap, bar_q, 0, g * G, row0 + i0);
+            tma_load_3d(sbase + kOffQ + kHalfTile, &qmap, bar_q, 64, g * G, row0 + i0);
         }
-        l = l * alpha + rs;
+        int cur = tile_block(0);
+        bool ok = load_k(0, cur);
+        for (int kt = 1; ok && kt < n_tiles; ++kt) {
+            const int prev = cur;
+            cur = tile_block(kt);
+            ok = load_k(kt, cur) && load_v(kt - 1, prev);
+        }
+        if (ok) load_v(n_tiles - 1, cur);
+    } else if (warp == kMmaWarp) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            auto mma_s = [&](int kt) -> bool {
+                const int s = kt & 1;
+                const int st = kt % kStages;
+                if (!wait(k_full(st), (kt / kStages) & 1)) return false;
+                // Buffer s held P(kt-2): P(kt-2) V(kt-2) must have consumed it.
+                if (kt >= 2 && !wait(o_done(s), ((kt - 2) >> 1) & 1)) return false;
+                tc_fence_after();
+                const uint32_t kb = sbase + kOffK + st * kOpBytes;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (kk >> 2) * kHalfTile + (kk & 3) * 32;
+                    umma_bf16(tmem + 128 * s, sw128_desc(sbase + kOffQ + off, 16, 1024), sw128_desc(kb + off, 16, 1024),
+                              kIdescQK, kk > 0);
+                }
+                umma_commit(s_full(s));
+                umma_commit(k_empty(st));
+                return true;
+            };
+            auto mma_pv = [&](int kt) -> bool {
+                const int s = kt & 1;
+                const int st = kt % kStages;
+                if (!wait(v_full(st), (kt / kStages) & 1)) return false;
+                if (!wait(p_full(s), (kt >> 1) & 1)) return false;
+                tc_fence_after();
+                const uint32_t vb = sbase + kOffV + st * kOpBytes;
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    // keys 16t .. 16t+15: half t/4 of buffer s, [head | remainder] columns
+                    const uint32_t a_hi = tmem + 128 * s + (t >> 2) * 64 + (t & 3) * 8;
+                    const uint64_t bd = sw128_desc(vb + t * 2048, kHalfTile, 1024);
+                    umma_bf16_tmem_a(tmem + kTmemO, a_hi, bd, kIdescPV, (kt > 0 || t > 0) ? 1u : 0u);
+                    umma_bf16_tmem_a(tmem + kTmemO, a_hi + 32, bd, kIdescPV, 1u);
+                }
+                umma_commit(o_done(s));
+                umma_commit(v_empty(st));
+                return true;
+            };
+            bool ok = wait(bar_q, 0) && mma_s(0);
+            for (int kt = 1; ok && kt < n_tiles; ++kt) ok = mma_s(kt) && mma_pv(kt - 1);
+            if (ok) mma_pv(n_tiles - 1);
+        }
+    } else {
+        // ---------------- softmax warps: one tile row and one column half per thread ----------------
+        // (every wait decision is made warp-uniform, so the .sync.aligned tensor-memory
+        // loads and stores below always see the full warp)
+        const int quarter = warp & 3;  // tensor-memory lanes 32*quarter .. +31
+        const int hc = warp >> 2;      // column half: keys / O dims [64*hc, 64*hc + 64)
+        const int r = quarter * 32 + lane;
+        const int ii = r / G;
+        const bool row_valid = ii < rows_here;
+        const int pos = c + i0 + (row_valid ? ii : 0);
+        const int limit = min(pos, ctx - 1);  // visible keys: j <= limit
+        const float sl2 = p.scale_log2;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+        const uint32_t t_o = lane_base + kTmemO + 64 * hc;
+        float *xch = reinterpret_cast<float *>(smem + kOffXch);  // [tile & 1][half][row]
+        float *xl = reinterpret_cast<float *>(smem + kOffXch);   // [half][row], epilogue only
+        auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory"); };
 
-        // Rescale O rows whose reference max moved (warp-uniform tensor-memory access).
-        if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        float m_ref = -INFINITY;  // exponent reference (raised lazily)
+        float l = 0.f;            // this half's share of the row sum
+        // Both warps of a pair pass exactly one pair barrier per tile and one in the
+        // epilogue on every path: after a wait gives up (`alive` false) the loop keeps
+        // turning without work, so the named barriers always match and never hang.
+        bool alive = true;
+        for (int kt = 0; kt < n_tiles; ++kt) {
+            const int s = kt & 1;
+            alive = alive && __all_sync(0xffffffffu, wait(s_full(s), (kt >> 1) & 1));
+            if (!alive) {
+                pair_sync();
+                continue;
+            }
+            tc_fence_after();
+            const uint32_t t_s = lane_base + 128 * s + 64 * hc;
+
+            // Which of this tile's blocks have an invalid id (their keys are masked):
+            // lane t < 8 checks block t, a ballot shares the answer.
+            const int jb = kt * 8 + lane;
+            const bool bad_lane = lane < 8 && jb < nblocks &&
+                                  static_cast<unsigned>(__ldg(table + jb)) >= static_cast<unsigned>(p.num_blocks);
+            const uint32_t bad = __ballot_sync(0xffffffffu, bad_lane);
+            if (bad && r == 0 && hc == 0 && p.status) atomicOr(p.status, kStatusBadBlockId);
+            const int key0 = kt * 128 + 64 * hc;  // first key of this half
+
+            uint32_t sr[2][32];
+            tmem_ld_32x32b_x32(t_s, sr[0]);
+            tmem_ld_32x32b_x32(t_s + 32, sr[1]);
+            tmem_wait_ld();
+            // Mask by index (skipped for chunks whose 32 keys are all visible); half max.
+            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint32_t orow[32];
-                tmem_ld_32x32b_x32(t_o + 32 * q, orow);
-                tmem_wait_ld();
+            for (int u = 0; u < 2; ++u) {
+                const int q = 2 * hc + u;  // 32-key chunk of the tile
+                const int kc = key0 + 32 * u;
+                if (!(kc + 31 <= limit && !((bad >> (2 * q)) & 3u))) {
 #pragma unroll
-                for (int k = 0; k < 32; ++k) orow[k] = __float_as_uint(__uint_as_float(orow[k]) * alpha);
-                tmem_st_32x32b_x32(t_o + 32 * q, orow);
+                    for (int k = 0; k < 32; ++k) {
+                        const bool ok = kc + k <= limit && !((bad >> ((32 * q + k) >> 4)) & 1u);
+                        if (!ok) sr[u][k] = __float_as_uint(-INFINITY);
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < 32; ++k) mx[k & 3] = fmaxf(mx[k & 3], __uint_as_float(sr[u][k]));
+            }
+            xch[(s * 2 + hc) * 128 + r] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+            pair_sync();
+            const float mraw = fmaxf(xch[(s * 2) * 128 + r], xch[(s * 2 + 1) * 128 + r]);
+            const float mt = mraw == -INFINITY ? -INFINITY : mraw * sl2;  // scale > 0 keeps the order
+            float alpha = 1.f;
+            if (mt > m_ref + 8.f) {  // also taken at the first visible key (m_ref = -inf)
+                alpha = fast_exp2(m_ref - mt);  // 0 when m_ref = -inf
+                m_ref = mt;
+            }
+            const float mu = m_ref == -INFINITY ? 0.f : m_ref;
+
+            // Rescaling O needs every earlier P V done (in-order: the latest, P(kt-1) V(kt-1)).
+            if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                alive = __all_sync(0xffffffffu, wait(o_done((kt - 1) & 1), ((kt - 1) >> 1) & 1));
+                if (!alive) continue;
+                tc_fence_after();
+#pragma unroll 1
+                for (int q = 0; q < 2; ++q) {
+                    uint32_t orow[32];
+                    tmem_ld_32x32b_x32(t_o + 32 * q, orow);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) orow[k] = __float_as_uint(__uint_as_float(orow[k]) * alpha);
+                    tmem_st_32x32b_x32(t_o + 32 * q, orow);
+                }
+                tmem_wait_st();
+            }
+
+            // P = 2^(s * scale * log2(e) - m), written back over this half as
+            // [32 columns bf16 head | 32 columns bf16 remainder] (two keys per
+            // column, the lower key in the low half).
+            float rsum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {  // 32 keys -> 16 head columns + 16 remainder columns
+                uint32_t hi[16], lo[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const float pa = fast_exp2(fmaf(__uint_as_float(sr[u][2 * e]), sl2, -mu));
+                    const float pb = fast_exp2(fmaf(__uint_as_float(sr[u][2 * e + 1]), sl2, -mu));
+                    rsum[e & 3] += pa + pb;
+                    const uint32_t w = pack_bf16x2(pa, pb);
+                    hi[e] = w;
+                    lo[e] = pack_bf16x2(pa - __uint_as_float(w << 16), pb - __uint_as_float(w & 0xffff0000u));
+                }
+                tmem_st_32x32b_x16(t_s + 16 * u, hi);
+                tmem_st_32x32b_x16(t_s + 32 + 16 * u, lo);
             }
             tmem_wait_st();
-        }
+            l = l * alpha + ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3]));
 
-        // Zero V rows of keys no row may see (past the context, or of a bad block).
-        {
-            const int rv = ctx - key0;  // keys [rv, 128) are past the context
+            // Zero V rows of keys no row may see (past the context, or of a bad block).
+            const int rv = ctx - kt * 128;  // keys [rv, 128) of the tile are past the context
             if (rv < 128 || bad) {
-                for (int idx = tid; idx < 128 * 16; idx += kThreads) {
+                alive = __all_sync(0xffffffffu, wait(v_full(kt % kStages), (kt / kStages) & 1));
+                if (!alive) continue;
+                const uint32_t vb = sbase + kOffV + (kt % kStages) * kOpBytes;
+                for (int idx = hc * 128 + r; idx < 128 * 16; idx += kSoftmaxWarps * 32) {
                     const int key = idx >> 4, ch = idx & 15;
                     if (key >= rv || ((bad >> (key >> 4)) & 1u)) {
-                        const uint32_t addr = vbase + (ch >> 3) * kHalfTile + key * 128 + (ch & 7) * 16;
+                        const uint32_t addr = vb + (ch >> 3) * kHalfTile + key * 128 + (ch & 7) * 16;
                         asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
                     }
                 }
             }
+
+            fence_proxy_async_smem();  // zeroed V rows -> the tensor core (async proxy)
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full(s));
         }
 
-        fence_proxy_async_smem();
-        tc_fence_before();
-        if (__syncthreads_or(fail)) {
-            fail = true;
-            break;
-        }
-
-        // ---- O += P_hi V + P_lo V ----
-        if (tid == 0) {
+        // ---- epilogue: out = O / l (the two halves add their row sums) ----
+        pair_sync();  // the last tile's maxima have been read: the exchange area is free
+        xl[hc * 128 + r] = l;
+        pair_sync();
+        if (alive && __all_sync(0xffffffffu, wait(o_done((n_tiles - 1) & 1), ((n_tiles - 1) >> 1) & 1))) {
             tc_fence_after();
+            const float lt = xl[r] + xl[128 + r];
+            const float inv = lt > 0.f ? 1.f / lt : 0.f;
+            const size_t orow_base =
+                (static_cast<size_t>(row0 + i0 + ii) * p.n_q + static_cast<size_t>(g) * G + (r % G)) * kHeadDim +
+                64 * hc;
 #pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                const uint32_t aoff = (t >> 2) * kHalfTile + (t & 3) * 32;
-                const uint64_t bd = sw128_desc(vbase + t * 2048, kHalfTile, 1024);
-                umma_bf16(tmem + 128, sw128_desc(sbase + kOffP + aoff, 16, 1024), bd, kIdescPV,
-                          (kt > 0 || t > 0) ? 1u : 0u);
-                umma_bf16(tmem + 128, sw128_desc(kbase + aoff, 16, 1024), bd, kIdescPV, 1u);
+            for (int q = 0; q < 2; ++q) {
+                uint32_t orow[32];
+                tmem_ld_32x32b_x32(t_o + 32 * q, orow);
+                tmem_wait_ld();
+                if (row_valid)
+                    store_row(p.out, p.out_bf16, orow_base + 32 * q, reinterpret_cast<float *>(orow), 32, inv);
             }
-            umma_commit(bar_o);
         }
     }
 
-    if (!fail) {
-        fail |= !mbar_wait(bar_o, (n_ktiles - 1) & 1);
-        tc_fence_after();
-    }
-    if (__syncthreads_or(fail)) {
-        if (tid == 0) {
-            if (p.status) atomicOr(p.status, kStatusTimeout);
-            // Best effort: let outstanding copies and MMAs finish before freeing.
-            mbar_wait(bar_o, (max(kt, 1) - 1) & 1);
-        }
-    } else {
-        // ---- epilogue: out = O / l ----
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        const size_t orow_base =
-            (static_cast<size_t>(row0 + i0 + ii) * p.n_q + static_cast<size_t>(g) * G + (r % G)) * kHeadDim;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            uint32_t orow[32];
-            tmem_ld_32x32b_x32(t_o + 32 * q, orow);
-            tmem_wait_ld();
-            if (row_valid) store_row(p.out, p.out_bf16, orow_base + 32 * q, reinterpret_cast<float *>(orow), 32, inv);
-        }
-    }
+    // ---- teardown: every role is done (or gave up); free tensor memory ----
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+    if (*abort_flag) {
+        if (tid == 0 && p.status) atomicOr(p.status, kStatusTimeout);
+        // Best effort: let MMAs still in flight finish before the columns are freed.
+        if (warp == kMmaWarp && lane == 0) mbar_wait(o_done((n_tiles - 1) & 1), ((n_tiles - 1) >> 1) & 1);
+        __syncwarp();
+    }
+    if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace
@@ -369,7 +475,7 @@ cudaError_t prefill_prepare_device() {
 
 cudaError_t launch_prefill_chunk(const CUtensorMap &qmap, const CUtensorMap &kmap, const CUtensorMap &vmap,
                                  const PrefillParams &p, int max_q_len, cudaStream_t stream) {
-    const dim3 grid((max_q_len + p.rows_per_tile - 1) / p.rows_per_tile, p.n_kv, p.num_seqs);
+    const dim3 grid(p.n_kv, p.num_seqs, (max_q_len + p.rows_per_tile - 1) / p.rows_per_tile);
     return launch_pdl(prefill_chunk_kernel, grid, dim3(kThreads), kSmemBytes, stream, qmap, kmap, vmap, p);
 }
 
