@@ -254,14 +254,18 @@ PKV_API size_t paged_attention_prefill_workspace_size(int32_t num_seqs, int32_t 
  * computes (same page, 变革 3; walkthrough page, Chunked Prefill: "formula
  * unchanged").  With q_len = 1 a row is a decode row.
  *
- *   out        : out_dtype [cu_q_lens[num_seqs]][num_q_heads][head_dim], device
- *   q          : bf16 [cu_q_lens[num_seqs]][num_q_heads][head_dim], device
+ *   out        : out_dtype [cu_q_lens[num_seqs]][num_q_heads][head_dim], device,
+ *                16-B aligned
+ *   q          : bf16 [cu_q_lens[num_seqs]][num_q_heads][head_dim], device,
+ *                16-B aligned
  *   cu_q_lens  : int32 [num_seqs + 1], device, non-decreasing, cu_q_lens[0] = 0
  *   max_q_len  : host upper bound of every q_len (sizes the launch grid)
  *   total_q_rows : host value of cu_q_lens[num_seqs] (bounds the q/out tensors)
  *   workspace  : >= paged_attention_prefill_workspace_size() bytes (status word)
  * Uses the 5th-generation tensor cores (tcgen05, accumulators in tensor memory).
- * Errors: PKV_ERR_INVALID_ARG / PKV_ERR_UNSUPPORTED /
+ * Errors: PKV_ERR_INVALID_ARG (null or misaligned pointer, bad size) /
+ *         PKV_ERR_UNSUPPORTED (group size not in {1,2,4,8,16}, more than 65535
+ *         row tiles x group, or num_blocks x num_kv_heads above INT32_MAX) /
  *         PKV_ERR_WORKSPACE_TOO_SMALL / PKV_ERR_CUDA.
  */
 PKV_API int paged_attention_prefill_chunk(void *out, int32_t out_dtype, const void *q, const int32_t *cu_q_lens,

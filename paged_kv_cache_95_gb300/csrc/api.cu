@@ -89,18 +89,43 @@ bool encode_pool_map(CUtensorMap *map, const void *base, int32_t num_blocks, int
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Query tensor [rows][n_q][128] bf16 viewed as 3-D (head_dim, head, row); box =
-// 64 dims x G heads x (128 / G) rows, 128-byte swizzle: one box is 128 rows of
-// 128 bytes ordered (row, head).
-bool encode_q_map(CUtensorMap *map, const void *base, int32_t rows, int32_t n_q, int32_t group) {
+// The same pool viewed as 5-D so that ONE box is a whole 4 KB (block, head) tile
+// in the order the tensor core wants it: dims inner->outer are 64 dims (128 B),
+// 8 slots (stride 256 B), the two 64-dim halves (stride 128 B), the two 8-slot
+// groups (stride 2 KB) and the (block, head) tile index block * n_kv + head
+// (stride 4 KB).  The box (64, 8, 2, 2, 1) lands in shared memory as
+// [slot group][dim half][8 slots][128 B], i.e. four 1 KB swizzle atoms.
+bool encode_pool_tile_map(CUtensorMap *map, const void *base, int32_t num_blocks, int32_t n_kv) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
+    const uint64_t tiles = static_cast<uint64_t>(num_blocks) * static_cast<uint64_t>(n_kv);
+    if (tiles > static_cast<uint64_t>(INT32_MAX)) return false;  // tile index is a 32-bit coordinate
+    const cuuint64_t dims[5] = {64, 8, 2, 2, static_cast<cuuint64_t>(tiles)};
+    const cuuint64_t strides[4] = {256, 128, 2048, 4096};
+    const cuuint32_t box[5] = {64, 8, 2, 2, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Row tensor [rows][n_q][128] (the chunk's q, bf16, or its output, bf16 or fp32)
+// viewed as 3-D (head_dim, head, row); box = 128 bytes of dims (bf16: 64, fp32:
+// 32) x G heads x (128 / G) rows, 128-byte swizzle: one box is 128 tile rows of
+// 128 bytes ordered (row, head), the layout of the Q tile and of a staged
+// output tile.
+bool encode_rows_map(CUtensorMap *map, const void *base, int32_t rows, int32_t n_q, int32_t group, bool fp32) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t es = fp32 ? 4 : 2;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(n_q),
                                 static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim) * 2, static_cast<cuuint64_t>(kHeadDim) * 2 * n_q};
-    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(128 / group)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim) * es, static_cast<cuuint64_t>(kHeadDim) * es * n_q};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), static_cast<cuuint32_t>(group),
+                               static_cast<cuuint32_t>(128 / group)};
     const cuuint32_t estr[3] = {1, 1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+    return fn(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+              const_cast<void *>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -338,8 +363,10 @@ int paged_attention_prefill_chunk(void *out, int32_t out_dtype, const void *q, c
         return PKV_ERR_INVALID_ARG;
     if ((static_cast<int64_t>(max_q_len) + 127) / 128 * G > 65535) return PKV_ERR_UNSUPPORTED;  // grid z
     if (static_cast<int64_t>(max_blocks_per_seq) * kBlockSize > INT32_MAX) return PKV_ERR_INVALID_ARG;
+    // K/V tiles are addressed by the 32-bit index block * n_kv + head.
+    if (static_cast<int64_t>(cache->num_blocks) * cache->num_kv_heads > INT32_MAX) return PKV_ERR_UNSUPPORTED;
     if (!std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
-    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 16) || !aligned(out, 4) ||
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 16) || !aligned(out, 16) ||
         !aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(cu_q_lens, 4))
         return PKV_ERR_INVALID_ARG;
     if (!workspace || !aligned(workspace, 256)) return PKV_ERR_INVALID_ARG;
@@ -349,10 +376,11 @@ int paged_attention_prefill_chunk(void *out, int32_t out_dtype, const void *q, c
     const int dev = current_device();
     if (dev < 0 || dev >= kMaxDevices) return PKV_ERR_CUDA;
 
-    CUtensorMap qmap, kmap, vmap;
-    if (!encode_q_map(&qmap, q, total_q_rows, num_q_heads, G) ||
-        !encode_pool_map(&kmap, k_cache, cache->num_blocks, cache->num_kv_heads) ||
-        !encode_pool_map(&vmap, v_cache, cache->num_blocks, cache->num_kv_heads))
+    CUtensorMap qmap, kmap, vmap, omap;
+    if (!encode_rows_map(&qmap, q, total_q_rows, num_q_heads, G, false) ||
+        !encode_rows_map(&omap, out, total_q_rows, num_q_heads, G, out_dtype == PKV_DTYPE_FLOAT32) ||
+        !encode_pool_tile_map(&kmap, k_cache, cache->num_blocks, cache->num_kv_heads) ||
+        !encode_pool_tile_map(&vmap, v_cache, cache->num_blocks, cache->num_kv_heads))
         return PKV_ERR_CUDA;
     std::call_once(g_prefill_prepared[dev], [&] { g_prefill_prep_err[dev] = pkv::prefill_prepare_device(); });
     if (g_prefill_prep_err[dev] != cudaSuccess) return PKV_ERR_CUDA;
@@ -373,7 +401,8 @@ int paged_attention_prefill_chunk(void *out, int32_t out_dtype, const void *q, c
     p.total_rows = total_q_rows;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     p.out_bf16 = out_dtype == PKV_DTYPE_BF16;
-    if (pkv::launch_prefill_chunk(qmap, kmap, vmap, p, max_q_len, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    if (pkv::launch_prefill_chunk(qmap, kmap, vmap, omap, p, max_q_len, static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
         return PKV_ERR_CUDA;
     return PKV_OK;
 }

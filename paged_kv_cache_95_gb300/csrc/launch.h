@@ -96,6 +96,6 @@ struct PrefillParams {
 size_t prefill_smem_bytes();
 cudaError_t prefill_prepare_device();
 cudaError_t launch_prefill_chunk(const CUtensorMap &qmap, const CUtensorMap &kmap, const CUtensorMap &vmap,
-                                 const PrefillParams &p, int max_q_len, cudaStream_t stream);
+                                 const CUtensorMap &omap, const PrefillParams &p, int max_q_len, cudaStream_t stream);
 
 }  // namespace pkv

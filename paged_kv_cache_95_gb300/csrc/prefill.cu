@@ -12,16 +12,21 @@
 //    the group (row r = position (r / G), head (r % G)), so every K/V tile is
 //    shared by the whole group.  Q is loaded once by TMA (128-byte swizzle).
 //  * Keys are walked in tiles of 128 (= 8 paged blocks of 16).  Each paged
-//    block's K and V tiles (4 KB each) are gathered with TMA from the block
-//    table into separate 3-deep K and V rings; the blocks' halves are placed so
-//    that every operand is one canonical 128-byte-swizzled UMMA layout: K as a
-//    K-major B operand, V as an MN-major B operand.
+//    block's K and V tiles (4 KB each) are gathered from the block table with
+//    ONE TMA copy apiece into separate 3-deep K and V rings.  The copy's 5-D
+//    view of the pool lands a tile as [slot group (keys 0-7 | 8-15)][dim half]
+//    [8 slots][128 B], four 1 KB 128-byte-swizzle atoms, so that eight tiles
+//    side by side form one canonical UMMA operand: K as a K-major B operand
+//    (8-key groups 2 KB apart, the upper dim half 1 KB in), V per 16-key step
+//    as an MN-major B operand (dim halves 1 KB apart, key groups 2 KB apart).
 //
 // Warp roles (warp specialisation, all hand-offs through mbarriers):
-//  * warp 8: TMA producer (lane 0 issues; lanes 0-7 read a tile's block-table
-//    entries in parallel).  Loads in the order the MMAs consume them
-//    -- K0, K1, V0, K2, V1, ... -- refilling a K slot as soon as the S MMA that
-//    read it completes and a V slot as soon as its P V MMAs complete.
+//  * warps 8 and 10: TMA producers for K and V.  Lane t < 8 reads block t of a
+//    key tile from the block table (one tile ahead) and issues that block's
+//    copy: the eight copies go out as one warp instruction, which keeps more
+//    of them in flight than a loop in one lane.  A K slot is
+//    refilled as soon as the S MMA that read it completes, a V slot as soon as
+//    its P V MMAs complete.
 //  * warp 9 (one lane): MMA issuer; also owns the tensor-memory allocation.
 //    S(k) = Q K(k)^T (M=128, N=128, K=128) goes to tensor-memory buffer k % 2
 //    (columns [0,128) or [128,256)); O += P(k) V(k) accumulates in columns
@@ -35,13 +40,17 @@
 //    their row maxima through shared memory (a 64-thread named barrier per
 //    pair).  Each updates the running max and its half of the running sum
 //    (fp32, log2 domain) and writes P = 2^(s - m) back over its half as
-//    [bf16 head | bf16 remainder] (P V = P_hi V + P_lo V keeps
-//    the weights to ~2^-17 relative).  P is thereby double-buffered with S, so
+//    [bf16 head | bf16 remainder] (head = P truncated to bf16, remainder = the
+//    rest rounded to bf16; P V = P_hi V + P_lo V keeps the weights to ~2^-16
+//    relative, with integer and byte-permute operations only).  P is thereby double-buffered with S, so
 //    the softmax of tile k+1 never waits for P(k) V(k); it waits for it only
 //    when it must rescale O.  The exponent reference is only raised when a
 //    row's max grows by more than 2^8, in which case the row's O is rescaled in
 //    tensor memory; P stays <= 256.
-//  * Epilogue: O / l from tensor memory to global memory.
+//  * Epilogue: O / l from tensor memory; a full tile is staged in shared
+//    memory (the K ring is free by then, same 128-byte-swizzled layout as the Q
+//    tile) and leaves by TMA store, a ragged last tile by 16-byte stores of its
+//    valid rows only (a whole-box store would overwrite the next sequence).
 //  * Keys at or past the context length and keys of blocks with an invalid id
 //    are masked by index and their V rows are zeroed in shared memory, so stale
 //    or NaN bytes cannot reach the result.
@@ -62,19 +71,22 @@ namespace pkv {
 namespace {
 
 constexpr int kSoftmaxWarps = 8;  // warps 0-7: warps w and w+4 share lanes 32*(w%4).. and split the columns
-constexpr int kProducerWarp = 8;
+constexpr int kProducerK = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kThreads = 10 * 32;
+constexpr int kProducerV = 10;
+constexpr int kThreads = 11 * 32;
 
-constexpr uint32_t kHalfTile = 128 * 128;     // 16 KB: 128 rows x 64 bf16
-constexpr uint32_t kOpBytes = 2 * kHalfTile;  // 32 KB: a 128 x 128 bf16 operand (lo | hi halves)
-constexpr uint32_t kOffQ = 0;
-constexpr int kStages = 3;                              // depth of the K and V rings
-constexpr uint32_t kOffK = kOffQ + kOpBytes;            // K ring: kStages x 32 KB
-constexpr uint32_t kOffV = kOffK + kStages * kOpBytes;  // V ring: kStages x 32 KB
-constexpr uint32_t kOffBar = kOffV + kStages * kOpBytes;
-constexpr uint32_t kNumBars = 1 + 4 * kStages + 6;  // q_full, k_full/k_empty/v_full/v_empty[kStages],
-                                                    // s_full[2], p_full[2], o_done[2]
+constexpr uint32_t kHalfTile = 128 * 128;     // 16 KB: 128 rows x 128 bytes (Q dim half; staged output box)
+constexpr uint32_t kOpBytes = 2 * kHalfTile;  // 32 KB: a 128 x 128 bf16 operand
+constexpr uint32_t kBlkBytes = 4096;          // one paged (block, head) tile inside a K/V operand
+constexpr int kStagesK = 3;                              // K ring depth
+constexpr int kStagesV = 3;                              // V ring depth
+constexpr uint32_t kOffQ = 0;                            // Q tile: [dim half][128 rows][128 B]
+constexpr uint32_t kOffK = kOffQ + kOpBytes;             // K ring: kStagesK x 32 KB
+constexpr uint32_t kOffV = kOffK + kStagesK * kOpBytes;  // V ring: kStagesV x 32 KB
+constexpr uint32_t kOffBar = kOffV + kStagesV * kOpBytes;
+constexpr int kBarS = 1 + 2 * kStagesK + 2 * kStagesV;  // q_full, k_full/k_empty[kStagesK], v_full/v_empty[kStagesV],
+constexpr uint32_t kNumBars = kBarS + 6;                 // then s_full[2], p_full[2], o_done[2]
 constexpr uint32_t kOffTmem = kOffBar + 8 * 24;
 constexpr uint32_t kOffAbort = kOffTmem + 8;
 constexpr uint32_t kOffXch = kOffAbort + 8;  // per-row partial maxima [2 tiles][2 halves][128]; after the
@@ -82,7 +94,7 @@ constexpr uint32_t kOffXch = kOffAbort + 8;  // per-row partial maxima [2 tiles]
 // The dynamic shared memory is declared 1024-byte aligned (the swizzle period of
 // the TMA/UMMA operands); the kernel checks it and refuses to run otherwise.
 constexpr uint32_t kSmemBytes = kOffXch + 2 * 2 * 128 * 4;
-constexpr uint32_t kTmemCols = 512;                     // S/P 0 [0,128), S/P 1 [128,256), O [256,384)
+constexpr uint32_t kTmemCols = 512;  // S/P 0 [0,128), S/P 1 [128,256), O [256,384)
 constexpr uint32_t kTmemO = 256;
 static_assert(kSmemBytes <= 232448, "prefill shared memory exceeds the per-CTA limit");
 static_assert(kNumBars <= 24, "barrier area");
@@ -98,19 +110,51 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
            (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-__device__ __forceinline__ void store_row(void *out, int32_t bf16, size_t base, const float *v, int n, float inv) {
+// 32 consecutive output values of one row (v scaled by inv) straight to global
+// memory in 16-byte stores; base is a multiple of 32 elements.
+__device__ __forceinline__ void store_row(void *out, int32_t bf16, size_t base, const uint32_t (&v)[32], float inv) {
+    auto f = [&](int i) { return __uint_as_float(v[i]) * inv; };
     if (bf16) {
-        uint32_t *o = reinterpret_cast<uint32_t *>(static_cast<__nv_bfloat16 *>(out) + base);
-        for (int i = 0; i < n; i += 2) o[i / 2] = pack_bf16x2(v[i] * inv, v[i + 1] * inv);
+        uint4 *o = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(out) + base);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            o[c] = make_uint4(pack_bf16x2(f(8 * c), f(8 * c + 1)), pack_bf16x2(f(8 * c + 2), f(8 * c + 3)),
+                              pack_bf16x2(f(8 * c + 4), f(8 * c + 5)), pack_bf16x2(f(8 * c + 6), f(8 * c + 7)));
     } else {
         float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(out) + base);
-        for (int i = 0; i < n; i += 4) o[i / 4] = make_float4(v[i] * inv, v[i + 1] * inv, v[i + 2] * inv, v[i + 3] * inv);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) o[c] = make_float4(f(4 * c), f(4 * c + 1), f(4 * c + 2), f(4 * c + 3));
+    }
+}
+
+// The same 32 values (dims 64 * hc + 32 * q ..) into the staged output tile: boxes
+// of 128 rows x 128 bytes (bf16: 64 dims, fp32: 32 dims), 16-byte chunk c of row
+// r at chunk c ^ (r & 7) -- the layout the output tensor map's TMA store reads.
+__device__ __forceinline__ void stage_row(uint32_t stage, int32_t bf16, int r, int hc, int q, const uint32_t (&v)[32],
+                                          float inv) {
+    auto f = [&](int i) { return __uint_as_float(v[i]) * inv; };
+    if (bf16) {
+        const uint32_t row = stage + hc * (128 * 128) + r * 128;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + (((4 * q + c) ^ (r & 7)) << 4)),
+                         "r"(pack_bf16x2(f(8 * c), f(8 * c + 1))), "r"(pack_bf16x2(f(8 * c + 2), f(8 * c + 3))),
+                         "r"(pack_bf16x2(f(8 * c + 4), f(8 * c + 5))), "r"(pack_bf16x2(f(8 * c + 6), f(8 * c + 7)))
+                         : "memory");
+    } else {
+        const uint32_t row = stage + (2 * hc + q) * (128 * 128) + r * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(row + ((c ^ (r & 7)) << 4)), "f"(f(4 * c)),
+                         "f"(f(4 * c + 1)), "f"(f(4 * c + 2)), "f"(f(4 * c + 3))
+                         : "memory");
     }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_chunk_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-                         const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
+                         const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
+                         const PrefillParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_u32(smem);
     const int tid = threadIdx.x;
@@ -128,6 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tensormap(&qmap);
         prefetch_tensormap(&kmap);
         prefetch_tensormap(&vmap);
+        prefetch_tensormap(&omap);
     }
     griddep_launch_dependents();
     griddep_wait();  // the KV append (or any producer of q) before us on the stream
@@ -155,22 +200,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t *table = p.block_tables + static_cast<size_t>(b) * p.max_blocks;
 
     const uint32_t bar_q = sbase + kOffBar;
-    // K/V ring slot kt % kStages (use number kt / kStages); S/P buffer kt % 2.
+    // K slot kt % kStagesK (use kt / kStagesK), V slot kt % kStagesV (use kt / kStagesV), S/P buffer kt % 2.
     auto k_full = [&](int st) { return sbase + kOffBar + 8 * (1 + st); };
-    auto k_empty = [&](int st) { return sbase + kOffBar + 8 * (1 + kStages + st); };
-    auto v_full = [&](int st) { return sbase + kOffBar + 8 * (1 + 2 * kStages + st); };
-    auto v_empty = [&](int st) { return sbase + kOffBar + 8 * (1 + 3 * kStages + st); };
-    auto s_full = [&](int s) { return sbase + kOffBar + 8 * (1 + 4 * kStages + s); };
-    auto p_full = [&](int s) { return sbase + kOffBar + 8 * (3 + 4 * kStages + s); };
-    auto o_done = [&](int s) { return sbase + kOffBar + 8 * (5 + 4 * kStages + s); };
+    auto k_empty = [&](int st) { return sbase + kOffBar + 8 * (1 + kStagesK + st); };
+    auto v_full = [&](int st) { return sbase + kOffBar + 8 * (1 + 2 * kStagesK + st); };
+    auto v_empty = [&](int st) { return sbase + kOffBar + 8 * (1 + 2 * kStagesK + kStagesV + st); };
+    auto s_full = [&](int s) { return sbase + kOffBar + 8 * (kBarS + s); };
+    auto p_full = [&](int s) { return sbase + kOffBar + 8 * (kBarS + 2 + s); };
+    auto o_done = [&](int s) { return sbase + kOffBar + 8 * (kBarS + 4 + s); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffTmem);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + kOffAbort);
 
     if (tid == 0) {
         mbar_init(bar_q, 1);
-        for (int st = 0; st < kStages; ++st) {
+        for (int st = 0; st < kStagesK; ++st) {
             mbar_init(k_full(st), 1);
             mbar_init(k_empty(st), 1);
+        }
+        for (int st = 0; st < kStagesV; ++st) {
             mbar_init(v_full(st), 1);
             mbar_init(v_empty(st), 1);
         }
@@ -198,75 +245,73 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 1u;
         return false;
     };
+    // The same for a whole warp: lane 0 polls (one poller per warp keeps the
+    // barrier words free for the copies' transaction updates), the warp barrier
+    // hands its view of memory to the other lanes.
+    auto warp_wait = [&](uint32_t bar, uint32_t parity) -> bool {
+        bool ok = false;
+        if (lane == 0) ok = wait(bar, parity);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        __syncwarp();
+        return ok;
+    };
 
-    if (warp == kProducerWarp) {
-        // ---------------- TMA producer (lane 0 issues; lanes 0-7 read the block table) ----------------
-        // Physical block of key tile kt's t-th paged block, read by lane t (one parallel
-        // load per tile instead of eight dependent ones); lane 0 fetches it by shuffle.
-        auto tile_block = [&](int kt) -> int {
-            const int jb = kt * 8 + lane;
-            int mine = 0;
-            if (lane < 8 && jb < nblocks) {
-                mine = __ldg(table + jb);
-                if (static_cast<unsigned>(mine) >= static_cast<unsigned>(p.num_blocks)) mine = 0;  // masked
-            }
-            return mine;
-        };
-        // Gather key tile kt's 8 blocks (K or V) into ring slot `dst`; lane t holds block t's id.
-        auto gather = [&](const CUtensorMap *map, uint32_t dst, uint32_t bar, int kt, int mine) {
-            const int nload = min(8, nblocks - kt * 8);
-            if (lane == 0) mbar_arrive_expect_tx(bar, nload * 2 * 2048);
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                const int phys = __shfl_sync(0xffffffffu, mine, t);
-                if (lane == 0 && t < nload) {
-                    tma_load_4d(dst + t * 2048, map, bar, 0, 0, g, phys);
-                    tma_load_4d(dst + kHalfTile + t * 2048, map, bar, 64, 0, g, phys);
-                }
-            }
-        };
-        // All lanes walk the schedule (their waits agree through __all_sync); lane 0 issues.
-        auto load_k = [&](int kt, int mine) -> bool {
-            const int st = kt % kStages;
-            if (kt >= kStages && !__all_sync(0xffffffffu, wait(k_empty(st), ((kt / kStages) - 1) & 1))) return false;
-            gather(&kmap, sbase + kOffK + st * kOpBytes, k_full(st), kt, mine);
-            return true;
-        };
-        auto load_v = [&](int kt, int mine) -> bool {
-            const int st = kt % kStages;
-            if (kt >= kStages && !__all_sync(0xffffffffu, wait(v_empty(st), ((kt / kStages) - 1) & 1))) return false;
-            gather(&vmap, sbase + kOffV + st * kOpBytes, v_full(st), kt, mine);
-            return true;
-        };
-        if (lane == 0) {
+    if (warp == kProducerK || warp == kProducerV) {
+        // ---------------- TMA producers: warp 8 fills the K ring, warp 10 the V ring ----------------
+        const bool is_k = warp == kProducerK;
+        const CUtensorMap *map = is_k ? &kmap : &vmap;
+        const uint32_t ring = sbase + (is_k ? kOffK : kOffV);
+        const int stages = is_k ? kStagesK : kStagesV;
+        if (is_k && lane == 0) {
             mbar_arrive_expect_tx(bar_q, kOpBytes);
             tma_load_3d(sbase + kOffQ, &qmap, bar_q, 0, g * G, row0 + i0);
             tma_load_3d(sbase + kOffQ + kHalfTile, &qmap, bar_q, 64, g * G, row0 + i0);
         }
-        int cur = tile_block(0);
-        bool ok = load_k(0, cur);
-        for (int kt = 1; ok && kt < n_tiles; ++kt) {
-            const int prev = cur;
-            cur = tile_block(kt);
-            ok = load_k(kt, cur) && load_v(kt - 1, prev);
+        // (block, head) tile index of key tile kt's t-th paged block, read by lane t
+        // (one parallel load per tile); invalid ids fetch tile 0 and are masked.
+        auto tile_index = [&](int kt) -> int {
+            const int jb = kt * 8 + lane;
+            int mine = 0;
+            if (lane < 8 && jb < nblocks) {
+                mine = __ldg(table + jb);
+                if (static_cast<unsigned>(mine) >= static_cast<unsigned>(p.num_blocks)) mine = 0;
+            }
+            return mine * p.n_kv + g;
+        };
+        // All lanes walk the schedule (lane 0 waits for the warp); lane t
+        // issues block t.  The next tile's table entries are read before this tile's wait.
+        int next = tile_index(0);
+        for (int kt = 0; kt < n_tiles; ++kt) {
+            const int mine = next;
+            if (kt + 1 < n_tiles) next = tile_index(kt + 1);
+            const int st = kt % stages;
+            if (kt >= stages &&
+                !warp_wait(is_k ? k_empty(st) : v_empty(st), ((kt / stages) - 1) & 1))
+                break;
+            const uint32_t bar = is_k ? k_full(st) : v_full(st);
+            const uint32_t dst = ring + st * kOpBytes;
+            const int nload = min(8, nblocks - kt * 8);
+            if (lane == 0) mbar_arrive_expect_tx(bar, nload * kBlkBytes);
+            __syncwarp();
+            if (lane < nload) tma_load_5d(dst + lane * kBlkBytes, map, bar, 0, 0, 0, 0, mine);
         }
-        if (ok) load_v(n_tiles - 1, cur);
     } else if (warp == kMmaWarp) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             auto mma_s = [&](int kt) -> bool {
                 const int s = kt & 1;
-                const int st = kt % kStages;
-                if (!wait(k_full(st), (kt / kStages) & 1)) return false;
+                const int st = kt % kStagesK;
+                if (!wait(k_full(st), (kt / kStagesK) & 1)) return false;
                 // Buffer s held P(kt-2): P(kt-2) V(kt-2) must have consumed it.
                 if (kt >= 2 && !wait(o_done(s), ((kt - 2) >> 1) & 1)) return false;
                 tc_fence_after();
                 const uint32_t kb = sbase + kOffK + st * kOpBytes;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t off = (kk >> 2) * kHalfTile + (kk & 3) * 32;
-                    umma_bf16(tmem + 128 * s, sw128_desc(sbase + kOffQ + off, 16, 1024), sw128_desc(kb + off, 16, 1024),
-                              kIdescQK, kk > 0);
+                for (int kk = 0; kk < 8; ++kk) {  // 16 dims per step: dim half kk / 4, 32 B into the row
+                    const uint32_t qoff = (kk >> 2) * kHalfTile + (kk & 3) * 32;
+                    const uint32_t koff = (kk >> 2) * 1024 + (kk & 3) * 32;
+                    umma_bf16(tmem + 128 * s, sw128_desc(sbase + kOffQ + qoff, 16, 1024),
+                              sw128_desc(kb + koff, 16, 2048), kIdescQK, kk > 0);
                 }
                 umma_commit(s_full(s));
                 umma_commit(k_empty(st));
@@ -274,8 +319,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             auto mma_pv = [&](int kt) -> bool {
                 const int s = kt & 1;
-                const int st = kt % kStages;
-                if (!wait(v_full(st), (kt / kStages) & 1)) return false;
+                const int st = kt % kStagesV;
+                if (!wait(v_full(st), (kt / kStagesV) & 1)) return false;
                 if (!wait(p_full(s), (kt >> 1) & 1)) return false;
                 tc_fence_after();
                 const uint32_t vb = sbase + kOffV + st * kOpBytes;
@@ -283,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int t = 0; t < 8; ++t) {
                     // keys 16t .. 16t+15: half t/4 of buffer s, [head | remainder] columns
                     const uint32_t a_hi = tmem + 128 * s + (t >> 2) * 64 + (t & 3) * 8;
-                    const uint64_t bd = sw128_desc(vb + t * 2048, kHalfTile, 1024);
+                    const uint64_t bd = sw128_desc(vb + t * kBlkBytes, 1024, 2048);
                     umma_bf16_tmem_a(tmem + kTmemO, a_hi, bd, kIdescPV, (kt > 0 || t > 0) ? 1u : 0u);
                     umma_bf16_tmem_a(tmem + kTmemO, a_hi + 32, bd, kIdescPV, 1u);
                 }
@@ -321,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool alive = true;
         for (int kt = 0; kt < n_tiles; ++kt) {
             const int s = kt & 1;
-            alive = alive && __all_sync(0xffffffffu, wait(s_full(s), (kt >> 1) & 1));
+            alive = alive && warp_wait(s_full(s), (kt >> 1) & 1);
             if (!alive) {
                 pair_sync();
                 continue;
@@ -371,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             // Rescaling O needs every earlier P V done (in-order: the latest, P(kt-1) V(kt-1)).
             if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                alive = __all_sync(0xffffffffu, wait(o_done((kt - 1) & 1), ((kt - 1) >> 1) & 1));
+                alive = warp_wait(o_done((kt - 1) & 1), ((kt - 1) >> 1) & 1);
                 if (!alive) continue;
                 tc_fence_after();
 #pragma unroll 1
@@ -398,9 +443,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float pa = fast_exp2(fmaf(__uint_as_float(sr[u][2 * e]), sl2, -mu));
                     const float pb = fast_exp2(fmaf(__uint_as_float(sr[u][2 * e + 1]), sl2, -mu));
                     rsum[e & 3] += pa + pb;
-                    const uint32_t w = pack_bf16x2(pa, pb);
-                    hi[e] = w;
-                    lo[e] = pack_bf16x2(pa - __uint_as_float(w << 16), pb - __uint_as_float(w & 0xffff0000u));
+                    // head: the upper 16 bits of each (bf16 truncation, exact in fp32);
+                    // remainder: P - head >= 0, rounded to nearest bf16 by adding half a unit.
+                    const uint32_t ua = __float_as_uint(pa), ub = __float_as_uint(pb);
+                    hi[e] = __byte_perm(ua, ub, 0x7632);
+                    const float ra = pa - __uint_as_float(ua & 0xffff0000u);
+                    const float rb = pb - __uint_as_float(ub & 0xffff0000u);
+                    lo[e] = __byte_perm(__float_as_uint(ra) + 0x8000u, __float_as_uint(rb) + 0x8000u, 0x7632);
                 }
                 tmem_st_32x32b_x16(t_s + 16 * u, hi);
                 tmem_st_32x32b_x16(t_s + 32 + 16 * u, lo);
@@ -411,13 +460,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Zero V rows of keys no row may see (past the context, or of a bad block).
             const int rv = ctx - kt * 128;  // keys [rv, 128) of the tile are past the context
             if (rv < 128 || bad) {
-                alive = __all_sync(0xffffffffu, wait(v_full(kt % kStages), (kt / kStages) & 1));
+                alive = warp_wait(v_full(kt % kStagesV), (kt / kStagesV) & 1);
                 if (!alive) continue;
-                const uint32_t vb = sbase + kOffV + (kt % kStages) * kOpBytes;
+                const uint32_t vb = sbase + kOffV + (kt % kStagesV) * kOpBytes;
                 for (int idx = hc * 128 + r; idx < 128 * 16; idx += kSoftmaxWarps * 32) {
-                    const int key = idx >> 4, ch = idx & 15;
+                    const int key = idx >> 4, ch = idx & 15;  // (all 16 chunks of a row: swizzle is moot)
                     if (key >= rv || ((bad >> (key >> 4)) & 1u)) {
-                        const uint32_t addr = vb + (ch >> 3) * kHalfTile + key * 128 + (ch & 7) * 16;
+                        const uint32_t addr = vb + (key >> 4) * kBlkBytes + ((key >> 3) & 1) * 2048 + (ch >> 3) * 1024 +
+                                              (key & 7) * 128 + (ch & 7) * 16;
                         asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
                     }
                 }
@@ -433,7 +483,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         pair_sync();  // the last tile's maxima have been read: the exchange area is free
         xl[hc * 128 + r] = l;
         pair_sync();
-        if (alive && __all_sync(0xffffffffu, wait(o_done((n_tiles - 1) & 1), ((n_tiles - 1) >> 1) & 1))) {
+        const bool staged = rows_here == rpt;  // CTA-uniform: a full tile leaves by TMA store
+        if (alive && warp_wait(o_done((n_tiles - 1) & 1), ((n_tiles - 1) >> 1) & 1)) {
             tc_fence_after();
             const float lt = xl[r] + xl[128 + r];
             const float inv = lt > 0.f ? 1.f / lt : 0.f;
@@ -445,8 +496,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t orow[32];
                 tmem_ld_32x32b_x32(t_o + 32 * q, orow);
                 tmem_wait_ld();
-                if (row_valid)
-                    store_row(p.out, p.out_bf16, orow_base + 32 * q, reinterpret_cast<float *>(orow), 32, inv);
+                if (staged)
+                    stage_row(sbase + kOffK, p.out_bf16, r, hc, q, orow, inv);
+                else if (row_valid)
+                    store_row(p.out, p.out_bf16, orow_base + 32 * q, orow, inv);
+            }
+        }
+        if (staged) {
+            // Every softmax warp reaches this barrier on every path (staged is uniform).
+            fence_proxy_async_smem();
+            asm volatile("bar.sync 5, %0;" ::"r"(kSoftmaxWarps * 32) : "memory");
+            if (warp == 0 && lane == 0 && !*abort_flag) {
+                const int nbox = p.out_bf16 ? 2 : 4;
+#pragma unroll 1
+                for (int bx = 0; bx < nbox; ++bx)
+                    tma_store_3d(&omap, sbase + kOffK + bx * kHalfTile, bx * (p.out_bf16 ? 64 : 32), g * G, row0 + i0);
+                bulk_commit_group();
+                bulk_wait_group_read_all();  // shared memory must outlive the reads
             }
         }
     }
@@ -474,9 +540,9 @@ cudaError_t prefill_prepare_device() {
 }
 
 cudaError_t launch_prefill_chunk(const CUtensorMap &qmap, const CUtensorMap &kmap, const CUtensorMap &vmap,
-                                 const PrefillParams &p, int max_q_len, cudaStream_t stream) {
+                                 const CUtensorMap &omap, const PrefillParams &p, int max_q_len, cudaStream_t stream) {
     const dim3 grid(p.n_kv, p.num_seqs, (max_q_len + p.rows_per_tile - 1) / p.rows_per_tile);
-    return launch_pdl(prefill_chunk_kernel, grid, dim3(kThreads), kSmemBytes, stream, qmap, kmap, vmap, p);
+    return launch_pdl(prefill_chunk_kernel, grid, dim3(kThreads), kSmemBytes, stream, qmap, kmap, vmap, omap, p);
 }
 
 }  // namespace pkv

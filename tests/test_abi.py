@@ -130,6 +130,7 @@ def test_prefill_argument_errors(lib):
     assert call(nq=24) == P.PKV_ERR_UNSUPPORTED         # G = 3 does not tile 128 rows
     assert call(mq=-1) == P.PKV_ERR_INVALID_ARG
     assert call(q=FAKE + 4) == P.PKV_ERR_INVALID_ARG    # TMA needs a 16-byte aligned q
+    assert call(out=FAKE + 4) == P.PKV_ERR_INVALID_ARG  # ... and out (full tiles leave by TMA store)
     assert call(wsb=8) == P.PKV_ERR_WORKSPACE_TOO_SMALL
     assert call(ws=None) == P.PKV_ERR_INVALID_ARG
     assert call(mq=0) == P.PKV_OK                        # empty chunk: nothing enqueued
