@@ -310,6 +310,182 @@ def check_lse(lib):
             assert abs(lse[b, h] - math.log(np.sum(np.exp(s)))) <= 1e-10
 
 
+# ---- sliding window ("LLM 推理全过程的维度变化与核心公式", section "KV Cache 的形状与增长":
+# only the most recent W tokens' K and V are kept) ---------------------------------------------
+
+def _contiguous_pool(logical_k, logical_v, n_kv):
+    """Lay sequences' logical K/V out block after block: returns (k_cache, v_cache, tables, lens)."""
+    bs = W.BLOCK_SIZE
+    nblk = [-(-k.shape[0] // bs) for k in logical_k]
+    total = sum(nblk)
+    d = logical_k[0].shape[-1]
+    kc = np.zeros((total, n_kv, bs, d), dtype=np.uint16)
+    vc = np.zeros_like(kc)
+    tables = np.zeros((len(logical_k), max(nblk)), dtype=np.int32)
+    base = 0
+    for b, (K, V) in enumerate(zip(logical_k, logical_v)):
+        for j in range(K.shape[0]):
+            kc[base + j // bs, :, j % bs] = K[j]
+            vc[base + j // bs, :, j % bs] = V[j]
+        tables[b, :nblk[b]] = np.arange(base, base + nblk[b])
+        base += nblk[b]
+    lens = np.array([k.shape[0] for k in logical_k], dtype=np.int32)
+    return kc, vc, tables, lens
+
+
+def check_window_covering_context_changes_nothing(lib):
+    """A window at least as long as every row's visible range is no window at all (bitwise)."""
+    wl, batch = W.make_custom(16, 4, [40, 17, 96], q_lens=[1, 5, 9], seed=21)
+    kc, vc = _appended(wl, lib)
+    base = _attn(wl, batch, kc, vc, lib)
+    for win in (96, 97, 1000):
+        assert np.array_equal(_attn(wl, batch, kc, vc, lib, window=win), base), win
+
+
+def check_window_of_one_returns_newest_v(lib):
+    """W = 1: each row sees only its own position, so its output is that V row exactly."""
+    wl, batch = W.make_custom(16, 4, [40, 17], q_lens=[3, 1], seed=22)
+    kc, vc = _appended(wl, lib)
+    out = _attn(wl, batch, kc, vc, lib, window=1)
+    G = wl.n_q // wl.n_kv
+    for b in range(2):
+        r0, r1 = int(batch.cu_q_lens[b]), int(batch.cu_q_lens[b + 1])
+        ctx = int(batch.context_lens[b])
+        for i, row in enumerate(range(r0, r1)):
+            pos = ctx - (r1 - r0) + i
+            v = W.f32_from_bf16_bits(batch.logical_v[b][pos]).astype(np.float64)
+            assert np.array_equal(out[row], np.repeat(v, G, axis=0)), (b, i)
+
+
+def check_window_equals_truncated_context(lib):
+    """Decode with window W equals plain decode of a sequence holding only its last W tokens."""
+    wl, batch = W.make_custom(32, 8, [100, 33, 16, 300], seed=23)
+    kc, vc = _appended(wl, lib)
+    for win in (1, 15, 16, 17, 64):
+        got = _attn(wl, batch, kc, vc, lib, window=win)
+        lk = [k[max(0, k.shape[0] - win):] for k in batch.logical_k]
+        lv = [v[max(0, v.shape[0] - win):] for v in batch.logical_v]
+        tk, tv, tt, tl = _contiguous_pool(lk, lv, wl.n_kv)
+        ref = oracle.paged_attention(batch.q, batch.cu_q_lens, tk, tv, tt, tl, wl.scale, n_q=wl.n_q, lib=lib)
+        assert np.max(np.abs(got - ref)) <= TOL, win
+
+
+# ---- FP8 (E4M3) KV cache (walkthrough page, section "KV Cache 的形状与增长", INT8 / FP8 KV
+# Cache item: per-token quantisation; vLLM concepts deep dive, section 1: FP8 is 1 byte) --------
+
+# Codes fixed by the E4M3 definition (sign, 4 exponent bits with bias 7, 3 mantissa bits, no
+# infinities): e > 0 -> 2^(e-7) (1 + m/8), e = 0 -> 2^-6 (m/8).
+E4M3_EXACT = [
+    (0.0, 0x00), (2.0 ** -9, 0x01), (7 * 2.0 ** -9, 0x07), (2.0 ** -6, 0x08), (0.5, 0x30),
+    (1.0, 0x38), (1.125, 0x39), (1.75, 0x3E), (2.0, 0x40), (3.0, 0x44), (240.0, 0x77),
+    (256.0, 0x78), (448.0, 0x7E), (-1.0, 0xB8), (-448.0, 0xFE), (-2.0 ** -9, 0x81),
+]
+# Round to nearest, ties to the even code; beyond 448 saturate.
+E4M3_ROUNDED = [
+    (1.0625, 0x38),          # halfway 1 | 1.125  -> even mantissa 0
+    (1.1875, 0x3A),          # halfway 1.125 | 1.25 -> even mantissa 2
+    (1.0626, 0x39),          # just above halfway
+    (2.0 ** -10, 0x00),      # halfway 0 | 2^-9 -> even 0
+    (3 * 2.0 ** -10, 0x02),  # halfway 2^-9 | 2^-8 -> even 2
+    (15 * 2.0 ** -10, 0x08), # halfway 7*2^-9 | 2^-6 -> even (the first normal)
+    (464.0, 0x7E),           # halfway 448 | 480 (480 would be the NaN code) -> saturate
+    (1e6, 0x7E), (-1e6, 0xFE),
+]
+
+
+def check_e4m3_code_table(lib):
+    for v, c in E4M3_EXACT + E4M3_ROUNDED:
+        got = int(oracle.e4m3_encode(np.float32(v), lib=lib))
+        assert got == c, f"encode({v}) = {got:#04x}, want {c:#04x}"
+    for v, c in E4M3_EXACT:
+        assert oracle.e4m3_decode(np.uint8(c), lib=lib) == v, f"decode({c:#04x})"
+    assert math.isnan(float(oracle.e4m3_decode(np.uint8(0x7F), lib=lib)))
+
+
+def check_e4m3_monotone_and_roundtrip(lib):
+    """All 126 positive finite codes decode to increasing values and encode back to themselves."""
+    codes = np.arange(0x00, 0x7F, dtype=np.uint8)
+    vals = oracle.e4m3_decode(codes, lib=lib)
+    assert np.all(np.diff(vals) > 0)
+    assert np.array_equal(oracle.e4m3_encode(vals.astype(np.float32), lib=lib), codes)
+    assert np.array_equal(oracle.e4m3_encode(-vals[1:].astype(np.float32), lib=lib), codes[1:] | 0x80)
+
+
+def check_e4m3_matches_torch(lib):
+    """Inside the finite range the encoder agrees with torch's float8_e4m3fn conversion (RNE)."""
+    import torch
+    rng = np.random.default_rng(24)
+    x = np.concatenate([rng.standard_normal(3000) * 10.0, rng.uniform(-448, 448, 1000),
+                        rng.standard_normal(1000) * 2.0 ** -7]).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.e4m3_encode(x, lib=lib), ref)
+
+
+def _fp8_appended(wl, lib):
+    nb = wl.k_cache.shape[0]
+    kc = np.zeros(wl.k_cache.shape, dtype=np.uint8)
+    vc = np.zeros_like(kc)
+    ks = np.zeros(wl.k_cache.shape[:3], dtype=np.float32)
+    vs = np.zeros_like(ks)
+    return oracle.kv_reshape_and_cache_fp8(wl.new_key, wl.new_value, kc, vc, ks, vs, wl.slot_mapping, lib=lib)
+
+
+def check_fp8_cache_write(lib):
+    """Per (token, head): scale = amax / 448, the largest magnitude codes to +-448, and every
+    value is recovered to half a code step (2^-4 relative for normal codes, 2^-10 scale below)."""
+    wl, batch = W.make_custom(8, 2, [5, 20], seed=25)
+    wl.new_key[0, 1, 7] = _bits([-9.5])[0]  # a negative element carries the row's magnitude
+    kc, vc, ks, vs = _fp8_appended(wl, lib)
+    for t, slot in enumerate(wl.slot_mapping):
+        blk, off = divmod(int(slot), W.BLOCK_SIZE)
+        for h in range(wl.n_kv):
+            for src, codes, sc in ((wl.new_key, kc, ks), (wl.new_value, vc, vs)):
+                x = W.f32_from_bf16_bits(src[t, h]).astype(np.float64)
+                amax = np.max(np.abs(x))
+                assert sc[blk, h, off] == np.float32(np.float32(amax) / np.float32(448.0))
+                row = codes[blk, h, off]
+                k = int(np.argmax(np.abs(x)))
+                assert int(row[k]) & 0x7F == 0x7E and (int(row[k]) >> 7) == int(x[k] < 0), (t, h)
+                deq = oracle.e4m3_decode(row, lib=lib) * float(sc[blk, h, off])
+                bound = np.maximum(np.abs(x) * 2.0 ** -4, float(sc[blk, h, off]) * 2.0 ** -10) * (1 + 1e-6)
+                assert np.all(np.abs(deq - x) <= bound), (t, h)
+
+
+def check_fp8_attention_reduces_to_bf16(lib):
+    """With codes whose scaled values are exactly bf16, the FP8 attention equals the bf16 one."""
+    wl, batch = W.make_custom(16, 4, [23, 64, 5], q_lens=[1, 4, 1], seed=26)
+    rng = np.random.default_rng(27)
+    nb, n_kv, bs, d = wl.k_cache.shape
+    kq = rng.integers(0, 0x7F, size=(nb, n_kv, bs, d), dtype=np.uint8) | (rng.integers(0, 2, (nb, n_kv, bs, d), dtype=np.uint8) << 7)
+    vq = rng.integers(0, 0x7F, size=(nb, n_kv, bs, d), dtype=np.uint8) | (rng.integers(0, 2, (nb, n_kv, bs, d), dtype=np.uint8) << 7)
+    ks = (2.0 ** rng.integers(-6, 1, size=(nb, n_kv, bs))).astype(np.float32)  # powers of two keep values exact
+    vs = (2.0 ** rng.integers(-6, 1, size=(nb, n_kv, bs))).astype(np.float32)
+    kb = _bits(oracle.e4m3_decode(kq, lib=lib) * ks[..., None])
+    vb = _bits(oracle.e4m3_decode(vq, lib=lib) * vs[..., None])
+    f8 = _attn(wl, batch, kq, vq, lib, k_scale=ks, v_scale=vs)
+    b16 = _attn(wl, batch, kb, vb, lib)
+    assert np.array_equal(f8, b16)
+
+
+# ---- block copy at a branch (xinc.fun archive 233, section 6) -------------------------------
+
+def check_copy_blocks(lib):
+    rng = np.random.default_rng(28)
+    cache = rng.integers(0, 2 ** 16, size=(12, 2, 16, 128), dtype=np.uint16)
+    pairs = [(3, 7), (0, 11), (5, 2)]
+    got = oracle.copy_blocks(cache, pairs, lib=lib)
+    ref = cache.copy()
+    for s_, d_ in pairs:
+        ref[d_] = ref[s_]
+    assert np.array_equal(got, ref)
+    scales = rng.standard_normal((12, 2, 16)).astype(np.float32)
+    got = oracle.copy_blocks(scales, pairs, lib=lib)
+    ref = scales.copy()
+    for s_, d_ in pairs:
+        ref[d_] = ref[s_]
+    assert np.array_equal(got, ref)
+
+
 ALL_CHECKS = [
     check_kv_sizes, check_kv_groups, check_slot_rule,
     check_cache_write_roundtrip, check_cache_write_skips_padding,
@@ -320,4 +496,9 @@ ALL_CHECKS = [
     check_repeat_interleave_equivalence, check_block_permutation_invariance,
     check_shared_prefix_invariance, check_chunk_last_row_equals_decode, check_chunk_split_invariance,
     check_split_merge_identity, check_lse,
+    check_window_covering_context_changes_nothing, check_window_of_one_returns_newest_v,
+    check_window_equals_truncated_context,
+    check_e4m3_code_table, check_e4m3_monotone_and_roundtrip, check_e4m3_matches_torch,
+    check_fp8_cache_write, check_fp8_attention_reduces_to_bf16,
+    check_copy_blocks,
 ]
