@@ -75,8 +75,9 @@ extern "C" {
 
 /* Element types. */
 typedef enum pkv_dtype {
-    PKV_DTYPE_BF16 = 0,    /* bfloat16 */
-    PKV_DTYPE_FLOAT32 = 1  /* IEEE binary32 */
+    PKV_DTYPE_BF16 = 0,     /* bfloat16 */
+    PKV_DTYPE_FLOAT32 = 1,  /* IEEE binary32 */
+    PKV_DTYPE_FP8_E4M3 = 2  /* 8-bit float: 1 sign, 4 exponent (bias 7), 3 mantissa bits, max 448 */
 } pkv_dtype;
 
 /* Description of the physical block pool shared by K and V. */
@@ -85,7 +86,8 @@ typedef struct pkv_cache_desc {
     int32_t block_size;    /* tokens per block; must be 16 */
     int32_t num_kv_heads;  /* KV heads n_kv (>= 1) */
     int32_t head_dim;      /* per-head dimension; must be 128 */
-    int32_t dtype;         /* pkv_dtype of K/V; must be PKV_DTYPE_BF16 */
+    int32_t dtype;         /* pkv_dtype of K/V: PKV_DTYPE_BF16, or PKV_DTYPE_FP8_E4M3 for the
+                              *_fp8 entry points and kv_copy_blocks */
 } pkv_cache_desc;
 
 /* Return codes. */
@@ -94,6 +96,7 @@ typedef struct pkv_cache_desc {
 #define PKV_ERR_UNSUPPORTED (-2)         /* head_dim, block_size, dtype or group size not supported */
 #define PKV_ERR_WORKSPACE_TOO_SMALL (-3) /* workspace_bytes below the *_workspace_size() answer */
 #define PKV_ERR_CUDA (-4)                /* a CUDA runtime call or launch failed */
+#define PKV_ERR_OUT_OF_BLOCKS (-5)       /* block manager: not enough free blocks (nothing changed) */
 
 /* Bits ORed into the device status word (workspace byte 0). */
 #define PKV_STATUS_BAD_CONTEXT_LEN 0x1u /* context_len < 1 or > max_blocks_per_seq * block_size */
@@ -124,6 +127,28 @@ typedef struct pkv_cache_desc {
 PKV_API int kv_reshape_and_cache(const void *key, const void *value, void *k_cache, void *v_cache,
                          const int32_t *slot_mapping, int32_t num_tokens,
                          const pkv_cache_desc *cache, void *stream);
+
+/*
+ * kv_copy_blocks -- copy whole physical blocks (the copy at a branch point).
+ *
+ * Sequences that share a prefix, or parallel candidates, reference the same
+ * physical blocks until they branch; there the branch gets a new block
+ * (xinc.fun archive 233, section 6).  The host block manager (pkv_bm_append)
+ * reports such (source, destination) pairs; this call performs them:
+ *     for i < num_pairs: block block_pairs[2i+1] := block block_pairs[2i]
+ * in k_cache and v_cache (every head and slot), and for an FP8 cache also in
+ * k_scale and v_scale (fp32 [num_blocks][num_kv_heads][block_size]).
+ *
+ *   block_pairs : int32 [num_pairs][2] = {source, destination}, DEVICE memory
+ *   k_scale, v_scale : NULL for a bf16 cache; required when cache->dtype is
+ *                      PKV_DTYPE_FP8_E4M3 (16-byte aligned)
+ * The copies run concurrently: destinations must be distinct and must not be
+ * sources of the same call.  A pair with an id outside [0, num_blocks) is
+ * skipped.  Bit-exact.
+ * Errors: PKV_ERR_INVALID_ARG / PKV_ERR_UNSUPPORTED / PKV_ERR_CUDA.
+ */
+PKV_API int kv_copy_blocks(void *k_cache, void *v_cache, float *k_scale, float *v_scale, const int32_t *block_pairs,
+                           int32_t num_pairs, const pkv_cache_desc *cache, void *stream);
 
 /*
  * paged_attention_workspace_size -- bytes of device workspace that
@@ -274,6 +299,83 @@ PKV_API int paged_attention_prefill_chunk(void *out, int32_t out_dtype, const vo
                                   const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
                                   int32_t max_blocks_per_seq, float scale, const pkv_cache_desc *cache,
                                   void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * ---- Host block manager ---------------------------------------------------------
+ * Hands out the pool's physical blocks to sequences and emits the block tables
+ * and slot mappings the kernels above consume.  Sources: "注意力演进与推理流程",
+ * 变革 1 (the cache is cut into fixed-size blocks of e.g. 16 tokens and a block
+ * is allocated on demand as a sequence grows) and 变革 3 (prefix caching: a
+ * repeated prefix hits cached KV and skips its prefill); xinc.fun archive 233,
+ * section 6 (sequences sharing a prefix, or parallel candidates, reference the
+ * same physical blocks until they branch, where a new block is allocated).
+ *
+ * Model: every block has a reference count (sequences whose table holds it).
+ * A sequence is a list of blocks plus a length in tokens.  Appending never
+ * writes into a block that another sequence also references: if a sequence's
+ * partially filled last block is shared, the append first moves the sequence
+ * to a fresh block and reports a (source, destination) pair that the caller
+ * must copy on the device (kv_copy_blocks) before the tokens are written.
+ * Full blocks can be published under a hash of all token ids up to their end;
+ * a new sequence whose prompt starts with published blocks takes them over
+ * (reference +1).  A block whose count drops to 0 becomes free; a published
+ * free block stays findable until the allocator reuses it (unpublished free
+ * blocks are reused first, published ones oldest first).
+ *
+ * Host memory only; needs no GPU.  Not thread-safe: one thread owns a manager.
+ * Sequence ids are the caller's 64-bit keys.  Every call either succeeds or
+ * returns an error with the manager unchanged.
+ */
+typedef struct pkv_block_manager pkv_block_manager;
+
+/* A manager for blocks 0 .. num_blocks-1 (all free).  *out receives it. */
+PKV_API int pkv_bm_create(int32_t num_blocks, pkv_block_manager **out);
+PKV_API void pkv_bm_destroy(pkv_block_manager *bm);
+/* Free blocks (including published ones that no sequence holds). */
+PKV_API int32_t pkv_bm_num_free(const pkv_block_manager *bm);
+/* Reference count of one block (0 when free). */
+PKV_API int pkv_bm_ref_count(const pkv_block_manager *bm, int32_t block, int32_t *count);
+
+/* A new, empty sequence.  PKV_ERR_INVALID_ARG if the id is taken. */
+PKV_API int pkv_bm_add_sequence(pkv_block_manager *bm, int64_t seq_id);
+/* child_id starts as a copy of parent_id's table and length, sharing every block. */
+PKV_API int pkv_bm_fork(pkv_block_manager *bm, int64_t parent_id, int64_t child_id);
+/*
+ * Reserve slots for num_tokens new tokens at positions length .. length+num_tokens-1:
+ * slot_mapping[t] = table[p / 16] * 16 + p % 16 (host array of num_tokens).
+ * New blocks are allocated as positions cross a block boundary.  copy_pair
+ * (host int32[2]) receives {source, destination} and *num_copies is 1 when
+ * the shared last block had to be replaced first (0 otherwise).
+ * PKV_ERR_OUT_OF_BLOCKS if the free blocks do not suffice.
+ */
+PKV_API int pkv_bm_append(pkv_block_manager *bm, int64_t seq_id, int32_t num_tokens, int32_t *slot_mapping,
+                          int32_t *copy_pair, int32_t *num_copies);
+/* Drop a sequence: every block's count decreases; blocks reaching 0 become free. */
+PKV_API int pkv_bm_free_sequence(pkv_block_manager *bm, int64_t seq_id);
+PKV_API int pkv_bm_sequence_length(const pkv_block_manager *bm, int64_t seq_id, int64_t *length);
+/*
+ * Emit the block-table rows and context lengths of num_seqs sequences (host
+ * arrays): block_tables [num_seqs][max_blocks_per_seq], entries past a
+ * sequence's blocks set to pad_block.  PKV_ERR_INVALID_ARG if a sequence
+ * needs more than max_blocks_per_seq blocks (nothing written).
+ */
+PKV_API int pkv_bm_block_tables(const pkv_block_manager *bm, const int64_t *seq_ids, int32_t num_seqs,
+                                int32_t max_blocks_per_seq, int32_t pad_block, int32_t *block_tables,
+                                int32_t *context_lens);
+/*
+ * Prefix caching.  pkv_bm_publish: tokens[0 .. num_tokens) are the token ids
+ * at positions 0.. of seq_id (num_tokens <= its length); every full block
+ * among them is published under a hash of tokens[0 .. end of block) unless
+ * that prefix is already published.  pkv_bm_add_sequence_cached: a new
+ * sequence whose prompt is tokens[0 .. num_tokens); it takes over the
+ * longest run of published leading blocks, leaving at least one prompt token
+ * to compute, and *num_cached_tokens = 16 x blocks taken (its length).
+ * Matches compare the stored token ids, so a hash collision never shares a
+ * block.
+ */
+PKV_API int pkv_bm_publish(pkv_block_manager *bm, int64_t seq_id, const int32_t *tokens, int32_t num_tokens);
+PKV_API int pkv_bm_add_sequence_cached(pkv_block_manager *bm, int64_t seq_id, const int32_t *tokens,
+                                       int32_t num_tokens, int32_t *num_cached_tokens);
 
 /* Human-readable name of a return code (static string, never NULL). */
 PKV_API const char *pagedkv_status_string(int status);

@@ -9,13 +9,16 @@ from .pagedkv import (  # noqa: F401
     HEAD_DIM,
     PKV_DTYPE_BF16,
     PKV_DTYPE_FLOAT32,
+    PKV_DTYPE_FP8_E4M3,
     PKV_STATUS_BAD_BLOCK_ID,
     PKV_STATUS_BAD_CONTEXT_LEN,
     PKV_STATUS_BAD_Q_LEN,
     PKV_STATUS_TIMEOUT,
+    BlockManager,
     CacheDesc,
     PagedKVError,
     cache_desc,
+    kv_copy_blocks,
     kv_reshape_and_cache,
     load_library,
     paged_attention_decode,

@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG_DIR)
 CSRC = os.path.join(PKG_DIR, "csrc")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libpagedkv.so")
-SOURCES = ["api.cu", "cache_write.cu", "decode.cu", "prefill.cu"]
+SOURCES = ["api.cu", "cache_write.cu", "decode.cu", "prefill.cu", "block_manager.cpp"]
 HEADERS = ["launch.h", "ptx.cuh", "decode_core.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -49,7 +49,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     exe = nvcc()
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        o = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
         objs.append(o)
         if force or _stale(o, [s, *hdrs]):
             jobs.append([exe, *_flags(extra_flags), "-c", s, "-o", o])

@@ -232,6 +232,7 @@ const char *pagedkv_status_string(int status) {
     case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED: unsupported shape or type";
     case PKV_ERR_WORKSPACE_TOO_SMALL: return "PKV_ERR_WORKSPACE_TOO_SMALL: workspace too small";
     case PKV_ERR_CUDA: return "PKV_ERR_CUDA: CUDA runtime error";
+    case PKV_ERR_OUT_OF_BLOCKS: return "PKV_ERR_OUT_OF_BLOCKS: not enough free blocks";
     default: return "unknown pagedkv status";
     }
 }
@@ -251,6 +252,25 @@ int kv_reshape_and_cache(const void *key, const void *value, void *k_cache, void
     const cudaError_t e =
         pkv::launch_kv_cache_write(key, value, k_cache, v_cache, slot_mapping, num_tokens, cache->num_kv_heads,
                                    cache->num_blocks, sm_count(dev), static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+int kv_copy_blocks(void *k_cache, void *v_cache, float *k_scale, float *v_scale, const int32_t *block_pairs,
+                   int32_t num_pairs, const pkv_cache_desc *cache, void *stream) {
+    if (!cache || cache->num_blocks < 1 || cache->num_kv_heads < 1) return PKV_ERR_INVALID_ARG;
+    if (cache->block_size != kBlockSize || cache->head_dim != kHeadDim) return PKV_ERR_UNSUPPORTED;
+    const bool fp8 = cache->dtype == PKV_DTYPE_FP8_E4M3;
+    if (!fp8 && cache->dtype != PKV_DTYPE_BF16) return PKV_ERR_UNSUPPORTED;
+    if (num_pairs < 0 || num_pairs > 65535) return PKV_ERR_INVALID_ARG;  // one CTA column per pair
+    if (num_pairs == 0) return PKV_OK;
+    if (!k_cache || !v_cache || !block_pairs || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(block_pairs, 4))
+        return PKV_ERR_INVALID_ARG;
+    if (fp8 ? (!k_scale || !v_scale || !aligned(k_scale, 16) || !aligned(v_scale, 16)) : (k_scale || v_scale))
+        return PKV_ERR_INVALID_ARG;
+    const cudaError_t e = pkv::launch_kv_copy_blocks(k_cache, v_cache, k_scale, v_scale, block_pairs, num_pairs,
+                                                     cache->num_kv_heads, fp8 ? 1 : 2, cache->num_blocks,
+                                                     static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

@@ -44,7 +44,36 @@ kv_cache_write_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ v
     }
 }
 
+// Block copy at a branch point: CTA (i, c) copies block pairs[2i] onto block
+// pairs[2i+1] of cache c (0: K, 1: V), the block's codes then (FP8) its scales,
+// in coalesced 16-byte vectors.  Ids outside [0, num_blocks) skip the pair.
+__global__ void __launch_bounds__(256)
+kv_copy_blocks_kernel(uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache, uint4 *__restrict__ k_scale,
+                      uint4 *__restrict__ v_scale, const int32_t *__restrict__ pairs, int64_t block_vec,
+                      int64_t scale_vec, int32_t num_blocks) {
+    griddep_launch_dependents();
+    griddep_wait();  // kernels before us may still read or write the pool
+    const int64_t src = __ldg(pairs + 2 * blockIdx.x), dst = __ldg(pairs + 2 * blockIdx.x + 1);
+    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) return;
+    uint4 *data = blockIdx.y == 0 ? k_cache : v_cache;
+    for (int64_t i = threadIdx.x; i < block_vec; i += blockDim.x) data[dst * block_vec + i] = data[src * block_vec + i];
+    uint4 *sc = blockIdx.y == 0 ? k_scale : v_scale;
+    if (sc)
+        for (int64_t i = threadIdx.x; i < scale_vec; i += blockDim.x) sc[dst * scale_vec + i] = sc[src * scale_vec + i];
+}
+
 }  // namespace
+
+cudaError_t launch_kv_copy_blocks(void *k_cache, void *v_cache, float *k_scale, float *v_scale, const int32_t *pairs,
+                                  int32_t num_pairs, int32_t n_kv, int32_t elem_bytes, int32_t num_blocks,
+                                  cudaStream_t stream) {
+    if (num_pairs == 0) return cudaSuccess;
+    const int64_t block_vec = static_cast<int64_t>(n_kv) * kBlockSize * kHeadDim * elem_bytes / 16;
+    const int64_t scale_vec = static_cast<int64_t>(n_kv) * kBlockSize * 4 / 16;  // fp32 per (slot, head)
+    return launch_pdl(kv_copy_blocks_kernel, dim3(static_cast<unsigned>(num_pairs), 2), dim3(256), 0, stream,
+                      static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), reinterpret_cast<uint4 *>(k_scale),
+                      reinterpret_cast<uint4 *>(v_scale), pairs, block_vec, scale_vec, num_blocks);
+}
 
 cudaError_t launch_kv_cache_write(const void *key, const void *value, void *k_cache, void *v_cache,
                                   const int32_t *slot_mapping, int32_t num_tokens, int32_t n_kv,

@@ -36,6 +36,9 @@ constexpr uint32_t kStatusBadQLen = 0x4u;
 constexpr uint32_t kStatusTimeout = 0x8u;
 
 // ---- K1: cache write ----------------------------------------------------------
+cudaError_t launch_kv_copy_blocks(void *k_cache, void *v_cache, float *k_scale, float *v_scale, const int32_t *pairs,
+                                  int32_t num_pairs, int32_t n_kv, int32_t elem_bytes, int32_t num_blocks,
+                                  cudaStream_t stream);
 cudaError_t launch_kv_cache_write(const void *key, const void *value, void *k_cache, void *v_cache,
                                   const int32_t *slot_mapping, int32_t num_tokens, int32_t n_kv,
                                   int32_t num_blocks, int sm_count, cudaStream_t stream);

@@ -17,12 +17,14 @@ from typing import Optional
 
 PKV_DTYPE_BF16 = 0
 PKV_DTYPE_FLOAT32 = 1
+PKV_DTYPE_FP8_E4M3 = 2
 
 PKV_OK = 0
 PKV_ERR_INVALID_ARG = -1
 PKV_ERR_UNSUPPORTED = -2
 PKV_ERR_WORKSPACE_TOO_SMALL = -3
 PKV_ERR_CUDA = -4
+PKV_ERR_OUT_OF_BLOCKS = -5
 
 PKV_STATUS_BAD_CONTEXT_LEN = 0x1
 PKV_STATUS_BAD_BLOCK_ID = 0x2
@@ -82,6 +84,33 @@ def _declare(lib):
     lib.paged_attention_prefill_chunk.restype = ctypes.c_int
     lib.paged_attention_decode_static_scratch.argtypes = [P, i32, P, P, P, P, P, i32, i32, i32, f32, i32, D, P, P]
     lib.paged_attention_decode_static_scratch.restype = ctypes.c_int
+    lib.kv_copy_blocks.argtypes = [P, P, P, P, P, i32, D, P]
+    lib.kv_copy_blocks.restype = ctypes.c_int
+    i64, I = ctypes.c_int64, ctypes.c_int
+    lib.pkv_bm_create.argtypes = [i32, ctypes.POINTER(P)]
+    lib.pkv_bm_create.restype = I
+    lib.pkv_bm_destroy.argtypes = [P]
+    lib.pkv_bm_destroy.restype = None
+    lib.pkv_bm_num_free.argtypes = [P]
+    lib.pkv_bm_num_free.restype = i32
+    lib.pkv_bm_ref_count.argtypes = [P, i32, P]
+    lib.pkv_bm_ref_count.restype = I
+    lib.pkv_bm_add_sequence.argtypes = [P, i64]
+    lib.pkv_bm_add_sequence.restype = I
+    lib.pkv_bm_fork.argtypes = [P, i64, i64]
+    lib.pkv_bm_fork.restype = I
+    lib.pkv_bm_append.argtypes = [P, i64, i32, P, P, P]
+    lib.pkv_bm_append.restype = I
+    lib.pkv_bm_free_sequence.argtypes = [P, i64]
+    lib.pkv_bm_free_sequence.restype = I
+    lib.pkv_bm_sequence_length.argtypes = [P, i64, P]
+    lib.pkv_bm_sequence_length.restype = I
+    lib.pkv_bm_block_tables.argtypes = [P, P, i32, i32, i32, P, P]
+    lib.pkv_bm_block_tables.restype = I
+    lib.pkv_bm_publish.argtypes = [P, i64, P, i32]
+    lib.pkv_bm_publish.restype = I
+    lib.pkv_bm_add_sequence_cached.argtypes = [P, i64, P, i32, P]
+    lib.pkv_bm_add_sequence_cached.restype = I
     lib.pagedkv_status_string.argtypes = [ctypes.c_int]
     lib.pagedkv_status_string.restype = ctypes.c_char_p
     lib.pagedkv_version.argtypes = []
@@ -136,11 +165,13 @@ def _check(t, name, dtype, ndim=None, last=None):
 
 
 def cache_desc(k_cache) -> CacheDesc:
-    """Descriptor of a pool tensor [num_blocks, n_kv, 16, 128] (bf16)."""
+    """Descriptor of a pool tensor [num_blocks, n_kv, 16, 128]: bf16, or FP8 E4M3 codes
+    (torch.float8_e4m3fn or uint8)."""
     torch = _torch()
-    _check(k_cache, "k_cache", torch.bfloat16, ndim=4, last=HEAD_DIM)
+    fp8 = k_cache.dtype in (torch.uint8, torch.float8_e4m3fn)
+    _check(k_cache, "k_cache", k_cache.dtype if fp8 else torch.bfloat16, ndim=4, last=HEAD_DIM)
     nb, n_kv, bs, d = k_cache.shape
-    return CacheDesc(int(nb), int(bs), int(n_kv), int(d), PKV_DTYPE_BF16)
+    return CacheDesc(int(nb), int(bs), int(n_kv), int(d), PKV_DTYPE_FP8_E4M3 if fp8 else PKV_DTYPE_BF16)
 
 
 def _out_dtype(out) -> int:
@@ -173,6 +204,112 @@ def kv_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, stream=None
     rc = load_library().kv_reshape_and_cache(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache),
                                              _ptr(slot_mapping), int(T), ctypes.byref(desc), _stream(stream))
     _raise("kv_reshape_and_cache", rc)
+
+
+def kv_copy_blocks(k_cache, v_cache, block_pairs, k_scale=None, v_scale=None, stream=None) -> None:
+    """Copy block pairs {source, destination} (int32 CUDA tensor [n, 2]) in both caches
+    (and, for an FP8 cache, in both scale arrays)."""
+    torch = _torch()
+    desc = cache_desc(k_cache)
+    _check(v_cache, "v_cache", k_cache.dtype, ndim=4)
+    _need(tuple(v_cache.shape) == tuple(k_cache.shape), "v_cache shape must equal k_cache shape")
+    _check(block_pairs, "block_pairs", torch.int32, ndim=2, last=2)
+    fp8 = desc.dtype == PKV_DTYPE_FP8_E4M3
+    _need(fp8 == (k_scale is not None) and fp8 == (v_scale is not None),
+          "k_scale and v_scale are required for an FP8 cache and not allowed otherwise")
+    if fp8:
+        for name, t in (("k_scale", k_scale), ("v_scale", v_scale)):
+            _check(t, name, torch.float32, ndim=3)
+            _need(tuple(t.shape) == tuple(k_cache.shape[:3]), f"{name} must be [num_blocks, n_kv, 16]")
+    rc = load_library().kv_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(k_scale) if fp8 else None,
+                                       _ptr(v_scale) if fp8 else None, _ptr(block_pairs),
+                                       int(block_pairs.shape[0]), ctypes.byref(desc), _stream(stream))
+    _raise("kv_copy_blocks", rc)
+
+
+class BlockManager:
+    """Host block manager of the paged pool (``pkv_bm_*`` in include/pagedkv.h).
+
+    Sequences are keyed by caller-chosen integers.  ``append`` returns the slot
+    mapping of the new tokens and, when the sequence's shared last block had to
+    be replaced first, the (source, destination) block pair to copy on the
+    device with :func:`kv_copy_blocks` before writing the tokens.
+    """
+
+    def __init__(self, num_blocks: int):
+        self._lib = load_library()
+        h = ctypes.c_void_p()
+        _raise("pkv_bm_create", self._lib.pkv_bm_create(int(num_blocks), ctypes.byref(h)))
+        self._h = h
+        self.num_blocks = int(num_blocks)
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self._lib.pkv_bm_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        self.close()
+
+    @property
+    def num_free(self) -> int:
+        return int(self._lib.pkv_bm_num_free(self._h))
+
+    def ref_count(self, block: int) -> int:
+        c = ctypes.c_int32()
+        _raise("pkv_bm_ref_count", self._lib.pkv_bm_ref_count(self._h, int(block), ctypes.byref(c)))
+        return c.value
+
+    def add(self, seq_id: int) -> None:
+        _raise("pkv_bm_add_sequence", self._lib.pkv_bm_add_sequence(self._h, int(seq_id)))
+
+    def fork(self, parent_id: int, child_id: int) -> None:
+        _raise("pkv_bm_fork", self._lib.pkv_bm_fork(self._h, int(parent_id), int(child_id)))
+
+    def append(self, seq_id: int, num_tokens: int):
+        """Returns (slot_mapping int32 numpy [num_tokens], copy pair (src, dst) or None)."""
+        import numpy as np
+        slots = np.zeros(max(int(num_tokens), 1), dtype=np.int32)
+        pair = np.zeros(2, dtype=np.int32)
+        n = ctypes.c_int32()
+        rc = self._lib.pkv_bm_append(self._h, int(seq_id), int(num_tokens), slots.ctypes.data,
+                                     pair.ctypes.data, ctypes.byref(n))
+        _raise("pkv_bm_append", rc)
+        return slots[:int(num_tokens)], ((int(pair[0]), int(pair[1])) if n.value else None)
+
+    def free(self, seq_id: int) -> None:
+        _raise("pkv_bm_free_sequence", self._lib.pkv_bm_free_sequence(self._h, int(seq_id)))
+
+    def length(self, seq_id: int) -> int:
+        n = ctypes.c_int64()
+        _raise("pkv_bm_sequence_length", self._lib.pkv_bm_sequence_length(self._h, int(seq_id), ctypes.byref(n)))
+        return n.value
+
+    def block_tables(self, seq_ids, max_blocks_per_seq: int, pad_block: int = 0):
+        """Returns (block_tables int32 [B, max_blocks], context_lens int32 [B]) as numpy arrays."""
+        import numpy as np
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        tables = np.zeros((max(len(ids), 1), int(max_blocks_per_seq)), dtype=np.int32)
+        lens = np.zeros(max(len(ids), 1), dtype=np.int32)
+        rc = self._lib.pkv_bm_block_tables(self._h, ids.ctypes.data, int(len(ids)), int(max_blocks_per_seq),
+                                           int(pad_block), tables.ctypes.data, lens.ctypes.data)
+        _raise("pkv_bm_block_tables", rc)
+        return tables[:len(ids)], lens[:len(ids)]
+
+    def publish(self, seq_id: int, tokens) -> None:
+        import numpy as np
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        _raise("pkv_bm_publish", self._lib.pkv_bm_publish(self._h, int(seq_id), t.ctypes.data, int(t.shape[0])))
+
+    def add_cached(self, seq_id: int, tokens) -> int:
+        """New sequence for prompt `tokens`; returns how many leading tokens are already cached."""
+        import numpy as np
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        n = ctypes.c_int32()
+        rc = self._lib.pkv_bm_add_sequence_cached(self._h, int(seq_id), t.ctypes.data, int(t.shape[0]),
+                                                  ctypes.byref(n))
+        _raise("pkv_bm_add_sequence_cached", rc)
+        return n.value
 
 
 def paged_attention_workspace_size(num_seqs: int, num_q_heads: int, max_blocks_per_seq: int,
