@@ -333,6 +333,10 @@ def run_ours(args):
     # kv_cache_write + (prefill chunk) + paged decode + split-KV merge (when a context is split)
     launches_per_step = 2 + (1 if chunk is not None else 0) + (1 if ws_bytes > 256 else 0)
 
+    # the next hot-path rows on the same batch (single-GPU runs; outside the timed region)
+    rows = _row_variants(P, torch, dev, wl, batch, k_cache, v_cache, new_k, new_v, slots, q, tables, lens,
+                         decode_ms, kv_bytes, steps=min(args.steps, 200)) if world == 1 else None
+
     if rank == 0:
         peak, peak_src = measured_peaks()
         achieved = kv_bytes / (decode_ms / 1e3) / 1e9
@@ -369,12 +373,92 @@ def run_ours(args):
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": bi,
                     "d2h_bytes_per_step": bo, "ms_per_step": round(e2e_t / args.steps * 1e3, 5)},
             "prefill": None if chunk is None else _prefill_report(chunk_flops, prefill_ms, chunk, wl),
+            "rows": rows,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks.summary(),
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def _time_events(torch, stream, fn, steps, warmup=3):
+    """Mean ms of fn() over `steps` calls, CUDA events on `stream` around each call."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in ev:
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+
+def _row_variants(P, torch, dev, wl, batch, k_cache, v_cache, new_k, new_v, slots, q, tables, lens, decode_ms,
+                  kv_bytes, steps):
+    """FP8 cache, sliding window and host block manager on the bench batch."""
+    peak, _ = measured_peaks()
+    stream = torch.cuda.current_stream(dev)
+    B = batch.num_seqs
+    ctx = batch.context_lens.astype(np.int64)
+    res = {}
+
+    # FP8 (E4M3) pool: the bf16 pool quantised slot by slot by the library's own FP8 append
+    nb, n_kv, bs, d = k_cache.shape
+    k8 = torch.empty((nb, n_kv, bs, d), dtype=torch.uint8, device=dev)
+    v8 = torch.empty_like(k8)
+    ks = torch.empty((nb, n_kv, bs), dtype=torch.float32, device=dev)
+    vs = torch.empty_like(ks)
+    all_slots = torch.arange(nb * bs, dtype=torch.int32, device=dev)
+    P.kv_reshape_and_cache_fp8(k_cache.permute(0, 2, 1, 3).reshape(nb * bs, n_kv, d).contiguous(),
+                               v_cache.permute(0, 2, 1, 3).reshape(nb * bs, n_kv, d).contiguous(), k8, v8, ks, vs,
+                               all_slots)
+    out = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+    desc8 = P.cache_desc(k8)
+    ws8 = torch.zeros(P.paged_attention_workspace_size(B, wl.n_q, batch.max_blocks_per_seq, 0, desc8),
+                      dtype=torch.uint8, device=dev)
+    ms8 = _time_events(torch, stream, lambda: P.paged_attention_decode(out, q, k8, v8, tables, lens, wl.scale,
+                                                                       workspace=ws8, k_scale=ks, v_scale=vs), steps)
+    ms8_app = _time_events(torch, stream, lambda: P.kv_reshape_and_cache_fp8(new_k, new_v, k8, v8, ks, vs, slots),
+                           steps)
+    b8 = int(ctx.sum()) * n_kv * (2 * d + 2 * 4)  # codes of K and V plus their two fp32 scales
+    res["fp8_decode"] = {
+        "cache": "E4M3 codes + fp32 scale per token and KV head", "bytes_per_launch": b8,
+        "avg_launch_ms": round(ms8, 5), "gbs": round(b8 / ms8 / 1e6, 2), "frac_of_hbm": round(b8 / ms8 / 1e6 / peak, 4),
+        "sequences_per_s": round(B / ms8 * 1e3, 1), "speedup_vs_bf16_decode": round(decode_ms / ms8, 3),
+        "append_avg_ms": round(ms8_app, 5)}
+
+    # sliding window of 1024 tokens: only the visible keys' blocks are read
+    win = 1024
+    wsw = torch.zeros(P.paged_attention_workspace_size(B, wl.n_q, batch.max_blocks_per_seq, 0, P.cache_desc(k_cache)),
+                      dtype=torch.uint8, device=dev)
+    msw = _time_events(torch, stream, lambda: P.paged_attention_decode(out, q, k_cache, v_cache, tables, lens,
+                                                                       wl.scale, workspace=wsw, window=win), steps)
+    bw = int(np.minimum(ctx, win).sum()) * n_kv * 2 * d * 2
+    res["window_decode"] = {"window": win, "bytes_per_launch": bw, "avg_launch_ms": round(msw, 5),
+                            "gbs": round(bw / msw / 1e6, 2), "frac_of_hbm": round(bw / msw / 1e6 / peak, 4),
+                            "sequences_per_s": round(B / msw * 1e3, 1)}
+
+    # host block manager: one decode step of this batch = one appended token per sequence + table emission
+    reps = 200
+    bm = P.BlockManager(nb + B * (reps // 16 + 2))
+    for i, c in enumerate(ctx):
+        bm.add(i)
+        bm.append(i, int(c))
+    ids = np.arange(B, dtype=np.int64)
+    width = batch.max_blocks_per_seq + reps // 16 + 2
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        for i in range(B):
+            bm.append(i, 1)
+        bm.block_tables(ids, width)
+    host_us = (time.perf_counter() - t0) / reps * 1e6
+    res["block_manager"] = {"sequences": B, "us_per_step": round(host_us, 2),
+                            "note": "host C++ via ctypes: B appends of one token + block-table emission"}
+    bm.close()
+    return res
 
 
 def _chunk_flops(chunk, wl) -> int:

@@ -129,6 +129,32 @@ PKV_API int kv_reshape_and_cache(const void *key, const void *value, void *k_cac
                          const pkv_cache_desc *cache, void *stream);
 
 /*
+ * kv_reshape_and_cache_fp8 -- append new tokens' K and V to an FP8 (E4M3) pool.
+ *
+ * INT8 / FP8 KV caches quantise the cache per channel or per token, halving it
+ * or more ("LLM 推理全过程的维度变化与核心公式", section "KV Cache 的形状与增长";
+ * the error depends on the group size and the scaling: xinc.fun archive 233,
+ * section 7).  Here: per token and KV head, one fp32 scale for its 128 values.
+ * For each token t < num_tokens and KV head h, with x = key[t][h][:] (and the
+ * same for value), slot = slot_mapping[t] (negative: skipped):
+ *     a     = max(max_k |x_k|, 2^-100)
+ *     code  = E4M3(x_k * (448 / a))   nearest even, saturating at +-448
+ *     scale = a / 448
+ *     k_cache[block][h][off][k] = code_k;  k_scale[block][h][off] = scale
+ * Each step is one correctly rounded fp32 operation, so the codes are exactly
+ * reproducible; x_k is recovered as E4M3 value(code_k) * scale.
+ *
+ *   key, value       : bf16 [num_tokens][num_kv_heads][head_dim], device, 16-B aligned
+ *   k_cache, v_cache : uint8 E4M3 codes [num_blocks][num_kv_heads][16][128], device
+ *   k_scale, v_scale : fp32 [num_blocks][num_kv_heads][16], device, 16-B aligned
+ *   cache->dtype     : PKV_DTYPE_FP8_E4M3
+ * Errors: as kv_reshape_and_cache.
+ */
+PKV_API int kv_reshape_and_cache_fp8(const void *key, const void *value, void *k_cache, void *v_cache, float *k_scale,
+                                     float *v_scale, const int32_t *slot_mapping, int32_t num_tokens,
+                                     const pkv_cache_desc *cache, void *stream);
+
+/*
  * kv_copy_blocks -- copy whole physical blocks (the copy at a branch point).
  *
  * Sequences that share a prefix, or parallel candidates, reference the same
@@ -258,6 +284,51 @@ PKV_API int paged_attention_decode_static_scratch(void *out, int32_t out_dtype, 
                                                   int32_t num_q_heads, int32_t max_blocks_per_seq, float scale,
                                                   int32_t partition_size, const pkv_cache_desc *cache,
                                                   uint32_t *status, void *stream);
+
+/*
+ * paged_attention_decode_window -- decode attention under a sliding window.
+ *
+ * As paged_attention_decode, except that sequence b's row sees only its newest
+ * `window` keys, j >= max(0, ctx_b - window): Sliding Window Attention keeps
+ * only the most recent W tokens' K and V ("LLM 推理全过程的维度变化与核心公式",
+ * section "KV Cache 的形状与增长").  Blocks wholly before the window are never
+ * read (their table entries may be stale or freed ids); the work and bytes per
+ * row are bounded by the window, not by the context.  window >= ctx gives
+ * exactly paged_attention_decode's result.
+ *   window : >= 1 (PKV_ERR_INVALID_ARG otherwise)
+ * The workspace that paged_attention_workspace_size() gives for the same
+ * arguments is always enough (a window needs at most that).
+ */
+PKV_API int paged_attention_decode_window(void *out, int32_t out_dtype, const void *q, const void *k_cache,
+                                          const void *v_cache, const int32_t *block_tables,
+                                          const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                          int32_t max_blocks_per_seq, float scale, int32_t window,
+                                          int32_t partition_size, const pkv_cache_desc *cache, void *workspace,
+                                          size_t workspace_bytes, void *stream);
+
+/*
+ * paged_attention_decode_fp8 -- decode attention over an FP8 (E4M3) pool.
+ *
+ * As paged_attention_decode_window (window 0 = no window), with K_j and V_j the
+ * dequantised rows code * scale written by kv_reshape_and_cache_fp8:
+ *     s_j = scale * <q, K_j>,  out = sum_j softmax(s)_j V_j
+ * Every K/V byte read per token and head is halved.  The dot products run on
+ * fp16 tensor-core MMAs: E4M3 values are exact fp16 numbers, q is scaled by a
+ * power of two per CTA into the fp16 range (exact), the K scale multiplies the
+ * scores and the V scale is folded into the softmax weights (kept to about
+ * 2^-22 relative as an fp16 head and remainder).
+ *   k_cache, v_cache : uint8 E4M3 codes, cache->dtype PKV_DTYPE_FP8_E4M3
+ *   k_scale, v_scale : fp32 [num_blocks][num_kv_heads][16], device, 16-B aligned
+ *   window           : 0, or >= 1 as in paged_attention_decode_window
+ * Workspace: paged_attention_workspace_size() with this cache descriptor.
+ * Errors: as paged_attention_decode.
+ */
+PKV_API int paged_attention_decode_fp8(void *out, int32_t out_dtype, const void *q, const void *k_cache,
+                                       const void *v_cache, const float *k_scale, const float *v_scale,
+                                       const int32_t *block_tables, const int32_t *context_lens, int32_t num_seqs,
+                                       int32_t num_q_heads, int32_t max_blocks_per_seq, float scale, int32_t window,
+                                       int32_t partition_size, const pkv_cache_desc *cache, void *workspace,
+                                       size_t workspace_bytes, void *stream);
 
 /*
  * paged_attention_prefill_workspace_size -- bytes of workspace that

@@ -460,6 +460,8 @@ void oracle_kv_reshape_and_cache_fp8(const uint16_t *key, const uint16_t *value,
                                      const int32_t *slot_mapping, int32_t num_tokens, int32_t num_blocks,
                                      int32_t block_size, int32_t n_kv, int32_t head_dim)
 {
+    /* Tokens are independent (slots are distinct), so they may run in parallel. */
+#pragma omp parallel for schedule(static)
     for (int32_t t = 0; t < num_tokens; ++t) {
         int64_t slot = slot_mapping[t];
         if (slot < 0 || slot >= (int64_t)num_blocks * block_size)

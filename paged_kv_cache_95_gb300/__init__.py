@@ -20,6 +20,7 @@ from .pagedkv import (  # noqa: F401
     cache_desc,
     kv_copy_blocks,
     kv_reshape_and_cache,
+    kv_reshape_and_cache_fp8,
     load_library,
     paged_attention_decode,
     paged_attention_decode_static_scratch,

@@ -6,6 +6,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -35,7 +36,9 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 std::atomic<int> g_sm_count[kMaxDevices];
 std::once_flag g_decode_prepared[kMaxDevices][8];
 std::once_flag g_prefill_prepared[kMaxDevices];
+std::once_flag g_decode_fp8_prepared[kMaxDevices];
 cudaError_t g_decode_prep_err[kMaxDevices][8];
+cudaError_t g_decode_fp8_prep_err[kMaxDevices];
 cudaError_t g_prefill_prep_err[kMaxDevices];
 
 int current_device() {
@@ -89,6 +92,22 @@ bool encode_pool_map(CUtensorMap *map, const void *base, int32_t num_blocks, int
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// An FP8 pool [num_blocks][n_kv][16][128] of one-byte codes viewed as 4-D; one box
+// = a whole 2 KB (block, head) tile (128 codes = 128 bytes x 16 slots), 128-byte swizzle.
+bool encode_pool_map_fp8(CUtensorMap *map, const void *base, int32_t num_blocks, int32_t n_kv) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(kBlockSize),
+                                static_cast<cuuint64_t>(n_kv), static_cast<cuuint64_t>(num_blocks)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(kHeadDim) * kBlockSize,
+                                   static_cast<cuuint64_t>(kHeadDim) * kBlockSize * n_kv};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(kHeadDim), static_cast<cuuint32_t>(kBlockSize), 1, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // The same pool viewed as 5-D so that ONE box is a whole 4 KB (block, head) tile
 // in the order the tensor core wants it: dims inner->outer are 64 dims (128 B),
 // 8 slots (stride 256 B), the two 64-dim halves (stride 128 B), the two 8-slot
@@ -138,6 +157,15 @@ int check_cache(const pkv_cache_desc *c) {
         return PKV_ERR_UNSUPPORTED;
     // The pool's byte size must stay addressable by the kernels' 64-bit index math
     // and by the 32-bit block coordinate of the tensor map.
+    return PKV_OK;
+}
+
+// A pool of FP8 (E4M3) codes, for the *_fp8 entry points.
+int check_cache_fp8(const pkv_cache_desc *c) {
+    if (!c) return PKV_ERR_INVALID_ARG;
+    if (c->num_blocks < 1 || c->num_kv_heads < 1) return PKV_ERR_INVALID_ARG;
+    if (c->block_size != kBlockSize || c->head_dim != kHeadDim || c->dtype != PKV_DTYPE_FP8_E4M3)
+        return PKV_ERR_UNSUPPORTED;
     return PKV_OK;
 }
 
@@ -255,6 +283,24 @@ int kv_reshape_and_cache(const void *key, const void *value, void *k_cache, void
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
+int kv_reshape_and_cache_fp8(const void *key, const void *value, void *k_cache, void *v_cache, float *k_scale,
+                             float *v_scale, const int32_t *slot_mapping, int32_t num_tokens, const pkv_cache_desc *cache,
+                             void *stream) {
+    if (int rc = check_cache_fp8(cache)) return rc;
+    if (num_tokens < 0) return PKV_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PKV_OK;
+    if (!key || !value || !k_cache || !v_cache || !k_scale || !v_scale || !slot_mapping) return PKV_ERR_INVALID_ARG;
+    if (!aligned(key, 16) || !aligned(value, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(k_scale, 16) || !aligned(v_scale, 16) || !aligned(slot_mapping, 4))
+        return PKV_ERR_INVALID_ARG;
+    const int dev = current_device();
+    if (dev < 0) return PKV_ERR_CUDA;
+    const cudaError_t e = pkv::launch_kv_cache_write_fp8(key, value, k_cache, v_cache, k_scale, v_scale, slot_mapping,
+                                                         num_tokens, cache->num_kv_heads, cache->num_blocks,
+                                                         sm_count(dev), static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
 int kv_copy_blocks(void *k_cache, void *v_cache, float *k_scale, float *v_scale, const int32_t *block_pairs,
                    int32_t num_pairs, const pkv_cache_desc *cache, void *stream) {
     if (!cache || cache->num_blocks < 1 || cache->num_kv_heads < 1) return PKV_ERR_INVALID_ARG;
@@ -276,18 +322,27 @@ int kv_copy_blocks(void *k_cache, void *v_cache, float *k_scale, float *v_scale,
 
 size_t paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq,
                                       int32_t partition_size, const pkv_cache_desc *cache) {
-    if (check_cache(cache) != PKV_OK || num_seqs < 1 || max_blocks_per_seq < 1) return 0;
+    // The workspace does not depend on the cache's element type.
+    if ((check_cache(cache) != PKV_OK && check_cache_fp8(cache) != PKV_OK) || num_seqs < 1 || max_blocks_per_seq < 1)
+        return 0;
     if (check_group(num_q_heads, cache->num_kv_heads) != PKV_OK) return 0;
     if (partition_size < 0 || partition_size % kBlockSize != 0) return 0;
     const int32_t pb = partition_size > 0 ? partition_size / kBlockSize : kMinPartBlocks;
     return plan_decode(num_seqs, num_q_heads, cache->num_kv_heads, max_blocks_per_seq, pb).total;
 }
 
-int paged_attention_decode(void *out, int32_t out_dtype, const void *q, const void *k_cache, const void *v_cache,
-                           const int32_t *block_tables, const int32_t *context_lens, int32_t num_seqs,
-                           int32_t num_q_heads, int32_t max_blocks_per_seq, float scale, int32_t partition_size,
-                           const pkv_cache_desc *cache, void *workspace, size_t workspace_bytes, void *stream) {
-    if (int rc = check_cache(cache)) return rc;
+namespace {
+
+// Shared by the decode entry points; window = 0 means no sliding window; k_scale /
+// v_scale non-null select the FP8 cache (cache->dtype PKV_DTYPE_FP8_E4M3).
+int decode_impl(void *out, int32_t out_dtype, const void *q, const void *k_cache, const void *v_cache,
+                const float *k_scale, const float *v_scale, const int32_t *block_tables,
+                const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq,
+                float scale, int32_t window, int32_t partition_size, const pkv_cache_desc *cache, void *workspace,
+                size_t workspace_bytes, void *stream) {
+    const bool fp8 = k_scale != nullptr;
+    if (int rc = fp8 ? check_cache_fp8(cache) : check_cache(cache)) return rc;
+    if (fp8 && (!v_scale || !aligned(k_scale, 16) || !aligned(v_scale, 16))) return PKV_ERR_INVALID_ARG;
     if (int rc = check_group(num_q_heads, cache->num_kv_heads)) return rc;
     if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PKV_ERR_INVALID_ARG;
     if (out_dtype != PKV_DTYPE_FLOAT32 && out_dtype != PKV_DTYPE_BF16) return PKV_ERR_UNSUPPORTED;
@@ -299,9 +354,16 @@ int paged_attention_decode(void *out, int32_t out_dtype, const void *q, const vo
         !aligned(block_tables, 4) || !aligned(context_lens, 4))
         return PKV_ERR_INVALID_ARG;
     if (!workspace || !aligned(workspace, 256)) return PKV_ERR_INVALID_ARG;
-    // The documented contract: at least what paged_attention_workspace_size() answers.
+    if (window < 0) return PKV_ERR_INVALID_ARG;
+    // Blocks one row can touch: all of its table, or at most ceil(W / 16) + 1 under a window.
+    const int32_t span_blocks =
+        window > 0 ? static_cast<int32_t>(std::min<int64_t>(max_blocks_per_seq, (static_cast<int64_t>(window) + 15) /
+                                                                                         kBlockSize + 1))
+                   : max_blocks_per_seq;
+    // The documented contract: at least what paged_attention_workspace_size() answers for
+    // the blocks a row can touch (for a window that is no more than for the whole table).
     if (workspace_bytes <
-        paged_attention_workspace_size(num_seqs, num_q_heads, max_blocks_per_seq, partition_size, cache))
+        paged_attention_workspace_size(num_seqs, num_q_heads, span_blocks, partition_size, cache))
         return PKV_ERR_WORKSPACE_TOO_SMALL;
 
     const int32_t n_kv = cache->num_kv_heads;
@@ -315,19 +377,27 @@ int paged_attention_decode(void *out, int32_t out_dtype, const void *q, const vo
     const int sms = sm_count(dev);
 
     const int32_t pb = partition_size > 0 ? partition_size / kBlockSize
-                                          : auto_part_blocks(num_seqs, n_kv, head_splits, max_blocks_per_seq, sms);
-    const DecodePlan pl = plan_decode(num_seqs, num_q_heads, n_kv, max_blocks_per_seq, pb);
+                                          : auto_part_blocks(num_seqs, n_kv, head_splits, span_blocks, sms);
+    const DecodePlan pl = plan_decode(num_seqs, num_q_heads, n_kv, span_blocks, pb);
     if (workspace_bytes < pl.total) return PKV_ERR_WORKSPACE_TOO_SMALL;  // cannot happen for auto plans
 
     CUtensorMap kmap, vmap;
-    if (!encode_pool_map(&kmap, k_cache, cache->num_blocks, n_kv) ||
-        !encode_pool_map(&vmap, v_cache, cache->num_blocks, n_kv))
+    if (fp8 ? (!encode_pool_map_fp8(&kmap, k_cache, cache->num_blocks, n_kv) ||
+               !encode_pool_map_fp8(&vmap, v_cache, cache->num_blocks, n_kv))
+            : (!encode_pool_map(&kmap, k_cache, cache->num_blocks, n_kv) ||
+               !encode_pool_map(&vmap, v_cache, cache->num_blocks, n_kv)))
         return PKV_ERR_CUDA;
 
     const pkv::DecodeVariant var = decode_variant();
     const int vi = variant_index(var);
-    std::call_once(g_decode_prepared[dev][vi], [&] { g_decode_prep_err[dev][vi] = pkv::decode_prepare_device(var); });
-    if (g_decode_prep_err[dev][vi] != cudaSuccess) return PKV_ERR_CUDA;
+    if (fp8) {
+        std::call_once(g_decode_fp8_prepared[dev], [&] { g_decode_fp8_prep_err[dev] = pkv::decode_fp8_prepare_device(); });
+        if (g_decode_fp8_prep_err[dev] != cudaSuccess) return PKV_ERR_CUDA;
+    } else {
+        std::call_once(g_decode_prepared[dev][vi],
+                       [&] { g_decode_prep_err[dev][vi] = pkv::decode_prepare_device(var); });
+        if (g_decode_prep_err[dev][vi] != cudaSuccess) return PKV_ERR_CUDA;
+    }
 
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     pkv::DecodeParams p{};
@@ -353,10 +423,53 @@ int paged_attention_decode(void *out, int32_t out_dtype, const void *q, const vo
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     p.out_bf16 = out_dtype == PKV_DTYPE_BF16;
     p.fused_merge = fused_merge() ? 1 : 0;
+    p.window = window;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (pkv::launch_paged_decode(kmap, vmap, p, var, s) != cudaSuccess) return PKV_ERR_CUDA;
-    return PKV_OK;
+    cudaError_t e;
+    if (fp8) {
+        pkv::DecodeParamsFp8 p8{};
+        static_cast<pkv::DecodeParams &>(p8) = p;
+        p8.k_scale = k_scale;
+        p8.v_scale = v_scale;
+        e = pkv::launch_paged_decode_fp8(kmap, vmap, p8, s);
+    } else {
+        e = pkv::launch_paged_decode(kmap, vmap, p, var, s);
+    }
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // namespace
+
+int paged_attention_decode(void *out, int32_t out_dtype, const void *q, const void *k_cache, const void *v_cache,
+                           const int32_t *block_tables, const int32_t *context_lens, int32_t num_seqs,
+                           int32_t num_q_heads, int32_t max_blocks_per_seq, float scale, int32_t partition_size,
+                           const pkv_cache_desc *cache, void *workspace, size_t workspace_bytes, void *stream) {
+    return decode_impl(out, out_dtype, q, k_cache, v_cache, nullptr, nullptr, block_tables, context_lens, num_seqs,
+                       num_q_heads, max_blocks_per_seq, scale, 0, partition_size, cache, workspace, workspace_bytes,
+                       stream);
+}
+
+int paged_attention_decode_window(void *out, int32_t out_dtype, const void *q, const void *k_cache,
+                                  const void *v_cache, const int32_t *block_tables, const int32_t *context_lens,
+                                  int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq, float scale,
+                                  int32_t window, int32_t partition_size, const pkv_cache_desc *cache,
+                                  void *workspace, size_t workspace_bytes, void *stream) {
+    if (window < 1) return PKV_ERR_INVALID_ARG;
+    return decode_impl(out, out_dtype, q, k_cache, v_cache, nullptr, nullptr, block_tables, context_lens, num_seqs,
+                       num_q_heads, max_blocks_per_seq, scale, window, partition_size, cache, workspace,
+                       workspace_bytes, stream);
+}
+
+int paged_attention_decode_fp8(void *out, int32_t out_dtype, const void *q, const void *k_cache, const void *v_cache,
+                               const float *k_scale, const float *v_scale, const int32_t *block_tables,
+                               const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                               int32_t max_blocks_per_seq, float scale, int32_t window, int32_t partition_size,
+                               const pkv_cache_desc *cache, void *workspace, size_t workspace_bytes, void *stream) {
+    if (!k_scale || !v_scale || window < 0) return PKV_ERR_INVALID_ARG;
+    return decode_impl(out, out_dtype, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, num_seqs,
+                       num_q_heads, max_blocks_per_seq, scale, window, partition_size, cache, workspace,
+                       workspace_bytes, stream);
 }
 
 size_t paged_attention_prefill_workspace_size(int32_t num_seqs, int32_t num_q_heads, const pkv_cache_desc *cache) {

@@ -30,6 +30,15 @@
 //  * Keys at or past ctx (the tail of the last block) are masked by index, never
 //    by value, and their V rows are zeroed in registers, so stale or NaN bytes in
 //    unused slots cannot leak into the result.
+//  * FP8 (E4M3) caches (FP8 = true): a stage holds the block's 2 KB K and V code
+//    tiles (one TMA box each) and their 64 B scale rows (bulk copies); the MMAs
+//    run in fp16 as laid out in decode_core.cuh, the K scale multiplies the
+//    scores and the V scale is folded into P.  Bytes per token and head halve.
+//  * Sliding window W ("LLM 推理全过程的维度变化与核心公式", section "KV Cache 的
+//    形状与增长": only the most recent W tokens' K and V are kept): the row sees
+//    keys j >= j0 = max(0, ctx - W); partitions cover only the blocks from
+//    j0 / 16 on, so whole blocks before the window are never fetched, and the
+//    keys of the first block that precede j0 are masked like the tail.
 //  * At the end the warps' (m, l, O) are combined through shared memory; with a
 //    single partition the CTA writes out = O / l directly, otherwise it writes
 //    the unnormalised partial (m, l, O) to the workspace and counts itself on
@@ -39,6 +48,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <type_traits>
 
 #include "decode_core.cuh"
 #include "launch.h"
@@ -48,10 +58,11 @@ namespace pkv {
 
 namespace {
 
-template <int NW, int ST>
+template <int NW, int ST, bool FP8>
 __global__ void __launch_bounds__(NW * 32)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                        const DecodeParams p) {
+                        const std::conditional_t<FP8, DecodeParamsFp8, DecodeParams> p) {
+    constexpr uint32_t kStage = FP8 ? kStageBytes8 : kStageBytes;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem =
         reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -87,15 +98,19 @@ __global__ void __launch_bounds__(NW * 32)
         return;
     }
     const int nblocks = (ctx + kBlockSize - 1) / kBlockSize;
-    const int nparts = (nblocks + p.part_blocks - 1) / p.part_blocks;
+    const int j0 = (p.window > 0 && ctx > p.window) ? ctx - p.window : 0;  // first visible key
+    const int first_blk = j0 / kBlockSize;
+    const int nparts = (nblocks - first_blk + p.part_blocks - 1) / p.part_blocks;
     if (part >= nparts) return;
-    const int blk_begin = part * p.part_blocks;
+    const int blk_begin = first_blk + part * p.part_blocks;
     const int nblk = min(p.part_blocks, nblocks - blk_begin);
     const int nmine = nblk > warp ? (nblk - warp + NW - 1) / NW : 0;
     const int32_t *table = p.block_tables + static_cast<size_t>(b) * p.max_blocks;
 
-    const uint32_t stage_base = smem_u32(smem) + warp * (ST * kStageBytes);
-    const uint32_t bar_base = smem_u32(smem) + NW * ST * kStageBytes + warp * ST * 8;
+    const uint32_t stage_base = smem_u32(smem) + warp * (ST * kStage);
+    // FP8: the scale rows of each stage sit after all warps' code rings.
+    const uint32_t scale_base = smem_u32(smem) + NW * ST * kStage + warp * (FP8 ? ST * kStageScaleBytes : 0);
+    const uint32_t bar_base = smem_u32(smem) + NW * ST * kStage + (FP8 ? NW * ST * kStageScaleBytes : 0) + warp * ST * 8;
 
     if (lane == 0) {
         for (int s = 0; s < ST; ++s) mbar_init(bar_base + 8 * s, 1);
@@ -109,7 +124,11 @@ __global__ void __launch_bounds__(NW * 32)
         const int j = blk_begin + warp + NW * i;
         int phys = __ldg(table + j);
         if (static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_blocks)) phys = 0;  // masked below
-        issue_block_copy(&kmap, &vmap, stage_base + s * kStageBytes, bar_base + 8 * s, g, phys);
+        if constexpr (FP8)
+            issue_block_copy_fp8(&kmap, &vmap, p.k_scale, p.v_scale, stage_base + s * kStage,
+                                 scale_base + s * kStageScaleBytes, bar_base + 8 * s, g, p.n_kv, phys);
+        else
+            issue_block_copy(&kmap, &vmap, stage_base + s * kStage, bar_base + 8 * s, g, phys);
     };
     if (lane == 0)
         for (int i = 0; i < ST && i < nmine; ++i) issue(i);
@@ -118,12 +137,17 @@ __global__ void __launch_bounds__(NW * 32)
     const int n = lane >> 2;  // head column of B / row group of C
     const int q4 = lane & 3;
     uint32_t bq[8][2];
-    load_q_frag(bq, p.q, static_cast<size_t>(b) * p.n_q + h0, hpc, lane);
+    float sl2 = p.scale_log2;
+    if constexpr (FP8) {
+        const int qexp = load_q_frag_fp8(bq, p.q, static_cast<size_t>(b) * p.n_q + h0, hpc, lane);
+        sl2 *= ldexpf(1.f, -qexp);
+    } else {
+        load_q_frag(bq, p.q, static_cast<size_t>(b) * p.n_q + h0, hpc, lane);
+    }
 
     DecodeAcc acc;
     acc.reset();
 
-    const float sl2 = p.scale_log2;
     int consumed = 0;
     bool timed_out = false;
     for (int i = 0; i < nmine; ++i) {
@@ -138,12 +162,16 @@ __global__ void __launch_bounds__(NW * 32)
         const int j = blk_begin + warp + NW * i;
         const int phys = __ldg(table + j);
         int valid = min(kBlockSize, ctx - j * kBlockSize);
+        const int lo = j == first_blk ? j0 - j * kBlockSize : 0;
         if (static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_blocks)) {
             valid = 0;
             if (lane == 0 && p.status) atomicOr(p.status, kStatusBadBlockId);
         }
-        const uint32_t kb = stage_base + s * kStageBytes;
-        decode_block(acc, bq, kb, kb + kTileBytes, valid, sl2, lane);
+        const uint32_t kb = stage_base + s * kStage;
+        if constexpr (FP8)
+            decode_block_fp8(acc, bq, kb, kb + kTileBytes8, scale_base + s * kStageScaleBytes, lo, valid, sl2, lane);
+        else
+            decode_block(acc, bq, kb, kb + kTileBytes, lo, valid, sl2, lane);
         consumed = i + 1;
 
         __syncwarp();
@@ -170,11 +198,14 @@ __global__ void __launch_bounds__(NW * 32)
     float *red_l = red_m + NW * 8;                   // [NW][8]
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
-        const int d0 = 16 * mt + n;
+        // O^T fragment rows n and n + 8 of MMA mt are dims d0 and d1 (bf16: 16mt + n, +8;
+        // FP8: the permuted order 16n + 2mt, +1)
+        const int d0 = FP8 ? 16 * n + 2 * mt : 16 * mt + n;
+        const int d1 = FP8 ? d0 + 1 : d0 + 8;
         red_o[(warp * 8 + 2 * q4) * kHeadDim + d0] = acc.o[mt][0];
         red_o[(warp * 8 + 2 * q4 + 1) * kHeadDim + d0] = acc.o[mt][1];
-        red_o[(warp * 8 + 2 * q4) * kHeadDim + d0 + 8] = acc.o[mt][2];
-        red_o[(warp * 8 + 2 * q4 + 1) * kHeadDim + d0 + 8] = acc.o[mt][3];
+        red_o[(warp * 8 + 2 * q4) * kHeadDim + d1] = acc.o[mt][2];
+        red_o[(warp * 8 + 2 * q4 + 1) * kHeadDim + d1] = acc.o[mt][3];
     }
     if (lane < 4) {
         red_m[warp * 8 + 2 * lane] = acc.m0;
@@ -283,7 +314,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lse_merge_kernel(const Decod
     int ctx = __ldg(p.context_lens + b);
     const int max_ctx = p.max_blocks * kBlockSize;
     ctx = ctx < 1 ? 0 : (ctx > max_ctx ? max_ctx : ctx);
-    const int nparts = ((ctx + kBlockSize - 1) / kBlockSize + p.part_blocks - 1) / p.part_blocks;
+    const int first_blk = ((p.window > 0 && ctx > p.window) ? ctx - p.window : 0) / kBlockSize;
+    const int nparts = ((ctx + kBlockSize - 1) / kBlockSize - first_blk + p.part_blocks - 1) / p.part_blocks;
     if (nparts <= 1) return;  // written directly by the decode kernel
     const size_t base = (static_cast<size_t>(b) * p.n_q + h) * p.max_parts;
     float M = -INFINITY;
@@ -323,23 +355,27 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lse_merge_kernel(const Decod
     }
 }
 
-template <int NW, int ST>
-cudaError_t launch_variant(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParams &p,
-                           cudaStream_t stream) {
+template <int NW, int ST, bool FP8 = false>
+cudaError_t launch_variant(const CUtensorMap &kmap, const CUtensorMap &vmap,
+                           const std::conditional_t<FP8, DecodeParamsFp8, DecodeParams> &p, cudaStream_t stream) {
     const dim3 grid(p.max_parts, p.n_kv * p.head_splits, p.num_seqs);
-    cudaError_t e = launch_pdl(paged_decode_kernel<NW, ST>, grid, dim3(NW * 32), decode_smem_bytes({NW, ST}), stream,
-                               kmap, vmap, p);
+    cudaError_t e = launch_pdl(paged_decode_kernel<NW, ST, FP8>, grid, dim3(NW * 32),
+                               FP8 ? decode_fp8_smem_bytes() : decode_smem_bytes({NW, ST}), stream, kmap, vmap, p);
     if (e != cudaSuccess) return e;
     if (p.max_parts > 1 && !p.fused_merge)
-        e = launch_pdl(lse_merge_kernel, dim3(p.n_q, p.num_seqs), dim3(kMergeWarps * 32), 0, stream, p);
+        e = launch_pdl(lse_merge_kernel, dim3(p.n_q, p.num_seqs), dim3(kMergeWarps * 32), 0, stream,
+                       static_cast<const DecodeParams &>(p));
     return e;
 }
 
 template <int NW, int ST>
 cudaError_t prepare_variant() {
-    return cudaFuncSetAttribute(paged_decode_kernel<NW, ST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(paged_decode_kernel<NW, ST, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(decode_smem_bytes({NW, ST})));
 }
+
+// The FP8 decode: 4 warps, 4 stages of 4 KB codes (+ 128 B of scales) per warp.
+constexpr int kFp8Warps = 4, kFp8Stages = 4;
 
 }  // namespace
 
@@ -358,6 +394,20 @@ cudaError_t decode_prepare_device(DecodeVariant v) {
     if (v.warps == 4 && v.stages == 4) return prepare_variant<4, 4>();
     if (v.warps == 8 && v.stages == 2) return prepare_variant<8, 2>();
     return cudaErrorInvalidValue;
+}
+
+size_t decode_fp8_smem_bytes() {
+    return static_cast<size_t>(kFp8Warps) * kFp8Stages * (kStageBytes8 + kStageScaleBytes + 8) + 1024;
+}
+
+cudaError_t decode_fp8_prepare_device() {
+    return cudaFuncSetAttribute(paged_decode_kernel<kFp8Warps, kFp8Stages, true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(decode_fp8_smem_bytes()));
+}
+
+cudaError_t launch_paged_decode_fp8(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParamsFp8 &p,
+                                    cudaStream_t stream) {
+    return launch_variant<kFp8Warps, kFp8Stages, true>(kmap, vmap, p, stream);
 }
 
 cudaError_t launch_paged_decode(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParams &p,

@@ -71,10 +71,11 @@ __device__ __forceinline__ void load_q_frag(uint32_t (&bq)[8][2], const void *q,
 }
 
 // One block: kb / vb are the shared addresses of the stage's K and V tiles;
-// keys >= valid are masked by index (their V rows are zeroed in registers, so
-// stale or NaN bytes in unused slots never reach the result).
+// only keys lo <= k < valid take part (lo > 0 only in the block where a sliding
+// window starts); the others are masked by index and their V rows are zeroed in
+// registers, so stale or NaN bytes in those slots never reach the result.
 __device__ __forceinline__ void decode_block(DecodeAcc &acc, const uint32_t (&bq)[8][2], uint32_t kb, uint32_t vb,
-                                             int valid, float sl2, int lane) {
+                                             int lo, int valid, float sl2, int lane) {
     const int n = lane >> 2, q4 = lane & 3;
     const int kkey = (lane & 7) | (((lane >> 3) & 1) << 3);  // K: matrices (keys 0-7 | 8-15) x (dims lo | hi)
     const int khi = lane >> 4;
@@ -94,10 +95,11 @@ __device__ __forceinline__ void decode_block(DecodeAcc &acc, const uint32_t (&bq
 
     // Online softmax in the log2 domain (scale * log2(e) folded into the scores).
     const int key_a = n, key_b = n + 8;
-    const float s00 = key_a < valid ? c[0] * sl2 : -INFINITY;
-    const float s01 = key_a < valid ? c[1] * sl2 : -INFINITY;
-    const float s10 = key_b < valid ? c[2] * sl2 : -INFINITY;
-    const float s11 = key_b < valid ? c[3] * sl2 : -INFINITY;
+    const bool in_a = key_a >= lo && key_a < valid, in_b = key_b >= lo && key_b < valid;
+    const float s00 = in_a ? c[0] * sl2 : -INFINITY;
+    const float s01 = in_a ? c[1] * sl2 : -INFINITY;
+    const float s10 = in_b ? c[2] * sl2 : -INFINITY;
+    const float s11 = in_b ? c[3] * sl2 : -INFINITY;
     float bm0 = fmaxf(s00, s10), bm1 = fmaxf(s01, s11);
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
@@ -133,12 +135,13 @@ __device__ __forceinline__ void decode_block(DecodeAcc &acc, const uint32_t (&bq
     const uint32_t pr0 = movmatrix_trans(pl0);
     const uint32_t pr1 = movmatrix_trans(pl1);
 
-    // Zero V rows of keys >= valid (their P is 0, but 0 * NaN would not be).
+    // Zero V rows of keys outside [lo, valid) (their P is 0, but 0 * NaN would not be).
     uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;
-    if (valid < kBlockSize) {
+    if (lo > 0 || valid < kBlockSize) {
+        auto keep = [&](int k) { return k >= lo && k < valid; };
         const int ka = 2 * q4, kb2 = 2 * q4 + 8;
-        vm_lo = (ka < valid ? 0x0000ffffu : 0u) | (ka + 1 < valid ? 0xffff0000u : 0u);
-        vm_hi = (kb2 < valid ? 0x0000ffffu : 0u) | (kb2 + 1 < valid ? 0xffff0000u : 0u);
+        vm_lo = (keep(ka) ? 0x0000ffffu : 0u) | (keep(ka + 1) ? 0xffff0000u : 0u);
+        vm_hi = (keep(kb2) ? 0x0000ffffu : 0u) | (keep(kb2 + 1) ? 0xffff0000u : 0u);
     }
 
     // O^T += V^T P^T  (rows: head dims, columns: heads)
@@ -166,6 +169,181 @@ __device__ __forceinline__ void issue_block_copy(const CUtensorMap *kmap, const 
     tma_load_4d(dst + kBoxBytes, kmap, bar, 64, 0, kv_head, phys_block);
     tma_load_4d(dst + kTileBytes, vmap, bar, 0, 0, kv_head, phys_block);
     tma_load_4d(dst + kTileBytes + kBoxBytes, vmap, bar, 64, 0, kv_head, phys_block);
+}
+
+// ---- FP8 (E4M3) cache: one code per element, one fp32 scale per (slot, head) ----
+//
+// The MMAs run in fp16, which holds every E4M3 value exactly.  S^T = K Q^T
+// contracts over the head dims in a permuted order -- k-step kk, lane column
+// t = lane % 4 covers dims 32t + 4kk + {0,1} and 32t + 4kk + {2,3} -- so each lane
+// reads 32 contiguous code bytes of a key row; Q follows the same order (the dot
+// product does not depend on it).  O^T += V^T P^T assigns fragment row g of MMA
+// mt to output dim 16g + 2mt and row g + 8 to 16g + 2mt + 1, so each lane reads
+// 16 contiguous code bytes of four key rows and builds key pairs with byte
+// permutes; the combine step undoes the order.
+constexpr uint32_t kTileBytes8 = kBlockSize * kHeadDim;   // 2 KB: 16 slots x 128 codes
+constexpr uint32_t kStageBytes8 = 2 * kTileBytes8;        // K tile + V tile
+constexpr uint32_t kScaleBytes = kBlockSize * 4;          // 64 B: one (block, head)'s scales
+constexpr uint32_t kStageScaleBytes = 2 * kScaleBytes;    // K scales + V scales
+
+// Q (bf16) as fp16 B fragments in the permuted dim order, times 2^qexp.  qexp is
+// chosen so that the largest |q| of the CTA's heads lands in [2^13, 2^14): the
+// power-of-two scaling is exact and keeps every value inside the fp16 range.
+// Returns qexp (the caller multiplies the scores by 2^-qexp).
+__device__ __forceinline__ int load_q_frag_fp8(uint32_t (&bq)[8][2], const void *q, size_t head0_row, int hpc,
+                                               int lane) {
+    const int n = lane >> 2, q4 = lane & 3;
+    const bool hv = n < hpc;
+    const uint32_t *qrow =
+        reinterpret_cast<const uint32_t *>(static_cast<const __nv_bfloat16 *>(q) + (head0_row + n) * kHeadDim);
+    float amax = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        bq[kk][0] = hv ? __ldg(qrow + (32 * q4 + 4 * kk) / 2) : 0u;
+        bq[kk][1] = hv ? __ldg(qrow + (32 * q4 + 4 * kk + 2) / 2) : 0u;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            amax = fmaxf(amax, fabsf(__uint_as_float(bq[kk][j] << 16)));
+            amax = fmaxf(amax, fabsf(__uint_as_float(bq[kk][j] & 0xffff0000u)));
+        }
+    }
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    int qexp = 0;
+    if (amax > 0.f) {
+        const int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xff) - 127;  // floor(log2) for normals
+        qexp = min(100, max(-100, 13 - e));
+    }
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const float lo = ldexpf(__uint_as_float(bq[kk][j] << 16), qexp);
+            const float hi = ldexpf(__uint_as_float(bq[kk][j] & 0xffff0000u), qexp);
+            bq[kk][j] = pack_f16x2(lo, hi);
+        }
+    return qexp;
+}
+
+// One FP8 block.  kb / vb: the stage's K and V code tiles (16 rows x 128 B,
+// 128-byte swizzled); sc: its scales (16 K scales, then 16 V scales).  Keys
+// outside [lo, valid) are masked by index; their V codes and scales are never
+// used, so stale or NaN bytes in those slots do not reach the result.
+// fsl2 = scale * log2(e) * 2^-qexp.
+__device__ __forceinline__ void decode_block_fp8(DecodeAcc &acc, const uint32_t (&bq)[8][2], uint32_t kb,
+                                                 uint32_t vb, uint32_t sc, int lo, int valid, float fsl2, int lane) {
+    const int n = lane >> 2, q4 = lane & 3;
+    const int key_a = n, key_b = n + 8;
+    const bool in_a = key_a >= lo && key_a < valid, in_b = key_b >= lo && key_b < valid;
+
+    // S^T = K Q^T: key rows n and n + 8, code bytes 32*q4 .. +31 (chunks 2*q4, 2*q4+1, swizzled)
+    const uint32_t sw = static_cast<uint32_t>(n & 7);
+    const uint4 ka0 = lds128(kb + key_a * 128 + (((2 * q4) ^ sw) << 4));
+    const uint4 ka1 = lds128(kb + key_a * 128 + (((2 * q4 + 1) ^ sw) << 4));
+    const uint4 kb0 = lds128(kb + key_b * 128 + (((2 * q4) ^ sw) << 4));
+    const uint4 kb1 = lds128(kb + key_b * 128 + (((2 * q4 + 1) ^ sw) << 4));
+    const uint32_t wa[8] = {ka0.x, ka0.y, ka0.z, ka0.w, ka1.x, ka1.y, ka1.z, ka1.w};
+    const uint32_t wb[8] = {kb0.x, kb0.y, kb0.z, kb0.w, kb1.x, kb1.y, kb1.z, kb1.w};
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t a[4] = {e4m3x2_to_f16x2(wa[kk]), e4m3x2_to_f16x2(wb[kk]), e4m3x2_to_f16x2(wa[kk] >> 16),
+                               e4m3x2_to_f16x2(wb[kk] >> 16)};
+        mma_f16_16816(c, a, bq[kk][0], bq[kk][1]);
+    }
+
+    // Scores with each key's K scale; online softmax in the log2 domain.
+    const float fa = lds_f32(sc + 4 * key_a) * fsl2, fb = lds_f32(sc + 4 * key_b) * fsl2;
+    const float s00 = in_a ? c[0] * fa : -INFINITY;
+    const float s01 = in_a ? c[1] * fa : -INFINITY;
+    const float s10 = in_b ? c[2] * fb : -INFINITY;
+    const float s11 = in_b ? c[3] * fb : -INFINITY;
+    float bm0 = fmaxf(s00, s10), bm1 = fmaxf(s01, s11);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
+        bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
+    }
+    const float mn0 = fmaxf(acc.m0, bm0), mn1 = fmaxf(acc.m1, bm1);
+    const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
+    const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
+    const float al0 = fast_exp2(acc.m0 - mu0), al1 = fast_exp2(acc.m1 - mu1);
+    const float p00 = fast_exp2(s00 - mu0), p01 = fast_exp2(s01 - mu1);
+    const float p10 = fast_exp2(s10 - mu0), p11 = fast_exp2(s11 - mu1);
+    acc.l0 = acc.l0 * al0 + p00 + p10;
+    acc.l1 = acc.l1 * al1 + p01 + p11;
+    acc.m0 = mn0;
+    acc.m1 = mn1;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+        acc.o[mt][0] *= al0;
+        acc.o[mt][1] *= al1;
+        acc.o[mt][2] *= al0;
+        acc.o[mt][3] *= al1;
+    }
+
+    // V scales folded into P: P'' = p * sv * 2^r, with 2^r putting the block's
+    // largest (unmasked) scale in [2^9, 2^10) so that P'' is a normal fp16 number
+    // for every weight that matters; P'' as an fp16 head + remainder.  Each MMA
+    // pair accumulates into a fresh tile that is added to O times 2^-r.
+    const float sva = in_a ? lds_f32(sc + kScaleBytes + 4 * key_a) : 0.f;
+    const float svb = in_b ? lds_f32(sc + kScaleBytes + 4 * key_b) : 0.f;
+    float svmax = fmaxf(sva, svb);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) svmax = fmaxf(svmax, __shfl_xor_sync(0xffffffffu, svmax, off));
+    int r = 0;
+    if (svmax > 0.f) r = min(100, max(-100, 9 - (static_cast<int>((__float_as_uint(svmax) >> 23) & 0xff) - 127)));
+    const float up = ldexpf(1.f, r), down = ldexpf(1.f, -r);
+    const float q00 = p00 * sva * up, q01 = p01 * sva * up, q10 = p10 * svb * up, q11 = p11 * svb * up;
+    const uint32_t ph0 = pack_f16x2(q00, q01), ph1 = pack_f16x2(q10, q11);
+    const float2 h0 = unpack_f16x2(ph0), h1 = unpack_f16x2(ph1);
+    const uint32_t pl0 = pack_f16x2(q00 - h0.x, q01 - h0.y), pl1 = pack_f16x2(q10 - h1.x, q11 - h1.y);
+    const uint32_t pb0 = movmatrix_trans(ph0), pb1 = movmatrix_trans(ph1);
+    const uint32_t pr0 = movmatrix_trans(pl0), pr1 = movmatrix_trans(pl1);
+
+    // V^T: key rows 2*q4, 2*q4+1, 2*q4+8, 2*q4+9, code bytes 16n .. 16n+15 (chunk n, swizzled);
+    // masked keys contribute zero codes.
+    auto keep = [&](int k) { return k >= lo && k < valid; };
+    const int k0 = 2 * q4;
+    uint4 v0 = lds128(vb + k0 * 128 + ((n ^ (k0 & 7)) << 4));
+    uint4 v1 = lds128(vb + (k0 + 1) * 128 + ((n ^ ((k0 + 1) & 7)) << 4));
+    uint4 v2 = lds128(vb + (k0 + 8) * 128 + ((n ^ ((k0 + 8) & 7)) << 4));
+    uint4 v3 = lds128(vb + (k0 + 9) * 128 + ((n ^ ((k0 + 9) & 7)) << 4));
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    if (!keep(k0)) v0 = zero;
+    if (!keep(k0 + 1)) v1 = zero;
+    if (!keep(k0 + 8)) v2 = zero;
+    if (!keep(k0 + 9)) v3 = zero;
+    const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w}, w1[4] = {v1.x, v1.y, v1.z, v1.w};
+    const uint32_t w2[4] = {v2.x, v2.y, v2.z, v2.w}, w3[4] = {v3.x, v3.y, v3.z, v3.w};
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+        // bytes 2mt, 2mt+1 of each row: [row k.b, row k+1.b, row k.b+1, row k+1.b+1]
+        const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+        const uint32_t pa = __byte_perm(w0[mt >> 1], w1[mt >> 1], sel);
+        const uint32_t pb = __byte_perm(w2[mt >> 1], w3[mt >> 1], sel);
+        const uint32_t a[4] = {e4m3x2_to_f16x2(pa), e4m3x2_to_f16x2(pa >> 16), e4m3x2_to_f16x2(pb),
+                               e4m3x2_to_f16x2(pb >> 16)};
+        float t[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_f16_16816(t, a, pb0, pb1);
+        mma_f16_16816(t, a, pr0, pr1);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc.o[mt][j] = fmaf(t[j], down, acc.o[mt][j]);
+    }
+}
+
+// Copies of one (block, head) FP8 tile pair and its scales into a stage: two
+// 2 KB TMA boxes and two 64 B bulk copies, completing on `bar`.
+__device__ __forceinline__ void issue_block_copy_fp8(const CUtensorMap *kmap, const CUtensorMap *vmap,
+                                                     const float *k_scale, const float *v_scale, uint32_t dst,
+                                                     uint32_t dst_scale, uint32_t bar, int kv_head, int n_kv,
+                                                     int phys_block) {
+    mbar_arrive_expect_tx(bar, kStageBytes8 + kStageScaleBytes);
+    tma_load_4d(dst, kmap, bar, 0, 0, kv_head, phys_block);
+    tma_load_4d(dst + kTileBytes8, vmap, bar, 0, 0, kv_head, phys_block);
+    const size_t row = (static_cast<size_t>(phys_block) * n_kv + kv_head) * kBlockSize;
+    bulk_copy_g2s(dst_scale, k_scale + row, kScaleBytes, bar);
+    bulk_copy_g2s(dst_scale + kScaleBytes, v_scale + row, kScaleBytes, bar);
 }
 
 }  // namespace pkv

@@ -39,6 +39,9 @@ constexpr uint32_t kStatusTimeout = 0x8u;
 cudaError_t launch_kv_copy_blocks(void *k_cache, void *v_cache, float *k_scale, float *v_scale, const int32_t *pairs,
                                   int32_t num_pairs, int32_t n_kv, int32_t elem_bytes, int32_t num_blocks,
                                   cudaStream_t stream);
+cudaError_t launch_kv_cache_write_fp8(const void *key, const void *value, void *k_cache, void *v_cache, float *k_scale,
+                                      float *v_scale, const int32_t *slot_mapping, int32_t num_tokens, int32_t n_kv,
+                                      int32_t num_blocks, int sm_count, cudaStream_t stream);
 cudaError_t launch_kv_cache_write(const void *key, const void *value, void *k_cache, void *v_cache,
                                   const int32_t *slot_mapping, int32_t num_tokens, int32_t n_kv,
                                   int32_t num_blocks, int sm_count, cudaStream_t stream);
@@ -65,6 +68,14 @@ struct DecodeParams {
     float scale_log2;            // scale * log2(e)
     int32_t out_bf16;            // 1: bf16 output, 0: f32
     int32_t fused_merge;         // 1: last partition CTA merges; 0: a separate merge kernel runs
+    int32_t window;              // sliding window W (keys j >= ctx - W visible); 0: none
+};
+
+// The FP8 decode's parameters: the same plus the per-token scales (a separate
+// type, so the bf16 kernels' parameter block stays as it is).
+struct DecodeParamsFp8 : DecodeParams {
+    const float *k_scale;  // [num_blocks][n_kv][16]
+    const float *v_scale;
 };
 
 struct DecodeVariant {
@@ -80,6 +91,11 @@ cudaError_t decode_prepare_device(DecodeVariant v);  // sets the dynamic shared 
 // merge kernel), both with programmatic dependent launch.
 cudaError_t launch_paged_decode(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParams &p,
                                 DecodeVariant v, cudaStream_t stream);
+// The FP8 (E4M3 codes + per-token scales) decode: fixed variant, same merge.
+size_t decode_fp8_smem_bytes();
+cudaError_t decode_fp8_prepare_device();
+cudaError_t launch_paged_decode_fp8(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParamsFp8 &p,
+                                    cudaStream_t stream);
 
 // ---- K4: causal chunked prefill on tcgen05 ---------------------------------------
 struct PrefillParams {

@@ -78,6 +78,12 @@ def _declare(lib):
     lib.paged_attention_workspace_size.restype = sz
     lib.paged_attention_decode.argtypes = [P, i32, P, P, P, P, P, i32, i32, i32, f32, i32, D, P, sz, P]
     lib.paged_attention_decode.restype = ctypes.c_int
+    lib.paged_attention_decode_window.argtypes = [P, i32, P, P, P, P, P, i32, i32, i32, f32, i32, i32, D, P, sz, P]
+    lib.paged_attention_decode_window.restype = ctypes.c_int
+    lib.paged_attention_decode_fp8.argtypes = [P, i32, P, P, P, P, P, P, P, i32, i32, i32, f32, i32, i32, D, P, sz, P]
+    lib.paged_attention_decode_fp8.restype = ctypes.c_int
+    lib.kv_reshape_and_cache_fp8.argtypes = [P, P, P, P, P, P, P, i32, D, P]
+    lib.kv_reshape_and_cache_fp8.restype = ctypes.c_int
     lib.paged_attention_prefill_workspace_size.argtypes = [i32, i32, D]
     lib.paged_attention_prefill_workspace_size.restype = sz
     lib.paged_attention_prefill_chunk.argtypes = [P, i32, P, P, i32, i32, P, P, P, P, i32, i32, i32, f32, D, P, sz, P]
@@ -206,6 +212,35 @@ def kv_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, stream=None
     _raise("kv_reshape_and_cache", rc)
 
 
+def _check_fp8_pool(k_cache, v_cache, k_scale, v_scale):
+    torch = _torch()
+    desc = cache_desc(k_cache)
+    _need(desc.dtype == PKV_DTYPE_FP8_E4M3, "k_cache must hold E4M3 codes (torch.float8_e4m3fn or uint8)")
+    _check(v_cache, "v_cache", k_cache.dtype, ndim=4)
+    _need(tuple(v_cache.shape) == tuple(k_cache.shape), "v_cache shape must equal k_cache shape")
+    for name, t in (("k_scale", k_scale), ("v_scale", v_scale)):
+        _need(t is not None, f"{name} is required for an FP8 cache")
+        _check(t, name, torch.float32, ndim=3)
+        _need(tuple(t.shape) == tuple(k_cache.shape[:3]), f"{name} must be [num_blocks, n_kv, 16]")
+    return desc
+
+
+def kv_reshape_and_cache_fp8(key, value, k_cache, v_cache, k_scale, v_scale, slot_mapping, stream=None) -> None:
+    """Quantise new tokens' K/V to E4M3 (one fp32 scale per token and KV head) into their slots."""
+    torch = _torch()
+    desc = _check_fp8_pool(k_cache, v_cache, k_scale, v_scale)
+    _check(key, "key", torch.bfloat16, ndim=3, last=HEAD_DIM)
+    _check(value, "value", torch.bfloat16, ndim=3, last=HEAD_DIM)
+    _check(slot_mapping, "slot_mapping", torch.int32, ndim=1)
+    T = slot_mapping.shape[0]
+    _need(tuple(key.shape) == (T, desc.num_kv_heads, HEAD_DIM), "key must be [num_tokens, n_kv, 128]")
+    _need(tuple(value.shape) == tuple(key.shape), "value shape must equal key shape")
+    rc = load_library().kv_reshape_and_cache_fp8(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                                 _ptr(v_scale), _ptr(slot_mapping), int(T), ctypes.byref(desc),
+                                                 _stream(stream))
+    _raise("kv_reshape_and_cache_fp8", rc)
+
+
 def kv_copy_blocks(k_cache, v_cache, block_pairs, k_scale=None, v_scale=None, stream=None) -> None:
     """Copy block pairs {source, destination} (int32 CUDA tensor [n, 2]) in both caches
     (and, for an FP8 cache, in both scale arrays)."""
@@ -319,11 +354,20 @@ def paged_attention_workspace_size(num_seqs: int, num_q_heads: int, max_blocks_p
 
 
 def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale: float,
-                           workspace=None, partition_size: int = 0, stream=None):
-    """Decode attention; ``workspace`` (uint8 CUDA tensor) is allocated if None."""
+                           workspace=None, partition_size: int = 0, stream=None, window: int = 0,
+                           k_scale=None, v_scale=None):
+    """Decode attention; ``workspace`` (uint8 CUDA tensor) is allocated if None.
+    ``window`` > 0 calls paged_attention_decode_window (each row sees its newest
+    ``window`` keys only).  An FP8 pool (E4M3 codes) with ``k_scale`` /
+    ``v_scale`` calls paged_attention_decode_fp8."""
     torch = _torch()
     desc = cache_desc(k_cache)
-    _check(v_cache, "v_cache", torch.bfloat16, ndim=4)
+    fp8 = desc.dtype == PKV_DTYPE_FP8_E4M3
+    if fp8:
+        _check_fp8_pool(k_cache, v_cache, k_scale, v_scale)
+    else:
+        _need(k_scale is None and v_scale is None, "scales are only for an FP8 cache")
+        _check(v_cache, "v_cache", torch.bfloat16, ndim=4)
     _need(tuple(v_cache.shape) == tuple(k_cache.shape), "v_cache shape must equal k_cache shape")
     _check(q, "q", torch.bfloat16, ndim=3, last=HEAD_DIM)
     B, n_q, _ = q.shape
@@ -338,7 +382,22 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
         _need(nbytes > 0, "invalid sizes for paged_attention_decode")
         workspace = torch.zeros(nbytes, dtype=torch.uint8, device=q.device)  # status word starts clear
     _check(workspace, "workspace", torch.uint8, ndim=1)
-    rc = load_library().paged_attention_decode(
+    lib = load_library()
+    if fp8:
+        rc = lib.paged_attention_decode_fp8(
+            _ptr(out), _out_dtype(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+            _ptr(block_tables), _ptr(context_lens), int(B), int(n_q), max_blocks, float(scale), int(window),
+            int(partition_size), ctypes.byref(desc), _ptr(workspace), int(workspace.numel()), _stream(stream))
+        _raise("paged_attention_decode_fp8", rc)
+        return workspace
+    if window:
+        rc = lib.paged_attention_decode_window(
+            _ptr(out), _out_dtype(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+            _ptr(context_lens), int(B), int(n_q), max_blocks, float(scale), int(window), int(partition_size),
+            ctypes.byref(desc), _ptr(workspace), int(workspace.numel()), _stream(stream))
+        _raise("paged_attention_decode_window", rc)
+        return workspace
+    rc = lib.paged_attention_decode(
         _ptr(out), _out_dtype(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
         int(B), int(n_q), max_blocks, float(scale), int(partition_size), ctypes.byref(desc), _ptr(workspace),
         int(workspace.numel()), _stream(stream))

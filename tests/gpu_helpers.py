@@ -57,13 +57,14 @@ class DevWorkload:
     def append(self):
         P.kv_reshape_and_cache(self.new_key, self.new_value, self.k_cache, self.v_cache, self.slot_mapping)
 
-    def decode(self, batch: W.Batch, out_dtype=None, partition_size=0, workspace=None):
+    def decode(self, batch: W.Batch, out_dtype=None, partition_size=0, workspace=None, window=0, tables=None):
         t = torch()
         q = bf16_to_dev(batch.q)
         out = t.empty(q.shape, dtype=out_dtype or t.float32, device="cuda")
-        ws = P.paged_attention_decode(out, q, self.k_cache, self.v_cache, i32_to_dev(batch.block_tables),
+        tab = batch.block_tables if tables is None else tables
+        ws = P.paged_attention_decode(out, q, self.k_cache, self.v_cache, i32_to_dev(tab),
                                       i32_to_dev(batch.context_lens), self.wl.scale, workspace=workspace,
-                                      partition_size=partition_size)
+                                      partition_size=partition_size, window=window)
         return out, ws
 
     def prefill(self, batch: W.Batch, out_dtype=None, workspace=None):

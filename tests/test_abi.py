@@ -93,6 +93,49 @@ def test_decode_argument_errors(lib, kw, want):
     assert _decode(lib, desc(), **kw) == want
 
 
+def test_decode_window_argument_errors(lib):
+    c = desc()
+
+    def call(window, **kw):
+        a = dict(out=FAKE, out_dtype=1, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, cl=FAKE, B=4, nq=32, mb=8, scale=0.088,
+                 part=0, ws=FAKE, wsb=1 << 20)
+        a.update(kw)
+        return lib.paged_attention_decode_window(a["out"], a["out_dtype"], a["q"], a["k"], a["v"], a["bt"], a["cl"],
+                                                 a["B"], a["nq"], a["mb"], a["scale"], window, a["part"],
+                                                 ctypes.byref(c), a["ws"], a["wsb"], None)
+    assert call(0) == P.PKV_ERR_INVALID_ARG      # a window holds at least one key
+    assert call(-5) == P.PKV_ERR_INVALID_ARG
+    assert call(64, q=None) == P.PKV_ERR_INVALID_ARG
+    assert call(64, nq=96) == P.PKV_ERR_UNSUPPORTED
+    assert call(64, wsb=100) == P.PKV_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_fp8_argument_errors(lib):
+    c8, c16 = desc(dtype=P.PKV_DTYPE_FP8_E4M3), desc()
+    # cache write: needs an FP8 descriptor and both scale arrays
+    w = lambda c, **kw: lib.kv_reshape_and_cache_fp8(kw.get("k", FAKE), FAKE, FAKE, FAKE, kw.get("ks", FAKE), FAKE,
+                                                     FAKE, kw.get("T", 4), ctypes.byref(c), None)
+    assert w(c16) == P.PKV_ERR_UNSUPPORTED
+    assert w(c8, ks=None) == P.PKV_ERR_INVALID_ARG
+    assert w(c8, ks=FAKE + 4) == P.PKV_ERR_INVALID_ARG   # scales 16-byte aligned
+    assert w(c8, T=-1) == P.PKV_ERR_INVALID_ARG
+    assert w(c8, T=0) == P.PKV_OK
+
+    def d(c, **kw):
+        a = dict(ks=FAKE, vs=FAKE, window=0, wsb=1 << 20)
+        a.update(kw)
+        return lib.paged_attention_decode_fp8(FAKE, 1, FAKE, FAKE, FAKE, a["ks"], a["vs"], FAKE, FAKE, 4, 32, 8, 0.088,
+                                              a["window"], 0, ctypes.byref(c), FAKE, a["wsb"], None)
+    assert d(c16) == P.PKV_ERR_UNSUPPORTED
+    assert d(c8, ks=None) == P.PKV_ERR_INVALID_ARG
+    assert d(c8, vs=None) == P.PKV_ERR_INVALID_ARG
+    assert d(c8, window=-1) == P.PKV_ERR_INVALID_ARG
+    assert d(c8, wsb=100) == P.PKV_ERR_WORKSPACE_TOO_SMALL
+    # the workspace does not depend on the element type
+    assert lib.paged_attention_workspace_size(64, 32, 256, 0, ctypes.byref(c8)) == \
+        lib.paged_attention_workspace_size(64, 32, 256, 0, ctypes.byref(c16))
+
+
 @pytest.mark.parametrize("c,want", [
     (desc(bs=32), P.PKV_ERR_UNSUPPORTED),
     (desc(d=64), P.PKV_ERR_UNSUPPORTED),

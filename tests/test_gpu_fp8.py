@@ -1,0 +1,149 @@
+"""FP8 (E4M3) KV cache on the GPU against the fp64 oracle.
+
+The cache write must be bit-exact (codes and fp32 scales: the quantisation is
+taken in fp32, one correctly rounded operation per step, on both sides).  The
+decode over the FP8 pool is compared with the oracle's attention over the same
+dequantised values (code * scale) within the decode tolerances (max abs 4e-3,
+max rel 1e-2); the quantisation error itself is the cache's, not the kernel's.
+Source: "LLM 推理全过程的维度变化与核心公式", section "KV Cache 的形状与增长",
+INT8 / FP8 KV Cache item (per-token quantisation).
+
+Initial pools are the bf16 workloads' pools quantised row by row by the
+oracle, so unowned slots and the slots about to be appended hold the NaN code
+(their rows are bf16 NaN): reading any of them shows up as non-finite output.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from gpu_helpers import assert_close, bf16_to_dev, i32_to_dev, status_word, torch
+from paged_kv_cache_95_gb300 import pagedkv as P
+from paged_kv_cache_95_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(built_library):
+    P.load_library()
+
+
+def fp8_pool(wl):
+    """Quantise every slot of the workload's bf16 pool (slot order) with the oracle."""
+    nb, n_kv, bs, d = wl.k_cache.shape
+    rows_k = wl.k_cache.transpose(0, 2, 1, 3).reshape(nb * bs, n_kv, d)  # [slot][head][d]
+    rows_v = wl.v_cache.transpose(0, 2, 1, 3).reshape(nb * bs, n_kv, d)
+    kc = np.zeros((nb, n_kv, bs, d), dtype=np.uint8)
+    vc = np.zeros_like(kc)
+    ks = np.zeros((nb, n_kv, bs), dtype=np.float32)
+    vs = np.zeros_like(ks)
+    return oracle.kv_reshape_and_cache_fp8(rows_k, rows_v, kc, vc, ks, vs, np.arange(nb * bs, dtype=np.int32))
+
+
+class Fp8Dev:
+    def __init__(self, wl):
+        t = torch()
+        self.wl = wl
+        self.host = fp8_pool(wl)
+        self.k_cache, self.v_cache, self.k_scale, self.v_scale = (t.from_numpy(a.copy()).cuda() for a in self.host)
+        self.after = oracle.kv_reshape_and_cache_fp8(wl.new_key, wl.new_value, *self.host, wl.slot_mapping)
+
+    def append(self):
+        P.kv_reshape_and_cache_fp8(bf16_to_dev(self.wl.new_key), bf16_to_dev(self.wl.new_value), self.k_cache,
+                                   self.v_cache, self.k_scale, self.v_scale, i32_to_dev(self.wl.slot_mapping))
+
+    def decode(self, batch, window=0, partition_size=0, out_dtype=None):
+        t = torch()
+        q = bf16_to_dev(batch.q)
+        out = t.empty(q.shape, dtype=out_dtype or t.float32, device="cuda")
+        ws = P.paged_attention_decode(out, q, self.k_cache, self.v_cache, i32_to_dev(batch.block_tables),
+                                      i32_to_dev(batch.context_lens), self.wl.scale, window=window,
+                                      partition_size=partition_size, k_scale=self.k_scale, v_scale=self.v_scale)
+        return out, ws
+
+    def oracle(self, batch, window=0):
+        kc, vc, ks, vs = self.after
+        return oracle.paged_attention(batch.q, batch.cu_q_lens, kc, vc, batch.block_tables, batch.context_lens,
+                                      self.wl.scale, n_q=self.wl.n_q, window=window, k_scale=ks, v_scale=vs)
+
+
+_pools = {}
+
+
+def pool(name):
+    """The named workload on an FP8 pool, appended on the GPU (built once per module)."""
+    if name not in _pools:
+        d = Fp8Dev(W.make_workload(name, materialize_logical=False))
+        d.append()
+        _pools[name] = d
+    return _pools[name]
+
+
+@pytest.mark.parametrize("name", ["tiny", "llama3_8b_b64"])
+def test_fp8_cache_write_bit_exact(name):
+    d = pool(name)
+    torch().cuda.synchronize()
+    for dev, ref in zip((d.k_cache, d.v_cache, d.k_scale, d.v_scale), d.after):
+        got = dev.cpu().numpy()
+        assert np.array_equal(got.view(np.uint8), ref.view(np.uint8)), "FP8 cache write differs from the oracle"
+
+
+def test_fp8_cache_write_extreme_rows():
+    """Rows of zeros, tiny values, huge values and mixed signs quantise exactly as the oracle."""
+    t = torch()
+    rng = np.random.default_rng(50)
+    n_kv, T = 2, 12
+    x = rng.standard_normal((T, n_kv, 128)).astype(np.float32)
+    x[0] = 0.0
+    x[1] *= 1e-30
+    x[2] *= 1e30
+    x[3, 0] = 448.0
+    x[4, :, ::2] = -x[4, :, ::2] * 1000
+    x[5] = 1e-38
+    key, value = W.bf16_bits_from_f32(x), W.bf16_bits_from_f32(x[::-1].copy())
+    nb = 4
+    host = (np.zeros((nb, n_kv, 16, 128), np.uint8), np.zeros((nb, n_kv, 16, 128), np.uint8),
+            np.zeros((nb, n_kv, 16), np.float32), np.zeros((nb, n_kv, 16), np.float32))
+    slots = np.array([3, 17, 40, 63, 0, 5, 33, 34, 35, 50, -1, 62], dtype=np.int32)
+    ref = oracle.kv_reshape_and_cache_fp8(key, value, *host, slots)
+    dev = [t.from_numpy(a.copy()).cuda() for a in host]
+    P.kv_reshape_and_cache_fp8(bf16_to_dev(key), bf16_to_dev(value), *dev, i32_to_dev(slots))
+    t.cuda.synchronize()
+    for g, r in zip(dev, ref):
+        assert np.array_equal(g.cpu().numpy().view(np.uint8), r.view(np.uint8))
+
+
+@pytest.mark.parametrize("name", ["tiny", "llama3_8b_b64", "sweep_mqa", "sweep_mha"])
+def test_fp8_decode_parity(name):
+    d = pool(name)
+    wl = d.wl
+    out, ws = d.decode(wl.decode)
+    assert_close(out.cpu().numpy(), d.oracle(wl.decode), what=f"fp8 decode {name}")
+    assert status_word(ws) == 0
+
+
+@pytest.mark.parametrize("n_q,n_kv", [(32, 32), (32, 8), (64, 8), (32, 1), (128, 8)])
+def test_fp8_decode_edge_lengths_all_groups(n_q, n_kv):
+    ctx = [1, 2, 15, 16, 17, 31, 33, 255, 256, 257, 1000]
+    wl, batch = W.make_custom(n_q, n_kv, ctx, seed=400 + n_q + n_kv, materialize_logical=False)
+    d = Fp8Dev(wl)
+    d.append()
+    ref = d.oracle(batch)
+    for part in (0, 16, 256):
+        out, ws = d.decode(batch, partition_size=part)
+        assert_close(out.cpu().numpy(), ref, what=f"fp8 G={n_q // n_kv} part={part}")
+        assert status_word(ws) == 0
+
+
+def test_fp8_decode_window_and_bf16_out():
+    t = torch()
+    wl, batch = W.make_custom(32, 8, [40, 300, 1024, 17], seed=410, materialize_logical=False)
+    d = Fp8Dev(wl)
+    d.append()
+    for win in (16, 100):
+        out, ws = d.decode(batch, window=win)
+        assert_close(out.cpu().numpy(), d.oracle(batch, window=win), what=f"fp8 W={win}")
+    o16, _ = d.decode(batch, out_dtype=t.bfloat16)
+    o32, _ = d.decode(batch)
+    want = o32.to(t.bfloat16).view(t.int16).cpu().numpy().astype(np.int32)
+    assert np.max(np.abs(o16.view(t.int16).cpu().numpy().astype(np.int32) - want)) <= 1
