@@ -113,12 +113,13 @@ __global__ void __launch_bounds__(NW * 32)
     const uint32_t bar_base = smem_u32(smem) + NW * ST * kStage + (FP8 ? NW * ST * kStageScaleBytes : 0) + warp * ST * 8;
 
     if (lane == 0) {
-        for (int s = 0; s < ST; ++s) mbar_init(bar_base + 8 * s, 1);
+        for (int s = 0; s < ST; ++s) mbar_init(bar_base + 8 * s, FP8 ? kFp8StageArrivals : 1);
         fence_mbar_init();
     }
     __syncwarp();
+    constexpr int kIssueLanes = FP8 ? 8 : 1;  // lanes that take part in a stage's copies
 
-    // Lane 0: start the copies of this warp's i-th block into stage i % ST.
+    // Lanes < kIssueLanes: start the copies of this warp's i-th block into stage i % ST.
     auto issue = [&](int i) {
         const int s = i % ST;
         const int j = blk_begin + warp + NW * i;
@@ -126,11 +127,11 @@ __global__ void __launch_bounds__(NW * 32)
         if (static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_blocks)) phys = 0;  // masked below
         if constexpr (FP8)
             issue_block_copy_fp8(&kmap, &vmap, p.k_scale, p.v_scale, stage_base + s * kStage,
-                                 scale_base + s * kStageScaleBytes, bar_base + 8 * s, g, p.n_kv, phys);
+                                 scale_base + s * kStageScaleBytes, bar_base + 8 * s, g, p.n_kv, phys, lane);
         else
             issue_block_copy(&kmap, &vmap, stage_base + s * kStage, bar_base + 8 * s, g, phys);
     };
-    if (lane == 0)
+    if (lane < kIssueLanes)
         for (int i = 0; i < ST && i < nmine; ++i) issue(i);
 
     // ---- Q^T as the B operand (16 dims x 8 heads per k-step), kept in registers ----
@@ -175,7 +176,7 @@ __global__ void __launch_bounds__(NW * 32)
         consumed = i + 1;
 
         __syncwarp();
-        if (lane == 0 && i + ST < nmine) {
+        if (lane < kIssueLanes && i + ST < nmine) {
             fence_proxy_async_smem();
             issue(i + ST);
         }
@@ -188,6 +189,7 @@ __global__ void __launch_bounds__(NW * 32)
         for (int i = consumed; i < issued; ++i) mbar_wait(bar_base + 8 * (i % ST), (i / ST) & 1);
     }
 
+    if constexpr (FP8) fp8_finish(acc);
     // Full row sums of this warp: add the shares of the 8 lanes of a head column.
     acc.reduce_sums();
 
@@ -374,8 +376,9 @@ cudaError_t prepare_variant() {
                                 static_cast<int>(decode_smem_bytes({NW, ST})));
 }
 
-// The FP8 decode: 4 warps, 4 stages of 4 KB codes (+ 128 B of scales) per warp.
-constexpr int kFp8Warps = 4, kFp8Stages = 4;
+// The FP8 decode: 4 warps, 3 stages of 4 KB codes (+ 128 B of scales) per warp;
+// 128 registers and 52 KB of shared memory let 4 CTAs share an SM.
+constexpr int kFp8Warps = 4, kFp8Stages = 3;
 
 }  // namespace
 

@@ -22,6 +22,7 @@
 namespace pkv {
 
 constexpr uint32_t kTileBytes = kBlockSize * kHeadDim * 2;  // 4096 B: one (block, head) tile
+constexpr int kNoVexp = 1 << 20;                            // "no V scale seen yet"
 constexpr uint32_t kBoxBytes = kTileBytes / 2;              // 2048 B: 16 rows x 64 dims (128-B rows)
 constexpr uint32_t kStageBytes = 2 * kTileBytes;            // K tile + V tile
 
@@ -39,9 +40,12 @@ __device__ __forceinline__ void store_out(void *out, int32_t bf16, size_t idx, f
 struct DecodeAcc {
     float m0, m1, l0, l1;
     float o[8][4];
+    // FP8 only: O is held times 2^vexp (vexp set by the largest V scale seen so far).
+    int vexp;
     __device__ __forceinline__ void reset() {
         m0 = m1 = -INFINITY;
         l0 = l1 = 0.f;
+        vexp = kNoVexp;
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
     }
@@ -230,27 +234,40 @@ __device__ __forceinline__ int load_q_frag_fp8(uint32_t (&bq)[8][2], const void 
 // outside [lo, valid) are masked by index; their V codes and scales are never
 // used, so stale or NaN bytes in those slots do not reach the result.
 // fsl2 = scale * log2(e) * 2^-qexp.
+//
+// V scales are folded into the weights: P'' = p * sv * 2^vexp, with vexp the
+// running exponent that puts the largest V scale seen so far in [2^9, 2^10), so
+// P'' <= 2^10 and every weight that matters is a normal fp16 number; O is held
+// times 2^vexp (rescaled with the softmax correction when vexp drops) and
+// brought back by fp8_finish().  P'' goes in as an fp16 head + remainder.
 __device__ __forceinline__ void decode_block_fp8(DecodeAcc &acc, const uint32_t (&bq)[8][2], uint32_t kb,
                                                  uint32_t vb, uint32_t sc, int lo, int valid, float fsl2, int lane) {
     const int n = lane >> 2, q4 = lane & 3;
     const int key_a = n, key_b = n + 8;
     const bool in_a = key_a >= lo && key_a < valid, in_b = key_b >= lo && key_b < valid;
 
-    // S^T = K Q^T: key rows n and n + 8, code bytes 32*q4 .. +31 (chunks 2*q4, 2*q4+1, swizzled)
+    // S^T = K Q^T: key rows n and n + 8, code bytes 32*q4 .. +31 (chunks 2*q4, 2*q4+1, swizzled);
+    // two accumulators halve the dependent MMA chain.
     const uint32_t sw = static_cast<uint32_t>(n & 7);
-    const uint4 ka0 = lds128(kb + key_a * 128 + (((2 * q4) ^ sw) << 4));
-    const uint4 ka1 = lds128(kb + key_a * 128 + (((2 * q4 + 1) ^ sw) << 4));
-    const uint4 kb0 = lds128(kb + key_b * 128 + (((2 * q4) ^ sw) << 4));
-    const uint4 kb1 = lds128(kb + key_b * 128 + (((2 * q4 + 1) ^ sw) << 4));
-    const uint32_t wa[8] = {ka0.x, ka0.y, ka0.z, ka0.w, ka1.x, ka1.y, ka1.z, ka1.w};
-    const uint32_t wb[8] = {kb0.x, kb0.y, kb0.z, kb0.w, kb1.x, kb1.y, kb1.z, kb1.w};
-    float c[4] = {0.f, 0.f, 0.f, 0.f};
+    float c[4] = {0.f, 0.f, 0.f, 0.f}, c2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t a[4] = {e4m3x2_to_f16x2(wa[kk]), e4m3x2_to_f16x2(wb[kk]), e4m3x2_to_f16x2(wa[kk] >> 16),
-                               e4m3x2_to_f16x2(wb[kk] >> 16)};
-        mma_f16_16816(c, a, bq[kk][0], bq[kk][1]);
+    for (int h = 0; h < 2; ++h) {
+        const uint4 ka = lds128(kb + key_a * 128 + (((2 * q4 + h) ^ sw) << 4));
+        const uint4 kb4 = lds128(kb + key_b * 128 + (((2 * q4 + h) ^ sw) << 4));
+        const uint32_t wa[4] = {ka.x, ka.y, ka.z, ka.w}, wb[4] = {kb4.x, kb4.y, kb4.z, kb4.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int kk = 4 * h + i;
+            const uint32_t a[4] = {e4m3x2_to_f16x2(wa[i]), e4m3x2_to_f16x2(wb[i]), e4m3x2_to_f16x2(wa[i] >> 16),
+                                   e4m3x2_to_f16x2(wb[i] >> 16)};
+            if (i & 1)
+                mma_f16_16816(c2, a, bq[kk][0], bq[kk][1]);
+            else
+                mma_f16_16816(c, a, bq[kk][0], bq[kk][1]);
+        }
     }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) c[j] += c2[j];
 
     // Scores with each key's K scale; online softmax in the log2 domain.
     const float fa = lds_f32(sc + 4 * key_a) * fsl2, fb = lds_f32(sc + 4 * key_b) * fsl2;
@@ -259,19 +276,34 @@ __device__ __forceinline__ void decode_block_fp8(DecodeAcc &acc, const uint32_t 
     const float s10 = in_b ? c[2] * fb : -INFINITY;
     const float s11 = in_b ? c[3] * fb : -INFINITY;
     float bm0 = fmaxf(s00, s10), bm1 = fmaxf(s01, s11);
+    const float sva = in_a ? lds_f32(sc + kScaleBytes + 4 * key_a) : 0.f;
+    const float svb = in_b ? lds_f32(sc + kScaleBytes + 4 * key_b) : 0.f;
+    float svmax = fmaxf(sva, svb);
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
         bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
         bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
+        svmax = fmaxf(svmax, __shfl_xor_sync(0xffffffffu, svmax, off));
     }
     const float mn0 = fmaxf(acc.m0, bm0), mn1 = fmaxf(acc.m1, bm1);
     const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
     const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float al0 = fast_exp2(acc.m0 - mu0), al1 = fast_exp2(acc.m1 - mu1);
+    const float as0 = fast_exp2(acc.m0 - mu0), as1 = fast_exp2(acc.m1 - mu1);  // softmax correction
+    float al0 = as0, al1 = as1;                                                  // ... and O's
+    // A larger V scale lowers vexp: O (held times 2^vexp) shrinks by the same power of two.
+    if (svmax > 0.f) {
+        const int ve = 9 - (static_cast<int>((__float_as_uint(svmax) >> 23) & 0xff) - 127);
+        if (ve < acc.vexp) {
+            const float f = acc.vexp == kNoVexp ? 1.f : ldexpf(1.f, ve - acc.vexp);
+            al0 *= f;
+            al1 *= f;
+            acc.vexp = ve;
+        }
+    }
     const float p00 = fast_exp2(s00 - mu0), p01 = fast_exp2(s01 - mu1);
     const float p10 = fast_exp2(s10 - mu0), p11 = fast_exp2(s11 - mu1);
-    acc.l0 = acc.l0 * al0 + p00 + p10;
-    acc.l1 = acc.l1 * al1 + p01 + p11;
+    acc.l0 = acc.l0 * as0 + p00 + p10;
+    acc.l1 = acc.l1 * as1 + p01 + p11;
     acc.m0 = mn0;
     acc.m1 = mn1;
 #pragma unroll
@@ -282,19 +314,9 @@ __device__ __forceinline__ void decode_block_fp8(DecodeAcc &acc, const uint32_t 
         acc.o[mt][3] *= al1;
     }
 
-    // V scales folded into P: P'' = p * sv * 2^r, with 2^r putting the block's
-    // largest (unmasked) scale in [2^9, 2^10) so that P'' is a normal fp16 number
-    // for every weight that matters; P'' as an fp16 head + remainder.  Each MMA
-    // pair accumulates into a fresh tile that is added to O times 2^-r.
-    const float sva = in_a ? lds_f32(sc + kScaleBytes + 4 * key_a) : 0.f;
-    const float svb = in_b ? lds_f32(sc + kScaleBytes + 4 * key_b) : 0.f;
-    float svmax = fmaxf(sva, svb);
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) svmax = fmaxf(svmax, __shfl_xor_sync(0xffffffffu, svmax, off));
-    int r = 0;
-    if (svmax > 0.f) r = min(100, max(-100, 9 - (static_cast<int>((__float_as_uint(svmax) >> 23) & 0xff) - 127)));
-    const float up = ldexpf(1.f, r), down = ldexpf(1.f, -r);
-    const float q00 = p00 * sva * up, q01 = p01 * sva * up, q10 = p10 * svb * up, q11 = p11 * svb * up;
+    const float up = acc.vexp == kNoVexp ? 0.f : ldexpf(1.f, acc.vexp);
+    const float wa2 = sva * up, wb2 = svb * up;
+    const float q00 = p00 * wa2, q01 = p01 * wa2, q10 = p10 * wb2, q11 = p11 * wb2;
     const uint32_t ph0 = pack_f16x2(q00, q01), ph1 = pack_f16x2(q10, q11);
     const float2 h0 = unpack_f16x2(ph0), h1 = unpack_f16x2(ph1);
     const uint32_t pl0 = pack_f16x2(q00 - h0.x, q01 - h0.y), pl1 = pack_f16x2(q10 - h1.x, q11 - h1.y);
@@ -324,26 +346,41 @@ __device__ __forceinline__ void decode_block_fp8(DecodeAcc &acc, const uint32_t 
         const uint32_t pb = __byte_perm(w2[mt >> 1], w3[mt >> 1], sel);
         const uint32_t a[4] = {e4m3x2_to_f16x2(pa), e4m3x2_to_f16x2(pa >> 16), e4m3x2_to_f16x2(pb),
                                e4m3x2_to_f16x2(pb >> 16)};
-        float t[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_f16_16816(t, a, pb0, pb1);
-        mma_f16_16816(t, a, pr0, pr1);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc.o[mt][j] = fmaf(t[j], down, acc.o[mt][j]);
+        mma_f16_16816(acc.o[mt], a, pb0, pb1);
+        mma_f16_16816(acc.o[mt], a, pr0, pr1);
     }
 }
 
-// Copies of one (block, head) FP8 tile pair and its scales into a stage: two
-// 2 KB TMA boxes and two 64 B bulk copies, completing on `bar`.
+// After the last FP8 block: O back to its true scale (it is held times 2^vexp).
+__device__ __forceinline__ void fp8_finish(DecodeAcc &acc) {
+    if (acc.vexp == kNoVexp) return;  // no key seen: O is zero
+    const float down = ldexpf(1.f, -acc.vexp);
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc.o[mt][j] *= down;
+}
+
+// Copies of one (block, head) FP8 tile pair and its scales into a stage, run by
+// lanes 0-7 of the warp: lane 0 sends the two 2 KB code tiles through the TMA unit
+// (4 KB of transactions on `bar`); lanes 0-3 / 4-7 each copy 16 B of the K / V scale
+// row with cp.async and arrive on `bar` when it lands (so `bar` counts 1 + 8
+// arrivals per phase).  Keeping the 64 B rows off the TMA unit halves the TMA
+// operations per block.
+constexpr uint32_t kFp8StageArrivals = 1 + 8;
 __device__ __forceinline__ void issue_block_copy_fp8(const CUtensorMap *kmap, const CUtensorMap *vmap,
                                                      const float *k_scale, const float *v_scale, uint32_t dst,
                                                      uint32_t dst_scale, uint32_t bar, int kv_head, int n_kv,
-                                                     int phys_block) {
-    mbar_arrive_expect_tx(bar, kStageBytes8 + kStageScaleBytes);
-    tma_load_4d(dst, kmap, bar, 0, 0, kv_head, phys_block);
-    tma_load_4d(dst + kTileBytes8, vmap, bar, 0, 0, kv_head, phys_block);
+                                                     int phys_block, int lane) {
+    if (lane == 0) {
+        mbar_arrive_expect_tx(bar, kStageBytes8);
+        tma_load_4d(dst, kmap, bar, 0, 0, kv_head, phys_block);
+        tma_load_4d(dst + kTileBytes8, vmap, bar, 0, 0, kv_head, phys_block);
+    }
     const size_t row = (static_cast<size_t>(phys_block) * n_kv + kv_head) * kBlockSize;
-    bulk_copy_g2s(dst_scale, k_scale + row, kScaleBytes, bar);
-    bulk_copy_g2s(dst_scale + kScaleBytes, v_scale + row, kScaleBytes, bar);
+    const int part = lane & 3;
+    cp_async_16(dst_scale + (lane < 4 ? 0u : kScaleBytes) + 16u * part, (lane < 4 ? k_scale : v_scale) + row + 4 * part);
+    cp_async_mbar_arrive_noinc(bar);
 }
 
 }  // namespace pkv

@@ -208,6 +208,18 @@ __device__ __forceinline__ float2 unpack_f16x2(uint32_t x) {
     return make_float2(lo, hi);
 }
 
+// 16-byte asynchronous copy global -> shared (LSU path, not the TMA unit).
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src))
+                 : "memory");
+}
+
+// One arrival on `bar` once this thread's earlier cp.async copies have landed; the
+// arrival is not added to the expected count, so the barrier's count includes it.
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 // 1-D bulk copy global -> shared, completing `bytes` transactions on `bar`
 // (both addresses 16-byte aligned, bytes a multiple of 16).
 __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
