@@ -372,6 +372,38 @@ PKV_API int paged_attention_prefill_chunk(void *out, int32_t out_dtype, const vo
                                   void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * paged_attention_verify -- attention of k draft positions per sequence
+ * (speculative decoding's verification step).
+ *
+ * A draft model proposes k tokens and the target model checks all k positions
+ * in one pass, turning k decode steps into one k-row computation
+ * ("LLM 推理全过程的维度变化与核心公式", section "工程优化怎么嵌进公式",
+ * Speculative Decoding; xinc.fun archive 233, section 7).  The k tokens' K/V
+ * are appended first, so ctx_b counts them; row i (0 <= i < k) of sequence b
+ * sits at position ctx_b - k + i and sees keys j <= ctx_b - k + i (the causal
+ * rule among the draft tokens; row k - 1 is an ordinary decode row).  The
+ * acceptance rule itself (sampling) is not part of this library.
+ *
+ *   q, out    : [num_seqs * q_per_seq][num_q_heads][head_dim]; sequence b owns
+ *               rows b * q_per_seq .. b * q_per_seq + q_per_seq - 1
+ *   q_per_seq : k, 1 .. 16
+ * Runs on the decode kernel (K/V read once per KV head, the CTA's 8 MMA columns
+ * holding the G heads x k positions) when G * k <= 8, else on the tcgen05
+ * prefill kernel (then q and out must be 16-B aligned).  A sequence with
+ * ctx < k sets PKV_STATUS_BAD_Q_LEN and gets zero rows.
+ * Workspace: paged_attention_verify_workspace_size() bytes, zero-filled once.
+ * Errors: as paged_attention_decode; PKV_ERR_INVALID_ARG for q_per_seq outside 1..16.
+ */
+PKV_API size_t paged_attention_verify_workspace_size(int32_t num_seqs, int32_t q_per_seq, int32_t num_q_heads,
+                                                     int32_t max_blocks_per_seq, int32_t partition_size,
+                                                     const pkv_cache_desc *cache);
+PKV_API int paged_attention_verify(void *out, int32_t out_dtype, const void *q, int32_t q_per_seq, const void *k_cache,
+                                   const void *v_cache, const int32_t *block_tables, const int32_t *context_lens,
+                                   int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq, float scale,
+                                   int32_t partition_size, const pkv_cache_desc *cache, void *workspace,
+                                   size_t workspace_bytes, void *stream);
+
+/*
  * ---- Host block manager ---------------------------------------------------------
  * Hands out the pool's physical blocks to sequences and emits the block tables
  * and slot mappings the kernels above consume.  Sources: "注意力演进与推理流程",

@@ -26,6 +26,7 @@ from .pagedkv import (  # noqa: F401
     paged_attention_decode_static_scratch,
     paged_attention_prefill_chunk,
     paged_attention_prefill_workspace_size,
+    paged_attention_verify,
     paged_attention_workspace_size,
     status_string,
     version,

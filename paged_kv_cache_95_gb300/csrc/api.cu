@@ -185,7 +185,9 @@ struct DecodePlan {
     size_t off_cnt, off_m, off_l, off_o, total;
 };
 
-DecodePlan plan_decode(int32_t num_seqs, int32_t n_q, int32_t n_kv, int32_t max_blocks, int32_t part_blocks) {
+// rows_per_seq: query rows per sequence (1 for decode, q_per_seq for verify).
+DecodePlan plan_decode(int32_t num_seqs, int32_t n_q, int32_t n_kv, int32_t max_blocks, int32_t part_blocks,
+                       int32_t rows_per_seq = 1) {
     DecodePlan pl{};
     pl.part_blocks = part_blocks >= max_blocks ? max_blocks : part_blocks;
     pl.max_parts = (max_blocks + pl.part_blocks - 1) / pl.part_blocks;
@@ -196,7 +198,7 @@ DecodePlan plan_decode(int32_t num_seqs, int32_t n_q, int32_t n_kv, int32_t max_
     }
     const int32_t G = n_q / n_kv;
     const int32_t groups = n_kv * (G <= 8 ? 1 : G / 8);  // CTAs per sequence and partition
-    const size_t rows = static_cast<size_t>(num_seqs) * n_q * pl.max_parts;
+    const size_t rows = static_cast<size_t>(num_seqs) * rows_per_seq * n_q * pl.max_parts;
     pl.off_m = pl.off_cnt + align_up(static_cast<size_t>(num_seqs) * groups * 4, 256);
     pl.off_l = pl.off_m + align_up(rows * 4, 256);
     pl.off_o = pl.off_l + align_up(rows * 4, 256);
@@ -478,18 +480,21 @@ size_t paged_attention_prefill_workspace_size(int32_t num_seqs, int32_t num_q_he
     return kStatusBytes;
 }
 
-int paged_attention_prefill_chunk(void *out, int32_t out_dtype, const void *q, const int32_t *cu_q_lens,
-                                  int32_t max_q_len, int32_t total_q_rows, const void *k_cache, const void *v_cache,
-                                  const int32_t *block_tables, const int32_t *context_lens, int32_t num_seqs,
-                                  int32_t num_q_heads, int32_t max_blocks_per_seq, float scale,
-                                  const pkv_cache_desc *cache, void *workspace, size_t workspace_bytes,
-                                  void *stream) {
+namespace {
+
+// Shared by the prefill-chunk and verify entry points.  cu_q_lens null: every sequence
+// has uniform_q_len rows (sequence b owns rows b * uniform_q_len ..).
+int prefill_impl(void *out, int32_t out_dtype, const void *q, const int32_t *cu_q_lens, int32_t uniform_q_len,
+                 int32_t max_q_len, int32_t total_q_rows, const void *k_cache, const void *v_cache,
+                 const int32_t *block_tables, const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                 int32_t max_blocks_per_seq, float scale, const pkv_cache_desc *cache, void *workspace,
+                 size_t workspace_bytes, void *stream) {
     if (int rc = check_cache(cache)) return rc;
     if (num_q_heads < 1 || num_q_heads % cache->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
     const int32_t G = num_q_heads / cache->num_kv_heads;
     // A 128-row MMA tile packs 128 / G query positions x the G heads of one KV group.
     if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return PKV_ERR_UNSUPPORTED;
-    if (!out || !q || !cu_q_lens || !k_cache || !v_cache || !block_tables || !context_lens)
+    if (!out || !q || (!cu_q_lens && uniform_q_len < 1) || !k_cache || !v_cache || !block_tables || !context_lens)
         return PKV_ERR_INVALID_ARG;
     if (out_dtype != PKV_DTYPE_FLOAT32 && out_dtype != PKV_DTYPE_BF16) return PKV_ERR_UNSUPPORTED;
     if (num_seqs < 1 || num_seqs > 65535 || max_blocks_per_seq < 1 || max_q_len < 0 || total_q_rows < 0)
@@ -521,6 +526,7 @@ int paged_attention_prefill_chunk(void *out, int32_t out_dtype, const void *q, c
     pkv::PrefillParams p{};
     p.out = out;
     p.cu_q_lens = cu_q_lens;
+    p.uniform_q_len = cu_q_lens ? 0 : uniform_q_len;
     p.block_tables = block_tables;
     p.context_lens = context_lens;
     p.status = static_cast<uint32_t *>(workspace);
@@ -539,6 +545,121 @@ int paged_attention_prefill_chunk(void *out, int32_t out_dtype, const void *q, c
         return PKV_ERR_CUDA;
     return PKV_OK;
 }
+
+}  // namespace
+
+int paged_attention_prefill_chunk(void *out, int32_t out_dtype, const void *q, const int32_t *cu_q_lens,
+                                  int32_t max_q_len, int32_t total_q_rows, const void *k_cache, const void *v_cache,
+                                  const int32_t *block_tables, const int32_t *context_lens, int32_t num_seqs,
+                                  int32_t num_q_heads, int32_t max_blocks_per_seq, float scale,
+                                  const pkv_cache_desc *cache, void *workspace, size_t workspace_bytes,
+                                  void *stream) {
+    if (!cu_q_lens) return PKV_ERR_INVALID_ARG;
+    return prefill_impl(out, out_dtype, q, cu_q_lens, 0, max_q_len, total_q_rows, k_cache, v_cache, block_tables,
+                        context_lens, num_seqs, num_q_heads, max_blocks_per_seq, scale, cache, workspace,
+                        workspace_bytes, stream);
+}
+
+namespace {
+constexpr int32_t kMaxVerifyRows = 16;  // draft positions per sequence
+
+// Verify runs on the decode kernel when a CTA's 8 MMA columns hold the group's
+// (position, head) pairs, else on the prefill kernel.
+bool verify_on_decode(int32_t q_per_seq, int32_t G) { return static_cast<int64_t>(q_per_seq) * G <= 8; }
+}  // namespace
+
+size_t paged_attention_verify_workspace_size(int32_t num_seqs, int32_t q_per_seq, int32_t num_q_heads,
+                                             int32_t max_blocks_per_seq, int32_t partition_size,
+                                             const pkv_cache_desc *cache) {
+    if (check_cache(cache) != PKV_OK || num_seqs < 1 || max_blocks_per_seq < 1) return 0;
+    if (q_per_seq < 1 || q_per_seq > kMaxVerifyRows) return 0;
+    if (check_group(num_q_heads, cache->num_kv_heads) != PKV_OK) return 0;
+    if (partition_size < 0 || partition_size % kBlockSize != 0) return 0;
+    const int32_t G = num_q_heads / cache->num_kv_heads;
+    if (!verify_on_decode(q_per_seq, G)) return kStatusBytes;
+    const int32_t pb = partition_size > 0 ? partition_size / kBlockSize : kMinPartBlocks;
+    return plan_decode(num_seqs, num_q_heads, cache->num_kv_heads, max_blocks_per_seq, pb, q_per_seq).total;
+}
+
+int paged_attention_verify(void *out, int32_t out_dtype, const void *q, int32_t q_per_seq, const void *k_cache,
+                           const void *v_cache, const int32_t *block_tables, const int32_t *context_lens,
+                           int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq, float scale,
+                           int32_t partition_size, const pkv_cache_desc *cache, void *workspace,
+                           size_t workspace_bytes, void *stream) {
+    if (int rc = check_cache(cache)) return rc;
+    if (int rc = check_group(num_q_heads, cache->num_kv_heads)) return rc;
+    if (q_per_seq < 1 || q_per_seq > kMaxVerifyRows) return PKV_ERR_INVALID_ARG;
+    const int32_t G = num_q_heads / cache->num_kv_heads;
+    if (!verify_on_decode(q_per_seq, G)) {
+        // Prefill kernel, uniform rows: sequence b owns q rows b * q_per_seq .. + q_per_seq - 1.
+        if (static_cast<int64_t>(num_seqs) * q_per_seq > INT32_MAX) return PKV_ERR_INVALID_ARG;
+        return prefill_impl(out, out_dtype, q, nullptr, q_per_seq, q_per_seq, num_seqs * q_per_seq, k_cache, v_cache,
+                            block_tables, context_lens, num_seqs, num_q_heads, max_blocks_per_seq, scale, cache,
+                            workspace, workspace_bytes, stream);
+    }
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PKV_ERR_INVALID_ARG;
+    if (out_dtype != PKV_DTYPE_FLOAT32 && out_dtype != PKV_DTYPE_BF16) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs < 1 || num_seqs > 65535 || max_blocks_per_seq < 1) return PKV_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(max_blocks_per_seq) * kBlockSize > INT32_MAX) return PKV_ERR_INVALID_ARG;
+    if (partition_size < 0 || partition_size % kBlockSize != 0) return PKV_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 4) || !aligned(out, 4) ||
+        !aligned(block_tables, 4) || !aligned(context_lens, 4))
+        return PKV_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 256)) return PKV_ERR_INVALID_ARG;
+    if (workspace_bytes < paged_attention_verify_workspace_size(num_seqs, q_per_seq, num_q_heads, max_blocks_per_seq,
+                                                                partition_size, cache))
+        return PKV_ERR_WORKSPACE_TOO_SMALL;
+
+    const int32_t n_kv = cache->num_kv_heads;
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return PKV_ERR_CUDA;
+    const int sms = sm_count(dev);
+    const int32_t pb = partition_size > 0 ? partition_size / kBlockSize
+                                          : auto_part_blocks(num_seqs, n_kv, 1, max_blocks_per_seq, sms);
+    const DecodePlan pl = plan_decode(num_seqs, num_q_heads, n_kv, max_blocks_per_seq, pb, q_per_seq);
+    if (workspace_bytes < pl.total) return PKV_ERR_WORKSPACE_TOO_SMALL;
+
+    CUtensorMap kmap, vmap;
+    if (!encode_pool_map(&kmap, k_cache, cache->num_blocks, n_kv) ||
+        !encode_pool_map(&vmap, v_cache, cache->num_blocks, n_kv))
+        return PKV_ERR_CUDA;
+    const pkv::DecodeVariant var = decode_variant();
+    const int vi = variant_index(var);
+    std::call_once(g_decode_prepared[dev][vi], [&] { g_decode_prep_err[dev][vi] = pkv::decode_prepare_device(var); });
+    if (g_decode_prep_err[dev][vi] != cudaSuccess) return PKV_ERR_CUDA;
+
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    pkv::DecodeParamsVerify p{};
+    p.q = q;
+    p.out = out;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.status = reinterpret_cast<uint32_t *>(ws);
+    p.part_m = pl.max_parts > 1 ? reinterpret_cast<float *>(ws + pl.off_m) : nullptr;
+    p.part_l = pl.max_parts > 1 ? reinterpret_cast<float *>(ws + pl.off_l) : nullptr;
+    p.part_o = pl.max_parts > 1 ? reinterpret_cast<float *>(ws + pl.off_o) : nullptr;
+    p.counters = pl.max_parts > 1 ? reinterpret_cast<uint32_t *>(ws + pl.off_cnt) : nullptr;
+    p.num_seqs = num_seqs;
+    p.n_q = num_q_heads;
+    p.n_kv = n_kv;
+    p.group = G;
+    p.heads_per_cta = G * q_per_seq;  // the CTA's columns: q_per_seq positions x G heads
+    p.head_splits = 1;
+    p.max_blocks = max_blocks_per_seq;
+    p.num_blocks = cache->num_blocks;
+    p.part_blocks = pl.part_blocks;
+    p.max_parts = pl.max_parts;
+    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    p.out_bf16 = out_dtype == PKV_DTYPE_BF16;
+    p.fused_merge = fused_merge() ? 1 : 0;
+    p.window = 0;
+    p.q_per_seq = q_per_seq;
+    return pkv::launch_paged_verify(kmap, vmap, p, var, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PKV_OK
+               : PKV_ERR_CUDA;
+}
+
 
 // ---- decode without a caller workspace ------------------------------------------
 // The scratch that paged_attention_decode would take as its workspace, as one

@@ -58,10 +58,14 @@ namespace pkv {
 
 namespace {
 
-template <int NW, int ST, bool FP8>
+template <bool FP8, bool VERIFY>
+using DecodeParamsT =
+    std::conditional_t<FP8, DecodeParamsFp8, std::conditional_t<VERIFY, DecodeParamsVerify, DecodeParams>>;
+
+template <int NW, int ST, bool FP8, bool VERIFY = false>
 __global__ void __launch_bounds__(NW * 32)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                        const std::conditional_t<FP8, DecodeParamsFp8, DecodeParams> p) {
+                        const DecodeParamsT<FP8, VERIFY> p) {
     constexpr uint32_t kStage = FP8 ? kStageBytes8 : kStageBytes;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem =
@@ -75,6 +79,15 @@ __global__ void __launch_bounds__(NW * 32)
     const int g = hs / p.head_splits;
     const int hpc = p.heads_per_cta;
     const int h0 = g * p.group + (hs - g * p.head_splits) * hpc;
+    // q / out row (in units of 128-element head rows) of CTA column c: decode, head h0 + c of
+    // sequence b; verify, position c / G of sequence b's q_per_seq rows, head g * G + c % G.
+    auto col_row = [&](int c) -> size_t {
+        if constexpr (VERIFY)
+            return (static_cast<size_t>(b) * p.q_per_seq + c / p.group) * p.n_q + static_cast<size_t>(g) * p.group +
+                   c % p.group;
+        else
+            return static_cast<size_t>(b) * p.n_q + h0 + c;
+    };
 
     if (threadIdx.x == 0) {
         prefetch_tensormap(&kmap);
@@ -90,11 +103,16 @@ __global__ void __launch_bounds__(NW * 32)
         if (part == 0 && threadIdx.x == 0 && p.status) atomicOr(p.status, kStatusBadContextLen);
         ctx = ctx < 1 ? 0 : max_ctx;
     }
+    if constexpr (VERIFY) {
+        if (ctx > 0 && ctx < p.q_per_seq) {  // the rows being verified must already be in the cache
+            if (part == 0 && threadIdx.x == 0 && p.status) atomicOr(p.status, kStatusBadQLen);
+            ctx = 0;
+        }
+    }
     if (ctx == 0) {
         if (part == 0)
             for (int i = threadIdx.x; i < hpc * kHeadDim; i += NW * 32)
-                store_out(p.out, p.out_bf16, (static_cast<size_t>(b) * p.n_q + h0 + (i >> 7)) * kHeadDim + (i & 127),
-                          0.f);
+                store_out(p.out, p.out_bf16, col_row(i >> 7) * kHeadDim + (i & 127), 0.f);
         return;
     }
     const int nblocks = (ctx + kBlockSize - 1) / kBlockSize;
@@ -142,8 +160,16 @@ __global__ void __launch_bounds__(NW * 32)
     if constexpr (FP8) {
         const int qexp = load_q_frag_fp8(bq, p.q, static_cast<size_t>(b) * p.n_q + h0, hpc, lane);
         sl2 *= ldexpf(1.f, -qexp);
+    } else if constexpr (VERIFY) {
+        load_q_frag_row(bq, p.q, col_row(n), n < hpc, lane);
     } else {
         load_q_frag(bq, p.q, static_cast<size_t>(b) * p.n_q + h0, hpc, lane);
+    }
+    // Verify: the absolute causal bound (exclusive) of this lane's columns 2*q4 and 2*q4 + 1.
+    int pos_end0 = 0, pos_end1 = 0;
+    if constexpr (VERIFY) {
+        pos_end0 = ctx - p.q_per_seq + (2 * q4) / p.group + 1;
+        pos_end1 = ctx - p.q_per_seq + (2 * q4 + 1) / p.group + 1;
     }
 
     DecodeAcc acc;
@@ -171,6 +197,9 @@ __global__ void __launch_bounds__(NW * 32)
         const uint32_t kb = stage_base + s * kStage;
         if constexpr (FP8)
             decode_block_fp8(acc, bq, kb, kb + kTileBytes8, scale_base + s * kStageScaleBytes, lo, valid, sl2, lane);
+        else if constexpr (VERIFY)
+            decode_block(acc, bq, kb, kb + kTileBytes, lo, valid, sl2, lane, pos_end0 - j * kBlockSize,
+                         pos_end1 - j * kBlockSize);
         else
             decode_block(acc, bq, kb, kb + kTileBytes, lo, valid, sl2, lane);
         consumed = i + 1;
@@ -230,7 +259,7 @@ __global__ void __launch_bounds__(NW * 32)
             L += f * red_l[w * 8 + hh];
             O += f * red_o[(w * 8 + hh) * kHeadDim + d];
         }
-        const size_t row = static_cast<size_t>(b) * p.n_q + h0 + hh;
+        const size_t row = col_row(hh);
         if (nparts == 1) {
             store_out(p.out, p.out_bf16, row * kHeadDim + d, L > 0.f ? O / L : 0.f);
         } else {
@@ -260,7 +289,7 @@ __global__ void __launch_bounds__(NW * 32)
 
     // Warp w folds the partitions p = w, w + NW, ...; lane owns dims 4*lane .. 4*lane+3.
     for (int hh = 0; hh < hpc; ++hh) {
-        const size_t base = (static_cast<size_t>(b) * p.n_q + h0 + hh) * p.max_parts;
+        const size_t base = col_row(hh) * p.max_parts;
         float M = -INFINITY;
         for (int i = lane; i < nparts; i += 32) M = fmaxf(M, __ldcg(p.part_m + base + i));
 #pragma unroll
@@ -289,8 +318,7 @@ __global__ void __launch_bounds__(NW * 32)
             L += red_l[w * 8 + hh];
             O += red_o[(w * 8 + hh) * kHeadDim + d];
         }
-        store_out(p.out, p.out_bf16, (static_cast<size_t>(b) * p.n_q + h0 + hh) * kHeadDim + d,
-                  L > 0.f ? O / L : 0.f);
+        store_out(p.out, p.out_bf16, col_row(hh) * kHeadDim + d, L > 0.f ? O / L : 0.f);
     }
     if (threadIdx.x == 0) p.counters[static_cast<size_t>(b) * gridDim.y + hs] = 0u;  // ready for the next call
 }
@@ -304,12 +332,13 @@ namespace {
 // the partitions p = w, w + 8, ...; lane owns dims 4*lane .. 4*lane + 3.
 constexpr int kMergeWarps = 8;
 
-__global__ void __launch_bounds__(kMergeWarps * 32) lse_merge_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kMergeWarps * 32) lse_merge_kernel(const DecodeParams p, int rows_per_seq) {
     __shared__ float red_o[kMergeWarps][kHeadDim];
     __shared__ float red_x[kMergeWarps];
     __shared__ float red_l[kMergeWarps];
     const int h = blockIdx.x;
-    const int b = blockIdx.y;
+    const int r = blockIdx.y;            // q row r of the call (decode: r = b)
+    const int b = r / rows_per_seq;      // its sequence
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     griddep_launch_dependents();
     griddep_wait();  // the decode grid's partials
@@ -319,7 +348,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lse_merge_kernel(const Decod
     const int first_blk = ((p.window > 0 && ctx > p.window) ? ctx - p.window : 0) / kBlockSize;
     const int nparts = ((ctx + kBlockSize - 1) / kBlockSize - first_blk + p.part_blocks - 1) / p.part_blocks;
     if (nparts <= 1) return;  // written directly by the decode kernel
-    const size_t base = (static_cast<size_t>(b) * p.n_q + h) * p.max_parts;
+    const size_t base = (static_cast<size_t>(r) * p.n_q + h) * p.max_parts;
     float M = -INFINITY;
     for (int i = threadIdx.x; i < nparts; i += kMergeWarps * 32) M = fmaxf(M, __ldcg(p.part_m + base + i));
 #pragma unroll
@@ -352,27 +381,32 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lse_merge_kernel(const Decod
             Ls += red_l[w];
             O += red_o[w][threadIdx.x];
         }
-        store_out(p.out, p.out_bf16, (static_cast<size_t>(b) * p.n_q + h) * kHeadDim + threadIdx.x,
+        store_out(p.out, p.out_bf16, (static_cast<size_t>(r) * p.n_q + h) * kHeadDim + threadIdx.x,
                   Ls > 0.f ? O / Ls : 0.f);
     }
 }
 
-template <int NW, int ST, bool FP8 = false>
-cudaError_t launch_variant(const CUtensorMap &kmap, const CUtensorMap &vmap,
-                           const std::conditional_t<FP8, DecodeParamsFp8, DecodeParams> &p, cudaStream_t stream) {
+template <int NW, int ST, bool FP8 = false, bool VERIFY = false>
+cudaError_t launch_variant(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParamsT<FP8, VERIFY> &p,
+                           cudaStream_t stream) {
     const dim3 grid(p.max_parts, p.n_kv * p.head_splits, p.num_seqs);
-    cudaError_t e = launch_pdl(paged_decode_kernel<NW, ST, FP8>, grid, dim3(NW * 32),
+    cudaError_t e = launch_pdl(paged_decode_kernel<NW, ST, FP8, VERIFY>, grid, dim3(NW * 32),
                                FP8 ? decode_fp8_smem_bytes() : decode_smem_bytes({NW, ST}), stream, kmap, vmap, p);
     if (e != cudaSuccess) return e;
+    int rows_per_seq = 1;
+    if constexpr (VERIFY) rows_per_seq = p.q_per_seq;
     if (p.max_parts > 1 && !p.fused_merge)
-        e = launch_pdl(lse_merge_kernel, dim3(p.n_q, p.num_seqs), dim3(kMergeWarps * 32), 0, stream,
-                       static_cast<const DecodeParams &>(p));
+        e = launch_pdl(lse_merge_kernel, dim3(p.n_q, p.num_seqs * rows_per_seq), dim3(kMergeWarps * 32), 0, stream,
+                       static_cast<const DecodeParams &>(p), rows_per_seq);
     return e;
 }
 
 template <int NW, int ST>
 cudaError_t prepare_variant() {
-    return cudaFuncSetAttribute(paged_decode_kernel<NW, ST, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<NW, ST, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(decode_smem_bytes({NW, ST})));
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(paged_decode_kernel<NW, ST, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(decode_smem_bytes({NW, ST})));
 }
 
@@ -411,6 +445,15 @@ cudaError_t decode_fp8_prepare_device() {
 cudaError_t launch_paged_decode_fp8(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParamsFp8 &p,
                                     cudaStream_t stream) {
     return launch_variant<kFp8Warps, kFp8Stages, true>(kmap, vmap, p, stream);
+}
+
+cudaError_t launch_paged_verify(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParamsVerify &p,
+                                DecodeVariant v, cudaStream_t stream) {
+    if (v.warps == 4 && v.stages == 2) return launch_variant<4, 2, false, true>(kmap, vmap, p, stream);
+    if (v.warps == 4 && v.stages == 3) return launch_variant<4, 3, false, true>(kmap, vmap, p, stream);
+    if (v.warps == 4 && v.stages == 4) return launch_variant<4, 4, false, true>(kmap, vmap, p, stream);
+    if (v.warps == 8 && v.stages == 2) return launch_variant<8, 2, false, true>(kmap, vmap, p, stream);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_paged_decode(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParams &p,

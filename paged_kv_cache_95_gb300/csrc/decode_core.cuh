@@ -59,14 +59,12 @@ struct DecodeAcc {
     }
 };
 
-// Q^T as the B operand of S^T = K Q^T: for k-step kk, lane (n, q4) holds head n,
-// dims 16*kk + 2*q4 (+1) and 16*kk + 8 + 2*q4 (+1).  Heads n >= hpc are zero.
-__device__ __forceinline__ void load_q_frag(uint32_t (&bq)[8][2], const void *q, size_t head0_row, int hpc,
-                                            int lane) {
-    const int n = lane >> 2, q4 = lane & 3;
-    const bool hv = n < hpc;
-    const uint32_t *qrow =
-        reinterpret_cast<const uint32_t *>(static_cast<const __nv_bfloat16 *>(q) + (head0_row + n) * kHeadDim);
+// Q^T as the B operand of S^T = K Q^T: for k-step kk, lane (n, q4) holds column n
+// (q row `row`, i.e. q + row * 128), dims 16*kk + 2*q4 (+1) and 16*kk + 8 + 2*q4 (+1).
+// Columns with hv false are zero.
+__device__ __forceinline__ void load_q_frag_row(uint32_t (&bq)[8][2], const void *q, size_t row, bool hv, int lane) {
+    const int q4 = lane & 3;
+    const uint32_t *qrow = reinterpret_cast<const uint32_t *>(static_cast<const __nv_bfloat16 *>(q) + row * kHeadDim);
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
         bq[kk][0] = hv ? __ldg(qrow + (16 * kk + 2 * q4) / 2) : 0u;
@@ -74,12 +72,23 @@ __device__ __forceinline__ void load_q_frag(uint32_t (&bq)[8][2], const void *q,
     }
 }
 
+// Decode: column n is head head0_row + n (heads n >= hpc are zero).
+__device__ __forceinline__ void load_q_frag(uint32_t (&bq)[8][2], const void *q, size_t head0_row, int hpc,
+                                            int lane) {
+    const int n = lane >> 2;
+    load_q_frag_row(bq, q, head0_row + n, n < hpc, lane);
+}
+
 // One block: kb / vb are the shared addresses of the stage's K and V tiles;
 // only keys lo <= k < valid take part (lo > 0 only in the block where a sliding
 // window starts); the others are masked by index and their V rows are zeroed in
 // registers, so stale or NaN bytes in those slots never reach the result.
+// Multi-token verify: column 2*q4 (2*q4 + 1) of this lane also only sees keys
+// k < lim0 (lim1) -- its causal bound; keys between a column's bound and `valid`
+// hold valid data, so only their weight is zeroed.
 __device__ __forceinline__ void decode_block(DecodeAcc &acc, const uint32_t (&bq)[8][2], uint32_t kb, uint32_t vb,
-                                             int lo, int valid, float sl2, int lane) {
+                                             int lo, int valid, float sl2, int lane, int lim0 = kBlockSize,
+                                             int lim1 = kBlockSize) {
     const int n = lane >> 2, q4 = lane & 3;
     const int kkey = (lane & 7) | (((lane >> 3) & 1) << 3);  // K: matrices (keys 0-7 | 8-15) x (dims lo | hi)
     const int khi = lane >> 4;
@@ -100,10 +109,10 @@ __device__ __forceinline__ void decode_block(DecodeAcc &acc, const uint32_t (&bq
     // Online softmax in the log2 domain (scale * log2(e) folded into the scores).
     const int key_a = n, key_b = n + 8;
     const bool in_a = key_a >= lo && key_a < valid, in_b = key_b >= lo && key_b < valid;
-    const float s00 = in_a ? c[0] * sl2 : -INFINITY;
-    const float s01 = in_a ? c[1] * sl2 : -INFINITY;
-    const float s10 = in_b ? c[2] * sl2 : -INFINITY;
-    const float s11 = in_b ? c[3] * sl2 : -INFINITY;
+    const float s00 = in_a && key_a < lim0 ? c[0] * sl2 : -INFINITY;
+    const float s01 = in_a && key_a < lim1 ? c[1] * sl2 : -INFINITY;
+    const float s10 = in_b && key_b < lim0 ? c[2] * sl2 : -INFINITY;
+    const float s11 = in_b && key_b < lim1 ? c[3] * sl2 : -INFINITY;
     float bm0 = fmaxf(s00, s10), bm1 = fmaxf(s01, s11);
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {

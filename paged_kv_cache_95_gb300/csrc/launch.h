@@ -78,6 +78,13 @@ struct DecodeParamsFp8 : DecodeParams {
     const float *v_scale;
 };
 
+// Multi-token verify on the decode kernel: each sequence has q_per_seq query rows
+// (positions ctx - q_per_seq .. ctx - 1, causal among themselves); a CTA's MMA
+// columns are the group's (position, head) pairs, heads_per_cta = G * q_per_seq <= 8.
+struct DecodeParamsVerify : DecodeParams {
+    int32_t q_per_seq;
+};
+
 struct DecodeVariant {
     int warps;
     int stages;
@@ -96,11 +103,13 @@ size_t decode_fp8_smem_bytes();
 cudaError_t decode_fp8_prepare_device();
 cudaError_t launch_paged_decode_fp8(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParamsFp8 &p,
                                     cudaStream_t stream);
+cudaError_t launch_paged_verify(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParamsVerify &p,
+                                DecodeVariant v, cudaStream_t stream);
 
 // ---- K4: causal chunked prefill on tcgen05 ---------------------------------------
 struct PrefillParams {
     void *out;                   // [total_rows][n_q][128]
-    const int32_t *cu_q_lens;    // [num_seqs + 1]
+    const int32_t *cu_q_lens;    // [num_seqs + 1]; null: every sequence has uniform_q_len rows
     const int32_t *block_tables; // [num_seqs][max_blocks]
     const int32_t *context_lens; // [num_seqs]
     uint32_t *status;
@@ -110,6 +119,7 @@ struct PrefillParams {
     int32_t total_rows;
     float scale_log2;
     int32_t out_bf16;
+    int32_t uniform_q_len;       // rows per sequence when cu_q_lens is null
 };
 
 size_t prefill_smem_bytes();

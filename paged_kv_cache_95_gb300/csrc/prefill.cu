@@ -182,8 +182,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---- sequence extent (device data: checked) ----
-    const int row0 = __ldg(p.cu_q_lens + b);
-    const int q_len = __ldg(p.cu_q_lens + b + 1) - row0;
+    const int row0 = p.cu_q_lens ? __ldg(p.cu_q_lens + b) : b * p.uniform_q_len;
+    const int q_len = p.cu_q_lens ? __ldg(p.cu_q_lens + b + 1) - row0 : p.uniform_q_len;
     const int ctx = __ldg(p.context_lens + b);
     if (q_len < 0 || q_len > ctx || ctx > p.max_blocks * kBlockSize || row0 < 0 || row0 + q_len > p.total_rows) {
         if (tile == 0 && g == 0 && tid == 0 && p.status) atomicOr(p.status, kStatusBadQLen);

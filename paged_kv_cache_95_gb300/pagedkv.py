@@ -82,6 +82,10 @@ def _declare(lib):
     lib.paged_attention_decode_window.restype = ctypes.c_int
     lib.paged_attention_decode_fp8.argtypes = [P, i32, P, P, P, P, P, P, P, i32, i32, i32, f32, i32, i32, D, P, sz, P]
     lib.paged_attention_decode_fp8.restype = ctypes.c_int
+    lib.paged_attention_verify_workspace_size.argtypes = [i32, i32, i32, i32, i32, D]
+    lib.paged_attention_verify_workspace_size.restype = sz
+    lib.paged_attention_verify.argtypes = [P, i32, P, i32, P, P, P, P, i32, i32, i32, f32, i32, D, P, sz, P]
+    lib.paged_attention_verify.restype = ctypes.c_int
     lib.kv_reshape_and_cache_fp8.argtypes = [P, P, P, P, P, P, P, i32, D, P]
     lib.kv_reshape_and_cache_fp8.restype = ctypes.c_int
     lib.paged_attention_prefill_workspace_size.argtypes = [i32, i32, D]
@@ -402,6 +406,38 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
         int(B), int(n_q), max_blocks, float(scale), int(partition_size), ctypes.byref(desc), _ptr(workspace),
         int(workspace.numel()), _stream(stream))
     _raise("paged_attention_decode", rc)
+    return workspace
+
+
+def paged_attention_verify(out, q, q_per_seq: int, k_cache, v_cache, block_tables, context_lens, scale: float,
+                           workspace=None, partition_size: int = 0, stream=None):
+    """Verify k = q_per_seq draft positions per sequence: q / out [num_seqs * k, n_q, 128],
+    row i of sequence b at position ctx_b - k + i (causal).  Returns the workspace."""
+    torch = _torch()
+    desc = cache_desc(k_cache)
+    _check(v_cache, "v_cache", torch.bfloat16, ndim=4)
+    _need(tuple(v_cache.shape) == tuple(k_cache.shape), "v_cache shape must equal k_cache shape")
+    _check(q, "q", torch.bfloat16, ndim=3, last=HEAD_DIM)
+    rows, n_q, _ = q.shape
+    _check(out, "out", out.dtype, ndim=3)
+    _need(tuple(out.shape) == tuple(q.shape), "out must have q's shape")
+    _check(block_tables, "block_tables", torch.int32, ndim=2)
+    _check(context_lens, "context_lens", torch.int32, ndim=1)
+    B = int(context_lens.shape[0])
+    _need(block_tables.shape[0] == B and rows == B * int(q_per_seq), "q must hold q_per_seq rows per sequence")
+    max_blocks = int(block_tables.shape[1])
+    lib = load_library()
+    if workspace is None:
+        nbytes = int(lib.paged_attention_verify_workspace_size(B, int(q_per_seq), n_q, max_blocks,
+                                                               int(partition_size), ctypes.byref(desc)))
+        _need(nbytes > 0, "invalid sizes for paged_attention_verify")
+        workspace = torch.zeros(nbytes, dtype=torch.uint8, device=q.device)
+    _check(workspace, "workspace", torch.uint8, ndim=1)
+    rc = lib.paged_attention_verify(_ptr(out), _out_dtype(out), _ptr(q), int(q_per_seq), _ptr(k_cache),
+                                    _ptr(v_cache), _ptr(block_tables), _ptr(context_lens), B, int(n_q), max_blocks,
+                                    float(scale), int(partition_size), ctypes.byref(desc), _ptr(workspace),
+                                    int(workspace.numel()), _stream(stream))
+    _raise("paged_attention_verify", rc)
     return workspace
 
 

@@ -110,6 +110,27 @@ def test_decode_window_argument_errors(lib):
     assert call(64, wsb=100) == P.PKV_ERR_WORKSPACE_TOO_SMALL
 
 
+def test_verify_argument_errors(lib):
+    c = desc()
+
+    def v(k, **kw):
+        a = dict(out=FAKE, q=FAKE, B=4, nq=32, wsb=1 << 20)
+        a.update(kw)
+        return lib.paged_attention_verify(a["out"], 1, a["q"], k, FAKE, FAKE, FAKE, FAKE, a["B"], a["nq"], 8, 0.088, 0,
+                                          ctypes.byref(c), FAKE, a["wsb"], None)
+    assert v(0) == P.PKV_ERR_INVALID_ARG
+    assert v(17) == P.PKV_ERR_INVALID_ARG
+    assert v(2, q=None) == P.PKV_ERR_INVALID_ARG
+    assert v(2, nq=96) == P.PKV_ERR_UNSUPPORTED                 # G = 12
+    assert v(2, wsb=100) == P.PKV_ERR_WORKSPACE_TOO_SMALL       # decode path (G * k = 8)
+    assert v(4, out=FAKE + 4) == P.PKV_ERR_INVALID_ARG          # prefill path (G * k = 16): 16-B out
+    ws = lambda k: lib.paged_attention_verify_workspace_size(64, k, 32, 256, 0, ctypes.byref(c))
+    assert ws(0) == 0 and ws(17) == 0
+    assert ws(4) == 256                                         # prefill path: the status word
+    # decode path: partials for 64 * k rows of 32 heads
+    assert ws(2) > lib.paged_attention_workspace_size(64, 32, 256, 0, ctypes.byref(c))
+
+
 def test_fp8_argument_errors(lib):
     c8, c16 = desc(dtype=P.PKV_DTYPE_FP8_E4M3), desc()
     # cache write: needs an FP8 descriptor and both scale arrays

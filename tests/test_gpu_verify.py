@@ -1,0 +1,83 @@
+"""Multi-token verify (paged_attention_verify) against the fp64 oracle (GPU).
+
+Row i of sequence b sits at position ctx_b - k + i and sees keys j <= ctx_b - k + i
+("LLM 推理全过程的维度变化与核心公式", section "工程优化怎么嵌进公式", Speculative
+Decoding: the target model checks the k draft positions in one pass) -- the
+oracle's causal-chunk rule with q_len = k.  G * k <= 8 runs on the decode kernel,
+larger products on the tcgen05 prefill kernel; both are covered.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from gpu_helpers import DevWorkload, assert_close, bf16_to_dev, i32_to_dev, oracle_after_append, status_word, torch
+from paged_kv_cache_95_gb300 import pagedkv as P
+from paged_kv_cache_95_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+CTX = [16, 17, 33, 100, 256, 257, 700, 1000]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(built_library):
+    P.load_library()
+
+
+def _verify(d, batch, k, partition_size=0, out_dtype=None, context_lens=None):
+    t = torch()
+    q = bf16_to_dev(batch.q)
+    out = t.empty(q.shape, dtype=out_dtype or t.float32, device="cuda")
+    lens = batch.context_lens if context_lens is None else context_lens
+    ws = P.paged_attention_verify(out, q, k, d.k_cache, d.v_cache, i32_to_dev(batch.block_tables), i32_to_dev(lens),
+                                  d.wl.scale, partition_size=partition_size)
+    return out, ws
+
+
+@pytest.mark.parametrize("n_q,n_kv", [(32, 32), (32, 16), (32, 8), (64, 8), (32, 2)])
+@pytest.mark.parametrize("k", [1, 2, 3, 4, 8, 16])
+def test_verify_parity(n_q, n_kv, k):
+    ctx = [max(c, k) for c in CTX] + [k, k + 1]
+    wl, batch = W.make_custom(n_q, n_kv, ctx, q_lens=[k] * len(ctx), seed=500 + 7 * k + n_q // n_kv,
+                              materialize_logical=False)
+    d = DevWorkload(wl)
+    d.append()
+    kc, vc = oracle_after_append(wl)
+    ref = oracle.paged_attention(batch.q, batch.cu_q_lens, kc, vc, batch.block_tables, batch.context_lens, wl.scale,
+                                 n_q=wl.n_q)
+    on_decode = (n_q // n_kv) * k <= 8
+    for part in ((0, 16, 256) if on_decode else (0,)):
+        out, ws = _verify(d, batch, k, partition_size=part)
+        assert_close(out.cpu().numpy(), ref, what=f"G={n_q // n_kv} k={k} part={part}")
+        assert status_word(ws) == 0
+
+
+def test_verify_last_row_is_decode_and_bf16_out():
+    """Row k-1 of each sequence equals the decode of that token."""
+    t = torch()
+    k = 4
+    wl, batch = W.make_custom(32, 8, [40, 300, 1024], q_lens=[k] * 3, seed=520, materialize_logical=False)
+    d = DevWorkload(wl)
+    d.append()
+    out, _ = _verify(d, batch, k)
+    last = np.arange(1, 4) * k - 1
+    dq = bf16_to_dev(batch.q[last])
+    dout = t.empty(dq.shape, dtype=t.float32, device="cuda")
+    P.paged_attention_decode(dout, dq, d.k_cache, d.v_cache, i32_to_dev(batch.block_tables),
+                             i32_to_dev(batch.context_lens), wl.scale)
+    assert np.max(np.abs(out.cpu().numpy()[last] - dout.cpu().numpy())) <= 2e-5
+    o16, _ = _verify(d, batch, k, out_dtype=t.bfloat16)
+    want = out.to(t.bfloat16).view(t.int16).cpu().numpy().astype(np.int32)
+    assert np.max(np.abs(o16.view(t.int16).cpu().numpy().astype(np.int32) - want)) <= 1
+
+
+@pytest.mark.parametrize("n_q,n_kv,k", [(32, 8, 2), (64, 8, 4)])  # decode path, prefill path
+def test_verify_short_context_flags(n_q, n_kv, k):
+    wl, batch = W.make_custom(n_q, n_kv, [50, 60], q_lens=[k, k], seed=530 + k, materialize_logical=False)
+    d = DevWorkload(wl)
+    d.append()
+    lens = batch.context_lens.copy()
+    lens[1] = k - 1
+    out, ws = _verify(d, batch, k, context_lens=lens)
+    assert status_word(ws) & P.PKV_STATUS_BAD_Q_LEN
+    assert np.all(np.isfinite(out[k:].cpu().numpy()))
