@@ -464,12 +464,12 @@ def _row_variants(P, torch, dev, wl, batch, k_cache, v_cache, new_k, new_v, slot
     width = batch.max_blocks_per_seq + reps // 16 + 2
     t0 = time.perf_counter()
     for _ in range(reps):
-        for i in range(B):
-            bm.append(i, 1)
+        bm.append_batch(ids)
         bm.block_tables(ids, width)
     host_us = (time.perf_counter() - t0) / reps * 1e6
     res["block_manager"] = {"sequences": B, "us_per_step": round(host_us, 2),
-                            "note": "host C++ via ctypes: B appends of one token + block-table emission"}
+                            "note": "host C++ through ctypes: one batched append of a token per sequence + "
+                                    "block-table emission"}
     bm.close()
     return res
 

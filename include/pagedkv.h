@@ -453,6 +453,17 @@ PKV_API int pkv_bm_fork(pkv_block_manager *bm, int64_t parent_id, int64_t child_
  */
 PKV_API int pkv_bm_append(pkv_block_manager *bm, int64_t seq_id, int32_t num_tokens, int32_t *slot_mapping,
                           int32_t *copy_pair, int32_t *num_copies);
+/*
+ * One call for a batch (e.g. one decode step): num_tokens[i] new tokens for
+ * seq_ids[i] (num_tokens NULL: one each), in order.  slot_mapping (host, sum of
+ * num_tokens) receives the slots sequence after sequence; copy_pairs (host,
+ * room for num_seqs pairs) receives the {source, destination} pairs to copy
+ * first, *num_copies of them.  All or nothing: PKV_ERR_OUT_OF_BLOCKS (or an
+ * invalid or repeated id) changes nothing.
+ */
+PKV_API int pkv_bm_append_batch(pkv_block_manager *bm, const int64_t *seq_ids, int32_t num_seqs,
+                                const int32_t *num_tokens, int32_t *slot_mapping, int32_t *copy_pairs,
+                                int32_t *num_copies);
 /* Drop a sequence: every block's count decreases; blocks reaching 0 become free. */
 PKV_API int pkv_bm_free_sequence(pkv_block_manager *bm, int64_t seq_id);
 PKV_API int pkv_bm_sequence_length(const pkv_block_manager *bm, int64_t seq_id, int64_t *length);

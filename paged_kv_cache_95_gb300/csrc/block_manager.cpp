@@ -233,6 +233,57 @@ int pkv_bm_append(pkv_block_manager *bm, int64_t seq_id, int32_t num_tokens, int
     return PKV_OK;
 }
 
+int pkv_bm_append_batch(pkv_block_manager *bm, const int64_t *seq_ids, int32_t num_seqs, const int32_t *num_tokens,
+                        int32_t *slot_mapping, int32_t *copy_pairs, int32_t *num_copies) {
+    if (!bm || num_seqs < 0 || !num_copies || (num_seqs > 0 && (!seq_ids || !slot_mapping || !copy_pairs)))
+        return PKV_ERR_INVALID_ARG;
+    *num_copies = 0;
+    return guarded([&] {
+        // Dry run in call order: the blocks needed, with each copy-on-write decision made
+        // as the real appends will make it (an earlier copy can leave a block unshared).
+        std::vector<Seq *> seqs(num_seqs);
+        std::unordered_map<int32_t, int32_t> dropped;  // references released earlier in this call
+        std::unordered_map<int64_t, int> seen;
+        int64_t need = 0;
+        for (int32_t i = 0; i < num_seqs; ++i) {
+            auto it = bm->seqs.find(seq_ids[i]);
+            if (it == bm->seqs.end() || seen[seq_ids[i]]++) return PKV_ERR_INVALID_ARG;  // unknown or repeated
+            const int32_t n = num_tokens ? num_tokens[i] : 1;
+            if (n < 0) return PKV_ERR_INVALID_ARG;
+            Seq &sq = it->second;
+            seqs[i] = &sq;
+            if (n == 0) continue;
+            const int64_t new_len = sq.len + n;
+            if ((new_len + kBlock - 1) / kBlock > INT32_MAX) return PKV_ERR_INVALID_ARG;
+            need += (new_len + kBlock - 1) / kBlock - static_cast<int64_t>(sq.blocks.size());
+            if (sq.len % kBlock != 0) {
+                const int32_t last = sq.blocks.back();
+                int32_t &d = dropped[last];
+                if (bm->info[last].ref - d > 1) {
+                    ++need;
+                    ++d;
+                }
+            }
+        }
+        if (need > bm->num_free()) return PKV_ERR_OUT_OF_BLOCKS;
+        for (int32_t i = 0; i < num_seqs; ++i) {  // reserve before the first change
+            const int32_t n = num_tokens ? num_tokens[i] : 1;
+            seqs[i]->blocks.reserve((seqs[i]->len + n + kBlock - 1) / kBlock);
+        }
+        int64_t off = 0;
+        int32_t copies = 0;
+        for (int32_t i = 0; i < num_seqs; ++i) {
+            const int32_t n = num_tokens ? num_tokens[i] : 1;
+            int32_t nc = 0;
+            pkv_bm_append(bm, seq_ids[i], n, slot_mapping + off, copy_pairs + 2 * copies, &nc);  // cannot fail now
+            off += n;
+            copies += nc;
+        }
+        *num_copies = copies;
+        return PKV_OK;
+    });
+}
+
 int pkv_bm_free_sequence(pkv_block_manager *bm, int64_t seq_id) {
     if (!bm) return PKV_ERR_INVALID_ARG;
     auto it = bm->seqs.find(seq_id);

@@ -111,6 +111,8 @@ def _declare(lib):
     lib.pkv_bm_fork.restype = I
     lib.pkv_bm_append.argtypes = [P, i64, i32, P, P, P]
     lib.pkv_bm_append.restype = I
+    lib.pkv_bm_append_batch.argtypes = [P, P, i32, P, P, P, P]
+    lib.pkv_bm_append_batch.restype = I
     lib.pkv_bm_free_sequence.argtypes = [P, i64]
     lib.pkv_bm_free_sequence.restype = I
     lib.pkv_bm_sequence_length.argtypes = [P, i64, P]
@@ -315,6 +317,22 @@ class BlockManager:
                                      pair.ctypes.data, ctypes.byref(n))
         _raise("pkv_bm_append", rc)
         return slots[:int(num_tokens)], ((int(pair[0]), int(pair[1])) if n.value else None)
+
+    def append_batch(self, seq_ids, num_tokens=None):
+        """One call for a batch: returns (slot_mapping int32 [sum of num_tokens],
+        copy pairs int32 [n_copies, 2]); num_tokens None means one token each."""
+        import numpy as np
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        n = len(ids)
+        nt = None if num_tokens is None else np.ascontiguousarray(num_tokens, dtype=np.int32)
+        total = n if nt is None else int(nt.sum())
+        slots = np.zeros(max(total, 1), dtype=np.int32)
+        pairs = np.zeros((max(n, 1), 2), dtype=np.int32)
+        c = ctypes.c_int32()
+        rc = self._lib.pkv_bm_append_batch(self._h, ids.ctypes.data, n, None if nt is None else nt.ctypes.data,
+                                           slots.ctypes.data, pairs.ctypes.data, ctypes.byref(c))
+        _raise("pkv_bm_append_batch", rc)
+        return slots[:total], pairs[:c.value]
 
     def free(self, seq_id: int) -> None:
         _raise("pkv_bm_free_sequence", self._lib.pkv_bm_free_sequence(self._h, int(seq_id)))

@@ -234,3 +234,58 @@ def test_random_operations_keep_every_sequence_intact(lib, seed):
                 continue
             assert sh.snapshot()[1:] == before[1:], f"failed {op} changed the manager"
         sh.check()
+
+
+def test_append_batch_matches_sequential_appends(lib):
+    rng = np.random.default_rng(77)
+    a, b = P.BlockManager(200), P.BlockManager(200)
+    for m in (a, b):
+        for i in range(6):
+            m.add(i)
+            m.append(i, int(10 + 9 * i))
+        m.fork(2, 10)
+        m.fork(2, 11)  # three sequences share block(s) of sequence 2
+    for _ in range(20):
+        ids = rng.permutation([0, 1, 2, 3, 4, 5, 10, 11])[: rng.integers(1, 9)]
+        nt = rng.integers(0, 20, len(ids)).astype(np.int32)
+        slots, pairs = a.append_batch(ids, nt)
+        want_slots, want_pairs = [], []
+        for i, n in zip(ids, nt):
+            s_, p_ = b.append(int(i), int(n))
+            want_slots.extend(s_.tolist())
+            if p_ is not None:
+                want_pairs.append(list(p_))
+        assert slots.tolist() == want_slots
+        assert pairs.tolist() == want_pairs
+    tabs = lambda m: m.block_tables([0, 1, 2, 3, 4, 5, 10, 11], 64)
+    assert all(np.array_equal(x, y) for x, y in zip(tabs(a), tabs(b)))
+
+
+def test_append_batch_forks_of_one_block(lib):
+    """Two forks appending into the same shared partial block in one call: the first
+    one copies, the second then owns the block alone and writes in place."""
+    bm = P.BlockManager(8)
+    bm.add(1)
+    bm.append(1, 20)
+    bm.fork(1, 2)
+    slots, pairs = bm.append_batch([1, 2])
+    assert len(pairs) == 1 and pairs[0][0] == 1
+    assert slots[0] // BS == pairs[0][1] and slots[1] == 1 * BS + 4
+    assert bm.ref_count(1) == 1
+
+
+def test_append_batch_all_or_nothing(lib):
+    bm = P.BlockManager(4)
+    for i in range(2):
+        bm.add(i)
+        bm.append(i, 16)
+    before = (bm.num_free, bm.block_tables([0, 1], 4))
+    with pytest.raises(P.PagedKVError) as e:
+        bm.append_batch([0, 1], [16, 17])   # needs 3 blocks, 2 are free
+    assert e.value.code == P.PKV_ERR_OUT_OF_BLOCKS
+    for bad in ([0, 0], [0, 9]):
+        with pytest.raises(P.PagedKVError) as e:
+            bm.append_batch(bad)
+        assert e.value.code == P.PKV_ERR_INVALID_ARG
+    after = (bm.num_free, bm.block_tables([0, 1], 4))
+    assert before[0] == after[0] and all(np.array_equal(x, y) for x, y in zip(before[1], after[1]))
