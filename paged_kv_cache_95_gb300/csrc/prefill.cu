@@ -387,6 +387,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld_32x32b_x32(t_s, sr[0]);
             tmem_ld_32x32b_x32(t_s + 32, sr[1]);
             tmem_wait_ld();
+            tmem_hold(sr[0]);
+            tmem_hold(sr[1]);
             // Mask by index (skipped for chunks whose 32 keys are all visible); half max.
             float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
@@ -424,6 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t orow[32];
                     tmem_ld_32x32b_x32(t_o + 32 * q, orow);
                     tmem_wait_ld();
+                    tmem_hold(orow);
 #pragma unroll
                     for (int k = 0; k < 32; ++k) orow[k] = __float_as_uint(__uint_as_float(orow[k]) * alpha);
                     tmem_st_32x32b_x32(t_o + 32 * q, orow);
@@ -491,11 +494,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const size_t orow_base =
                 (static_cast<size_t>(row0 + i0 + ii) * p.n_q + static_cast<size_t>(g) * G + (r % G)) * kHeadDim +
                 64 * hc;
-#pragma unroll
+            // Kept rolled: in a variant of this kernel the unrolled form of this loop
+            // wrote wrong values for the second 32-column chunk (no time is lost).
+#pragma unroll 1
             for (int q = 0; q < 2; ++q) {
                 uint32_t orow[32];
                 tmem_ld_32x32b_x32(t_o + 32 * q, orow);
                 tmem_wait_ld();
+                tmem_hold(orow);
                 if (staged)
                     stage_row(sbase + kOffK, p.out_bf16, r, hc, q, orow, inv);
                 else if (row_valid)

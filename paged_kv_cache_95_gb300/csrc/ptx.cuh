@@ -329,6 +329,15 @@ __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_
 }
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// Pins registers filled by tcgen05.ld behind the wait that precedes this call:
+// the load's outputs are valid only after tcgen05.wait::ld, and without a tie the
+// compiler may move their first use above the wait (the asm statements stay in
+// order; ordinary arithmetic on their outputs does not).
+template <int N>
+__device__ __forceinline__ void tmem_hold(uint32_t (&r)[N]) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 }  // namespace pkv
