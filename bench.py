@@ -442,7 +442,7 @@ def _row_variants(P, torch, dev, wl, batch, k_cache, v_cache, new_k, new_v, slot
                             "sequences_per_s": round(B / msw * 1e3, 1)}
 
     # multi-token verify: k = 4 draft positions per sequence (causal among them), same K/V bytes as the decode
-    kv = 4
+    kv, gv = 4, wl.n_q // n_kv  # draft positions, group size
     qv = torch.randn((B * kv, wl.n_q, d), device=dev).to(torch.bfloat16)
     outv = torch.empty(qv.shape, dtype=torch.bfloat16, device=dev)
     wsv = P.paged_attention_verify(outv, qv, kv, k_cache, v_cache, tables, lens, wl.scale)
@@ -452,7 +452,7 @@ def _row_variants(P, torch, dev, wl, batch, k_cache, v_cache, new_k, new_v, slot
                         "gbs": round(kv_bytes / msv / 1e6, 2), "frac_of_hbm": round(kv_bytes / msv / 1e6 / peak, 4),
                         "tokens_per_s": round(B * kv / msv * 1e3, 1),
                         "time_vs_one_decode": round(msv / decode_ms, 3),
-                        "path": "decode kernel" if (wl.n_q // n_kv) * kv <= 8 else "tcgen05 prefill kernel"}
+                        "path": "decode kernel" if gv * kv <= 32 or 128 % gv else "tcgen05 prefill kernel"}
 
     # host block manager: one decode step of this batch = one appended token per sequence + table emission
     reps = 200

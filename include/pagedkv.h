@@ -387,9 +387,11 @@ PKV_API int paged_attention_prefill_chunk(void *out, int32_t out_dtype, const vo
  *   q, out    : [num_seqs * q_per_seq][num_q_heads][head_dim]; sequence b owns
  *               rows b * q_per_seq .. b * q_per_seq + q_per_seq - 1
  *   q_per_seq : k, 1 .. 16
- * Runs on the decode kernel (K/V read once per KV head, the CTA's 8 MMA columns
- * holding the G heads x k positions) when G * k <= 8, else on the tcgen05
- * prefill kernel (then q and out must be 16-B aligned).  A sequence with
+ * Runs on the decode kernel when G * k <= 32 or G does not divide 128: the
+ * G heads x k positions of a KV head are the MMA columns of ceil(G * k / 16)
+ * CTAs of up to 16 columns (one or two 8-column tiles), each reading the K/V
+ * once; else on the tcgen05 prefill kernel (then q and out must be 16-B aligned).
+ * num_seqs * k must not exceed 65535 (PKV_ERR_UNSUPPORTED).  A sequence with
  * ctx < k sets PKV_STATUS_BAD_Q_LEN and gets zero rows.
  * Workspace: paged_attention_verify_workspace_size() bytes, zero-filled once.
  * Errors: as paged_attention_decode; PKV_ERR_INVALID_ARG for q_per_seq outside 1..16.

@@ -185,9 +185,10 @@ struct DecodePlan {
     size_t off_cnt, off_m, off_l, off_o, total;
 };
 
-// rows_per_seq: query rows per sequence (1 for decode, q_per_seq for verify).
+// rows_per_seq: query rows per sequence (1 for decode, q_per_seq for verify);
+// ctas_per_kv: CTAs per KV head and partition (0: the decode's, from G).
 DecodePlan plan_decode(int32_t num_seqs, int32_t n_q, int32_t n_kv, int32_t max_blocks, int32_t part_blocks,
-                       int32_t rows_per_seq = 1) {
+                       int32_t rows_per_seq = 1, int32_t ctas_per_kv = 0) {
     DecodePlan pl{};
     pl.part_blocks = part_blocks >= max_blocks ? max_blocks : part_blocks;
     pl.max_parts = (max_blocks + pl.part_blocks - 1) / pl.part_blocks;
@@ -197,7 +198,7 @@ DecodePlan plan_decode(int32_t num_seqs, int32_t n_q, int32_t n_kv, int32_t max_
         return pl;
     }
     const int32_t G = n_q / n_kv;
-    const int32_t groups = n_kv * (G <= 8 ? 1 : G / 8);  // CTAs per sequence and partition
+    const int32_t groups = n_kv * (ctas_per_kv > 0 ? ctas_per_kv : (G <= 8 ? 1 : G / 8));  // CTAs per sequence, partition
     const size_t rows = static_cast<size_t>(num_seqs) * rows_per_seq * n_q * pl.max_parts;
     pl.off_m = pl.off_cnt + align_up(static_cast<size_t>(num_seqs) * groups * 4, 256);
     pl.off_l = pl.off_m + align_up(rows * 4, 256);
@@ -562,10 +563,18 @@ int paged_attention_prefill_chunk(void *out, int32_t out_dtype, const void *q, c
 
 namespace {
 constexpr int32_t kMaxVerifyRows = 16;  // draft positions per sequence
+constexpr int32_t kMaxVerifyCols = 32;  // (position, head) pairs per KV head on the decode kernel
 
-// Verify runs on the decode kernel when a CTA's 8 MMA columns hold the group's
-// (position, head) pairs, else on the prefill kernel.
-bool verify_on_decode(int32_t q_per_seq, int32_t G) { return static_cast<int64_t>(q_per_seq) * G <= 8; }
+// Verify runs on the decode kernel when the group's G x k (position, head) pairs
+// fit in at most two CTAs of up to 16 MMA columns each (K/V read once per CTA),
+// or when the prefill kernel cannot pack the group (G does not divide its 128
+// tile rows); else on the prefill kernel.
+bool verify_on_decode(int32_t q_per_seq, int32_t G) {
+    return static_cast<int64_t>(q_per_seq) * G <= kMaxVerifyCols || 128 % G != 0;
+}
+// CTAs per KV head and the columns each takes (the last one may take fewer).
+int32_t verify_splits(int32_t cols) { return (cols + 15) / 16; }
+int32_t verify_cols_per_cta(int32_t cols) { return (cols + verify_splits(cols) - 1) / verify_splits(cols); }
 }  // namespace
 
 size_t paged_attention_verify_workspace_size(int32_t num_seqs, int32_t q_per_seq, int32_t num_q_heads,
@@ -578,7 +587,9 @@ size_t paged_attention_verify_workspace_size(int32_t num_seqs, int32_t q_per_seq
     const int32_t G = num_q_heads / cache->num_kv_heads;
     if (!verify_on_decode(q_per_seq, G)) return kStatusBytes;
     const int32_t pb = partition_size > 0 ? partition_size / kBlockSize : kMinPartBlocks;
-    return plan_decode(num_seqs, num_q_heads, cache->num_kv_heads, max_blocks_per_seq, pb, q_per_seq).total;
+    return plan_decode(num_seqs, num_q_heads, cache->num_kv_heads, max_blocks_per_seq, pb, q_per_seq,
+                       verify_splits(G * q_per_seq))
+        .total;
 }
 
 int paged_attention_verify(void *out, int32_t out_dtype, const void *q, int32_t q_per_seq, const void *k_cache,
@@ -615,9 +626,14 @@ int paged_attention_verify(void *out, int32_t out_dtype, const void *q, int32_t 
     const int dev = current_device();
     if (dev < 0 || dev >= kMaxDevices) return PKV_ERR_CUDA;
     const int sms = sm_count(dev);
+    const int32_t cols = G * q_per_seq;
+    const int32_t splits = verify_splits(cols);
+    // grid y of the decode kernel (KV heads x splits) and of the merge kernel (rows)
+    if (static_cast<int64_t>(n_kv) * splits > 65535 || static_cast<int64_t>(num_seqs) * q_per_seq > 65535)
+        return PKV_ERR_UNSUPPORTED;
     const int32_t pb = partition_size > 0 ? partition_size / kBlockSize
-                                          : auto_part_blocks(num_seqs, n_kv, 1, max_blocks_per_seq, sms);
-    const DecodePlan pl = plan_decode(num_seqs, num_q_heads, n_kv, max_blocks_per_seq, pb, q_per_seq);
+                                          : auto_part_blocks(num_seqs, n_kv, splits, max_blocks_per_seq, sms);
+    const DecodePlan pl = plan_decode(num_seqs, num_q_heads, n_kv, max_blocks_per_seq, pb, q_per_seq, splits);
     if (workspace_bytes < pl.total) return PKV_ERR_WORKSPACE_TOO_SMALL;
 
     CUtensorMap kmap, vmap;
@@ -644,8 +660,8 @@ int paged_attention_verify(void *out, int32_t out_dtype, const void *q, int32_t 
     p.n_q = num_q_heads;
     p.n_kv = n_kv;
     p.group = G;
-    p.heads_per_cta = G * q_per_seq;  // the CTA's columns: q_per_seq positions x G heads
-    p.head_splits = 1;
+    p.heads_per_cta = verify_cols_per_cta(cols);  // the CTA's share of the q_per_seq x G columns
+    p.head_splits = splits;
     p.max_blocks = max_blocks_per_seq;
     p.num_blocks = cache->num_blocks;
     p.part_blocks = pl.part_blocks;

@@ -62,7 +62,8 @@ template <bool FP8, bool VERIFY>
 using DecodeParamsT =
     std::conditional_t<FP8, DecodeParamsFp8, std::conditional_t<VERIFY, DecodeParamsVerify, DecodeParams>>;
 
-template <int NW, int ST, bool FP8, bool VERIFY = false>
+// NCT: 8-column MMA tiles per CTA (2 only for multi-token verify with 9..16 columns).
+template <int NW, int ST, bool FP8, bool VERIFY = false, int NCT = 1>
 __global__ void __launch_bounds__(NW * 32)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                         const DecodeParamsT<FP8, VERIFY> p) {
@@ -77,16 +78,25 @@ __global__ void __launch_bounds__(NW * 32)
     const int hs = blockIdx.y;
     const int b = blockIdx.z;
     const int g = hs / p.head_splits;
+    static_assert(NCT == 1 || (NCT == 2 && VERIFY && !FP8), "two column tiles: verify only");
     const int hpc = p.heads_per_cta;
-    const int h0 = g * p.group + (hs - g * p.head_splits) * hpc;
+    const int hsl = hs - g * p.head_splits;  // this CTA's share of the group's columns
+    const int h0 = g * p.group + hsl * hpc;
+    // Columns of this CTA: decode, heads h0 .. h0 + hpc - 1; verify, the group's
+    // (position, head) pairs hsl * hpc .. (the last share may be shorter).
+    int ncols = hpc;
+    if constexpr (VERIFY) ncols = min(hpc, p.group * p.q_per_seq - hsl * hpc);
     // q / out row (in units of 128-element head rows) of CTA column c: decode, head h0 + c of
-    // sequence b; verify, position c / G of sequence b's q_per_seq rows, head g * G + c % G.
+    // sequence b; verify, column cg = hsl * hpc + c is position cg / G of sequence b's
+    // q_per_seq rows and head g * G + cg % G.
     auto col_row = [&](int c) -> size_t {
-        if constexpr (VERIFY)
-            return (static_cast<size_t>(b) * p.q_per_seq + c / p.group) * p.n_q + static_cast<size_t>(g) * p.group +
-                   c % p.group;
-        else
+        if constexpr (VERIFY) {
+            const int cg = hsl * hpc + c;
+            return (static_cast<size_t>(b) * p.q_per_seq + cg / p.group) * p.n_q + static_cast<size_t>(g) * p.group +
+                   cg % p.group;
+        } else {
             return static_cast<size_t>(b) * p.n_q + h0 + c;
+        }
     };
 
     if (threadIdx.x == 0) {
@@ -111,7 +121,7 @@ __global__ void __launch_bounds__(NW * 32)
     }
     if (ctx == 0) {
         if (part == 0)
-            for (int i = threadIdx.x; i < hpc * kHeadDim; i += NW * 32)
+            for (int i = threadIdx.x; i < ncols * kHeadDim; i += NW * 32)
                 store_out(p.out, p.out_bf16, col_row(i >> 7) * kHeadDim + (i & 127), 0.f);
         return;
     }
@@ -155,25 +165,32 @@ __global__ void __launch_bounds__(NW * 32)
     // ---- Q^T as the B operand (16 dims x 8 heads per k-step), kept in registers ----
     const int n = lane >> 2;  // head column of B / row group of C
     const int q4 = lane & 3;
-    uint32_t bq[8][2];
+    uint32_t bqt[NCT][8][2];
+    auto &bq = bqt[0];
     float sl2 = p.scale_log2;
     if constexpr (FP8) {
         const int qexp = load_q_frag_fp8(bq, p.q, static_cast<size_t>(b) * p.n_q + h0, hpc, lane);
         sl2 *= ldexpf(1.f, -qexp);
     } else if constexpr (VERIFY) {
-        load_q_frag_row(bq, p.q, col_row(n), n < hpc, lane);
+#pragma unroll
+        for (int t = 0; t < NCT; ++t) load_q_frag_row(bqt[t], p.q, col_row(8 * t + n), 8 * t + n < ncols, lane);
     } else {
         load_q_frag(bq, p.q, static_cast<size_t>(b) * p.n_q + h0, hpc, lane);
     }
-    // Verify: the absolute causal bound (exclusive) of this lane's columns 2*q4 and 2*q4 + 1.
-    int pos_end0 = 0, pos_end1 = 0;
+    // Verify: the absolute causal bound (exclusive) of this lane's columns 8t + 2*q4 and 8t + 2*q4 + 1.
+    int pos_end[NCT][2] = {};
     if constexpr (VERIFY) {
-        pos_end0 = ctx - p.q_per_seq + (2 * q4) / p.group + 1;
-        pos_end1 = ctx - p.q_per_seq + (2 * q4 + 1) / p.group + 1;
+#pragma unroll
+        for (int t = 0; t < NCT; ++t)
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+                pos_end[t][u] = ctx - p.q_per_seq + (hsl * hpc + 8 * t + 2 * q4 + u) / p.group + 1;
     }
 
-    DecodeAcc acc;
-    acc.reset();
+    DecodeAcc acct[NCT];
+    auto &acc = acct[0];
+#pragma unroll
+    for (int t = 0; t < NCT; ++t) acct[t].reset();
 
     int consumed = 0;
     bool timed_out = false;
@@ -195,12 +212,16 @@ __global__ void __launch_bounds__(NW * 32)
             if (lane == 0 && p.status) atomicOr(p.status, kStatusBadBlockId);
         }
         const uint32_t kb = stage_base + s * kStage;
-        if constexpr (FP8)
+        if constexpr (FP8) {
             decode_block_fp8(acc, bq, kb, kb + kTileBytes8, scale_base + s * kStageScaleBytes, lo, valid, sl2, lane);
-        else if constexpr (VERIFY)
-            decode_block(acc, bq, kb, kb + kTileBytes, lo, valid, sl2, lane, pos_end0 - j * kBlockSize,
-                         pos_end1 - j * kBlockSize);
-        else
+        } else if constexpr (VERIFY && NCT == 2) {
+            const int lim[2][2] = {{pos_end[0][0] - j * kBlockSize, pos_end[0][1] - j * kBlockSize},
+                                   {pos_end[1][0] - j * kBlockSize, pos_end[1][1] - j * kBlockSize}};
+            decode_block_x2(acct, bqt, kb, kb + kTileBytes, lo, valid, sl2, lane, lim);
+        } else if constexpr (VERIFY) {
+            decode_block(acc, bq, kb, kb + kTileBytes, lo, valid, sl2, lane, pos_end[0][0] - j * kBlockSize,
+                         pos_end[0][1] - j * kBlockSize);
+        } else
             decode_block(acc, bq, kb, kb + kTileBytes, lo, valid, sl2, lane);
         consumed = i + 1;
 
@@ -220,44 +241,50 @@ __global__ void __launch_bounds__(NW * 32)
 
     if constexpr (FP8) fp8_finish(acc);
     // Full row sums of this warp: add the shares of the 8 lanes of a head column.
-    acc.reduce_sums();
+#pragma unroll
+    for (int t = 0; t < NCT; ++t) acct[t].reduce_sums();
 
     // ---- combine the warps of the CTA (shared memory reused after the pipeline) ----
+    constexpr int kCols = 8 * NCT;  // MMA columns per warp
     __syncthreads();
-    float *red_o = reinterpret_cast<float *>(smem);  // [NW][8 heads][128]
-    float *red_m = red_o + NW * 8 * kHeadDim;        // [NW][8]
-    float *red_l = red_m + NW * 8;                   // [NW][8]
+    float *red_o = reinterpret_cast<float *>(smem);  // [NW][kCols][128]
+    float *red_m = red_o + NW * kCols * kHeadDim;    // [NW][kCols]
+    float *red_l = red_m + NW * kCols;               // [NW][kCols]
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-        // O^T fragment rows n and n + 8 of MMA mt are dims d0 and d1 (bf16: 16mt + n, +8;
-        // FP8: the permuted order 16n + 2mt, +1)
-        const int d0 = FP8 ? 16 * n + 2 * mt : 16 * mt + n;
-        const int d1 = FP8 ? d0 + 1 : d0 + 8;
-        red_o[(warp * 8 + 2 * q4) * kHeadDim + d0] = acc.o[mt][0];
-        red_o[(warp * 8 + 2 * q4 + 1) * kHeadDim + d0] = acc.o[mt][1];
-        red_o[(warp * 8 + 2 * q4) * kHeadDim + d1] = acc.o[mt][2];
-        red_o[(warp * 8 + 2 * q4 + 1) * kHeadDim + d1] = acc.o[mt][3];
-    }
-    if (lane < 4) {
-        red_m[warp * 8 + 2 * lane] = acc.m0;
-        red_m[warp * 8 + 2 * lane + 1] = acc.m1;
-        red_l[warp * 8 + 2 * lane] = acc.l0;
-        red_l[warp * 8 + 2 * lane + 1] = acc.l1;
+    for (int t = 0; t < NCT; ++t) {
+        const int c0 = warp * kCols + 8 * t + 2 * q4;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            // O^T fragment rows n and n + 8 of MMA mt are dims d0 and d1 (bf16: 16mt + n, +8;
+            // FP8: the permuted order 16n + 2mt, +1)
+            const int d0 = FP8 ? 16 * n + 2 * mt : 16 * mt + n;
+            const int d1 = FP8 ? d0 + 1 : d0 + 8;
+            red_o[c0 * kHeadDim + d0] = acct[t].o[mt][0];
+            red_o[(c0 + 1) * kHeadDim + d0] = acct[t].o[mt][1];
+            red_o[c0 * kHeadDim + d1] = acct[t].o[mt][2];
+            red_o[(c0 + 1) * kHeadDim + d1] = acct[t].o[mt][3];
+        }
+        if (lane < 4) {
+            red_m[c0] = acct[t].m0;
+            red_m[c0 + 1] = acct[t].m1;
+            red_l[c0] = acct[t].l0;
+            red_l[c0 + 1] = acct[t].l1;
+        }
     }
     __syncthreads();
 
-    for (int idx = threadIdx.x; idx < hpc * kHeadDim; idx += NW * 32) {
+    for (int idx = threadIdx.x; idx < ncols * kHeadDim; idx += NW * 32) {
         const int hh = idx >> 7, d = idx & 127;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < NW; ++w) M = fmaxf(M, red_m[w * 8 + hh]);
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, red_m[w * kCols + hh]);
         const float Mu = M == -INFINITY ? 0.f : M;
         float L = 0.f, O = 0.f;
 #pragma unroll
         for (int w = 0; w < NW; ++w) {
-            const float f = fast_exp2(red_m[w * 8 + hh] - Mu);
-            L += f * red_l[w * 8 + hh];
-            O += f * red_o[(w * 8 + hh) * kHeadDim + d];
+            const float f = fast_exp2(red_m[w * kCols + hh] - Mu);
+            L += f * red_l[w * kCols + hh];
+            O += f * red_o[(w * kCols + hh) * kHeadDim + d];
         }
         const size_t row = col_row(hh);
         if (nparts == 1) {
@@ -278,7 +305,7 @@ __global__ void __launch_bounds__(NW * 32)
     // (Flash-Decoding's log-sum-exp reduction, in the log2 domain of the scores).
     // One acquire-release add per CTA publishes its partial (written by all
     // threads before the barrier) and, for the last arrival, acquires the others'.
-    uint32_t *last_flag = reinterpret_cast<uint32_t *>(red_l + NW * 8);
+    uint32_t *last_flag = reinterpret_cast<uint32_t *>(red_l + NW * kCols);
     __syncthreads();
     if (threadIdx.x == 0) {
         const uint32_t prev = atom_add_acq_rel_gpu(p.counters + static_cast<size_t>(b) * gridDim.y + hs, 1u);
@@ -288,7 +315,7 @@ __global__ void __launch_bounds__(NW * 32)
     if (*last_flag == 0) return;
 
     // Warp w folds the partitions p = w, w + NW, ...; lane owns dims 4*lane .. 4*lane+3.
-    for (int hh = 0; hh < hpc; ++hh) {
+    for (int hh = 0; hh < ncols; ++hh) {
         const size_t base = col_row(hh) * p.max_parts;
         float M = -INFINITY;
         for (int i = lane; i < nparts; i += 32) M = fmaxf(M, __ldcg(p.part_m + base + i));
@@ -306,17 +333,17 @@ __global__ void __launch_bounds__(NW * 32)
             acc.z += f * v.z;
             acc.w += f * v.w;
         }
-        reinterpret_cast<float4 *>(red_o + (warp * 8 + hh) * kHeadDim)[lane] = acc;
-        if (lane == 0) red_l[warp * 8 + hh] = L;
+        reinterpret_cast<float4 *>(red_o + (warp * kCols + hh) * kHeadDim)[lane] = acc;
+        if (lane == 0) red_l[warp * kCols + hh] = L;
     }
     __syncthreads();
-    for (int idx = threadIdx.x; idx < hpc * kHeadDim; idx += NW * 32) {
+    for (int idx = threadIdx.x; idx < ncols * kHeadDim; idx += NW * 32) {
         const int hh = idx >> 7, d = idx & 127;
         float L = 0.f, O = 0.f;
 #pragma unroll
         for (int w = 0; w < NW; ++w) {
-            L += red_l[w * 8 + hh];
-            O += red_o[(w * 8 + hh) * kHeadDim + d];
+            L += red_l[w * kCols + hh];
+            O += red_o[(w * kCols + hh) * kHeadDim + d];
         }
         store_out(p.out, p.out_bf16, col_row(hh) * kHeadDim + d, L > 0.f ? O / L : 0.f);
     }
@@ -386,11 +413,11 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lse_merge_kernel(const Decod
     }
 }
 
-template <int NW, int ST, bool FP8 = false, bool VERIFY = false>
+template <int NW, int ST, bool FP8 = false, bool VERIFY = false, int NCT = 1>
 cudaError_t launch_variant(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParamsT<FP8, VERIFY> &p,
                            cudaStream_t stream) {
     const dim3 grid(p.max_parts, p.n_kv * p.head_splits, p.num_seqs);
-    cudaError_t e = launch_pdl(paged_decode_kernel<NW, ST, FP8, VERIFY>, grid, dim3(NW * 32),
+    cudaError_t e = launch_pdl(paged_decode_kernel<NW, ST, FP8, VERIFY, NCT>, grid, dim3(NW * 32),
                                FP8 ? decode_fp8_smem_bytes() : decode_smem_bytes({NW, ST}), stream, kmap, vmap, p);
     if (e != cudaSuccess) return e;
     int rows_per_seq = 1;
@@ -406,7 +433,11 @@ cudaError_t prepare_variant() {
     cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<NW, ST, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(decode_smem_bytes({NW, ST})));
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(paged_decode_kernel<NW, ST, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(paged_decode_kernel<NW, ST, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(decode_smem_bytes({NW, ST})));
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(paged_decode_kernel<NW, ST, false, true, 2>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(decode_smem_bytes({NW, ST})));
 }
 
@@ -449,10 +480,20 @@ cudaError_t launch_paged_decode_fp8(const CUtensorMap &kmap, const CUtensorMap &
 
 cudaError_t launch_paged_verify(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParamsVerify &p,
                                 DecodeVariant v, cudaStream_t stream) {
-    if (v.warps == 4 && v.stages == 2) return launch_variant<4, 2, false, true>(kmap, vmap, p, stream);
-    if (v.warps == 4 && v.stages == 3) return launch_variant<4, 3, false, true>(kmap, vmap, p, stream);
-    if (v.warps == 4 && v.stages == 4) return launch_variant<4, 4, false, true>(kmap, vmap, p, stream);
-    if (v.warps == 8 && v.stages == 2) return launch_variant<8, 2, false, true>(kmap, vmap, p, stream);
+    if (p.heads_per_cta > 16) return cudaErrorInvalidValue;
+    const bool two = p.heads_per_cta > 8;  // 9..16 columns: two 8-column MMA tiles per warp
+    if (v.warps == 4 && v.stages == 2)
+        return two ? launch_variant<4, 2, false, true, 2>(kmap, vmap, p, stream)
+                   : launch_variant<4, 2, false, true>(kmap, vmap, p, stream);
+    if (v.warps == 4 && v.stages == 3)
+        return two ? launch_variant<4, 3, false, true, 2>(kmap, vmap, p, stream)
+                   : launch_variant<4, 3, false, true>(kmap, vmap, p, stream);
+    if (v.warps == 4 && v.stages == 4)
+        return two ? launch_variant<4, 4, false, true, 2>(kmap, vmap, p, stream)
+                   : launch_variant<4, 4, false, true>(kmap, vmap, p, stream);
+    if (v.warps == 8 && v.stages == 2)
+        return two ? launch_variant<8, 2, false, true, 2>(kmap, vmap, p, stream)
+                   : launch_variant<8, 2, false, true>(kmap, vmap, p, stream);
     return cudaErrorInvalidValue;
 }
 

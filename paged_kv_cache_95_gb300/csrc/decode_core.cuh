@@ -173,6 +173,101 @@ __device__ __forceinline__ void decode_block(DecodeAcc &acc, const uint32_t (&bq
     }
 }
 
+// One block for two 8-column tiles of the same KV head (16 MMA columns, e.g.
+// multi-token verify with G x q_per_seq in 9..16): each K and V fragment is read
+// from shared memory once and feeds both tiles' MMAs; each tile keeps its own
+// online-softmax state.  lim[t][0..1] are the causal bounds (exclusive, relative
+// to the block) of this lane's columns 2*q4 and 2*q4 + 1 of tile t.
+__device__ __forceinline__ void decode_block_x2(DecodeAcc (&acc)[2], const uint32_t (&bq)[2][8][2], uint32_t kb,
+                                                uint32_t vb, int lo, int valid, float sl2, int lane,
+                                                const int (&lim)[2][2]) {
+    const int n = lane >> 2, q4 = lane & 3;
+    const int kkey = (lane & 7) | (((lane >> 3) & 1) << 3);
+    const int khi = lane >> 4;
+    const int vkey = (lane & 7) | ((lane >> 4) << 3);
+    const int vhi = (lane >> 3) & 1;
+
+    // S^T = K Q^T for both column tiles
+    float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        const int chunk = 2 * kk + khi;
+        const uint32_t addr = kb + (chunk >> 3) * kBoxBytes + kkey * 128 + (((chunk & 7) ^ (lane & 7)) << 4);
+        uint32_t a[4];
+        ldmatrix_x4(a, addr);
+        mma_bf16_16816(c[0], a, bq[0][kk][0], bq[0][kk][1]);
+        mma_bf16_16816(c[1], a, bq[1][kk][0], bq[1][kk][1]);
+    }
+
+    // Online softmax per tile; P^T fragments (bf16 head + remainder) per tile.
+    const int key_a = n, key_b = n + 8;
+    const bool in_a = key_a >= lo && key_a < valid, in_b = key_b >= lo && key_b < valid;
+    uint32_t pb[2][4];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const float s00 = in_a && key_a < lim[t][0] ? c[t][0] * sl2 : -INFINITY;
+        const float s01 = in_a && key_a < lim[t][1] ? c[t][1] * sl2 : -INFINITY;
+        const float s10 = in_b && key_b < lim[t][0] ? c[t][2] * sl2 : -INFINITY;
+        const float s11 = in_b && key_b < lim[t][1] ? c[t][3] * sl2 : -INFINITY;
+        float bm0 = fmaxf(s00, s10), bm1 = fmaxf(s01, s11);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
+            bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
+        }
+        const float mn0 = fmaxf(acc[t].m0, bm0), mn1 = fmaxf(acc[t].m1, bm1);
+        const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
+        const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float al0 = fast_exp2(acc[t].m0 - mu0), al1 = fast_exp2(acc[t].m1 - mu1);
+        const float p00 = fast_exp2(s00 - mu0), p01 = fast_exp2(s01 - mu1);
+        const float p10 = fast_exp2(s10 - mu0), p11 = fast_exp2(s11 - mu1);
+        acc[t].l0 = acc[t].l0 * al0 + p00 + p10;
+        acc[t].l1 = acc[t].l1 * al1 + p01 + p11;
+        acc[t].m0 = mn0;
+        acc[t].m1 = mn1;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            acc[t].o[mt][0] *= al0;
+            acc[t].o[mt][1] *= al1;
+            acc[t].o[mt][2] *= al0;
+            acc[t].o[mt][3] *= al1;
+        }
+        const uint32_t ph0 = pack_bf16x2(p00, p01), ph1 = pack_bf16x2(p10, p11);
+        const uint32_t pl0 = pack_bf16x2(p00 - __uint_as_float(ph0 << 16), p01 - __uint_as_float(ph0 & 0xffff0000u));
+        const uint32_t pl1 = pack_bf16x2(p10 - __uint_as_float(ph1 << 16), p11 - __uint_as_float(ph1 & 0xffff0000u));
+        pb[t][0] = movmatrix_trans(ph0);
+        pb[t][1] = movmatrix_trans(ph1);
+        pb[t][2] = movmatrix_trans(pl0);
+        pb[t][3] = movmatrix_trans(pl1);
+    }
+
+    uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;
+    if (lo > 0 || valid < kBlockSize) {
+        auto keep = [&](int k) { return k >= lo && k < valid; };
+        const int ka = 2 * q4, kb2 = 2 * q4 + 8;
+        vm_lo = (keep(ka) ? 0x0000ffffu : 0u) | (keep(ka + 1) ? 0xffff0000u : 0u);
+        vm_hi = (keep(kb2) ? 0x0000ffffu : 0u) | (keep(kb2 + 1) ? 0xffff0000u : 0u);
+    }
+
+    // O^T += V^T P^T for both tiles (one V fragment per 16 dims)
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+        const int chunk = 2 * mt + vhi;
+        const uint32_t addr = vb + (chunk >> 3) * kBoxBytes + vkey * 128 + (((chunk & 7) ^ (lane & 7)) << 4);
+        uint32_t a[4];
+        ldmatrix_x4_trans(a, addr);
+        a[0] &= vm_lo;
+        a[1] &= vm_lo;
+        a[2] &= vm_hi;
+        a[3] &= vm_hi;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            mma_bf16_16816(acc[t].o[mt], a, pb[t][0], pb[t][1]);
+            mma_bf16_16816(acc[t].o[mt], a, pb[t][2], pb[t][3]);
+        }
+    }
+}
+
 // Copies of one (block, head) K and V tile into a stage: four TMA boxes of 64
 // dims x 16 slots, completing on `bar` with 8 KB of transactions.
 __device__ __forceinline__ void issue_block_copy(const CUtensorMap *kmap, const CUtensorMap *vmap, uint32_t dst,

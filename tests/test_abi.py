@@ -123,12 +123,14 @@ def test_verify_argument_errors(lib):
     assert v(2, q=None) == P.PKV_ERR_INVALID_ARG
     assert v(2, nq=96) == P.PKV_ERR_UNSUPPORTED                 # G = 12
     assert v(2, wsb=100) == P.PKV_ERR_WORKSPACE_TOO_SMALL       # decode path (G * k = 8)
-    assert v(4, out=FAKE + 4) == P.PKV_ERR_INVALID_ARG          # prefill path (G * k = 16): 16-B out
+    assert v(8, wsb=100) == P.PKV_ERR_WORKSPACE_TOO_SMALL       # decode path, two CTAs per KV head (G * k = 32)
+    assert v(16, out=FAKE + 4) == P.PKV_ERR_INVALID_ARG         # prefill path (G * k = 64): 16-B out
     ws = lambda k: lib.paged_attention_verify_workspace_size(64, k, 32, 256, 0, ctypes.byref(c))
     assert ws(0) == 0 and ws(17) == 0
-    assert ws(4) == 256                                         # prefill path: the status word
+    assert ws(16) == 256                                        # prefill path: the status word
     # decode path: partials for 64 * k rows of 32 heads
     assert ws(2) > lib.paged_attention_workspace_size(64, 32, 256, 0, ctypes.byref(c))
+    assert ws(8) > ws(4) > ws(2)
 
 
 def test_fp8_argument_errors(lib):

@@ -3,8 +3,10 @@
 Row i of sequence b sits at position ctx_b - k + i and sees keys j <= ctx_b - k + i
 ("LLM 推理全过程的维度变化与核心公式", section "工程优化怎么嵌进公式", Speculative
 Decoding: the target model checks the k draft positions in one pass) -- the
-oracle's causal-chunk rule with q_len = k.  G * k <= 8 runs on the decode kernel,
-larger products on the tcgen05 prefill kernel; both are covered.
+oracle's causal-chunk rule with q_len = k.  G * k <= 32 (or a G that does not
+divide 128) runs on the decode kernel (one 8-column MMA tile per CTA up to 8
+columns, two tiles up to 16, more CTAs per KV head above that, ragged shares
+included), larger products on the tcgen05 prefill kernel; all are covered.
 """
 import numpy as np
 import pytest
@@ -34,8 +36,8 @@ def _verify(d, batch, k, partition_size=0, out_dtype=None, context_lens=None):
     return out, ws
 
 
-@pytest.mark.parametrize("n_q,n_kv", [(32, 32), (32, 16), (32, 8), (64, 8), (32, 2)])
-@pytest.mark.parametrize("k", [1, 2, 3, 4, 8, 16])
+@pytest.mark.parametrize("n_q,n_kv", [(32, 32), (32, 16), (48, 16), (32, 8), (64, 8), (32, 2)])
+@pytest.mark.parametrize("k", [1, 2, 3, 4, 7, 8, 16])
 def test_verify_parity(n_q, n_kv, k):
     ctx = [max(c, k) for c in CTX] + [k, k + 1]
     wl, batch = W.make_custom(n_q, n_kv, ctx, q_lens=[k] * len(ctx), seed=500 + 7 * k + n_q // n_kv,
@@ -45,7 +47,8 @@ def test_verify_parity(n_q, n_kv, k):
     kc, vc = oracle_after_append(wl)
     ref = oracle.paged_attention(batch.q, batch.cu_q_lens, kc, vc, batch.block_tables, batch.context_lens, wl.scale,
                                  n_q=wl.n_q)
-    on_decode = (n_q // n_kv) * k <= 8
+    G = n_q // n_kv
+    on_decode = G * k <= 32 or 128 % G != 0
     for part in ((0, 16, 256) if on_decode else (0,)):
         out, ws = _verify(d, batch, k, partition_size=part)
         assert_close(out.cpu().numpy(), ref, what=f"G={n_q // n_kv} k={k} part={part}")
@@ -71,7 +74,7 @@ def test_verify_last_row_is_decode_and_bf16_out():
     assert np.max(np.abs(o16.view(t.int16).cpu().numpy().astype(np.int32) - want)) <= 1
 
 
-@pytest.mark.parametrize("n_q,n_kv,k", [(32, 8, 2), (64, 8, 4)])  # decode path, prefill path
+@pytest.mark.parametrize("n_q,n_kv,k", [(32, 8, 2), (64, 8, 4), (64, 8, 8)])  # decode: 1 and 2 CTAs; prefill
 def test_verify_short_context_flags(n_q, n_kv, k):
     wl, batch = W.make_custom(n_q, n_kv, [50, 60], q_lens=[k, k], seed=530 + k, materialize_logical=False)
     d = DevWorkload(wl)
