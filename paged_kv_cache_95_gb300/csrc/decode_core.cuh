@@ -362,8 +362,9 @@ __device__ __forceinline__ void decode_block_fp8(DecodeAcc &acc, const uint32_t 
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int kk = 4 * h + i;
-            const uint32_t a[4] = {e4m3x2_to_f16x2(wa[i]), e4m3x2_to_f16x2(wb[i]), e4m3x2_to_f16x2(wa[i] >> 16),
-                                   e4m3x2_to_f16x2(wb[i] >> 16)};
+            uint32_t a[4];
+            e4m3x4_to_f16x2x2(wa[i], a[0], a[2]);
+            e4m3x4_to_f16x2x2(wb[i], a[1], a[3]);
             if (i & 1)
                 mma_f16_16816(c2, a, bq[kk][0], bq[kk][1]);
             else
@@ -435,11 +436,13 @@ __device__ __forceinline__ void decode_block_fp8(DecodeAcc &acc, const uint32_t 
     uint4 v1 = lds128(vb + (k0 + 1) * 128 + ((n ^ ((k0 + 1) & 7)) << 4));
     uint4 v2 = lds128(vb + (k0 + 8) * 128 + ((n ^ ((k0 + 8) & 7)) << 4));
     uint4 v3 = lds128(vb + (k0 + 9) * 128 + ((n ^ ((k0 + 9) & 7)) << 4));
-    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-    if (!keep(k0)) v0 = zero;
-    if (!keep(k0 + 1)) v1 = zero;
-    if (!keep(k0 + 8)) v2 = zero;
-    if (!keep(k0 + 9)) v3 = zero;
+    if (lo > 0 || valid < kBlockSize) {  // (warp-uniform: only the window's first block and the last one)
+        const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+        if (!keep(k0)) v0 = zero;
+        if (!keep(k0 + 1)) v1 = zero;
+        if (!keep(k0 + 8)) v2 = zero;
+        if (!keep(k0 + 9)) v3 = zero;
+    }
     const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w}, w1[4] = {v1.x, v1.y, v1.z, v1.w};
     const uint32_t w2[4] = {v2.x, v2.y, v2.z, v2.w}, w3[4] = {v3.x, v3.y, v3.z, v3.w};
 #pragma unroll
@@ -448,8 +451,9 @@ __device__ __forceinline__ void decode_block_fp8(DecodeAcc &acc, const uint32_t 
         const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
         const uint32_t pa = __byte_perm(w0[mt >> 1], w1[mt >> 1], sel);
         const uint32_t pb = __byte_perm(w2[mt >> 1], w3[mt >> 1], sel);
-        const uint32_t a[4] = {e4m3x2_to_f16x2(pa), e4m3x2_to_f16x2(pa >> 16), e4m3x2_to_f16x2(pb),
-                               e4m3x2_to_f16x2(pb >> 16)};
+        uint32_t a[4];
+        e4m3x4_to_f16x2x2(pa, a[0], a[1]);
+        e4m3x4_to_f16x2x2(pb, a[2], a[3]);
         mma_f16_16816(acc.o[mt], a, pb0, pb1);
         mma_f16_16816(acc.o[mt], a, pr0, pr1);
     }

@@ -164,6 +164,16 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// D(16x8, f32) += A(16x32, E4M3, row) * B(32x8, E4M3, col): 8-bit operands, four
+// per register, the lower k in the lower byte.
+__device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 // 16-byte shared-memory load.
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     uint4 v;
@@ -184,6 +194,15 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
     const uint16_t c = static_cast<uint16_t>(two_codes & 0xFFFFu);
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(c));
     return r;
+}
+
+// Four E4M3 codes -> two packed f16x2 (bytes 0-1 -> lo, bytes 2-3 -> hi): the
+// register halves go straight to the conversions, with no shift.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four_codes, uint32_t &lo, uint32_t &hi) {
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, a;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(four_codes));
 }
 
 // Two floats -> two E4M3 codes, nearest even, saturating to +-448; `lo` in the low byte.
