@@ -2,11 +2,18 @@
 """Benchmark of the paged decode-attention hot path on GB300.
 
 One step = the whole decode path over one batch: append the step's new K/V
-through slot_mapping (kv_reshape_and_cache), then paged decode attention with
-split-KV partitions and their log-sum-exp merge (paged_attention_decode).
+and run paged decode attention with split-KV partitions and their log-sum-exp
+merge.  A decode-only batch does both in one call (paged_attention_decode_append:
+the decode kernel writes each sequence's new row itself); a mixed batch first
+appends its rows through slot_mapping (kv_reshape_and_cache), then runs its
+causal chunks (paged_attention_prefill_chunk) and the decodes
+(paged_attention_decode).  The two-call form of a decode-only step is reported
+alongside (rows.two_call_step).
 The metric is KV-read throughput: the logical K+V bytes the attention reads
 (sum over sequences of ctx * n_kv * 128 * 2 * 2) per second, with sequences/s
-and tokens/s alongside.
+and tokens/s alongside.  The step time is taken over the whole timed loop; the
+per-kernel times come from CUDA events recorded on a sample of its steps (about
+100), since an event between two launches costs them their overlap.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload NAME]
@@ -242,12 +249,21 @@ def run_ours(args):
     pool_bytes = 2 * k_cache.numel() * 2
 
     stream = torch.cuda.current_stream(dev)
-    ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(args.steps)]
+    # Per-kernel CUDA events on a sample of the timed steps (every `every`-th step):
+    # an event between two launches breaks their programmatic-dependent overlap, so
+    # recording them on every step would slow the very loop being timed.
+    every = max(1, args.steps // 100)
+    sampled = list(range(0, args.steps, every))
+    ev = {i: tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for i in sampled}
+    # Decode-only batches run the step as one call that appends each sequence's new
+    # row inside the decode kernel; a mixed batch appends its chunk rows first.
+    fused = chunk is None
 
     def step(i=None):
         if i is not None:
             ev[i][0].record(stream)
-        P.kv_reshape_and_cache(new_k, new_v, k_cache, v_cache, slots)
+        if not fused:
+            P.kv_reshape_and_cache(new_k, new_v, k_cache, v_cache, slots)
         if i is not None:
             ev[i][1].record(stream)
         if chunk is not None:
@@ -255,7 +271,11 @@ def run_ours(args):
                                             workspace=cws)
         if i is not None:
             ev[i][2].record(stream)
-        P.paged_attention_decode(out, q, k_cache, v_cache, tables, lens, wl.scale, workspace=ws)
+        if fused:
+            P.paged_attention_decode_append(out, q, new_k, new_v, k_cache, v_cache, tables, lens, wl.scale,
+                                            workspace=ws)
+        else:
+            P.paged_attention_decode(out, q, k_cache, v_cache, tables, lens, wl.scale, workspace=ws)
         if i is not None:
             ev[i][3].record(stream)
 
@@ -272,7 +292,7 @@ def run_ours(args):
     w0 = time.time()
     start.record(stream)
     for i in range(args.steps):
-        step(i)
+        step(i if i % every == 0 else None)
     end.record(stream)
     torch.cuda.synchronize(dev)
     w1 = time.time()
@@ -282,9 +302,9 @@ def run_ours(args):
     clocks.stop()
 
     total_ms = start.elapsed_time(end)
-    decode_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
-    prefill_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev) if chunk is not None else None
-    append_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    decode_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev.values())
+    prefill_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev.values()) if chunk is not None else None
+    append_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev.values())
     t_max = max_over_ranks(total_ms / 1e3, dist, device=dev)
     ms_per_step = t_max / args.steps * 1e3
     value = world * (kv_bytes + chunk_kv_bytes) * args.steps / t_max / 1e9
@@ -306,15 +326,23 @@ def run_ours(args):
     bi += sum(x.numel() * x.element_size() for x in c_in)
     bo += hc_out.numel() * hc_out.element_size() if chunk is not None else 0
 
+    if fused:  # the slot mapping is not an input of the one-call step
+        bi -= slots.numel() * slots.element_size()
+
     def e2e_step():
-        for h, d in zip(h_in + c_in, d_in + c_dev):
-            d.copy_(h, non_blocking=True)
-        P.kv_reshape_and_cache(d_in[1], d_in[2], k_cache, v_cache, d_in[3])
-        if chunk is not None:
-            P.paged_attention_prefill_chunk(cout, c_dev[0], c_dev[1], cmax, k_cache, v_cache, c_dev[2], c_dev[3],
-                                            wl.scale, workspace=cws)
-            hc_out.copy_(cout, non_blocking=True)
-        P.paged_attention_decode(out, d_in[0], k_cache, v_cache, d_in[4], d_in[5], wl.scale, workspace=ws)
+        for k_, (h, d) in enumerate(zip(h_in + c_in, d_in + c_dev)):
+            if not (fused and k_ == 3):
+                d.copy_(h, non_blocking=True)
+        if fused:
+            P.paged_attention_decode_append(out, d_in[0], d_in[1], d_in[2], k_cache, v_cache, d_in[4], d_in[5],
+                                            wl.scale, workspace=ws)
+        else:
+            P.kv_reshape_and_cache(d_in[1], d_in[2], k_cache, v_cache, d_in[3])
+            if chunk is not None:
+                P.paged_attention_prefill_chunk(cout, c_dev[0], c_dev[1], cmax, k_cache, v_cache, c_dev[2], c_dev[3],
+                                                wl.scale, workspace=cws)
+                hc_out.copy_(cout, non_blocking=True)
+            P.paged_attention_decode(out, d_in[0], k_cache, v_cache, d_in[4], d_in[5], wl.scale, workspace=ws)
         h_out.copy_(out, non_blocking=True)
 
     for _ in range(args.warmup):
@@ -330,12 +358,12 @@ def run_ours(args):
     e2e_t = max_over_ranks(e0.elapsed_time(e1) / 1e3, dist, device=dev)
     e2e_value = world * (kv_bytes + chunk_kv_bytes) * args.steps / e2e_t / 1e9
 
-    # kv_cache_write + (prefill chunk) + paged decode + split-KV merge (when a context is split)
-    launches_per_step = 2 + (1 if chunk is not None else 0) + (1 if ws_bytes > 256 else 0)
+    # [kv_cache_write] + (prefill chunk) + paged decode (with the append when fused) + split-KV merge
+    launches_per_step = (1 if fused else 2) + (1 if chunk is not None else 0) + (1 if ws_bytes > 256 else 0)
 
     # the next hot-path rows on the same batch (single-GPU runs; outside the timed region)
     rows = _row_variants(P, torch, dev, wl, batch, k_cache, v_cache, new_k, new_v, slots, q, tables, lens,
-                         decode_ms, kv_bytes, steps=min(args.steps, 200)) if world == 1 else None
+                         decode_ms, kv_bytes, steps=min(args.steps, 200), fused=fused) if world == 1 else None
 
     if rank == 0:
         peak, peak_src = measured_peaks()
@@ -362,7 +390,10 @@ def run_ours(args):
             "sequences_per_s": round(world * batch.num_seqs * args.steps / t_max, 1),
             "tokens_per_s": round(world * batch.num_seqs * args.steps / t_max, 1),
             "config": _config(wl, batch, kv_bytes, pool_bytes, world),
-            "roofline": {"bound": "hbm", "kernel": "paged_attention_decode (decode kernel + split-KV merge kernel)",
+            "roofline": {"bound": "hbm",
+                         "kernel": ("paged_attention_decode_append (decode kernel with the step's append + split-KV "
+                                    "merge kernel)") if fused else
+                         "paged_attention_decode (decode kernel + split-KV merge kernel)",
                          "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                          if peak_src == "measured" else "fallback 6.8 TB/s",
@@ -397,7 +428,7 @@ def _time_events(torch, stream, fn, steps, warmup=3):
 
 
 def _row_variants(P, torch, dev, wl, batch, k_cache, v_cache, new_k, new_v, slots, q, tables, lens, decode_ms,
-                  kv_bytes, steps):
+                  kv_bytes, steps, fused=False):
     """FP8 cache, sliding window and host block manager on the bench batch."""
     peak, _ = measured_peaks()
     stream = torch.cuda.current_stream(dev)
@@ -471,6 +502,18 @@ def _row_variants(P, torch, dev, wl, batch, k_cache, v_cache, new_k, new_v, slot
                             "note": "host C++ through ctypes: one batched append of a token per sequence + "
                                     "block-table emission"}
     bm.close()
+
+    if fused:  # the same step as two calls: append kernel, then decode (+ merge)
+        out2 = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+        ws2 = torch.zeros(P.paged_attention_workspace_size(B, wl.n_q, batch.max_blocks_per_seq, 0,
+                                                           P.cache_desc(k_cache)), dtype=torch.uint8, device=dev)
+
+        def two_calls():
+            P.kv_reshape_and_cache(new_k, new_v, k_cache, v_cache, slots)
+            P.paged_attention_decode(out2, q, k_cache, v_cache, tables, lens, wl.scale, workspace=ws2)
+        ms2 = _time_events(torch, stream, two_calls, steps)
+        res["two_call_step"] = {"append_then_decode_ms": round(ms2, 5), "one_call_ms": round(decode_ms, 5),
+                                "one_call_speedup": round(ms2 / decode_ms, 3)}
     return res
 
 

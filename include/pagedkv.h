@@ -241,6 +241,37 @@ PKV_API int paged_attention_decode(void *out, int32_t out_dtype, const void *q, 
 #define PKV_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
 
 /*
+ * paged_attention_decode_append -- one decode step in one launch: appends each
+ * sequence's new K/V row and attends over the cache including it.
+ *
+ * Same result as kv_reshape_and_cache() with slot_mapping[b] = the slot of
+ * position ctx_b - 1 (row (ctx_b - 1) % 16 of block
+ * block_tables[b][(ctx_b - 1) / 16]) followed by paged_attention_decode()
+ * (sections as for those two calls: "LLM 推理全过程的维度变化与核心公式", "Decode
+ * 阶段维度流转" -- the step's K/V is appended to the cache, then the single query
+ * row attends over all of it).  The CTAs that read a sequence's last block put
+ * the new row into their shared-memory copy of it, and one CTA per KV head
+ * writes it to the pool, so no separate append kernel runs and no CTA reads the
+ * slot from memory.  The pool afterwards equals the two-call result bit for bit.
+ *
+ *   key, value : bf16 [num_seqs][num_kv_heads][head_dim], device, 16-B aligned:
+ *                the row of position ctx_b - 1 of each sequence
+ *   k_cache, v_cache : the bf16 pool (written at those slots)
+ *   other arguments and the workspace: as paged_attention_decode (no window,
+ *   bf16 cache only).
+ * A sequence with an out-of-range context length or an invalid id in its last
+ * block gets no row written (the status word flags it, as for the decode).
+ * Errors: as paged_attention_decode; PKV_ERR_INVALID_ARG for a null or
+ * misaligned key / value.
+ */
+PKV_API int paged_attention_decode_append(void *out, int32_t out_dtype, const void *q, const void *key,
+                                          const void *value, void *k_cache, void *v_cache,
+                                          const int32_t *block_tables, const int32_t *context_lens, int32_t num_seqs,
+                                          int32_t num_q_heads, int32_t max_blocks_per_seq, float scale,
+                                          int32_t partition_size, const pkv_cache_desc *cache, void *workspace,
+                                          size_t workspace_bytes, void *stream);
+
+/*
  * paged_attention_decode_static_scratch -- paged_attention_decode without a
  * caller-provided workspace; it allocates nothing.  (The pages have no
  * counterpart: this is a deployment convenience, not part of the method.)

@@ -23,6 +23,7 @@ from .pagedkv import (  # noqa: F401
     kv_reshape_and_cache_fp8,
     load_library,
     paged_attention_decode,
+    paged_attention_decode_append,
     paged_attention_decode_static_scratch,
     paged_attention_prefill_chunk,
     paged_attention_prefill_workspace_size,

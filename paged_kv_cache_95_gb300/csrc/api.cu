@@ -337,13 +337,17 @@ size_t paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads, int
 namespace {
 
 // Shared by the decode entry points; window = 0 means no sliding window; k_scale /
-// v_scale non-null select the FP8 cache (cache->dtype PKV_DTYPE_FP8_E4M3).
+// v_scale non-null select the FP8 cache (cache->dtype PKV_DTYPE_FP8_E4M3); new_key /
+// new_value non-null append each sequence's new row at position ctx - 1 in the same launch.
 int decode_impl(void *out, int32_t out_dtype, const void *q, const void *k_cache, const void *v_cache,
                 const float *k_scale, const float *v_scale, const int32_t *block_tables,
                 const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq,
                 float scale, int32_t window, int32_t partition_size, const pkv_cache_desc *cache, void *workspace,
-                size_t workspace_bytes, void *stream) {
+                size_t workspace_bytes, void *stream, const void *new_key = nullptr,
+                const void *new_value = nullptr) {
     const bool fp8 = k_scale != nullptr;
+    const bool append = new_key != nullptr;
+    if (append && (fp8 || !new_value || !aligned(new_key, 16) || !aligned(new_value, 16))) return PKV_ERR_INVALID_ARG;
     if (int rc = fp8 ? check_cache_fp8(cache) : check_cache(cache)) return rc;
     if (fp8 && (!v_scale || !aligned(k_scale, 16) || !aligned(v_scale, 16))) return PKV_ERR_INVALID_ARG;
     if (int rc = check_group(num_q_heads, cache->num_kv_heads)) return rc;
@@ -430,7 +434,15 @@ int decode_impl(void *out, int32_t out_dtype, const void *q, const void *k_cache
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
-    if (fp8) {
+    if (append) {
+        pkv::DecodeParamsAppend pa{};
+        static_cast<pkv::DecodeParams &>(pa) = p;
+        pa.new_k = new_key;
+        pa.new_v = new_value;
+        pa.k_cache = const_cast<void *>(k_cache);
+        pa.v_cache = const_cast<void *>(v_cache);
+        e = pkv::launch_paged_decode_append(kmap, vmap, pa, var, s);
+    } else if (fp8) {
         pkv::DecodeParamsFp8 p8{};
         static_cast<pkv::DecodeParams &>(p8) = p;
         p8.k_scale = k_scale;
@@ -451,6 +463,17 @@ int paged_attention_decode(void *out, int32_t out_dtype, const void *q, const vo
     return decode_impl(out, out_dtype, q, k_cache, v_cache, nullptr, nullptr, block_tables, context_lens, num_seqs,
                        num_q_heads, max_blocks_per_seq, scale, 0, partition_size, cache, workspace, workspace_bytes,
                        stream);
+}
+
+int paged_attention_decode_append(void *out, int32_t out_dtype, const void *q, const void *key, const void *value,
+                                  void *k_cache, void *v_cache, const int32_t *block_tables,
+                                  const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                  int32_t max_blocks_per_seq, float scale, int32_t partition_size,
+                                  const pkv_cache_desc *cache, void *workspace, size_t workspace_bytes, void *stream) {
+    if (!key || !value) return PKV_ERR_INVALID_ARG;
+    return decode_impl(out, out_dtype, q, k_cache, v_cache, nullptr, nullptr, block_tables, context_lens, num_seqs,
+                       num_q_heads, max_blocks_per_seq, scale, 0, partition_size, cache, workspace, workspace_bytes,
+                       stream, key, value);
 }
 
 int paged_attention_decode_window(void *out, int32_t out_dtype, const void *q, const void *k_cache,

@@ -58,15 +58,17 @@ namespace pkv {
 
 namespace {
 
-template <bool FP8, bool VERIFY>
-using DecodeParamsT =
-    std::conditional_t<FP8, DecodeParamsFp8, std::conditional_t<VERIFY, DecodeParamsVerify, DecodeParams>>;
+template <bool FP8, bool VERIFY, bool APPEND = false>
+using DecodeParamsT = std::conditional_t<
+    FP8, DecodeParamsFp8,
+    std::conditional_t<VERIFY, DecodeParamsVerify, std::conditional_t<APPEND, DecodeParamsAppend, DecodeParams>>>;
 
 // NCT: 8-column MMA tiles per CTA (2 only for multi-token verify with 9..16 columns).
-template <int NW, int ST, bool FP8, bool VERIFY = false, int NCT = 1>
+// APPEND: the step's new K/V row of each sequence is appended in this launch.
+template <int NW, int ST, bool FP8, bool VERIFY = false, int NCT = 1, bool APPEND = false>
 __global__ void __launch_bounds__(NW * 32)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                        const DecodeParamsT<FP8, VERIFY> p) {
+                        const DecodeParamsT<FP8, VERIFY, APPEND> p) {
     constexpr uint32_t kStage = FP8 ? kStageBytes8 : kStageBytes;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem =
@@ -79,6 +81,7 @@ __global__ void __launch_bounds__(NW * 32)
     const int b = blockIdx.z;
     const int g = hs / p.head_splits;
     static_assert(NCT == 1 || (NCT == 2 && VERIFY && !FP8), "two column tiles: verify only");
+    static_assert(!APPEND || (!FP8 && !VERIFY && NCT == 1), "append: bf16 decode only");
     const int hpc = p.heads_per_cta;
     const int hsl = hs - g * p.head_splits;  // this CTA's share of the group's columns
     const int h0 = g * p.group + hsl * hpc;
@@ -109,7 +112,8 @@ __global__ void __launch_bounds__(NW * 32)
     // ---- sequence extent (device data: checked, never trusted) ----
     int ctx = __ldg(p.context_lens + b);
     const int max_ctx = p.max_blocks * kBlockSize;
-    if (ctx < 1 || ctx > max_ctx) {
+    const bool ctx_ok = ctx >= 1 && ctx <= max_ctx;
+    if (!ctx_ok) {
         if (part == 0 && threadIdx.x == 0 && p.status) atomicOr(p.status, kStatusBadContextLen);
         ctx = ctx < 1 ? 0 : max_ctx;
     }
@@ -134,6 +138,17 @@ __global__ void __launch_bounds__(NW * 32)
     const int nblk = min(p.part_blocks, nblocks - blk_begin);
     const int nmine = nblk > warp ? (nblk - warp + NW - 1) / NW : 0;
     const int32_t *table = p.block_tables + static_cast<size_t>(b) * p.max_blocks;
+
+    // Append: lane l holds 16 bytes of the new row (K for lanes 0-15, V for 16-31;
+    // dims 64 * ((l >> 3) & 1) + 8 * (l & 7) ..), loaded early by the last partition's CTAs.
+    uint4 app = make_uint4(0u, 0u, 0u, 0u);
+    if constexpr (APPEND) {
+        if (ctx_ok && part == nparts - 1) {
+            const size_t e = (static_cast<size_t>(b) * p.n_kv + g) * kHeadDim + 64 * ((lane >> 3) & 1) + 8 * (lane & 7);
+            const void *src = lane < 16 ? p.new_k : p.new_v;
+            app = __ldg(reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(src) + e));
+        }
+    }
 
     const uint32_t stage_base = smem_u32(smem) + warp * (ST * kStage);
     // FP8: the scale rows of each stage sit after all warps' code rings.
@@ -212,6 +227,22 @@ __global__ void __launch_bounds__(NW * 32)
             if (lane == 0 && p.status) atomicOr(p.status, kStatusBadBlockId);
         }
         const uint32_t kb = stage_base + s * kStage;
+        if constexpr (APPEND) {
+            if (ctx_ok && j == nblocks - 1 && valid > 0) {
+                // The new row r of the last block: into this warp's copy of the block (K and V,
+                // 16 bytes per lane at the swizzled position) and, from one CTA per KV head, to the pool.
+                const int r = (ctx - 1) & (kBlockSize - 1);
+                const int box = (lane >> 3) & 1, ch = lane & 7;
+                sts128(kb + (lane >> 4) * kTileBytes + box * kBoxBytes + r * 128 + ((ch ^ (r & 7)) << 4), app);
+                if (hsl == 0) {
+                    void *pool = lane < 16 ? p.k_cache : p.v_cache;
+                    const size_t e = ((static_cast<size_t>(phys) * p.n_kv + g) * kBlockSize + r) * kHeadDim +
+                                     64 * box + 8 * ch;
+                    *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(pool) + e) = app;
+                }
+                __syncwarp();
+            }
+        }
         if constexpr (FP8) {
             decode_block_fp8(acc, bq, kb, kb + kTileBytes8, scale_base + s * kStageScaleBytes, lo, valid, sl2, lane);
         } else if constexpr (VERIFY && NCT == 2) {
@@ -413,11 +444,11 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lse_merge_kernel(const Decod
     }
 }
 
-template <int NW, int ST, bool FP8 = false, bool VERIFY = false, int NCT = 1>
-cudaError_t launch_variant(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParamsT<FP8, VERIFY> &p,
-                           cudaStream_t stream) {
+template <int NW, int ST, bool FP8 = false, bool VERIFY = false, int NCT = 1, bool APPEND = false>
+cudaError_t launch_variant(const CUtensorMap &kmap, const CUtensorMap &vmap,
+                           const DecodeParamsT<FP8, VERIFY, APPEND> &p, cudaStream_t stream) {
     const dim3 grid(p.max_parts, p.n_kv * p.head_splits, p.num_seqs);
-    cudaError_t e = launch_pdl(paged_decode_kernel<NW, ST, FP8, VERIFY, NCT>, grid, dim3(NW * 32),
+    cudaError_t e = launch_pdl(paged_decode_kernel<NW, ST, FP8, VERIFY, NCT, APPEND>, grid, dim3(NW * 32),
                                FP8 ? decode_fp8_smem_bytes() : decode_smem_bytes({NW, ST}), stream, kmap, vmap, p);
     if (e != cudaSuccess) return e;
     int rows_per_seq = 1;
@@ -436,7 +467,10 @@ cudaError_t prepare_variant() {
     e = cudaFuncSetAttribute(paged_decode_kernel<NW, ST, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(decode_smem_bytes({NW, ST})));
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(paged_decode_kernel<NW, ST, false, true, 2>,
+    e = cudaFuncSetAttribute(paged_decode_kernel<NW, ST, false, true, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(decode_smem_bytes({NW, ST})));
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(paged_decode_kernel<NW, ST, false, false, 1, true>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(decode_smem_bytes({NW, ST})));
 }
@@ -494,6 +528,15 @@ cudaError_t launch_paged_verify(const CUtensorMap &kmap, const CUtensorMap &vmap
     if (v.warps == 8 && v.stages == 2)
         return two ? launch_variant<8, 2, false, true, 2>(kmap, vmap, p, stream)
                    : launch_variant<8, 2, false, true>(kmap, vmap, p, stream);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_paged_decode_append(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParamsAppend &p,
+                                       DecodeVariant v, cudaStream_t stream) {
+    if (v.warps == 4 && v.stages == 2) return launch_variant<4, 2, false, false, 1, true>(kmap, vmap, p, stream);
+    if (v.warps == 4 && v.stages == 3) return launch_variant<4, 3, false, false, 1, true>(kmap, vmap, p, stream);
+    if (v.warps == 4 && v.stages == 4) return launch_variant<4, 4, false, false, 1, true>(kmap, vmap, p, stream);
+    if (v.warps == 8 && v.stages == 2) return launch_variant<8, 2, false, false, 1, true>(kmap, vmap, p, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -85,6 +85,19 @@ struct DecodeParamsVerify : DecodeParams {
     int32_t q_per_seq;
 };
 
+// Decode with the step's token appended in the same launch: new_k / new_v (bf16
+// [num_seqs][n_kv][128]) hold each sequence's new K/V row, which belongs at
+// position ctx - 1.  The CTAs that read the sequence's last block put the row
+// into their shared-memory copy of that block, and the first CTA of each KV
+// head's last partition writes it to the pool (k_cache / v_cache), so no CTA of
+// the launch reads the slot from memory.
+struct DecodeParamsAppend : DecodeParams {
+    const void *new_k;
+    const void *new_v;
+    void *k_cache;
+    void *v_cache;
+};
+
 struct DecodeVariant {
     int warps;
     int stages;
@@ -105,6 +118,8 @@ cudaError_t launch_paged_decode_fp8(const CUtensorMap &kmap, const CUtensorMap &
                                     cudaStream_t stream);
 cudaError_t launch_paged_verify(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParamsVerify &p,
                                 DecodeVariant v, cudaStream_t stream);
+cudaError_t launch_paged_decode_append(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParamsAppend &p,
+                                       DecodeVariant v, cudaStream_t stream);
 
 // ---- K4: causal chunked prefill on tcgen05 ---------------------------------------
 struct PrefillParams {

@@ -78,6 +78,8 @@ def _declare(lib):
     lib.paged_attention_workspace_size.restype = sz
     lib.paged_attention_decode.argtypes = [P, i32, P, P, P, P, P, i32, i32, i32, f32, i32, D, P, sz, P]
     lib.paged_attention_decode.restype = ctypes.c_int
+    lib.paged_attention_decode_append.argtypes = [P, i32, P, P, P, P, P, P, P, i32, i32, i32, f32, i32, D, P, sz, P]
+    lib.paged_attention_decode_append.restype = ctypes.c_int
     lib.paged_attention_decode_window.argtypes = [P, i32, P, P, P, P, P, i32, i32, i32, f32, i32, i32, D, P, sz, P]
     lib.paged_attention_decode_window.restype = ctypes.c_int
     lib.paged_attention_decode_fp8.argtypes = [P, i32, P, P, P, P, P, P, P, i32, i32, i32, f32, i32, i32, D, P, sz, P]
@@ -489,6 +491,40 @@ def paged_attention_prefill_chunk(out, q, cu_q_lens, max_q_len: int, k_cache, v_
         _ptr(v_cache), _ptr(block_tables), _ptr(context_lens), B, int(n_q), int(block_tables.shape[1]),
         float(scale), ctypes.byref(desc), _ptr(workspace), int(workspace.numel()), _stream(stream))
     _raise("paged_attention_prefill_chunk", rc)
+    return workspace
+
+
+def paged_attention_decode_append(out, q, key, value, k_cache, v_cache, block_tables, context_lens, scale: float,
+                                  workspace=None, partition_size: int = 0, stream=None):
+    """One decode step in one launch: writes ``key`` / ``value`` (bf16
+    [B, n_kv, 128], each sequence's row of position ctx - 1) into the pool and
+    attends, as kv_reshape_and_cache + paged_attention_decode would."""
+    torch = _torch()
+    desc = cache_desc(k_cache)
+    _check(v_cache, "v_cache", torch.bfloat16, ndim=4)
+    _need(tuple(v_cache.shape) == tuple(k_cache.shape), "v_cache shape must equal k_cache shape")
+    _check(q, "q", torch.bfloat16, ndim=3, last=HEAD_DIM)
+    B, n_q, _ = q.shape
+    n_kv = int(k_cache.shape[1])
+    for name, t in (("key", key), ("value", value)):
+        _check(t, name, torch.bfloat16, ndim=3, last=HEAD_DIM)
+        _need(tuple(t.shape) == (B, n_kv, HEAD_DIM), f"{name} must be [num_seqs, num_kv_heads, 128]")
+    _check(out, "out", out.dtype, ndim=3)
+    _need(tuple(out.shape) == tuple(q.shape), "out must have q's shape")
+    _check(block_tables, "block_tables", torch.int32, ndim=2)
+    _check(context_lens, "context_lens", torch.int32, ndim=1)
+    _need(block_tables.shape[0] == B and context_lens.shape[0] == B, "one table row and length per sequence")
+    max_blocks = int(block_tables.shape[1])
+    if workspace is None:
+        nbytes = paged_attention_workspace_size(B, n_q, max_blocks, partition_size, desc)
+        _need(nbytes > 0, "invalid sizes for paged_attention_decode_append")
+        workspace = torch.zeros(nbytes, dtype=torch.uint8, device=q.device)
+    _check(workspace, "workspace", torch.uint8, ndim=1)
+    rc = load_library().paged_attention_decode_append(
+        _ptr(out), _out_dtype(out), _ptr(q), _ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache),
+        _ptr(block_tables), _ptr(context_lens), int(B), int(n_q), max_blocks, float(scale), int(partition_size),
+        ctypes.byref(desc), _ptr(workspace), int(workspace.numel()), _stream(stream))
+    _raise("paged_attention_decode_append", rc)
     return workspace
 
 

@@ -93,6 +93,26 @@ def test_decode_argument_errors(lib, kw, want):
     assert _decode(lib, desc(), **kw) == want
 
 
+def test_decode_append_argument_errors(lib):
+    c = desc()
+
+    def call(**kw):
+        a = dict(out=FAKE, q=FAKE, key=FAKE, value=FAKE, k=FAKE, B=4, nq=32, wsb=1 << 20)
+        a.update(kw)
+        return lib.paged_attention_decode_append(a["out"], 1, a["q"], a["key"], a["value"], a["k"], FAKE, FAKE, FAKE,
+                                                 a["B"], a["nq"], 8, 0.088, 0, ctypes.byref(c), FAKE, a["wsb"], None)
+    assert call(key=None) == P.PKV_ERR_INVALID_ARG
+    assert call(value=None) == P.PKV_ERR_INVALID_ARG
+    assert call(key=FAKE + 8) == P.PKV_ERR_INVALID_ARG     # new rows must be 16-byte aligned
+    assert call(value=FAKE + 4) == P.PKV_ERR_INVALID_ARG
+    assert call(q=None) == P.PKV_ERR_INVALID_ARG
+    assert call(nq=96) == P.PKV_ERR_UNSUPPORTED
+    assert call(wsb=100) == P.PKV_ERR_WORKSPACE_TOO_SMALL
+    c8 = desc(dtype=P.PKV_DTYPE_FP8_E4M3)                   # bf16 pool only
+    assert lib.paged_attention_decode_append(FAKE, 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 32, 8, 0.088, 0,
+                                             ctypes.byref(c8), FAKE, 1 << 20, None) == P.PKV_ERR_UNSUPPORTED
+
+
 def test_decode_window_argument_errors(lib):
     c = desc()
 
