@@ -7,13 +7,17 @@
 // j <= c + i of KV head g = floor(h / G):
 //     out[i][h] = sum_{j <= c+i} softmax_j(scale <q_i,h, K_j,g>) V_j,g
 //
-// Tiling (one CTA = one 128-row tile of one sequence and one KV group):
-//  * The 128 rows of the MMA tile pack 128/G query positions x the G heads of
+// Tiling (one CTA = two 128-row tiles of one sequence and one KV group):
+//  * The 128 rows of an MMA tile pack 128/G query positions x the G heads of
 //    the group (row r = position (r / G), head (r % G)), so every K/V tile is
-//    shared by the whole group.  Q is loaded once by TMA (128-byte swizzle).
+//    shared by the whole group.  A CTA holds two adjacent row tiles (Q0 and
+//    Q1, loaded once by TMA, 128-byte swizzle) and walks the key tiles once for
+//    both: each K and V tile copied into shared memory feeds two tiles' MMAs,
+//    which halves the copy bytes per flop (the copies landing in shared memory
+//    are what limits a one-tile CTA).  Tile 0 stops at its own last key tile.
 //  * Keys are walked in tiles of 128 (= 8 paged blocks of 16).  Each paged
 //    block's K and V tiles (4 KB each) are gathered from the block table with
-//    ONE TMA copy apiece into separate 3-deep K and V rings.  The copy's 5-D
+//    ONE TMA copy apiece into separate 2-deep K and V rings.  The copy's 5-D
 //    view of the pool lands a tile as [slot group (keys 0-7 | 8-15)][dim half]
 //    [8 slots][128 B], four 1 KB 128-byte-swizzle atoms, so that eight tiles
 //    side by side form one canonical UMMA operand: K as a K-major B operand
@@ -21,39 +25,43 @@
 //    as an MN-major B operand (dim halves 1 KB apart, key groups 2 KB apart).
 //
 // Warp roles (warp specialisation, all hand-offs through mbarriers):
-//  * warps 8 and 10: TMA producers for K and V.  Lane t < 8 reads block t of a
-//    key tile from the block table (one tile ahead) and issues that block's
-//    copy: the eight copies go out as one warp instruction, which keeps more
-//    of them in flight than a loop in one lane.  A K slot is
-//    refilled as soon as the S MMA that read it completes, a V slot as soon as
-//    its P V MMAs complete.
-//  * warp 9 (one lane): MMA issuer; also owns the tensor-memory allocation.
-//    S(k) = Q K(k)^T (M=128, N=128, K=128) goes to tensor-memory buffer k % 2
-//    (columns [0,128) or [128,256)); O += P(k) V(k) accumulates in columns
-//    [256,384), with P(k) read from tensor memory as the A operand.  S(k+1) is
-//    issued before P(k) V(k), so the tensor core works while the softmax warps
-//    work; S(k+2) reuses buffer k % 2 once P(k) V(k) has completed.
-//  * warps 0-7 (256 threads): warps w and w+4 own tensor-memory lanes
-//    32*(w%4) .. +31 (= tile rows) and split the 128 columns: each thread holds
-//    one row's 64 scores of its half, applies the causal/length mask by index
-//    (skipped for fully visible 32-key chunks), and the two halves exchange
-//    their row maxima through shared memory (a 64-thread named barrier per
-//    pair).  Each updates the running max and its half of the running sum
-//    (fp32, log2 domain) and writes P = 2^(s - m) back over its half as
-//    [bf16 head | bf16 remainder] (head = P truncated to bf16, remainder = the
-//    rest rounded to bf16; P V = P_hi V + P_lo V keeps the weights to ~2^-16
-//    relative, with integer and byte-permute operations only).  P is thereby double-buffered with S, so
-//    the softmax of tile k+1 never waits for P(k) V(k); it waits for it only
-//    when it must rescale O.  The exponent reference is only raised when a
-//    row's max grows by more than 2^8, in which case the row's O is rescaled in
-//    tensor memory; P stays <= 256.
-//  * Epilogue: O / l from tensor memory; a full tile is staged in shared
-//    memory (the K ring is free by then, same 128-byte-swizzled layout as the Q
-//    tile) and leaves by TMA store, a ragged last tile by 16-byte stores of its
-//    valid rows only (a whole-box store would overwrite the next sequence).
+//  * warps 16 and 18: TMA producers for K and V.  Lane t < 8 reads block t of
+//    a key tile from the block table (one tile ahead) and issues that block's
+//    copy: the eight copies go out as one warp instruction.  A K slot is
+//    refilled once both tiles' S MMAs that read it complete, a V slot once
+//    both tiles' P V MMAs complete.
+//  * warp 17 (one lane): MMA issuer; also owns the tensor-memory allocation
+//    (all 512 columns: S/P of tile t in [128t, 128t+128), O of tile t in
+//    [256 + 128t, +128)).  Per key tile k it issues, in this order,
+//        S0(k) = Q0 K(k)^T,  P1(k-1) V(k-1),  S1(k) = Q1 K(k)^T,  P0(k) V(k)
+//    (M=128, N=128), so the tensor core computes one tile's MMAs while the
+//    other tile's softmax runs (ping-pong).  An S MMA overwrites the columns
+//    of the P that the P V MMA issued just before it reads; MMAs of one thread
+//    execute in order, and the commit after S_t(k) completes only when every
+//    earlier MMA has, so when the softmax sees S_t(k) the previous P_t V is
+//    already in O_t.
+//  * warps 0-7 (tile 0) and 8-15 (tile 1), 256 threads per tile: warps w and
+//    w+4 of a tile own tensor-memory lanes 32*(w%4) .. +31 (= tile rows) and
+//    split the 128 columns: each thread handles one row's 64 scores of its
+//    half in two chunks of 32, applies the causal/length mask by index
+//    (skipped for fully visible chunks), and the two halves exchange their
+//    row maxima through shared memory (a 64-thread named barrier per pair).
+//    Each updates the running max and its half of the running sum (fp32,
+//    log2 domain) and writes P = 2^(s - m) back over each 32-key chunk as
+//    [16 columns bf16 head | 16 columns bf16 remainder] (head = P truncated
+//    to bf16, remainder = the rest rounded to bf16; P V = P_hi V + P_lo V
+//    keeps the weights to ~2^-16 relative).  The exponent reference is only
+//    raised when a row's max grows by more than 2^8, in which case the row's O
+//    is rescaled in tensor memory; P stays <= 256.
+//  * Epilogue per tile: O / l from tensor memory; a full tile is staged in
+//    shared memory (tile 1: in the K ring, free by then; tile 0, bf16 output:
+//    in its own Q buffer, whose MMAs have completed) in the output tensor map's
+//    128-byte-swizzled layout and leaves by TMA store; a ragged last tile (and
+//    tile 0 with fp32 output) by 16-byte stores of its valid rows only.
 //  * Keys at or past the context length and keys of blocks with an invalid id
-//    are masked by index and their V rows are zeroed in shared memory, so stale
-//    or NaN bytes cannot reach the result.
+//    are masked by index and their V rows are zeroed in shared memory (by each
+//    tile that reads them, before its P V), so stale or NaN bytes cannot reach
+//    the result.
 //
 // Every mbarrier wait is bounded; a role whose wait runs out raises a
 // CTA-wide abort flag, the others stop at their next wait, the CTA records
@@ -70,34 +78,36 @@ namespace pkv {
 
 namespace {
 
-constexpr int kSoftmaxWarps = 8;  // warps 0-7: warps w and w+4 share lanes 32*(w%4).. and split the columns
-constexpr int kProducerK = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kProducerV = 10;
-constexpr int kThreads = 11 * 32;
+constexpr int kRowTiles = 2;      // 128-row Q tiles per CTA
+constexpr int kSoftmaxWarps = 8;  // per tile: warps w and w+4 share lanes 32*(w%4).. and split the columns
+constexpr int kProducerK = kRowTiles * kSoftmaxWarps;  // warp 16
+constexpr int kMmaWarp = kProducerK + 1;               // warp 17
+constexpr int kProducerV = kProducerK + 2;             // warp 18
+constexpr int kThreads = (kProducerV + 1) * 32;        // 608
 
 constexpr uint32_t kHalfTile = 128 * 128;     // 16 KB: 128 rows x 128 bytes (Q dim half; staged output box)
 constexpr uint32_t kOpBytes = 2 * kHalfTile;  // 32 KB: a 128 x 128 bf16 operand
 constexpr uint32_t kBlkBytes = 4096;          // one paged (block, head) tile inside a K/V operand
-constexpr int kStagesK = 3;                              // K ring depth
-constexpr int kStagesV = 3;                              // V ring depth
-constexpr uint32_t kOffQ = 0;                            // Q tile: [dim half][128 rows][128 B]
-constexpr uint32_t kOffK = kOffQ + kOpBytes;             // K ring: kStagesK x 32 KB
-constexpr uint32_t kOffV = kOffK + kStagesK * kOpBytes;  // V ring: kStagesV x 32 KB
+constexpr int kStagesK = 2;                                // K ring depth
+constexpr int kStagesV = 2;                                // V ring depth
+constexpr uint32_t kOffQ = 0;                              // Q tiles: [tile][dim half][128 rows][128 B]
+constexpr uint32_t kOffK = kOffQ + kRowTiles * kOpBytes;   // K ring: kStagesK x 32 KB
+constexpr uint32_t kOffV = kOffK + kStagesK * kOpBytes;    // V ring: kStagesV x 32 KB
 constexpr uint32_t kOffBar = kOffV + kStagesV * kOpBytes;
-constexpr int kBarS = 1 + 2 * kStagesK + 2 * kStagesV;  // q_full, k_full/k_empty[kStagesK], v_full/v_empty[kStagesV],
-constexpr uint32_t kNumBars = kBarS + 6;                 // then s_full[2], p_full[2], o_done[2]
-constexpr uint32_t kOffTmem = kOffBar + 8 * 24;
+// q_full, k_full/k_empty[kStagesK], v_full/v_empty[kStagesV], then per tile s_full, p_full, o_done
+constexpr int kBarTile = 1 + 2 * kStagesK + 2 * kStagesV;
+constexpr uint32_t kNumBars = kBarTile + 3 * kRowTiles;
+constexpr uint32_t kOffTmem = kOffBar + 8 * 16;
 constexpr uint32_t kOffAbort = kOffTmem + 8;
-constexpr uint32_t kOffXch = kOffAbort + 8;  // per-row partial maxima [2 tiles][2 halves][128]; after the
-                                             // last tile, per-row partial sums [2 halves][128]
+constexpr uint32_t kXchBytes = 2 * 2 * 128 * 4;  // per tile: row maxima [key tile & 1][half][128]; then row sums
+constexpr uint32_t kOffXch = kOffAbort + 8;
 // The dynamic shared memory is declared 1024-byte aligned (the swizzle period of
 // the TMA/UMMA operands); the kernel checks it and refuses to run otherwise.
-constexpr uint32_t kSmemBytes = kOffXch + 2 * 2 * 128 * 4;
-constexpr uint32_t kTmemCols = 512;  // S/P 0 [0,128), S/P 1 [128,256), O [256,384)
+constexpr uint32_t kSmemBytes = kOffXch + kRowTiles * kXchBytes;
+constexpr uint32_t kTmemCols = 512;  // S/P of tile t: [128t, 128t + 128); O of tile t: [256 + 128t, +128)
 constexpr uint32_t kTmemO = 256;
 static_assert(kSmemBytes <= 232448, "prefill shared memory exceeds the per-CTA limit");
-static_assert(kNumBars <= 24, "barrier area");
+static_assert(kNumBars <= 16, "barrier area");
 
 // Instruction descriptor, kind::f16: D f32, A/B bf16, M = 128, N = 128.
 constexpr uint32_t kIdescBase = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
@@ -151,6 +161,8 @@ __device__ __forceinline__ void stage_row(uint32_t stage, int32_t bf16, int r, i
     }
 }
 
+// 608 threads, one CTA per SM (196 KB of shared memory); 19 warps put five on
+// some SM sub-partition, whose 16K registers then allow 96 a thread.
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_chunk_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                          const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
@@ -160,11 +172,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    // Grid (KV group, sequence, row tile), row tiles in reverse: later rows see
-    // more keys, so the longest CTAs start first and the last wave is short.
+    // Grid (KV group, sequence, pair of row tiles), pairs in reverse: later rows
+    // see more keys, so the longest CTAs start first and the last wave is short.
     const int g = blockIdx.x;
     const int b = blockIdx.y;
-    const int tile = gridDim.z - 1 - blockIdx.z;
+    const int pair = gridDim.z - 1 - blockIdx.z;
     const int G = p.group;
     const int rpt = p.rows_per_tile;
 
@@ -186,28 +198,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q_len = p.cu_q_lens ? __ldg(p.cu_q_lens + b + 1) - row0 : p.uniform_q_len;
     const int ctx = __ldg(p.context_lens + b);
     if (q_len < 0 || q_len > ctx || ctx > p.max_blocks * kBlockSize || row0 < 0 || row0 + q_len > p.total_rows) {
-        if (tile == 0 && g == 0 && tid == 0 && p.status) atomicOr(p.status, kStatusBadQLen);
+        if (pair == 0 && g == 0 && tid == 0 && p.status) atomicOr(p.status, kStatusBadQLen);
         return;
     }
-    const int i0 = tile * rpt;
-    if (i0 >= q_len) return;
-    const int rows_here = min(rpt, q_len - i0);
     const int c = ctx - q_len;
-    const int last_pos = c + i0 + rows_here - 1;
-    const int n_keys = last_pos + 1;  // keys 0 .. last_pos
-    const int n_tiles = (n_keys + 127) / 128;
+    // Row tile t of the pair: rows i0(t) .. i0(t) + rows(t) - 1 (0 rows: past the
+    // chunk), keys 0 .. c + i0(t) + rows(t) - 1, key tiles nt(t); nt(1) >= nt(0)
+    // whenever tile 1 has rows.
+    auto tile_i0 = [&](int t) { return (2 * pair + t) * rpt; };
+    auto tile_rows = [&](int t) { return max(0, min(rpt, q_len - tile_i0(t))); };
+    auto tile_nt = [&](int t) { return tile_rows(t) > 0 ? (c + tile_i0(t) + tile_rows(t) + 127) / 128 : 0; };
+    const int nt0 = tile_nt(0), nt1 = tile_nt(1);
+    const int n_tiles = max(nt0, nt1);
+    if (n_tiles == 0) return;
     const int nblocks = (ctx + kBlockSize - 1) / kBlockSize;
     const int32_t *table = p.block_tables + static_cast<size_t>(b) * p.max_blocks;
 
     const uint32_t bar_q = sbase + kOffBar;
-    // K slot kt % kStagesK (use kt / kStagesK), V slot kt % kStagesV (use kt / kStagesV), S/P buffer kt % 2.
+    // K slot kt % kStagesK (use kt / kStagesK), V slot kt % kStagesV; per tile t: S, P and O barriers.
     auto k_full = [&](int st) { return sbase + kOffBar + 8 * (1 + st); };
     auto k_empty = [&](int st) { return sbase + kOffBar + 8 * (1 + kStagesK + st); };
     auto v_full = [&](int st) { return sbase + kOffBar + 8 * (1 + 2 * kStagesK + st); };
     auto v_empty = [&](int st) { return sbase + kOffBar + 8 * (1 + 2 * kStagesK + kStagesV + st); };
-    auto s_full = [&](int s) { return sbase + kOffBar + 8 * (kBarS + s); };
-    auto p_full = [&](int s) { return sbase + kOffBar + 8 * (kBarS + 2 + s); };
-    auto o_done = [&](int s) { return sbase + kOffBar + 8 * (kBarS + 4 + s); };
+    auto s_full = [&](int t) { return sbase + kOffBar + 8 * (kBarTile + t); };
+    auto p_full = [&](int t) { return sbase + kOffBar + 8 * (kBarTile + kRowTiles + t); };
+    auto o_done = [&](int t) { return sbase + kOffBar + 8 * (kBarTile + 2 * kRowTiles + t); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffTmem);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + kOffAbort);
 
@@ -221,10 +236,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(v_full(st), 1);
             mbar_init(v_empty(st), 1);
         }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(s_full(s), 1);
-            mbar_init(p_full(s), kSoftmaxWarps);
-            mbar_init(o_done(s), 1);
+        for (int t = 0; t < kRowTiles; ++t) {
+            mbar_init(s_full(t), 1);
+            mbar_init(p_full(t), kSoftmaxWarps);
+            mbar_init(o_done(t), 1);
         }
         *abort_flag = 0u;
         fence_mbar_init();
@@ -257,15 +272,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     if (warp == kProducerK || warp == kProducerV) {
-        // ---------------- TMA producers: warp 8 fills the K ring, warp 10 the V ring ----------------
+        // ---------------- TMA producers: warp 16 fills the K ring, warp 18 the V ring ----------------
         const bool is_k = warp == kProducerK;
         const CUtensorMap *map = is_k ? &kmap : &vmap;
         const uint32_t ring = sbase + (is_k ? kOffK : kOffV);
         const int stages = is_k ? kStagesK : kStagesV;
-        if (is_k && lane == 0) {
-            mbar_arrive_expect_tx(bar_q, kOpBytes);
-            tma_load_3d(sbase + kOffQ, &qmap, bar_q, 0, g * G, row0 + i0);
-            tma_load_3d(sbase + kOffQ + kHalfTile, &qmap, bar_q, 64, g * G, row0 + i0);
+        if (is_k && lane == 0) {  // both Q tiles (rows past the chunk read as zeros or are never stored)
+            mbar_arrive_expect_tx(bar_q, kRowTiles * kOpBytes);
+            for (int t = 0; t < kRowTiles; ++t) {
+                tma_load_3d(sbase + kOffQ + t * kOpBytes, &qmap, bar_q, 0, g * G, row0 + tile_i0(t));
+                tma_load_3d(sbase + kOffQ + t * kOpBytes + kHalfTile, &qmap, bar_q, 64, g * G, row0 + tile_i0(t));
+            }
         }
         // (block, head) tile index of key tile kt's t-th paged block, read by lane t
         // (one parallel load per tile); invalid ids fetch tile 0 and are masked.
@@ -296,86 +313,121 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane < nload) tma_load_5d(dst + lane * kBlkBytes, map, bar, 0, 0, 0, 0, mine);
         }
     } else if (warp == kMmaWarp) {
-        // ---------------- MMA issuer ----------------
+        // ---------------- MMA issuer: S0(k), P1(k-1) V(k-1), S1(k), P0(k) V(k) ----------------
         if (lane == 0) {
-            auto mma_s = [&](int kt) -> bool {
-                const int s = kt & 1;
-                const int st = kt % kStagesK;
-                if (!wait(k_full(st), (kt / kStagesK) & 1)) return false;
-                // Buffer s held P(kt-2): P(kt-2) V(kt-2) must have consumed it.
-                if (kt >= 2 && !wait(o_done(s), ((kt - 2) >> 1) & 1)) return false;
-                tc_fence_after();
-                const uint32_t kb = sbase + kOffK + st * kOpBytes;
+            auto mma_s = [&](int t, int kt) {
+                const uint32_t kb = sbase + kOffK + (kt % kStagesK) * kOpBytes;
+                const uint32_t qb = sbase + kOffQ + t * kOpBytes;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {  // 16 dims per step: dim half kk / 4, 32 B into the row
                     const uint32_t qoff = (kk >> 2) * kHalfTile + (kk & 3) * 32;
                     const uint32_t koff = (kk >> 2) * 1024 + (kk & 3) * 32;
-                    umma_bf16(tmem + 128 * s, sw128_desc(sbase + kOffQ + qoff, 16, 1024),
-                              sw128_desc(kb + koff, 16, 2048), kIdescQK, kk > 0);
+                    umma_bf16(tmem + 128 * t, sw128_desc(qb + qoff, 16, 1024), sw128_desc(kb + koff, 16, 2048),
+                              kIdescQK, kk > 0);
                 }
-                umma_commit(s_full(s));
-                umma_commit(k_empty(st));
-                return true;
+                umma_commit(s_full(t));
             };
-            auto mma_pv = [&](int kt) -> bool {
-                const int s = kt & 1;
-                const int st = kt % kStagesV;
-                if (!wait(v_full(st), (kt / kStagesV) & 1)) return false;
-                if (!wait(p_full(s), (kt >> 1) & 1)) return false;
-                tc_fence_after();
-                const uint32_t vb = sbase + kOffV + st * kOpBytes;
+            auto mma_pv = [&](int t, int kt) {
+                const uint32_t vb = sbase + kOffV + (kt % kStagesV) * kOpBytes;
 #pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                    // keys 16t .. 16t+15: half t/4 of buffer s, [head | remainder] columns
-                    const uint32_t a_hi = tmem + 128 * s + (t >> 2) * 64 + (t & 3) * 8;
-                    const uint64_t bd = sw128_desc(vb + t * kBlkBytes, 1024, 2048);
-                    umma_bf16_tmem_a(tmem + kTmemO, a_hi, bd, kIdescPV, (kt > 0 || t > 0) ? 1u : 0u);
-                    umma_bf16_tmem_a(tmem + kTmemO, a_hi + 32, bd, kIdescPV, 1u);
+                for (int s8 = 0; s8 < 8; ++s8) {
+                    // keys 16 s8 .. +15: half s8 / 4, 32-key chunk (s8 / 2) % 2, [16 head | 16 remainder] columns
+                    const uint32_t a_hi = tmem + 128 * t + (s8 >> 2) * 64 + ((s8 >> 1) & 1) * 32 + (s8 & 1) * 8;
+                    const uint64_t bd = sw128_desc(vb + s8 * kBlkBytes, 1024, 2048);
+                    umma_bf16_tmem_a(tmem + kTmemO + 128 * t, a_hi, bd, kIdescPV, (kt > 0 || s8 > 0) ? 1u : 0u);
+                    umma_bf16_tmem_a(tmem + kTmemO + 128 * t, a_hi + 16, bd, kIdescPV, 1u);
                 }
-                umma_commit(o_done(s));
-                umma_commit(v_empty(st));
-                return true;
+                umma_commit(o_done(t));
             };
-            bool ok = wait(bar_q, 0) && mma_s(0);
-            for (int kt = 1; ok && kt < n_tiles; ++kt) ok = mma_s(kt) && mma_pv(kt - 1);
-            if (ok) mma_pv(n_tiles - 1);
+            bool ok = wait(bar_q, 0);
+            for (int kt = 0; ok && kt <= n_tiles; ++kt) {
+                const int st_k = kt % kStagesK, st_v = kt % kStagesV;
+                bool k_ready = false;  // K(kt) waited for (just before the first S that reads it)
+                auto need_k = [&]() -> bool {
+                    if (!k_ready) {
+                        if (!wait(k_full(st_k), (kt / kStagesK) & 1)) return false;
+                        tc_fence_after();
+                        k_ready = true;
+                    }
+                    return true;
+                };
+                if (kt < nt0) {
+                    if (!(ok = need_k())) break;
+                    mma_s(0, kt);
+                }
+                if (kt >= 1 && kt - 1 < nt1) {  // tile 1's P V of the previous key tile
+                    const int pk = kt - 1;
+                    if (!(ok = wait(p_full(1), pk & 1) && wait(v_full(pk % kStagesV), (pk / kStagesV) & 1))) break;
+                    tc_fence_after();
+                    mma_pv(1, pk);
+                    umma_commit(v_empty(pk % kStagesV));  // both tiles' P V of key tile pk are issued
+                }
+                if (kt < nt1) {
+                    if (!(ok = need_k())) break;
+                    mma_s(1, kt);
+                }
+                if (kt < n_tiles) umma_commit(k_empty(st_k));  // both tiles' S of key tile kt are issued
+                if (kt < nt0) {
+                    if (!(ok = wait(p_full(0), kt & 1) && wait(v_full(st_v), (kt / kStagesV) & 1))) break;
+                    tc_fence_after();
+                    mma_pv(0, kt);
+                    if (kt >= nt1) umma_commit(v_empty(st_v));  // tile 1 does not read this key tile
+                }
+            }
         }
     } else {
-        // ---------------- softmax warps: one tile row and one column half per thread ----------------
+        // ---------------- softmax warps: tile t = warp / 8; one row and one column half per thread ----------------
         // (every wait decision is made warp-uniform, so the .sync.aligned tensor-memory
         // loads and stores below always see the full warp)
-        const int quarter = warp & 3;  // tensor-memory lanes 32*quarter .. +31
-        const int hc = warp >> 2;      // column half: keys / O dims [64*hc, 64*hc + 64)
+        const int t = warp / kSoftmaxWarps;
+        const int w8 = warp % kSoftmaxWarps;
+        const int quarter = w8 & 3;  // tensor-memory lanes 32*quarter .. +31 (warp % 4 == quarter)
+        const int hc = w8 >> 2;      // column half: keys / O dims [64*hc, 64*hc + 64)
         const int r = quarter * 32 + lane;
         const int ii = r / G;
+        const int i0 = tile_i0(t);
+        const int rows_here = tile_rows(t);
+        const int my_nt = t == 0 ? nt0 : nt1;
         const bool row_valid = ii < rows_here;
         const int pos = c + i0 + (row_valid ? ii : 0);
         const int limit = min(pos, ctx - 1);  // visible keys: j <= limit
         const float sl2 = p.scale_log2;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-        const uint32_t t_o = lane_base + kTmemO + 64 * hc;
-        float *xch = reinterpret_cast<float *>(smem + kOffXch);  // [tile & 1][half][row]
-        float *xl = reinterpret_cast<float *>(smem + kOffXch);   // [half][row], epilogue only
-        auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory"); };
+        const uint32_t t_s0 = lane_base + 128 * t + 64 * hc;         // this thread's S/P half
+        const uint32_t t_o = lane_base + kTmemO + 128 * t + 64 * hc;  // this thread's O half
+        float *xch = reinterpret_cast<float *>(smem + kOffXch + t * kXchBytes);  // [key tile & 1][half][row]
+        float *xl = xch;                                                          // [half][row], epilogue only
+        const uint32_t pair_bar = 1 + 4 * t + quarter;  // named barriers 1..8: the two warps of a row quarter
+        auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory"); };
+
+        // Mask one 32-key chunk by index (keys past the row's position or in a bad block).
+        auto mask_chunk = [&](uint32_t (&v)[32], int kc, int q, uint32_t bad) {
+            if (!(kc + 31 <= limit && !((bad >> (2 * q)) & 3u))) {
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    const bool ok = kc + k <= limit && !((bad >> ((32 * q + k) >> 4)) & 1u);
+                    if (!ok) v[k] = __float_as_uint(-INFINITY);
+                }
+            }
+        };
 
         float m_ref = -INFINITY;  // exponent reference (raised lazily)
         float l = 0.f;            // this half's share of the row sum
-        // Both warps of a pair pass exactly one pair barrier per tile and one in the
-        // epilogue on every path: after a wait gives up (`alive` false) the loop keeps
-        // turning without work, so the named barriers always match and never hang.
+        // Both warps of a pair pass exactly one pair barrier per key tile and two in
+        // the epilogue on every path: after a wait gives up (`alive` false) the loop
+        // keeps turning without work, so the named barriers always match and never hang.
         bool alive = true;
-        for (int kt = 0; kt < n_tiles; ++kt) {
-            const int s = kt & 1;
-            alive = alive && warp_wait(s_full(s), (kt >> 1) & 1);
+        for (int kt = 0; kt < my_nt; ++kt) {
+            const int xb = kt & 1;
+            alive = alive && warp_wait(s_full(t), kt & 1);
             if (!alive) {
                 pair_sync();
                 continue;
             }
             tc_fence_after();
-            const uint32_t t_s = lane_base + 128 * s + 64 * hc;
 
             // Which of this tile's blocks have an invalid id (their keys are masked):
-            // lane t < 8 checks block t, a ballot shares the answer.
+            // lane j < 8 checks block j, a ballot shares the answer.
             const int jb = kt * 8 + lane;
             const bool bad_lane = lane < 8 && jb < nblocks &&
                                   static_cast<unsigned>(__ldg(table + jb)) >= static_cast<unsigned>(p.num_blocks);
@@ -383,31 +435,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (bad && r == 0 && hc == 0 && p.status) atomicOr(p.status, kStatusBadBlockId);
             const int key0 = kt * 128 + 64 * hc;  // first key of this half
 
-            uint32_t sr[2][32];
-            tmem_ld_32x32b_x32(t_s, sr[0]);
-            tmem_ld_32x32b_x32(t_s + 32, sr[1]);
-            tmem_wait_ld();
-            tmem_hold(sr[0]);
-            tmem_hold(sr[1]);
-            // Mask by index (skipped for chunks whose 32 keys are all visible); half max.
+            // Pass 1: the half's maximum over both 32-key chunks.
             float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
-                const int q = 2 * hc + u;  // 32-key chunk of the tile
-                const int kc = key0 + 32 * u;
-                if (!(kc + 31 <= limit && !((bad >> (2 * q)) & 3u))) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(t_s0 + 32 * u, v);
+                tmem_wait_ld();
+                tmem_hold(v);
+                mask_chunk(v, key0 + 32 * u, 2 * hc + u, bad);
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                        const bool ok = kc + k <= limit && !((bad >> ((32 * q + k) >> 4)) & 1u);
-                        if (!ok) sr[u][k] = __float_as_uint(-INFINITY);
-                    }
-                }
-#pragma unroll
-                for (int k = 0; k < 32; ++k) mx[k & 3] = fmaxf(mx[k & 3], __uint_as_float(sr[u][k]));
+                for (int k = 0; k < 32; ++k) mx[k & 3] = fmaxf(mx[k & 3], __uint_as_float(v[k]));
             }
-            xch[(s * 2 + hc) * 128 + r] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+            xch[(xb * 2 + hc) * 128 + r] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
             pair_sync();
-            const float mraw = fmaxf(xch[(s * 2) * 128 + r], xch[(s * 2 + 1) * 128 + r]);
+            const float mraw = fmaxf(xch[(xb * 2) * 128 + r], xch[(xb * 2 + 1) * 128 + r]);
             const float mt = mraw == -INFINITY ? -INFINITY : mraw * sl2;  // scale > 0 keeps the order
             float alpha = 1.f;
             if (mt > m_ref + 8.f) {  // also taken at the first visible key (m_ref = -inf)
@@ -416,11 +458,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float mu = m_ref == -INFINITY ? 0.f : m_ref;
 
-            // Rescaling O needs every earlier P V done (in-order: the latest, P(kt-1) V(kt-1)).
+            // Rescale O: every earlier P V of this tile completed before S(kt) did.
             if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                alive = warp_wait(o_done((kt - 1) & 1), ((kt - 1) >> 1) & 1);
-                if (!alive) continue;
-                tc_fence_after();
 #pragma unroll 1
                 for (int q = 0; q < 2; ++q) {
                     uint32_t orow[32];
@@ -434,17 +473,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_wait_st();
             }
 
-            // P = 2^(s * scale * log2(e) - m), written back over this half as
-            // [32 columns bf16 head | 32 columns bf16 remainder] (two keys per
-            // column, the lower key in the low half).
+            // Pass 2: P = 2^(s * scale * log2(e) - m) chunk by chunk, written back over the
+            // chunk's 32 columns as [16 columns bf16 head | 16 columns bf16 remainder]
+            // (two keys per column, the lower key in the low half).
             float rsum[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {  // 32 keys -> 16 head columns + 16 remainder columns
+            for (int u = 0; u < 2; ++u) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(t_s0 + 32 * u, v);
+                tmem_wait_ld();
+                tmem_hold(v);
+                mask_chunk(v, key0 + 32 * u, 2 * hc + u, bad);
                 uint32_t hi[16], lo[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const float pa = fast_exp2(fmaf(__uint_as_float(sr[u][2 * e]), sl2, -mu));
-                    const float pb = fast_exp2(fmaf(__uint_as_float(sr[u][2 * e + 1]), sl2, -mu));
+                    const float pa = fast_exp2(fmaf(__uint_as_float(v[2 * e]), sl2, -mu));
+                    const float pb = fast_exp2(fmaf(__uint_as_float(v[2 * e + 1]), sl2, -mu));
                     rsum[e & 3] += pa + pb;
                     // head: the upper 16 bits of each (bf16 truncation, exact in fp32);
                     // remainder: P - head >= 0, rounded to nearest bf16 by adding half a unit.
@@ -454,13 +498,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float rb = pb - __uint_as_float(ub & 0xffff0000u);
                     lo[e] = __byte_perm(__float_as_uint(ra) + 0x8000u, __float_as_uint(rb) + 0x8000u, 0x7632);
                 }
-                tmem_st_32x32b_x16(t_s + 16 * u, hi);
-                tmem_st_32x32b_x16(t_s + 32 + 16 * u, lo);
+                tmem_st_32x32b_x16(t_s0 + 32 * u, hi);
+                tmem_st_32x32b_x16(t_s0 + 32 * u + 16, lo);
             }
             tmem_wait_st();
             l = l * alpha + ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3]));
 
-            // Zero V rows of keys no row may see (past the context, or of a bad block).
+            // Zero V rows of keys no row may see (past the context, or of a bad block);
+            // each tile that reads the key tile does it before its P V (the two write the same zeros).
             const int rv = ctx - kt * 128;  // keys [rv, 128) of the tile are past the context
             if (rv < 128 || bad) {
                 alive = warp_wait(v_full(kt % kStagesV), (kt / kStagesV) & 1);
@@ -479,15 +524,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();  // zeroed V rows -> the tensor core (async proxy)
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full(s));
+            if (lane == 0) mbar_arrive(p_full(t));
         }
 
         // ---- epilogue: out = O / l (the two halves add their row sums) ----
-        pair_sync();  // the last tile's maxima have been read: the exchange area is free
+        pair_sync();  // the last key tile's maxima have been read: the exchange area is free
         xl[hc * 128 + r] = l;
         pair_sync();
-        const bool staged = rows_here == rpt;  // CTA-uniform: a full tile leaves by TMA store
-        if (alive && warp_wait(o_done((n_tiles - 1) & 1), ((n_tiles - 1) >> 1) & 1)) {
+        // Staged through shared memory and a TMA store when the tile is full: tile 1 in
+        // the K ring (every MMA has completed by its last P V), tile 0 in its own Q
+        // buffer (bf16 output only: 32 KB).  CTA-uniform per tile.
+        const bool staged = rows_here == rpt && (t == 1 || p.out_bf16);
+        const uint32_t stage = sbase + (t == 1 ? kOffK : kOffQ);
+        if (my_nt > 0 && alive && warp_wait(o_done(t), (my_nt - 1) & 1)) {
             tc_fence_after();
             const float lt = xl[r] + xl[128 + r];
             const float inv = lt > 0.f ? 1.f / lt : 0.f;
@@ -503,20 +552,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_wait_ld();
                 tmem_hold(orow);
                 if (staged)
-                    stage_row(sbase + kOffK, p.out_bf16, r, hc, q, orow, inv);
+                    stage_row(stage, p.out_bf16, r, hc, q, orow, inv);
                 else if (row_valid)
                     store_row(p.out, p.out_bf16, orow_base + 32 * q, orow, inv);
             }
         }
         if (staged) {
-            // Every softmax warp reaches this barrier on every path (staged is uniform).
+            // Every softmax warp of the tile reaches this barrier on every path (staged is tile-uniform).
             fence_proxy_async_smem();
-            asm volatile("bar.sync 5, %0;" ::"r"(kSoftmaxWarps * 32) : "memory");
-            if (warp == 0 && lane == 0 && !*abort_flag) {
+            asm volatile("bar.sync %0, %1;" ::"r"(9 + t), "r"(kSoftmaxWarps * 32) : "memory");
+            if (w8 == 0 && lane == 0 && !*abort_flag) {
                 const int nbox = p.out_bf16 ? 2 : 4;
 #pragma unroll 1
                 for (int bx = 0; bx < nbox; ++bx)
-                    tma_store_3d(&omap, sbase + kOffK + bx * kHalfTile, bx * (p.out_bf16 ? 64 : 32), g * G, row0 + i0);
+                    tma_store_3d(&omap, stage + bx * kHalfTile, bx * (p.out_bf16 ? 64 : 32), g * G, row0 + i0);
                 bulk_commit_group();
                 bulk_wait_group_read_all();  // shared memory must outlive the reads
             }
@@ -530,9 +579,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (*abort_flag) {
         if (tid == 0 && p.status) atomicOr(p.status, kStatusTimeout);
         // Best effort: let MMAs still in flight finish before the columns are freed.
-        if (warp == kMmaWarp && lane == 0) mbar_wait(o_done((n_tiles - 1) & 1), ((n_tiles - 1) >> 1) & 1);
+        if (warp == kMmaWarp && lane == 0) {
+            if (nt0 > 0) mbar_wait(o_done(0), (nt0 - 1) & 1);
+            if (nt1 > 0) mbar_wait(o_done(1), (nt1 - 1) & 1);
+        }
         __syncwarp();
     }
+    __syncthreads();
     if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
@@ -547,7 +600,9 @@ cudaError_t prefill_prepare_device() {
 
 cudaError_t launch_prefill_chunk(const CUtensorMap &qmap, const CUtensorMap &kmap, const CUtensorMap &vmap,
                                  const CUtensorMap &omap, const PrefillParams &p, int max_q_len, cudaStream_t stream) {
-    const dim3 grid(p.n_kv, p.num_seqs, (max_q_len + p.rows_per_tile - 1) / p.rows_per_tile);
+    // One CTA per pair of row tiles.
+    const int tiles = (max_q_len + p.rows_per_tile - 1) / p.rows_per_tile;
+    const dim3 grid(p.n_kv, p.num_seqs, (tiles + 1) / 2);
     return launch_pdl(prefill_chunk_kernel, grid, dim3(kThreads), kSmemBytes, stream, qmap, kmap, vmap, omap, p);
 }
 
