@@ -40,27 +40,30 @@
 //    execute in order, and the commit after S_t(k) completes only when every
 //    earlier MMA has, so when the softmax sees S_t(k) the previous P_t V is
 //    already in O_t.
-//  * warps 0-7 (tile 0) and 8-15 (tile 1), 256 threads per tile: warps w and
-//    w+4 of a tile own tensor-memory lanes 32*(w%4) .. +31 (= tile rows) and
-//    split the 128 columns: each thread handles one row's 64 scores of its
-//    half in two chunks of 32, applies the causal/length mask by index
-//    (skipped for fully visible chunks), and the two halves exchange their
-//    row maxima through shared memory (a 64-thread named barrier per pair).
-//    Each updates the running max and its half of the running sum (fp32,
-//    log2 domain) and writes P = 2^(s - m) back over each 32-key chunk as
-//    [16 columns bf16 head | 16 columns bf16 remainder] (head = P truncated
-//    to bf16, remainder = the rest rounded to bf16; P V = P_hi V + P_lo V
-//    keeps the weights to ~2^-16 relative).  The exponent reference is only
-//    raised when a row's max grows by more than 2^8, in which case the row's O
-//    is rescaled in tensor memory; P stays <= 256.
-//  * Epilogue per tile: O / l from tensor memory; a full tile is staged in
-//    shared memory (tile 1: in the K ring, free by then; tile 0, bf16 output:
-//    in its own Q buffer, whose MMAs have completed) in the output tensor map's
-//    128-byte-swizzled layout and leaves by TMA store; a ragged last tile (and
-//    tile 0 with fp32 output) by 16-byte stores of its valid rows only.
+//  * warps 0-15 (512 threads) work on tile 0's scores, then on tile 1's, for
+//    each key tile (the MMAs of one tile run while the other tile's softmax
+//    does): warps w, w+4, w+8, w+12 own tensor-memory lanes 32*(w%4) .. +31
+//    (= tile rows) and split the 128 columns in quarters, so each thread holds
+//    32 scores of one row in registers, applies the causal/length mask by
+//    index (skipped for fully visible chunks), and the four quarters exchange
+//    their row maxima through shared memory (a 128-thread named barrier per row
+//    quarter).  Each updates the running max and its quarter of the running
+//    sum (fp32, log2 domain, pairs of keys in packed f32x2 arithmetic) and
+//    writes P = 2^(s - m) back over its 32 columns as [16 columns bf16 head |
+//    16 columns bf16 remainder] (head = P truncated to bf16, remainder = the
+//    rest rounded to bf16; P V = P_hi V + P_lo V keeps the weights to ~2^-16
+//    relative).  The exponent reference is only raised when a row's max grows
+//    by more than 2^8, in which case the row's O is rescaled in tensor memory;
+//    P stays <= 256.
+//  * Epilogue per tile, after both tiles' last P V (every MMA has completed):
+//    O / l from tensor memory; a full tile is staged in a free ring (tile 0:
+//    the V ring, tile 1: the K ring) in the output tensor map's 128-byte-
+//    swizzled layout and leaves by TMA store; a ragged last tile by 16-byte
+//    stores of its valid rows only (a whole-box store would overwrite the next
+//    sequence).
 //  * Keys at or past the context length and keys of blocks with an invalid id
-//    are masked by index and their V rows are zeroed in shared memory (by each
-//    tile that reads them, before its P V), so stale or NaN bytes cannot reach
+//    are masked by index and their V rows are zeroed in shared memory (once,
+//    before the first P V that reads them), so stale or NaN bytes cannot reach
 //    the result.
 //
 // Every mbarrier wait is bounded; a role whose wait runs out raises a
@@ -79,8 +82,8 @@ namespace pkv {
 namespace {
 
 constexpr int kRowTiles = 2;      // 128-row Q tiles per CTA
-constexpr int kSoftmaxWarps = 8;  // per tile: warps w and w+4 share lanes 32*(w%4).. and split the columns
-constexpr int kProducerK = kRowTiles * kSoftmaxWarps;  // warp 16
+constexpr int kSoftmaxWarps = 16;  // warps w, w+4, w+8, w+12 share lanes 32*(w%4).. and split the columns
+constexpr int kProducerK = kSoftmaxWarps;              // warp 16
 constexpr int kMmaWarp = kProducerK + 1;               // warp 17
 constexpr int kProducerV = kProducerK + 2;             // warp 18
 constexpr int kThreads = (kProducerV + 1) * 32;        // 608
@@ -99,7 +102,7 @@ constexpr int kBarTile = 1 + 2 * kStagesK + 2 * kStagesV;
 constexpr uint32_t kNumBars = kBarTile + 3 * kRowTiles;
 constexpr uint32_t kOffTmem = kOffBar + 8 * 16;
 constexpr uint32_t kOffAbort = kOffTmem + 8;
-constexpr uint32_t kXchBytes = 2 * 2 * 128 * 4;  // per tile: row maxima [key tile & 1][half][128]; then row sums
+constexpr uint32_t kXchBytes = 2 * 4 * 128 * 4;  // per tile: row maxima [key tile & 1][column quarter][128]
 constexpr uint32_t kOffXch = kOffAbort + 8;
 // The dynamic shared memory is declared 1024-byte aligned (the swizzle period of
 // the TMA/UMMA operands); the kernel checks it and refuses to run otherwise.
@@ -161,7 +164,7 @@ __device__ __forceinline__ void stage_row(uint32_t stage, int32_t bf16, int r, i
     }
 }
 
-// 608 threads, one CTA per SM (196 KB of shared memory); 19 warps put five on
+// 608 threads, one CTA per SM (200 KB of shared memory); 19 warps put five on
 // some SM sub-partition, whose 16K registers then allow 96 a thread.
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_chunk_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
@@ -376,198 +379,196 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        // ---------------- softmax warps: tile t = warp / 8; one row and one column half per thread ----------------
+        // ---------------- softmax warps: both tiles in turn; one row and one column quarter per thread ----------------
         // (every wait decision is made warp-uniform, so the .sync.aligned tensor-memory
         // loads and stores below always see the full warp)
-        const int t = warp / kSoftmaxWarps;
-        const int w8 = warp % kSoftmaxWarps;
-        const int quarter = w8 & 3;  // tensor-memory lanes 32*quarter .. +31 (warp % 4 == quarter)
-        const int hc = w8 >> 2;      // column half: keys / O dims [64*hc, 64*hc + 64)
+        const int quarter = warp & 3;  // tensor-memory lanes 32*quarter .. +31 (warp % 4 == quarter)
+        const int cq = warp >> 2;      // column quarter: keys / O dims [32*cq, 32*cq + 32)
         const int r = quarter * 32 + lane;
         const int ii = r / G;
-        const int i0 = tile_i0(t);
-        const int rows_here = tile_rows(t);
-        const int my_nt = t == 0 ? nt0 : nt1;
-        const bool row_valid = ii < rows_here;
-        const int pos = c + i0 + (row_valid ? ii : 0);
-        const int limit = min(pos, ctx - 1);  // visible keys: j <= limit
         const float sl2 = p.scale_log2;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-        const uint32_t t_s0 = lane_base + 128 * t + 64 * hc;         // this thread's S/P half
-        const uint32_t t_o = lane_base + kTmemO + 128 * t + 64 * hc;  // this thread's O half
-        float *xch = reinterpret_cast<float *>(smem + kOffXch + t * kXchBytes);  // [key tile & 1][half][row]
-        float *xl = xch;                                                          // [half][row], epilogue only
-        const uint32_t pair_bar = 1 + 4 * t + quarter;  // named barriers 1..8: the two warps of a row quarter
-        auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory"); };
+        float *xch = reinterpret_cast<float *>(smem + kOffXch);  // [tile][key tile & 1][quarter][row]; then row sums
+        const uint32_t row_bar = 1 + quarter;  // named barriers 1..4: the four warps of a row quarter
+        auto row_sync = [&]() { asm volatile("bar.sync %0, 128;" ::"r"(row_bar) : "memory"); };
 
-        // Mask one 32-key chunk by index (keys past the row's position or in a bad block).
-        auto mask_chunk = [&](uint32_t (&v)[32], int kc, int q, uint32_t bad) {
-            if (!(kc + 31 <= limit && !((bad >> (2 * q)) & 3u))) {
+        // Per tile: the row's last visible key, running exponent reference and row-sum share.
+        int limit[kRowTiles];
+        float m_ref[kRowTiles], l[kRowTiles];
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    const bool ok = kc + k <= limit && !((bad >> ((32 * q + k) >> 4)) & 1u);
-                    if (!ok) v[k] = __float_as_uint(-INFINITY);
-                }
-            }
-        };
+        for (int t = 0; t < kRowTiles; ++t) {
+            const int pos = c + tile_i0(t) + (ii < tile_rows(t) ? ii : 0);
+            limit[t] = min(pos, ctx - 1);  // visible keys: j <= limit
+            m_ref[t] = -INFINITY;
+            l[t] = 0.f;
+        }
 
-        float m_ref = -INFINITY;  // exponent reference (raised lazily)
-        float l = 0.f;            // this half's share of the row sum
-        // Both warps of a pair pass exactly one pair barrier per key tile and two in
-        // the epilogue on every path: after a wait gives up (`alive` false) the loop
-        // keeps turning without work, so the named barriers always match and never hang.
+        // The four warps of a row quarter pass exactly one row barrier per (key tile,
+        // tile) and two per tile in the epilogue on every path: after a wait gives up
+        // (`alive` false) the loops keep turning without work, so the named barriers
+        // always match and never hang.
         bool alive = true;
-        for (int kt = 0; kt < my_nt; ++kt) {
-            const int xb = kt & 1;
-            alive = alive && warp_wait(s_full(t), kt & 1);
-            if (!alive) {
-                pair_sync();
-                continue;
-            }
-            tc_fence_after();
-
-            // Which of this tile's blocks have an invalid id (their keys are masked):
+        for (int kt = 0; kt < n_tiles; ++kt) {
+            // Which of this key tile's blocks have an invalid id (their keys are masked):
             // lane j < 8 checks block j, a ballot shares the answer.
             const int jb = kt * 8 + lane;
             const bool bad_lane = lane < 8 && jb < nblocks &&
                                   static_cast<unsigned>(__ldg(table + jb)) >= static_cast<unsigned>(p.num_blocks);
             const uint32_t bad = __ballot_sync(0xffffffffu, bad_lane);
-            if (bad && r == 0 && hc == 0 && p.status) atomicOr(p.status, kStatusBadBlockId);
-            const int key0 = kt * 128 + 64 * hc;  // first key of this half
+            if (bad && tid == 0 && p.status) atomicOr(p.status, kStatusBadBlockId);
+            const int kc = kt * 128 + 32 * cq;  // first key of this thread's chunk
+            const int rv = ctx - kt * 128;      // keys [rv, 128) of the key tile are past the context
 
-            // Pass 1: the half's maximum over both 32-key chunks.
-            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
+            for (int t = 0; t < kRowTiles; ++t) {
+                if (kt >= (t == 0 ? nt0 : nt1)) continue;  // (CTA-uniform)
+                alive = alive && warp_wait(s_full(t), kt & 1);
+                if (!alive) {
+                    row_sync();
+                    continue;
+                }
+                tc_fence_after();
+                const uint32_t t_s = lane_base + 128 * t + 32 * cq;
+                const uint32_t t_o = lane_base + kTmemO + 128 * t + 32 * cq;
+                float *xm = xch + ((t * 2 + (kt & 1)) * 4) * 128;
+
+                // This thread's 32 scores, masked by index (keys past the row's position or in a bad block).
                 uint32_t v[32];
-                tmem_ld_32x32b_x32(t_s0 + 32 * u, v);
+                tmem_ld_32x32b_x32(t_s, v);
                 tmem_wait_ld();
                 tmem_hold(v);
-                mask_chunk(v, key0 + 32 * u, 2 * hc + u, bad);
+                if (!(kc + 31 <= limit[t] && !((bad >> (2 * cq)) & 3u))) {
 #pragma unroll
-                for (int k = 0; k < 32; ++k) mx[k & 3] = fmaxf(mx[k & 3], __uint_as_float(v[k]));
-            }
-            xch[(xb * 2 + hc) * 128 + r] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-            pair_sync();
-            const float mraw = fmaxf(xch[(xb * 2) * 128 + r], xch[(xb * 2 + 1) * 128 + r]);
-            const float mt = mraw == -INFINITY ? -INFINITY : mraw * sl2;  // scale > 0 keeps the order
-            float alpha = 1.f;
-            if (mt > m_ref + 8.f) {  // also taken at the first visible key (m_ref = -inf)
-                alpha = fast_exp2(m_ref - mt);  // 0 when m_ref = -inf
-                m_ref = mt;
-            }
-            const float mu = m_ref == -INFINITY ? 0.f : m_ref;
+                    for (int k = 0; k < 32; ++k) {
+                        const bool ok = kc + k <= limit[t] && !((bad >> ((32 * cq + k) >> 4)) & 1u);
+                        if (!ok) v[k] = __float_as_uint(-INFINITY);
+                    }
+                }
+                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int k = 0; k < 32; k += 2)
+                    mx[(k >> 1) & 3] = fmax3(mx[(k >> 1) & 3], __uint_as_float(v[k]), __uint_as_float(v[k + 1]));
+                xm[cq * 128 + r] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+                row_sync();
+                const float mraw = fmaxf(fmaxf(xm[r], xm[128 + r]), fmaxf(xm[256 + r], xm[384 + r]));
+                const float mt = mraw == -INFINITY ? -INFINITY : mraw * sl2;  // scale > 0 keeps the order
+                float alpha = 1.f;
+                if (mt > m_ref[t] + 8.f) {  // also taken at the first visible key (m_ref = -inf)
+                    alpha = fast_exp2(m_ref[t] - mt);  // 0 when m_ref = -inf
+                    m_ref[t] = mt;
+                }
+                const float mu = m_ref[t] == -INFINITY ? 0.f : m_ref[t];
 
-            // Rescale O: every earlier P V of this tile completed before S(kt) did.
-            if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll 1
-                for (int q = 0; q < 2; ++q) {
+                // Rescale O: every earlier P V of this tile completed before S(kt) did.
+                if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
                     uint32_t orow[32];
-                    tmem_ld_32x32b_x32(t_o + 32 * q, orow);
+                    tmem_ld_32x32b_x32(t_o, orow);
                     tmem_wait_ld();
                     tmem_hold(orow);
 #pragma unroll
                     for (int k = 0; k < 32; ++k) orow[k] = __float_as_uint(__uint_as_float(orow[k]) * alpha);
-                    tmem_st_32x32b_x32(t_o + 32 * q, orow);
+                    tmem_st_32x32b_x32(t_o, orow);
                 }
-                tmem_wait_st();
-            }
 
-            // Pass 2: P = 2^(s * scale * log2(e) - m) chunk by chunk, written back over the
-            // chunk's 32 columns as [16 columns bf16 head | 16 columns bf16 remainder]
-            // (two keys per column, the lower key in the low half).
-            float rsum[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(t_s0 + 32 * u, v);
-                tmem_wait_ld();
-                tmem_hold(v);
-                mask_chunk(v, key0 + 32 * u, 2 * hc + u, bad);
+                // P = 2^(s * scale * log2(e) - m), written back over the chunk's 32 columns as
+                // [16 columns bf16 head | 16 columns bf16 remainder] (two keys per column, the
+                // lower key in the low half); pairs of keys go through packed f32x2 arithmetic.
+                const float2 sl2v = make_float2(sl2, sl2), nmu = make_float2(-mu, -mu);
+                float2 rs0 = make_float2(0.f, 0.f), rs1 = make_float2(0.f, 0.f);
                 uint32_t hi[16], lo[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const float pa = fast_exp2(fmaf(__uint_as_float(v[2 * e]), sl2, -mu));
-                    const float pb = fast_exp2(fmaf(__uint_as_float(v[2 * e + 1]), sl2, -mu));
-                    rsum[e & 3] += pa + pb;
+                    const float2 x =
+                        ffma2(make_float2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), sl2v, nmu);
+                    const float2 pr = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                    if (e & 1)
+                        rs1 = fadd2(rs1, pr);
+                    else
+                        rs0 = fadd2(rs0, pr);
                     // head: the upper 16 bits of each (bf16 truncation, exact in fp32);
-                    // remainder: P - head >= 0, rounded to nearest bf16 by adding half a unit.
-                    const uint32_t ua = __float_as_uint(pa), ub = __float_as_uint(pb);
+                    // remainder: P - head >= 0 (exact in fp32), rounded to nearest bf16.
+                    const uint32_t ua = __float_as_uint(pr.x), ub = __float_as_uint(pr.y);
                     hi[e] = __byte_perm(ua, ub, 0x7632);
-                    const float ra = pa - __uint_as_float(ua & 0xffff0000u);
-                    const float rb = pb - __uint_as_float(ub & 0xffff0000u);
-                    lo[e] = __byte_perm(__float_as_uint(ra) + 0x8000u, __float_as_uint(rb) + 0x8000u, 0x7632);
+                    const float2 rr =
+                        fsub2(pr, make_float2(__uint_as_float(ua & 0xffff0000u), __uint_as_float(ub & 0xffff0000u)));
+                    lo[e] = pack_bf16x2(rr.x, rr.y);
                 }
-                tmem_st_32x32b_x16(t_s0 + 32 * u, hi);
-                tmem_st_32x32b_x16(t_s0 + 32 * u + 16, lo);
-            }
-            tmem_wait_st();
-            l = l * alpha + ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3]));
+                tmem_st_32x32b_x16(t_s, hi);
+                tmem_st_32x32b_x16(t_s + 16, lo);
+                tmem_wait_st();
+                const float2 rs = fadd2(rs0, rs1);
+                l[t] = l[t] * alpha + (rs.x + rs.y);
 
-            // Zero V rows of keys no row may see (past the context, or of a bad block);
-            // each tile that reads the key tile does it before its P V (the two write the same zeros).
-            const int rv = ctx - kt * 128;  // keys [rv, 128) of the tile are past the context
-            if (rv < 128 || bad) {
-                alive = warp_wait(v_full(kt % kStagesV), (kt / kStagesV) & 1);
-                if (!alive) continue;
-                const uint32_t vb = sbase + kOffV + (kt % kStagesV) * kOpBytes;
-                for (int idx = hc * 128 + r; idx < 128 * 16; idx += kSoftmaxWarps * 32) {
-                    const int key = idx >> 4, ch = idx & 15;  // (all 16 chunks of a row: swizzle is moot)
-                    if (key >= rv || ((bad >> (key >> 4)) & 1u)) {
-                        const uint32_t addr = vb + (key >> 4) * kBlkBytes + ((key >> 3) & 1) * 2048 + (ch >> 3) * 1024 +
-                                              (key & 7) * 128 + (ch & 7) * 16;
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+                // Zero V rows of keys no row may see (past the context, or of a bad block),
+                // once per key tile, by the first tile that reads it, before its P V.
+                if ((rv < 128 || bad) && t == (kt < nt0 ? 0 : 1)) {
+                    alive = warp_wait(v_full(kt % kStagesV), (kt / kStagesV) & 1);
+                    if (!alive) continue;
+                    const uint32_t vb = sbase + kOffV + (kt % kStagesV) * kOpBytes;
+                    for (int idx = tid; idx < 128 * 16; idx += kSoftmaxWarps * 32) {
+                        const int key = idx >> 4, ch = idx & 15;  // (all 16 chunks of a row: swizzle is moot)
+                        if (key >= rv || ((bad >> (key >> 4)) & 1u)) {
+                            const uint32_t addr = vb + (key >> 4) * kBlkBytes + ((key >> 3) & 1) * 2048 +
+                                                  (ch >> 3) * 1024 + (key & 7) * 128 + (ch & 7) * 16;
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+                        }
                     }
                 }
-            }
 
-            fence_proxy_async_smem();  // zeroed V rows -> the tensor core (async proxy)
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(p_full(t));
+                fence_proxy_async_smem();  // zeroed V rows -> the tensor core (async proxy)
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(p_full(t));
+            }
         }
 
-        // ---- epilogue: out = O / l (the two halves add their row sums) ----
-        pair_sync();  // the last key tile's maxima have been read: the exchange area is free
-        xl[hc * 128 + r] = l;
-        pair_sync();
-        // Staged through shared memory and a TMA store when the tile is full: tile 1 in
-        // the K ring (every MMA has completed by its last P V), tile 0 in its own Q
-        // buffer (bf16 output only: 32 KB).  CTA-uniform per tile.
-        const bool staged = rows_here == rpt && (t == 1 || p.out_bf16);
-        const uint32_t stage = sbase + (t == 1 ? kOffK : kOffQ);
-        if (my_nt > 0 && alive && warp_wait(o_done(t), (my_nt - 1) & 1)) {
-            tc_fence_after();
-            const float lt = xl[r] + xl[128 + r];
-            const float inv = lt > 0.f ? 1.f / lt : 0.f;
-            const size_t orow_base =
-                (static_cast<size_t>(row0 + i0 + ii) * p.n_q + static_cast<size_t>(g) * G + (r % G)) * kHeadDim +
-                64 * hc;
-            // Kept rolled: in a variant of this kernel the unrolled form of this loop
-            // wrote wrong values for the second 32-column chunk (no time is lost).
+        // ---- epilogue per tile: out = O / l (the four column quarters add their row sums) ----
+        // Both tiles' last P V first: then every MMA has completed and a full tile is
+        // staged in a free ring (tile 0: the V ring, tile 1: the K ring) for a TMA store.
+        bool done = alive;
+        if (nt0 > 0) done = done && warp_wait(o_done(0), (nt0 - 1) & 1);
+        if (nt1 > 0) done = done && warp_wait(o_done(1), (nt1 - 1) & 1);
 #pragma unroll 1
-            for (int q = 0; q < 2; ++q) {
+        for (int t = 0; t < kRowTiles; ++t) {
+            const int my_nt = t == 0 ? nt0 : nt1;
+            const int i0 = tile_i0(t);
+            const int rows_here = tile_rows(t);
+            const bool row_valid = ii < rows_here;
+            row_sync();  // the last maxima have been read: the exchange area is free
+            xch[cq * 128 + r] = l[t];
+            row_sync();
+            const bool staged = rows_here == rpt;  // CTA-uniform
+            const uint32_t stage = sbase + (t == 0 ? kOffV : kOffK);
+            if (my_nt > 0 && done) {
+                tc_fence_after();
+                const float lt = (xch[r] + xch[128 + r]) + (xch[256 + r] + xch[384 + r]);
+                const float inv = lt > 0.f ? 1.f / lt : 0.f;
                 uint32_t orow[32];
-                tmem_ld_32x32b_x32(t_o + 32 * q, orow);
+                tmem_ld_32x32b_x32(lane_base + kTmemO + 128 * t + 32 * cq, orow);
                 tmem_wait_ld();
                 tmem_hold(orow);
-                if (staged)
-                    stage_row(stage, p.out_bf16, r, hc, q, orow, inv);
-                else if (row_valid)
-                    store_row(p.out, p.out_bf16, orow_base + 32 * q, orow, inv);
+                if (staged) {
+                    stage_row(stage, p.out_bf16, r, cq >> 1, cq & 1, orow, inv);
+                } else if (row_valid) {
+                    const size_t base =
+                        (static_cast<size_t>(row0 + i0 + ii) * p.n_q + static_cast<size_t>(g) * G + (r % G)) *
+                            kHeadDim +
+                        32 * cq;
+                    store_row(p.out, p.out_bf16, base, orow, inv);
+                }
             }
-        }
-        if (staged) {
-            // Every softmax warp of the tile reaches this barrier on every path (staged is tile-uniform).
-            fence_proxy_async_smem();
-            asm volatile("bar.sync %0, %1;" ::"r"(9 + t), "r"(kSoftmaxWarps * 32) : "memory");
-            if (w8 == 0 && lane == 0 && !*abort_flag) {
-                const int nbox = p.out_bf16 ? 2 : 4;
+            if (staged) {
+                // Every softmax warp reaches this barrier on every path (staged is CTA-uniform).
+                fence_proxy_async_smem();
+                asm volatile("bar.sync 9, %0;" ::"r"(kSoftmaxWarps * 32) : "memory");
+                if (tid == 0 && !*abort_flag) {
+                    const int nbox = p.out_bf16 ? 2 : 4;
 #pragma unroll 1
-                for (int bx = 0; bx < nbox; ++bx)
-                    tma_store_3d(&omap, stage + bx * kHalfTile, bx * (p.out_bf16 ? 64 : 32), g * G, row0 + i0);
-                bulk_commit_group();
-                bulk_wait_group_read_all();  // shared memory must outlive the reads
+                    for (int bx = 0; bx < nbox; ++bx)
+                        tma_store_3d(&omap, stage + bx * kHalfTile, bx * (p.out_bf16 ? 64 : 32), g * G, row0 + i0);
+                    bulk_commit_group();
+                    bulk_wait_group_read_all();  // shared memory must outlive the reads
+                }
             }
         }
     }
