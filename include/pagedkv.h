@@ -418,7 +418,7 @@ PKV_API int paged_attention_prefill_chunk(void *out, int32_t out_dtype, const vo
  *   q, out    : [num_seqs * q_per_seq][num_q_heads][head_dim]; sequence b owns
  *               rows b * q_per_seq .. b * q_per_seq + q_per_seq - 1
  *   q_per_seq : k, 1 .. 16
- * Runs on the decode kernel when G * k <= 32 or G does not divide 128: the
+ * Runs on the decode kernel when G * k <= 32, G > 16 or G does not divide 128: the
  * G heads x k positions of a KV head are the MMA columns of ceil(G * k / 16)
  * CTAs of up to 16 columns (one or two 8-column tiles), each reading the K/V
  * once; else on the tcgen05 prefill kernel (then q and out must be 16-B aligned).

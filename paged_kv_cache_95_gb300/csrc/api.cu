@@ -590,10 +590,10 @@ constexpr int32_t kMaxVerifyCols = 32;  // (position, head) pairs per KV head on
 
 // Verify runs on the decode kernel when the group's G x k (position, head) pairs
 // fit in at most two CTAs of up to 16 MMA columns each (K/V read once per CTA),
-// or when the prefill kernel cannot pack the group (G does not divide its 128
-// tile rows); else on the prefill kernel.
+// or when the prefill kernel cannot pack the group (G above 16, or G not dividing
+// its 128 tile rows); else on the prefill kernel.
 bool verify_on_decode(int32_t q_per_seq, int32_t G) {
-    return static_cast<int64_t>(q_per_seq) * G <= kMaxVerifyCols || 128 % G != 0;
+    return static_cast<int64_t>(q_per_seq) * G <= kMaxVerifyCols || G > 16 || 128 % G != 0;
 }
 // CTAs per KV head and the columns each takes (the last one may take fewer).
 int32_t verify_splits(int32_t cols) { return (cols + 15) / 16; }

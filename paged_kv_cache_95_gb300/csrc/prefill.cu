@@ -202,6 +202,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ctx = __ldg(p.context_lens + b);
     if (q_len < 0 || q_len > ctx || ctx > p.max_blocks * kBlockSize || row0 < 0 || row0 + q_len > p.total_rows) {
         if (pair == 0 && g == 0 && tid == 0 && p.status) atomicOr(p.status, kStatusBadQLen);
+        // The sequence's rows read as zeros when they can be addressed (this CTA's
+        // two row tiles of its KV group; 16-byte stores, out is 16-byte aligned).
+        if (q_len > 0 && row0 >= 0 && row0 + q_len <= p.total_rows) {
+            const int r_lo = 2 * pair * rpt, r_hi = min(q_len, r_lo + 2 * rpt);
+            const int chunks = p.out_bf16 ? 16 : 32;  // 16-byte chunks per (row, head)
+            const int per_row = G * chunks;
+            for (int idx = tid; idx < max(0, r_hi - r_lo) * per_row; idx += kThreads) {
+                const int i = r_lo + idx / per_row, h = (idx % per_row) / chunks, c = idx % chunks;
+                const size_t elem =
+                    (static_cast<size_t>(row0 + i) * p.n_q + static_cast<size_t>(g) * G + h) * kHeadDim;
+                reinterpret_cast<uint4 *>(static_cast<char *>(p.out) + elem * (p.out_bf16 ? 2 : 4))[c] =
+                    make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
         return;
     }
     const int c = ctx - q_len;

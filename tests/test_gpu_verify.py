@@ -3,8 +3,8 @@
 Row i of sequence b sits at position ctx_b - k + i and sees keys j <= ctx_b - k + i
 ("LLM 推理全过程的维度变化与核心公式", section "工程优化怎么嵌进公式", Speculative
 Decoding: the target model checks the k draft positions in one pass) -- the
-oracle's causal-chunk rule with q_len = k.  G * k <= 32 (or a G that does not
-divide 128) runs on the decode kernel (one 8-column MMA tile per CTA up to 8
+oracle's causal-chunk rule with q_len = k.  G * k <= 32 (or a G above 16 or
+one that does not divide 128) runs on the decode kernel (one 8-column MMA tile per CTA up to 8
 columns, two tiles up to 16, more CTAs per KV head above that, ragged shares
 included), larger products on the tcgen05 prefill kernel; all are covered.
 """
@@ -36,7 +36,7 @@ def _verify(d, batch, k, partition_size=0, out_dtype=None, context_lens=None):
     return out, ws
 
 
-@pytest.mark.parametrize("n_q,n_kv", [(32, 32), (32, 16), (48, 16), (32, 8), (64, 8), (32, 2)])
+@pytest.mark.parametrize("n_q,n_kv", [(32, 32), (32, 16), (48, 16), (32, 8), (64, 8), (32, 2), (32, 1)])
 @pytest.mark.parametrize("k", [1, 2, 3, 4, 7, 8, 16])
 def test_verify_parity(n_q, n_kv, k):
     ctx = [max(c, k) for c in CTX] + [k, k + 1]
@@ -48,7 +48,7 @@ def test_verify_parity(n_q, n_kv, k):
     ref = oracle.paged_attention(batch.q, batch.cu_q_lens, kc, vc, batch.block_tables, batch.context_lens, wl.scale,
                                  n_q=wl.n_q)
     G = n_q // n_kv
-    on_decode = G * k <= 32 or 128 % G != 0
+    on_decode = G * k <= 32 or G > 16 or 128 % G != 0
     for part in ((0, 16, 256) if on_decode else (0,)):
         out, ws = _verify(d, batch, k, partition_size=part)
         assert_close(out.cpu().numpy(), ref, what=f"G={n_q // n_kv} k={k} part={part}")
@@ -81,6 +81,12 @@ def test_verify_short_context_flags(n_q, n_kv, k):
     d.append()
     lens = batch.context_lens.copy()
     lens[1] = k - 1
-    out, ws = _verify(d, batch, k, context_lens=lens)
+    t = torch()
+    q = bf16_to_dev(batch.q)
+    out = t.full(q.shape, float("nan"), dtype=t.float32, device="cuda")  # every row must be written
+    ws = P.paged_attention_verify(out, q, k, d.k_cache, d.v_cache, i32_to_dev(batch.block_tables), i32_to_dev(lens),
+                                  d.wl.scale)
     assert status_word(ws) & P.PKV_STATUS_BAD_Q_LEN
-    assert np.all(np.isfinite(out[k:].cpu().numpy()))
+    o = out.cpu().numpy()
+    assert np.all(o[k:] == 0.0)          # the flagged sequence gets zero rows
+    assert np.all(np.isfinite(o[:k]))    # the valid one is computed
