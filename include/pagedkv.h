@@ -186,6 +186,26 @@ PKV_API size_t paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_he
                                       int32_t partition_size, const pkv_cache_desc *cache);
 
 /*
+ * paged_attention_decode_partitions -- how many partitions per sequence the
+ * decode entry points (paged_attention_decode, _append, _window, _fp8 and
+ * _static_scratch) split a row's keys into for these sizes: 1 means no split
+ * and no merge kernel; above 1 the log-sum-exp merge runs after the decode
+ * kernel.  window = 0 for no sliding window.  With partition_size = 0 the
+ * answer is the automatic choice for the current device (it reads the SM
+ * count, so it needs a GPU: PKV_ERR_CUDA otherwise).  The automatic choice
+ * uses 1024-token partitions; it does not split contexts of at most 2048
+ * tokens whose (sequence, KV head) units already fill one wave of the GPU; for
+ * a bf16 cache it never makes more than 32 partitions per sequence (the merge
+ * folds a row's partitions in sequence; the FP8 decode keeps the finer split);
+ * and with few units it shrinks the partitions (to no less than 256 tokens)
+ * until the grid covers every SM twice.
+ * Returns the count, or a negative PKV_ERR_* for invalid arguments.
+ */
+PKV_API int32_t paged_attention_decode_partitions(int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq,
+                                                  int32_t partition_size, int32_t window,
+                                                  const pkv_cache_desc *cache);
+
+/*
  * paged_attention_decode -- decode-phase attention over the paged cache.
  *
  * For each sequence b (ctx = context_lens[b], which already counts the token

@@ -26,6 +26,8 @@ using pkv::kHeadDim;
 constexpr int kMaxDevices = 64;
 constexpr int kMinPartBlocks = 16;      // automatic plans never go below 256 tokens per partition
 constexpr int kDefaultPartBlocks = 64;  // 1024 tokens
+constexpr int kMaxAutoParts = 32;       // automatic bf16 decode plans: at most 32 partitions per sequence
+constexpr int kDecodeCtasPerSm = 3;     // resident decode CTAs per SM (64 KB of shared memory each)
 constexpr size_t kStatusBytes = 256;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -207,21 +209,38 @@ DecodePlan plan_decode(int32_t num_seqs, int32_t n_q, int32_t n_kv, int32_t max_
     return pl;
 }
 
-int32_t auto_part_blocks(int32_t num_seqs, int32_t n_kv, int32_t head_splits, int32_t max_blocks, int sms) {
+int32_t auto_part_blocks(int32_t num_seqs, int32_t n_kv, int32_t head_splits, int32_t max_blocks, int sms,
+                         bool cap_parts) {
     // Partitions of 1024 tokens (measured best on ragged 8B-shaped batches and
-    // 70B-shaped long contexts) keep CTAs uniform and the merge small; a context
-    // that fits one partition is not split.  When few (sequence, head) units
-    // exist the partitions shrink (not below 256 tokens) until the grid covers
-    // every SM at least twice.
+    // 70B-shaped B=8 long contexts) keep CTAs uniform and the merge small; a
+    // context that fits one partition is not split.  Three refinements, each
+    // measured on a GB300 (decode call, L2 flushed):
+    //  (a) contexts of at most two default partitions whose unsplit grid already
+    //      covers every SM within one wave of resident CTAs are not split at all:
+    //      a second, ragged wave and the merge cost more than the split gains
+    //      (B=32 x 2048 tokens, 8 KV heads: 47.8 us unsplit vs 58.0 us);
+    //  (b) for the bf16 decode (cap_parts), at most 32 partitions per sequence,
+    //      since the merge folds a row's partitions in sequence (B=1 x 128K
+    //      tokens: 90.8 us with 4096-token partitions vs 103.1 us with 1024);
+    //      the FP8 decode and verify, bound by instruction issue, keep the finer
+    //      split (B=1 x 128K: 69.8 vs 73.3 us and 176 vs 184 us);
+    //  (c) when few (sequence, head) units exist the partitions shrink (not below
+    //      256 tokens, nor below (b)'s floor) until the grid covers every SM twice.
     if (const char *e = std::getenv("PAGEDKV_PART_BLOCKS")) {  // tuning sweeps
         const int v = std::atoi(e);
         if (v >= kMinPartBlocks) return v;
     }
-    int32_t pb = kDefaultPartBlocks;
     const int64_t units = static_cast<int64_t>(num_seqs) * n_kv * head_splits;
-    const int64_t want = static_cast<int64_t>(sms > 0 ? sms : 148) * 2;
-    while (pb > kMinPartBlocks && units * ((max_blocks + pb - 1) / pb) < want) pb /= 2;
-    return pb;
+    const int64_t nsm = sms > 0 ? sms : 148;
+    if (max_blocks <= 2 * kDefaultPartBlocks && units >= nsm && units <= nsm * kDecodeCtasPerSm)
+        return std::max(max_blocks, kMinPartBlocks);  // (a)
+    int32_t floor_pb = kMinPartBlocks;  // (b)
+    while (cap_parts && floor_pb < max_blocks && (max_blocks + floor_pb - 1) / floor_pb > kMaxAutoParts)
+        floor_pb *= 2;
+    int32_t pb = std::max(kDefaultPartBlocks, floor_pb);
+    const int64_t want = nsm * 2;  // (c)
+    while (pb > floor_pb && units * ((max_blocks + pb - 1) / pb) < want) pb /= 2;
+    return std::max(pb, floor_pb);
 }
 
 pkv::DecodeVariant decode_variant() {
@@ -334,6 +353,29 @@ size_t paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads, int
     return plan_decode(num_seqs, num_q_heads, cache->num_kv_heads, max_blocks_per_seq, pb).total;
 }
 
+int32_t paged_attention_decode_partitions(int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq,
+                                          int32_t partition_size, int32_t window, const pkv_cache_desc *cache) {
+    if (!cache) return PKV_ERR_INVALID_ARG;
+    if (int rc = cache->dtype == PKV_DTYPE_FP8_E4M3 ? check_cache_fp8(cache) : check_cache(cache)) return rc;
+    if (int rc = check_group(num_q_heads, cache->num_kv_heads)) return rc;
+    if (num_seqs < 1 || num_seqs > 65535 || max_blocks_per_seq < 1 || window < 0) return PKV_ERR_INVALID_ARG;
+    if (partition_size < 0 || partition_size % kBlockSize != 0) return PKV_ERR_INVALID_ARG;
+    // The same plan as the decode entry points: blocks a row can touch, CTAs per KV head.
+    const int32_t span = window > 0 ? static_cast<int32_t>(std::min<int64_t>(
+                                          max_blocks_per_seq, (static_cast<int64_t>(window) + 15) / kBlockSize + 1))
+                                    : max_blocks_per_seq;
+    const int32_t G = num_q_heads / cache->num_kv_heads;
+    const int32_t head_splits = G / (G < 8 ? G : 8);
+    int32_t pb = partition_size / kBlockSize;
+    if (partition_size == 0) {
+        const int dev = current_device();
+        if (dev < 0 || dev >= kMaxDevices) return PKV_ERR_CUDA;
+        pb = auto_part_blocks(num_seqs, cache->num_kv_heads, head_splits, span, sm_count(dev),
+                              cache->dtype != PKV_DTYPE_FP8_E4M3);
+    }
+    return plan_decode(num_seqs, num_q_heads, cache->num_kv_heads, span, pb).max_parts;
+}
+
 namespace {
 
 // Shared by the decode entry points; window = 0 means no sliding window; k_scale /
@@ -384,7 +426,7 @@ int decode_impl(void *out, int32_t out_dtype, const void *q, const void *k_cache
     const int sms = sm_count(dev);
 
     const int32_t pb = partition_size > 0 ? partition_size / kBlockSize
-                                          : auto_part_blocks(num_seqs, n_kv, head_splits, span_blocks, sms);
+                                          : auto_part_blocks(num_seqs, n_kv, head_splits, span_blocks, sms, !fp8);
     const DecodePlan pl = plan_decode(num_seqs, num_q_heads, n_kv, span_blocks, pb);
     if (workspace_bytes < pl.total) return PKV_ERR_WORKSPACE_TOO_SMALL;  // cannot happen for auto plans
 
@@ -655,7 +697,7 @@ int paged_attention_verify(void *out, int32_t out_dtype, const void *q, int32_t 
     if (static_cast<int64_t>(n_kv) * splits > 65535 || static_cast<int64_t>(num_seqs) * q_per_seq > 65535)
         return PKV_ERR_UNSUPPORTED;
     const int32_t pb = partition_size > 0 ? partition_size / kBlockSize
-                                          : auto_part_blocks(num_seqs, n_kv, splits, max_blocks_per_seq, sms);
+                                          : auto_part_blocks(num_seqs, n_kv, splits, max_blocks_per_seq, sms, false);
     const DecodePlan pl = plan_decode(num_seqs, num_q_heads, n_kv, max_blocks_per_seq, pb, q_per_seq, splits);
     if (workspace_bytes < pl.total) return PKV_ERR_WORKSPACE_TOO_SMALL;
 

@@ -76,6 +76,8 @@ def _declare(lib):
     lib.kv_reshape_and_cache.restype = ctypes.c_int
     lib.paged_attention_workspace_size.argtypes = [i32, i32, i32, i32, D]
     lib.paged_attention_workspace_size.restype = sz
+    lib.paged_attention_decode_partitions.argtypes = [i32, i32, i32, i32, i32, D]
+    lib.paged_attention_decode_partitions.restype = i32
     lib.paged_attention_decode.argtypes = [P, i32, P, P, P, P, P, i32, i32, i32, f32, i32, D, P, sz, P]
     lib.paged_attention_decode.restype = ctypes.c_int
     lib.paged_attention_decode_append.argtypes = [P, i32, P, P, P, P, P, P, P, i32, i32, i32, f32, i32, D, P, sz, P]
@@ -375,6 +377,15 @@ def paged_attention_workspace_size(num_seqs: int, num_q_heads: int, max_blocks_p
                                    partition_size: int, cache: CacheDesc) -> int:
     return int(load_library().paged_attention_workspace_size(num_seqs, num_q_heads, max_blocks_per_seq,
                                                              partition_size, ctypes.byref(cache)))
+
+
+def paged_attention_decode_partitions(num_seqs: int, num_q_heads: int, max_blocks_per_seq: int,
+                                      partition_size: int, cache: CacheDesc, window: int = 0) -> int:
+    """Partitions per sequence the decode entry points use (1: no merge kernel)."""
+    n = int(load_library().paged_attention_decode_partitions(num_seqs, num_q_heads, max_blocks_per_seq,
+                                                             partition_size, window, ctypes.byref(cache)))
+    _raise("paged_attention_decode_partitions", min(n, 0))
+    return n
 
 
 def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale: float,

@@ -61,6 +61,22 @@ def test_workspace_size_math(lib):
     assert lib.paged_attention_prefill_workspace_size(4, 32, ctypes.byref(c)) == 256
 
 
+def test_decode_partitions_with_explicit_size(lib):
+    """An explicit partition size gives ceil(blocks a row can touch / partition blocks); no GPU needed."""
+    c = desc()
+    n = lambda *a: lib.paged_attention_decode_partitions(*a, ctypes.byref(c))  # noqa: E731
+    assert n(64, 32, 256, 1024, 0) == 4       # 4096 tokens in 1024-token partitions
+    assert n(64, 32, 256, 4096, 0) == 1       # one partition: no merge kernel
+    assert n(64, 32, 256, 8192, 0) == 1
+    assert n(1, 64, 8192, 1024, 0) == 128
+    assert n(1, 64, 8192, 1024, 4096) == 5    # a 4096 window touches at most 257 blocks
+    assert n(64, 32, 256, 100, 0) == P.PKV_ERR_INVALID_ARG   # not a multiple of 16
+    assert n(64, 30, 256, 1024, 0) == P.PKV_ERR_INVALID_ARG  # 30 % 8 != 0
+    assert n(0, 32, 256, 1024, 0) == P.PKV_ERR_INVALID_ARG
+    assert n(64, 32, 256, 1024, -1) == P.PKV_ERR_INVALID_ARG
+    assert lib.paged_attention_decode_partitions(64, 32, 256, 1024, 0, None) == P.PKV_ERR_INVALID_ARG
+
+
 def _decode(lib, c, **kw):
     a = dict(out=FAKE, out_dtype=1, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, cl=FAKE, B=4, nq=32, mb=8, scale=0.088,
              part=0, ws=FAKE, wsb=1 << 20, stream=None)

@@ -291,3 +291,19 @@ def test_prefill_flags_inconsistent_lengths():
     ref = oracle_attention(wl, W.Batch(q=batch.q[:16], cu_q_lens=np.array([0, 16], np.int32),
                                        block_tables=batch.block_tables[:1], context_lens=batch.context_lens[:1]))
     assert_close(out[:16].cpu().numpy(), ref, what="valid sequence still computed")
+
+
+def test_auto_partitions_follow_the_measured_rules(built_library):
+    """The automatic split-KV plan: 1024-token partitions, no split for short
+    contexts whose unsplit grid fills one wave, at most 32 partitions per sequence."""
+    t = torch()
+    P.load_library()
+    sms = t.cuda.get_device_properties(0).multi_processor_count
+    c = P.CacheDesc(1000, 16, 8, 128, 0)
+    n = lambda B, nq, mb: P.paged_attention_decode_partitions(B, nq, mb, 0, c)  # noqa: E731
+    assert n(64, 32, 256) == 4          # ragged 8B-shaped batch, contexts up to 4096
+    assert n(8, 64, 2048) == 32         # 70B-shaped B=8 x 32K
+    assert n(1, 64, 8192) == 32         # B=1 x 128K: capped at 32 (4096-token partitions)
+    if sms <= 32 * 8 <= 3 * sms:
+        assert n(32, 32, 128) == 1      # B=32 x 2048, 8 KV heads: one wave unsplit
+    assert n(2, 32, 2) == 1             # a context inside one partition is never split
