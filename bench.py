@@ -383,6 +383,17 @@ def run_ours(args):
     rows = _row_variants(P, torch, dev, wl, batch, k_cache, v_cache, new_k, new_v, slots, q, tables, lens,
                          decode_ms, kv_bytes, steps=min(args.steps, 200), fused=fused) if world == 1 else None
 
+    if rows is not None and chunk is not None:
+        # the causal chunks under a 512-token window (each row sees its newest 512 keys)
+        pw = 512
+        mpw = _time_events(torch, stream, lambda: P.paged_attention_prefill_chunk(
+            cout, cq, ccu, cmax, k_cache, v_cache, ctab, clen, wl.scale, workspace=cws, window=pw),
+            min(args.steps, 200))
+        fw = _chunk_flops(chunk, wl, window=pw)
+        rows["window_prefill"] = {"window": pw, "algorithmic_flops": fw, "avg_launch_ms": round(mpw, 5),
+                                  "tflops": round(fw / mpw / 1e9, 2), "frac_of_bf16": round(fw / mpw / 1e9 / _bf16_peak()[0], 4),
+                                  "time_vs_unwindowed": round(mpw / prefill_ms, 3)}
+
     if rank == 0:
         peak, peak_src = measured_peaks()
         achieved = kv_bytes / (decode_ms / 1e3) / 1e9
@@ -537,12 +548,13 @@ def _row_variants(P, torch, dev, wl, batch, k_cache, v_cache, new_k, new_v, slot
     return res
 
 
-def _chunk_flops(chunk, wl) -> int:
-    """Algorithmic flops of the causal chunks: 4 * n_q * d per visible (query, key) pair."""
+def _chunk_flops(chunk, wl, window: int = 0) -> int:
+    """Algorithmic flops of the causal chunks: 4 * n_q * d per visible (query, key) pair
+    (row i at position c + i sees c + i + 1 keys, at most `window` of them under a window)."""
     pairs = 0
     for ql, ctx in zip(chunk.q_lens.tolist(), chunk.context_lens.tolist()):
         c = ctx - ql
-        pairs += sum(c + i + 1 for i in range(ql))
+        pairs += sum(min(c + i + 1, window) if window > 0 else c + i + 1 for i in range(ql))
     return 4 * wl.n_q * wl.head_dim * pairs
 
 

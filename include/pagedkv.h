@@ -423,6 +423,26 @@ PKV_API int paged_attention_prefill_chunk(void *out, int32_t out_dtype, const vo
                                   void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * paged_attention_prefill_chunk_window -- paged_attention_prefill_chunk with a
+ * sliding window of `window` >= 1 tokens ("LLM 推理全过程的维度变化与核心公式",
+ * section "KV Cache 的形状与增长", Sliding Window Attention: only the most
+ * recent W tokens' K and V are kept): row i at position pos = c + i sees keys
+ * pos - window < j <= pos.  Key tiles wholly before the earliest visible key
+ * of a CTA's rows are never fetched, and block_tables entries of blocks that
+ * lie wholly before it are never read (they may be stale); every other entry
+ * is checked as in paged_attention_prefill_chunk.  A window at least as long
+ * as the context gives exactly the unwindowed result.
+ * Errors: as paged_attention_prefill_chunk; PKV_ERR_INVALID_ARG for window < 1.
+ */
+PKV_API int paged_attention_prefill_chunk_window(void *out, int32_t out_dtype, const void *q,
+                                         const int32_t *cu_q_lens, int32_t max_q_len, int32_t total_q_rows,
+                                         const void *k_cache, const void *v_cache, const int32_t *block_tables,
+                                         const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                         int32_t max_blocks_per_seq, float scale, int32_t window,
+                                         const pkv_cache_desc *cache, void *workspace, size_t workspace_bytes,
+                                         void *stream);
+
+/*
  * paged_attention_verify -- attention of k draft positions per sequence
  * (speculative decoding's verification step).
  *

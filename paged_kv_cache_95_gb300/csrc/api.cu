@@ -554,9 +554,10 @@ int prefill_impl(void *out, int32_t out_dtype, const void *q, const int32_t *cu_
                  int32_t max_q_len, int32_t total_q_rows, const void *k_cache, const void *v_cache,
                  const int32_t *block_tables, const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
                  int32_t max_blocks_per_seq, float scale, const pkv_cache_desc *cache, void *workspace,
-                 size_t workspace_bytes, void *stream) {
+                 size_t workspace_bytes, void *stream, int32_t window = 0) {
     if (int rc = check_cache(cache)) return rc;
     if (num_q_heads < 1 || num_q_heads % cache->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+    if (window < 0) return PKV_ERR_INVALID_ARG;
     const int32_t G = num_q_heads / cache->num_kv_heads;
     // A 128-row MMA tile packs 128 / G query positions x the G heads of one KV group.
     if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return PKV_ERR_UNSUPPORTED;
@@ -606,6 +607,7 @@ int prefill_impl(void *out, int32_t out_dtype, const void *q, const int32_t *cu_
     p.total_rows = total_q_rows;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     p.out_bf16 = out_dtype == PKV_DTYPE_BF16;
+    p.window = window;
     if (pkv::launch_prefill_chunk(qmap, kmap, vmap, omap, p, max_q_len, static_cast<cudaStream_t>(stream)) !=
         cudaSuccess)
         return PKV_ERR_CUDA;
@@ -624,6 +626,19 @@ int paged_attention_prefill_chunk(void *out, int32_t out_dtype, const void *q, c
     return prefill_impl(out, out_dtype, q, cu_q_lens, 0, max_q_len, total_q_rows, k_cache, v_cache, block_tables,
                         context_lens, num_seqs, num_q_heads, max_blocks_per_seq, scale, cache, workspace,
                         workspace_bytes, stream);
+}
+
+int paged_attention_prefill_chunk_window(void *out, int32_t out_dtype, const void *q, const int32_t *cu_q_lens,
+                                         int32_t max_q_len, int32_t total_q_rows, const void *k_cache,
+                                         const void *v_cache, const int32_t *block_tables,
+                                         const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                         int32_t max_blocks_per_seq, float scale, int32_t window,
+                                         const pkv_cache_desc *cache, void *workspace, size_t workspace_bytes,
+                                         void *stream) {
+    if (!cu_q_lens || window < 1) return PKV_ERR_INVALID_ARG;
+    return prefill_impl(out, out_dtype, q, cu_q_lens, 0, max_q_len, total_q_rows, k_cache, v_cache, block_tables,
+                        context_lens, num_seqs, num_q_heads, max_blocks_per_seq, scale, cache, workspace,
+                        workspace_bytes, stream, window);
 }
 
 namespace {

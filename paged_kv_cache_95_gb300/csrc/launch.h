@@ -135,6 +135,7 @@ struct PrefillParams {
     float scale_log2;
     int32_t out_bf16;
     int32_t uniform_q_len;       // rows per sequence when cu_q_lens is null
+    int32_t window;              // sliding window W (> 0): a row at pos sees pos - W < j <= pos; 0: none
 };
 
 size_t prefill_smem_bytes();

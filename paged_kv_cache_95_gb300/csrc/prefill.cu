@@ -166,6 +166,9 @@ __device__ __forceinline__ void stage_row(uint32_t stage, int32_t bf16, int r, i
 
 // 608 threads, one CTA per SM (200 KB of shared memory); 19 warps put five on
 // some SM sub-partition, whose 16K registers then allow 96 a thread.
+// WINDOW: sliding-window instantiation (p.window > 0); the plain one compiles
+// without any of the window's bookkeeping.
+template <bool WINDOW>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_chunk_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                          const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
@@ -224,7 +227,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // whenever tile 1 has rows.
     auto tile_i0 = [&](int t) { return (2 * pair + t) * rpt; };
     auto tile_rows = [&](int t) { return max(0, min(rpt, q_len - tile_i0(t))); };
-    auto tile_nt = [&](int t) { return tile_rows(t) > 0 ? (c + tile_i0(t) + tile_rows(t) + 127) / 128 : 0; };
+    // Sliding window W: a row at position pos sees keys pos - W < j <= pos.  The
+    // CTA's earliest row sees nothing before kfirst, so key tiles before kt0 are
+    // never visited and blocks before fb are never read (their table entries may
+    // be stale).  Key tiles are counted from kt0 below: loop index kt is key tile
+    // kt0 + kt (keys 128 (kt0 + kt) ..).
+    const int W = WINDOW ? p.window : 0;
+    const int kfirst = W > 0 ? max(0, c + tile_i0(0) + 1 - W) : 0;
+    const int kt0 = kfirst / 128;
+    const int fb = kfirst / kBlockSize;
+    auto tile_nt = [&](int t) {
+        return tile_rows(t) > 0 ? (c + tile_i0(t) + tile_rows(t) + 127) / 128 - kt0 : 0;
+    };
     const int nt0 = tile_nt(0), nt1 = tile_nt(1);
     const int n_tiles = max(nt0, nt1);
     if (n_tiles == 0) return;
@@ -302,11 +316,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         // (block, head) tile index of key tile kt's t-th paged block, read by lane t
-        // (one parallel load per tile); invalid ids fetch tile 0 and are masked.
+        // (one parallel load per tile); invalid ids and blocks before the window
+        // fetch tile 0 and are masked.
         auto tile_index = [&](int kt) -> int {
-            const int jb = kt * 8 + lane;
+            const int jb = (kt0 + kt) * 8 + lane;
             int mine = 0;
-            if (lane < 8 && jb < nblocks) {
+            if (lane < 8 && (!WINDOW || jb >= fb) && jb < nblocks) {
                 mine = __ldg(table + jb);
                 if (static_cast<unsigned>(mine) >= static_cast<unsigned>(p.num_blocks)) mine = 0;
             }
@@ -324,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             const uint32_t bar = is_k ? k_full(st) : v_full(st);
             const uint32_t dst = ring + st * kOpBytes;
-            const int nload = min(8, nblocks - kt * 8);
+            const int nload = min(8, nblocks - (kt0 + kt) * 8);
             if (lane == 0) mbar_arrive_expect_tx(bar, nload * kBlkBytes);
             __syncwarp();
             if (lane < nload) tma_load_5d(dst + lane * kBlkBytes, map, bar, 0, 0, 0, 0, mine);
@@ -407,12 +422,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto row_sync = [&]() { asm volatile("bar.sync %0, 128;" ::"r"(row_bar) : "memory"); };
 
         // Per tile: the row's last visible key, running exponent reference and row-sum share.
-        int limit[kRowTiles];
+        int limit[kRowTiles], first[kRowTiles];
         float m_ref[kRowTiles], l[kRowTiles];
 #pragma unroll
         for (int t = 0; t < kRowTiles; ++t) {
             const int pos = c + tile_i0(t) + (ii < tile_rows(t) ? ii : 0);
-            limit[t] = min(pos, ctx - 1);  // visible keys: j <= limit
+            limit[t] = min(pos, ctx - 1);                  // visible keys: first <= j <= limit
+            first[t] = WINDOW ? max(0, pos + 1 - W) : 0;
             m_ref[t] = -INFINITY;
             l[t] = 0.f;
         }
@@ -423,15 +439,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         // always match and never hang.
         bool alive = true;
         for (int kt = 0; kt < n_tiles; ++kt) {
-            // Which of this key tile's blocks have an invalid id (their keys are masked):
-            // lane j < 8 checks block j, a ballot shares the answer.
-            const int jb = kt * 8 + lane;
-            const bool bad_lane = lane < 8 && jb < nblocks &&
+            // Which of this key tile's blocks have an invalid id (flagged) or lie wholly
+            // before the window (never read): their keys are masked.  Lane j < 8
+            // checks block j, a ballot shares the answer.
+            const int jb = (kt0 + kt) * 8 + lane;
+            const bool bad_lane = lane < 8 && (!WINDOW || jb >= fb) && jb < nblocks &&
                                   static_cast<unsigned>(__ldg(table + jb)) >= static_cast<unsigned>(p.num_blocks);
-            const uint32_t bad = __ballot_sync(0xffffffffu, bad_lane);
-            if (bad && tid == 0 && p.status) atomicOr(p.status, kStatusBadBlockId);
-            const int kc = kt * 128 + 32 * cq;  // first key of this thread's chunk
-            const int rv = ctx - kt * 128;      // keys [rv, 128) of the key tile are past the context
+            const uint32_t invalid = __ballot_sync(0xffffffffu, bad_lane);
+            if (invalid && tid == 0 && p.status) atomicOr(p.status, kStatusBadBlockId);
+            uint32_t bad = invalid;
+            if constexpr (WINDOW) bad |= (1u << min(8, max(0, fb - (kt0 + kt) * 8))) - 1u;
+            const int kc = (kt0 + kt) * 128 + 32 * cq;  // first key of this thread's chunk
+            const int rv = ctx - (kt0 + kt) * 128;      // keys [rv, 128) of the key tile are past the context
 
 #pragma unroll
             for (int t = 0; t < kRowTiles; ++t) {
@@ -451,10 +470,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld_32x32b_x32(t_s, v);
                 tmem_wait_ld();
                 tmem_hold(v);
-                if (!(kc + 31 <= limit[t] && !((bad >> (2 * cq)) & 3u))) {
+                if (!(kc + 31 <= limit[t] && (!WINDOW || kc >= first[t]) && !((bad >> (2 * cq)) & 3u))) {
 #pragma unroll
                     for (int k = 0; k < 32; ++k) {
-                        const bool ok = kc + k <= limit[t] && !((bad >> ((32 * cq + k) >> 4)) & 1u);
+                        const bool ok = kc + k <= limit[t] && (!WINDOW || kc + k >= first[t]) &&
+                                        !((bad >> ((32 * cq + k) >> 4)) & 1u);
                         if (!ok) v[k] = __float_as_uint(-INFINITY);
                     }
                 }
@@ -513,8 +533,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float2 rs = fadd2(rs0, rs1);
                 l[t] = l[t] * alpha + (rs.x + rs.y);
 
-                // Zero V rows of keys no row may see (past the context, or of a bad block),
-                // once per key tile, by the first tile that reads it, before its P V.
+                // Zero V rows of keys no row may see (past the context, of a bad block or
+                // of a block before the window), once per key tile, by the first tile that
+                // reads it, before its P V.
                 if ((rv < 128 || bad) && t == (kt < nt0 ? 0 : 1)) {
                     alive = warp_wait(v_full(kt % kStagesV), (kt / kStagesV) & 1);
                     if (!alive) continue;
@@ -609,7 +630,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 size_t prefill_smem_bytes() { return kSmemBytes; }
 
 cudaError_t prefill_prepare_device() {
-    return cudaFuncSetAttribute(prefill_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const cudaError_t e = cudaFuncSetAttribute(prefill_chunk_kernel<false>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(prefill_chunk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(kSmemBytes));
 }
 
@@ -618,7 +642,10 @@ cudaError_t launch_prefill_chunk(const CUtensorMap &qmap, const CUtensorMap &kma
     // One CTA per pair of row tiles.
     const int tiles = (max_q_len + p.rows_per_tile - 1) / p.rows_per_tile;
     const dim3 grid(p.n_kv, p.num_seqs, (tiles + 1) / 2);
-    return launch_pdl(prefill_chunk_kernel, grid, dim3(kThreads), kSmemBytes, stream, qmap, kmap, vmap, omap, p);
+    return p.window > 0 ? launch_pdl(prefill_chunk_kernel<true>, grid, dim3(kThreads), kSmemBytes, stream, qmap, kmap,
+                                     vmap, omap, p)
+                        : launch_pdl(prefill_chunk_kernel<false>, grid, dim3(kThreads), kSmemBytes, stream, qmap, kmap,
+                                     vmap, omap, p);
 }
 
 }  // namespace pkv

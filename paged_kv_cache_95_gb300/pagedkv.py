@@ -96,6 +96,9 @@ def _declare(lib):
     lib.paged_attention_prefill_workspace_size.restype = sz
     lib.paged_attention_prefill_chunk.argtypes = [P, i32, P, P, i32, i32, P, P, P, P, i32, i32, i32, f32, D, P, sz, P]
     lib.paged_attention_prefill_chunk.restype = ctypes.c_int
+    lib.paged_attention_prefill_chunk_window.argtypes = [P, i32, P, P, i32, i32, P, P, P, P, i32, i32, i32, f32, i32,
+                                                         D, P, sz, P]
+    lib.paged_attention_prefill_chunk_window.restype = ctypes.c_int
     lib.paged_attention_decode_static_scratch.argtypes = [P, i32, P, P, P, P, P, i32, i32, i32, f32, i32, D, P, P]
     lib.paged_attention_decode_static_scratch.restype = ctypes.c_int
     lib.kv_copy_blocks.argtypes = [P, P, P, P, P, i32, D, P]
@@ -477,8 +480,10 @@ def paged_attention_prefill_workspace_size(num_seqs: int, num_q_heads: int, cach
 
 
 def paged_attention_prefill_chunk(out, q, cu_q_lens, max_q_len: int, k_cache, v_cache, block_tables, context_lens,
-                                  scale: float, workspace=None, stream=None):
-    """Causal chunked-prefill attention; ``workspace`` is allocated if None."""
+                                  scale: float, workspace=None, stream=None, window: int = 0):
+    """Causal chunked-prefill attention; ``workspace`` is allocated if None.
+    ``window`` > 0 calls paged_attention_prefill_chunk_window (row at pos sees
+    keys pos - window < j <= pos)."""
     torch = _torch()
     desc = cache_desc(k_cache)
     _check(v_cache, "v_cache", torch.bfloat16, ndim=4)
@@ -497,7 +502,15 @@ def paged_attention_prefill_chunk(out, q, cu_q_lens, max_q_len: int, k_cache, v_
         _need(nbytes > 0, "invalid sizes for paged_attention_prefill_chunk")
         workspace = torch.zeros(nbytes, dtype=torch.uint8, device=q.device)  # status word starts clear
     _check(workspace, "workspace", torch.uint8, ndim=1)
-    rc = load_library().paged_attention_prefill_chunk(
+    lib = load_library()
+    if window:
+        rc = lib.paged_attention_prefill_chunk_window(
+            _ptr(out), _out_dtype(out), _ptr(q), _ptr(cu_q_lens), int(max_q_len), int(rows), _ptr(k_cache),
+            _ptr(v_cache), _ptr(block_tables), _ptr(context_lens), B, int(n_q), int(block_tables.shape[1]),
+            float(scale), int(window), ctypes.byref(desc), _ptr(workspace), int(workspace.numel()), _stream(stream))
+        _raise("paged_attention_prefill_chunk_window", rc)
+        return workspace
+    rc = lib.paged_attention_prefill_chunk(
         _ptr(out), _out_dtype(out), _ptr(q), _ptr(cu_q_lens), int(max_q_len), int(rows), _ptr(k_cache),
         _ptr(v_cache), _ptr(block_tables), _ptr(context_lens), B, int(n_q), int(block_tables.shape[1]),
         float(scale), ctypes.byref(desc), _ptr(workspace), int(workspace.numel()), _stream(stream))

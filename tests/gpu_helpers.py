@@ -67,13 +67,15 @@ class DevWorkload:
                                       partition_size=partition_size, window=window)
         return out, ws
 
-    def prefill(self, batch: W.Batch, out_dtype=None, workspace=None):
+    def prefill(self, batch: W.Batch, out_dtype=None, workspace=None, window=0, tables=None):
         t = torch()
         q = bf16_to_dev(batch.q)
-        out = t.empty(q.shape, dtype=out_dtype or t.float32, device="cuda")
+        out = t.full(q.shape, float("nan"), dtype=out_dtype or t.float32, device="cuda")  # every row is written
         ws = P.paged_attention_prefill_chunk(out, q, i32_to_dev(batch.cu_q_lens), int(batch.q_lens.max()),
-                                             self.k_cache, self.v_cache, i32_to_dev(batch.block_tables),
-                                             i32_to_dev(batch.context_lens), self.wl.scale, workspace=workspace)
+                                             self.k_cache, self.v_cache,
+                                             i32_to_dev(batch.block_tables if tables is None else tables),
+                                             i32_to_dev(batch.context_lens), self.wl.scale, workspace=workspace,
+                                             window=window)
         return out, ws
 
 

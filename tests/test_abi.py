@@ -236,3 +236,21 @@ def test_prefill_argument_errors(lib):
     assert call(wsb=8) == P.PKV_ERR_WORKSPACE_TOO_SMALL
     assert call(ws=None) == P.PKV_ERR_INVALID_ARG
     assert call(mq=0) == P.PKV_OK                        # empty chunk: nothing enqueued
+
+
+def test_prefill_window_argument_errors(lib):
+    c = desc()
+
+    def call(win, **kw):
+        a = dict(out=FAKE, dt=1, q=FAKE, cu=FAKE, mq=512, rows=2048, k=FAKE, v=FAKE, bt=FAKE, cl=FAKE, B=4, nq=32,
+                 mb=96, scale=0.088, ws=FAKE, wsb=256)
+        a.update(kw)
+        return lib.paged_attention_prefill_chunk_window(a["out"], a["dt"], a["q"], a["cu"], a["mq"], a["rows"],
+                                                        a["k"], a["v"], a["bt"], a["cl"], a["B"], a["nq"], a["mb"],
+                                                        a["scale"], win, ctypes.byref(c), a["ws"], a["wsb"], None)
+    assert call(0) == P.PKV_ERR_INVALID_ARG              # a window holds at least one token
+    assert call(-5) == P.PKV_ERR_INVALID_ARG
+    assert call(64, cu=None) == P.PKV_ERR_INVALID_ARG
+    assert call(64, nq=24) == P.PKV_ERR_UNSUPPORTED
+    assert call(64, wsb=8) == P.PKV_ERR_WORKSPACE_TOO_SMALL
+    assert call(64, mq=0) == P.PKV_OK                    # empty chunk: nothing enqueued

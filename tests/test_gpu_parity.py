@@ -282,12 +282,13 @@ def test_prefill_flags_inconsistent_lengths():
     lens = batch.context_lens.copy()
     lens[1] = 8  # fewer keys than query rows
     q = bf16_to_dev(batch.q)
-    out = t.zeros(q.shape, dtype=t.float32, device="cuda")
+    out = t.full(q.shape, float("nan"), dtype=t.float32, device="cuda")
     ws = t.zeros(256, dtype=t.uint8, device="cuda")
     P.paged_attention_prefill_chunk(out, q, i32_to_dev(batch.cu_q_lens), 16, d.k_cache, d.v_cache,
                                     i32_to_dev(batch.block_tables), i32_to_dev(lens), wl.scale, workspace=ws)
     t.cuda.synchronize()
     assert status_word(ws) & P.PKV_STATUS_BAD_Q_LEN
+    assert np.all(out[16:].cpu().numpy() == 0.0)  # the flagged sequence gets zero rows
     ref = oracle_attention(wl, W.Batch(q=batch.q[:16], cu_q_lens=np.array([0, 16], np.int32),
                                        block_tables=batch.block_tables[:1], context_lens=batch.context_lens[:1]))
     assert_close(out[:16].cpu().numpy(), ref, what="valid sequence still computed")

@@ -1,4 +1,5 @@
-"""Sliding-window decode (paged_attention_decode_window) against the fp64 oracle (GPU).
+"""Sliding-window decode (paged_attention_decode_window) and causal prefill chunk
+(paged_attention_prefill_chunk_window) against the fp64 oracle (GPU).
 
 A row at position p sees keys p - W < j <= p ("LLM 推理全过程的维度变化与核心公式",
 section "KV Cache 的形状与增长", Sliding Window Attention: only the most recent W
@@ -86,3 +87,58 @@ def test_window_argument_errors():
     d = DevWorkload(wl)
     with pytest.raises(P.PagedKVError):
         d.decode(batch, window=-3)
+
+
+@pytest.mark.parametrize("n_q,n_kv", [(32, 32), (32, 8), (64, 8), (32, 2), (32, 16)])
+def test_prefill_window_parity(n_q, n_kv):
+    """Causal chunks under a window: every row at pos sees pos - W < j <= pos; the
+    windows span one key, a partial block, a block, a key tile and beyond."""
+    ctx = [1, 7, 40, 33, 300, 128, 600, 1100]
+    q_lens = [1, 7, 32, 33, 100, 128, 129, 300]
+    wl, batch = W.make_custom(n_q, n_kv, ctx, q_lens=q_lens, seed=320 + n_q + n_kv, materialize_logical=False)
+    d = DevWorkload(wl)
+    d.append()
+    kc, vc = oracle_after_append(wl)
+    for win in (1, 15, 16, 100, 128, 129, 700, 5000):
+        ref = _oracle(wl, batch, kc, vc, win)
+        out, ws = d.prefill(batch, window=win)
+        assert_close(out.cpu().numpy(), ref, what=f"G={n_q // n_kv} W={win}")
+        assert status_word(ws) == 0
+
+
+def test_prefill_window_mixed_chunks_and_stale_entries():
+    """The mixed workload's 512-row chunks over 1024 cached tokens under a 300-token
+    window; table entries wholly before every row's window get invalid ids: the result
+    is unchanged and no bad-block flag is raised."""
+    wl = W.make_workload("mixed", materialize_logical=False)
+    d = DevWorkload(wl)
+    d.append()
+    kc, vc = oracle_after_append(wl)
+    ch = wl.chunk
+    win = 300
+    ref = _oracle(wl, ch, kc, vc, win)
+    tables = ch.block_tables.copy()
+    for b in range(ch.num_seqs):
+        c = int(ch.context_lens[b]) - int(ch.q_lens[b])
+        first = max(0, c + 1 - win) // 16  # the chunk's first row sees nothing before this block
+        tables[b, :first] = wl.k_cache.shape[0] + 11
+    out, ws = d.prefill(ch, window=win, tables=tables)
+    assert_close(out.cpu().numpy(), ref, what="mixed chunks, W=300")
+    assert status_word(ws) == 0
+
+
+def test_prefill_window_covering_context_is_exact():
+    """A window at least as long as the context gives the unwindowed result bit for bit."""
+    wl, batch = W.make_custom(32, 8, [700, 250, 1536], q_lens=[200, 250, 512], seed=330, materialize_logical=False)
+    d = DevWorkload(wl)
+    d.append()
+    plain, _ = d.prefill(batch)
+    wide, _ = d.prefill(batch, window=1536)
+    assert np.array_equal(plain.cpu().numpy(), wide.cpu().numpy())
+
+
+def test_prefill_window_argument_errors():
+    wl, batch = W.make_custom(8, 2, [20], q_lens=[4], seed=331, materialize_logical=False)
+    d = DevWorkload(wl)
+    with pytest.raises(P.PagedKVError):
+        d.prefill(batch, window=-3)
