@@ -477,6 +477,21 @@ PKV_API int paged_attention_verify(void *out, int32_t out_dtype, const void *q, 
                                    size_t workspace_bytes, void *stream);
 
 /*
+ * paged_attention_verify_window -- paged_attention_verify with a sliding window
+ * of `window` >= 1 tokens (same page and section as the decode's window): row i
+ * of a sequence, at position pos = ctx - k + i, sees keys pos - window < j <=
+ * pos.  Blocks wholly before the first row's window are not fetched and their
+ * table entries are not read.  Same paths, workspace and errors as
+ * paged_attention_verify; PKV_ERR_INVALID_ARG for window < 1.
+ */
+PKV_API int paged_attention_verify_window(void *out, int32_t out_dtype, const void *q, int32_t q_per_seq,
+                                          const void *k_cache, const void *v_cache, const int32_t *block_tables,
+                                          const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                          int32_t max_blocks_per_seq, float scale, int32_t partition_size,
+                                          int32_t window, const pkv_cache_desc *cache, void *workspace,
+                                          size_t workspace_bytes, void *stream);
+
+/*
  * ---- Host block manager ---------------------------------------------------------
  * Hands out the pool's physical blocks to sequences and emits the block tables
  * and slot mappings the kernels above consume.  Sources: "注意力演进与推理流程",

@@ -672,11 +672,14 @@ size_t paged_attention_verify_workspace_size(int32_t num_seqs, int32_t q_per_seq
         .total;
 }
 
-int paged_attention_verify(void *out, int32_t out_dtype, const void *q, int32_t q_per_seq, const void *k_cache,
-                           const void *v_cache, const int32_t *block_tables, const int32_t *context_lens,
-                           int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq, float scale,
-                           int32_t partition_size, const pkv_cache_desc *cache, void *workspace,
-                           size_t workspace_bytes, void *stream) {
+namespace {
+
+// Shared by paged_attention_verify and paged_attention_verify_window (window 0: none).
+int verify_impl(void *out, int32_t out_dtype, const void *q, int32_t q_per_seq, const void *k_cache,
+                const void *v_cache, const int32_t *block_tables, const int32_t *context_lens, int32_t num_seqs,
+                int32_t num_q_heads, int32_t max_blocks_per_seq, float scale, int32_t partition_size, int32_t window,
+                const pkv_cache_desc *cache, void *workspace, size_t workspace_bytes, void *stream) {
+    if (window < 0) return PKV_ERR_INVALID_ARG;
     if (int rc = check_cache(cache)) return rc;
     if (int rc = check_group(num_q_heads, cache->num_kv_heads)) return rc;
     if (q_per_seq < 1 || q_per_seq > kMaxVerifyRows) return PKV_ERR_INVALID_ARG;
@@ -686,7 +689,7 @@ int paged_attention_verify(void *out, int32_t out_dtype, const void *q, int32_t 
         if (static_cast<int64_t>(num_seqs) * q_per_seq > INT32_MAX) return PKV_ERR_INVALID_ARG;
         return prefill_impl(out, out_dtype, q, nullptr, q_per_seq, q_per_seq, num_seqs * q_per_seq, k_cache, v_cache,
                             block_tables, context_lens, num_seqs, num_q_heads, max_blocks_per_seq, scale, cache,
-                            workspace, workspace_bytes, stream);
+                            workspace, workspace_bytes, stream, window);
     }
     if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PKV_ERR_INVALID_ARG;
     if (out_dtype != PKV_DTYPE_FLOAT32 && out_dtype != PKV_DTYPE_BF16) return PKV_ERR_UNSUPPORTED;
@@ -711,9 +714,15 @@ int paged_attention_verify(void *out, int32_t out_dtype, const void *q, int32_t 
     // grid y of the decode kernel (KV heads x splits) and of the merge kernel (rows)
     if (static_cast<int64_t>(n_kv) * splits > 65535 || static_cast<int64_t>(num_seqs) * q_per_seq > 65535)
         return PKV_ERR_UNSUPPORTED;
+    // Blocks a sequence's rows can touch: all of its table, or under a window the
+    // keys from the first row's window start (ctx - k + 1 - W) to ctx - 1.
+    const int32_t span =
+        window > 0 ? static_cast<int32_t>(std::min<int64_t>(
+                         max_blocks_per_seq, (static_cast<int64_t>(window) + q_per_seq - 1 + 15) / kBlockSize + 1))
+                   : max_blocks_per_seq;
     const int32_t pb = partition_size > 0 ? partition_size / kBlockSize
-                                          : auto_part_blocks(num_seqs, n_kv, splits, max_blocks_per_seq, sms, false);
-    const DecodePlan pl = plan_decode(num_seqs, num_q_heads, n_kv, max_blocks_per_seq, pb, q_per_seq, splits);
+                                          : auto_part_blocks(num_seqs, n_kv, splits, span, sms, false);
+    const DecodePlan pl = plan_decode(num_seqs, num_q_heads, n_kv, span, pb, q_per_seq, splits);
     if (workspace_bytes < pl.total) return PKV_ERR_WORKSPACE_TOO_SMALL;
 
     CUtensorMap kmap, vmap;
@@ -749,11 +758,35 @@ int paged_attention_verify(void *out, int32_t out_dtype, const void *q, int32_t 
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     p.out_bf16 = out_dtype == PKV_DTYPE_BF16;
     p.fused_merge = fused_merge() ? 1 : 0;
-    p.window = 0;
+    p.window = window;
     p.q_per_seq = q_per_seq;
     return pkv::launch_paged_verify(kmap, vmap, p, var, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? PKV_OK
                : PKV_ERR_CUDA;
+}
+
+}  // namespace
+
+int paged_attention_verify(void *out, int32_t out_dtype, const void *q, int32_t q_per_seq, const void *k_cache,
+                           const void *v_cache, const int32_t *block_tables, const int32_t *context_lens,
+                           int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq, float scale,
+                           int32_t partition_size, const pkv_cache_desc *cache, void *workspace,
+                           size_t workspace_bytes, void *stream) {
+    return verify_impl(out, out_dtype, q, q_per_seq, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                       num_q_heads, max_blocks_per_seq, scale, partition_size, 0, cache, workspace, workspace_bytes,
+                       stream);
+}
+
+int paged_attention_verify_window(void *out, int32_t out_dtype, const void *q, int32_t q_per_seq,
+                                  const void *k_cache, const void *v_cache, const int32_t *block_tables,
+                                  const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                  int32_t max_blocks_per_seq, float scale, int32_t partition_size, int32_t window,
+                                  const pkv_cache_desc *cache, void *workspace, size_t workspace_bytes,
+                                  void *stream) {
+    if (window < 1) return PKV_ERR_INVALID_ARG;
+    return verify_impl(out, out_dtype, q, q_per_seq, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                       num_q_heads, max_blocks_per_seq, scale, partition_size, window, cache, workspace,
+                       workspace_bytes, stream);
 }
 
 

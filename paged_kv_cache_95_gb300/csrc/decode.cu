@@ -130,7 +130,10 @@ __global__ void __launch_bounds__(NW * 32)
         return;
     }
     const int nblocks = (ctx + kBlockSize - 1) / kBlockSize;
-    const int j0 = (p.window > 0 && ctx > p.window) ? ctx - p.window : 0;  // first visible key
+    int j0 = (p.window > 0 && ctx > p.window) ? ctx - p.window : 0;  // first visible key
+    if constexpr (VERIFY) {  // the earliest verified row (position ctx - q_per_seq) bounds the window
+        if (p.window > 0) j0 = max(0, ctx - p.q_per_seq + 1 - p.window);
+    }
     const int first_blk = j0 / kBlockSize;
     const int nparts = (nblocks - first_blk + p.part_blocks - 1) / p.part_blocks;
     if (part >= nparts) return;
@@ -246,12 +249,16 @@ __global__ void __launch_bounds__(NW * 32)
         if constexpr (FP8) {
             decode_block_fp8(acc, bq, kb, kb + kTileBytes8, scale_base + s * kStageScaleBytes, lo, valid, sl2, lane);
         } else if constexpr (VERIFY && NCT == 2) {
+            // column window starts (pos_end - W; far below any key without a window)
+            const int w = p.window > 0 ? p.window : (1 << 30);
             const int lim[2][2] = {{pos_end[0][0] - j * kBlockSize, pos_end[0][1] - j * kBlockSize},
                                    {pos_end[1][0] - j * kBlockSize, pos_end[1][1] - j * kBlockSize}};
-            decode_block_x2(acct, bqt, kb, kb + kTileBytes, lo, valid, sl2, lane, lim);
+            const int low[2][2] = {{lim[0][0] - w, lim[0][1] - w}, {lim[1][0] - w, lim[1][1] - w}};
+            decode_block_x2(acct, bqt, kb, kb + kTileBytes, lo, valid, sl2, lane, lim, low);
         } else if constexpr (VERIFY) {
-            decode_block(acc, bq, kb, kb + kTileBytes, lo, valid, sl2, lane, pos_end[0][0] - j * kBlockSize,
-                         pos_end[0][1] - j * kBlockSize);
+            const int w = p.window > 0 ? p.window : (1 << 30);
+            const int lim0 = pos_end[0][0] - j * kBlockSize, lim1 = pos_end[0][1] - j * kBlockSize;
+            decode_block<true>(acc, bq, kb, kb + kTileBytes, lo, valid, sl2, lane, lim0, lim1, lim0 - w, lim1 - w);
         } else
             decode_block(acc, bq, kb, kb + kTileBytes, lo, valid, sl2, lane);
         consumed = i + 1;
@@ -403,7 +410,9 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lse_merge_kernel(const Decod
     int ctx = __ldg(p.context_lens + b);
     const int max_ctx = p.max_blocks * kBlockSize;
     ctx = ctx < 1 ? 0 : (ctx > max_ctx ? max_ctx : ctx);
-    const int first_blk = ((p.window > 0 && ctx > p.window) ? ctx - p.window : 0) / kBlockSize;
+    // first visible key of the call's earliest row of this sequence, as the decode kernel has it
+    // (decode: rows_per_seq = 1, key ctx - W; verify: the first of the q_per_seq rows)
+    const int first_blk = (p.window > 0 ? max(0, ctx - rows_per_seq + 1 - p.window) : 0) / kBlockSize;
     const int nparts = ((ctx + kBlockSize - 1) / kBlockSize - first_blk + p.part_blocks - 1) / p.part_blocks;
     if (nparts <= 1) return;  // written directly by the decode kernel
     const size_t base = (static_cast<size_t>(r) * p.n_q + h) * p.max_parts;

@@ -84,11 +84,13 @@ __device__ __forceinline__ void load_q_frag(uint32_t (&bq)[8][2], const void *q,
 // window starts); the others are masked by index and their V rows are zeroed in
 // registers, so stale or NaN bytes in those slots never reach the result.
 // Multi-token verify: column 2*q4 (2*q4 + 1) of this lane also only sees keys
-// k < lim0 (lim1) -- its causal bound; keys between a column's bound and `valid`
-// hold valid data, so only their weight is zeroed.
+// k < lim0 (lim1) -- its causal bound -- and, with a sliding window (LOW), keys
+// k >= low0 (low1); keys between a column's bounds and [lo, valid) hold valid
+// data, so only their weight is zeroed.
+template <bool LOW = false>
 __device__ __forceinline__ void decode_block(DecodeAcc &acc, const uint32_t (&bq)[8][2], uint32_t kb, uint32_t vb,
                                              int lo, int valid, float sl2, int lane, int lim0 = kBlockSize,
-                                             int lim1 = kBlockSize) {
+                                             int lim1 = kBlockSize, int low0 = 0, int low1 = 0) {
     const int n = lane >> 2, q4 = lane & 3;
     const int kkey = (lane & 7) | (((lane >> 3) & 1) << 3);  // K: matrices (keys 0-7 | 8-15) x (dims lo | hi)
     const int khi = lane >> 4;
@@ -109,10 +111,18 @@ __device__ __forceinline__ void decode_block(DecodeAcc &acc, const uint32_t (&bq
     // Online softmax in the log2 domain (scale * log2(e) folded into the scores).
     const int key_a = n, key_b = n + 8;
     const bool in_a = key_a >= lo && key_a < valid, in_b = key_b >= lo && key_b < valid;
-    const float s00 = in_a && key_a < lim0 ? c[0] * sl2 : -INFINITY;
-    const float s01 = in_a && key_a < lim1 ? c[1] * sl2 : -INFINITY;
-    const float s10 = in_b && key_b < lim0 ? c[2] * sl2 : -INFINITY;
-    const float s11 = in_b && key_b < lim1 ? c[3] * sl2 : -INFINITY;
+    bool v00 = in_a && key_a < lim0, v01 = in_a && key_a < lim1;
+    bool v10 = in_b && key_b < lim0, v11 = in_b && key_b < lim1;
+    if constexpr (LOW) {
+        v00 = v00 && key_a >= low0;
+        v01 = v01 && key_a >= low1;
+        v10 = v10 && key_b >= low0;
+        v11 = v11 && key_b >= low1;
+    }
+    const float s00 = v00 ? c[0] * sl2 : -INFINITY;
+    const float s01 = v01 ? c[1] * sl2 : -INFINITY;
+    const float s10 = v10 ? c[2] * sl2 : -INFINITY;
+    const float s11 = v11 ? c[3] * sl2 : -INFINITY;
     float bm0 = fmaxf(s00, s10), bm1 = fmaxf(s01, s11);
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
@@ -177,10 +187,11 @@ __device__ __forceinline__ void decode_block(DecodeAcc &acc, const uint32_t (&bq
 // multi-token verify with G x q_per_seq in 9..16): each K and V fragment is read
 // from shared memory once and feeds both tiles' MMAs; each tile keeps its own
 // online-softmax state.  lim[t][0..1] are the causal bounds (exclusive, relative
-// to the block) of this lane's columns 2*q4 and 2*q4 + 1 of tile t.
+// to the block) of this lane's columns 2*q4 and 2*q4 + 1 of tile t; low[t][0..1]
+// their sliding-window starts (inclusive; 0 or below without a window).
 __device__ __forceinline__ void decode_block_x2(DecodeAcc (&acc)[2], const uint32_t (&bq)[2][8][2], uint32_t kb,
                                                 uint32_t vb, int lo, int valid, float sl2, int lane,
-                                                const int (&lim)[2][2]) {
+                                                const int (&lim)[2][2], const int (&low)[2][2]) {
     const int n = lane >> 2, q4 = lane & 3;
     const int kkey = (lane & 7) | (((lane >> 3) & 1) << 3);
     const int khi = lane >> 4;
@@ -205,10 +216,10 @@ __device__ __forceinline__ void decode_block_x2(DecodeAcc (&acc)[2], const uint3
     uint32_t pb[2][4];
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
-        const float s00 = in_a && key_a < lim[t][0] ? c[t][0] * sl2 : -INFINITY;
-        const float s01 = in_a && key_a < lim[t][1] ? c[t][1] * sl2 : -INFINITY;
-        const float s10 = in_b && key_b < lim[t][0] ? c[t][2] * sl2 : -INFINITY;
-        const float s11 = in_b && key_b < lim[t][1] ? c[t][3] * sl2 : -INFINITY;
+        const float s00 = in_a && key_a < lim[t][0] && key_a >= low[t][0] ? c[t][0] * sl2 : -INFINITY;
+        const float s01 = in_a && key_a < lim[t][1] && key_a >= low[t][1] ? c[t][1] * sl2 : -INFINITY;
+        const float s10 = in_b && key_b < lim[t][0] && key_b >= low[t][0] ? c[t][2] * sl2 : -INFINITY;
+        const float s11 = in_b && key_b < lim[t][1] && key_b >= low[t][1] ? c[t][3] * sl2 : -INFINITY;
         float bm0 = fmaxf(s00, s10), bm1 = fmaxf(s01, s11);
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {

@@ -90,6 +90,9 @@ def _declare(lib):
     lib.paged_attention_verify_workspace_size.restype = sz
     lib.paged_attention_verify.argtypes = [P, i32, P, i32, P, P, P, P, i32, i32, i32, f32, i32, D, P, sz, P]
     lib.paged_attention_verify.restype = ctypes.c_int
+    lib.paged_attention_verify_window.argtypes = [P, i32, P, i32, P, P, P, P, i32, i32, i32, f32, i32, i32, D, P, sz,
+                                                  P]
+    lib.paged_attention_verify_window.restype = ctypes.c_int
     lib.kv_reshape_and_cache_fp8.argtypes = [P, P, P, P, P, P, P, i32, D, P]
     lib.kv_reshape_and_cache_fp8.restype = ctypes.c_int
     lib.paged_attention_prefill_workspace_size.argtypes = [i32, i32, D]
@@ -444,9 +447,11 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
 
 
 def paged_attention_verify(out, q, q_per_seq: int, k_cache, v_cache, block_tables, context_lens, scale: float,
-                           workspace=None, partition_size: int = 0, stream=None):
+                           workspace=None, partition_size: int = 0, stream=None, window: int = 0):
     """Verify k = q_per_seq draft positions per sequence: q / out [num_seqs * k, n_q, 128],
-    row i of sequence b at position ctx_b - k + i (causal).  Returns the workspace."""
+    row i of sequence b at position ctx_b - k + i (causal).  ``window`` > 0 calls
+    paged_attention_verify_window (row at pos sees pos - window < j <= pos).
+    Returns the workspace."""
     torch = _torch()
     desc = cache_desc(k_cache)
     _check(v_cache, "v_cache", torch.bfloat16, ndim=4)
@@ -467,6 +472,14 @@ def paged_attention_verify(out, q, q_per_seq: int, k_cache, v_cache, block_table
         _need(nbytes > 0, "invalid sizes for paged_attention_verify")
         workspace = torch.zeros(nbytes, dtype=torch.uint8, device=q.device)
     _check(workspace, "workspace", torch.uint8, ndim=1)
+    if window:
+        rc = lib.paged_attention_verify_window(_ptr(out), _out_dtype(out), _ptr(q), int(q_per_seq), _ptr(k_cache),
+                                               _ptr(v_cache), _ptr(block_tables), _ptr(context_lens), B, int(n_q),
+                                               max_blocks, float(scale), int(partition_size), int(window),
+                                               ctypes.byref(desc), _ptr(workspace), int(workspace.numel()),
+                                               _stream(stream))
+        _raise("paged_attention_verify_window", rc)
+        return workspace
     rc = lib.paged_attention_verify(_ptr(out), _out_dtype(out), _ptr(q), int(q_per_seq), _ptr(k_cache),
                                     _ptr(v_cache), _ptr(block_tables), _ptr(context_lens), B, int(n_q), max_blocks,
                                     float(scale), int(partition_size), ctypes.byref(desc), _ptr(workspace),

@@ -254,3 +254,19 @@ def test_prefill_window_argument_errors(lib):
     assert call(64, nq=24) == P.PKV_ERR_UNSUPPORTED
     assert call(64, wsb=8) == P.PKV_ERR_WORKSPACE_TOO_SMALL
     assert call(64, mq=0) == P.PKV_OK                    # empty chunk: nothing enqueued
+
+
+def test_verify_window_argument_errors(lib):
+    c = desc()
+
+    def v(k, win, **kw):
+        a = dict(out=FAKE, q=FAKE, B=4, nq=32, wsb=1 << 20)
+        a.update(kw)
+        return lib.paged_attention_verify_window(a["out"], 1, a["q"], k, FAKE, FAKE, FAKE, FAKE, a["B"], a["nq"], 8,
+                                                 0.088, 0, win, ctypes.byref(c), FAKE, a["wsb"], None)
+    assert v(2, 0) == P.PKV_ERR_INVALID_ARG                     # a window holds at least one token
+    assert v(2, -7) == P.PKV_ERR_INVALID_ARG
+    assert v(0, 64) == P.PKV_ERR_INVALID_ARG
+    assert v(2, 64, nq=96) == P.PKV_ERR_UNSUPPORTED             # G = 12
+    assert v(2, 64, wsb=100) == P.PKV_ERR_WORKSPACE_TOO_SMALL   # decode path
+    assert v(16, 64, out=FAKE + 4) == P.PKV_ERR_INVALID_ARG     # prefill path: 16-B out

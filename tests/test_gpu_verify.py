@@ -26,13 +26,14 @@ def _lib(built_library):
     P.load_library()
 
 
-def _verify(d, batch, k, partition_size=0, out_dtype=None, context_lens=None):
+def _verify(d, batch, k, partition_size=0, out_dtype=None, context_lens=None, window=0, tables=None):
     t = torch()
     q = bf16_to_dev(batch.q)
-    out = t.empty(q.shape, dtype=out_dtype or t.float32, device="cuda")
+    out = t.full(q.shape, float("nan"), dtype=out_dtype or t.float32, device="cuda")  # every row is written
     lens = batch.context_lens if context_lens is None else context_lens
-    ws = P.paged_attention_verify(out, q, k, d.k_cache, d.v_cache, i32_to_dev(batch.block_tables), i32_to_dev(lens),
-                                  d.wl.scale, partition_size=partition_size)
+    ws = P.paged_attention_verify(out, q, k, d.k_cache, d.v_cache,
+                                  i32_to_dev(batch.block_tables if tables is None else tables), i32_to_dev(lens),
+                                  d.wl.scale, partition_size=partition_size, window=window)
     return out, ws
 
 
@@ -90,3 +91,37 @@ def test_verify_short_context_flags(n_q, n_kv, k):
     o = out.cpu().numpy()
     assert np.all(o[k:] == 0.0)          # the flagged sequence gets zero rows
     assert np.all(np.isfinite(o[:k]))    # the valid one is computed
+
+
+@pytest.mark.parametrize("n_q,n_kv,k", [(32, 8, 2), (32, 8, 4), (64, 8, 4), (64, 8, 8), (32, 1, 3), (32, 32, 16)])
+def test_verify_window_parity(n_q, n_kv, k):
+    """Verify under a sliding window: row i at pos = ctx - k + i sees pos - W < j <= pos
+    (decode kernel with one or two column tiles and several CTAs per KV head; the
+    tcgen05 prefill kernel for G * k > 32), with split partitions, and table entries
+    wholly before the first row's window set to invalid ids (never read, no flag)."""
+    ctx = [max(c, k) for c in CTX] + [k, k + 1]
+    wl, batch = W.make_custom(n_q, n_kv, ctx, q_lens=[k] * len(ctx), seed=540 + 7 * k + n_q // n_kv,
+                              materialize_logical=False)
+    d = DevWorkload(wl)
+    d.append()
+    kc, vc = oracle_after_append(wl)
+    G = n_q // n_kv
+    on_decode = G * k <= 32 or G > 16 or 128 % G != 0
+    for win in (1, 5, 16, 17, 100, 300):
+        ref = oracle.paged_attention(batch.q, batch.cu_q_lens, kc, vc, batch.block_tables, batch.context_lens,
+                                     wl.scale, n_q=wl.n_q, window=win)
+        tables = batch.block_tables.copy()
+        for b, c in enumerate(batch.context_lens):
+            first = max(0, int(c) - k + 1 - win) // 16
+            tables[b, :first] = wl.k_cache.shape[0] + 5
+        for part in ((0, 16) if on_decode else (0,)):
+            out, ws = _verify(d, batch, k, partition_size=part, window=win, tables=tables)
+            assert_close(out.cpu().numpy(), ref, what=f"G={G} k={k} W={win} part={part}")
+            assert status_word(ws) == 0
+
+
+def test_verify_window_errors():
+    wl, batch = W.make_custom(32, 8, [50], q_lens=[4], seed=545, materialize_logical=False)
+    d = DevWorkload(wl)
+    with pytest.raises(P.PagedKVError):
+        _verify(d, batch, 4, window=-1)
