@@ -196,9 +196,11 @@ PKV_API size_t paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_he
  * uses 1024-token partitions; it does not split contexts of at most 2048
  * tokens whose (sequence, KV head) units already fill one wave of the GPU; for
  * a bf16 cache it never makes more than 32 partitions per sequence (the merge
- * folds a row's partitions in sequence; the FP8 decode keeps the finer split);
- * and with few units it shrinks the partitions (to no less than 256 tokens)
- * until the grid covers every SM twice.
+ * folds a row's partitions in sequence); and with few units it shrinks the
+ * partitions (to no less than 256 tokens) until the grid covers every SM
+ * twice.  For an FP8 cache (half the bytes per CTA) contexts of at most 2048
+ * tokens whose units fill every SM are not split, and contexts of 16K tokens
+ * and more double the partition while at least 3 CTAs per SM remain.
  * Returns the count, or a negative PKV_ERR_* for invalid arguments.
  */
 PKV_API int32_t paged_attention_decode_partitions(int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq,

@@ -210,7 +210,7 @@ DecodePlan plan_decode(int32_t num_seqs, int32_t n_q, int32_t n_kv, int32_t max_
 }
 
 int32_t auto_part_blocks(int32_t num_seqs, int32_t n_kv, int32_t head_splits, int32_t max_blocks, int sms,
-                         bool cap_parts) {
+                         bool cap_parts, bool fp8 = false) {
     // Partitions of 1024 tokens (measured best on ragged 8B-shaped batches and
     // 70B-shaped B=8 long contexts) keep CTAs uniform and the merge small; a
     // context that fits one partition is not split.  Three refinements, each
@@ -232,6 +232,22 @@ int32_t auto_part_blocks(int32_t num_seqs, int32_t n_kv, int32_t head_splits, in
     }
     const int64_t units = static_cast<int64_t>(num_seqs) * n_kv * head_splits;
     const int64_t nsm = sms > 0 ? sms : 148;
+    if (fp8) {
+        // The FP8 decode moves half the bytes per CTA, so it prefers fewer, longer
+        // CTAs (back-to-back decode calls, GB300): contexts of at most 2048 tokens
+        // whose units fill every SM are not split (MHA B=32 x 2048: 94.8 us vs
+        // 101.3 us with 1024-token partitions), and contexts of 16K tokens and more
+        // double the partition while at least 3 CTAs per SM remain (B=8 x 32K:
+        // 4096-token partitions, 108.4 vs 113.3 us; B=1 x 128K: 2048-token, 62.7 vs
+        // 72.3 us).  Ragged batches of shorter contexts keep 1024-token partitions
+        // (8B-shaped B=64: 68.5 us; 2048-token partitions: 80.5 us).
+        if (max_blocks <= 2 * kDefaultPartBlocks && units >= nsm) return std::max(max_blocks, kMinPartBlocks);
+        if (max_blocks >= 16 * kDefaultPartBlocks) {
+            int32_t pb = kDefaultPartBlocks;
+            while (units * ((max_blocks + 2 * pb - 1) / (2 * pb)) >= kDecodeCtasPerSm * nsm) pb *= 2;
+            return pb;
+        }
+    }
     if (max_blocks <= 2 * kDefaultPartBlocks && units >= nsm && units <= nsm * kDecodeCtasPerSm)
         return std::max(max_blocks, kMinPartBlocks);  // (a)
     int32_t floor_pb = kMinPartBlocks;  // (b)
@@ -370,8 +386,8 @@ int32_t paged_attention_decode_partitions(int32_t num_seqs, int32_t num_q_heads,
     if (partition_size == 0) {
         const int dev = current_device();
         if (dev < 0 || dev >= kMaxDevices) return PKV_ERR_CUDA;
-        pb = auto_part_blocks(num_seqs, cache->num_kv_heads, head_splits, span, sm_count(dev),
-                              cache->dtype != PKV_DTYPE_FP8_E4M3);
+        const bool fp8 = cache->dtype == PKV_DTYPE_FP8_E4M3;
+        pb = auto_part_blocks(num_seqs, cache->num_kv_heads, head_splits, span, sm_count(dev), !fp8, fp8);
     }
     return plan_decode(num_seqs, num_q_heads, cache->num_kv_heads, span, pb).max_parts;
 }
@@ -426,7 +442,7 @@ int decode_impl(void *out, int32_t out_dtype, const void *q, const void *k_cache
     const int sms = sm_count(dev);
 
     const int32_t pb = partition_size > 0 ? partition_size / kBlockSize
-                                          : auto_part_blocks(num_seqs, n_kv, head_splits, span_blocks, sms, !fp8);
+                                          : auto_part_blocks(num_seqs, n_kv, head_splits, span_blocks, sms, !fp8, fp8);
     const DecodePlan pl = plan_decode(num_seqs, num_q_heads, n_kv, span_blocks, pb);
     if (workspace_bytes < pl.total) return PKV_ERR_WORKSPACE_TOO_SMALL;  // cannot happen for auto plans
 

@@ -308,3 +308,11 @@ def test_auto_partitions_follow_the_measured_rules(built_library):
     if sms <= 32 * 8 <= 3 * sms:
         assert n(32, 32, 128) == 1      # B=32 x 2048, 8 KV heads: one wave unsplit
     assert n(2, 32, 2) == 1             # a context inside one partition is never split
+    # FP8 cache: fewer, longer CTAs (half the bytes per CTA)
+    c8 = P.CacheDesc(1000, 16, 8, 128, P.PKV_DTYPE_FP8_E4M3)
+    n8 = lambda B, nq, mb: P.paged_attention_decode_partitions(B, nq, mb, 0, c8)  # noqa: E731
+    assert n8(64, 32, 256) == 4         # ragged 8B-shaped batch: 1024-token partitions
+    if sms == 152:
+        assert n8(8, 64, 2048) == 8     # B=8 x 32K: 4096-token partitions
+        assert n8(1, 64, 8192) == 64    # B=1 x 128K: 2048-token partitions
+    assert n8(32, 256, 128) == 1        # MHA-shaped 2048-token contexts filling the GPU: unsplit
