@@ -494,6 +494,26 @@ PKV_API int paged_attention_verify_window(void *out, int32_t out_dtype, const vo
                                           size_t workspace_bytes, void *stream);
 
 /*
+ * paged_attention_verify_fp8 -- paged_attention_verify over an FP8 (E4M3) cache
+ * (cache->dtype PKV_DTYPE_FP8_E4M3; codes and scales as written by
+ * kv_reshape_and_cache_fp8, attention over code * scale as in
+ * paged_attention_decode_fp8), with an optional sliding window (window = 0:
+ * none).  Always on the decode kernel, one 8-column MMA tile per CTA: the
+ * G * k (position, head) columns of a KV head are shared out over
+ * ceil(G * k / 8) CTAs, each reading the K/V codes once.  Workspace:
+ * paged_attention_verify_workspace_size() with the FP8 cache descriptor.
+ * Errors: as paged_attention_verify; PKV_ERR_INVALID_ARG for a missing or
+ * misaligned scale array.
+ */
+PKV_API int paged_attention_verify_fp8(void *out, int32_t out_dtype, const void *q, int32_t q_per_seq,
+                                       const void *k_cache, const void *v_cache, const float *k_scale,
+                                       const float *v_scale, const int32_t *block_tables,
+                                       const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                       int32_t max_blocks_per_seq, float scale, int32_t window,
+                                       int32_t partition_size, const pkv_cache_desc *cache, void *workspace,
+                                       size_t workspace_bytes, void *stream);
+
+/*
  * ---- Host block manager ---------------------------------------------------------
  * Hands out the pool's physical blocks to sequences and emits the block tables
  * and slot mappings the kernels above consume.  Sources: "注意力演进与推理流程",

@@ -668,39 +668,50 @@ constexpr int32_t kMaxVerifyCols = 32;  // (position, head) pairs per KV head on
 bool verify_on_decode(int32_t q_per_seq, int32_t G) {
     return static_cast<int64_t>(q_per_seq) * G <= kMaxVerifyCols || G > 16 || 128 % G != 0;
 }
-// CTAs per KV head and the columns each takes (the last one may take fewer).
-int32_t verify_splits(int32_t cols) { return (cols + 15) / 16; }
-int32_t verify_cols_per_cta(int32_t cols) { return (cols + verify_splits(cols) - 1) / verify_splits(cols); }
+// CTAs per KV head and the columns each takes (the last one may take fewer): up to
+// 16 columns (two 8-column MMA tiles) per CTA, 8 over an FP8 cache (one tile).
+int32_t verify_splits(int32_t cols, bool fp8 = false) { return fp8 ? (cols + 7) / 8 : (cols + 15) / 16; }
+int32_t verify_cols_per_cta(int32_t cols, bool fp8 = false) {
+    return (cols + verify_splits(cols, fp8) - 1) / verify_splits(cols, fp8);
+}
 }  // namespace
 
 size_t paged_attention_verify_workspace_size(int32_t num_seqs, int32_t q_per_seq, int32_t num_q_heads,
                                              int32_t max_blocks_per_seq, int32_t partition_size,
                                              const pkv_cache_desc *cache) {
-    if (check_cache(cache) != PKV_OK || num_seqs < 1 || max_blocks_per_seq < 1) return 0;
+    if (!cache) return 0;
+    const bool fp8 = cache->dtype == PKV_DTYPE_FP8_E4M3;
+    if ((fp8 ? check_cache_fp8(cache) : check_cache(cache)) != PKV_OK || num_seqs < 1 || max_blocks_per_seq < 1)
+        return 0;
     if (q_per_seq < 1 || q_per_seq > kMaxVerifyRows) return 0;
     if (check_group(num_q_heads, cache->num_kv_heads) != PKV_OK) return 0;
     if (partition_size < 0 || partition_size % kBlockSize != 0) return 0;
     const int32_t G = num_q_heads / cache->num_kv_heads;
-    if (!verify_on_decode(q_per_seq, G)) return kStatusBytes;
+    if (!fp8 && !verify_on_decode(q_per_seq, G)) return kStatusBytes;
     const int32_t pb = partition_size > 0 ? partition_size / kBlockSize : kMinPartBlocks;
     return plan_decode(num_seqs, num_q_heads, cache->num_kv_heads, max_blocks_per_seq, pb, q_per_seq,
-                       verify_splits(G * q_per_seq))
+                       verify_splits(G * q_per_seq, fp8))
         .total;
 }
 
 namespace {
 
 // Shared by paged_attention_verify and paged_attention_verify_window (window 0: none).
+// k_scale / v_scale non-null: an FP8 cache (cache->dtype PKV_DTYPE_FP8_E4M3), always
+// on the decode kernel with one 8-column MMA tile per CTA.
 int verify_impl(void *out, int32_t out_dtype, const void *q, int32_t q_per_seq, const void *k_cache,
                 const void *v_cache, const int32_t *block_tables, const int32_t *context_lens, int32_t num_seqs,
                 int32_t num_q_heads, int32_t max_blocks_per_seq, float scale, int32_t partition_size, int32_t window,
-                const pkv_cache_desc *cache, void *workspace, size_t workspace_bytes, void *stream) {
+                const pkv_cache_desc *cache, void *workspace, size_t workspace_bytes, void *stream,
+                const float *k_scale = nullptr, const float *v_scale = nullptr) {
     if (window < 0) return PKV_ERR_INVALID_ARG;
-    if (int rc = check_cache(cache)) return rc;
+    const bool fp8 = k_scale != nullptr;
+    if (int rc = fp8 ? check_cache_fp8(cache) : check_cache(cache)) return rc;
+    if (fp8 && (!v_scale || !aligned(k_scale, 16) || !aligned(v_scale, 16))) return PKV_ERR_INVALID_ARG;
     if (int rc = check_group(num_q_heads, cache->num_kv_heads)) return rc;
     if (q_per_seq < 1 || q_per_seq > kMaxVerifyRows) return PKV_ERR_INVALID_ARG;
     const int32_t G = num_q_heads / cache->num_kv_heads;
-    if (!verify_on_decode(q_per_seq, G)) {
+    if (!fp8 && !verify_on_decode(q_per_seq, G)) {
         // Prefill kernel, uniform rows: sequence b owns q rows b * q_per_seq .. + q_per_seq - 1.
         if (static_cast<int64_t>(num_seqs) * q_per_seq > INT32_MAX) return PKV_ERR_INVALID_ARG;
         return prefill_impl(out, out_dtype, q, nullptr, q_per_seq, q_per_seq, num_seqs * q_per_seq, k_cache, v_cache,
@@ -726,7 +737,7 @@ int verify_impl(void *out, int32_t out_dtype, const void *q, int32_t q_per_seq, 
     if (dev < 0 || dev >= kMaxDevices) return PKV_ERR_CUDA;
     const int sms = sm_count(dev);
     const int32_t cols = G * q_per_seq;
-    const int32_t splits = verify_splits(cols);
+    const int32_t splits = verify_splits(cols, fp8);
     // grid y of the decode kernel (KV heads x splits) and of the merge kernel (rows)
     if (static_cast<int64_t>(n_kv) * splits > 65535 || static_cast<int64_t>(num_seqs) * q_per_seq > 65535)
         return PKV_ERR_UNSUPPORTED;
@@ -742,16 +753,24 @@ int verify_impl(void *out, int32_t out_dtype, const void *q, int32_t q_per_seq, 
     if (workspace_bytes < pl.total) return PKV_ERR_WORKSPACE_TOO_SMALL;
 
     CUtensorMap kmap, vmap;
-    if (!encode_pool_map(&kmap, k_cache, cache->num_blocks, n_kv) ||
-        !encode_pool_map(&vmap, v_cache, cache->num_blocks, n_kv))
+    if (fp8 ? (!encode_pool_map_fp8(&kmap, k_cache, cache->num_blocks, n_kv) ||
+               !encode_pool_map_fp8(&vmap, v_cache, cache->num_blocks, n_kv))
+            : (!encode_pool_map(&kmap, k_cache, cache->num_blocks, n_kv) ||
+               !encode_pool_map(&vmap, v_cache, cache->num_blocks, n_kv)))
         return PKV_ERR_CUDA;
     const pkv::DecodeVariant var = decode_variant();
     const int vi = variant_index(var);
-    std::call_once(g_decode_prepared[dev][vi], [&] { g_decode_prep_err[dev][vi] = pkv::decode_prepare_device(var); });
-    if (g_decode_prep_err[dev][vi] != cudaSuccess) return PKV_ERR_CUDA;
+    if (fp8) {
+        std::call_once(g_decode_fp8_prepared[dev], [&] { g_decode_fp8_prep_err[dev] = pkv::decode_fp8_prepare_device(); });
+        if (g_decode_fp8_prep_err[dev] != cudaSuccess) return PKV_ERR_CUDA;
+    } else {
+        std::call_once(g_decode_prepared[dev][vi],
+                       [&] { g_decode_prep_err[dev][vi] = pkv::decode_prepare_device(var); });
+        if (g_decode_prep_err[dev][vi] != cudaSuccess) return PKV_ERR_CUDA;
+    }
 
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    pkv::DecodeParamsVerify p{};
+    pkv::DecodeParamsFp8Verify p{};
     p.q = q;
     p.out = out;
     p.block_tables = block_tables;
@@ -765,7 +784,7 @@ int verify_impl(void *out, int32_t out_dtype, const void *q, int32_t q_per_seq, 
     p.n_q = num_q_heads;
     p.n_kv = n_kv;
     p.group = G;
-    p.heads_per_cta = verify_cols_per_cta(cols);  // the CTA's share of the q_per_seq x G columns
+    p.heads_per_cta = verify_cols_per_cta(cols, fp8);  // the CTA's share of the q_per_seq x G columns
     p.head_splits = splits;
     p.max_blocks = max_blocks_per_seq;
     p.num_blocks = cache->num_blocks;
@@ -776,9 +795,18 @@ int verify_impl(void *out, int32_t out_dtype, const void *q, int32_t q_per_seq, 
     p.fused_merge = fused_merge() ? 1 : 0;
     p.window = window;
     p.q_per_seq = q_per_seq;
-    return pkv::launch_paged_verify(kmap, vmap, p, var, static_cast<cudaStream_t>(stream)) == cudaSuccess
-               ? PKV_OK
-               : PKV_ERR_CUDA;
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
+    cudaError_t e;
+    if (fp8) {
+        e = pkv::launch_paged_verify_fp8(kmap, vmap, p, static_cast<cudaStream_t>(stream));
+    } else {
+        pkv::DecodeParamsVerify pv{};
+        static_cast<pkv::DecodeParams &>(pv) = static_cast<const pkv::DecodeParams &>(p);
+        pv.q_per_seq = q_per_seq;
+        e = pkv::launch_paged_verify(kmap, vmap, pv, var, static_cast<cudaStream_t>(stream));
+    }
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 }  // namespace
@@ -803,6 +831,18 @@ int paged_attention_verify_window(void *out, int32_t out_dtype, const void *q, i
     return verify_impl(out, out_dtype, q, q_per_seq, k_cache, v_cache, block_tables, context_lens, num_seqs,
                        num_q_heads, max_blocks_per_seq, scale, partition_size, window, cache, workspace,
                        workspace_bytes, stream);
+}
+
+int paged_attention_verify_fp8(void *out, int32_t out_dtype, const void *q, int32_t q_per_seq, const void *k_cache,
+                               const void *v_cache, const float *k_scale, const float *v_scale,
+                               const int32_t *block_tables, const int32_t *context_lens, int32_t num_seqs,
+                               int32_t num_q_heads, int32_t max_blocks_per_seq, float scale, int32_t window,
+                               int32_t partition_size, const pkv_cache_desc *cache, void *workspace,
+                               size_t workspace_bytes, void *stream) {
+    if (!k_scale || !v_scale) return PKV_ERR_INVALID_ARG;
+    return verify_impl(out, out_dtype, q, q_per_seq, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                       num_q_heads, max_blocks_per_seq, scale, partition_size, window, cache, workspace,
+                       workspace_bytes, stream, k_scale, v_scale);
 }
 
 

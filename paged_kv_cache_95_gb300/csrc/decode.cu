@@ -60,7 +60,7 @@ namespace {
 
 template <bool FP8, bool VERIFY, bool APPEND = false>
 using DecodeParamsT = std::conditional_t<
-    FP8, DecodeParamsFp8,
+    FP8, std::conditional_t<VERIFY, DecodeParamsFp8Verify, DecodeParamsFp8>,
     std::conditional_t<VERIFY, DecodeParamsVerify, std::conditional_t<APPEND, DecodeParamsAppend, DecodeParams>>>;
 
 // NCT: 8-column MMA tiles per CTA (2 only for multi-token verify with 9..16 columns).
@@ -186,7 +186,10 @@ __global__ void __launch_bounds__(NW * 32)
     uint32_t bqt[NCT][8][2];
     auto &bq = bqt[0];
     float sl2 = p.scale_log2;
-    if constexpr (FP8) {
+    if constexpr (FP8 && VERIFY) {
+        const int qexp = load_q_frag_fp8_row(bq, p.q, col_row(n), n < ncols, lane);
+        sl2 *= ldexpf(1.f, -qexp);
+    } else if constexpr (FP8) {
         const int qexp = load_q_frag_fp8(bq, p.q, static_cast<size_t>(b) * p.n_q + h0, hpc, lane);
         sl2 *= ldexpf(1.f, -qexp);
     } else if constexpr (VERIFY) {
@@ -246,7 +249,12 @@ __global__ void __launch_bounds__(NW * 32)
                 __syncwarp();
             }
         }
-        if constexpr (FP8) {
+        if constexpr (FP8 && VERIFY) {
+            const int w = p.window > 0 ? p.window : (1 << 30);
+            const int lim0 = pos_end[0][0] - j * kBlockSize, lim1 = pos_end[0][1] - j * kBlockSize;
+            decode_block_fp8<true>(acc, bq, kb, kb + kTileBytes8, scale_base + s * kStageScaleBytes, lo, valid, sl2,
+                                   lane, lim0, lim1, lim0 - w, lim1 - w);
+        } else if constexpr (FP8) {
             decode_block_fp8(acc, bq, kb, kb + kTileBytes8, scale_base + s * kStageScaleBytes, lo, valid, sl2, lane);
         } else if constexpr (VERIFY && NCT == 2) {
             // column window starts (pos_end - W; far below any key without a window)
@@ -518,8 +526,18 @@ size_t decode_fp8_smem_bytes() {
 }
 
 cudaError_t decode_fp8_prepare_device() {
-    return cudaFuncSetAttribute(paged_decode_kernel<kFp8Warps, kFp8Stages, true>,
+    const cudaError_t e =
+        cudaFuncSetAttribute(paged_decode_kernel<kFp8Warps, kFp8Stages, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(decode_fp8_smem_bytes()));
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(paged_decode_kernel<kFp8Warps, kFp8Stages, true, true>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(decode_fp8_smem_bytes()));
+}
+
+cudaError_t launch_paged_verify_fp8(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParamsFp8Verify &p,
+                                    cudaStream_t stream) {
+    if (p.heads_per_cta > 8) return cudaErrorInvalidValue;  // one 8-column MMA tile per CTA
+    return launch_variant<kFp8Warps, kFp8Stages, true, true>(kmap, vmap, p, stream);
 }
 
 cudaError_t launch_paged_decode_fp8(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParamsFp8 &p,

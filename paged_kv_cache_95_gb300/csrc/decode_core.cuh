@@ -309,12 +309,11 @@ constexpr uint32_t kStageScaleBytes = 2 * kScaleBytes;    // K scales + V scales
 // chosen so that the largest |q| of the CTA's heads lands in [2^13, 2^14): the
 // power-of-two scaling is exact and keeps every value inside the fp16 range.
 // Returns qexp (the caller multiplies the scores by 2^-qexp).
-__device__ __forceinline__ int load_q_frag_fp8(uint32_t (&bq)[8][2], const void *q, size_t head0_row, int hpc,
-                                               int lane) {
-    const int n = lane >> 2, q4 = lane & 3;
-    const bool hv = n < hpc;
-    const uint32_t *qrow =
-        reinterpret_cast<const uint32_t *>(static_cast<const __nv_bfloat16 *>(q) + (head0_row + n) * kHeadDim);
+// Column n reads q row `row` (multiples of 128 elements); columns with hv false are zero.
+__device__ __forceinline__ int load_q_frag_fp8_row(uint32_t (&bq)[8][2], const void *q, size_t row, bool hv,
+                                                   int lane) {
+    const int q4 = lane & 3;
+    const uint32_t *qrow = reinterpret_cast<const uint32_t *>(static_cast<const __nv_bfloat16 *>(q) + row * kHeadDim);
     float amax = 0.f;
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
@@ -344,6 +343,13 @@ __device__ __forceinline__ int load_q_frag_fp8(uint32_t (&bq)[8][2], const void 
     return qexp;
 }
 
+// Decode: column n is head head0_row + n (heads n >= hpc are zero).
+__device__ __forceinline__ int load_q_frag_fp8(uint32_t (&bq)[8][2], const void *q, size_t head0_row, int hpc,
+                                               int lane) {
+    const int n = lane >> 2;
+    return load_q_frag_fp8_row(bq, q, head0_row + n, n < hpc, lane);
+}
+
 // One FP8 block.  kb / vb: the stage's K and V code tiles (16 rows x 128 B,
 // 128-byte swizzled); sc: its scales (16 K scales, then 16 V scales).  Keys
 // outside [lo, valid) are masked by index; their V codes and scales are never
@@ -355,8 +361,14 @@ __device__ __forceinline__ int load_q_frag_fp8(uint32_t (&bq)[8][2], const void 
 // P'' <= 2^10 and every weight that matters is a normal fp16 number; O is held
 // times 2^vexp (rescaled with the softmax correction when vexp drops) and
 // brought back by fp8_finish().  P'' goes in as an fp16 head + remainder.
+// Multi-token verify (BOUNDS): column 2*q4 (2*q4 + 1) of this lane only sees keys
+// low0 <= k < lim0 (low1 <= k < lim1) of the block; those keys hold valid data,
+// so only their weight is zeroed.
+template <bool BOUNDS = false>
 __device__ __forceinline__ void decode_block_fp8(DecodeAcc &acc, const uint32_t (&bq)[8][2], uint32_t kb,
-                                                 uint32_t vb, uint32_t sc, int lo, int valid, float fsl2, int lane) {
+                                                 uint32_t vb, uint32_t sc, int lo, int valid, float fsl2, int lane,
+                                                 int lim0 = kBlockSize, int lim1 = kBlockSize, int low0 = 0,
+                                                 int low1 = 0) {
     const int n = lane >> 2, q4 = lane & 3;
     const int key_a = n, key_b = n + 8;
     const bool in_a = key_a >= lo && key_a < valid, in_b = key_b >= lo && key_b < valid;
@@ -387,10 +399,17 @@ __device__ __forceinline__ void decode_block_fp8(DecodeAcc &acc, const uint32_t 
 
     // Scores with each key's K scale; online softmax in the log2 domain.
     const float fa = lds_f32(sc + 4 * key_a) * fsl2, fb = lds_f32(sc + 4 * key_b) * fsl2;
-    const float s00 = in_a ? c[0] * fa : -INFINITY;
-    const float s01 = in_a ? c[1] * fa : -INFINITY;
-    const float s10 = in_b ? c[2] * fb : -INFINITY;
-    const float s11 = in_b ? c[3] * fb : -INFINITY;
+    bool v00 = in_a, v01 = in_a, v10 = in_b, v11 = in_b;
+    if constexpr (BOUNDS) {
+        v00 = v00 && key_a < lim0 && key_a >= low0;
+        v01 = v01 && key_a < lim1 && key_a >= low1;
+        v10 = v10 && key_b < lim0 && key_b >= low0;
+        v11 = v11 && key_b < lim1 && key_b >= low1;
+    }
+    const float s00 = v00 ? c[0] * fa : -INFINITY;
+    const float s01 = v01 ? c[1] * fa : -INFINITY;
+    const float s10 = v10 ? c[2] * fb : -INFINITY;
+    const float s11 = v11 ? c[3] * fb : -INFINITY;
     float bm0 = fmaxf(s00, s10), bm1 = fmaxf(s01, s11);
     const float sva = in_a ? lds_f32(sc + kScaleBytes + 4 * key_a) : 0.f;
     const float svb = in_b ? lds_f32(sc + kScaleBytes + 4 * key_b) : 0.f;

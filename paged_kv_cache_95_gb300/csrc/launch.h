@@ -85,6 +85,11 @@ struct DecodeParamsVerify : DecodeParams {
     int32_t q_per_seq;
 };
 
+// Multi-token verify over an FP8 cache (one 8-column MMA tile per CTA).
+struct DecodeParamsFp8Verify : DecodeParamsFp8 {
+    int32_t q_per_seq;
+};
+
 // Decode with the step's token appended in the same launch: new_k / new_v (bf16
 // [num_seqs][n_kv][128]) hold each sequence's new K/V row, which belongs at
 // position ctx - 1.  The CTAs that read the sequence's last block put the row
@@ -118,6 +123,8 @@ cudaError_t launch_paged_decode_fp8(const CUtensorMap &kmap, const CUtensorMap &
                                     cudaStream_t stream);
 cudaError_t launch_paged_verify(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParamsVerify &p,
                                 DecodeVariant v, cudaStream_t stream);
+cudaError_t launch_paged_verify_fp8(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParamsFp8Verify &p,
+                                    cudaStream_t stream);
 cudaError_t launch_paged_decode_append(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParamsAppend &p,
                                        DecodeVariant v, cudaStream_t stream);
 

@@ -93,6 +93,9 @@ def _declare(lib):
     lib.paged_attention_verify_window.argtypes = [P, i32, P, i32, P, P, P, P, i32, i32, i32, f32, i32, i32, D, P, sz,
                                                   P]
     lib.paged_attention_verify_window.restype = ctypes.c_int
+    lib.paged_attention_verify_fp8.argtypes = [P, i32, P, i32, P, P, P, P, P, P, i32, i32, i32, f32, i32, i32, D, P,
+                                               sz, P]
+    lib.paged_attention_verify_fp8.restype = ctypes.c_int
     lib.kv_reshape_and_cache_fp8.argtypes = [P, P, P, P, P, P, P, i32, D, P]
     lib.kv_reshape_and_cache_fp8.restype = ctypes.c_int
     lib.paged_attention_prefill_workspace_size.argtypes = [i32, i32, D]
@@ -447,14 +450,20 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
 
 
 def paged_attention_verify(out, q, q_per_seq: int, k_cache, v_cache, block_tables, context_lens, scale: float,
-                           workspace=None, partition_size: int = 0, stream=None, window: int = 0):
+                           workspace=None, partition_size: int = 0, stream=None, window: int = 0,
+                           k_scale=None, v_scale=None):
     """Verify k = q_per_seq draft positions per sequence: q / out [num_seqs * k, n_q, 128],
-    row i of sequence b at position ctx_b - k + i (causal).  ``window`` > 0 calls
-    paged_attention_verify_window (row at pos sees pos - window < j <= pos).
-    Returns the workspace."""
+    row i of sequence b at position ctx_b - k + i (causal).  ``window`` > 0: row at pos
+    sees pos - window < j <= pos.  An FP8 pool with ``k_scale`` / ``v_scale`` calls
+    paged_attention_verify_fp8.  Returns the workspace."""
     torch = _torch()
     desc = cache_desc(k_cache)
-    _check(v_cache, "v_cache", torch.bfloat16, ndim=4)
+    fp8 = desc.dtype == PKV_DTYPE_FP8_E4M3
+    if fp8:
+        _check_fp8_pool(k_cache, v_cache, k_scale, v_scale)
+    else:
+        _need(k_scale is None and v_scale is None, "scales are only for an FP8 cache")
+        _check(v_cache, "v_cache", torch.bfloat16, ndim=4)
     _need(tuple(v_cache.shape) == tuple(k_cache.shape), "v_cache shape must equal k_cache shape")
     _check(q, "q", torch.bfloat16, ndim=3, last=HEAD_DIM)
     rows, n_q, _ = q.shape
@@ -472,6 +481,14 @@ def paged_attention_verify(out, q, q_per_seq: int, k_cache, v_cache, block_table
         _need(nbytes > 0, "invalid sizes for paged_attention_verify")
         workspace = torch.zeros(nbytes, dtype=torch.uint8, device=q.device)
     _check(workspace, "workspace", torch.uint8, ndim=1)
+    if fp8:
+        rc = lib.paged_attention_verify_fp8(_ptr(out), _out_dtype(out), _ptr(q), int(q_per_seq), _ptr(k_cache),
+                                            _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_tables),
+                                            _ptr(context_lens), B, int(n_q), max_blocks, float(scale), int(window),
+                                            int(partition_size), ctypes.byref(desc), _ptr(workspace),
+                                            int(workspace.numel()), _stream(stream))
+        _raise("paged_attention_verify_fp8", rc)
+        return workspace
     if window:
         rc = lib.paged_attention_verify_window(_ptr(out), _out_dtype(out), _ptr(q), int(q_per_seq), _ptr(k_cache),
                                                _ptr(v_cache), _ptr(block_tables), _ptr(context_lens), B, int(n_q),

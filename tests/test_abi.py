@@ -270,3 +270,20 @@ def test_verify_window_argument_errors(lib):
     assert v(2, 64, nq=96) == P.PKV_ERR_UNSUPPORTED             # G = 12
     assert v(2, 64, wsb=100) == P.PKV_ERR_WORKSPACE_TOO_SMALL   # decode path
     assert v(16, 64, out=FAKE + 4) == P.PKV_ERR_INVALID_ARG     # prefill path: 16-B out
+
+
+def test_verify_fp8_argument_errors(lib):
+    c8 = desc(dtype=P.PKV_DTYPE_FP8_E4M3)
+
+    def v(k, c=c8, ks=FAKE, vs=FAKE, **kw):
+        a = dict(out=FAKE, q=FAKE, B=4, nq=32, wsb=1 << 20)
+        a.update(kw)
+        return lib.paged_attention_verify_fp8(a["out"], 1, a["q"], k, FAKE, FAKE, ks, vs, FAKE, FAKE, a["B"],
+                                              a["nq"], 8, 0.088, 0, 0, ctypes.byref(c), FAKE, a["wsb"], None)
+    assert v(2, ks=None) == P.PKV_ERR_INVALID_ARG                # scales are required
+    assert v(2, vs=FAKE + 4) == P.PKV_ERR_INVALID_ARG            # ... 16-byte aligned
+    assert v(2, c=desc()) == P.PKV_ERR_UNSUPPORTED               # a bf16 cache descriptor
+    assert v(0) == P.PKV_ERR_INVALID_ARG
+    assert v(2, wsb=100) == P.PKV_ERR_WORKSPACE_TOO_SMALL
+    ws = lambda k: lib.paged_attention_verify_workspace_size(64, k, 32, 256, 0, ctypes.byref(c8))  # noqa: E731
+    assert ws(16) > ws(8) > 256                                  # FP8 verify always runs on the decode kernel

@@ -147,3 +147,43 @@ def test_fp8_decode_window_and_bf16_out():
     o32, _ = d.decode(batch)
     want = o32.to(t.bfloat16).view(t.int16).cpu().numpy().astype(np.int32)
     assert np.max(np.abs(o16.view(t.int16).cpu().numpy().astype(np.int32) - want)) <= 1
+
+
+@pytest.mark.parametrize("n_q,n_kv,k", [(32, 8, 1), (32, 8, 2), (64, 8, 4), (32, 32, 16), (32, 1, 3)])
+def test_fp8_verify_parity(n_q, n_kv, k):
+    """Verify over the FP8 cache (paged_attention_verify_fp8): row i at pos = ctx - k + i
+    sees keys j <= pos (and pos - W < j under a window), one 8-column MMA tile per CTA,
+    so G * k = 8, 32, 96 columns take 1, 4, 12 CTAs per KV head; split partitions."""
+    t = torch()
+    ctx = [max(c, k) for c in (16, 17, 33, 100, 256, 257, 700, 1000)] + [k, k + 1]
+    wl, batch = W.make_custom(n_q, n_kv, ctx, q_lens=[k] * len(ctx), seed=560 + 3 * k + n_q // n_kv,
+                              materialize_logical=False)
+    d = Fp8Dev(wl)
+    d.append()
+    q = bf16_to_dev(batch.q)
+    for win in (0, 17, 300):
+        ref = d.oracle(batch, window=win)
+        for part in (0, 16):
+            out = t.full(q.shape, float("nan"), dtype=t.float32, device="cuda")
+            ws = P.paged_attention_verify(out, q, k, d.k_cache, d.v_cache, i32_to_dev(batch.block_tables),
+                                          i32_to_dev(batch.context_lens), wl.scale, partition_size=part,
+                                          window=win, k_scale=d.k_scale, v_scale=d.v_scale)
+            assert_close(out.cpu().numpy(), ref, what=f"G={n_q // n_kv} k={k} W={win} part={part}")
+            assert status_word(ws) == 0
+
+
+def test_fp8_verify_last_row_is_fp8_decode():
+    t = torch()
+    k = 4
+    wl, batch = W.make_custom(32, 8, [40, 300, 1024], q_lens=[k] * 3, seed=570, materialize_logical=False)
+    d = Fp8Dev(wl)
+    d.append()
+    q = bf16_to_dev(batch.q)
+    out = t.empty(q.shape, dtype=t.float32, device="cuda")
+    P.paged_attention_verify(out, q, k, d.k_cache, d.v_cache, i32_to_dev(batch.block_tables),
+                             i32_to_dev(batch.context_lens), wl.scale, k_scale=d.k_scale, v_scale=d.v_scale)
+    last = np.arange(1, 4) * k - 1
+    dec_batch = W.Batch(q=batch.q[last], cu_q_lens=np.arange(4, dtype=np.int32), block_tables=batch.block_tables,
+                        context_lens=batch.context_lens)
+    dec, _ = d.decode(dec_batch)
+    assert np.max(np.abs(out.cpu().numpy()[last] - dec.cpu().numpy())) <= 2e-5
