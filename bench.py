@@ -680,7 +680,8 @@ def run_reference(args):
         "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-        "config": _config(wl, sample.decode, kv, 2 * wl.k_cache.nbytes, 1),
+        "config": dict(_config(wl, sample.decode, kv, 2 * wl.k_cache.nbytes, 1),
+                       l2="fp64 oracle on the host cores (no GPU, no L2 flush)"),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": sdesc},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
