@@ -76,8 +76,11 @@ __global__ void __launch_bounds__(NW * 32)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int part = blockIdx.x;
-    const int hs = blockIdx.y;
+    // Verify with several CTAs per KV head: the split is the fastest grid index, so
+    // the CTAs that read the same K/V tiles run side by side and share them in L2.
+    const int part = VERIFY ? static_cast<int>(blockIdx.x) / p.head_splits : static_cast<int>(blockIdx.x);
+    const int hs = VERIFY ? static_cast<int>(blockIdx.y) * p.head_splits + static_cast<int>(blockIdx.x) % p.head_splits
+                          : static_cast<int>(blockIdx.y);
     const int b = blockIdx.z;
     const int g = hs / p.head_splits;
     static_assert(NCT == 1 || (NCT == 2 && VERIFY && !FP8), "two column tiles: verify only");
@@ -354,7 +357,7 @@ __global__ void __launch_bounds__(NW * 32)
     uint32_t *last_flag = reinterpret_cast<uint32_t *>(red_l + NW * kCols);
     __syncthreads();
     if (threadIdx.x == 0) {
-        const uint32_t prev = atom_add_acq_rel_gpu(p.counters + static_cast<size_t>(b) * gridDim.y + hs, 1u);
+        const uint32_t prev = atom_add_acq_rel_gpu(p.counters + static_cast<size_t>(b) * (VERIFY ? p.n_kv * p.head_splits : gridDim.y) + hs, 1u);
         *last_flag = prev == static_cast<uint32_t>(nparts - 1);
     }
     __syncthreads();
@@ -393,7 +396,8 @@ __global__ void __launch_bounds__(NW * 32)
         }
         store_out(p.out, p.out_bf16, col_row(hh) * kHeadDim + d, L > 0.f ? O / L : 0.f);
     }
-    if (threadIdx.x == 0) p.counters[static_cast<size_t>(b) * gridDim.y + hs] = 0u;  // ready for the next call
+    if (threadIdx.x == 0)  // ready for the next call
+        p.counters[static_cast<size_t>(b) * (VERIFY ? p.n_kv * p.head_splits : gridDim.y) + hs] = 0u;
 }
 
 }  // namespace
@@ -470,7 +474,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lse_merge_kernel(const Decod
 template <int NW, int ST, bool FP8 = false, bool VERIFY = false, int NCT = 1, bool APPEND = false>
 cudaError_t launch_variant(const CUtensorMap &kmap, const CUtensorMap &vmap,
                            const DecodeParamsT<FP8, VERIFY, APPEND> &p, cudaStream_t stream) {
-    const dim3 grid(p.max_parts, p.n_kv * p.head_splits, p.num_seqs);
+    const dim3 grid = VERIFY ? dim3(p.max_parts * p.head_splits, p.n_kv, p.num_seqs)
+                             : dim3(p.max_parts, p.n_kv * p.head_splits, p.num_seqs);
     cudaError_t e = launch_pdl(paged_decode_kernel<NW, ST, FP8, VERIFY, NCT, APPEND>, grid, dim3(NW * 32),
                                FP8 ? decode_fp8_smem_bytes() : decode_smem_bytes({NW, ST}), stream, kmap, vmap, p);
     if (e != cudaSuccess) return e;
