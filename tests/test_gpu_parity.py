@@ -316,3 +316,31 @@ def test_auto_partitions_follow_the_measured_rules(built_library):
         assert n8(8, 64, 2048) == 8     # B=8 x 32K: 4096-token partitions
         assert n8(1, 64, 8192) == 64    # B=1 x 128K: 2048-token partitions
     assert n8(32, 256, 128) == 1        # MHA-shaped 2048-token contexts filling the GPU: unsplit
+
+
+def test_decode_maximum_batch():
+    """The largest batch the boundary accepts: 65535 sequences (grid z at its limit),
+    contexts 1..39 tokens, one head; the decode and the one-launch decode with the
+    append both match the oracle, and the pool holds exactly the oracle's appends."""
+    t = torch()
+    rng = np.random.default_rng(3)
+    ctx = rng.integers(1, 40, size=65535).tolist()
+    wl, batch = W.make_custom(1, 1, ctx, seed=5, materialize_logical=False)
+    kc, vc = oracle_after_append(wl)
+    ref = oracle.paged_attention(batch.q, batch.cu_q_lens, kc, vc, batch.block_tables, batch.context_lens,
+                                 wl.scale, n_q=wl.n_q)
+    d = DevWorkload(wl)
+    d.append()
+    out, ws = d.decode(batch)
+    assert_close(out.cpu().numpy(), ref, what="B=65535 decode")
+    assert status_word(ws) == 0
+    # the same step in one launch, on a fresh pool
+    d2 = DevWorkload(wl)
+    q = bf16_to_dev(batch.q)
+    out2 = t.empty(q.shape, dtype=t.float32, device="cuda")
+    ws2 = P.paged_attention_decode_append(out2, q, bf16_to_dev(wl.new_key), bf16_to_dev(wl.new_value), d2.k_cache,
+                                          d2.v_cache, i32_to_dev(batch.block_tables),
+                                          i32_to_dev(batch.context_lens), wl.scale)
+    assert_close(out2.cpu().numpy(), ref, what="B=65535 decode with the append")
+    assert status_word(ws2) == 0
+    assert np.array_equal(dev_to_bf16_bits(d2.k_cache), kc) and np.array_equal(dev_to_bf16_bits(d2.v_cache), vc)
