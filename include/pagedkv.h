@@ -445,6 +445,28 @@ PKV_API int paged_attention_prefill_chunk_window(void *out, int32_t out_dtype, c
                                          void *stream);
 
 /*
+ * paged_attention_prefill_chunk_fp8 -- paged_attention_prefill_chunk over an FP8
+ * (E4M3) cache (cache->dtype PKV_DTYPE_FP8_E4M3; codes and per-slot scales as
+ * written by kv_reshape_and_cache_fp8; attention over code * scale as in
+ * paged_attention_decode_fp8), with an optional sliding window (window = 0:
+ * none; else as paged_attention_prefill_chunk_window).  The codes are fetched
+ * by TMA and expanded to bf16 in shared memory (exact: every E4M3 value is a
+ * bf16 value); the scales are applied in fp32, the K scale to the scores and
+ * the V scale to the probabilities before P V.  Workspace:
+ * paged_attention_prefill_workspace_size() with the FP8 cache descriptor.
+ *   k_scale, v_scale : float [num_blocks][num_kv_heads][16], device, 16-B aligned
+ * Errors: as paged_attention_prefill_chunk; PKV_ERR_INVALID_ARG for a missing or
+ * misaligned scale array or window < 0.
+ */
+PKV_API int paged_attention_prefill_chunk_fp8(void *out, int32_t out_dtype, const void *q, const int32_t *cu_q_lens,
+                                              int32_t max_q_len, int32_t total_q_rows, const void *k_cache,
+                                              const void *v_cache, const float *k_scale, const float *v_scale,
+                                              const int32_t *block_tables, const int32_t *context_lens,
+                                              int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq,
+                                              float scale, int32_t window, const pkv_cache_desc *cache,
+                                              void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * paged_attention_verify -- attention of k draft positions per sequence
  * (speculative decoding's verification step).
  *

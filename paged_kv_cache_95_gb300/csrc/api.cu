@@ -557,7 +557,7 @@ int paged_attention_decode_fp8(void *out, int32_t out_dtype, const void *q, cons
 }
 
 size_t paged_attention_prefill_workspace_size(int32_t num_seqs, int32_t num_q_heads, const pkv_cache_desc *cache) {
-    if (check_cache(cache) != PKV_OK || num_seqs < 1) return 0;
+    if ((check_cache(cache) != PKV_OK && check_cache_fp8(cache) != PKV_OK) || num_seqs < 1) return 0;
     if (check_group(num_q_heads, cache->num_kv_heads) != PKV_OK) return 0;
     return kStatusBytes;
 }
@@ -570,8 +570,12 @@ int prefill_impl(void *out, int32_t out_dtype, const void *q, const int32_t *cu_
                  int32_t max_q_len, int32_t total_q_rows, const void *k_cache, const void *v_cache,
                  const int32_t *block_tables, const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
                  int32_t max_blocks_per_seq, float scale, const pkv_cache_desc *cache, void *workspace,
-                 size_t workspace_bytes, void *stream, int32_t window = 0) {
-    if (int rc = check_cache(cache)) return rc;
+                 size_t workspace_bytes, void *stream, int32_t window = 0, const float *k_scale = nullptr,
+                 const float *v_scale = nullptr) {
+    // FP8 cache: E4M3 codes with per-slot scales, expanded to bf16 in shared memory.
+    const bool fp8 = k_scale != nullptr;
+    if (int rc = fp8 ? check_cache_fp8(cache) : check_cache(cache)) return rc;
+    if (fp8 && (!v_scale || !aligned(k_scale, 16) || !aligned(v_scale, 16))) return PKV_ERR_INVALID_ARG;
     if (num_q_heads < 1 || num_q_heads % cache->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
     if (window < 0) return PKV_ERR_INVALID_ARG;
     const int32_t G = num_q_heads / cache->num_kv_heads;
@@ -600,8 +604,10 @@ int prefill_impl(void *out, int32_t out_dtype, const void *q, const int32_t *cu_
     CUtensorMap qmap, kmap, vmap, omap;
     if (!encode_rows_map(&qmap, q, total_q_rows, num_q_heads, G, false) ||
         !encode_rows_map(&omap, out, total_q_rows, num_q_heads, G, out_dtype == PKV_DTYPE_FLOAT32) ||
-        !encode_pool_tile_map(&kmap, k_cache, cache->num_blocks, cache->num_kv_heads) ||
-        !encode_pool_tile_map(&vmap, v_cache, cache->num_blocks, cache->num_kv_heads))
+        !(fp8 ? encode_pool_map_fp8(&kmap, k_cache, cache->num_blocks, cache->num_kv_heads)
+              : encode_pool_tile_map(&kmap, k_cache, cache->num_blocks, cache->num_kv_heads)) ||
+        !(fp8 ? encode_pool_map_fp8(&vmap, v_cache, cache->num_blocks, cache->num_kv_heads)
+              : encode_pool_tile_map(&vmap, v_cache, cache->num_blocks, cache->num_kv_heads)))
         return PKV_ERR_CUDA;
     std::call_once(g_prefill_prepared[dev], [&] { g_prefill_prep_err[dev] = pkv::prefill_prepare_device(); });
     if (g_prefill_prep_err[dev] != cudaSuccess) return PKV_ERR_CUDA;
@@ -624,6 +630,8 @@ int prefill_impl(void *out, int32_t out_dtype, const void *q, const int32_t *cu_
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     p.out_bf16 = out_dtype == PKV_DTYPE_BF16;
     p.window = window;
+    p.k_scale = k_scale;
+    p.v_scale = fp8 ? v_scale : nullptr;
     if (pkv::launch_prefill_chunk(qmap, kmap, vmap, omap, p, max_q_len, static_cast<cudaStream_t>(stream)) !=
         cudaSuccess)
         return PKV_ERR_CUDA;
@@ -655,6 +663,19 @@ int paged_attention_prefill_chunk_window(void *out, int32_t out_dtype, const voi
     return prefill_impl(out, out_dtype, q, cu_q_lens, 0, max_q_len, total_q_rows, k_cache, v_cache, block_tables,
                         context_lens, num_seqs, num_q_heads, max_blocks_per_seq, scale, cache, workspace,
                         workspace_bytes, stream, window);
+}
+
+int paged_attention_prefill_chunk_fp8(void *out, int32_t out_dtype, const void *q, const int32_t *cu_q_lens,
+                                      int32_t max_q_len, int32_t total_q_rows, const void *k_cache,
+                                      const void *v_cache, const float *k_scale, const float *v_scale,
+                                      const int32_t *block_tables, const int32_t *context_lens, int32_t num_seqs,
+                                      int32_t num_q_heads, int32_t max_blocks_per_seq, float scale, int32_t window,
+                                      const pkv_cache_desc *cache, void *workspace, size_t workspace_bytes,
+                                      void *stream) {
+    if (!cu_q_lens || !k_scale || !v_scale || window < 0) return PKV_ERR_INVALID_ARG;
+    return prefill_impl(out, out_dtype, q, cu_q_lens, 0, max_q_len, total_q_rows, k_cache, v_cache, block_tables,
+                        context_lens, num_seqs, num_q_heads, max_blocks_per_seq, scale, cache, workspace,
+                        workspace_bytes, stream, window, k_scale, v_scale);
 }
 
 namespace {

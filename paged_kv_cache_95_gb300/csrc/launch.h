@@ -143,6 +143,8 @@ struct PrefillParams {
     int32_t out_bf16;
     int32_t uniform_q_len;       // rows per sequence when cu_q_lens is null
     int32_t window;              // sliding window W (> 0): a row at pos sees pos - W < j <= pos; 0: none
+    const float *k_scale;        // FP8 cache: per-slot scales [num_blocks][n_kv][16]; null for bf16
+    const float *v_scale;
 };
 
 size_t prefill_smem_bytes();

@@ -97,25 +97,68 @@ constexpr uint32_t kOffQ = 0;                              // Q tiles: [tile][di
 constexpr uint32_t kOffK = kOffQ + kRowTiles * kOpBytes;   // K ring: kStagesK x 32 KB
 constexpr uint32_t kOffV = kOffK + kStagesK * kOpBytes;    // V ring: kStagesV x 32 KB
 constexpr uint32_t kOffBar = kOffV + kStagesV * kOpBytes;
-// q_full, k_full/k_empty[kStagesK], v_full/v_empty[kStagesV], then per tile s_full, p_full, o_done
+// q_full, k_full/k_empty[kStagesK], v_full/v_empty[kStagesV], then per tile s_full, p_full, o_done,
+// then (FP8 cache) k_conv[kStagesK], v_conv[kStagesV]
 constexpr int kBarTile = 1 + 2 * kStagesK + 2 * kStagesV;
-constexpr uint32_t kNumBars = kBarTile + 3 * kRowTiles;
-constexpr uint32_t kOffTmem = kOffBar + 8 * 16;
+constexpr int kBarConv = kBarTile + 3 * kRowTiles;
+constexpr uint32_t kNumBars = kBarConv + kStagesK + kStagesV;
+constexpr uint32_t kOffTmem = kOffBar + 8 * 24;
 constexpr uint32_t kOffAbort = kOffTmem + 8;
 constexpr uint32_t kXchBytes = 2 * 4 * 128 * 4;  // per tile: row maxima [key tile & 1][column quarter][128]
 constexpr uint32_t kOffXch = kOffAbort + 8;
 // The dynamic shared memory is declared 1024-byte aligned (the swizzle period of
 // the TMA/UMMA operands); the kernel checks it and refuses to run otherwise.
-constexpr uint32_t kSmemBytes = kOffXch + kRowTiles * kXchBytes;
+// FP8 cache: the key tiles' per-slot scales, [K slot | V slot][8 blocks][16 slots] fp32.
+// K scales are read by tile 1's softmax after the K stage is released (its S is
+// done), so they live in a ring twice as deep as the K ring: key tile kt's K
+// scales in slot kt % kScaleSlotsK stay until key tile kt + 2 kStagesK loads,
+// which waits for S of key tile kt + kStagesK, i.e. for both tiles' softmax of
+// key tile kt.  V scales share the V stage's life (released after both P V).
+constexpr uint32_t kScaleStage = 8 * kBlockSize * 4;  // 512 B
+constexpr int kScaleSlotsK = 2 * kStagesK;
+constexpr uint32_t kOffScale = kOffXch + kRowTiles * kXchBytes;
+constexpr uint32_t kSmemBytes = kOffScale + (kScaleSlotsK + kStagesV) * kScaleStage;
+constexpr uint32_t kCodeOff = kOpBytes / 2;  // FP8 codes land in the upper half of a stage, then expand to bf16
+constexpr uint32_t kCodeTile = kBlockSize * kHeadDim;  // 2 KB: one (block, head) tile of E4M3 codes
 constexpr uint32_t kTmemCols = 512;  // S/P of tile t: [128t, 128t + 128); O of tile t: [256 + 128t, +128)
 constexpr uint32_t kTmemO = 256;
 static_assert(kSmemBytes <= 232448, "prefill shared memory exceeds the per-CTA limit");
-static_assert(kNumBars <= 16, "barrier area");
+static_assert(kNumBars <= 24, "barrier area");
+static_assert(kOffScale % 16 == 0, "bulk copies land on 16-byte boundaries");
 
 // Instruction descriptor, kind::f16: D f32, A/B bf16, M = 128, N = 128.
 constexpr uint32_t kIdescBase = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
 constexpr uint32_t kIdescQK = kIdescBase;               // A K-major, B K-major
 constexpr uint32_t kIdescPV = kIdescBase | (1u << 16);  // B MN-major
+
+// Two fp32 values from shared memory.
+__device__ __forceinline__ float2 lds_f32x2(uint32_t addr) {
+    float2 r;
+    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(r.x), "=f"(r.y) : "r"(addr));
+    return r;
+}
+
+// Sixteen E4M3 codes (dims d .. d + 15) to bf16 (exact: E4M3 values are bf16
+// values): w0 holds dims d .. d + 7, w1 dims d + 8 .. d + 15.
+__device__ __forceinline__ void e4m3x16_to_bf16(const uint4 &c, uint4 &w0, uint4 &w1) {
+    auto two = [](uint32_t f16x2) {
+        const float2 f = unpack_f16x2(f16x2);
+        return pack_bf16x2(f.x, f.y);
+    };
+    uint32_t a, b;
+    e4m3x4_to_f16x2x2(c.x, a, b);
+    w0.x = two(a);
+    w0.y = two(b);
+    e4m3x4_to_f16x2x2(c.y, a, b);
+    w0.z = two(a);
+    w0.w = two(b);
+    e4m3x4_to_f16x2x2(c.z, a, b);
+    w1.x = two(a);
+    w1.y = two(b);
+    e4m3x4_to_f16x2x2(c.w, a, b);
+    w1.z = two(a);
+    w1.w = two(b);
+}
 
 // Shared-memory matrix descriptor for a 128-byte-swizzled canonical layout.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
@@ -167,8 +210,13 @@ __device__ __forceinline__ void stage_row(uint32_t stage, int32_t bf16, int r, i
 // 608 threads, one CTA per SM (200 KB of shared memory); 19 warps put five on
 // some SM sub-partition, whose 16K registers then allow 96 a thread.
 // WINDOW: sliding-window instantiation (p.window > 0); the plain one compiles
-// without any of the window's bookkeeping.
-template <bool WINDOW>
+// without any of the window's bookkeeping.  FP8: the cache holds E4M3 codes with
+// per-slot scales (p.k_scale / p.v_scale): each block's 2 KB code tile lands in
+// the upper half of a ring stage and the softmax warps expand it in place to the
+// bf16 operand layout (E4M3 values are exact in bf16) between two key tiles'
+// softmax passes; the K scale multiplies the scores and the V scale the weights
+// that enter P V (the row sums keep the unscaled weights).
+template <bool WINDOW, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_chunk_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                          const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
@@ -254,6 +302,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto s_full = [&](int t) { return sbase + kOffBar + 8 * (kBarTile + t); };
     auto p_full = [&](int t) { return sbase + kOffBar + 8 * (kBarTile + kRowTiles + t); };
     auto o_done = [&](int t) { return sbase + kOffBar + 8 * (kBarTile + 2 * kRowTiles + t); };
+    auto k_conv = [&](int st) { return sbase + kOffBar + 8 * (kBarConv + st); };  // FP8: K stage in bf16
+    auto v_conv = [&](int st) { return sbase + kOffBar + 8 * (kBarConv + kStagesK + st); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffTmem);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + kOffAbort);
 
@@ -272,6 +322,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(p_full(t), kSoftmaxWarps);
             mbar_init(o_done(t), 1);
         }
+        for (int st = 0; st < kStagesK; ++st) mbar_init(k_conv(st), kSoftmaxWarps);
+        for (int st = 0; st < kStagesV; ++st) mbar_init(v_conv(st), kSoftmaxWarps);
         *abort_flag = 0u;
         fence_mbar_init();
     }
@@ -340,9 +392,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t bar = is_k ? k_full(st) : v_full(st);
             const uint32_t dst = ring + st * kOpBytes;
             const int nload = min(8, nblocks - (kt0 + kt) * 8);
-            if (lane == 0) mbar_arrive_expect_tx(bar, nload * kBlkBytes);
-            __syncwarp();
-            if (lane < nload) tma_load_5d(dst + lane * kBlkBytes, map, bar, 0, 0, 0, 0, mine);
+            if constexpr (FP8) {
+                // Block t's 2 KB code tile (one box: 128 codes x 16 slots, 128-byte swizzle) into the
+                // stage's upper half, and its 64 B of scales into the stage's scale row.
+                if (lane == 0) mbar_arrive_expect_tx(bar, nload * (kCodeTile + kBlockSize * 4));
+                __syncwarp();
+                if (lane < nload) {
+                    const int phys = mine / p.n_kv;
+                    tma_load_4d(dst + kCodeOff + lane * kCodeTile, map, bar, 0, 0, g, phys);
+                    const float *sc = is_k ? p.k_scale : p.v_scale;
+                    const int slot = is_k ? kt % kScaleSlotsK : kScaleSlotsK + st;
+                    bulk_copy_g2s(sbase + kOffScale + slot * kScaleStage + lane * 64,
+                                  sc + (static_cast<size_t>(phys) * p.n_kv + g) * kBlockSize, 64, bar);
+                }
+            } else {
+                if (lane == 0) mbar_arrive_expect_tx(bar, nload * kBlkBytes);
+                __syncwarp();
+                if (lane < nload) tma_load_5d(dst + lane * kBlkBytes, map, bar, 0, 0, 0, 0, mine);
+            }
         }
     } else if (warp == kMmaWarp) {
         // ---------------- MMA issuer: S0(k), P1(k-1) V(k-1), S1(k), P0(k) V(k) ----------------
@@ -377,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool k_ready = false;  // K(kt) waited for (just before the first S that reads it)
                 auto need_k = [&]() -> bool {
                     if (!k_ready) {
-                        if (!wait(k_full(st_k), (kt / kStagesK) & 1)) return false;
+                        if (!wait(FP8 ? k_conv(st_k) : k_full(st_k), (kt / kStagesK) & 1)) return false;
                         tc_fence_after();
                         k_ready = true;
                     }
@@ -389,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (kt >= 1 && kt - 1 < nt1) {  // tile 1's P V of the previous key tile
                     const int pk = kt - 1;
-                    if (!(ok = wait(p_full(1), pk & 1) && wait(v_full(pk % kStagesV), (pk / kStagesV) & 1))) break;
+                    if (!(ok = wait(p_full(1), pk & 1) && wait(FP8 ? v_conv(pk % kStagesV) : v_full(pk % kStagesV), (pk / kStagesV) & 1))) break;
                     tc_fence_after();
                     mma_pv(1, pk);
                     umma_commit(v_empty(pk % kStagesV));  // both tiles' P V of key tile pk are issued
@@ -400,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (kt < n_tiles) umma_commit(k_empty(st_k));  // both tiles' S of key tile kt are issued
                 if (kt < nt0) {
-                    if (!(ok = wait(p_full(0), kt & 1) && wait(v_full(st_v), (kt / kStagesV) & 1))) break;
+                    if (!(ok = wait(p_full(0), kt & 1) && wait(FP8 ? v_conv(st_v) : v_full(st_v), (kt / kStagesV) & 1))) break;
                     tc_fence_after();
                     mma_pv(0, kt);
                     if (kt >= nt1) umma_commit(v_empty(st_v));  // tile 1 does not read this key tile
@@ -438,6 +505,61 @@ __global__ void __launch_bounds__(kThreads, 1)
         // (`alive` false) the loops keep turning without work, so the named barriers
         // always match and never hang.
         bool alive = true;
+        // FP8: key tile kx's K (is_v false) or V codes, once landed, expanded in place to
+        // the bf16 operand layout by all 512 softmax threads (a CTA-uniform call): each
+        // thread takes two 16-code chunks of a slot row (chunk c: block c / 128, slot
+        // (c / 8) % 16, dims 16 (c % 8) ..), reads them, and after a barrier over all
+        // softmax warps (so every code is read before any bf16 overwrites it) writes
+        // them as two swizzled 16-byte bf16 chunks.  V rows no row may see (past the
+        // context, of an invalid block or of a block before the window) become zeros.
+        auto expand = [&](bool is_v, int kx) {
+            const int stages = is_v ? kStagesV : kStagesK;
+            const int st = kx % stages;
+            const uint32_t stage = sbase + (is_v ? kOffV : kOffK) + st * kOpBytes;
+            const bool ok = alive && warp_wait(is_v ? v_full(st) : k_full(st), (kx / stages) & 1);
+            uint32_t zmask = 0;
+            int rvx = 128;
+            if (is_v) {
+                const int jb = (kt0 + kx) * 8 + lane;
+                const bool bad_lane = lane < 8 && (!WINDOW || jb >= fb) && jb < nblocks &&
+                                      static_cast<unsigned>(__ldg(table + jb)) >= static_cast<unsigned>(p.num_blocks);
+                zmask = __ballot_sync(0xffffffffu, bad_lane);
+                if constexpr (WINDOW) zmask |= (1u << min(8, max(0, fb - (kt0 + kx) * 8))) - 1u;
+                rvx = ctx - (kt0 + kx) * 128;
+            }
+            uint4 cd[2];
+            bool zero[2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int cc = tid + i * kSoftmaxWarps * 32;
+                const int blk = cc >> 7, sl = (cc >> 3) & 15, ch = cc & 7;
+                zero[i] = is_v && (blk * 16 + sl >= rvx || ((zmask >> blk) & 1u));
+                cd[i] = make_uint4(0u, 0u, 0u, 0u);
+                if (ok && !zero[i]) cd[i] = lds128(stage + kCodeOff + blk * kCodeTile + sl * 128 + ((ch ^ (sl & 7)) << 4));
+            }
+            asm volatile("bar.sync 10, %0;" ::"r"(kSoftmaxWarps * 32) : "memory");
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int cc = tid + i * kSoftmaxWarps * 32;
+                const int blk = cc >> 7, sl = (cc >> 3) & 15, ch = cc & 7;
+                uint4 w0 = make_uint4(0u, 0u, 0u, 0u), w1 = w0;
+                if (!zero[i]) e4m3x16_to_bf16(cd[i], w0, w1);
+                const int s8 = sl & 7, j0 = 2 * (ch & 3);
+                const uint32_t row = stage + blk * kBlkBytes + (sl >> 3) * 2048 + (ch >> 2) * 1024 + s8 * 128;
+                if (ok) {
+                    sts128(row + ((j0 ^ s8) << 4), w0);
+                    sts128(row + (((j0 + 1) ^ s8) << 4), w1);
+                }
+            }
+            fence_proxy_async_smem();  // generic stores -> the tensor core (async proxy)
+            __syncwarp();
+            if (ok && lane == 0) mbar_arrive(is_v ? v_conv(st) : k_conv(st));
+            alive = ok;
+        };
+        if constexpr (FP8) {
+            expand(false, 0);
+            expand(true, 0);
+        }
         for (int kt = 0; kt < n_tiles; ++kt) {
             // Which of this key tile's blocks have an invalid id (flagged) or lie wholly
             // before the window (never read): their keys are masked.  Lane j < 8
@@ -454,6 +576,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 #pragma unroll
             for (int t = 0; t < kRowTiles; ++t) {
+                // FP8: the next key tile's K right after tile 0's pass (S0(kt+1) waits for it).
+                if constexpr (FP8) {
+                    if (t == 1 && kt + 1 < n_tiles) expand(false, kt + 1);
+                }
                 if (kt >= (t == 0 ? nt0 : nt1)) continue;  // (CTA-uniform)
                 alive = alive && warp_wait(s_full(t), kt & 1);
                 if (!alive) {
@@ -470,12 +596,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld_32x32b_x32(t_s, v);
                 tmem_wait_ld();
                 tmem_hold(v);
+                uint32_t vm = 0xffffffffu;  // FP8: keys whose weight may enter P V
+                if constexpr (FP8) {        // scores times each key's K scale
+                    const uint32_t ks = sbase + kOffScale + (kt % kScaleSlotsK) * kScaleStage + 128 * cq;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const uint4 w = lds128(ks + 16 * i);
+                        v[4 * i] = __float_as_uint(__uint_as_float(v[4 * i]) * __uint_as_float(w.x));
+                        v[4 * i + 1] = __float_as_uint(__uint_as_float(v[4 * i + 1]) * __uint_as_float(w.y));
+                        v[4 * i + 2] = __float_as_uint(__uint_as_float(v[4 * i + 2]) * __uint_as_float(w.z));
+                        v[4 * i + 3] = __float_as_uint(__uint_as_float(v[4 * i + 3]) * __uint_as_float(w.w));
+                    }
+                }
                 if (!(kc + 31 <= limit[t] && (!WINDOW || kc >= first[t]) && !((bad >> (2 * cq)) & 3u))) {
 #pragma unroll
                     for (int k = 0; k < 32; ++k) {
                         const bool ok = kc + k <= limit[t] && (!WINDOW || kc + k >= first[t]) &&
                                         !((bad >> ((32 * cq + k) >> 4)) & 1u);
-                        if (!ok) v[k] = __float_as_uint(-INFINITY);
+                        if (!ok) {
+                            v[k] = __float_as_uint(-INFINITY);
+                            if constexpr (FP8) vm &= ~(1u << k);
+                        }
                     }
                 }
                 float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -519,12 +660,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                         rs1 = fadd2(rs1, pr);
                     else
                         rs0 = fadd2(rs0, pr);
+                    // FP8: the weights entering P V carry each key's V scale (masked keys: 0,
+                    // whatever their stale scale holds); the row sums keep the plain weights.
+                    float2 pw = pr;
+                    if constexpr (FP8) {
+                        const float2 sv =
+                            lds_f32x2(sbase + kOffScale + (kScaleSlotsK + kt % kStagesV) * kScaleStage + 128 * cq + 8 * e);
+                        pw.x = ((vm >> (2 * e)) & 1u) ? pr.x * sv.x : 0.f;
+                        pw.y = ((vm >> (2 * e + 1)) & 1u) ? pr.y * sv.y : 0.f;
+                    }
                     // head: the upper 16 bits of each (bf16 truncation, exact in fp32);
                     // remainder: P - head >= 0 (exact in fp32), rounded to nearest bf16.
-                    const uint32_t ua = __float_as_uint(pr.x), ub = __float_as_uint(pr.y);
+                    const uint32_t ua = __float_as_uint(pw.x), ub = __float_as_uint(pw.y);
                     hi[e] = __byte_perm(ua, ub, 0x7632);
                     const float2 rr =
-                        fsub2(pr, make_float2(__uint_as_float(ua & 0xffff0000u), __uint_as_float(ub & 0xffff0000u)));
+                        fsub2(pw, make_float2(__uint_as_float(ua & 0xffff0000u), __uint_as_float(ub & 0xffff0000u)));
                     lo[e] = pack_bf16x2(rr.x, rr.y);
                 }
                 tmem_st_32x32b_x16(t_s, hi);
@@ -536,7 +686,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Zero V rows of keys no row may see (past the context, of a bad block or
                 // of a block before the window), once per key tile, by the first tile that
                 // reads it, before its P V.
-                if ((rv < 128 || bad) && t == (kt < nt0 ? 0 : 1)) {
+                if (!FP8 && (rv < 128 || bad) && t == (kt < nt0 ? 0 : 1)) {  // (FP8: done by expand)
                     alive = warp_wait(v_full(kt % kStagesV), (kt / kStagesV) & 1);
                     if (!alive) continue;
                     const uint32_t vb = sbase + kOffV + (kt % kStagesV) * kOpBytes;
@@ -554,6 +704,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(p_full(t));
+            }
+            // FP8: the next key tile's V (P0(kt+1) V waits for it).
+            if constexpr (FP8) {
+                if (kt + 1 < n_tiles) expand(true, kt + 1);
             }
         }
 
@@ -630,11 +784,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 size_t prefill_smem_bytes() { return kSmemBytes; }
 
 cudaError_t prefill_prepare_device() {
-    const cudaError_t e = cudaFuncSetAttribute(prefill_chunk_kernel<false>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(prefill_chunk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(kSmemBytes));
+    const int smem = static_cast<int>(kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(prefill_chunk_kernel<false, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(prefill_chunk_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(prefill_chunk_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(prefill_chunk_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    return e;
 }
 
 cudaError_t launch_prefill_chunk(const CUtensorMap &qmap, const CUtensorMap &kmap, const CUtensorMap &vmap,
@@ -642,10 +801,10 @@ cudaError_t launch_prefill_chunk(const CUtensorMap &qmap, const CUtensorMap &kma
     // One CTA per pair of row tiles.
     const int tiles = (max_q_len + p.rows_per_tile - 1) / p.rows_per_tile;
     const dim3 grid(p.n_kv, p.num_seqs, (tiles + 1) / 2);
-    return p.window > 0 ? launch_pdl(prefill_chunk_kernel<true>, grid, dim3(kThreads), kSmemBytes, stream, qmap, kmap,
-                                     vmap, omap, p)
-                        : launch_pdl(prefill_chunk_kernel<false>, grid, dim3(kThreads), kSmemBytes, stream, qmap, kmap,
-                                     vmap, omap, p);
+    const bool fp8 = p.k_scale != nullptr;
+    auto kernel = p.window > 0 ? (fp8 ? prefill_chunk_kernel<true, true> : prefill_chunk_kernel<true, false>)
+                               : (fp8 ? prefill_chunk_kernel<false, true> : prefill_chunk_kernel<false, false>);
+    return launch_pdl(kernel, grid, dim3(kThreads), kSmemBytes, stream, qmap, kmap, vmap, omap, p);
 }
 
 }  // namespace pkv

@@ -105,6 +105,9 @@ def _declare(lib):
     lib.paged_attention_prefill_chunk_window.argtypes = [P, i32, P, P, i32, i32, P, P, P, P, i32, i32, i32, f32, i32,
                                                          D, P, sz, P]
     lib.paged_attention_prefill_chunk_window.restype = ctypes.c_int
+    lib.paged_attention_prefill_chunk_fp8.argtypes = [P, i32, P, P, i32, i32, P, P, P, P, P, P, i32, i32, i32, f32,
+                                                      i32, D, P, sz, P]
+    lib.paged_attention_prefill_chunk_fp8.restype = ctypes.c_int
     lib.paged_attention_decode_static_scratch.argtypes = [P, i32, P, P, P, P, P, i32, i32, i32, f32, i32, D, P, P]
     lib.paged_attention_decode_static_scratch.restype = ctypes.c_int
     lib.kv_copy_blocks.argtypes = [P, P, P, P, P, i32, D, P]
@@ -510,14 +513,20 @@ def paged_attention_prefill_workspace_size(num_seqs: int, num_q_heads: int, cach
 
 
 def paged_attention_prefill_chunk(out, q, cu_q_lens, max_q_len: int, k_cache, v_cache, block_tables, context_lens,
-                                  scale: float, workspace=None, stream=None, window: int = 0):
+                                  scale: float, workspace=None, stream=None, window: int = 0, k_scale=None,
+                                  v_scale=None):
     """Causal chunked-prefill attention; ``workspace`` is allocated if None.
     ``window`` > 0 calls paged_attention_prefill_chunk_window (row at pos sees
-    keys pos - window < j <= pos)."""
+    keys pos - window < j <= pos); an FP8 cache with ``k_scale`` / ``v_scale``
+    calls paged_attention_prefill_chunk_fp8."""
     torch = _torch()
-    desc = cache_desc(k_cache)
-    _check(v_cache, "v_cache", torch.bfloat16, ndim=4)
-    _need(tuple(v_cache.shape) == tuple(k_cache.shape), "v_cache shape must equal k_cache shape")
+    fp8 = k_scale is not None or v_scale is not None
+    if fp8:
+        desc = _check_fp8_pool(k_cache, v_cache, k_scale, v_scale)
+    else:
+        desc = cache_desc(k_cache)
+        _check(v_cache, "v_cache", torch.bfloat16, ndim=4)
+        _need(tuple(v_cache.shape) == tuple(k_cache.shape), "v_cache shape must equal k_cache shape")
     _check(q, "q", torch.bfloat16, ndim=3, last=HEAD_DIM)
     rows, n_q, _ = q.shape
     _check(out, "out", out.dtype, ndim=3)
@@ -533,6 +542,14 @@ def paged_attention_prefill_chunk(out, q, cu_q_lens, max_q_len: int, k_cache, v_
         workspace = torch.zeros(nbytes, dtype=torch.uint8, device=q.device)  # status word starts clear
     _check(workspace, "workspace", torch.uint8, ndim=1)
     lib = load_library()
+    if fp8:
+        rc = lib.paged_attention_prefill_chunk_fp8(
+            _ptr(out), _out_dtype(out), _ptr(q), _ptr(cu_q_lens), int(max_q_len), int(rows), _ptr(k_cache),
+            _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), _ptr(context_lens), B, int(n_q),
+            int(block_tables.shape[1]), float(scale), int(window), ctypes.byref(desc), _ptr(workspace),
+            int(workspace.numel()), _stream(stream))
+        _raise("paged_attention_prefill_chunk_fp8", rc)
+        return workspace
     if window:
         rc = lib.paged_attention_prefill_chunk_window(
             _ptr(out), _out_dtype(out), _ptr(q), _ptr(cu_q_lens), int(max_q_len), int(rows), _ptr(k_cache),

@@ -287,3 +287,19 @@ def test_verify_fp8_argument_errors(lib):
     assert v(2, wsb=100) == P.PKV_ERR_WORKSPACE_TOO_SMALL
     ws = lambda k: lib.paged_attention_verify_workspace_size(64, k, 32, 256, 0, ctypes.byref(c8))  # noqa: E731
     assert ws(16) > ws(8) > 256                                  # FP8 verify always runs on the decode kernel
+
+
+def test_prefill_fp8_argument_errors(lib):
+    c8 = desc(dtype=P.PKV_DTYPE_FP8_E4M3)
+
+    def f(c=c8, ks=FAKE, vs=FAKE, window=0, cu=FAKE, wsb=1 << 20):
+        return lib.paged_attention_prefill_chunk_fp8(FAKE, 1, FAKE, cu, 64, 256, FAKE, FAKE, ks, vs, FAKE, FAKE, 4,
+                                                     32, 8, 0.088, window, ctypes.byref(c), FAKE, wsb, None)
+    assert f(ks=None) == P.PKV_ERR_INVALID_ARG                   # scales are required
+    assert f(vs=None) == P.PKV_ERR_INVALID_ARG
+    assert f(ks=FAKE + 4) == P.PKV_ERR_INVALID_ARG               # ... 16-byte aligned
+    assert f(cu=None) == P.PKV_ERR_INVALID_ARG
+    assert f(window=-1) == P.PKV_ERR_INVALID_ARG
+    assert f(c=desc()) == P.PKV_ERR_UNSUPPORTED                  # a bf16 cache descriptor
+    assert f(wsb=2) == P.PKV_ERR_WORKSPACE_TOO_SMALL
+    assert lib.paged_attention_prefill_workspace_size(4, 32, ctypes.byref(c8)) > 0

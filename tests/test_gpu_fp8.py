@@ -61,6 +61,17 @@ class Fp8Dev:
                                       partition_size=partition_size, k_scale=self.k_scale, v_scale=self.v_scale)
         return out, ws
 
+    def prefill(self, batch, window=0, out_dtype=None, tables=None):
+        t = torch()
+        q = bf16_to_dev(batch.q)
+        out = t.full(q.shape, float("nan"), dtype=out_dtype or t.float32, device="cuda")  # every row is written
+        ws = P.paged_attention_prefill_chunk(out, q, i32_to_dev(batch.cu_q_lens), int(batch.q_lens.max()),
+                                             self.k_cache, self.v_cache,
+                                             i32_to_dev(batch.block_tables if tables is None else tables),
+                                             i32_to_dev(batch.context_lens), self.wl.scale, window=window,
+                                             k_scale=self.k_scale, v_scale=self.v_scale)
+        return out, ws
+
     def oracle(self, batch, window=0):
         kc, vc, ks, vs = self.after
         return oracle.paged_attention(batch.q, batch.cu_q_lens, kc, vc, batch.block_tables, batch.context_lens,
@@ -187,3 +198,60 @@ def test_fp8_verify_last_row_is_fp8_decode():
                         context_lens=batch.context_lens)
     dec, _ = d.decode(dec_batch)
     assert np.max(np.abs(out.cpu().numpy()[last] - dec.cpu().numpy())) <= 2e-5
+
+
+@pytest.mark.parametrize("n_q,n_kv", [(32, 32), (32, 8), (64, 8), (32, 2), (32, 16)])
+def test_fp8_prefill_parity(n_q, n_kv):
+    """Causal chunks over an FP8 cache on the tensor-core prefill: chunk lengths from
+    one row to several row tiles, contexts spanning several key tiles with ragged
+    tails, with and without a sliding window."""
+    ctx = [1, 7, 40, 33, 300, 128, 600, 1100]
+    q_lens = [1, 7, 32, 33, 100, 128, 129, 300]
+    wl, batch = W.make_custom(n_q, n_kv, ctx, q_lens=q_lens, seed=420 + n_q + n_kv, materialize_logical=False)
+    d = Fp8Dev(wl)
+    d.append()
+    for win in (0, 17, 300):
+        ref = d.oracle(batch, window=win)
+        out, ws = d.prefill(batch, window=win)
+        assert_close(out.cpu().numpy(), ref, what=f"fp8 prefill G={n_q // n_kv} W={win}")
+        assert status_word(ws) == 0
+
+
+def test_fp8_prefill_mixed_chunks_stale_entries_and_bf16_out():
+    """The mixed workload's 512-row chunks over 1024 cached tokens on an FP8 pool:
+    plain, and under a 300-token window with invalid ids in the table entries wholly
+    before every row's window (never read, no flag); bf16 output too."""
+    t = torch()
+    wl = W.make_workload("mixed", materialize_logical=False)
+    d = Fp8Dev(wl)
+    d.append()
+    ch = wl.chunk
+    ref = d.oracle(ch)
+    out, ws = d.prefill(ch)
+    assert_close(out.cpu().numpy(), ref, what="fp8 mixed chunks")
+    assert status_word(ws) == 0
+    out16, _ = d.prefill(ch, out_dtype=t.bfloat16)
+    assert_close(out16.float().cpu().numpy(), ref, abs_tol=2e-2, rel_tol=2e-2, what="fp8 mixed chunks, bf16 out")
+    win = 300
+    tables = ch.block_tables.copy()
+    for b in range(ch.num_seqs):
+        c = int(ch.context_lens[b]) - int(ch.q_lens[b])
+        tables[b, :max(0, c + 1 - win) // 16] = wl.k_cache.shape[0] + 11
+    out, ws = d.prefill(ch, window=win, tables=tables)
+    assert_close(out.cpu().numpy(), d.oracle(ch, window=win), what="fp8 mixed chunks, W=300")
+    assert status_word(ws) == 0
+
+
+def test_fp8_prefill_invalid_block_is_masked_and_flagged():
+    """An out-of-range block id inside the context: its keys are left out (the oracle
+    given the same table skips them too) and the bad-block status bit is set."""
+    wl, batch = W.make_custom(32, 8, [300, 600], q_lens=[100, 200], seed=431, materialize_logical=False)
+    d = Fp8Dev(wl)
+    d.append()
+    tables = batch.block_tables.copy()
+    tables[1, 3] = wl.k_cache.shape[0] + 5
+    out, ws = d.prefill(batch, tables=tables)
+    assert status_word(ws) & P.PKV_STATUS_BAD_BLOCK_ID
+    ok = out[:100].cpu().numpy()  # sequence 0 does not touch the bad entry
+    assert_close(ok, d.oracle(batch)[:100], what="fp8 prefill, sequence beside a bad block")
+    assert np.all(np.isfinite(out.cpu().numpy()))
