@@ -511,7 +511,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // (c / 8) % 16, dims 16 (c % 8) ..), reads them, and after a barrier over all
         // softmax warps (so every code is read before any bf16 overwrites it) writes
         // them as two swizzled 16-byte bf16 chunks.  V rows no row may see (past the
-        // context, of an invalid block or of a block before the window) become zeros.
+        // context, of an invalid block or of a block before the window) become zeros,
+        // and so do their V scales (before the barrier, so every later reader sees
+        // it): a masked key then enters P V with weight p * 0 = 0 whatever stale or
+        // uninitialised scale its slot held.
         auto expand = [&](bool is_v, int kx) {
             const int stages = is_v ? kStagesV : kStagesK;
             const int st = kx % stages;
@@ -536,6 +539,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 zero[i] = is_v && (blk * 16 + sl >= rvx || ((zmask >> blk) & 1u));
                 cd[i] = make_uint4(0u, 0u, 0u, 0u);
                 if (ok && !zero[i]) cd[i] = lds128(stage + kCodeOff + blk * kCodeTile + sl * 128 + ((ch ^ (sl & 7)) << 4));
+                if (ok && zero[i] && ch == 0)
+                    asm volatile("st.shared.f32 [%0], %1;" ::"r"(sbase + kOffScale + (kScaleSlotsK + st) * kScaleStage +
+                                                                  (blk * kBlockSize + sl) * 4),
+                                 "f"(0.f)
+                                 : "memory");
             }
             asm volatile("bar.sync 10, %0;" ::"r"(kSoftmaxWarps * 32) : "memory");
 #pragma unroll
@@ -596,16 +604,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld_32x32b_x32(t_s, v);
                 tmem_wait_ld();
                 tmem_hold(v);
-                uint32_t vm = 0xffffffffu;  // FP8: keys whose weight may enter P V
                 if constexpr (FP8) {        // scores times each key's K scale
                     const uint32_t ks = sbase + kOffScale + (kt % kScaleSlotsK) * kScaleStage + 128 * cq;
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const uint4 w = lds128(ks + 16 * i);
-                        v[4 * i] = __float_as_uint(__uint_as_float(v[4 * i]) * __uint_as_float(w.x));
-                        v[4 * i + 1] = __float_as_uint(__uint_as_float(v[4 * i + 1]) * __uint_as_float(w.y));
-                        v[4 * i + 2] = __float_as_uint(__uint_as_float(v[4 * i + 2]) * __uint_as_float(w.z));
-                        v[4 * i + 3] = __float_as_uint(__uint_as_float(v[4 * i + 3]) * __uint_as_float(w.w));
+                        const float2 a = fmul2(make_float2(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1])),
+                                               make_float2(__uint_as_float(w.x), __uint_as_float(w.y)));
+                        const float2 c = fmul2(make_float2(__uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])),
+                                               make_float2(__uint_as_float(w.z), __uint_as_float(w.w)));
+                        v[4 * i] = __float_as_uint(a.x);
+                        v[4 * i + 1] = __float_as_uint(a.y);
+                        v[4 * i + 2] = __float_as_uint(c.x);
+                        v[4 * i + 3] = __float_as_uint(c.y);
                     }
                 }
                 if (!(kc + 31 <= limit[t] && (!WINDOW || kc >= first[t]) && !((bad >> (2 * cq)) & 3u))) {
@@ -613,10 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int k = 0; k < 32; ++k) {
                         const bool ok = kc + k <= limit[t] && (!WINDOW || kc + k >= first[t]) &&
                                         !((bad >> ((32 * cq + k) >> 4)) & 1u);
-                        if (!ok) {
-                            v[k] = __float_as_uint(-INFINITY);
-                            if constexpr (FP8) vm &= ~(1u << k);
-                        }
+                        if (!ok) v[k] = __float_as_uint(-INFINITY);
                     }
                 }
                 float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -660,14 +668,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         rs1 = fadd2(rs1, pr);
                     else
                         rs0 = fadd2(rs0, pr);
-                    // FP8: the weights entering P V carry each key's V scale (masked keys: 0,
-                    // whatever their stale scale holds); the row sums keep the plain weights.
+                    // FP8: the weights entering P V carry each key's V scale (a masked key's
+                    // scale was zeroed by the expansion); the row sums keep the plain weights.
                     float2 pw = pr;
                     if constexpr (FP8) {
                         const float2 sv =
                             lds_f32x2(sbase + kOffScale + (kScaleSlotsK + kt % kStagesV) * kScaleStage + 128 * cq + 8 * e);
-                        pw.x = ((vm >> (2 * e)) & 1u) ? pr.x * sv.x : 0.f;
-                        pw.y = ((vm >> (2 * e + 1)) & 1u) ? pr.y * sv.y : 0.f;
+                        pw = fmul2(pr, sv);
                     }
                     // head: the upper 16 bits of each (bf16 truncation, exact in fp32);
                     // remainder: P - head >= 0 (exact in fp32), rounded to nearest bf16.
