@@ -414,8 +414,19 @@ def run_ours(args):
     launches_per_step = (1 if fused else 2) + (1 if chunk is not None else 0) + (1 if nparts > 1 else 0)
 
     # the next hot-path rows on the same batch (single-GPU runs; outside the timed region)
+    fp8_chunk = None
+    if chunk is not None:
+        def fp8_chunk(k8, v8, ks, vs):
+            """The causal chunks over the FP8 copy of the pool."""
+            ms = _time_events(torch, stream, lambda: P.paged_attention_prefill_chunk(
+                cout, cq, ccu, cmax, k8, v8, ctab, clen, wl.scale, workspace=cws, k_scale=ks, v_scale=vs),
+                min(args.steps, 200))
+            return {"avg_launch_ms": round(ms, 5), "tflops": round(chunk_flops / ms / 1e9, 2),
+                    "frac_of_bf16": round(chunk_flops / ms / 1e9 / _bf16_peak()[0], 4),
+                    "time_vs_bf16_cache": round(ms / prefill_ms, 3)}
     rows = _row_variants(P, torch, dev, wl, batch, k_cache, v_cache, new_k, new_v, slots, q, tables, lens,
-                         decode_ms, kv_bytes, steps=min(args.steps, 200), fused=fused) if world == 1 else None
+                         decode_ms, kv_bytes, steps=min(args.steps, 200), fused=fused,
+                         fp8_chunk=fp8_chunk) if world == 1 else None
 
     if rows is not None and chunk is not None:
         # the causal chunks under a 512-token window (each row sees its newest 512 keys)
@@ -492,8 +503,9 @@ def _time_events(torch, stream, fn, steps, warmup=3):
 
 
 def _row_variants(P, torch, dev, wl, batch, k_cache, v_cache, new_k, new_v, slots, q, tables, lens, decode_ms,
-                  kv_bytes, steps, fused=False):
-    """FP8 cache, sliding window and host block manager on the bench batch."""
+                  kv_bytes, steps, fused=False, fp8_chunk=None):
+    """FP8 cache, sliding window and host block manager on the bench batch
+    (``fp8_chunk``: times the workload's prefill chunks over the FP8 pool)."""
     peak, _ = measured_peaks()
     stream = torch.cuda.current_stream(dev)
     B = batch.num_seqs
@@ -524,6 +536,8 @@ def _row_variants(P, torch, dev, wl, batch, k_cache, v_cache, new_k, new_v, slot
         "avg_launch_ms": round(ms8, 5), "gbs": round(b8 / ms8 / 1e6, 2), "frac_of_hbm": round(b8 / ms8 / 1e6 / peak, 4),
         "sequences_per_s": round(B / ms8 * 1e3, 1), "speedup_vs_bf16_decode": round(decode_ms / ms8, 3),
         "append_avg_ms": round(ms8_app, 5)}
+    if fp8_chunk is not None:
+        res["fp8_prefill"] = fp8_chunk(k8, v8, ks, vs)
 
     # sliding window of 1024 tokens: only the visible keys' blocks are read
     win = 1024
