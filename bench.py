@@ -538,6 +538,17 @@ def _row_variants(P, torch, dev, wl, batch, k_cache, v_cache, new_k, new_v, slot
         "append_avg_ms": round(ms8_app, 5)}
     if fp8_chunk is not None:
         res["fp8_prefill"] = fp8_chunk(k8, v8, ks, vs)
+    # FP8 verify with k = 16 draft positions: G * 16 columns per KV head (the FP8 prefill
+    # kernel where it is faster than ceil(G * 16 / 8) decode CTAs per KV head)
+    k16 = 16
+    q16 = torch.randn((B * k16, wl.n_q, d), device=dev).to(torch.bfloat16)
+    out16 = torch.empty(q16.shape, dtype=torch.bfloat16, device=dev)
+    ws16 = P.paged_attention_verify(out16, q16, k16, k8, v8, tables, lens, wl.scale, k_scale=ks, v_scale=vs)
+    ms16 = _time_events(torch, stream, lambda: P.paged_attention_verify(
+        out16, q16, k16, k8, v8, tables, lens, wl.scale, workspace=ws16, k_scale=ks, v_scale=vs), steps)
+    res["fp8_verify_k16"] = {"q_per_seq": k16, "bytes_per_launch": b8, "avg_launch_ms": round(ms16, 5),
+                             "tokens_per_s": round(B * k16 / ms16 * 1e3, 1),
+                             "time_vs_one_fp8_decode": round(ms16 / ms8, 3)}
 
     # sliding window of 1024 tokens: only the visible keys' blocks are read
     win = 1024

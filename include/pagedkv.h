@@ -520,10 +520,14 @@ PKV_API int paged_attention_verify_window(void *out, int32_t out_dtype, const vo
  * (cache->dtype PKV_DTYPE_FP8_E4M3; codes and scales as written by
  * kv_reshape_and_cache_fp8, attention over code * scale as in
  * paged_attention_decode_fp8), with an optional sliding window (window = 0:
- * none).  Always on the decode kernel, one 8-column MMA tile per CTA: the
- * G * k (position, head) columns of a KV head are shared out over
- * ceil(G * k / 8) CTAs, each reading the K/V codes once.  Workspace:
- * paged_attention_verify_workspace_size() with the FP8 cache descriptor.
+ * none).  On the decode kernel, one 8-column MMA tile per CTA: the G * k
+ * (position, head) columns of a KV head are shared out over ceil(G * k / 8)
+ * CTAs, each reading the K/V codes once; or, where G * k >= 40 and
+ * G * k * min(num_seqs * num_kv_heads, SMs) >= 40 * SMs (G in {1,2,4,8,16}, q and
+ * out 16-B aligned), on the FP8 prefill kernel (paged_attention_prefill_chunk_fp8
+ * with k rows per sequence), which reads the codes once per KV head.  Workspace:
+ * paged_attention_verify_workspace_size() with the FP8 cache descriptor (sized
+ * for the decode route, enough for both).
  * Errors: as paged_attention_verify; PKV_ERR_INVALID_ARG for a missing or
  * misaligned scale array.
  */

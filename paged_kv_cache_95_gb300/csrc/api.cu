@@ -695,6 +695,26 @@ int32_t verify_splits(int32_t cols, bool fp8 = false) { return fp8 ? (cols + 7) 
 int32_t verify_cols_per_cta(int32_t cols, bool fp8 = false) {
     return (cols + verify_splits(cols, fp8) - 1) / verify_splits(cols, fp8);
 }
+
+// FP8 verify: the decode kernel reads a KV head's codes once per 8 columns, so its
+// time grows with ceil(G * k / 8); the prefill kernel reads them once per 256
+// rows but has no split-KV, so its time is set by how many SMs its
+// num_seqs x n_kv CTAs fill.  Measured on the 8B- and 70B-shaped batches, the
+// decode route costs about cols x min(units, SMs) / (8 x 4.6 x SMs) times the
+// prefill route (units = num_seqs x n_kv); the prefill route is taken from a
+// ratio of 40 / 37 up (and only where it can run: G packs its tiles, q and out
+// 16-byte aligned, the device known).
+constexpr int32_t kVerifyFp8PrefillCols = 40;
+bool verify_fp8_on_prefill(int32_t num_seqs, int32_t q_per_seq, int32_t G, int32_t n_kv, const void *q,
+                           const void *out) {
+    const int64_t cols = static_cast<int64_t>(G) * q_per_seq;
+    if (cols < kVerifyFp8PrefillCols || G > 16 || 128 % G != 0 || !aligned(q, 16) || !aligned(out, 16)) return false;
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return false;
+    const int64_t sms = sm_count(dev);
+    const int64_t units = std::min<int64_t>(static_cast<int64_t>(num_seqs) * n_kv, sms);
+    return cols * units >= kVerifyFp8PrefillCols * sms;
+}
 }  // namespace
 
 size_t paged_attention_verify_workspace_size(int32_t num_seqs, int32_t q_per_seq, int32_t num_q_heads,
@@ -718,8 +738,9 @@ size_t paged_attention_verify_workspace_size(int32_t num_seqs, int32_t q_per_seq
 namespace {
 
 // Shared by paged_attention_verify and paged_attention_verify_window (window 0: none).
-// k_scale / v_scale non-null: an FP8 cache (cache->dtype PKV_DTYPE_FP8_E4M3), always
-// on the decode kernel with one 8-column MMA tile per CTA.
+// k_scale / v_scale non-null: an FP8 cache (cache->dtype PKV_DTYPE_FP8_E4M3), on the
+// decode kernel with one 8-column MMA tile per CTA, or on the FP8 prefill kernel
+// where verify_fp8_on_prefill says it is faster.
 int verify_impl(void *out, int32_t out_dtype, const void *q, int32_t q_per_seq, const void *k_cache,
                 const void *v_cache, const int32_t *block_tables, const int32_t *context_lens, int32_t num_seqs,
                 int32_t num_q_heads, int32_t max_blocks_per_seq, float scale, int32_t partition_size, int32_t window,
@@ -732,12 +753,13 @@ int verify_impl(void *out, int32_t out_dtype, const void *q, int32_t q_per_seq, 
     if (int rc = check_group(num_q_heads, cache->num_kv_heads)) return rc;
     if (q_per_seq < 1 || q_per_seq > kMaxVerifyRows) return PKV_ERR_INVALID_ARG;
     const int32_t G = num_q_heads / cache->num_kv_heads;
-    if (!fp8 && !verify_on_decode(q_per_seq, G)) {
+    if (fp8 ? verify_fp8_on_prefill(num_seqs, q_per_seq, G, cache->num_kv_heads, q, out)
+            : !verify_on_decode(q_per_seq, G)) {
         // Prefill kernel, uniform rows: sequence b owns q rows b * q_per_seq .. + q_per_seq - 1.
         if (static_cast<int64_t>(num_seqs) * q_per_seq > INT32_MAX) return PKV_ERR_INVALID_ARG;
         return prefill_impl(out, out_dtype, q, nullptr, q_per_seq, q_per_seq, num_seqs * q_per_seq, k_cache, v_cache,
                             block_tables, context_lens, num_seqs, num_q_heads, max_blocks_per_seq, scale, cache,
-                            workspace, workspace_bytes, stream, window);
+                            workspace, workspace_bytes, stream, window, k_scale, v_scale);
     }
     if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PKV_ERR_INVALID_ARG;
     if (out_dtype != PKV_DTYPE_FLOAT32 && out_dtype != PKV_DTYPE_BF16) return PKV_ERR_UNSUPPORTED;

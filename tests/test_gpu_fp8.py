@@ -183,6 +183,33 @@ def test_fp8_verify_parity(n_q, n_kv, k):
             assert status_word(ws) == 0
 
 
+@pytest.mark.parametrize("n_q,n_kv,k,nseq", [(32, 8, 16, 16), (32, 2, 8, 24)])
+def test_fp8_verify_prefill_route(n_q, n_kv, k, nseq):
+    """FP8 verify with many columns (G * k = 64 over 128 KV-head units, 128 over 48)
+    runs on the FP8 prefill kernel on a 152-SM GPU: parity with the oracle, and the
+    result is bit-identical to paged_attention_prefill_chunk_fp8 with k rows per
+    sequence (the route's own kernel)."""
+    t = torch()
+    base = (16, 17, 33, 100, 256, 257, 700, 1000, 5, 129, 128, 300, 64, 999, 2000, 31)
+    ctx = [max(base[i % len(base)] + 7 * (i // len(base)), k) for i in range(nseq)]
+    wl, batch = W.make_custom(n_q, n_kv, ctx, q_lens=[k] * nseq, seed=580 + k + n_q // n_kv,
+                              materialize_logical=False)
+    d = Fp8Dev(wl)
+    d.append()
+    q = bf16_to_dev(batch.q)
+    for win in (0, 17, 300):
+        ref = d.oracle(batch, window=win)
+        out = t.full(q.shape, float("nan"), dtype=t.float32, device="cuda")
+        ws = P.paged_attention_verify(out, q, k, d.k_cache, d.v_cache, i32_to_dev(batch.block_tables),
+                                      i32_to_dev(batch.context_lens), wl.scale, window=win,
+                                      k_scale=d.k_scale, v_scale=d.v_scale)
+        assert_close(out.cpu().numpy(), ref, what=f"G={n_q // n_kv} k={k} W={win}")
+        assert status_word(ws) == 0
+        pf, _ = d.prefill(batch, window=win)
+        if t.cuda.get_device_properties(0).multi_processor_count == 152:
+            assert t.equal(out, pf), "FP8 verify did not take the prefill route"
+
+
 def test_fp8_verify_last_row_is_fp8_decode():
     t = torch()
     k = 4
