@@ -482,13 +482,18 @@ PKV_API int paged_attention_prefill_chunk_fp8(void *out, int32_t out_dtype, cons
  *   q, out    : [num_seqs * q_per_seq][num_q_heads][head_dim]; sequence b owns
  *               rows b * q_per_seq .. b * q_per_seq + q_per_seq - 1
  *   q_per_seq : k, 1 .. 16
- * Runs on the decode kernel when G * k <= 32, G > 16 or G does not divide 128: the
- * G heads x k positions of a KV head are the MMA columns of ceil(G * k / 16)
- * CTAs of up to 16 columns (one or two 8-column tiles), each reading the K/V
- * once; else on the tcgen05 prefill kernel (then q and out must be 16-B aligned).
+ * Runs on the decode kernel, where the G heads x k positions of a KV head are
+ * the MMA columns of ceil(G * k / 16) CTAs of up to 16 columns (one or two
+ * 8-column tiles), each reading the K/V once; or on the tcgen05 prefill kernel
+ * (then q and out must be 16-B aligned), which reads them once per KV head but
+ * has no split-KV, when G is in {1,2,4,8,16} and
+ * ceil(G * k / 16) * min(num_seqs * num_kv_heads, SMs) * 10 >= 21 * SMs
+ * (SMs: the current device's multiprocessors; 152 if none is found) -- the
+ * route measured faster.
  * num_seqs * k must not exceed 65535 (PKV_ERR_UNSUPPORTED).  A sequence with
  * ctx < k sets PKV_STATUS_BAD_Q_LEN and gets zero rows.
- * Workspace: paged_attention_verify_workspace_size() bytes, zero-filled once.
+ * Workspace: paged_attention_verify_workspace_size() bytes (sized for the route
+ * taken with the current device), zero-filled once.
  * Errors: as paged_attention_decode; PKV_ERR_INVALID_ARG for q_per_seq outside 1..16.
  */
 PKV_API size_t paged_attention_verify_workspace_size(int32_t num_seqs, int32_t q_per_seq, int32_t num_q_heads,
@@ -522,12 +527,11 @@ PKV_API int paged_attention_verify_window(void *out, int32_t out_dtype, const vo
  * paged_attention_decode_fp8), with an optional sliding window (window = 0:
  * none).  On the decode kernel, one 8-column MMA tile per CTA: the G * k
  * (position, head) columns of a KV head are shared out over ceil(G * k / 8)
- * CTAs, each reading the K/V codes once; or, where G * k >= 40 and
- * G * k * min(num_seqs * num_kv_heads, SMs) >= 40 * SMs (G in {1,2,4,8,16}, q and
- * out 16-B aligned), on the FP8 prefill kernel (paged_attention_prefill_chunk_fp8
- * with k rows per sequence), which reads the codes once per KV head.  Workspace:
- * paged_attention_verify_workspace_size() with the FP8 cache descriptor (sized
- * for the decode route, enough for both).
+ * CTAs, each reading the K/V codes once; or, when G is in {1,2,4,8,16} and
+ * G * k * min(num_seqs * num_kv_heads, SMs) >= 40 * SMs, on the FP8 prefill
+ * kernel (paged_attention_prefill_chunk_fp8 with k rows per sequence; q and out
+ * then 16-B aligned), which reads the codes once per KV head.  Workspace:
+ * paged_attention_verify_workspace_size() with the FP8 cache descriptor.
  * Errors: as paged_attention_verify; PKV_ERR_INVALID_ARG for a missing or
  * misaligned scale array.
  */

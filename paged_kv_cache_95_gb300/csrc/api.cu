@@ -680,14 +680,28 @@ int paged_attention_prefill_chunk_fp8(void *out, int32_t out_dtype, const void *
 
 namespace {
 constexpr int32_t kMaxVerifyRows = 16;  // draft positions per sequence
-constexpr int32_t kMaxVerifyCols = 32;  // (position, head) pairs per KV head on the decode kernel
+// SMs the verify routing below counts with: the current device's, else 152 (GB300).
+int64_t route_sms() {
+    const int dev = current_device();
+    return dev >= 0 && dev < kMaxDevices ? sm_count(dev) : 152;
+}
 
-// Verify runs on the decode kernel when the group's G x k (position, head) pairs
-// fit in at most two CTAs of up to 16 MMA columns each (K/V read once per CTA),
-// or when the prefill kernel cannot pack the group (G above 16, or G not dividing
-// its 128 tile rows); else on the prefill kernel.
-bool verify_on_decode(int32_t q_per_seq, int32_t G) {
-    return static_cast<int64_t>(q_per_seq) * G <= kMaxVerifyCols || G > 16 || 128 % G != 0;
+// Verify runs on the decode kernel (the G x k (position, head) columns of a KV head
+// shared out over ceil(G * k / 16) CTAs of up to 16 MMA columns, 8 over an FP8
+// cache, each reading the K/V) or on the prefill kernel (uniform q_len; K/V read
+// once per 256 rows, no split-KV, so its time is set by how many SMs its
+// num_seqs x n_kv CTAs fill).  Measured on the 8B-shaped (B=64, G=4) and
+// 70B-shaped (B=8 x 32K, G=8) batches, the decode route costs about
+// ceil(cols / 16) x 0.44 x min(units, SMs) / SMs times the prefill route for
+// bf16 and cols x min(units, SMs) / (37 x SMs) for FP8 (units = num_seqs x n_kv);
+// the prefill route is taken from a ratio of about 0.92 (bf16) / 1.08 (FP8) up,
+// where the prefill kernel can pack the group (G in {1, 2, 4, 8, 16}).
+bool verify_on_prefill(bool fp8, int32_t num_seqs, int32_t q_per_seq, int32_t G, int32_t n_kv) {
+    if (G > 16 || 128 % G != 0) return false;
+    const int64_t cols = static_cast<int64_t>(G) * q_per_seq;
+    const int64_t sms = route_sms();
+    const int64_t units = std::min<int64_t>(static_cast<int64_t>(num_seqs) * n_kv, sms);
+    return fp8 ? cols * units >= 40 * sms : (cols + 15) / 16 * units * 10 >= 21 * sms;
 }
 // CTAs per KV head and the columns each takes (the last one may take fewer): up to
 // 16 columns (two 8-column MMA tiles) per CTA, 8 over an FP8 cache (one tile).
@@ -696,25 +710,6 @@ int32_t verify_cols_per_cta(int32_t cols, bool fp8 = false) {
     return (cols + verify_splits(cols, fp8) - 1) / verify_splits(cols, fp8);
 }
 
-// FP8 verify: the decode kernel reads a KV head's codes once per 8 columns, so its
-// time grows with ceil(G * k / 8); the prefill kernel reads them once per 256
-// rows but has no split-KV, so its time is set by how many SMs its
-// num_seqs x n_kv CTAs fill.  Measured on the 8B- and 70B-shaped batches, the
-// decode route costs about cols x min(units, SMs) / (8 x 4.6 x SMs) times the
-// prefill route (units = num_seqs x n_kv); the prefill route is taken from a
-// ratio of 40 / 37 up (and only where it can run: G packs its tiles, q and out
-// 16-byte aligned, the device known).
-constexpr int32_t kVerifyFp8PrefillCols = 40;
-bool verify_fp8_on_prefill(int32_t num_seqs, int32_t q_per_seq, int32_t G, int32_t n_kv, const void *q,
-                           const void *out) {
-    const int64_t cols = static_cast<int64_t>(G) * q_per_seq;
-    if (cols < kVerifyFp8PrefillCols || G > 16 || 128 % G != 0 || !aligned(q, 16) || !aligned(out, 16)) return false;
-    const int dev = current_device();
-    if (dev < 0 || dev >= kMaxDevices) return false;
-    const int64_t sms = sm_count(dev);
-    const int64_t units = std::min<int64_t>(static_cast<int64_t>(num_seqs) * n_kv, sms);
-    return cols * units >= kVerifyFp8PrefillCols * sms;
-}
 }  // namespace
 
 size_t paged_attention_verify_workspace_size(int32_t num_seqs, int32_t q_per_seq, int32_t num_q_heads,
@@ -728,7 +723,7 @@ size_t paged_attention_verify_workspace_size(int32_t num_seqs, int32_t q_per_seq
     if (check_group(num_q_heads, cache->num_kv_heads) != PKV_OK) return 0;
     if (partition_size < 0 || partition_size % kBlockSize != 0) return 0;
     const int32_t G = num_q_heads / cache->num_kv_heads;
-    if (!fp8 && !verify_on_decode(q_per_seq, G)) return kStatusBytes;
+    if (verify_on_prefill(fp8, num_seqs, q_per_seq, G, cache->num_kv_heads)) return kStatusBytes;
     const int32_t pb = partition_size > 0 ? partition_size / kBlockSize : kMinPartBlocks;
     return plan_decode(num_seqs, num_q_heads, cache->num_kv_heads, max_blocks_per_seq, pb, q_per_seq,
                        verify_splits(G * q_per_seq, fp8))
@@ -738,9 +733,8 @@ size_t paged_attention_verify_workspace_size(int32_t num_seqs, int32_t q_per_seq
 namespace {
 
 // Shared by paged_attention_verify and paged_attention_verify_window (window 0: none).
-// k_scale / v_scale non-null: an FP8 cache (cache->dtype PKV_DTYPE_FP8_E4M3), on the
-// decode kernel with one 8-column MMA tile per CTA, or on the FP8 prefill kernel
-// where verify_fp8_on_prefill says it is faster.
+// k_scale / v_scale non-null: an FP8 cache (cache->dtype PKV_DTYPE_FP8_E4M3).  The
+// kernel is chosen by verify_on_prefill.
 int verify_impl(void *out, int32_t out_dtype, const void *q, int32_t q_per_seq, const void *k_cache,
                 const void *v_cache, const int32_t *block_tables, const int32_t *context_lens, int32_t num_seqs,
                 int32_t num_q_heads, int32_t max_blocks_per_seq, float scale, int32_t partition_size, int32_t window,
@@ -753,8 +747,7 @@ int verify_impl(void *out, int32_t out_dtype, const void *q, int32_t q_per_seq, 
     if (int rc = check_group(num_q_heads, cache->num_kv_heads)) return rc;
     if (q_per_seq < 1 || q_per_seq > kMaxVerifyRows) return PKV_ERR_INVALID_ARG;
     const int32_t G = num_q_heads / cache->num_kv_heads;
-    if (fp8 ? verify_fp8_on_prefill(num_seqs, q_per_seq, G, cache->num_kv_heads, q, out)
-            : !verify_on_decode(q_per_seq, G)) {
+    if (verify_on_prefill(fp8, num_seqs, q_per_seq, G, cache->num_kv_heads)) {
         // Prefill kernel, uniform rows: sequence b owns q rows b * q_per_seq .. + q_per_seq - 1.
         if (static_cast<int64_t>(num_seqs) * q_per_seq > INT32_MAX) return PKV_ERR_INVALID_ARG;
         return prefill_impl(out, out_dtype, q, nullptr, q_per_seq, q_per_seq, num_seqs * q_per_seq, k_cache, v_cache,

@@ -160,13 +160,16 @@ def test_verify_argument_errors(lib):
     assert v(2, nq=96) == P.PKV_ERR_UNSUPPORTED                 # G = 12
     assert v(2, wsb=100) == P.PKV_ERR_WORKSPACE_TOO_SMALL       # decode path (G * k = 8)
     assert v(8, wsb=100) == P.PKV_ERR_WORKSPACE_TOO_SMALL       # decode path, two CTAs per KV head (G * k = 32)
-    assert v(16, out=FAKE + 4) == P.PKV_ERR_INVALID_ARG         # prefill path (G * k = 64): 16-B out
+    assert v(16, out=FAKE + 4, B=64) == P.PKV_ERR_INVALID_ARG   # prefill path (G * k = 64, 512 units): 16-B out
     ws = lambda k: lib.paged_attention_verify_workspace_size(64, k, 32, 256, 0, ctypes.byref(c))
     assert ws(0) == 0 and ws(17) == 0
     assert ws(16) == 256                                        # prefill path: the status word
     # decode path: partials for 64 * k rows of 32 heads
     assert ws(2) > lib.paged_attention_workspace_size(64, 32, 256, 0, ctypes.byref(c))
     assert ws(8) > ws(4) > ws(2)
+    # 4 sequences x 8 KV heads = 32 units fill few SMs: G * k = 64 stays on the decode kernel
+    ws4 = lambda k: lib.paged_attention_verify_workspace_size(4, k, 32, 256, 0, ctypes.byref(c))  # noqa: E731
+    assert ws4(16) > ws4(8) > 256
 
 
 def test_fp8_argument_errors(lib):
@@ -269,7 +272,7 @@ def test_verify_window_argument_errors(lib):
     assert v(0, 64) == P.PKV_ERR_INVALID_ARG
     assert v(2, 64, nq=96) == P.PKV_ERR_UNSUPPORTED             # G = 12
     assert v(2, 64, wsb=100) == P.PKV_ERR_WORKSPACE_TOO_SMALL   # decode path
-    assert v(16, 64, out=FAKE + 4) == P.PKV_ERR_INVALID_ARG     # prefill path: 16-B out
+    assert v(16, 64, out=FAKE + 4, B=64) == P.PKV_ERR_INVALID_ARG  # prefill path (512 units): 16-B out
 
 
 def test_verify_fp8_argument_errors(lib):
@@ -286,7 +289,10 @@ def test_verify_fp8_argument_errors(lib):
     assert v(0) == P.PKV_ERR_INVALID_ARG
     assert v(2, wsb=100) == P.PKV_ERR_WORKSPACE_TOO_SMALL
     ws = lambda k: lib.paged_attention_verify_workspace_size(64, k, 32, 256, 0, ctypes.byref(c8))  # noqa: E731
-    assert ws(16) > ws(8) > 256                                  # FP8 verify always runs on the decode kernel
+    assert ws(8) > ws(4) > 256                                   # decode kernel, one 8-column tile per CTA
+    assert ws(16) == 256                                         # G * k = 64 over 512 units: the prefill kernel
+    ws4 = lambda k: lib.paged_attention_verify_workspace_size(4, k, 32, 256, 0, ctypes.byref(c8))  # noqa: E731
+    assert ws4(16) > ws4(8) > 256                                # 32 units: the decode kernel
 
 
 def test_prefill_fp8_argument_errors(lib):

@@ -3,10 +3,11 @@
 Row i of sequence b sits at position ctx_b - k + i and sees keys j <= ctx_b - k + i
 ("LLM 推理全过程的维度变化与核心公式", section "工程优化怎么嵌进公式", Speculative
 Decoding: the target model checks the k draft positions in one pass) -- the
-oracle's causal-chunk rule with q_len = k.  G * k <= 32 (or a G above 16 or
-one that does not divide 128) runs on the decode kernel (one 8-column MMA tile per CTA up to 8
-columns, two tiles up to 16, more CTAs per KV head above that, ragged shares
-included), larger products on the tcgen05 prefill kernel; all are covered.
+oracle's causal-chunk rule with q_len = k.  The decode kernel (one 8-column MMA
+tile per CTA up to 8 columns, two tiles up to 16, more CTAs per KV head above
+that, ragged shares included) and the tcgen05 prefill kernel (taken when G * k
+columns over enough sequences x KV heads make it faster, and G packs its tiles)
+are both covered, and a test pins which one a batch takes.
 """
 import numpy as np
 import pytest
@@ -24,6 +25,15 @@ CTX = [16, 17, 33, 100, 256, 257, 700, 1000]
 @pytest.fixture(scope="module", autouse=True)
 def _lib(built_library):
     P.load_library()
+
+
+def _on_decode(G, k, nseq, n_kv):
+    """The library's route: the prefill kernel when it can pack the group and
+    ceil(G k / 16) x min(units, SMs) x 10 >= 21 x SMs (units = sequences x KV heads)."""
+    if G > 16 or 128 % G:
+        return True
+    sms = torch().cuda.get_device_properties(0).multi_processor_count
+    return -(-G * k // 16) * min(nseq * n_kv, sms) * 10 < 21 * sms
 
 
 def _verify(d, batch, k, partition_size=0, out_dtype=None, context_lens=None, window=0, tables=None):
@@ -49,7 +59,7 @@ def test_verify_parity(n_q, n_kv, k):
     ref = oracle.paged_attention(batch.q, batch.cu_q_lens, kc, vc, batch.block_tables, batch.context_lens, wl.scale,
                                  n_q=wl.n_q)
     G = n_q // n_kv
-    on_decode = G * k <= 32 or G > 16 or 128 % G != 0
+    on_decode = _on_decode(G, k, len(ctx), n_kv)
     for part in ((0, 16, 256) if on_decode else (0,)):
         out, ws = _verify(d, batch, k, partition_size=part)
         assert_close(out.cpu().numpy(), ref, what=f"G={n_q // n_kv} k={k} part={part}")
@@ -106,7 +116,7 @@ def test_verify_window_parity(n_q, n_kv, k):
     d.append()
     kc, vc = oracle_after_append(wl)
     G = n_q // n_kv
-    on_decode = G * k <= 32 or G > 16 or 128 % G != 0
+    on_decode = _on_decode(G, k, len(ctx), n_kv)
     for win in (1, 5, 16, 17, 100, 300):
         ref = oracle.paged_attention(batch.q, batch.cu_q_lens, kc, vc, batch.block_tables, batch.context_lens,
                                      wl.scale, n_q=wl.n_q, window=win)
@@ -125,3 +135,31 @@ def test_verify_window_errors():
     d = DevWorkload(wl)
     with pytest.raises(P.PagedKVError):
         _verify(d, batch, 4, window=-1)
+
+
+@pytest.mark.parametrize("n_q,n_kv,k,nseq", [(32, 8, 16, 16), (64, 8, 16, 12), (64, 8, 8, 4), (32, 8, 16, 3)])
+def test_verify_route_by_units(n_q, n_kv, k, nseq):
+    """G * k = 64 or 128 columns: over 96-128 sequence x KV-head units the prefill
+    kernel (the result is bit-identical to paged_attention_prefill_chunk with k rows
+    per sequence on a 152-SM GPU); over 24-32 units the decode kernel with 4 to 8
+    CTAs of 16 columns per KV head.  Both against the oracle."""
+    t = torch()
+    base = (16, 17, 33, 100, 256, 257, 700, 1000, 5, 129, 128, 300, 64, 999, 2000, 31)
+    ctx = [max(base[i], k) for i in range(nseq)]
+    wl, batch = W.make_custom(n_q, n_kv, ctx, q_lens=[k] * nseq, seed=590 + k + nseq, materialize_logical=False)
+    d = DevWorkload(wl)
+    d.append()
+    kc, vc = oracle_after_append(wl)
+    ref = oracle.paged_attention(batch.q, batch.cu_q_lens, kc, vc, batch.block_tables, batch.context_lens, wl.scale,
+                                 n_q=wl.n_q)
+    G = n_q // n_kv
+    on_decode = _on_decode(G, k, nseq, n_kv)
+    for part in ((0, 16) if on_decode else (0,)):
+        out, ws = _verify(d, batch, k, partition_size=part)
+        assert_close(out.cpu().numpy(), ref, what=f"G={G} k={k} B={nseq} part={part}")
+        assert status_word(ws) == 0
+    if t.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert on_decode == (nseq * n_kv < 64)
+        if not on_decode:
+            pf, _ = d.prefill(batch)
+            assert t.equal(out, pf), "verify did not take the prefill route"
