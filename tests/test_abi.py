@@ -309,3 +309,27 @@ def test_prefill_fp8_argument_errors(lib):
     assert f(c=desc()) == P.PKV_ERR_UNSUPPORTED                  # a bf16 cache descriptor
     assert f(wsb=2) == P.PKV_ERR_WORKSPACE_TOO_SMALL
     assert lib.paged_attention_prefill_workspace_size(4, 32, ctypes.byref(c8)) > 0
+
+
+# (sequences, q heads, KV heads, k, FP8, the route measured faster on a 152-SM GB300):
+# 8B-shaped B=64 (G=4) and 70B-shaped B=8 x 32K (G=8), decode route vs prefill route.
+MEASURED_VERIFY_ROUTES = [
+    *[(64, 32, 8, k, False, "decode") for k in (4, 5, 6, 8)],          # 120-194 us vs ~205 us
+    *[(64, 32, 8, k, False, "prefill") for k in (12, 16)],             # 278 / 365 vs 205 / 207 us
+    *[(8, 64, 8, k, False, "decode") for k in (4, 5, 6, 8)],           # 287-559 vs ~604 us
+    *[(8, 64, 8, k, False, "prefill") for k in (12, 16)],              # 833 / 1106 vs 605 us
+    *[(64, 32, 8, k, True, "decode") for k in (1, 2, 4, 8)],           # 69-248 vs ~283 us
+    (64, 32, 8, 16, True, "prefill"),                                  # 481 vs 285 us
+    *[(8, 64, 8, k, True, "decode") for k in (1, 2, 4, 8)],            # 114-772 vs ~945 us
+    (8, 64, 8, 16, True, "prefill"),                                   # 1530 vs 945 us
+]
+
+
+@pytest.mark.parametrize("nseq,nq,nkv,k,fp8,faster", MEASURED_VERIFY_ROUTES)
+def test_verify_route_follows_measurements(lib, nseq, nq, nkv, k, fp8, faster):
+    """Without a device the routing counts 152 SMs; the workspace query answers the
+    status word alone (256 bytes) exactly when the prefill kernel is chosen."""
+    c = desc(num_blocks=40000, n_kv=nkv, dtype=P.PKV_DTYPE_FP8_E4M3 if fp8 else 0)
+    nbytes = lib.paged_attention_verify_workspace_size(nseq, k, nq, 2048, 0, ctypes.byref(c))
+    assert nbytes > 0
+    assert ("prefill" if nbytes == 256 else "decode") == faster
