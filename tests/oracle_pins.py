@@ -219,6 +219,22 @@ def check_linearity_in_v(lib):
 
 # ---- invariances -----------------------------------------------------------------
 
+def check_score_shift_invariance(lib):
+    """Softmax is invariant under s -> s + c per row and head: adding one vector u
+    to every key adds scale q.u to all of a row's scores, so the output stays.
+    K holds small integers and u = 8 e_0, so both pools are exact in bf16; decode
+    rows and causal-chunk rows are covered."""
+    wl, batch = W.make_custom(8, 2, [23, 50], q_lens=[1, 5], seed=11)
+    rng = np.random.default_rng(11)
+    kc, vc = _appended(wl, lib)
+    k_int = rng.integers(-4, 5, size=kc.shape).astype(np.float32)
+    k_shift = k_int.copy()
+    k_shift[..., 0] += 8.0
+    base = _attn(wl, batch, _bits(k_int), vc, lib)
+    shifted = _attn(wl, batch, _bits(k_shift), vc, lib)
+    assert np.all(np.isfinite(base))
+    assert np.max(np.abs(shifted - base)) <= TOL
+
 def check_repeat_interleave_equivalence(lib):
     """GQA equals MHA on K/V repeated G times along the head axis (page 1, section 3.2)."""
     wl, batch = W.make_custom(32, 8, [9, 30, 64], q_lens=[1, 4, 1], seed=9)
@@ -491,7 +507,7 @@ ALL_CHECKS = [
     check_cache_write_roundtrip, check_cache_write_skips_padding,
     check_tiny_vs_brute, check_group_sizes_vs_brute, check_chunks_vs_brute,
     check_single_key_returns_v, check_constant_scores_give_mean, check_two_keys_sigmoid,
-    check_linearity_in_v,
+    check_linearity_in_v, check_score_shift_invariance,
     check_repeat_interleave_equivalence, check_block_permutation_invariance,
     check_shared_prefix_invariance, check_chunk_last_row_equals_decode, check_chunk_split_invariance,
     check_split_merge_identity, check_lse,
