@@ -394,7 +394,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nload = min(8, nblocks - (kt0 + kt) * 8);
             if constexpr (FP8) {
                 // Block t's 2 KB code tile (one box: 128 codes x 16 slots, 128-byte swizzle) into the
-                // stage's upper half, and its 64 B of scales into the stage's scale row.
+                // stage's upper half, and its 64 B of scales into the key tile's scale slot (K: slot
+                // kt % kScaleSlotsK of the deeper K-scale ring; V: the V stage's slot).
                 if (lane == 0) mbar_arrive_expect_tx(bar, nload * (kCodeTile + kBlockSize * 4));
                 __syncwarp();
                 if (lane < nload) {
