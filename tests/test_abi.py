@@ -333,3 +333,26 @@ def test_verify_route_follows_measurements(lib, nseq, nq, nkv, k, fp8, faster):
     nbytes = lib.paged_attention_verify_workspace_size(nseq, k, nq, 2048, 0, ctypes.byref(c))
     assert nbytes > 0
     assert ("prefill" if nbytes == 256 else "decode") == faster
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_verify_route_is_monotone(lib, fp8):
+    """More draft positions or more sequences never move a batch from the prefill
+    kernel back to the decode kernel (152 SMs without a device), for every group
+    size the prefill kernel packs; group sizes it cannot pack never leave the
+    decode kernel."""
+    def on_prefill(nseq, n_kv, G, k):
+        c = desc(num_blocks=40000, n_kv=n_kv, dtype=P.PKV_DTYPE_FP8_E4M3 if fp8 else 0)
+        n = lib.paged_attention_verify_workspace_size(nseq, k, G * n_kv, 512, 0, ctypes.byref(c))
+        assert n > 0
+        return n == 256
+    for n_kv in (1, 8):
+        for G in (1, 2, 4, 8, 16, 24):
+            for nseq in (1, 4, 8, 19, 64, 200):
+                route = [on_prefill(nseq, n_kv, G, k) for k in range(1, 17)]
+                if G == 24:
+                    assert not any(route)
+                    continue
+                assert route == sorted(route), (n_kv, G, nseq)           # once prefill, stays prefill in k
+                more = [on_prefill(nseq + 5, n_kv, G, k) for k in range(1, 17)]
+                assert all(m or not r for r, m in zip(route, more)), (n_kv, G, nseq)
