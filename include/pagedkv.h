@@ -29,8 +29,11 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - All data pointers are DEVICE pointers owned by the caller; the library
- *    allocates nothing, keeps no pointer after it returns and has no global
- *    state besides a per-device cache of SM counts and kernel attributes.
+ *    allocates nothing at run time and keeps no pointer after it returns.
+ *    Its global state: a per-device cache of SM counts and kernel attributes,
+ *    and one file-scope device array of PKV_STATIC_SCRATCH_BYTES (held by every
+ *    GPU that loads the library) with its cached per-device address, used only
+ *    by paged_attention_decode_static_scratch and shared by all its calls.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  Every call only enqueues work on that stream and returns; it
  *    never synchronises.  Ordering between calls is the caller's: append the
@@ -235,14 +238,11 @@ PKV_API int32_t paged_attention_decode_partitions(int32_t num_seqs, int32_t num_
  *   workspace      : device scratch, 256-B aligned, of at least
  *                    paged_attention_workspace_size(num_seqs, num_q_heads,
  *                    max_blocks_per_seq, partition_size, cache) bytes; holds
- *                    the status word, per-group arrival counters and the
- *                    per-partition partials.  Zero-fill it once before its
- *                    first use (e.g. cudaMemsetAsync); every call that
- *                    completes leaves the counters at zero again, so the same
- *                    workspace serves later calls without clearing (after a
- *                    call that set PKV_STATUS_TIMEOUT, zero-fill it again).
- *                    Calls that share a workspace must not overlap in time
- *                    (they race on it).
+ *                    the status word (byte 0) and the per-partition partials
+ *                    (written before they are read, so only the status word
+ *                    needs clearing; it is sticky).  The same workspace serves
+ *                    later calls.  Calls that share a workspace must not
+ *                    overlap in time (they race on it).
  * Enqueues the decode kernel and, when a context is split into partitions,
  * the log-sum-exp merge kernel (both with programmatic dependent launch).
  * Errors: PKV_ERR_INVALID_ARG / PKV_ERR_UNSUPPORTED /
@@ -305,8 +305,8 @@ PKV_API int paged_attention_decode_append(void *out, int32_t out_dtype, const vo
  * device and stall, and callers such as plugins or other libraries that are
  * handed only the input and output buffers.
  *
- * The split-KV scratch (status word, arrival counters and per-partition
- * partials) lives in one file-scope device array of PKV_STATIC_SCRATCH_BYTES
+ * The split-KV scratch (status word and per-partition partials) lives in one
+ * file-scope device array of PKV_STATIC_SCRATCH_BYTES
  * bytes instead of a workspace argument.  Everything else -- arguments,
  * layouts, result and error codes -- is exactly paged_attention_decode's.
  *
@@ -320,11 +320,13 @@ PKV_API int paged_attention_decode_append(void *out, int32_t out_dtype, const vo
  *    before anything is enqueued (use a larger partition_size, fewer
  *    sequences per call, or paged_attention_decode with a workspace).
  *  - The first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress, with that device current) and caches it; make
+ *    (cudaGetSymbolAddress, with that device current) and caches it once the
+ *    lookup succeeds (a failed lookup is retried by the next call); make
  *    that first call outside any stream capture.
  *  - Every call on a device shares the one array, which keeps the last
- *    call's contents: each call clears the status word and counters it needs
- *    (an asynchronous memset on `stream`) before its kernels run.  Calls
+ *    call's contents: each call clears the 256-byte status word (an
+ *    asynchronous memset on `stream`) before its kernels run; the partials
+ *    are written before they are read.  Calls
  *    whose execution overlaps on the GPU (different streams without ordering
  *    between them, or different host threads) race on the array and give
  *    undefined results; serialise them.

@@ -36,10 +36,10 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 // ---- per-device caches -----------------------------------------------------------
 std::atomic<int> g_sm_count[kMaxDevices];
-std::once_flag g_decode_prepared[kMaxDevices][8];
+std::once_flag g_decode_prepared[kMaxDevices];
 std::once_flag g_prefill_prepared[kMaxDevices];
 std::once_flag g_decode_fp8_prepared[kMaxDevices];
-cudaError_t g_decode_prep_err[kMaxDevices][8];
+cudaError_t g_decode_prep_err[kMaxDevices];
 cudaError_t g_decode_fp8_prep_err[kMaxDevices];
 cudaError_t g_prefill_prep_err[kMaxDevices];
 
@@ -179,30 +179,26 @@ int check_group(int32_t n_q, int32_t n_kv) {
 }
 
 // ---- decode plan -----------------------------------------------------------------------
-// Workspace layout: [status word | arrival counters | part_m | part_l | part_o],
-// each region 256-byte aligned; only the status word when nothing is split.
+// Workspace layout: [status word | part_m | part_l | part_o], each region
+// 256-byte aligned; only the status word when nothing is split.
 struct DecodePlan {
     int32_t part_blocks;
     int32_t max_parts;
-    size_t off_cnt, off_m, off_l, off_o, total;
+    size_t off_m, off_l, off_o, total;
 };
 
-// rows_per_seq: query rows per sequence (1 for decode, q_per_seq for verify);
-// ctas_per_kv: CTAs per KV head and partition (0: the decode's, from G).
-DecodePlan plan_decode(int32_t num_seqs, int32_t n_q, int32_t n_kv, int32_t max_blocks, int32_t part_blocks,
-                       int32_t rows_per_seq = 1, int32_t ctas_per_kv = 0) {
+// rows_per_seq: query rows per sequence (1 for decode, q_per_seq for verify).
+DecodePlan plan_decode(int32_t num_seqs, int32_t n_q, int32_t max_blocks, int32_t part_blocks,
+                       int32_t rows_per_seq = 1) {
     DecodePlan pl{};
     pl.part_blocks = part_blocks >= max_blocks ? max_blocks : part_blocks;
     pl.max_parts = (max_blocks + pl.part_blocks - 1) / pl.part_blocks;
-    pl.off_cnt = kStatusBytes;
     if (pl.max_parts <= 1) {
         pl.off_m = pl.off_l = pl.off_o = pl.total = kStatusBytes;
         return pl;
     }
-    const int32_t G = n_q / n_kv;
-    const int32_t groups = n_kv * (ctas_per_kv > 0 ? ctas_per_kv : (G <= 8 ? 1 : G / 8));  // CTAs per sequence, partition
     const size_t rows = static_cast<size_t>(num_seqs) * rows_per_seq * n_q * pl.max_parts;
-    pl.off_m = pl.off_cnt + align_up(static_cast<size_t>(num_seqs) * groups * 4, 256);
+    pl.off_m = kStatusBytes;
     pl.off_l = pl.off_m + align_up(rows * 4, 256);
     pl.off_o = pl.off_l + align_up(rows * 4, 256);
     pl.total = pl.off_o + align_up(rows * kHeadDim * 4, 256);
@@ -226,10 +222,6 @@ int32_t auto_part_blocks(int32_t num_seqs, int32_t n_kv, int32_t head_splits, in
     //      split (B=1 x 128K: 69.8 vs 73.3 us and 176 vs 184 us);
     //  (c) when few (sequence, head) units exist the partitions shrink (not below
     //      256 tokens, nor below (b)'s floor) until the grid covers every SM twice.
-    if (const char *e = std::getenv("PAGEDKV_PART_BLOCKS")) {  // tuning sweeps
-        const int v = std::atoi(e);
-        if (v >= kMinPartBlocks) return v;
-    }
     const int64_t units = static_cast<int64_t>(num_seqs) * n_kv * head_splits;
     const int64_t nsm = sms > 0 ? sms : 148;
     if (fp8) {
@@ -257,32 +249,6 @@ int32_t auto_part_blocks(int32_t num_seqs, int32_t n_kv, int32_t head_splits, in
     const int64_t want = nsm * 2;  // (c)
     while (pb > floor_pb && units * ((max_blocks + pb - 1) / pb) < want) pb /= 2;
     return std::max(pb, floor_pb);
-}
-
-pkv::DecodeVariant decode_variant() {
-    static pkv::DecodeVariant v = [] {
-        pkv::DecodeVariant d{4, 2};  // 4 warps x 2 stages: 64 KB, 3 CTAs per SM (measured best)
-        if (const char *e = std::getenv("PAGEDKV_DECODE_VARIANT")) {  // "warps,stages", for tuning sweeps
-            int w = 0, s = 0;
-            if (sscanf(e, "%d,%d", &w, &s) == 2 && pkv::decode_variant_supported({w, s})) d = {w, s};
-        }
-        return d;
-    }();
-    return v;
-}
-
-int variant_index(pkv::DecodeVariant v) { return (v.warps == 8 ? 4 : 0) + (v.stages - 1) % 4; }
-
-// How split partitions are merged: by a separate merge kernel launched with
-// programmatic dependent launch (default, measured faster), or inside the
-// decode kernel by the last CTA of each group ("PAGEDKV_MERGE=fused", for
-// tuning sweeps).  Both compute the same log-sum-exp reduction.
-bool fused_merge() {
-    static const bool fused = [] {
-        const char *e = std::getenv("PAGEDKV_MERGE");
-        return e && std::strcmp(e, "fused") == 0;
-    }();
-    return fused;
 }
 
 }  // namespace
@@ -366,7 +332,7 @@ size_t paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads, int
     if (check_group(num_q_heads, cache->num_kv_heads) != PKV_OK) return 0;
     if (partition_size < 0 || partition_size % kBlockSize != 0) return 0;
     const int32_t pb = partition_size > 0 ? partition_size / kBlockSize : kMinPartBlocks;
-    return plan_decode(num_seqs, num_q_heads, cache->num_kv_heads, max_blocks_per_seq, pb).total;
+    return plan_decode(num_seqs, num_q_heads, max_blocks_per_seq, pb).total;
 }
 
 int32_t paged_attention_decode_partitions(int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq,
@@ -389,7 +355,7 @@ int32_t paged_attention_decode_partitions(int32_t num_seqs, int32_t num_q_heads,
         const bool fp8 = cache->dtype == PKV_DTYPE_FP8_E4M3;
         pb = auto_part_blocks(num_seqs, cache->num_kv_heads, head_splits, span, sm_count(dev), !fp8, fp8);
     }
-    return plan_decode(num_seqs, num_q_heads, cache->num_kv_heads, span, pb).max_parts;
+    return plan_decode(num_seqs, num_q_heads, span, pb).max_parts;
 }
 
 namespace {
@@ -443,7 +409,7 @@ int decode_impl(void *out, int32_t out_dtype, const void *q, const void *k_cache
 
     const int32_t pb = partition_size > 0 ? partition_size / kBlockSize
                                           : auto_part_blocks(num_seqs, n_kv, head_splits, span_blocks, sms, !fp8, fp8);
-    const DecodePlan pl = plan_decode(num_seqs, num_q_heads, n_kv, span_blocks, pb);
+    const DecodePlan pl = plan_decode(num_seqs, num_q_heads, span_blocks, pb);
     if (workspace_bytes < pl.total) return PKV_ERR_WORKSPACE_TOO_SMALL;  // cannot happen for auto plans
 
     CUtensorMap kmap, vmap;
@@ -453,15 +419,12 @@ int decode_impl(void *out, int32_t out_dtype, const void *q, const void *k_cache
                !encode_pool_map(&vmap, v_cache, cache->num_blocks, n_kv)))
         return PKV_ERR_CUDA;
 
-    const pkv::DecodeVariant var = decode_variant();
-    const int vi = variant_index(var);
     if (fp8) {
         std::call_once(g_decode_fp8_prepared[dev], [&] { g_decode_fp8_prep_err[dev] = pkv::decode_fp8_prepare_device(); });
         if (g_decode_fp8_prep_err[dev] != cudaSuccess) return PKV_ERR_CUDA;
     } else {
-        std::call_once(g_decode_prepared[dev][vi],
-                       [&] { g_decode_prep_err[dev][vi] = pkv::decode_prepare_device(var); });
-        if (g_decode_prep_err[dev][vi] != cudaSuccess) return PKV_ERR_CUDA;
+        std::call_once(g_decode_prepared[dev], [&] { g_decode_prep_err[dev] = pkv::decode_prepare_device(); });
+        if (g_decode_prep_err[dev] != cudaSuccess) return PKV_ERR_CUDA;
     }
 
     uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -474,7 +437,6 @@ int decode_impl(void *out, int32_t out_dtype, const void *q, const void *k_cache
     p.part_m = pl.max_parts > 1 ? reinterpret_cast<float *>(ws + pl.off_m) : nullptr;
     p.part_l = pl.max_parts > 1 ? reinterpret_cast<float *>(ws + pl.off_l) : nullptr;
     p.part_o = pl.max_parts > 1 ? reinterpret_cast<float *>(ws + pl.off_o) : nullptr;
-    p.counters = pl.max_parts > 1 ? reinterpret_cast<uint32_t *>(ws + pl.off_cnt) : nullptr;
     p.num_seqs = num_seqs;
     p.n_q = num_q_heads;
     p.n_kv = n_kv;
@@ -487,7 +449,6 @@ int decode_impl(void *out, int32_t out_dtype, const void *q, const void *k_cache
     p.max_parts = pl.max_parts;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     p.out_bf16 = out_dtype == PKV_DTYPE_BF16;
-    p.fused_merge = fused_merge() ? 1 : 0;
     p.window = window;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -499,7 +460,7 @@ int decode_impl(void *out, int32_t out_dtype, const void *q, const void *k_cache
         pa.new_v = new_value;
         pa.k_cache = const_cast<void *>(k_cache);
         pa.v_cache = const_cast<void *>(v_cache);
-        e = pkv::launch_paged_decode_append(kmap, vmap, pa, var, s);
+        e = pkv::launch_paged_decode_append(kmap, vmap, pa, s);
     } else if (fp8) {
         pkv::DecodeParamsFp8 p8{};
         static_cast<pkv::DecodeParams &>(p8) = p;
@@ -507,7 +468,7 @@ int decode_impl(void *out, int32_t out_dtype, const void *q, const void *k_cache
         p8.v_scale = v_scale;
         e = pkv::launch_paged_decode_fp8(kmap, vmap, p8, s);
     } else {
-        e = pkv::launch_paged_decode(kmap, vmap, p, var, s);
+        e = pkv::launch_paged_decode(kmap, vmap, p, s);
     }
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
@@ -725,9 +686,7 @@ size_t paged_attention_verify_workspace_size(int32_t num_seqs, int32_t q_per_seq
     const int32_t G = num_q_heads / cache->num_kv_heads;
     if (verify_on_prefill(fp8, num_seqs, q_per_seq, G, cache->num_kv_heads)) return kStatusBytes;
     const int32_t pb = partition_size > 0 ? partition_size / kBlockSize : kMinPartBlocks;
-    return plan_decode(num_seqs, num_q_heads, cache->num_kv_heads, max_blocks_per_seq, pb, q_per_seq,
-                       verify_splits(G * q_per_seq, fp8))
-        .total;
+    return plan_decode(num_seqs, num_q_heads, max_blocks_per_seq, pb, q_per_seq).total;
 }
 
 namespace {
@@ -785,7 +744,7 @@ int verify_impl(void *out, int32_t out_dtype, const void *q, int32_t q_per_seq, 
                    : max_blocks_per_seq;
     const int32_t pb = partition_size > 0 ? partition_size / kBlockSize
                                           : auto_part_blocks(num_seqs, n_kv, splits, span, sms, false);
-    const DecodePlan pl = plan_decode(num_seqs, num_q_heads, n_kv, span, pb, q_per_seq, splits);
+    const DecodePlan pl = plan_decode(num_seqs, num_q_heads, span, pb, q_per_seq);
     if (workspace_bytes < pl.total) return PKV_ERR_WORKSPACE_TOO_SMALL;
 
     CUtensorMap kmap, vmap;
@@ -794,15 +753,12 @@ int verify_impl(void *out, int32_t out_dtype, const void *q, int32_t q_per_seq, 
             : (!encode_pool_map(&kmap, k_cache, cache->num_blocks, n_kv) ||
                !encode_pool_map(&vmap, v_cache, cache->num_blocks, n_kv)))
         return PKV_ERR_CUDA;
-    const pkv::DecodeVariant var = decode_variant();
-    const int vi = variant_index(var);
     if (fp8) {
         std::call_once(g_decode_fp8_prepared[dev], [&] { g_decode_fp8_prep_err[dev] = pkv::decode_fp8_prepare_device(); });
         if (g_decode_fp8_prep_err[dev] != cudaSuccess) return PKV_ERR_CUDA;
     } else {
-        std::call_once(g_decode_prepared[dev][vi],
-                       [&] { g_decode_prep_err[dev][vi] = pkv::decode_prepare_device(var); });
-        if (g_decode_prep_err[dev][vi] != cudaSuccess) return PKV_ERR_CUDA;
+        std::call_once(g_decode_prepared[dev], [&] { g_decode_prep_err[dev] = pkv::decode_prepare_device(); });
+        if (g_decode_prep_err[dev] != cudaSuccess) return PKV_ERR_CUDA;
     }
 
     uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -815,7 +771,6 @@ int verify_impl(void *out, int32_t out_dtype, const void *q, int32_t q_per_seq, 
     p.part_m = pl.max_parts > 1 ? reinterpret_cast<float *>(ws + pl.off_m) : nullptr;
     p.part_l = pl.max_parts > 1 ? reinterpret_cast<float *>(ws + pl.off_l) : nullptr;
     p.part_o = pl.max_parts > 1 ? reinterpret_cast<float *>(ws + pl.off_o) : nullptr;
-    p.counters = pl.max_parts > 1 ? reinterpret_cast<uint32_t *>(ws + pl.off_cnt) : nullptr;
     p.num_seqs = num_seqs;
     p.n_q = num_q_heads;
     p.n_kv = n_kv;
@@ -828,7 +783,6 @@ int verify_impl(void *out, int32_t out_dtype, const void *q, int32_t q_per_seq, 
     p.max_parts = pl.max_parts;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     p.out_bf16 = out_dtype == PKV_DTYPE_BF16;
-    p.fused_merge = fused_merge() ? 1 : 0;
     p.window = window;
     p.q_per_seq = q_per_seq;
     p.k_scale = k_scale;
@@ -840,7 +794,7 @@ int verify_impl(void *out, int32_t out_dtype, const void *q, int32_t q_per_seq, 
         pkv::DecodeParamsVerify pv{};
         static_cast<pkv::DecodeParams &>(pv) = static_cast<const pkv::DecodeParams &>(p);
         pv.q_per_seq = q_per_seq;
-        e = pkv::launch_paged_verify(kmap, vmap, pv, var, static_cast<cudaStream_t>(stream));
+        e = pkv::launch_paged_verify(kmap, vmap, pv, static_cast<cudaStream_t>(stream));
     }
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
@@ -891,16 +845,18 @@ static_assert(PKV_STATIC_SCRATCH_BYTES % 256 == 0, "scratch size must keep 256-b
 static __device__ __align__(256) uint8_t g_decode_scratch[PKV_STATIC_SCRATCH_BYTES];
 
 namespace {
-std::once_flag g_scratch_once[kMaxDevices];
+std::mutex g_scratch_mutex;
 void *g_scratch_addr[kMaxDevices];
 
-// Device address of g_decode_scratch on `dev` (which must be current); nullptr on failure.
+// Device address of g_decode_scratch on `dev` (which must be current); nullptr on
+// failure.  Only a successful lookup is kept, so a failed first call (for example
+// one made during stream capture) is retried by the next one.
 void *decode_scratch_address(int dev) {
-    std::call_once(g_scratch_once[dev], [dev] {
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (!g_scratch_addr[dev]) {
         void *ptr = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&ptr, g_decode_scratch);
-        g_scratch_addr[dev] = e == cudaSuccess ? ptr : nullptr;
-    });
+        if (cudaGetSymbolAddress(&ptr, g_decode_scratch) == cudaSuccess) g_scratch_addr[dev] = ptr;
+    }
     return g_scratch_addr[dev];
 }
 }  // namespace
@@ -922,11 +878,10 @@ int paged_attention_decode_static_scratch(void *out, int32_t out_dtype, const vo
     uint8_t *scratch = static_cast<uint8_t *>(decode_scratch_address(dev));
     if (!scratch) return PKV_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // What must start at zero: the status word and the arrival counters, which
-    // follow it; the partials are always written before they are read.
-    const int32_t G = num_q_heads / cache->num_kv_heads;
-    const size_t counters = static_cast<size_t>(num_seqs) * cache->num_kv_heads * (G <= 8 ? 1 : G / 8) * 4;
-    if (cudaMemsetAsync(scratch, 0, kStatusBytes + align_up(counters, 256), s) != cudaSuccess) return PKV_ERR_CUDA;
+    // What must start at zero: the status word alone (the split-KV partials are
+    // always written before they are read).
+    static_assert(kStatusBytes <= PKV_STATIC_SCRATCH_BYTES, "the status word lies inside the scratch array");
+    if (cudaMemsetAsync(scratch, 0, kStatusBytes, s) != cudaSuccess) return PKV_ERR_CUDA;
     const int rc = paged_attention_decode(out, out_dtype, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
                                           num_q_heads, max_blocks_per_seq, scale, partition_size, cache, scratch,
                                           PKV_STATIC_SCRATCH_BYTES, stream);

@@ -1,7 +1,7 @@
 // decode.cu -- paged decode attention: one CTA per sequence x KV head x
 // partition serves the whole GQA group; the partitions of a split context are
-// combined by a log-sum-exp merge (Flash-Decoding) done by the last CTA of the
-// group to finish, so one launch computes the whole decode.
+// combined by a separate log-sum-exp merge kernel (Flash-Decoding) launched
+// right behind the decode grid with programmatic dependent launch.
 //
 // What is computed ("LLM 推理全过程的维度变化与核心公式", section "Decode 阶段
 // 维度流转"; "注意力演进与推理流程", section 3.1):
@@ -41,9 +41,8 @@
 //    keys of the first block that precede j0 are masked like the tail.
 //  * At the end the warps' (m, l, O) are combined through shared memory; with a
 //    single partition the CTA writes out = O / l directly, otherwise it writes
-//    the unnormalised partial (m, l, O) to the workspace and counts itself on
-//    the group's arrival counter; the CTA that arrives last merges all
-//    partitions and resets the counter to zero for the next call.
+//    the unnormalised partial (m, l, O) to the workspace, and lse_merge_kernel
+//    folds the partitions of each (sequence, query head) row.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -347,66 +346,17 @@ __global__ void __launch_bounds__(NW * 32)
             }
         }
     }
-    if (nparts == 1 || !p.fused_merge) return;
-
-    // ---- split-KV: the last partition of this (sequence, head group) to finish merges ----
-    // out = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p,  M = max_p m_p
-    // (Flash-Decoding's log-sum-exp reduction, in the log2 domain of the scores).
-    // One acquire-release add per CTA publishes its partial (written by all
-    // threads before the barrier) and, for the last arrival, acquires the others'.
-    uint32_t *last_flag = reinterpret_cast<uint32_t *>(red_l + NW * kCols);
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const uint32_t prev = atom_add_acq_rel_gpu(p.counters + static_cast<size_t>(b) * (VERIFY ? p.n_kv * p.head_splits : gridDim.y) + hs, 1u);
-        *last_flag = prev == static_cast<uint32_t>(nparts - 1);
-    }
-    __syncthreads();
-    if (*last_flag == 0) return;
-
-    // Warp w folds the partitions p = w, w + NW, ...; lane owns dims 4*lane .. 4*lane+3.
-    for (int hh = 0; hh < ncols; ++hh) {
-        const size_t base = col_row(hh) * p.max_parts;
-        float M = -INFINITY;
-        for (int i = lane; i < nparts; i += 32) M = fmaxf(M, __ldcg(p.part_m + base + i));
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-        const float Mu = M == -INFINITY ? 0.f : M;
-        float L = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int i = warp; i < nparts; i += NW) {
-            const float f = fast_exp2(__ldcg(p.part_m + base + i) - Mu);
-            L += f * __ldcg(p.part_l + base + i);
-            const float4 v = __ldcg(reinterpret_cast<const float4 *>(p.part_o + (base + i) * kHeadDim) + lane);
-            acc.x += f * v.x;
-            acc.y += f * v.y;
-            acc.z += f * v.z;
-            acc.w += f * v.w;
-        }
-        reinterpret_cast<float4 *>(red_o + (warp * kCols + hh) * kHeadDim)[lane] = acc;
-        if (lane == 0) red_l[warp * kCols + hh] = L;
-    }
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < ncols * kHeadDim; idx += NW * 32) {
-        const int hh = idx >> 7, d = idx & 127;
-        float L = 0.f, O = 0.f;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-            L += red_l[w * kCols + hh];
-            O += red_o[(w * kCols + hh) * kHeadDim + d];
-        }
-        store_out(p.out, p.out_bf16, col_row(hh) * kHeadDim + d, L > 0.f ? O / L : 0.f);
-    }
-    if (threadIdx.x == 0)  // ready for the next call
-        p.counters[static_cast<size_t>(b) * (VERIFY ? p.n_kv * p.head_splits : gridDim.y) + hs] = 0u;
 }
 
 }  // namespace
 
 namespace {
 
-// Standalone log-sum-exp merge of the partitions (one CTA per sequence and query
-// head), for decodes that do not merge inside the decode kernel.  8 warps fold
-// the partitions p = w, w + 8, ...; lane owns dims 4*lane .. 4*lane + 3.
+// Log-sum-exp merge of the partitions (one CTA per query row and query head):
+//   out = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p,  M = max_p m_p
+// ("LLM 推理全过程的维度变化与核心公式", section "工程优化怎么嵌进公式", Flash
+// Decoding; scores in the log2 domain).  8 warps fold the partitions
+// p = w, w + 8, ...; lane owns dims 4*lane .. 4*lane + 3.
 constexpr int kMergeWarps = 8;
 
 __global__ void __launch_bounds__(kMergeWarps * 32) lse_merge_kernel(const DecodeParams p, int rows_per_seq) {
@@ -477,31 +427,20 @@ cudaError_t launch_variant(const CUtensorMap &kmap, const CUtensorMap &vmap,
     const dim3 grid = VERIFY ? dim3(p.max_parts * p.head_splits, p.n_kv, p.num_seqs)
                              : dim3(p.max_parts, p.n_kv * p.head_splits, p.num_seqs);
     cudaError_t e = launch_pdl(paged_decode_kernel<NW, ST, FP8, VERIFY, NCT, APPEND>, grid, dim3(NW * 32),
-                               FP8 ? decode_fp8_smem_bytes() : decode_smem_bytes({NW, ST}), stream, kmap, vmap, p);
+                               FP8 ? decode_fp8_smem_bytes() : decode_smem_bytes(), stream, kmap, vmap, p);
     if (e != cudaSuccess) return e;
     int rows_per_seq = 1;
     if constexpr (VERIFY) rows_per_seq = p.q_per_seq;
-    if (p.max_parts > 1 && !p.fused_merge)
+    if (p.max_parts > 1)
         e = launch_pdl(lse_merge_kernel, dim3(p.n_q, p.num_seqs * rows_per_seq), dim3(kMergeWarps * 32), 0, stream,
                        static_cast<const DecodeParams &>(p), rows_per_seq);
     return e;
 }
 
-template <int NW, int ST>
-cudaError_t prepare_variant() {
-    cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<NW, ST, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(decode_smem_bytes({NW, ST})));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(paged_decode_kernel<NW, ST, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(decode_smem_bytes({NW, ST})));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(paged_decode_kernel<NW, ST, false, true, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(decode_smem_bytes({NW, ST})));
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(paged_decode_kernel<NW, ST, false, false, 1, true>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(decode_smem_bytes({NW, ST})));
-}
+// The bf16 decode: 4 warps, 2 stages of one K and one V tile per warp; 64 KB of
+// shared memory let 3 CTAs share an SM (measured best of 4 x 2, 4 x 3, 4 x 4
+// and 8 x 2 warps x stages).
+constexpr int kWarps = 4, kStages = 2;
 
 // The FP8 decode: 4 warps, 3 stages of 4 KB codes (+ 128 B of scales) per warp;
 // 128 registers and 52 KB of shared memory let 4 CTAs share an SM.
@@ -509,21 +448,24 @@ constexpr int kFp8Warps = 4, kFp8Stages = 3;
 
 }  // namespace
 
-size_t decode_smem_bytes(DecodeVariant v) {
+size_t decode_smem_bytes() {
     // stage ring + mbarriers + 1 KB for aligning the base to the 1 KB swizzle period
-    return static_cast<size_t>(v.warps) * v.stages * kStageBytes + static_cast<size_t>(v.warps) * v.stages * 8 + 1024;
+    return static_cast<size_t>(kWarps) * kStages * kStageBytes + static_cast<size_t>(kWarps) * kStages * 8 + 1024;
 }
 
-bool decode_variant_supported(DecodeVariant v) {
-    return (v.warps == 4 && (v.stages == 2 || v.stages == 3 || v.stages == 4)) || (v.warps == 8 && v.stages == 2);
-}
-
-cudaError_t decode_prepare_device(DecodeVariant v) {
-    if (v.warps == 4 && v.stages == 2) return prepare_variant<4, 2>();
-    if (v.warps == 4 && v.stages == 3) return prepare_variant<4, 3>();
-    if (v.warps == 4 && v.stages == 4) return prepare_variant<4, 4>();
-    if (v.warps == 8 && v.stages == 2) return prepare_variant<8, 2>();
-    return cudaErrorInvalidValue;
+cudaError_t decode_prepare_device() {
+    const int smem = static_cast<int>(decode_smem_bytes());
+    cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<kWarps, kStages, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(paged_decode_kernel<kWarps, kStages, false, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(paged_decode_kernel<kWarps, kStages, false, true, 2>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(paged_decode_kernel<kWarps, kStages, false, false, 1, true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
 }
 
 size_t decode_fp8_smem_bytes() {
@@ -551,41 +493,21 @@ cudaError_t launch_paged_decode_fp8(const CUtensorMap &kmap, const CUtensorMap &
 }
 
 cudaError_t launch_paged_verify(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParamsVerify &p,
-                                DecodeVariant v, cudaStream_t stream) {
+                                cudaStream_t stream) {
     if (p.heads_per_cta > 16) return cudaErrorInvalidValue;
-    const bool two = p.heads_per_cta > 8;  // 9..16 columns: two 8-column MMA tiles per warp
-    if (v.warps == 4 && v.stages == 2)
-        return two ? launch_variant<4, 2, false, true, 2>(kmap, vmap, p, stream)
-                   : launch_variant<4, 2, false, true>(kmap, vmap, p, stream);
-    if (v.warps == 4 && v.stages == 3)
-        return two ? launch_variant<4, 3, false, true, 2>(kmap, vmap, p, stream)
-                   : launch_variant<4, 3, false, true>(kmap, vmap, p, stream);
-    if (v.warps == 4 && v.stages == 4)
-        return two ? launch_variant<4, 4, false, true, 2>(kmap, vmap, p, stream)
-                   : launch_variant<4, 4, false, true>(kmap, vmap, p, stream);
-    if (v.warps == 8 && v.stages == 2)
-        return two ? launch_variant<8, 2, false, true, 2>(kmap, vmap, p, stream)
-                   : launch_variant<8, 2, false, true>(kmap, vmap, p, stream);
-    return cudaErrorInvalidValue;
+    // 9..16 columns: two 8-column MMA tiles per warp
+    return p.heads_per_cta > 8 ? launch_variant<kWarps, kStages, false, true, 2>(kmap, vmap, p, stream)
+                               : launch_variant<kWarps, kStages, false, true>(kmap, vmap, p, stream);
 }
 
 cudaError_t launch_paged_decode_append(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParamsAppend &p,
-                                       DecodeVariant v, cudaStream_t stream) {
-    if (v.warps == 4 && v.stages == 2) return launch_variant<4, 2, false, false, 1, true>(kmap, vmap, p, stream);
-    if (v.warps == 4 && v.stages == 3) return launch_variant<4, 3, false, false, 1, true>(kmap, vmap, p, stream);
-    if (v.warps == 4 && v.stages == 4) return launch_variant<4, 4, false, false, 1, true>(kmap, vmap, p, stream);
-    if (v.warps == 8 && v.stages == 2) return launch_variant<8, 2, false, false, 1, true>(kmap, vmap, p, stream);
-    return cudaErrorInvalidValue;
+                                       cudaStream_t stream) {
+    return launch_variant<kWarps, kStages, false, false, 1, true>(kmap, vmap, p, stream);
 }
 
 cudaError_t launch_paged_decode(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParams &p,
-                                DecodeVariant v, cudaStream_t stream) {
-    if (v.warps == 4 && v.stages == 2) return launch_variant<4, 2>(kmap, vmap, p, stream);
-    if (v.warps == 4 && v.stages == 3) return launch_variant<4, 3>(kmap, vmap, p, stream);
-    if (v.warps == 4 && v.stages == 4) return launch_variant<4, 4>(kmap, vmap, p, stream);
-    if (v.warps == 8 && v.stages == 2) return launch_variant<8, 2>(kmap, vmap, p, stream);
-    return cudaErrorInvalidValue;
+                                cudaStream_t stream) {
+    return launch_variant<kWarps, kStages>(kmap, vmap, p, stream);
 }
-
 
 }  // namespace pkv

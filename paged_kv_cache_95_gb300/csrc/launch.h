@@ -46,7 +46,7 @@ cudaError_t launch_kv_cache_write(const void *key, const void *value, void *k_ca
                                   const int32_t *slot_mapping, int32_t num_tokens, int32_t n_kv,
                                   int32_t num_blocks, int sm_count, cudaStream_t stream);
 
-// ---- K2: decode with optional split-KV and its fused log-sum-exp merge ------------
+// ---- K2: decode with optional split-KV, K3: its log-sum-exp merge -----------------
 struct DecodeParams {
     const void *q;               // bf16 [num_seqs][n_q][128]
     void *out;                   // [num_seqs][n_q][128], f32 or bf16
@@ -55,7 +55,6 @@ struct DecodeParams {
     float *part_m;               // [num_seqs][n_q][max_parts]   (log2 domain, scale folded in)
     float *part_l;               // [num_seqs][n_q][max_parts]
     float *part_o;               // [num_seqs][n_q][max_parts][128] (unnormalised)
-    uint32_t *counters;          // [num_seqs][n_kv * head_splits] arrivals; zero between calls
     uint32_t *status;            // device status word
     int32_t num_seqs, n_q, n_kv;
     int32_t group;               // G = n_q / n_kv
@@ -67,7 +66,6 @@ struct DecodeParams {
     int32_t max_parts;           // partitions of the longest possible context
     float scale_log2;            // scale * log2(e)
     int32_t out_bf16;            // 1: bf16 output, 0: f32
-    int32_t fused_merge;         // 1: last partition CTA merges; 0: a separate merge kernel runs
     int32_t window;              // sliding window W (keys j >= ctx - W visible); 0: none
 };
 
@@ -103,30 +101,24 @@ struct DecodeParamsAppend : DecodeParams {
     void *v_cache;
 };
 
-struct DecodeVariant {
-    int warps;
-    int stages;
-};
-
-// Shared-memory bytes and supported variants of the decode kernel.
-size_t decode_smem_bytes(DecodeVariant v);
-bool decode_variant_supported(DecodeVariant v);
-cudaError_t decode_prepare_device(DecodeVariant v);  // sets the dynamic shared memory limit
-// Enqueues the decode kernel (and, when partitions are merged separately, the
-// merge kernel), both with programmatic dependent launch.
+// Shared-memory bytes of the decode kernel; sets its dynamic shared memory limit.
+size_t decode_smem_bytes();
+cudaError_t decode_prepare_device();
+// Enqueues the decode kernel and, when a context is split into partitions, the
+// merge kernel, both with programmatic dependent launch.
 cudaError_t launch_paged_decode(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParams &p,
-                                DecodeVariant v, cudaStream_t stream);
-// The FP8 (E4M3 codes + per-token scales) decode: fixed variant, same merge.
+                                cudaStream_t stream);
+// The FP8 (E4M3 codes + per-token scales) decode: its own stage layout, same merge.
 size_t decode_fp8_smem_bytes();
 cudaError_t decode_fp8_prepare_device();
 cudaError_t launch_paged_decode_fp8(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParamsFp8 &p,
                                     cudaStream_t stream);
 cudaError_t launch_paged_verify(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParamsVerify &p,
-                                DecodeVariant v, cudaStream_t stream);
+                                cudaStream_t stream);
 cudaError_t launch_paged_verify_fp8(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParamsFp8Verify &p,
                                     cudaStream_t stream);
 cudaError_t launch_paged_decode_append(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParamsAppend &p,
-                                       DecodeVariant v, cudaStream_t stream);
+                                       cudaStream_t stream);
 
 // ---- K4: causal chunked prefill on tcgen05 ---------------------------------------
 struct PrefillParams {

@@ -48,8 +48,7 @@ def test_workspace_size_math(lib):
     c = desc()
     # 64 seqs, 32 heads, 256 blocks/seq, 512-token partitions -> 8 parts
     rows = 64 * 32 * 8
-    counters = 64 * 8 * 4  # one arrival counter per (sequence, KV head)
-    want = 256 + counters + 2 * ((rows * 4 + 255) // 256 * 256) + rows * 128 * 4
+    want = 256 + 2 * ((rows * 4 + 255) // 256 * 256) + rows * 128 * 4  # status | m | l | O
     assert lib.paged_attention_workspace_size(64, 32, 256, 512, ctypes.byref(c)) == want
     # a partition that covers the whole context needs only the status word
     assert lib.paged_attention_workspace_size(64, 32, 256, 4096, ctypes.byref(c)) == 256

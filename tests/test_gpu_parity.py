@@ -90,8 +90,8 @@ def test_decode_partition_invariance(part):
 
 
 def test_decode_repeated_calls_share_a_workspace():
-    """The split-KV arrival counters reset themselves: reusing one workspace for
-    many calls (with different partition sizes) gives bitwise-identical results."""
+    """Reusing one workspace for many calls (with different partition sizes)
+    gives bitwise-identical results: no state carries over between calls."""
     t = torch()
     wl, _, _, _ = workload("llama3_8b_b64")
     d = DevWorkload(wl)
