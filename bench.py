@@ -11,9 +11,14 @@ causal chunks (paged_attention_prefill_chunk) and the decodes
 alongside (rows.two_call_step).
 The metric is KV-read throughput: the logical K+V bytes the attention reads
 (sum over sequences of ctx * n_kv * 128 * 2 * 2) per second, with sequences/s
-and tokens/s alongside.  The step time is taken over the whole timed loop; the
-per-kernel times come from CUDA events recorded on a sample of its steps (about
-100), since an event between two launches costs them their overlap.
+and tokens/s alongside.  The step time is taken over the whole timed loop, with
+no event between its steps (an event between two launches costs them their
+programmatic-dependent overlap); the per-kernel times come from a separate
+pass with CUDA events around each call.  On one GPU the line also carries
+`configs`: the same measurement on the other workloads of the five
+configurations (70B-shaped long contexts, the head-sharing sweep, the mixed
+continuous batch with its prefill chunk, the tiny batch), each with its own
+clock record.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload NAME]
@@ -134,9 +139,12 @@ class ClockSampler:
         if self.thread is not None:
             self.thread.join(timeout=2)
 
-    def summary(self):
+    def summary(self, window=None):
+        """Median SM clock, max clock and throttle reasons of the samples inside
+        `window` (t0, t1) (default: the marked one), +-0.1 s."""
+        window = window or self.window
         rows = []
-        for ts, line in self.samples:
+        for ts, line in list(self.samples):
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -146,7 +154,7 @@ class ClockSampler:
                 continue
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
-        inside = [r for r in rows if self.window and self.window[0] - 0.1 <= r[0] <= self.window[1] + 0.1]
+        inside = [r for r in rows if window and window[0] - 0.1 <= r[0] <= window[1] + 0.1]
         use = inside if inside else rows
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = set()
@@ -249,82 +257,67 @@ def run_ours(args):
     pool_bytes = 2 * k_cache.numel() * 2
 
     stream = torch.cuda.current_stream(dev)
-    # Per-kernel CUDA events on a sample of the timed steps (every `every`-th step):
-    # an event between two launches breaks their programmatic-dependent overlap, so
-    # recording them on every step would slow the very loop being timed.
-    every = max(1, args.steps // 100)
-    sampled = list(range(0, args.steps, every))
-    ev = {i: tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for i in sampled}
     # Decode-only batches run the step as one call that appends each sequence's new
     # row inside the decode kernel; a mixed batch appends its chunk rows first.
     fused = chunk is None
 
-    def step(i=None):
-        if i is not None:
-            ev[i][0].record(stream)
+    def step(ev=None):
+        """One step; `ev` (four CUDA events) splits it into append / chunk / decode."""
+        if ev is not None:
+            ev[0].record(stream)
         if not fused:
             P.kv_reshape_and_cache(new_k, new_v, k_cache, v_cache, slots)
-        if i is not None:
-            ev[i][1].record(stream)
+        if ev is not None:
+            ev[1].record(stream)
         if chunk is not None:
             P.paged_attention_prefill_chunk(cout, cq, ccu, cmax, k_cache, v_cache, ctab, clen, wl.scale,
                                             workspace=cws)
-        if i is not None:
-            ev[i][2].record(stream)
+        if ev is not None:
+            ev[2].record(stream)
         if fused:
             P.paged_attention_decode_append(out, q, new_k, new_v, k_cache, v_cache, tables, lens, wl.scale,
                                             workspace=ws)
         else:
             P.paged_attention_decode(out, q, k_cache, v_cache, tables, lens, wl.scale, workspace=ws)
-        if i is not None:
-            ev[i][3].record(stream)
+        if ev is not None:
+            ev[3].record(stream)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
 
+    # The clock sampler runs for the whole bench; each timed region marks its window.
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
     barrier(dist)
     torch.cuda.synchronize(dev)
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    # A batch whose bytes fit in L2 twice over is timed step by step with L2
-    # flushed (a write larger than L2) between steps, outside each step's events.
+    # A batch whose bytes fit in L2 twice over is timed step by step with L2 flushed
+    # (a write larger than L2, then a read) between steps, outside each step's events;
+    # a larger one back to back between two events, with nothing recorded in between
+    # (an event between two launches would cost them their programmatic-dependent overlap).
     small = kv_bytes + chunk_kv_bytes < 2 * L2_BYTES
-    if small:
-        # the write evicts the inputs; the read of a second buffer then evicts the
-        # written (dirty) lines, so their write-back does not land inside the step
-        flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
-        flush_rd = torch.zeros(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
-        flush_sink = torch.empty((), dtype=torch.float32, device=dev)
-        step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                   for _ in range(args.steps)]
+    flush = _L2Flush(torch, dev) if small else None
     w0 = time.time()
-    start.record(stream)
-    for i in range(args.steps):
-        if small:
-            flush_buf.zero_()
-            torch.sum(flush_rd, 0, out=flush_sink)
-            step_ev[i][0].record(stream)
-        step(i if i % every == 0 else None)
-        if small:
-            step_ev[i][1].record(stream)
-    end.record(stream)
-    torch.cuda.synchronize(dev)
+    total_ms = _timed_loop(torch, stream, step, args.steps, flush)
     w1 = time.time()
     barrier(dist)
     clocks.mark(w0, w1)
-    time.sleep(0.3)
-    clocks.stop()
-
-    total_ms = sum(a.elapsed_time(b) for a, b in step_ev) if small else start.elapsed_time(end)
-    decode_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev.values())
-    prefill_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev.values()) if chunk is not None else None
-    append_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev.values())
     t_max = max_over_ranks(total_ms / 1e3, dist, device=dev)
     ms_per_step = t_max / args.steps * 1e3
     value = world * (kv_bytes + chunk_kv_bytes) * args.steps / t_max / 1e9
+
+    # Per-kernel times from a separate sampled pass (events between the calls).
+    nsample = max(20, min(args.steps, 100))
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(nsample)]
+    for e in evs:
+        if flush is not None:
+            flush()
+        step(e)
+    torch.cuda.synchronize(dev)
+    append_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    prefill_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) if chunk is not None else None
+    decode_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
     st = int(ws[:4].view(torch.int32).item()) & 0xFFFFFFFF
     if st:
         raise RuntimeError(f"device status word set during the bench: {st:#x}")
@@ -419,25 +412,30 @@ def run_ours(args):
         def fp8_chunk(k8, v8, ks, vs):
             """The causal chunks over the FP8 copy of the pool."""
             ms = _time_events(torch, stream, lambda: P.paged_attention_prefill_chunk(
-                cout, cq, ccu, cmax, k8, v8, ctab, clen, wl.scale, workspace=cws, k_scale=ks, v_scale=vs),
-                min(args.steps, 200))
+                cout, cq, ccu, cmax, k8, v8, ctab, clen, wl.scale, workspace=cws, k_scale=ks, v_scale=vs), 200)
             return {"avg_launch_ms": round(ms, 5), "tflops": round(chunk_flops / ms / 1e9, 2),
                     "frac_of_bf16": round(chunk_flops / ms / 1e9 / _bf16_peak()[0], 4),
                     "time_vs_bf16_cache": round(ms / prefill_ms, 3)}
     rows = _row_variants(P, torch, dev, wl, batch, k_cache, v_cache, new_k, new_v, slots, q, tables, lens,
-                         decode_ms, kv_bytes, steps=min(args.steps, 200), fused=fused,
+                         decode_ms, kv_bytes, steps=200, fused=fused,
                          fp8_chunk=fp8_chunk) if world == 1 else None
 
     if rows is not None and chunk is not None:
         # the causal chunks under a 512-token window (each row sees its newest 512 keys)
         pw = 512
         mpw = _time_events(torch, stream, lambda: P.paged_attention_prefill_chunk(
-            cout, cq, ccu, cmax, k_cache, v_cache, ctab, clen, wl.scale, workspace=cws, window=pw),
-            min(args.steps, 200))
+            cout, cq, ccu, cmax, k_cache, v_cache, ctab, clen, wl.scale, workspace=cws, window=pw), 200)
         fw = _chunk_flops(chunk, wl, window=pw)
         rows["window_prefill"] = {"window": pw, "algorithmic_flops": fw, "avg_launch_ms": round(mpw, 5),
                                   "tflops": round(fw / mpw / 1e9, 2), "frac_of_bf16": round(fw / mpw / 1e9 / _bf16_peak()[0], 4),
                                   "time_vs_unwindowed": round(mpw / prefill_ms, 3)}
+    # the other workloads of the five configurations, each timed the same way (one GPU)
+    configs = None
+    if world == 1 and args.configs:
+        del h_in, d_set, d_out, h_out, d_cout, hc_out
+        torch.cuda.empty_cache()
+        configs = _config_rows(P, torch, dev, clocks, skip=args.workload)
+    clocks.stop()
 
     if rank == 0:
         peak, peak_src = measured_peaks()
@@ -474,18 +472,197 @@ def run_ours(args):
                          if peak_src == "measured" else "fallback 6.8 TB/s",
                          "traffic": _profiled_traffic(args.workload),
                          "bytes_per_launch": kv_bytes, "avg_launch_ms": round(decode_ms, 5),
-                         "append_avg_ms": round(append_ms, 5)},
+                         "append_avg_ms": round(append_ms, 5),
+                         "timing": f"CUDA events around each call on {nsample} steps after the timed loop"},
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": bi,
                     "d2h_bytes_per_step": bo, "ms_per_step": round(e2e_t / args.steps * 1e3, 5)},
             "prefill": None if chunk is None else _prefill_report(chunk_flops, prefill_ms, chunk, wl),
             "rows": rows,
+            "configs": configs,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks.summary(),
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+class _L2Flush:
+    """Evicts L2 between steps: a write larger than L2, then a read of another
+    buffer that large, so the written (dirty) lines are written back before the
+    next step rather than during it."""
+
+    def __init__(self, torch, dev):
+        self.buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+        self.rd = torch.zeros(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+        self.sink = torch.empty((), dtype=torch.float32, device=dev)
+        self.torch = torch
+
+    def __call__(self):
+        self.buf.zero_()
+        self.torch.sum(self.rd, 0, out=self.sink)
+
+
+def _timed_loop(torch, stream, fn, steps, flush=None):
+    """Total ms of `steps` calls of fn().  Without `flush`: back to back between two
+    events.  With it: L2 flushed before every call, outside per-call events."""
+    if flush is None:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in ev:
+        flush()
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in ev)
+
+
+def _config_rows(P, torch, dev, clocks, skip=None):
+    """Throughput of the five configurations' other workloads on one GPU.
+
+    Structure (contexts, block tables, slots, shared prefix) is each workload's
+    own (workloads.py, structure only); q, K/V and the new rows are N(0,1) draws
+    rounded to bf16 from a seeded device generator, so building a 1.3 GB pool
+    takes milliseconds instead of the host draw's minute.  Each row's timed
+    region is sized to about 0.3 s so the clock sampler sees it."""
+    peak, _ = measured_peaks()
+    bpeak, _ = _bf16_peak()
+    stream = torch.cuda.current_stream(dev)
+    res = {}
+    for name in ("llama3_70b_b8_32k", "llama3_70b_b1_128k", "sweep_mha", "sweep_gqa", "sweep_mqa", "mixed", "tiny"):
+        if name == skip:
+            continue
+        wl = W.make_workload(name, values=False)
+        g = torch.Generator(device=dev)
+        g.manual_seed(W._FAMILY_SEED[name])
+
+        def randn(*shape):
+            return torch.randn(shape, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+
+        def i32(a):
+            return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+
+        b = wl.decode
+        B = b.num_seqs
+        q = randn(B, wl.n_q, wl.head_dim)  # drawn first: the sweep's three variants share it
+        shape = (wl.num_blocks, wl.n_kv, wl.block_size, wl.head_dim)
+        kc, vc = randn(*shape), randn(*shape)
+        tab, ln = i32(b.block_tables), i32(b.context_lens)
+        nk, nv = randn(B, wl.n_kv, wl.head_dim), randn(B, wl.n_kv, wl.head_dim)
+        out = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+        desc = P.cache_desc(kc)
+        ws = torch.zeros(P.paged_attention_workspace_size(B, wl.n_q, b.max_blocks_per_seq, 0, desc),
+                         dtype=torch.uint8, device=dev)
+        nparts = P.paged_attention_decode_partitions(B, wl.n_q, b.max_blocks_per_seq, 0, desc)
+        ctx = b.context_lens.astype(np.int64)
+        dec_bytes = int(ctx.sum()) * wl.n_kv * wl.head_dim * 2 * 2
+        row = {"n_q": wl.n_q, "n_kv": wl.n_kv, "num_seqs": B, "context_min": int(ctx.min()),
+               "context_max": int(ctx.max()), "partitions_per_sequence": nparts}
+        ch = wl.chunk
+        if ch is None:
+            def step():
+                P.paged_attention_decode_append(out, q, nk, nv, kc, vc, tab, ln, wl.scale, workspace=ws)
+            step_bytes = dec_bytes
+        else:
+            rows_c = int(ch.cu_q_lens[-1])
+            cq, ccu, ctab, clen = (randn(rows_c, wl.n_q, wl.head_dim), i32(ch.cu_q_lens), i32(ch.block_tables),
+                                   i32(ch.context_lens))
+            cout = torch.empty(cq.shape, dtype=torch.bfloat16, device=dev)
+            cws = torch.zeros(256, dtype=torch.uint8, device=dev)
+            cmax = int(ch.q_lens.max())
+            tk, tv = randn(len(wl.slot_mapping), wl.n_kv, wl.head_dim), randn(len(wl.slot_mapping), wl.n_kv,
+                                                                             wl.head_dim)
+            sl = i32(wl.slot_mapping)
+            step_bytes = dec_bytes + wl.kv_read_bytes(ch)
+
+            def step(ev=None):
+                if ev is not None:
+                    ev[0].record(stream)
+                P.kv_reshape_and_cache(tk, tv, kc, vc, sl)
+                if ev is not None:
+                    ev[1].record(stream)
+                P.paged_attention_prefill_chunk(cout, cq, ccu, cmax, kc, vc, ctab, clen, wl.scale, workspace=cws)
+                if ev is not None:
+                    ev[2].record(stream)
+                P.paged_attention_decode(out, q, kc, vc, tab, ln, wl.scale, workspace=ws)
+                if ev is not None:
+                    ev[3].record(stream)
+        small = step_bytes < 2 * L2_BYTES
+        flush = _L2Flush(torch, dev) if small else None
+        for _ in range(5):
+            step()
+        torch.cuda.synchronize()
+        probe = _timed_loop(torch, stream, step, 5, flush) / 5
+        steps = int(min(20000, max(20, 0.3 / max(probe * 1e-3 * (1.0 if flush is None else 3.0), 1e-6))))
+        w0 = time.time()
+        total = _timed_loop(torch, stream, step, steps, flush)
+        w1 = time.time()
+        ms = total / steps
+        row.update({"steps": steps, "step_ms": round(ms, 5),
+                    "l2": "flushed before every step" if small else "inputs larger than L2; back to back"})
+        if ch is None:
+            row.update({"kv_read_bytes": dec_bytes, "gbs": round(dec_bytes / ms / 1e6, 2),
+                        "frac_of_hbm": round(dec_bytes / ms / 1e6 / peak, 4),
+                        "sequences_per_s": round(B / ms * 1e3, 1), "step": "paged_attention_decode_append"})
+            if not small:  # the decode call alone, events around each call
+                mc = _time_events(torch, stream, step, 100)
+                row.update({"call_ms": round(mc, 5), "call_frac_of_hbm": round(dec_bytes / mc / 1e6 / peak, 4)})
+        else:
+            evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(100)]
+            for e in evs:
+                step(e)
+            torch.cuda.synchronize()
+            t_app = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+            t_pre = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+            t_dec = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+            flops = _chunk_flops(ch, wl)
+            shared = len(wl.shared_prefix_seqs)
+            uniq = dec_bytes - max(0, shared - 1) * 1024 * wl.n_kv * wl.head_dim * 2 * 2
+            row.update({"step": "kv_reshape_and_cache + paged_attention_prefill_chunk + paged_attention_decode",
+                        "kv_read_bytes": step_bytes, "gbs": round(step_bytes / ms / 1e6, 2),
+                        "append_ms": round(t_app, 5),
+                        "prefill": {"ms": round(t_pre, 5), "algorithmic_flops": flops,
+                                    "tflops": round(flops / t_pre / 1e9, 2),
+                                    "frac_of_bf16": round(flops / t_pre / 1e9 / bpeak, 4)},
+                        "decode": {"ms": round(t_dec, 5), "logical_bytes": dec_bytes, "unique_bytes": uniq,
+                                   "gbs_logical": round(dec_bytes / t_dec / 1e6, 2),
+                                   "frac_of_hbm_unique": round(uniq / t_dec / 1e6 / peak, 4)}})
+        if name.startswith("llama3_70b"):  # the FP8 cache on the same batch
+            nb_ = wl.num_blocks
+            k8 = torch.empty(shape, dtype=torch.uint8, device=dev)
+            v8 = torch.empty_like(k8)
+            ks = torch.empty(shape[:3], dtype=torch.float32, device=dev)
+            vs = torch.empty_like(ks)
+            all_slots = torch.arange(nb_ * wl.block_size, dtype=torch.int32, device=dev)
+            P.kv_reshape_and_cache_fp8(kc.permute(0, 2, 1, 3).reshape(-1, wl.n_kv, wl.head_dim).contiguous(),
+                                       vc.permute(0, 2, 1, 3).reshape(-1, wl.n_kv, wl.head_dim).contiguous(),
+                                       k8, v8, ks, vs, all_slots)
+            ws8 = torch.zeros(P.paged_attention_workspace_size(B, wl.n_q, b.max_blocks_per_seq, 0, P.cache_desc(k8)),
+                              dtype=torch.uint8, device=dev)
+            m8 = _time_events(torch, stream, lambda: P.paged_attention_decode(out, q, k8, v8, tab, ln, wl.scale,
+                                                                              workspace=ws8, k_scale=ks, v_scale=vs),
+                              200)
+            b8 = int(ctx.sum()) * wl.n_kv * (2 * wl.head_dim + 2 * 4)
+            row["fp8_decode"] = {"bytes_per_launch": b8, "avg_launch_ms": round(m8, 5),
+                                 "gbs": round(b8 / m8 / 1e6, 2), "frac_of_hbm": round(b8 / m8 / 1e6 / peak, 4)}
+            del k8, v8, ks, vs, ws8, all_slots
+        row["clocks"] = clocks.summary((w0, w1))
+        st = int(ws[:4].view(torch.int32).item()) & 0xFFFFFFFF
+        if st:
+            raise RuntimeError(f"device status word set during the {name} row: {st:#x}")
+        res[name] = row
+        del kc, vc, q, out, ws
+        flush = None
+        torch.cuda.empty_cache()
+    return res
 
 
 def _time_events(torch, stream, fn, steps, warmup=3):
@@ -724,6 +901,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=W.WORKLOAD_NAMES)
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=120.0, help="seconds of oracle time for --impl reference")
+    ap.add_argument("--no-configs", dest="configs", action="store_false",
+                    help="skip the rows of the other workloads (one GPU only)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

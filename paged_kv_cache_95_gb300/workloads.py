@@ -75,9 +75,13 @@ _FAMILY_SEED = {
 
 def bf16_bits_from_f32(x: np.ndarray) -> np.ndarray:
     """Round float32 values to bf16 (round to nearest, ties to even); return the bits."""
-    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
-    return u.astype(np.uint16)
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    r = ((u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)).astype(np.uint16)
+    big = u > np.uint32(0xFFFF7FFF)  # (negative NaNs) the 32-bit sum would wrap: redo those in 64 bits
+    if big.any():
+        w = u[big].astype(np.uint64)
+        r[big] = ((w + 0x7FFF + ((w >> 16) & 1)) >> 16).astype(np.uint16)
+    return r
 
 
 def f32_from_bf16_bits(b: np.ndarray) -> np.ndarray:
@@ -151,7 +155,7 @@ class _SeqSpec:
 
 
 def _build(name, rng, n_q, n_kv, specs, q_override=None, pool_blocks=None,
-           shared_prefix_blocks=0, materialize_logical=False, table_width=None):
+           shared_prefix_blocks=0, materialize_logical=False, table_width=None, values=True):
     d, bs = HEAD_DIM, BLOCK_SIZE
     nseq = len(specs)
     nblk = [math.ceil(s.ctx / bs) for s in specs]
@@ -183,6 +187,23 @@ def _build(name, rng, n_q, n_kv, specs, q_override=None, pool_blocks=None,
     block_tables = np.full((nseq, width), poison_block, dtype=np.int32)
     for i, t in enumerate(tables):
         block_tables[i, :len(t)] = t
+
+    if not values:
+        # Structure only (the physical placement above was drawn first, so tables,
+        # lengths and slots equal those of the full build); no K/V/q values.
+        slots = []
+        for i, s in enumerate(specs):
+            npos = np.arange(s.ctx - s.q_len, s.ctx)
+            slots.append((block_tables[i, npos // bs].astype(np.int64) * bs + npos % bs).astype(np.int32))
+        cu = np.zeros(nseq + 1, dtype=np.int32)
+        cu[1:] = np.cumsum([s.q_len for s in specs])
+        batch = Batch(q=None, cu_q_lens=cu, block_tables=block_tables,
+                      context_lens=np.array([s.ctx for s in specs], dtype=np.int32))
+        wl = Workload(name=name, n_q=n_q, n_kv=n_kv, head_dim=d, block_size=bs, num_blocks=pool_blocks,
+                      poison_block=poison_block, k_cache=None, v_cache=None, new_key=None, new_value=None,
+                      slot_mapping=np.concatenate(slots).astype(np.int32),
+                      scale=float(np.float32(1.0 / math.sqrt(d))))
+        return wl, batch
 
     k_cache = np.full((pool_blocks, n_kv, bs, d), BF16_NAN, dtype=np.uint16)
     v_cache = np.full((pool_blocks, n_kv, bs, d), BF16_NAN, dtype=np.uint16)
@@ -244,7 +265,7 @@ def _split_batch(batch: Batch, idx: np.ndarray) -> Batch:
     cu = np.zeros(len(idx) + 1, dtype=np.int32)
     cu[1:] = np.cumsum(q_lens[idx])
     used = int(max(math.ceil(int(batch.context_lens[i]) / BLOCK_SIZE) for i in idx))
-    return Batch(q=np.ascontiguousarray(batch.q[rows]), cu_q_lens=cu,
+    return Batch(q=None if batch.q is None else np.ascontiguousarray(batch.q[rows]), cu_q_lens=cu,
                  block_tables=np.ascontiguousarray(batch.block_tables[idx, :used]),
                  context_lens=np.ascontiguousarray(batch.context_lens[idx]),
                  logical_k=None if batch.logical_k is None else [batch.logical_k[i] for i in idx],
@@ -252,11 +273,13 @@ def _split_batch(batch: Batch, idx: np.ndarray) -> Batch:
 
 
 def make_workload(name: str, seed: Optional[int] = None, materialize_logical: bool = False,
-                  batch_scale: float = 1.0) -> Workload:
+                  batch_scale: float = 1.0, values: bool = True) -> Workload:
     """Build one named workload.  ``seed`` defaults to 1000 + family index.
 
     ``batch_scale`` < 1 keeps the same per-sequence structure but fewer
     sequences (used for bounded CPU samples); 1.0 is the full workload.
+    ``values=False`` builds the structure alone (contexts, block tables, slot
+    mapping, identical to the full build's) and leaves K/V/q to the caller.
     """
     if name not in _FAMILY_SEED:
         raise ValueError(f"unknown workload {name!r}; expected one of {WORKLOAD_NAMES}")
@@ -269,25 +292,25 @@ def make_workload(name: str, seed: Optional[int] = None, materialize_logical: bo
     if name == "tiny":
         specs = [_SeqSpec(10, 1), _SeqSpec(17, 1)]
         wl, b = _build(name, rng, 32, 8, specs, pool_blocks=16,
-                       materialize_logical=materialize_logical)
+                       materialize_logical=materialize_logical, values=values)
         wl.decode = b
         return wl
 
     if name == "llama3_8b_b64":
         ctx = rng.integers(512, 4096, size=nb(64), endpoint=True)
         specs = [_SeqSpec(int(c), 1) for c in ctx]
-        wl, b = _build(name, rng, 32, 8, specs, materialize_logical=materialize_logical)
+        wl, b = _build(name, rng, 32, 8, specs, materialize_logical=materialize_logical, values=values)
         wl.decode = b
         return wl
 
     if name.startswith("sweep_"):
         n_kv = {"sweep_mha": 32, "sweep_gqa": 8, "sweep_mqa": 1}[name]
         B = nb(32)
-        q = _normal_bf16(rng, (B, 32, HEAD_DIM))  # identical across the three variants
+        q = _normal_bf16(rng, (B, 32, HEAD_DIM)) if values else None  # identical across the three variants
         sub = np.random.default_rng([seed, n_kv])
         specs = [_SeqSpec(2048, 1) for _ in range(B)]
         wl, b = _build(name, sub, 32, n_kv, specs, q_override=q,
-                       materialize_logical=materialize_logical)
+                       materialize_logical=materialize_logical, values=values)
         wl.decode = b
         return wl
 
@@ -295,7 +318,7 @@ def make_workload(name: str, seed: Optional[int] = None, materialize_logical: bo
         B, ctx = (8, 32768) if name.endswith("32k") else (1, 131072)
         sub = np.random.default_rng([seed, B])
         specs = [_SeqSpec(ctx, 1) for _ in range(nb(B))]
-        wl, b = _build(name, sub, 64, 8, specs, materialize_logical=materialize_logical)
+        wl, b = _build(name, sub, 64, 8, specs, materialize_logical=materialize_logical, values=values)
         wl.decode = b
         return wl
 
@@ -309,7 +332,7 @@ def make_workload(name: str, seed: Optional[int] = None, materialize_logical: bo
         for i, c in enumerate(dec_ctx):
             specs.append(_SeqSpec(int(c), 1, prefix_group=0 if i in set(shared.tolist()) else None))
         wl, full = _build(name, rng, 32, 8, specs, shared_prefix_blocks=1024 // BLOCK_SIZE,
-                          materialize_logical=materialize_logical)
+                          materialize_logical=materialize_logical, values=values)
         wl.chunk = _split_batch(full, np.arange(n_chunk))
         wl.decode = _split_batch(full, np.arange(n_chunk, n_chunk + n_dec))
         wl.shared_prefix_seqs = [int(i) for i in shared]
