@@ -386,11 +386,30 @@ PKV_API int paged_attention_decode_fp8(void *out, int32_t out_dtype, const void 
                                        size_t workspace_bytes, void *stream);
 
 /*
- * paged_attention_prefill_workspace_size -- bytes of workspace that
- * paged_attention_prefill_chunk needs (the status word).  Needs no GPU.
+ * paged_attention_prefill_workspace_size -- the least workspace that
+ * paged_attention_prefill_chunk accepts: the status word (256 bytes).  With
+ * it the kernel runs one CTA per (KV head, sequence, pair of 128-row tiles).
+ * Needs no GPU.
  */
 PKV_API size_t paged_attention_prefill_workspace_size(int32_t num_seqs, int32_t num_q_heads,
                                               const pkv_cache_desc *cache);
+
+/*
+ * paged_attention_prefill_chunk_workspace_size -- the workspace with which
+ * paged_attention_prefill_chunk (and its _window / _fp8 forms) may split the
+ * keys (split-KV) for these sizes on the current device: when its CTAs would
+ * not fill the GPU (few sequences, short chunks, long contexts), each pair of
+ * row tiles walks 2..16 key ranges in separate CTAs whose partials (m, l, O)
+ * a log-sum-exp merge folds ("LLM 推理全过程的维度变化与核心公式", section "工程
+ * 优化怎么嵌进公式", Flash-Decoding, applied to a chunk's rows).  The result does
+ * not depend on the split beyond float rounding.  Layout [status 256 B | m | l |
+ * O], fp32 partials of total_q_rows x num_q_heads rows per split; 256 bytes
+ * (no split) when the CTAs already fill the GPU.  Reads the current device's
+ * SM count (152 assumed without a GPU).  Returns 0 for invalid arguments.
+ */
+PKV_API size_t paged_attention_prefill_chunk_workspace_size(int32_t num_seqs, int32_t num_q_heads,
+                                                            int32_t total_q_rows, int32_t max_q_len,
+                                                            int32_t max_blocks_per_seq, const pkv_cache_desc *cache);
 
 /*
  * paged_attention_prefill_chunk -- causal attention of a chunk of new query
@@ -412,7 +431,11 @@ PKV_API size_t paged_attention_prefill_workspace_size(int32_t num_seqs, int32_t 
  *   cu_q_lens  : int32 [num_seqs + 1], device, non-decreasing, cu_q_lens[0] = 0
  *   max_q_len  : host upper bound of every q_len (sizes the launch grid)
  *   total_q_rows : host value of cu_q_lens[num_seqs] (bounds the q/out tensors)
- *   workspace  : >= paged_attention_prefill_workspace_size() bytes (status word)
+ *   workspace  : device, 256-B aligned, >= paged_attention_prefill_workspace_size()
+ *                bytes (the status word); with at least
+ *                paged_attention_prefill_chunk_workspace_size() bytes for the
+ *                same sizes the call may split the keys (and then launches the
+ *                merge kernel after the prefill kernel)
  * Uses the 5th-generation tensor cores (tcgen05, accumulators in tensor memory).
  * Errors: PKV_ERR_INVALID_ARG (null or misaligned pointer, bad size) /
  *         PKV_ERR_UNSUPPORTED (group size not in {1,2,4,8,16}, more than 65535
@@ -501,6 +524,44 @@ PKV_API int paged_attention_prefill_chunk_fp8(void *out, int32_t out_dtype, cons
 PKV_API size_t paged_attention_verify_workspace_size(int32_t num_seqs, int32_t q_per_seq, int32_t num_q_heads,
                                                      int32_t max_blocks_per_seq, int32_t partition_size,
                                                      const pkv_cache_desc *cache);
+/*
+ * The kernel a verify call runs on: PKV_VERIFY_AUTO lets the measured rule
+ * above choose; the other two force one (the prefill kernel only for G in
+ * {1, 2, 4, 8, 16}).  The result does not depend on the kernel beyond float
+ * rounding.
+ */
+#define PKV_VERIFY_AUTO (-1)
+#define PKV_VERIFY_DECODE_KERNEL 0
+#define PKV_VERIFY_PREFILL_KERNEL 1
+
+/*
+ * paged_attention_verify_workspace_size_on / paged_attention_verify_on --
+ * paged_attention_verify_workspace_size and paged_attention_verify (with the
+ * sliding window and the FP8 cache of _window / _fp8: window 0 for none,
+ * k_scale and v_scale NULL for a bf16 cache) on the kernel `kernel` chooses.
+ * Workspace: paged_attention_verify_workspace_size_on() for the same kernel.
+ * Errors: as paged_attention_verify; PKV_ERR_UNSUPPORTED for the prefill
+ * kernel with a group size it cannot pack; the size query returns 0.
+ */
+PKV_API size_t paged_attention_verify_workspace_size_on(int32_t kernel, int32_t num_seqs, int32_t q_per_seq,
+                                                        int32_t num_q_heads, int32_t max_blocks_per_seq,
+                                                        int32_t partition_size, const pkv_cache_desc *cache);
+PKV_API int paged_attention_verify_on(int32_t kernel, void *out, int32_t out_dtype, const void *q, int32_t q_per_seq,
+                                      const void *k_cache, const void *v_cache, const float *k_scale,
+                                      const float *v_scale, const int32_t *block_tables,
+                                      const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                      int32_t max_blocks_per_seq, float scale, int32_t window,
+                                      int32_t partition_size, const pkv_cache_desc *cache, void *workspace,
+                                      size_t workspace_bytes, void *stream);
+
+/*
+ * paged_attention_verify_on_prefill -- the kernel paged_attention_verify (and
+ * _window / _fp8, per cache->dtype) takes for these sizes on the current
+ * device: 1 the tcgen05 prefill kernel, 0 the decode kernel; a negative
+ * PKV_ERR_* for invalid arguments.  Needs no GPU (152 SMs assumed).
+ */
+PKV_API int paged_attention_verify_on_prefill(int32_t num_seqs, int32_t q_per_seq, int32_t num_q_heads,
+                                              const pkv_cache_desc *cache);
 PKV_API int paged_attention_verify(void *out, int32_t out_dtype, const void *q, int32_t q_per_seq, const void *k_cache,
                                    const void *v_cache, const int32_t *block_tables, const int32_t *context_lens,
                                    int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq, float scale,

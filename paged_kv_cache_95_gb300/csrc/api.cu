@@ -178,6 +178,21 @@ int check_group(int32_t n_q, int32_t n_kv) {
     return PKV_OK;
 }
 
+// Query heads (MMA columns) per decode CTA and 8-column tiles per block group: a
+// group of up to 8 heads fills one tile; groups of 16 and 32 heads (and their
+// multiples) run as 2 or 4 tiles side by side in one CTA, one per warp of a
+// block group, so each K/V tile still leaves HBM once per KV head.
+struct DecodeTiles {
+    int32_t heads_per_cta, col_tiles, head_splits;
+};
+DecodeTiles decode_tiles(int32_t G) {
+    DecodeTiles t{G < 8 ? G : 8, 1, 1};
+    if (G % 32 == 0) t = {32, 4, 1};
+    else if (G % 16 == 0) t = {16, 2, 1};
+    t.head_splits = G / t.heads_per_cta;
+    return t;
+}
+
 // ---- decode plan -----------------------------------------------------------------------
 // Workspace layout: [status word | part_m | part_l | part_o], each region
 // 256-byte aligned; only the status word when nothing is split.
@@ -347,7 +362,7 @@ int32_t paged_attention_decode_partitions(int32_t num_seqs, int32_t num_q_heads,
                                           max_blocks_per_seq, (static_cast<int64_t>(window) + 15) / kBlockSize + 1))
                                     : max_blocks_per_seq;
     const int32_t G = num_q_heads / cache->num_kv_heads;
-    const int32_t head_splits = G / (G < 8 ? G : 8);
+    const int32_t head_splits = decode_tiles(G).head_splits;
     int32_t pb = partition_size / kBlockSize;
     if (partition_size == 0) {
         const int dev = current_device();
@@ -399,8 +414,9 @@ int decode_impl(void *out, int32_t out_dtype, const void *q, const void *k_cache
 
     const int32_t n_kv = cache->num_kv_heads;
     const int32_t G = num_q_heads / n_kv;
-    const int32_t hpc = G < 8 ? G : 8;
-    const int32_t head_splits = G / hpc;
+    const DecodeTiles tiles = decode_tiles(G);
+    const int32_t hpc = tiles.heads_per_cta;
+    const int32_t head_splits = tiles.head_splits;
     if (static_cast<int64_t>(n_kv) * head_splits > 65535) return PKV_ERR_UNSUPPORTED;
 
     const int dev = current_device();
@@ -443,6 +459,7 @@ int decode_impl(void *out, int32_t out_dtype, const void *q, const void *k_cache
     p.group = G;
     p.heads_per_cta = hpc;
     p.head_splits = head_splits;
+    p.col_tiles = tiles.col_tiles;
     p.max_blocks = max_blocks_per_seq;
     p.num_blocks = cache->num_blocks;
     p.part_blocks = pl.part_blocks;
@@ -525,6 +542,74 @@ size_t paged_attention_prefill_workspace_size(int32_t num_seqs, int32_t num_q_he
 
 namespace {
 
+// Split-KV plan of the prefill kernel.  Its CTAs (one per KV head, sequence and
+// pair of 128-row tiles; one CTA per SM) can be too few to fill the GPU -- a
+// long chunk of one or two sequences, or a verify of few sequences -- and then
+// each pair's key tiles are cut into `splits` ranges whose partials (m, l, O)
+// the merge kernel folds ("LLM 推理全过程的维度变化与核心公式", section "工程优化
+// 怎么嵌进公式": Flash-Decoding's split of cache_len and log-sum-exp reduction
+// apply to the rows of a chunk alike).  The count is chosen from the sizes
+// alone (context lengths are device data): at least 8 key tiles of the longest
+// possible context per split, and the number of waves of CTAs closest to whole.
+// Workspace: [status | part_m | part_l | part_o], each region 256-byte aligned.
+struct PrefillPlan {
+    int32_t splits;
+    size_t off_m, off_l, off_o, total;
+};
+PrefillPlan plan_prefill(int32_t num_seqs, int32_t n_q, int32_t n_kv, int32_t total_rows, int32_t max_q_len,
+                         int32_t max_blocks, int64_t sms) {
+    PrefillPlan pl{1, kStatusBytes, kStatusBytes, kStatusBytes, kStatusBytes};
+    const int32_t G = n_q / n_kv;
+    if (G < 1 || 128 % G != 0 || max_q_len < 1 || total_rows < 1) return pl;
+    const int64_t tiles = (static_cast<int64_t>(max_q_len) + 128 / G - 1) / (128 / G);
+    const int64_t units = static_cast<int64_t>(n_kv) * num_seqs * ((tiles + 1) / 2);
+    const int64_t key_tiles = (static_cast<int64_t>(max_blocks) * kBlockSize + 127) / 128;
+    const int64_t max_splits = std::min<int64_t>(16, key_tiles / 8);
+    if (sms < 1 || units >= sms || max_splits < 2) return pl;
+    double best = 0.0;
+    for (int64_t sp = 2; sp <= max_splits; ++sp) {
+        if (units * sp < sms) continue;
+        const double waves = static_cast<double>(units * sp) / static_cast<double>(sms);
+        const double eff = waves / std::ceil(waves);
+        if (eff > best + 1e-9) {
+            best = eff;
+            pl.splits = static_cast<int32_t>(sp);
+        }
+        if (eff >= 0.9) break;  // the fewest splits that fill the waves well
+    }
+    if (pl.splits <= 1) pl.splits = static_cast<int32_t>(max_splits);  // under one wave even so: take them all
+    if ((tiles + 1) / 2 * pl.splits > 65535) {  // grid z: pairs x splits
+        pl.splits = 1;
+        return pl;
+    }
+    const size_t rows = static_cast<size_t>(total_rows) * n_q * pl.splits;
+    pl.off_m = kStatusBytes;
+    pl.off_l = pl.off_m + align_up(rows * 4, 256);
+    pl.off_o = pl.off_l + align_up(rows * 4, 256);
+    pl.total = pl.off_o + align_up(rows * kHeadDim * 4, 256);
+    return pl;
+}
+
+int64_t device_sms_or_default() {
+    const int dev = current_device();
+    return dev >= 0 && dev < kMaxDevices ? sm_count(dev) : 152;
+}
+
+}  // namespace
+
+size_t paged_attention_prefill_chunk_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t total_q_rows,
+                                                    int32_t max_q_len, int32_t max_blocks_per_seq,
+                                                    const pkv_cache_desc *cache) {
+    if ((check_cache(cache) != PKV_OK && check_cache_fp8(cache) != PKV_OK) || num_seqs < 1 || max_blocks_per_seq < 1)
+        return 0;
+    if (check_group(num_q_heads, cache->num_kv_heads) != PKV_OK || total_q_rows < 0 || max_q_len < 0) return 0;
+    return plan_prefill(num_seqs, num_q_heads, cache->num_kv_heads, total_q_rows, max_q_len, max_blocks_per_seq,
+                        device_sms_or_default())
+        .total;
+}
+
+namespace {
+
 // Shared by the prefill-chunk and verify entry points.  cu_q_lens null: every sequence
 // has uniform_q_len rows (sequence b owns rows b * uniform_q_len ..).
 int prefill_impl(void *out, int32_t out_dtype, const void *q, const int32_t *cu_q_lens, int32_t uniform_q_len,
@@ -561,6 +646,11 @@ int prefill_impl(void *out, int32_t out_dtype, const void *q, const int32_t *cu_
 
     const int dev = current_device();
     if (dev < 0 || dev >= kMaxDevices) return PKV_ERR_CUDA;
+    // Split-KV when the CTAs cannot fill the GPU and the workspace holds the partials
+    // (a workspace of the status word alone keeps one CTA per pair of row tiles).
+    PrefillPlan pl = plan_prefill(num_seqs, num_q_heads, cache->num_kv_heads, total_q_rows, max_q_len,
+                                  max_blocks_per_seq, sm_count(dev));
+    if (pl.splits > 1 && workspace_bytes < pl.total) pl.splits = 1;
 
     CUtensorMap qmap, kmap, vmap, omap;
     if (!encode_rows_map(&qmap, q, total_q_rows, num_q_heads, G, false) ||
@@ -593,6 +683,11 @@ int prefill_impl(void *out, int32_t out_dtype, const void *q, const int32_t *cu_
     p.window = window;
     p.k_scale = k_scale;
     p.v_scale = fp8 ? v_scale : nullptr;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    p.kv_splits = pl.splits;
+    p.part_m = pl.splits > 1 ? reinterpret_cast<float *>(ws + pl.off_m) : nullptr;
+    p.part_l = pl.splits > 1 ? reinterpret_cast<float *>(ws + pl.off_l) : nullptr;
+    p.part_o = pl.splits > 1 ? reinterpret_cast<float *>(ws + pl.off_o) : nullptr;
     if (pkv::launch_prefill_chunk(qmap, kmap, vmap, omap, p, max_q_len, static_cast<cudaStream_t>(stream)) !=
         cudaSuccess)
         return PKV_ERR_CUDA;
@@ -673,9 +768,9 @@ int32_t verify_cols_per_cta(int32_t cols, bool fp8 = false) {
 
 }  // namespace
 
-size_t paged_attention_verify_workspace_size(int32_t num_seqs, int32_t q_per_seq, int32_t num_q_heads,
-                                             int32_t max_blocks_per_seq, int32_t partition_size,
-                                             const pkv_cache_desc *cache) {
+size_t paged_attention_verify_workspace_size_on(int32_t kernel, int32_t num_seqs, int32_t q_per_seq,
+                                                int32_t num_q_heads, int32_t max_blocks_per_seq,
+                                                int32_t partition_size, const pkv_cache_desc *cache) {
     if (!cache) return 0;
     const bool fp8 = cache->dtype == PKV_DTYPE_FP8_E4M3;
     if ((fp8 ? check_cache_fp8(cache) : check_cache(cache)) != PKV_OK || num_seqs < 1 || max_blocks_per_seq < 1)
@@ -683,10 +778,36 @@ size_t paged_attention_verify_workspace_size(int32_t num_seqs, int32_t q_per_seq
     if (q_per_seq < 1 || q_per_seq > kMaxVerifyRows) return 0;
     if (check_group(num_q_heads, cache->num_kv_heads) != PKV_OK) return 0;
     if (partition_size < 0 || partition_size % kBlockSize != 0) return 0;
+    if (kernel < PKV_VERIFY_AUTO || kernel > PKV_VERIFY_PREFILL_KERNEL) return 0;
     const int32_t G = num_q_heads / cache->num_kv_heads;
-    if (verify_on_prefill(fp8, num_seqs, q_per_seq, G, cache->num_kv_heads)) return kStatusBytes;
+    if (kernel == PKV_VERIFY_PREFILL_KERNEL && (G > 16 || 128 % G != 0)) return 0;
+    if (kernel == PKV_VERIFY_PREFILL_KERNEL ||
+        (kernel == PKV_VERIFY_AUTO && verify_on_prefill(fp8, num_seqs, q_per_seq, G, cache->num_kv_heads))) {
+        if (static_cast<int64_t>(num_seqs) * q_per_seq > INT32_MAX) return 0;
+        return plan_prefill(num_seqs, num_q_heads, cache->num_kv_heads, num_seqs * q_per_seq, q_per_seq,
+                            max_blocks_per_seq, route_sms())
+            .total;
+    }
     const int32_t pb = partition_size > 0 ? partition_size / kBlockSize : kMinPartBlocks;
     return plan_decode(num_seqs, num_q_heads, max_blocks_per_seq, pb, q_per_seq).total;
+}
+
+size_t paged_attention_verify_workspace_size(int32_t num_seqs, int32_t q_per_seq, int32_t num_q_heads,
+                                             int32_t max_blocks_per_seq, int32_t partition_size,
+                                             const pkv_cache_desc *cache) {
+    return paged_attention_verify_workspace_size_on(PKV_VERIFY_AUTO, num_seqs, q_per_seq, num_q_heads,
+                                                    max_blocks_per_seq, partition_size, cache);
+}
+
+int paged_attention_verify_on_prefill(int32_t num_seqs, int32_t q_per_seq, int32_t num_q_heads,
+                                      const pkv_cache_desc *cache) {
+    if (!cache) return PKV_ERR_INVALID_ARG;
+    const bool fp8 = cache->dtype == PKV_DTYPE_FP8_E4M3;
+    if (int rc = fp8 ? check_cache_fp8(cache) : check_cache(cache)) return rc;
+    if (int rc = check_group(num_q_heads, cache->num_kv_heads)) return rc;
+    if (num_seqs < 1 || q_per_seq < 1 || q_per_seq > kMaxVerifyRows) return PKV_ERR_INVALID_ARG;
+    return verify_on_prefill(fp8, num_seqs, q_per_seq, num_q_heads / cache->num_kv_heads, cache->num_kv_heads) ? 1
+                                                                                                                : 0;
 }
 
 namespace {
@@ -698,15 +819,18 @@ int verify_impl(void *out, int32_t out_dtype, const void *q, int32_t q_per_seq, 
                 const void *v_cache, const int32_t *block_tables, const int32_t *context_lens, int32_t num_seqs,
                 int32_t num_q_heads, int32_t max_blocks_per_seq, float scale, int32_t partition_size, int32_t window,
                 const pkv_cache_desc *cache, void *workspace, size_t workspace_bytes, void *stream,
-                const float *k_scale = nullptr, const float *v_scale = nullptr) {
+                const float *k_scale = nullptr, const float *v_scale = nullptr, int32_t kernel = PKV_VERIFY_AUTO) {
     if (window < 0) return PKV_ERR_INVALID_ARG;
     const bool fp8 = k_scale != nullptr;
     if (int rc = fp8 ? check_cache_fp8(cache) : check_cache(cache)) return rc;
     if (fp8 && (!v_scale || !aligned(k_scale, 16) || !aligned(v_scale, 16))) return PKV_ERR_INVALID_ARG;
     if (int rc = check_group(num_q_heads, cache->num_kv_heads)) return rc;
     if (q_per_seq < 1 || q_per_seq > kMaxVerifyRows) return PKV_ERR_INVALID_ARG;
+    if (kernel < PKV_VERIFY_AUTO || kernel > PKV_VERIFY_PREFILL_KERNEL) return PKV_ERR_INVALID_ARG;
     const int32_t G = num_q_heads / cache->num_kv_heads;
-    if (verify_on_prefill(fp8, num_seqs, q_per_seq, G, cache->num_kv_heads)) {
+    if (kernel == PKV_VERIFY_PREFILL_KERNEL && (G > 16 || 128 % G != 0)) return PKV_ERR_UNSUPPORTED;
+    if (kernel == PKV_VERIFY_PREFILL_KERNEL ||
+        (kernel == PKV_VERIFY_AUTO && verify_on_prefill(fp8, num_seqs, q_per_seq, G, cache->num_kv_heads))) {
         // Prefill kernel, uniform rows: sequence b owns q rows b * q_per_seq .. + q_per_seq - 1.
         if (static_cast<int64_t>(num_seqs) * q_per_seq > INT32_MAX) return PKV_ERR_INVALID_ARG;
         return prefill_impl(out, out_dtype, q, nullptr, q_per_seq, q_per_seq, num_seqs * q_per_seq, k_cache, v_cache,
@@ -723,8 +847,9 @@ int verify_impl(void *out, int32_t out_dtype, const void *q, int32_t q_per_seq, 
         !aligned(block_tables, 4) || !aligned(context_lens, 4))
         return PKV_ERR_INVALID_ARG;
     if (!workspace || !aligned(workspace, 256)) return PKV_ERR_INVALID_ARG;
-    if (workspace_bytes < paged_attention_verify_workspace_size(num_seqs, q_per_seq, num_q_heads, max_blocks_per_seq,
-                                                                partition_size, cache))
+    if (workspace_bytes < paged_attention_verify_workspace_size_on(PKV_VERIFY_DECODE_KERNEL, num_seqs, q_per_seq,
+                                                                   num_q_heads, max_blocks_per_seq, partition_size,
+                                                                   cache))
         return PKV_ERR_WORKSPACE_TOO_SMALL;
 
     const int32_t n_kv = cache->num_kv_heads;
@@ -777,6 +902,7 @@ int verify_impl(void *out, int32_t out_dtype, const void *q, int32_t q_per_seq, 
     p.group = G;
     p.heads_per_cta = verify_cols_per_cta(cols, fp8);  // the CTA's share of the q_per_seq x G columns
     p.head_splits = splits;
+    p.col_tiles = 1;
     p.max_blocks = max_blocks_per_seq;
     p.num_blocks = cache->num_blocks;
     p.part_blocks = pl.part_blocks;
@@ -821,6 +947,18 @@ int paged_attention_verify_window(void *out, int32_t out_dtype, const void *q, i
     return verify_impl(out, out_dtype, q, q_per_seq, k_cache, v_cache, block_tables, context_lens, num_seqs,
                        num_q_heads, max_blocks_per_seq, scale, partition_size, window, cache, workspace,
                        workspace_bytes, stream);
+}
+
+int paged_attention_verify_on(int32_t kernel, void *out, int32_t out_dtype, const void *q, int32_t q_per_seq,
+                              const void *k_cache, const void *v_cache, const float *k_scale, const float *v_scale,
+                              const int32_t *block_tables, const int32_t *context_lens, int32_t num_seqs,
+                              int32_t num_q_heads, int32_t max_blocks_per_seq, float scale, int32_t window,
+                              int32_t partition_size, const pkv_cache_desc *cache, void *workspace,
+                              size_t workspace_bytes, void *stream) {
+    if ((k_scale == nullptr) != (v_scale == nullptr)) return PKV_ERR_INVALID_ARG;
+    return verify_impl(out, out_dtype, q, q_per_seq, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                       num_q_heads, max_blocks_per_seq, scale, partition_size, window, cache, workspace,
+                       workspace_bytes, stream, k_scale, v_scale, kernel);
 }
 
 int paged_attention_verify_fp8(void *out, int32_t out_dtype, const void *q, int32_t q_per_seq, const void *k_cache,

@@ -141,7 +141,18 @@ __global__ void __launch_bounds__(NW * 32)
     if (part >= nparts) return;
     const int blk_begin = first_blk + part * p.part_blocks;
     const int nblk = min(p.part_blocks, nblocks - blk_begin);
-    const int nmine = nblk > warp ? (nblk - warp + NW - 1) / NW : 0;
+    // Block groups: the warps form NG = NW / T groups of T warps.  Group gi consumes
+    // blocks blk_begin + gi, + NG, ... through one ring of R = ST * T stages that its
+    // T warps all read; warp ti of the group owns the group's ti-th 8-column MMA tile
+    // (heads h0 + 8 ti ..).  T = 1 (groups of up to 8 heads): every warp is a group
+    // with its own ring.  T = 2, 4 (16, 32 heads): the CTA still reads each K/V tile
+    // from HBM once for the whole group.
+    const int T = VERIFY ? 1 : p.col_tiles;
+    const int NG = NW / T;
+    const int gi = warp / T, ti = warp - gi * T;
+    const int R = ST * T;
+    const bool producer = ti == 0;  // the group's first warp issues its copies
+    const int nmine = nblk > gi ? (nblk - gi + NG - 1) / NG : 0;
     const int32_t *table = p.block_tables + static_cast<size_t>(b) * p.max_blocks;
 
     // Append: lane l holds 16 bytes of the new row (K for lanes 0-15, V for 16-31;
@@ -155,22 +166,30 @@ __global__ void __launch_bounds__(NW * 32)
         }
     }
 
-    const uint32_t stage_base = smem_u32(smem) + warp * (ST * kStage);
-    // FP8: the scale rows of each stage sit after all warps' code rings.
-    const uint32_t scale_base = smem_u32(smem) + NW * ST * kStage + warp * (FP8 ? ST * kStageScaleBytes : 0);
-    const uint32_t bar_base = smem_u32(smem) + NW * ST * kStage + (FP8 ? NW * ST * kStageScaleBytes : 0) + warp * ST * 8;
+    // Shared memory: [stage rings (NW * ST stages) | FP8 scale rows | full barriers |
+    // empty barriers | append barriers (one per group)].
+    const uint32_t stage_base = smem_u32(smem) + gi * (R * kStage);
+    const uint32_t scale_base = smem_u32(smem) + NW * ST * kStage + gi * (FP8 ? R * kStageScaleBytes : 0);
+    const uint32_t bars = smem_u32(smem) + NW * ST * kStage + (FP8 ? NW * ST * kStageScaleBytes : 0);
+    const uint32_t bar_base = bars + gi * R * 8;                   // stage s full: its copies landed
+    const uint32_t empty_base = bars + NW * ST * 8 + gi * R * 8;   // stage s empty: T warps done with it
+    const uint32_t app_bar = bars + 2 * NW * ST * 8 + gi * 8;      // the appended row is in the stage
 
-    if (lane == 0) {
-        for (int s = 0; s < ST; ++s) mbar_init(bar_base + 8 * s, FP8 ? kFp8StageArrivals : 1);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NW * ST; ++s) {
+            mbar_init(bars + 8 * s, FP8 ? kFp8StageArrivals : 1);
+            mbar_init(bars + NW * ST * 8 + 8 * s, T);
+        }
+        for (int q = 0; q < NW; ++q) mbar_init(bars + 2 * NW * ST * 8 + 8 * q, 32);
         fence_mbar_init();
     }
-    __syncwarp();
+    __syncthreads();
     constexpr int kIssueLanes = FP8 ? 8 : 1;  // lanes that take part in a stage's copies
 
-    // Lanes < kIssueLanes: start the copies of this warp's i-th block into stage i % ST.
+    // Lanes < kIssueLanes of the producer: start the copies of the group's i-th block into stage i % R.
     auto issue = [&](int i) {
-        const int s = i % ST;
-        const int j = blk_begin + warp + NW * i;
+        const int s = i % R;
+        const int j = blk_begin + gi + NG * i;
         int phys = __ldg(table + j);
         if (static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_blocks)) phys = 0;  // masked below
         if constexpr (FP8)
@@ -179,8 +198,12 @@ __global__ void __launch_bounds__(NW * 32)
         else
             issue_block_copy(&kmap, &vmap, stage_base + s * kStage, bar_base + 8 * s, g, phys);
     };
-    if (lane < kIssueLanes)
-        for (int i = 0; i < ST && i < nmine; ++i) issue(i);
+    int issued = 0;
+    if (producer) {
+        issued = min(R, nmine);
+        if (lane < kIssueLanes)
+            for (int i = 0; i < issued; ++i) issue(i);
+    }
 
     // ---- Q^T as the B operand (16 dims x 8 heads per k-step), kept in registers ----
     const int n = lane >> 2;  // head column of B / row group of C
@@ -188,17 +211,18 @@ __global__ void __launch_bounds__(NW * 32)
     uint32_t bqt[NCT][8][2];
     auto &bq = bqt[0];
     float sl2 = p.scale_log2;
+    const int tcols = min(8, hpc - 8 * ti);  // decode: heads of this warp's tile
     if constexpr (FP8 && VERIFY) {
         const int qexp = load_q_frag_fp8_row(bq, p.q, col_row(n), n < ncols, lane);
         sl2 *= ldexpf(1.f, -qexp);
     } else if constexpr (FP8) {
-        const int qexp = load_q_frag_fp8(bq, p.q, static_cast<size_t>(b) * p.n_q + h0, hpc, lane);
+        const int qexp = load_q_frag_fp8(bq, p.q, static_cast<size_t>(b) * p.n_q + h0 + 8 * ti, tcols, lane);
         sl2 *= ldexpf(1.f, -qexp);
     } else if constexpr (VERIFY) {
 #pragma unroll
         for (int t = 0; t < NCT; ++t) load_q_frag_row(bqt[t], p.q, col_row(8 * t + n), 8 * t + n < ncols, lane);
     } else {
-        load_q_frag(bq, p.q, static_cast<size_t>(b) * p.n_q + h0, hpc, lane);
+        load_q_frag(bq, p.q, static_cast<size_t>(b) * p.n_q + h0 + 8 * ti, tcols, lane);
     }
     // Verify: the absolute causal bound (exclusive) of this lane's columns 8t + 2*q4 and 8t + 2*q4 + 1.
     int pos_end[NCT][2] = {};
@@ -218,37 +242,47 @@ __global__ void __launch_bounds__(NW * 32)
     int consumed = 0;
     bool timed_out = false;
     for (int i = 0; i < nmine; ++i) {
-        const int s = i % ST;
+        const int s = i % R;
         const uint32_t bar = bar_base + 8 * s;
-        bool ok = mbar_wait(bar, (i / ST) & 1);
+        bool ok = mbar_wait(bar, (i / R) & 1);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) {
             timed_out = true;
             break;
         }
-        const int j = blk_begin + warp + NW * i;
+        const int j = blk_begin + gi + NG * i;
         const int phys = __ldg(table + j);
         int valid = min(kBlockSize, ctx - j * kBlockSize);
         const int lo = j == first_blk ? j0 - j * kBlockSize : 0;
         if (static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_blocks)) {
             valid = 0;
-            if (lane == 0 && p.status) atomicOr(p.status, kStatusBadBlockId);
+            if (lane == 0 && ti == 0 && p.status) atomicOr(p.status, kStatusBadBlockId);
         }
         const uint32_t kb = stage_base + s * kStage;
         if constexpr (APPEND) {
             if (ctx_ok && j == nblocks - 1 && valid > 0) {
-                // The new row r of the last block: into this warp's copy of the block (K and V,
-                // 16 bytes per lane at the swizzled position) and, from one CTA per KV head, to the pool.
-                const int r = (ctx - 1) & (kBlockSize - 1);
-                const int box = (lane >> 3) & 1, ch = lane & 7;
-                sts128(kb + (lane >> 4) * kTileBytes + box * kBoxBytes + r * 128 + ((ch ^ (r & 7)) << 4), app);
-                if (hsl == 0) {
-                    void *pool = lane < 16 ? p.k_cache : p.v_cache;
-                    const size_t e = ((static_cast<size_t>(phys) * p.n_kv + g) * kBlockSize + r) * kHeadDim +
-                                     64 * box + 8 * ch;
-                    *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(pool) + e) = app;
+                if (producer) {
+                    // The new row r of the last block: into the group's copy of the block (K and V,
+                    // 16 bytes per lane at the swizzled position) and, from one CTA per KV head, to the pool.
+                    const int r = (ctx - 1) & (kBlockSize - 1);
+                    const int box = (lane >> 3) & 1, ch = lane & 7;
+                    sts128(kb + (lane >> 4) * kTileBytes + box * kBoxBytes + r * 128 + ((ch ^ (r & 7)) << 4), app);
+                    if (hsl == 0) {
+                        void *pool = lane < 16 ? p.k_cache : p.v_cache;
+                        const size_t e = ((static_cast<size_t>(phys) * p.n_kv + g) * kBlockSize + r) * kHeadDim +
+                                         64 * box + 8 * ch;
+                        *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(pool) + e) = app;
+                    }
+                    if (T > 1) mbar_arrive(app_bar);  // every lane: its 16 bytes are in the stage
+                    __syncwarp();
+                } else {
+                    bool aok = mbar_wait(app_bar, 0);
+                    aok = __all_sync(0xffffffffu, aok);
+                    if (!aok) {
+                        timed_out = true;
+                        break;
+                    }
                 }
-                __syncwarp();
             }
         }
         if constexpr (FP8 && VERIFY) {
@@ -274,17 +308,28 @@ __global__ void __launch_bounds__(NW * 32)
         consumed = i + 1;
 
         __syncwarp();
-        if (lane < kIssueLanes && i + ST < nmine) {
-            fence_proxy_async_smem();
-            issue(i + ST);
+        if (T > 1 && lane == 0) mbar_arrive(empty_base + 8 * s);  // this warp is done with stage s
+        if (producer && i + R < nmine) {
+            if (T > 1) {  // the group's other warps must be done with stage s before it is refilled
+                bool eok = mbar_wait(empty_base + 8 * s, (i / R) & 1);
+                eok = __all_sync(0xffffffffu, eok);
+                if (!eok) {
+                    timed_out = true;
+                    break;
+                }
+            }
+            if (lane < kIssueLanes) {
+                fence_proxy_async_smem();
+                issue(i + R);
+            }
+            ++issued;
         }
     }
 
     if (timed_out) {
         if (lane == 0 && p.status) atomicOr(p.status, kStatusTimeout);
-        // Let this warp's copies still in flight land before the CTA exits.
-        const int issued = min(nmine, consumed + ST);
-        for (int i = consumed; i < issued; ++i) mbar_wait(bar_base + 8 * (i % ST), (i / ST) & 1);
+        // Let the copies this warp issued that are still in flight land before the CTA exits.
+        for (int i = consumed; i < issued; ++i) mbar_wait(bar_base + 8 * (i % R), (i / R) & 1);
     }
 
     if constexpr (FP8) fp8_finish(acc);
@@ -321,18 +366,19 @@ __global__ void __launch_bounds__(NW * 32)
     }
     __syncthreads();
 
+    // Column hh is column hh % kCols of tile hh / kCols, held by warp gg * T + hh / kCols of
+    // every group gg: slot (gg * T + hh / kCols) * kCols + hh % kCols = gg * T * kCols + hh.
     for (int idx = threadIdx.x; idx < ncols * kHeadDim; idx += NW * 32) {
         const int hh = idx >> 7, d = idx & 127;
         float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) M = fmaxf(M, red_m[w * kCols + hh]);
+        for (int gg = 0; gg < NG; ++gg) M = fmaxf(M, red_m[gg * T * kCols + hh]);
         const float Mu = M == -INFINITY ? 0.f : M;
         float L = 0.f, O = 0.f;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-            const float f = fast_exp2(red_m[w * kCols + hh] - Mu);
-            L += f * red_l[w * kCols + hh];
-            O += f * red_o[(w * kCols + hh) * kHeadDim + d];
+        for (int gg = 0; gg < NG; ++gg) {
+            const int slot = gg * T * kCols + hh;
+            const float f = fast_exp2(red_m[slot] - Mu);
+            L += f * red_l[slot];
+            O += f * red_o[slot * kHeadDim + d];
         }
         const size_t row = col_row(hh);
         if (nparts == 1) {
@@ -359,58 +405,67 @@ namespace {
 // p = w, w + 8, ...; lane owns dims 4*lane .. 4*lane + 3.
 constexpr int kMergeWarps = 8;
 
-__global__ void __launch_bounds__(kMergeWarps * 32) lse_merge_kernel(const DecodeParams p, int rows_per_seq) {
+// Rows r = blockIdx.y, + gridDim.y, ... < rows.  fixed_parts > 0: every row has that
+// many partials (the prefill's key splits); 0: a row's partition count follows
+// from its sequence's context length as the decode kernel derived it.
+__global__ void __launch_bounds__(kMergeWarps * 32)
+    lse_merge_kernel(const DecodeParams p, int rows, int rows_per_seq, int fixed_parts) {
     __shared__ float red_o[kMergeWarps][kHeadDim];
     __shared__ float red_x[kMergeWarps];
     __shared__ float red_l[kMergeWarps];
     const int h = blockIdx.x;
-    const int r = blockIdx.y;            // q row r of the call (decode: r = b)
-    const int b = r / rows_per_seq;      // its sequence
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    griddep_wait();  // the decode grid's partials
-    int ctx = __ldg(p.context_lens + b);
-    const int max_ctx = p.max_blocks * kBlockSize;
-    ctx = ctx < 1 ? 0 : (ctx > max_ctx ? max_ctx : ctx);
-    // first visible key of the call's earliest row of this sequence, as the decode kernel has it
-    // (decode: rows_per_seq = 1, key ctx - W; verify: the first of the q_per_seq rows)
-    const int first_blk = (p.window > 0 ? max(0, ctx - rows_per_seq + 1 - p.window) : 0) / kBlockSize;
-    const int nparts = ((ctx + kBlockSize - 1) / kBlockSize - first_blk + p.part_blocks - 1) / p.part_blocks;
-    if (nparts <= 1) return;  // written directly by the decode kernel
-    const size_t base = (static_cast<size_t>(r) * p.n_q + h) * p.max_parts;
-    float M = -INFINITY;
-    for (int i = threadIdx.x; i < nparts; i += kMergeWarps * 32) M = fmaxf(M, __ldcg(p.part_m + base + i));
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    if (lane == 0) red_x[warp] = M;
-    __syncthreads();
-    M = red_x[0];
-#pragma unroll
-    for (int w = 1; w < kMergeWarps; ++w) M = fmaxf(M, red_x[w]);
-    const float Mu = M == -INFINITY ? 0.f : M;
-    float L = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int i = warp; i < nparts; i += kMergeWarps) {
-        const float f = fast_exp2(__ldcg(p.part_m + base + i) - Mu);
-        L += f * __ldcg(p.part_l + base + i);
-        const float4 v = __ldcg(reinterpret_cast<const float4 *>(p.part_o + (base + i) * kHeadDim) + lane);
-        acc.x += f * v.x;
-        acc.y += f * v.y;
-        acc.z += f * v.z;
-        acc.w += f * v.w;
-    }
-    reinterpret_cast<float4 *>(red_o[warp])[lane] = acc;
-    if (lane == 0) red_l[warp] = L;
-    __syncthreads();
-    if (threadIdx.x < kHeadDim) {
-        float Ls = 0.f, O = 0.f;
-#pragma unroll
-        for (int w = 0; w < kMergeWarps; ++w) {
-            Ls += red_l[w];
-            O += red_o[w][threadIdx.x];
+    griddep_wait();  // the producing grid's partials
+    for (int r = blockIdx.y; r < rows; r += gridDim.y) {  // q row r of the call (decode: r = b)
+        int nparts = fixed_parts;
+        if (nparts == 0) {
+            const int b = r / rows_per_seq;  // its sequence
+            int ctx = __ldg(p.context_lens + b);
+            const int max_ctx = p.max_blocks * kBlockSize;
+            ctx = ctx < 1 ? 0 : (ctx > max_ctx ? max_ctx : ctx);
+            // first visible key of the call's earliest row of this sequence, as the decode kernel has it
+            // (decode: rows_per_seq = 1, key ctx - W; verify: the first of the q_per_seq rows)
+            const int first_blk = (p.window > 0 ? max(0, ctx - rows_per_seq + 1 - p.window) : 0) / kBlockSize;
+            nparts = ((ctx + kBlockSize - 1) / kBlockSize - first_blk + p.part_blocks - 1) / p.part_blocks;
         }
-        store_out(p.out, p.out_bf16, (static_cast<size_t>(r) * p.n_q + h) * kHeadDim + threadIdx.x,
-                  Ls > 0.f ? O / Ls : 0.f);
+        if (nparts <= 1) continue;  // written directly by the decode kernel (CTA-uniform)
+        const size_t base = (static_cast<size_t>(r) * p.n_q + h) * p.max_parts;
+        float M = -INFINITY;
+        for (int i = threadIdx.x; i < nparts; i += kMergeWarps * 32) M = fmaxf(M, __ldcg(p.part_m + base + i));
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        if (lane == 0) red_x[warp] = M;
+        __syncthreads();
+        M = red_x[0];
+#pragma unroll
+        for (int w = 1; w < kMergeWarps; ++w) M = fmaxf(M, red_x[w]);
+        const float Mu = M == -INFINITY ? 0.f : M;
+        float L = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+        for (int i = warp; i < nparts; i += kMergeWarps) {
+            const float f = fast_exp2(__ldcg(p.part_m + base + i) - Mu);
+            L += f * __ldcg(p.part_l + base + i);
+            const float4 v = __ldcg(reinterpret_cast<const float4 *>(p.part_o + (base + i) * kHeadDim) + lane);
+            acc.x += f * v.x;
+            acc.y += f * v.y;
+            acc.z += f * v.z;
+            acc.w += f * v.w;
+        }
+        reinterpret_cast<float4 *>(red_o[warp])[lane] = acc;
+        if (lane == 0) red_l[warp] = L;
+        __syncthreads();
+        if (threadIdx.x < kHeadDim) {
+            float Ls = 0.f, O = 0.f;
+#pragma unroll
+            for (int w = 0; w < kMergeWarps; ++w) {
+                Ls += red_l[w];
+                O += red_o[w][threadIdx.x];
+            }
+            store_out(p.out, p.out_bf16, (static_cast<size_t>(r) * p.n_q + h) * kHeadDim + threadIdx.x,
+                      Ls > 0.f ? O / Ls : 0.f);
+        }
+        __syncthreads();  // red_* are reused by the next row
     }
     // The next kernel on the stream (often the next step's decode) launches only as
     // the merge ends: launched earlier, its CTAs would take whatever SM slots were
@@ -420,6 +475,15 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lse_merge_kernel(const Decod
     // merge's start; the 8B-shaped batch of 2048 CTAs is unchanged).
     griddep_launch_dependents();
 }
+
+}  // namespace
+
+cudaError_t launch_merge(const DecodeParams &p, int rows, int rows_per_seq, int fixed_parts, cudaStream_t stream) {
+    return launch_pdl(lse_merge_kernel, dim3(p.n_q, rows < 65535 ? rows : 65535), dim3(kMergeWarps * 32), 0, stream, p,
+                      rows, rows_per_seq, fixed_parts);
+}
+
+namespace {
 
 template <int NW, int ST, bool FP8 = false, bool VERIFY = false, int NCT = 1, bool APPEND = false>
 cudaError_t launch_variant(const CUtensorMap &kmap, const CUtensorMap &vmap,
@@ -431,9 +495,7 @@ cudaError_t launch_variant(const CUtensorMap &kmap, const CUtensorMap &vmap,
     if (e != cudaSuccess) return e;
     int rows_per_seq = 1;
     if constexpr (VERIFY) rows_per_seq = p.q_per_seq;
-    if (p.max_parts > 1)
-        e = launch_pdl(lse_merge_kernel, dim3(p.n_q, p.num_seqs * rows_per_seq), dim3(kMergeWarps * 32), 0, stream,
-                       static_cast<const DecodeParams &>(p), rows_per_seq);
+    if (p.max_parts > 1) e = launch_merge(p, p.num_seqs * rows_per_seq, rows_per_seq, 0, stream);
     return e;
 }
 
@@ -449,8 +511,9 @@ constexpr int kFp8Warps = 4, kFp8Stages = 3;
 }  // namespace
 
 size_t decode_smem_bytes() {
-    // stage ring + mbarriers + 1 KB for aligning the base to the 1 KB swizzle period
-    return static_cast<size_t>(kWarps) * kStages * kStageBytes + static_cast<size_t>(kWarps) * kStages * 8 + 1024;
+    // stage rings + full and empty mbarriers per stage + one append mbarrier per warp
+    // + 1 KB for aligning the base to the 1 KB swizzle period
+    return static_cast<size_t>(kWarps) * kStages * (kStageBytes + 16) + static_cast<size_t>(kWarps) * 8 + 1024;
 }
 
 cudaError_t decode_prepare_device() {
@@ -469,7 +532,8 @@ cudaError_t decode_prepare_device() {
 }
 
 size_t decode_fp8_smem_bytes() {
-    return static_cast<size_t>(kFp8Warps) * kFp8Stages * (kStageBytes8 + kStageScaleBytes + 8) + 1024;
+    return static_cast<size_t>(kFp8Warps) * kFp8Stages * (kStageBytes8 + kStageScaleBytes + 16) +
+           static_cast<size_t>(kFp8Warps) * 8 + 1024;
 }
 
 cudaError_t decode_fp8_prepare_device() {

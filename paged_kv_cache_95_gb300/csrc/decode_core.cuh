@@ -5,7 +5,8 @@
 // heads of its GQA group ("注意力演进与推理流程", section 3.1: head h reads KV
 // group floor(h / G)):
 //   S^T[16 keys x 8 heads] = K[16 x 128] Q^T[128 x 8]      (mma.sync m16n8k16)
-//   online softmax in the log2 domain (running max m, sum l, rescale of O)
+//   online softmax in the log2 domain (lazy exponent reference m, sum l,
+//   rescale of O when m is raised)
 //   O^T[128 x 8] += V^T[128 x 16] P^T[16 x 8]
 // K and V tiles sit in shared memory as two 2 KB boxes each (64 dims x 16 rows,
 // 128-byte swizzle: 16-byte chunk c of row r at chunk c ^ (r & 7)), so the
@@ -34,18 +35,27 @@ __device__ __forceinline__ void store_out(void *out, int32_t bf16, size_t idx, f
 }
 
 // Online-softmax state of one warp for the 8 head columns of its MMA tile.  Lane
-// (n = lane / 4, q4 = lane % 4) holds columns 2*q4 and 2*q4 + 1: the running max
-// (identical across the 8 lanes of a column), its share of the running sum, and
-// O^T rows 16*mt + n and 16*mt + n + 8 of those columns.
+// (n = lane / 4, q4 = lane % 4) holds columns 2*q4 and 2*q4 + 1: the exponent
+// reference m (identical across the 8 lanes of a column), its share of the
+// running sum l = sum 2^(s - m), and O^T rows 16*mt + n and 16*mt + n + 8 of
+// those columns (O = sum 2^(s - m) v).  The reference is lazy: it is raised (and
+// l and O rescaled) only when a score exceeds it by more than kLazyExp, so every
+// weight stays <= 2^kLazyExp and most blocks skip the block maximum and the
+// rescale; the result is the same softmax, since out = O / l for any reference.
+constexpr float kLazyExp = 8.f;
 struct DecodeAcc {
     float m0, m1, l0, l1;
     float o[8][4];
-    // FP8 only: O is held times 2^vexp (vexp set by the largest V scale seen so far).
+    // FP8 only: O is held times 2^vexp (vexp set by the largest V scale seen so
+    // far, which it puts in [2, 4)); vthr = 2^(2 - vexp): a V scale at or above it
+    // lowers vexp.
     int vexp;
+    float vthr;
     __device__ __forceinline__ void reset() {
         m0 = m1 = -INFINITY;
         l0 = l1 = 0.f;
         vexp = kNoVexp;
+        vthr = 0.f;
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
     }
@@ -77,6 +87,43 @@ __device__ __forceinline__ void load_q_frag(uint32_t (&bq)[8][2], const void *q,
                                             int lane) {
     const int n = lane >> 2;
     load_q_frag_row(bq, q, head0_row + n, n < hpc, lane);
+}
+
+// O columns 2*q4 and 2*q4 + 1 of this lane times a0 and a1.
+__device__ __forceinline__ void rescale_o(DecodeAcc &acc, float a0, float a1) {
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+        acc.o[mt][0] *= a0;
+        acc.o[mt][1] *= a1;
+        acc.o[mt][2] *= a0;
+        acc.o[mt][3] *= a1;
+    }
+}
+// Raises the exponent references of this lane's two columns when a score of the
+// block exceeds them by more than kLazyExp (a warp vote; most blocks skip it):
+// the column's block maximum becomes its reference and l and O are rescaled.
+__device__ __forceinline__ void raise_reference(DecodeAcc &acc, float s00, float s01, float s10, float s11) {
+    const bool up = s00 > acc.m0 + kLazyExp || s10 > acc.m0 + kLazyExp || s01 > acc.m1 + kLazyExp ||
+                    s11 > acc.m1 + kLazyExp;
+    if (!__any_sync(0xffffffffu, up)) return;
+    float bm0 = fmaxf(s00, s10), bm1 = fmaxf(s01, s11);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
+        bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
+    }
+    float al0 = 1.f, al1 = 1.f;
+    if (bm0 > acc.m0 + kLazyExp) {  // also the first visible key (m = -inf: alpha = 0, l and O are 0)
+        al0 = fast_exp2(acc.m0 - bm0);
+        acc.m0 = bm0;
+    }
+    if (bm1 > acc.m1 + kLazyExp) {
+        al1 = fast_exp2(acc.m1 - bm1);
+        acc.m1 = bm1;
+    }
+    acc.l0 *= al0;
+    acc.l1 *= al1;
+    rescale_o(acc, al0, al1);
 }
 
 // One block: kb / vb are the shared addresses of the stage's K and V tiles;
@@ -123,29 +170,13 @@ __device__ __forceinline__ void decode_block(DecodeAcc &acc, const uint32_t (&bq
     const float s01 = v01 ? c[1] * sl2 : -INFINITY;
     const float s10 = v10 ? c[2] * sl2 : -INFINITY;
     const float s11 = v11 ? c[3] * sl2 : -INFINITY;
-    float bm0 = fmaxf(s00, s10), bm1 = fmaxf(s01, s11);
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-        bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
-        bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
-    }
-    const float mn0 = fmaxf(acc.m0, bm0), mn1 = fmaxf(acc.m1, bm1);
-    const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
-    const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float al0 = fast_exp2(acc.m0 - mu0), al1 = fast_exp2(acc.m1 - mu1);
+    raise_reference(acc, s00, s01, s10, s11);
+    const float mu0 = acc.m0 == -INFINITY ? 0.f : acc.m0;
+    const float mu1 = acc.m1 == -INFINITY ? 0.f : acc.m1;
     const float p00 = fast_exp2(s00 - mu0), p01 = fast_exp2(s01 - mu1);
     const float p10 = fast_exp2(s10 - mu0), p11 = fast_exp2(s11 - mu1);
-    acc.l0 = acc.l0 * al0 + p00 + p10;
-    acc.l1 = acc.l1 * al1 + p01 + p11;
-    acc.m0 = mn0;
-    acc.m1 = mn1;
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-        acc.o[mt][0] *= al0;
-        acc.o[mt][1] *= al1;
-        acc.o[mt][2] *= al0;
-        acc.o[mt][3] *= al1;
-    }
+    acc.l0 += p00 + p10;
+    acc.l1 += p01 + p11;
 
     // P (C layout: row key, col head) -> P^T in the B-operand layout.  P is
     // split into a bf16 head and a bf16 remainder (P = hi + lo to ~2^-17), so
@@ -220,29 +251,13 @@ __device__ __forceinline__ void decode_block_x2(DecodeAcc (&acc)[2], const uint3
         const float s01 = in_a && key_a < lim[t][1] && key_a >= low[t][1] ? c[t][1] * sl2 : -INFINITY;
         const float s10 = in_b && key_b < lim[t][0] && key_b >= low[t][0] ? c[t][2] * sl2 : -INFINITY;
         const float s11 = in_b && key_b < lim[t][1] && key_b >= low[t][1] ? c[t][3] * sl2 : -INFINITY;
-        float bm0 = fmaxf(s00, s10), bm1 = fmaxf(s01, s11);
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
-            bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
-        }
-        const float mn0 = fmaxf(acc[t].m0, bm0), mn1 = fmaxf(acc[t].m1, bm1);
-        const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
-        const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
-        const float al0 = fast_exp2(acc[t].m0 - mu0), al1 = fast_exp2(acc[t].m1 - mu1);
+        raise_reference(acc[t], s00, s01, s10, s11);
+        const float mu0 = acc[t].m0 == -INFINITY ? 0.f : acc[t].m0;
+        const float mu1 = acc[t].m1 == -INFINITY ? 0.f : acc[t].m1;
         const float p00 = fast_exp2(s00 - mu0), p01 = fast_exp2(s01 - mu1);
         const float p10 = fast_exp2(s10 - mu0), p11 = fast_exp2(s11 - mu1);
-        acc[t].l0 = acc[t].l0 * al0 + p00 + p10;
-        acc[t].l1 = acc[t].l1 * al1 + p01 + p11;
-        acc[t].m0 = mn0;
-        acc[t].m1 = mn1;
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-            acc[t].o[mt][0] *= al0;
-            acc[t].o[mt][1] *= al1;
-            acc[t].o[mt][2] *= al0;
-            acc[t].o[mt][3] *= al1;
-        }
+        acc[t].l0 += p00 + p10;
+        acc[t].l1 += p01 + p11;
         const uint32_t ph0 = pack_bf16x2(p00, p01), ph1 = pack_bf16x2(p10, p11);
         const uint32_t pl0 = pack_bf16x2(p00 - __uint_as_float(ph0 << 16), p01 - __uint_as_float(ph0 & 0xffff0000u));
         const uint32_t pl1 = pack_bf16x2(p10 - __uint_as_float(ph1 << 16), p11 - __uint_as_float(ph1 & 0xffff0000u));
@@ -357,10 +372,11 @@ __device__ __forceinline__ int load_q_frag_fp8(uint32_t (&bq)[8][2], const void 
 // fsl2 = scale * log2(e) * 2^-qexp.
 //
 // V scales are folded into the weights: P'' = p * sv * 2^vexp, with vexp the
-// running exponent that puts the largest V scale seen so far in [2^9, 2^10), so
-// P'' <= 2^10 and every weight that matters is a normal fp16 number; O is held
-// times 2^vexp (rescaled with the softmax correction when vexp drops) and
-// brought back by fp8_finish().  P'' goes in as an fp16 head + remainder.
+// running exponent that puts the largest V scale seen so far in [2, 4); with the
+// lazy reference p <= 2^8, so P'' <= 2^10 and every weight that matters is a
+// normal fp16 number; O is held times 2^vexp (rescaled with the softmax
+// correction when vexp drops) and brought back by fp8_finish().  P'' goes in as
+// an fp16 head + remainder.
 // Multi-token verify (BOUNDS): column 2*q4 (2*q4 + 1) of this lane only sees keys
 // low0 <= k < lim0 (low1 <= k < lim1) of the block; those keys hold valid data,
 // so only their weight is zeroed.
@@ -410,44 +426,49 @@ __device__ __forceinline__ void decode_block_fp8(DecodeAcc &acc, const uint32_t 
     const float s01 = v01 ? c[1] * fa : -INFINITY;
     const float s10 = v10 ? c[2] * fb : -INFINITY;
     const float s11 = v11 ? c[3] * fb : -INFINITY;
-    float bm0 = fmaxf(s00, s10), bm1 = fmaxf(s01, s11);
     const float sva = in_a ? lds_f32(sc + kScaleBytes + 4 * key_a) : 0.f;
     const float svb = in_b ? lds_f32(sc + kScaleBytes + 4 * key_b) : 0.f;
-    float svmax = fmaxf(sva, svb);
+    // Lazy exponent reference (as for bf16) and lazy V exponent: both are revisited only
+    // when a score exceeds its column's reference by more than kLazyExp or a V scale
+    // reaches vthr (one warp vote; most blocks skip the reductions and the rescale).
+    const bool raise = s00 > acc.m0 + kLazyExp || s10 > acc.m0 + kLazyExp || s01 > acc.m1 + kLazyExp ||
+                       s11 > acc.m1 + kLazyExp || sva >= acc.vthr || svb >= acc.vthr;
+    if (__any_sync(0xffffffffu, raise)) {
+        float bm0 = fmaxf(s00, s10), bm1 = fmaxf(s01, s11), svmax = fmaxf(sva, svb);
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-        bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
-        bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
-        svmax = fmaxf(svmax, __shfl_xor_sync(0xffffffffu, svmax, off));
-    }
-    const float mn0 = fmaxf(acc.m0, bm0), mn1 = fmaxf(acc.m1, bm1);
-    const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
-    const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float as0 = fast_exp2(acc.m0 - mu0), as1 = fast_exp2(acc.m1 - mu1);  // softmax correction
-    float al0 = as0, al1 = as1;                                                  // ... and O's
-    // A larger V scale lowers vexp: O (held times 2^vexp) shrinks by the same power of two.
-    if (svmax > 0.f) {
-        const int ve = 9 - (static_cast<int>((__float_as_uint(svmax) >> 23) & 0xff) - 127);
-        if (ve < acc.vexp) {
-            const float f = acc.vexp == kNoVexp ? 1.f : ldexpf(1.f, ve - acc.vexp);
-            al0 *= f;
-            al1 *= f;
-            acc.vexp = ve;
+        for (int off = 4; off < 32; off <<= 1) {
+            bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
+            bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
+            svmax = fmaxf(svmax, __shfl_xor_sync(0xffffffffu, svmax, off));
         }
+        float as0 = 1.f, as1 = 1.f;  // softmax corrections (l and O)
+        if (bm0 > acc.m0 + kLazyExp) {
+            as0 = fast_exp2(acc.m0 - bm0);
+            acc.m0 = bm0;
+        }
+        if (bm1 > acc.m1 + kLazyExp) {
+            as1 = fast_exp2(acc.m1 - bm1);
+            acc.m1 = bm1;
+        }
+        acc.l0 *= as0;
+        acc.l1 *= as1;
+        // A larger V scale lowers vexp (svmax * 2^vexp in [2, 4)): O, held times 2^vexp,
+        // shrinks by the same power of two.
+        float f = 1.f;
+        if (svmax > 0.f && svmax >= acc.vthr) {
+            const int ve = 1 - (static_cast<int>((__float_as_uint(svmax) >> 23) & 0xff) - 127);
+            f = acc.vexp == kNoVexp ? 1.f : ldexpf(1.f, ve - acc.vexp);
+            acc.vexp = ve;
+            acc.vthr = ldexpf(1.f, 2 - ve);
+        }
+        rescale_o(acc, as0 * f, as1 * f);
     }
+    const float mu0 = acc.m0 == -INFINITY ? 0.f : acc.m0;
+    const float mu1 = acc.m1 == -INFINITY ? 0.f : acc.m1;
     const float p00 = fast_exp2(s00 - mu0), p01 = fast_exp2(s01 - mu1);
     const float p10 = fast_exp2(s10 - mu0), p11 = fast_exp2(s11 - mu1);
-    acc.l0 = acc.l0 * as0 + p00 + p10;
-    acc.l1 = acc.l1 * as1 + p01 + p11;
-    acc.m0 = mn0;
-    acc.m1 = mn1;
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-        acc.o[mt][0] *= al0;
-        acc.o[mt][1] *= al1;
-        acc.o[mt][2] *= al0;
-        acc.o[mt][3] *= al1;
-    }
+    acc.l0 += p00 + p10;
+    acc.l1 += p01 + p11;
 
     const float up = acc.vexp == kNoVexp ? 0.f : ldexpf(1.f, acc.vexp);
     const float wa2 = sva * up, wb2 = svb * up;

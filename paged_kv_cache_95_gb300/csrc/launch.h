@@ -58,8 +58,9 @@ struct DecodeParams {
     uint32_t *status;            // device status word
     int32_t num_seqs, n_q, n_kv;
     int32_t group;               // G = n_q / n_kv
-    int32_t heads_per_cta;       // min(G, 8)
+    int32_t heads_per_cta;       // query heads (MMA columns) per CTA: G <= 8: G; 16 or 32 for larger groups
     int32_t head_splits;         // G / heads_per_cta
+    int32_t col_tiles;           // T: 8-column tiles per CTA, one per warp of a block group (1, 2 or 4)
     int32_t max_blocks;          // block-table row length
     int32_t num_blocks;          // pool size
     int32_t part_blocks;         // blocks per partition
@@ -101,6 +102,12 @@ struct DecodeParamsAppend : DecodeParams {
     void *v_cache;
 };
 
+// The log-sum-exp merge of split partials (m, l, O) into out, one CTA per (row,
+// query head): rows_per_seq maps a row to its sequence's context length when the
+// partition count follows from it (fixed_parts = 0); fixed_parts > 0 merges that
+// many partials per row (the prefill's key splits).
+cudaError_t launch_merge(const DecodeParams &p, int rows, int rows_per_seq, int fixed_parts, cudaStream_t stream);
+
 // Shared-memory bytes of the decode kernel; sets its dynamic shared memory limit.
 size_t decode_smem_bytes();
 cudaError_t decode_prepare_device();
@@ -137,6 +144,12 @@ struct PrefillParams {
     int32_t window;              // sliding window W (> 0): a row at pos sees pos - W < j <= pos; 0: none
     const float *k_scale;        // FP8 cache: per-slot scales [num_blocks][n_kv][16]; null for bf16
     const float *v_scale;
+    // Split-KV (kv_splits > 1): CTA split s of a pair of row tiles takes key tiles
+    // [s * per, (s + 1) * per) of the pair's n key tiles (per = ceil(n / kv_splits)) and
+    // writes the unnormalised partial (m, l, O) of every row it owns to part_* (indexed
+    // [(row * n_q + head) * kv_splits + s]); the merge kernel folds the splits.
+    int32_t kv_splits;
+    float *part_m, *part_l, *part_o;
 };
 
 size_t prefill_smem_bytes();

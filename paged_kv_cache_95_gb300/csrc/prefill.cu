@@ -226,11 +226,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    // Grid (KV group, sequence, pair of row tiles), pairs in reverse: later rows
-    // see more keys, so the longest CTAs start first and the last wave is short.
+    // Grid (KV group, sequence, pair of row tiles x key split), pairs in reverse:
+    // later rows see more keys, so the longest CTAs start first and the last wave
+    // is short; the splits of a pair are adjacent.
     const int g = blockIdx.x;
     const int b = blockIdx.y;
-    const int pair = gridDim.z - 1 - blockIdx.z;
+    const int S = p.kv_splits;
+    const int pair = static_cast<int>(gridDim.z) / S - 1 - static_cast<int>(blockIdx.z) / S;
+    const int split = static_cast<int>(blockIdx.z) % S;
     const int G = p.group;
     const int rpt = p.rows_per_tile;
 
@@ -251,11 +254,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row0 = p.cu_q_lens ? __ldg(p.cu_q_lens + b) : b * p.uniform_q_len;
     const int q_len = p.cu_q_lens ? __ldg(p.cu_q_lens + b + 1) - row0 : p.uniform_q_len;
     const int ctx = __ldg(p.context_lens + b);
+    // Split-KV: this split's partial for rows [r_lo, r_hi) of the pair is empty
+    // (m = -inf, l = 0, O = 0): the merge then gives those rows nothing from it.
+    auto empty_partials = [&](int r_lo, int r_hi) {
+        for (int idx = tid; idx < max(0, r_hi - r_lo) * G * 32; idx += kThreads) {
+            const int i = r_lo + idx / (G * 32), h = (idx / 32) % G, c4 = idx % 32;
+            const size_t pi = (static_cast<size_t>(row0 + i) * p.n_q + static_cast<size_t>(g) * G + h) * S + split;
+            reinterpret_cast<float4 *>(p.part_o + pi * kHeadDim)[c4] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (c4 == 0) {
+                p.part_m[pi] = -INFINITY;
+                p.part_l[pi] = 0.f;
+            }
+        }
+    };
     if (q_len < 0 || q_len > ctx || ctx > p.max_blocks * kBlockSize || row0 < 0 || row0 + q_len > p.total_rows) {
-        if (pair == 0 && g == 0 && tid == 0 && p.status) atomicOr(p.status, kStatusBadQLen);
+        if (pair == 0 && split == 0 && g == 0 && tid == 0 && p.status) atomicOr(p.status, kStatusBadQLen);
         // The sequence's rows read as zeros when they can be addressed (this CTA's
         // two row tiles of its KV group; 16-byte stores, out is 16-byte aligned).
-        if (q_len > 0 && row0 >= 0 && row0 + q_len <= p.total_rows) {
+        if (S > 1 && q_len > 0 && row0 >= 0 && row0 + q_len <= p.total_rows) {
+            empty_partials(2 * pair * rpt, min(q_len, (2 * pair + 2) * rpt));
+        } else if (q_len > 0 && row0 >= 0 && row0 + q_len <= p.total_rows) {
             const int r_lo = 2 * pair * rpt, r_hi = min(q_len, r_lo + 2 * rpt);
             const int chunks = p.out_bf16 ? 16 : 32;  // 16-byte chunks per (row, head)
             const int per_row = G * chunks;
@@ -282,13 +300,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     // kt0 + kt (keys 128 (kt0 + kt) ..).
     const int W = WINDOW ? p.window : 0;
     const int kfirst = W > 0 ? max(0, c + tile_i0(0) + 1 - W) : 0;
-    const int kt0 = kfirst / 128;
+    int kt0 = kfirst / 128;
     const int fb = kfirst / kBlockSize;
     auto tile_nt = [&](int t) {
         return tile_rows(t) > 0 ? (c + tile_i0(t) + tile_rows(t) + 127) / 128 - kt0 : 0;
     };
-    const int nt0 = tile_nt(0), nt1 = tile_nt(1);
-    const int n_tiles = max(nt0, nt1);
+    int nt0 = tile_nt(0), nt1 = tile_nt(1);
+    int n_tiles = max(nt0, nt1);
+    if (S > 1) {
+        // This split's key tiles [ks, ke) of the pair's n_tiles; counted from kt0 + ks below.
+        const int per = (n_tiles + S - 1) / S;
+        const int ks = min(n_tiles, split * per), ke = min(n_tiles, ks + per);
+        nt0 = max(0, min(nt0, ke) - ks);
+        nt1 = max(0, min(nt1, ke) - ks);
+        kt0 += ks;
+        n_tiles = max(nt0, nt1);
+        if (n_tiles == 0) {
+            empty_partials(tile_i0(0), tile_i0(0) + tile_rows(0) + tile_rows(1));
+            return;
+        }
+    }
     if (n_tiles == 0) return;
     const int nblocks = (ctx + kBlockSize - 1) / kBlockSize;
     const int32_t *table = p.block_tables + static_cast<size_t>(b) * p.max_blocks;
@@ -734,8 +765,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             row_sync();  // the last maxima have been read: the exchange area is free
             xch[cq * 128 + r] = l[t];
             row_sync();
-            const bool staged = rows_here == rpt;  // CTA-uniform
+            const bool staged = S == 1 && rows_here == rpt;  // CTA-uniform
             const uint32_t stage = sbase + (t == 0 ? kOffV : kOffK);
+            // Split-KV: row (row0 + i0 + ii, head g G + r % G)'s partial of this split.
+            const size_t pi = (static_cast<size_t>(row0 + i0 + ii) * p.n_q + static_cast<size_t>(g) * G + (r % G)) * S +
+                              split;
+            if (S > 1 && my_nt == 0 && row_valid) {  // no key tile of this split reaches the tile
+                float4 *po = reinterpret_cast<float4 *>(p.part_o + pi * kHeadDim + 32 * cq);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) po[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (cq == 0) {
+                    p.part_m[pi] = -INFINITY;
+                    p.part_l[pi] = 0.f;
+                }
+            }
             if (my_nt > 0 && done) {
                 tc_fence_after();
                 const float lt = (xch[r] + xch[128 + r]) + (xch[256 + r] + xch[384 + r]);
@@ -744,7 +787,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld_32x32b_x32(lane_base + kTmemO + 128 * t + 32 * cq, orow);
                 tmem_wait_ld();
                 tmem_hold(orow);
-                if (staged) {
+                if (S > 1) {
+                    // the unnormalised partial: O and l relative to the row's exponent reference m
+                    if (row_valid) {
+                        float4 *po = reinterpret_cast<float4 *>(p.part_o + pi * kHeadDim + 32 * cq);
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            po[k] = make_float4(__uint_as_float(orow[4 * k]), __uint_as_float(orow[4 * k + 1]),
+                                                __uint_as_float(orow[4 * k + 2]), __uint_as_float(orow[4 * k + 3]));
+                        if (cq == 0) {
+                            p.part_m[pi] = m_ref[t];
+                            p.part_l[pi] = lt;
+                        }
+                    }
+                } else if (staged) {
                     stage_row(stage, p.out_bf16, r, cq >> 1, cq & 1, orow, inv);
                 } else if (row_valid) {
                     const size_t base =
@@ -806,13 +862,25 @@ cudaError_t prefill_prepare_device() {
 
 cudaError_t launch_prefill_chunk(const CUtensorMap &qmap, const CUtensorMap &kmap, const CUtensorMap &vmap,
                                  const CUtensorMap &omap, const PrefillParams &p, int max_q_len, cudaStream_t stream) {
-    // One CTA per pair of row tiles.
+    // One CTA per pair of row tiles and key split.
     const int tiles = (max_q_len + p.rows_per_tile - 1) / p.rows_per_tile;
-    const dim3 grid(p.n_kv, p.num_seqs, (tiles + 1) / 2);
+    const dim3 grid(p.n_kv, p.num_seqs, (tiles + 1) / 2 * p.kv_splits);
     const bool fp8 = p.k_scale != nullptr;
     auto kernel = p.window > 0 ? (fp8 ? prefill_chunk_kernel<true, true> : prefill_chunk_kernel<true, false>)
                                : (fp8 ? prefill_chunk_kernel<false, true> : prefill_chunk_kernel<false, false>);
-    return launch_pdl(kernel, grid, dim3(kThreads), kSmemBytes, stream, qmap, kmap, vmap, omap, p);
+    cudaError_t e = launch_pdl(kernel, grid, dim3(kThreads), kSmemBytes, stream, qmap, kmap, vmap, omap, p);
+    if (e != cudaSuccess || p.kv_splits <= 1) return e;
+    // The splits' partials, folded per (row, query head) by the decode path's merge kernel.
+    DecodeParams m{};
+    m.out = p.out;
+    m.context_lens = p.context_lens;
+    m.part_m = p.part_m;
+    m.part_l = p.part_l;
+    m.part_o = p.part_o;
+    m.n_q = p.n_q;
+    m.max_parts = p.kv_splits;
+    m.out_bf16 = p.out_bf16;
+    return launch_merge(m, p.total_rows, 1, p.kv_splits, stream);
 }
 
 }  // namespace pkv

@@ -31,6 +31,10 @@ PKV_STATUS_BAD_BLOCK_ID = 0x2
 PKV_STATUS_BAD_Q_LEN = 0x4
 PKV_STATUS_TIMEOUT = 0x8
 
+PKV_VERIFY_AUTO = -1
+PKV_VERIFY_DECODE_KERNEL = 0
+PKV_VERIFY_PREFILL_KERNEL = 1
+
 HEAD_DIM = 128
 BLOCK_SIZE = 16
 STATIC_SCRATCH_BYTES = 16 * 1024 * 1024  # PKV_STATIC_SCRATCH_BYTES
@@ -96,10 +100,19 @@ def _declare(lib):
     lib.paged_attention_verify_fp8.argtypes = [P, i32, P, i32, P, P, P, P, P, P, i32, i32, i32, f32, i32, i32, D, P,
                                                sz, P]
     lib.paged_attention_verify_fp8.restype = ctypes.c_int
+    lib.paged_attention_verify_workspace_size_on.argtypes = [i32, i32, i32, i32, i32, i32, D]
+    lib.paged_attention_verify_workspace_size_on.restype = sz
+    lib.paged_attention_verify_on.argtypes = [i32, P, i32, P, i32, P, P, P, P, P, P, i32, i32, i32, f32, i32, i32, D,
+                                              P, sz, P]
+    lib.paged_attention_verify_on.restype = ctypes.c_int
     lib.kv_reshape_and_cache_fp8.argtypes = [P, P, P, P, P, P, P, i32, D, P]
     lib.kv_reshape_and_cache_fp8.restype = ctypes.c_int
     lib.paged_attention_prefill_workspace_size.argtypes = [i32, i32, D]
     lib.paged_attention_prefill_workspace_size.restype = sz
+    lib.paged_attention_verify_on_prefill.argtypes = [i32, i32, i32, D]
+    lib.paged_attention_verify_on_prefill.restype = ctypes.c_int
+    lib.paged_attention_prefill_chunk_workspace_size.argtypes = [i32, i32, i32, i32, i32, D]
+    lib.paged_attention_prefill_chunk_workspace_size.restype = sz
     lib.paged_attention_prefill_chunk.argtypes = [P, i32, P, P, i32, i32, P, P, P, P, i32, i32, i32, f32, D, P, sz, P]
     lib.paged_attention_prefill_chunk.restype = ctypes.c_int
     lib.paged_attention_prefill_chunk_window.argtypes = [P, i32, P, P, i32, i32, P, P, P, P, i32, i32, i32, f32, i32,
@@ -454,11 +467,13 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
 
 def paged_attention_verify(out, q, q_per_seq: int, k_cache, v_cache, block_tables, context_lens, scale: float,
                            workspace=None, partition_size: int = 0, stream=None, window: int = 0,
-                           k_scale=None, v_scale=None):
+                           k_scale=None, v_scale=None, kernel: int = -1):
     """Verify k = q_per_seq draft positions per sequence: q / out [num_seqs * k, n_q, 128],
     row i of sequence b at position ctx_b - k + i (causal).  ``window`` > 0: row at pos
     sees pos - window < j <= pos.  An FP8 pool with ``k_scale`` / ``v_scale`` calls
-    paged_attention_verify_fp8.  Returns the workspace."""
+    paged_attention_verify_fp8.  ``kernel`` (PKV_VERIFY_DECODE_KERNEL or
+    PKV_VERIFY_PREFILL_KERNEL) forces one kernel through paged_attention_verify_on;
+    PKV_VERIFY_AUTO lets the library's measured rule choose.  Returns the workspace."""
     torch = _torch()
     desc = cache_desc(k_cache)
     fp8 = desc.dtype == PKV_DTYPE_FP8_E4M3
@@ -479,11 +494,20 @@ def paged_attention_verify(out, q, q_per_seq: int, k_cache, v_cache, block_table
     max_blocks = int(block_tables.shape[1])
     lib = load_library()
     if workspace is None:
-        nbytes = int(lib.paged_attention_verify_workspace_size(B, int(q_per_seq), n_q, max_blocks,
-                                                               int(partition_size), ctypes.byref(desc)))
+        nbytes = int(lib.paged_attention_verify_workspace_size_on(int(kernel), B, int(q_per_seq), n_q, max_blocks,
+                                                                  int(partition_size), ctypes.byref(desc)))
         _need(nbytes > 0, "invalid sizes for paged_attention_verify")
         workspace = torch.zeros(nbytes, dtype=torch.uint8, device=q.device)
     _check(workspace, "workspace", torch.uint8, ndim=1)
+    if kernel != PKV_VERIFY_AUTO:
+        rc = lib.paged_attention_verify_on(int(kernel), _ptr(out), _out_dtype(out), _ptr(q), int(q_per_seq),
+                                           _ptr(k_cache), _ptr(v_cache), _ptr(k_scale) if fp8 else None,
+                                           _ptr(v_scale) if fp8 else None, _ptr(block_tables), _ptr(context_lens), B,
+                                           int(n_q), max_blocks, float(scale), int(window), int(partition_size),
+                                           ctypes.byref(desc), _ptr(workspace), int(workspace.numel()),
+                                           _stream(stream))
+        _raise("paged_attention_verify_on", rc)
+        return workspace
     if fp8:
         rc = lib.paged_attention_verify_fp8(_ptr(out), _out_dtype(out), _ptr(q), int(q_per_seq), _ptr(k_cache),
                                             _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_tables),
@@ -512,6 +536,13 @@ def paged_attention_prefill_workspace_size(num_seqs: int, num_q_heads: int, cach
     return int(load_library().paged_attention_prefill_workspace_size(num_seqs, num_q_heads, ctypes.byref(cache)))
 
 
+def paged_attention_prefill_chunk_workspace_size(num_seqs: int, num_q_heads: int, total_q_rows: int, max_q_len: int,
+                                                 max_blocks_per_seq: int, cache: CacheDesc) -> int:
+    """Workspace bytes with which the prefill chunk may split its keys (split-KV)."""
+    return int(load_library().paged_attention_prefill_chunk_workspace_size(
+        num_seqs, num_q_heads, total_q_rows, max_q_len, max_blocks_per_seq, ctypes.byref(cache)))
+
+
 def paged_attention_prefill_chunk(out, q, cu_q_lens, max_q_len: int, k_cache, v_cache, block_tables, context_lens,
                                   scale: float, workspace=None, stream=None, window: int = 0, k_scale=None,
                                   v_scale=None):
@@ -537,7 +568,8 @@ def paged_attention_prefill_chunk(out, q, cu_q_lens, max_q_len: int, k_cache, v_
     B = int(context_lens.shape[0])
     _need(cu_q_lens.shape[0] == B + 1 and block_tables.shape[0] == B, "cu_q_lens is [B+1], block_tables [B, *]")
     if workspace is None:
-        nbytes = paged_attention_prefill_workspace_size(B, n_q, desc)
+        nbytes = paged_attention_prefill_chunk_workspace_size(B, n_q, int(rows), int(max_q_len),
+                                                              int(block_tables.shape[1]), desc)
         _need(nbytes > 0, "invalid sizes for paged_attention_prefill_chunk")
         workspace = torch.zeros(nbytes, dtype=torch.uint8, device=q.device)  # status word starts clear
     _check(workspace, "workspace", torch.uint8, ndim=1)

@@ -326,12 +326,11 @@ MEASURED_VERIFY_ROUTES = [
 
 @pytest.mark.parametrize("nseq,nq,nkv,k,fp8,faster", MEASURED_VERIFY_ROUTES)
 def test_verify_route_follows_measurements(lib, nseq, nq, nkv, k, fp8, faster):
-    """Without a device the routing counts 152 SMs; the workspace query answers the
-    status word alone (256 bytes) exactly when the prefill kernel is chosen."""
+    """Without a device the routing counts 152 SMs."""
     c = desc(num_blocks=40000, n_kv=nkv, dtype=P.PKV_DTYPE_FP8_E4M3 if fp8 else 0)
-    nbytes = lib.paged_attention_verify_workspace_size(nseq, k, nq, 2048, 0, ctypes.byref(c))
-    assert nbytes > 0
-    assert ("prefill" if nbytes == 256 else "decode") == faster
+    assert lib.paged_attention_verify_workspace_size(nseq, k, nq, 2048, 0, ctypes.byref(c)) > 0
+    route = lib.paged_attention_verify_on_prefill(nseq, k, nq, ctypes.byref(c))
+    assert ("prefill" if route == 1 else "decode") == faster
 
 
 @pytest.mark.parametrize("fp8", [False, True])
@@ -342,9 +341,10 @@ def test_verify_route_is_monotone(lib, fp8):
     decode kernel."""
     def on_prefill(nseq, n_kv, G, k):
         c = desc(num_blocks=40000, n_kv=n_kv, dtype=P.PKV_DTYPE_FP8_E4M3 if fp8 else 0)
-        n = lib.paged_attention_verify_workspace_size(nseq, k, G * n_kv, 512, 0, ctypes.byref(c))
-        assert n > 0
-        return n == 256
+        assert lib.paged_attention_verify_workspace_size(nseq, k, G * n_kv, 512, 0, ctypes.byref(c)) > 0
+        r = lib.paged_attention_verify_on_prefill(nseq, k, G * n_kv, ctypes.byref(c))
+        assert r in (0, 1)
+        return r == 1
     for n_kv in (1, 8):
         for G in (1, 2, 4, 8, 16, 24):
             for nseq in (1, 4, 8, 19, 64, 200):

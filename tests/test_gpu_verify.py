@@ -163,3 +163,61 @@ def test_verify_route_by_units(n_q, n_kv, k, nseq):
         if not on_decode:
             pf, _ = d.prefill(batch)
             assert t.equal(out, pf), "verify did not take the prefill route"
+
+
+@pytest.mark.parametrize("n_q,n_kv,k", [(32, 8, 1), (32, 8, 4), (32, 8, 16), (64, 8, 2), (64, 8, 16), (32, 32, 3),
+                                        (32, 2, 7), (32, 16, 5)])
+def test_verify_on_each_kernel(n_q, n_kv, k):
+    """paged_attention_verify_on with each kernel forced: both match the oracle."""
+    ctx = [max(c, k) for c in CTX]
+    wl, batch = W.make_custom(n_q, n_kv, ctx, q_lens=[k] * len(ctx), seed=540 + 3 * k + n_q // n_kv,
+                              materialize_logical=False)
+    d = DevWorkload(wl)
+    d.append()
+    kc, vc = oracle_after_append(wl)
+    ref = oracle.paged_attention(batch.q, batch.cu_q_lens, kc, vc, batch.block_tables, batch.context_lens, wl.scale,
+                                 n_q=wl.n_q)
+    t = torch()
+    q = bf16_to_dev(batch.q)
+    for kernel in (P.PKV_VERIFY_DECODE_KERNEL, P.PKV_VERIFY_PREFILL_KERNEL):
+        out = t.full(q.shape, float("nan"), dtype=t.float32, device="cuda")
+        ws = P.paged_attention_verify(out, q, k, d.k_cache, d.v_cache, i32_to_dev(batch.block_tables),
+                                      i32_to_dev(batch.context_lens), wl.scale, kernel=kernel)
+        assert_close(out.cpu().numpy(), ref, what=f"G={n_q // n_kv} k={k} kernel={kernel}")
+        assert status_word(ws) == 0
+
+
+def test_verify_long_contexts_few_sequences_on_each_kernel():
+    """Two sequences over long contexts: the prefill kernel splits the keys (its
+    workspace holds the partials), the decode kernel splits them into partitions;
+    both match the oracle, plain and under a window."""
+    k = 8
+    wl, batch = W.make_custom(64, 8, [20000, 7001], q_lens=[k, k], seed=550, materialize_logical=False)
+    d = DevWorkload(wl)
+    d.append()
+    kc, vc = oracle_after_append(wl)
+    t = torch()
+    q = bf16_to_dev(batch.q)
+    for win in (0, 5000):
+        ref = oracle.paged_attention(batch.q, batch.cu_q_lens, kc, vc, batch.block_tables, batch.context_lens,
+                                     wl.scale, n_q=wl.n_q, window=win)
+        for kernel in (P.PKV_VERIFY_DECODE_KERNEL, P.PKV_VERIFY_PREFILL_KERNEL):
+            out = t.full(q.shape, float("nan"), dtype=t.float32, device="cuda")
+            ws = P.paged_attention_verify(out, q, k, d.k_cache, d.v_cache, i32_to_dev(batch.block_tables),
+                                          i32_to_dev(batch.context_lens), wl.scale, kernel=kernel, window=win)
+            if kernel == P.PKV_VERIFY_PREFILL_KERNEL:
+                assert ws.numel() > 256  # the split plan's partials
+            assert_close(out.cpu().numpy(), ref, what=f"k={k} W={win} kernel={kernel}")
+            assert status_word(ws) == 0
+
+
+def test_verify_prefill_kernel_refuses_unpackable_groups():
+    t = torch()
+    wl, batch = W.make_custom(24, 1, [100, 50], q_lens=[2, 2], seed=560, materialize_logical=False)
+    d = DevWorkload(wl)
+    q = bf16_to_dev(batch.q)
+    out = t.empty(q.shape, dtype=t.float32, device="cuda")
+    with pytest.raises(Exception):
+        P.paged_attention_verify(out, q, 2, d.k_cache, d.v_cache, i32_to_dev(batch.block_tables),
+                                 i32_to_dev(batch.context_lens), wl.scale, kernel=P.PKV_VERIFY_PREFILL_KERNEL,
+                                 workspace=t.zeros(1 << 20, dtype=t.uint8, device="cuda"))
