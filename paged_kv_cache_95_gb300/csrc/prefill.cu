@@ -634,8 +634,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // This thread's 32 scores, masked by index (keys past the row's position or in a bad block).
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(t_s, v);
-                tmem_wait_ld();
-                tmem_hold(v);
                 if constexpr (FP8) {        // scores times each key's K scale
                     const uint32_t ks = sbase + kOffScale + (kt % kScaleSlotsK) * kScaleStage + 128 * cq;
 #pragma unroll
@@ -678,8 +676,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
                     uint32_t orow[32];
                     tmem_ld_32x32b_x32(t_o, orow);
-                    tmem_wait_ld();
-                    tmem_hold(orow);
 #pragma unroll
                     for (int k = 0; k < 32; ++k) orow[k] = __float_as_uint(__uint_as_float(orow[k]) * alpha);
                     tmem_st_32x32b_x32(t_o, orow);
@@ -768,9 +764,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool staged = S == 1 && rows_here == rpt;  // CTA-uniform
             const uint32_t stage = sbase + (t == 0 ? kOffV : kOffK);
             // Split-KV: row (row0 + i0 + ii, head g G + r % G)'s partial of this split.
-            const size_t pi = (static_cast<size_t>(row0 + i0 + ii) * p.n_q + static_cast<size_t>(g) * G + (r % G)) * S +
-                              split;
+            auto part_index = [&]() {
+                return (static_cast<size_t>(row0 + i0 + ii) * p.n_q + static_cast<size_t>(g) * G + (r % G)) * S + split;
+            };
             if (S > 1 && my_nt == 0 && row_valid) {  // no key tile of this split reaches the tile
+                const size_t pi = part_index();
                 float4 *po = reinterpret_cast<float4 *>(p.part_o + pi * kHeadDim + 32 * cq);
 #pragma unroll
                 for (int k = 0; k < 8; ++k) po[k] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -785,11 +783,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float inv = lt > 0.f ? 1.f / lt : 0.f;
                 uint32_t orow[32];
                 tmem_ld_32x32b_x32(lane_base + kTmemO + 128 * t + 32 * cq, orow);
-                tmem_wait_ld();
-                tmem_hold(orow);
                 if (S > 1) {
                     // the unnormalised partial: O and l relative to the row's exponent reference m
                     if (row_valid) {
+                        const size_t pi = part_index();
                         float4 *po = reinterpret_cast<float4 *>(p.part_o + pi * kHeadDim + 32 * cq);
 #pragma unroll
                         for (int k = 0; k < 8; ++k)
