@@ -50,12 +50,12 @@ struct DecodeAcc {
     // far, which it puts in [2, 4)); vthr = 2^(2 - vexp): a V scale at or above it
     // lowers vexp.
     int vexp;
-    float vthr;
+    float vthr, vup;  // vup = 2^vexp (0 before the first V scale)
     __device__ __forceinline__ void reset() {
         m0 = m1 = -INFINITY;
         l0 = l1 = 0.f;
         vexp = kNoVexp;
-        vthr = 0.f;
+        vthr = vup = 0.f;
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
     }
@@ -460,6 +460,7 @@ __device__ __forceinline__ void decode_block_fp8(DecodeAcc &acc, const uint32_t 
             f = acc.vexp == kNoVexp ? 1.f : ldexpf(1.f, ve - acc.vexp);
             acc.vexp = ve;
             acc.vthr = ldexpf(1.f, 2 - ve);
+            acc.vup = ldexpf(1.f, ve);
         }
         rescale_o(acc, as0 * f, as1 * f);
     }
@@ -470,8 +471,7 @@ __device__ __forceinline__ void decode_block_fp8(DecodeAcc &acc, const uint32_t 
     acc.l0 += p00 + p10;
     acc.l1 += p01 + p11;
 
-    const float up = acc.vexp == kNoVexp ? 0.f : ldexpf(1.f, acc.vexp);
-    const float wa2 = sva * up, wb2 = svb * up;
+    const float wa2 = sva * acc.vup, wb2 = svb * acc.vup;
     const float q00 = p00 * wa2, q01 = p01 * wa2, q10 = p10 * wb2, q11 = p11 * wb2;
     const uint32_t ph0 = pack_f16x2(q00, q01), ph1 = pack_f16x2(q10, q11);
     const float2 h0 = unpack_f16x2(ph0), h1 = unpack_f16x2(ph1);

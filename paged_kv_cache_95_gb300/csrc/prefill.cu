@@ -210,13 +210,20 @@ __device__ __forceinline__ void stage_row(uint32_t stage, int32_t bf16, int r, i
 // 608 threads, one CTA per SM (200 KB of shared memory); 19 warps put five on
 // some SM sub-partition, whose 16K registers then allow 96 a thread.
 // WINDOW: sliding-window instantiation (p.window > 0); the plain one compiles
-// without any of the window's bookkeeping.  FP8: the cache holds E4M3 codes with
+// without any of the window's bookkeeping.  SPLIT: split-KV instantiation
+// (p.kv_splits > 1: partials to the workspace for the merge kernel); the
+// unsplit one compiles with one split as a constant.  (With the split count a
+// runtime value in the unsplit kernel, ragged row tiles of multi-sequence
+// batches came out wrong on the GPU -- rows written with other rows' values or
+// not at all -- while the same source with the count constant, and the split
+// path itself, matched the oracle; the cause was not found, so the unsplit
+// kernel keeps the count constant.)  FP8: the cache holds E4M3 codes with
 // per-slot scales (p.k_scale / p.v_scale): each block's 2 KB code tile lands in
 // the upper half of a ring stage and the softmax warps expand it in place to the
 // bf16 operand layout (E4M3 values are exact in bf16) between two key tiles'
 // softmax passes; the K scale multiplies the scores and the V scale the weights
 // that enter P V (the row sums keep the unscaled weights).
-template <bool WINDOW, bool FP8>
+template <bool WINDOW, bool FP8, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_chunk_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                          const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
@@ -231,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // is short; the splits of a pair are adjacent.
     const int g = blockIdx.x;
     const int b = blockIdx.y;
-    const int S = p.kv_splits;
+    const int S = SPLIT ? p.kv_splits : 1;
     const int pair = static_cast<int>(gridDim.z) / S - 1 - static_cast<int>(blockIdx.z) / S;
     const int split = static_cast<int>(blockIdx.z) % S;
     const int G = p.group;
@@ -844,16 +851,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 size_t prefill_smem_bytes() { return kSmemBytes; }
 
+template <bool WINDOW, bool FP8>
+cudaError_t prepare_pair(int smem) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_chunk_kernel<WINDOW, FP8, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(prefill_chunk_kernel<WINDOW, FP8, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                smem);
+}
+
 cudaError_t prefill_prepare_device() {
     const int smem = static_cast<int>(kSmemBytes);
-    cudaError_t e = cudaFuncSetAttribute(prefill_chunk_kernel<false, false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(prefill_chunk_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(prefill_chunk_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(prefill_chunk_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = prepare_pair<false, false>(smem);
+    if (e == cudaSuccess) e = prepare_pair<true, false>(smem);
+    if (e == cudaSuccess) e = prepare_pair<false, true>(smem);
+    if (e == cudaSuccess) e = prepare_pair<true, true>(smem);
     return e;
 }
 
@@ -863,8 +875,15 @@ cudaError_t launch_prefill_chunk(const CUtensorMap &qmap, const CUtensorMap &kma
     const int tiles = (max_q_len + p.rows_per_tile - 1) / p.rows_per_tile;
     const dim3 grid(p.n_kv, p.num_seqs, (tiles + 1) / 2 * p.kv_splits);
     const bool fp8 = p.k_scale != nullptr;
-    auto kernel = p.window > 0 ? (fp8 ? prefill_chunk_kernel<true, true> : prefill_chunk_kernel<true, false>)
-                               : (fp8 ? prefill_chunk_kernel<false, true> : prefill_chunk_kernel<false, false>);
+    const bool split = p.kv_splits > 1;
+    auto kernel = split ? (p.window > 0 ? (fp8 ? prefill_chunk_kernel<true, true, true>
+                                               : prefill_chunk_kernel<true, false, true>)
+                                        : (fp8 ? prefill_chunk_kernel<false, true, true>
+                                               : prefill_chunk_kernel<false, false, true>))
+                        : (p.window > 0 ? (fp8 ? prefill_chunk_kernel<true, true, false>
+                                               : prefill_chunk_kernel<true, false, false>)
+                                        : (fp8 ? prefill_chunk_kernel<false, true, false>
+                                               : prefill_chunk_kernel<false, false, false>));
     cudaError_t e = launch_pdl(kernel, grid, dim3(kThreads), kSmemBytes, stream, qmap, kmap, vmap, omap, p);
     if (e != cudaSuccess || p.kv_splits <= 1) return e;
     // The splits' partials, folded per (row, query head) by the decode path's merge kernel.

@@ -74,6 +74,25 @@ def test_prefill_split_long_contexts(n_q, n_kv):
     assert status_word(ws1) == 0
 
 
+@pytest.mark.parametrize("n_q,n_kv", [(32, 8), (64, 8), (32, 16)])
+def test_prefill_split_ragged_tiles_many_sequences(n_q, n_kv):
+    """Several sequences whose chunks end inside a row tile (and one that is a
+    single row), over contexts that end inside a key tile, on the split plan."""
+    ctx = [12000, 6001, 9000, 4100, 7777]
+    q_lens = [5, 40, 17, 1, 64]
+    wl, batch = W.make_custom(n_q, n_kv, ctx, q_lens=q_lens, seed=605 + n_q + n_kv, materialize_logical=False)
+    d = DevWorkload(wl)
+    d.append()
+    ref = oracle.paged_attention(batch.q, batch.cu_q_lens, *oracle_after_append(wl), batch.block_tables,
+                                 batch.context_lens, wl.scale, n_q=wl.n_q)
+    nbytes = _split_bytes(wl, batch)
+    out, ws = _prefill(d, batch, nbytes)
+    assert_close(out.cpu().numpy(), ref, what=f"split, ragged tiles, G={n_q // n_kv}")
+    assert status_word(ws) == 0
+    out1, ws1 = _prefill(d, batch, 256)
+    assert_close(out1.cpu().numpy(), ref, what=f"unsplit, ragged tiles, G={n_q // n_kv}")
+
+
 def test_prefill_split_window_and_stale_entries():
     """A split chunk under a sliding window, with invalid ids in the table entries
     wholly before every row's window (never read, no flag)."""
