@@ -510,11 +510,10 @@ PKV_API int paged_attention_prefill_chunk_fp8(void *out, int32_t out_dtype, cons
  * Runs on the decode kernel, where the G heads x k positions of a KV head are
  * the MMA columns of ceil(G * k / 16) CTAs of up to 16 columns (one or two
  * 8-column tiles), each reading the K/V once; or on the tcgen05 prefill kernel
- * (then q and out must be 16-B aligned), which reads them once per KV head but
- * has no split-KV, when G is in {1,2,4,8,16} and
- * ceil(G * k / 16) * min(num_seqs * num_kv_heads, SMs) * 10 >= 21 * SMs
- * (SMs: the current device's multiprocessors; 152 if none is found) -- the
- * route measured faster.
+ * (then q and out must be 16-B aligned), which reads them once per row tile and
+ * splits the keys when its CTAs cannot fill the GPU, when G is in {1,2,4,8,16}
+ * and G * k >= 32 -- the route measured faster (paged_attention_verify_on
+ * picks one explicitly).
  * num_seqs * k must not exceed 65535 (PKV_ERR_UNSUPPORTED).  A sequence with
  * ctx < k sets PKV_STATUS_BAD_Q_LEN and gets zero rows.
  * Workspace: paged_attention_verify_workspace_size() bytes (sized for the route
@@ -558,7 +557,7 @@ PKV_API int paged_attention_verify_on(int32_t kernel, void *out, int32_t out_dty
  * paged_attention_verify_on_prefill -- the kernel paged_attention_verify (and
  * _window / _fp8, per cache->dtype) takes for these sizes on the current
  * device: 1 the tcgen05 prefill kernel, 0 the decode kernel; a negative
- * PKV_ERR_* for invalid arguments.  Needs no GPU (152 SMs assumed).
+ * PKV_ERR_* for invalid arguments.  Needs no GPU.
  */
 PKV_API int paged_attention_verify_on_prefill(int32_t num_seqs, int32_t q_per_seq, int32_t num_q_heads,
                                               const pkv_cache_desc *cache);
@@ -591,9 +590,9 @@ PKV_API int paged_attention_verify_window(void *out, int32_t out_dtype, const vo
  * none).  On the decode kernel, one 8-column MMA tile per CTA: the G * k
  * (position, head) columns of a KV head are shared out over ceil(G * k / 8)
  * CTAs, each reading the K/V codes once; or, when G is in {1,2,4,8,16} and
- * G * k * min(num_seqs * num_kv_heads, SMs) >= 40 * SMs, on the FP8 prefill
- * kernel (paged_attention_prefill_chunk_fp8 with k rows per sequence; q and out
- * then 16-B aligned), which reads the codes once per KV head.  Workspace:
+ * G * k >= 32, on the FP8 prefill kernel (paged_attention_prefill_chunk_fp8
+ * with k rows per sequence, split-KV for few units; q and out then 16-B
+ * aligned), which reads the codes once per row tile.  Workspace:
  * paged_attention_verify_workspace_size() with the FP8 cache descriptor.
  * Errors: as paged_attention_verify; PKV_ERR_INVALID_ARG for a missing or
  * misaligned scale array.

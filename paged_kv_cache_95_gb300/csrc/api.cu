@@ -744,20 +744,19 @@ int64_t route_sms() {
 
 // Verify runs on the decode kernel (the G x k (position, head) columns of a KV head
 // shared out over ceil(G * k / 16) CTAs of up to 16 MMA columns, 8 over an FP8
-// cache, each reading the K/V) or on the prefill kernel (uniform q_len; K/V read
-// once per 256 rows, no split-KV, so its time is set by how many SMs its
-// num_seqs x n_kv CTAs fill).  Measured on the 8B-shaped (B=64, G=4) and
-// 70B-shaped (B=8 x 32K, G=8) batches, the decode route costs about
-// ceil(cols / 16) x 0.44 x min(units, SMs) / SMs times the prefill route for
-// bf16 and cols x min(units, SMs) / (37 x SMs) for FP8 (units = num_seqs x n_kv);
-// the prefill route is taken from a ratio of about 0.92 (bf16) / 1.08 (FP8) up,
-// where the prefill kernel can pack the group (G in {1, 2, 4, 8, 16}).
-bool verify_on_prefill(bool fp8, int32_t num_seqs, int32_t q_per_seq, int32_t G, int32_t n_kv) {
+// cache, each reading the K/V) or on the prefill kernel (uniform q_len, K/V read
+// once per row tile, split-KV when its CTAs cannot fill the GPU).  The decode
+// route's time grows with the columns; the prefill route's is flat in k.
+// Measured on a GB300 (us, decode route / prefill route):
+//   8B-shaped B=64, G=4, k = 2 4 6 8 12 16:  104/207 128/207 191/207 206/207 296/207 388/207
+//     FP8:                                   78/243 134/244 189/244 244/244 357/244 471/244
+//   70B-shaped B=8 x 32K, G=8, k = 1 2 4 8 16: 171/283 200/286 295/290 570/295 1122/310
+//     FP8:                                   116/338 195/340 373/343 730/350 1445/364
+// so the prefill kernel is taken from G * k >= 32 columns on, where it can pack
+// the group (G in {1, 2, 4, 8, 16}); below, the decode kernel.
+bool verify_on_prefill(bool /*fp8*/, int32_t /*num_seqs*/, int32_t q_per_seq, int32_t G, int32_t /*n_kv*/) {
     if (G > 16 || 128 % G != 0) return false;
-    const int64_t cols = static_cast<int64_t>(G) * q_per_seq;
-    const int64_t sms = route_sms();
-    const int64_t units = std::min<int64_t>(static_cast<int64_t>(num_seqs) * n_kv, sms);
-    return fp8 ? cols * units >= 40 * sms : (cols + 15) / 16 * units * 10 >= 21 * sms;
+    return static_cast<int64_t>(G) * q_per_seq >= 32;
 }
 // CTAs per KV head and the columns each takes (the last one may take fewer): up to
 // 16 columns (two 8-column MMA tiles) per CTA, 8 over an FP8 cache (one tile).

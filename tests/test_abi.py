@@ -158,15 +158,16 @@ def test_verify_argument_errors(lib):
     assert v(2, q=None) == P.PKV_ERR_INVALID_ARG
     assert v(2, nq=96) == P.PKV_ERR_UNSUPPORTED                 # G = 12
     assert v(2, wsb=100) == P.PKV_ERR_WORKSPACE_TOO_SMALL       # decode path (G * k = 8)
-    assert v(8, wsb=100) == P.PKV_ERR_WORKSPACE_TOO_SMALL       # decode path, two CTAs per KV head (G * k = 32)
+    assert v(6, wsb=100) == P.PKV_ERR_WORKSPACE_TOO_SMALL       # decode path, two CTAs per KV head (G * k = 24)
     assert v(16, out=FAKE + 4, B=64) == P.PKV_ERR_INVALID_ARG   # prefill path (G * k = 64, 512 units): 16-B out
     ws = lambda k: lib.paged_attention_verify_workspace_size(64, k, 32, 256, 0, ctypes.byref(c))
     assert ws(0) == 0 and ws(17) == 0
     assert ws(16) == 256                                        # prefill path: the status word
     # decode path: partials for 64 * k rows of 32 heads
     assert ws(2) > lib.paged_attention_workspace_size(64, 32, 256, 0, ctypes.byref(c))
-    assert ws(8) > ws(4) > ws(2)
-    # 4 sequences x 8 KV heads = 32 units fill few SMs: G * k = 64 stays on the decode kernel
+    assert ws(6) > ws(4) > ws(2)
+    # 4 sequences x 8 KV heads = 32 units fill few SMs: the prefill kernel splits the keys
+    # (partials of 4 * k rows of 32 heads per split in the workspace)
     ws4 = lambda k: lib.paged_attention_verify_workspace_size(4, k, 32, 256, 0, ctypes.byref(c))  # noqa: E731
     assert ws4(16) > ws4(8) > 256
 
@@ -288,10 +289,10 @@ def test_verify_fp8_argument_errors(lib):
     assert v(0) == P.PKV_ERR_INVALID_ARG
     assert v(2, wsb=100) == P.PKV_ERR_WORKSPACE_TOO_SMALL
     ws = lambda k: lib.paged_attention_verify_workspace_size(64, k, 32, 256, 0, ctypes.byref(c8))  # noqa: E731
-    assert ws(8) > ws(4) > 256                                   # decode kernel, one 8-column tile per CTA
+    assert ws(6) > ws(4) > 256                                   # decode kernel, one 8-column tile per CTA
     assert ws(16) == 256                                         # G * k = 64 over 512 units: the prefill kernel
     ws4 = lambda k: lib.paged_attention_verify_workspace_size(4, k, 32, 256, 0, ctypes.byref(c8))  # noqa: E731
-    assert ws4(16) > ws4(8) > 256                                # 32 units: the decode kernel
+    assert ws4(16) > ws4(8) > 256                                # 32 units: the prefill kernel splits the keys
 
 
 def test_prefill_fp8_argument_errors(lib):
@@ -310,17 +311,18 @@ def test_prefill_fp8_argument_errors(lib):
     assert lib.paged_attention_prefill_workspace_size(4, 32, ctypes.byref(c8)) > 0
 
 
-# (sequences, q heads, KV heads, k, FP8, the route measured faster on a 152-SM GB300):
-# 8B-shaped B=64 (G=4) and 70B-shaped B=8 x 32K (G=8), decode route vs prefill route.
+# (sequences, q heads, KV heads, k, FP8, the route measured faster on a GB300;
+# decode route / prefill route in us, the prefill kernel splitting the keys of the
+# 70B-shaped batch): 8B-shaped B=64 (G=4) and 70B-shaped B=8 x 32K (G=8).
 MEASURED_VERIFY_ROUTES = [
-    *[(64, 32, 8, k, False, "decode") for k in (4, 5, 6, 8)],          # 120-194 us vs ~205 us
-    *[(64, 32, 8, k, False, "prefill") for k in (12, 16)],             # 278 / 365 vs 205 / 207 us
-    *[(8, 64, 8, k, False, "decode") for k in (4, 5, 6, 8)],           # 287-559 vs ~604 us
-    *[(8, 64, 8, k, False, "prefill") for k in (12, 16)],              # 833 / 1106 vs 605 us
-    *[(64, 32, 8, k, True, "decode") for k in (1, 2, 4, 8)],           # 69-248 vs ~283 us
-    (64, 32, 8, 16, True, "prefill"),                                  # 481 vs 285 us
-    *[(8, 64, 8, k, True, "decode") for k in (1, 2, 4, 8)],            # 114-772 vs ~945 us
-    (8, 64, 8, 16, True, "prefill"),                                   # 1530 vs 945 us
+    *[(64, 32, 8, k, False, "decode") for k in (2, 4, 6)],             # 104-191 vs ~207 us
+    *[(64, 32, 8, k, False, "prefill") for k in (12, 16)],             # 296 / 388 vs 207 us
+    *[(8, 64, 8, k, False, "decode") for k in (1, 2)],                 # 171 / 200 vs 283 / 286 us
+    *[(8, 64, 8, k, False, "prefill") for k in (4, 8, 16)],            # 295 / 570 / 1122 vs 290 / 295 / 310 us
+    *[(64, 32, 8, k, True, "decode") for k in (1, 2, 4, 6)],           # 70-189 vs ~244 us
+    (64, 32, 8, 16, True, "prefill"),                                  # 471 vs 244 us
+    *[(8, 64, 8, k, True, "decode") for k in (1, 2)],                  # 116 / 195 vs 338 / 340 us
+    *[(8, 64, 8, k, True, "prefill") for k in (4, 8, 16)],             # 373 / 730 / 1445 vs 343 / 350 / 364 us
 ]
 
 

@@ -162,9 +162,10 @@ def test_fp8_decode_window_and_bf16_out():
 
 @pytest.mark.parametrize("n_q,n_kv,k", [(32, 8, 1), (32, 8, 2), (64, 8, 4), (32, 32, 16), (32, 1, 3)])
 def test_fp8_verify_parity(n_q, n_kv, k):
-    """Verify over the FP8 cache (paged_attention_verify_fp8): row i at pos = ctx - k + i
-    sees keys j <= pos (and pos - W < j under a window), one 8-column MMA tile per CTA,
-    so G * k = 8, 32, 96 columns take 1, 4, 12 CTAs per KV head; split partitions."""
+    """Verify over the FP8 cache: row i at pos = ctx - k + i sees keys j <= pos (and
+    pos - W < j under a window).  On the decode kernel (forced), one 8-column MMA tile
+    per CTA, so G * k = 8, 32, 96 columns take 1, 4, 12 CTAs per KV head, with split
+    partitions; on the library's own route (paged_attention_verify_fp8) too."""
     t = torch()
     ctx = [max(c, k) for c in (16, 17, 33, 100, 256, 257, 700, 1000)] + [k, k + 1]
     wl, batch = W.make_custom(n_q, n_kv, ctx, q_lens=[k] * len(ctx), seed=560 + 3 * k + n_q // n_kv,
@@ -174,21 +175,22 @@ def test_fp8_verify_parity(n_q, n_kv, k):
     q = bf16_to_dev(batch.q)
     for win in (0, 17, 300):
         ref = d.oracle(batch, window=win)
-        for part in (0, 16):
+        for kernel, part in ((P.PKV_VERIFY_DECODE_KERNEL, 0), (P.PKV_VERIFY_DECODE_KERNEL, 16),
+                             (P.PKV_VERIFY_AUTO, 0)):
             out = t.full(q.shape, float("nan"), dtype=t.float32, device="cuda")
             ws = P.paged_attention_verify(out, q, k, d.k_cache, d.v_cache, i32_to_dev(batch.block_tables),
                                           i32_to_dev(batch.context_lens), wl.scale, partition_size=part,
-                                          window=win, k_scale=d.k_scale, v_scale=d.v_scale)
-            assert_close(out.cpu().numpy(), ref, what=f"G={n_q // n_kv} k={k} W={win} part={part}")
+                                          window=win, k_scale=d.k_scale, v_scale=d.v_scale, kernel=kernel)
+            assert_close(out.cpu().numpy(), ref, what=f"G={n_q // n_kv} k={k} W={win} kernel={kernel} part={part}")
             assert status_word(ws) == 0
 
 
 @pytest.mark.parametrize("n_q,n_kv,k,nseq", [(32, 8, 16, 16), (32, 2, 8, 24)])
 def test_fp8_verify_prefill_route(n_q, n_kv, k, nseq):
     """FP8 verify with many columns (G * k = 64 over 128 KV-head units, 128 over 48)
-    runs on the FP8 prefill kernel on a 152-SM GPU: parity with the oracle, and the
-    result is bit-identical to paged_attention_prefill_chunk_fp8 with k rows per
-    sequence (the route's own kernel)."""
+    runs on the FP8 prefill kernel: parity with the oracle, and the result is
+    bit-identical to paged_attention_prefill_chunk_fp8 with k rows per sequence (the
+    route's own kernel, with the same split plan)."""
     t = torch()
     base = (16, 17, 33, 100, 256, 257, 700, 1000, 5, 129, 128, 300, 64, 999, 2000, 31)
     ctx = [max(base[i % len(base)] + 7 * (i // len(base)), k) for i in range(nseq)]
@@ -206,8 +208,7 @@ def test_fp8_verify_prefill_route(n_q, n_kv, k, nseq):
         assert_close(out.cpu().numpy(), ref, what=f"G={n_q // n_kv} k={k} W={win}")
         assert status_word(ws) == 0
         pf, _ = d.prefill(batch, window=win)
-        if t.cuda.get_device_properties(0).multi_processor_count == 152:
-            assert t.equal(out, pf), "FP8 verify did not take the prefill route"
+        assert t.equal(out, pf), "FP8 verify did not take the prefill route"
 
 
 def test_fp8_verify_last_row_is_fp8_decode():

@@ -9,6 +9,8 @@ that, ragged shares included) and the tcgen05 prefill kernel (taken when G * k
 columns over enough sequences x KV heads make it faster, and G packs its tiles)
 are both covered, and a test pins which one a batch takes.
 """
+import ctypes
+
 import numpy as np
 import pytest
 
@@ -28,12 +30,10 @@ def _lib(built_library):
 
 
 def _on_decode(G, k, nseq, n_kv):
-    """The library's route: the prefill kernel when it can pack the group and
-    ceil(G k / 16) x min(units, SMs) x 10 >= 21 x SMs (units = sequences x KV heads)."""
+    """The library's route: the prefill kernel when it can pack the group and G k >= 32."""
     if G > 16 or 128 % G:
         return True
-    sms = torch().cuda.get_device_properties(0).multi_processor_count
-    return -(-G * k // 16) * min(nseq * n_kv, sms) * 10 < 21 * sms
+    return G * k < 32
 
 
 def _verify(d, batch, k, partition_size=0, out_dtype=None, context_lens=None, window=0, tables=None):
@@ -139,10 +139,10 @@ def test_verify_window_errors():
 
 @pytest.mark.parametrize("n_q,n_kv,k,nseq", [(32, 8, 16, 16), (64, 8, 16, 12), (64, 8, 8, 4), (32, 8, 16, 3)])
 def test_verify_route_by_units(n_q, n_kv, k, nseq):
-    """G * k = 64 or 128 columns: over 96-128 sequence x KV-head units the prefill
-    kernel (the result is bit-identical to paged_attention_prefill_chunk with k rows
-    per sequence on a 152-SM GPU); over 24-32 units the decode kernel with 4 to 8
-    CTAs of 16 columns per KV head.  Both against the oracle."""
+    """G * k = 64 or 128 columns over 24-128 sequence x KV-head units: the prefill
+    kernel (splitting the keys where its CTAs cannot fill the GPU); the result is
+    bit-identical to paged_attention_prefill_chunk with k rows per sequence (same
+    split plan), and both kernels forced match the oracle."""
     t = torch()
     base = (16, 17, 33, 100, 256, 257, 700, 1000, 5, 129, 128, 300, 64, 999, 2000, 31)
     ctx = [max(base[i], k) for i in range(nseq)]
@@ -158,11 +158,17 @@ def test_verify_route_by_units(n_q, n_kv, k, nseq):
         out, ws = _verify(d, batch, k, partition_size=part)
         assert_close(out.cpu().numpy(), ref, what=f"G={G} k={k} B={nseq} part={part}")
         assert status_word(ws) == 0
-    if t.cuda.get_device_properties(0).multi_processor_count == 152:
-        assert on_decode == (nseq * n_kv < 64)
-        if not on_decode:
-            pf, _ = d.prefill(batch)
-            assert t.equal(out, pf), "verify did not take the prefill route"
+    c = P.CacheDesc(wl.num_blocks, 16, n_kv, 128, P.PKV_DTYPE_BF16)
+    assert P.load_library().paged_attention_verify_on_prefill(nseq, k, n_q, ctypes.byref(c)) == (0 if on_decode else 1)
+    if not on_decode:
+        pf, _ = d.prefill(batch)
+        assert t.equal(out, pf), "verify did not take the prefill route"
+    q = bf16_to_dev(batch.q)
+    for kernel in (P.PKV_VERIFY_DECODE_KERNEL, P.PKV_VERIFY_PREFILL_KERNEL):
+        o = t.full(q.shape, float("nan"), dtype=t.float32, device="cuda")
+        P.paged_attention_verify(o, q, k, d.k_cache, d.v_cache, i32_to_dev(batch.block_tables),
+                                 i32_to_dev(batch.context_lens), wl.scale, kernel=kernel)
+        assert_close(o.cpu().numpy(), ref, what=f"G={G} k={k} B={nseq} kernel={kernel}")
 
 
 @pytest.mark.parametrize("n_q,n_kv,k", [(32, 8, 1), (32, 8, 4), (32, 8, 16), (64, 8, 2), (64, 8, 16), (32, 32, 3),
