@@ -186,9 +186,9 @@ __global__ void __launch_bounds__(NW * 32)
     __syncthreads();
     constexpr int kIssueLanes = FP8 ? 8 : 1;  // lanes that take part in a stage's copies
 
-    // Lanes < kIssueLanes of the producer: start the copies of the group's i-th block into stage i % R.
-    auto issue = [&](int i) {
-        const int s = i % R;
+    // Lanes < kIssueLanes of the producer: start the copies of the group's i-th block into
+    // stage s (= i % R; the ring position is tracked incrementally, R is a runtime value).
+    auto issue = [&](int i, int s) {
         const int j = blk_begin + gi + NG * i;
         int phys = __ldg(table + j);
         if (static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_blocks)) phys = 0;  // masked below
@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(NW * 32)
     if (producer) {
         issued = min(R, nmine);
         if (lane < kIssueLanes)
-            for (int i = 0; i < issued; ++i) issue(i);
+            for (int i = 0; i < issued; ++i) issue(i, i);
     }
 
     // ---- Q^T as the B operand (16 dims x 8 heads per k-step), kept in registers ----
@@ -241,10 +241,11 @@ __global__ void __launch_bounds__(NW * 32)
 
     int consumed = 0;
     bool timed_out = false;
+    int s = 0;         // stage of block i: i % R
+    uint32_t ph = 0;   // its phase parity: (i / R) & 1
     for (int i = 0; i < nmine; ++i) {
-        const int s = i % R;
         const uint32_t bar = bar_base + 8 * s;
-        bool ok = mbar_wait(bar, (i / R) & 1);
+        bool ok = mbar_wait(bar, ph);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) {
             timed_out = true;
@@ -311,7 +312,7 @@ __global__ void __launch_bounds__(NW * 32)
         if (T > 1 && lane == 0) mbar_arrive(empty_base + 8 * s);  // this warp is done with stage s
         if (producer && i + R < nmine) {
             if (T > 1) {  // the group's other warps must be done with stage s before it is refilled
-                bool eok = mbar_wait(empty_base + 8 * s, (i / R) & 1);
+                bool eok = mbar_wait(empty_base + 8 * s, ph);
                 eok = __all_sync(0xffffffffu, eok);
                 if (!eok) {
                     timed_out = true;
@@ -320,9 +321,13 @@ __global__ void __launch_bounds__(NW * 32)
             }
             if (lane < kIssueLanes) {
                 fence_proxy_async_smem();
-                issue(i + R);
+                issue(i + R, s);
             }
             ++issued;
+        }
+        if (++s == R) {
+            s = 0;
+            ph ^= 1u;
         }
     }
 
