@@ -178,21 +178,6 @@ int check_group(int32_t n_q, int32_t n_kv) {
     return PKV_OK;
 }
 
-// Query heads (MMA columns) per decode CTA and 8-column tiles per block group: a
-// group of up to 8 heads fills one tile; groups of 16 and 32 heads (and their
-// multiples) run as 2 or 4 tiles side by side in one CTA, one per warp of a
-// block group, so each K/V tile still leaves HBM once per KV head.
-struct DecodeTiles {
-    int32_t heads_per_cta, col_tiles, head_splits;
-};
-DecodeTiles decode_tiles(int32_t G) {
-    DecodeTiles t{G < 8 ? G : 8, 1, 1};
-    if (G % 32 == 0) t = {32, 4, 1};
-    else if (G % 16 == 0) t = {16, 2, 1};
-    t.head_splits = G / t.heads_per_cta;
-    return t;
-}
-
 // ---- decode plan -----------------------------------------------------------------------
 // Workspace layout: [status word | part_m | part_l | part_o], each region
 // 256-byte aligned; only the status word when nothing is split.
@@ -362,7 +347,7 @@ int32_t paged_attention_decode_partitions(int32_t num_seqs, int32_t num_q_heads,
                                           max_blocks_per_seq, (static_cast<int64_t>(window) + 15) / kBlockSize + 1))
                                     : max_blocks_per_seq;
     const int32_t G = num_q_heads / cache->num_kv_heads;
-    const int32_t head_splits = decode_tiles(G).head_splits;
+    const int32_t head_splits = G / (G < 8 ? G : 8);
     int32_t pb = partition_size / kBlockSize;
     if (partition_size == 0) {
         const int dev = current_device();
@@ -414,9 +399,8 @@ int decode_impl(void *out, int32_t out_dtype, const void *q, const void *k_cache
 
     const int32_t n_kv = cache->num_kv_heads;
     const int32_t G = num_q_heads / n_kv;
-    const DecodeTiles tiles = decode_tiles(G);
-    const int32_t hpc = tiles.heads_per_cta;
-    const int32_t head_splits = tiles.head_splits;
+    const int32_t hpc = G < 8 ? G : 8;  // query heads per CTA; larger groups are split over CTAs
+    const int32_t head_splits = G / hpc;
     if (static_cast<int64_t>(n_kv) * head_splits > 65535) return PKV_ERR_UNSUPPORTED;
 
     const int dev = current_device();
@@ -459,7 +443,6 @@ int decode_impl(void *out, int32_t out_dtype, const void *q, const void *k_cache
     p.group = G;
     p.heads_per_cta = hpc;
     p.head_splits = head_splits;
-    p.col_tiles = tiles.col_tiles;
     p.max_blocks = max_blocks_per_seq;
     p.num_blocks = cache->num_blocks;
     p.part_blocks = pl.part_blocks;
@@ -901,7 +884,6 @@ int verify_impl(void *out, int32_t out_dtype, const void *q, int32_t q_per_seq, 
     p.group = G;
     p.heads_per_cta = verify_cols_per_cta(cols, fp8);  // the CTA's share of the q_per_seq x G columns
     p.head_splits = splits;
-    p.col_tiles = 1;
     p.max_blocks = max_blocks_per_seq;
     p.num_blocks = cache->num_blocks;
     p.part_blocks = pl.part_blocks;

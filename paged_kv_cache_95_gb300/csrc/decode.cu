@@ -141,18 +141,7 @@ __global__ void __launch_bounds__(NW * 32)
     if (part >= nparts) return;
     const int blk_begin = first_blk + part * p.part_blocks;
     const int nblk = min(p.part_blocks, nblocks - blk_begin);
-    // Block groups: the warps form NG = NW / T groups of T warps.  Group gi consumes
-    // blocks blk_begin + gi, + NG, ... through one ring of R = ST * T stages that its
-    // T warps all read; warp ti of the group owns the group's ti-th 8-column MMA tile
-    // (heads h0 + 8 ti ..).  T = 1 (groups of up to 8 heads): every warp is a group
-    // with its own ring.  T = 2, 4 (16, 32 heads): the CTA still reads each K/V tile
-    // from HBM once for the whole group.
-    const int T = VERIFY ? 1 : p.col_tiles;
-    const int NG = NW / T;
-    const int gi = warp / T, ti = warp - gi * T;
-    const int R = ST * T;
-    const bool producer = ti == 0;  // the group's first warp issues its copies
-    const int nmine = nblk > gi ? (nblk - gi + NG - 1) / NG : 0;
+    const int nmine = nblk > warp ? (nblk - warp + NW - 1) / NW : 0;
     const int32_t *table = p.block_tables + static_cast<size_t>(b) * p.max_blocks;
 
     // Append: lane l holds 16 bytes of the new row (K for lanes 0-15, V for 16-31;
@@ -166,30 +155,22 @@ __global__ void __launch_bounds__(NW * 32)
         }
     }
 
-    // Shared memory: [stage rings (NW * ST stages) | FP8 scale rows | full barriers |
-    // empty barriers | append barriers (one per group)].
-    const uint32_t stage_base = smem_u32(smem) + gi * (R * kStage);
-    const uint32_t scale_base = smem_u32(smem) + NW * ST * kStage + gi * (FP8 ? R * kStageScaleBytes : 0);
-    const uint32_t bars = smem_u32(smem) + NW * ST * kStage + (FP8 ? NW * ST * kStageScaleBytes : 0);
-    const uint32_t bar_base = bars + gi * R * 8;                   // stage s full: its copies landed
-    const uint32_t empty_base = bars + NW * ST * 8 + gi * R * 8;   // stage s empty: T warps done with it
-    const uint32_t app_bar = bars + 2 * NW * ST * 8 + gi * 8;      // the appended row is in the stage
+    const uint32_t stage_base = smem_u32(smem) + warp * (ST * kStage);
+    // FP8: the scale rows of each stage sit after all warps' code rings.
+    const uint32_t scale_base = smem_u32(smem) + NW * ST * kStage + warp * (FP8 ? ST * kStageScaleBytes : 0);
+    const uint32_t bar_base = smem_u32(smem) + NW * ST * kStage + (FP8 ? NW * ST * kStageScaleBytes : 0) + warp * ST * 8;
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < NW * ST; ++s) {
-            mbar_init(bars + 8 * s, FP8 ? kFp8StageArrivals : 1);
-            mbar_init(bars + NW * ST * 8 + 8 * s, T);
-        }
-        for (int q = 0; q < NW; ++q) mbar_init(bars + 2 * NW * ST * 8 + 8 * q, 32);
+    if (lane == 0) {
+        for (int s = 0; s < ST; ++s) mbar_init(bar_base + 8 * s, FP8 ? kFp8StageArrivals : 1);
         fence_mbar_init();
     }
-    __syncthreads();
+    __syncwarp();
     constexpr int kIssueLanes = FP8 ? 8 : 1;  // lanes that take part in a stage's copies
 
-    // Lanes < kIssueLanes of the producer: start the copies of the group's i-th block into
-    // stage s (= i % R; the ring position is tracked incrementally, R is a runtime value).
-    auto issue = [&](int i, int s) {
-        const int j = blk_begin + gi + NG * i;
+    // Lanes < kIssueLanes: start the copies of this warp's i-th block into stage i % ST.
+    auto issue = [&](int i) {
+        const int s = i % ST;
+        const int j = blk_begin + warp + NW * i;
         int phys = __ldg(table + j);
         if (static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_blocks)) phys = 0;  // masked below
         if constexpr (FP8)
@@ -198,12 +179,8 @@ __global__ void __launch_bounds__(NW * 32)
         else
             issue_block_copy(&kmap, &vmap, stage_base + s * kStage, bar_base + 8 * s, g, phys);
     };
-    int issued = 0;
-    if (producer) {
-        issued = min(R, nmine);
-        if (lane < kIssueLanes)
-            for (int i = 0; i < issued; ++i) issue(i, i);
-    }
+    if (lane < kIssueLanes)
+        for (int i = 0; i < ST && i < nmine; ++i) issue(i);
 
     // ---- Q^T as the B operand (16 dims x 8 heads per k-step), kept in registers ----
     const int n = lane >> 2;  // head column of B / row group of C
@@ -211,18 +188,17 @@ __global__ void __launch_bounds__(NW * 32)
     uint32_t bqt[NCT][8][2];
     auto &bq = bqt[0];
     float sl2 = p.scale_log2;
-    const int tcols = min(8, hpc - 8 * ti);  // decode: heads of this warp's tile
     if constexpr (FP8 && VERIFY) {
         const int qexp = load_q_frag_fp8_row(bq, p.q, col_row(n), n < ncols, lane);
         sl2 *= ldexpf(1.f, -qexp);
     } else if constexpr (FP8) {
-        const int qexp = load_q_frag_fp8(bq, p.q, static_cast<size_t>(b) * p.n_q + h0 + 8 * ti, tcols, lane);
+        const int qexp = load_q_frag_fp8(bq, p.q, static_cast<size_t>(b) * p.n_q + h0, hpc, lane);
         sl2 *= ldexpf(1.f, -qexp);
     } else if constexpr (VERIFY) {
 #pragma unroll
         for (int t = 0; t < NCT; ++t) load_q_frag_row(bqt[t], p.q, col_row(8 * t + n), 8 * t + n < ncols, lane);
     } else {
-        load_q_frag(bq, p.q, static_cast<size_t>(b) * p.n_q + h0 + 8 * ti, tcols, lane);
+        load_q_frag(bq, p.q, static_cast<size_t>(b) * p.n_q + h0, hpc, lane);
     }
     // Verify: the absolute causal bound (exclusive) of this lane's columns 8t + 2*q4 and 8t + 2*q4 + 1.
     int pos_end[NCT][2] = {};
@@ -241,49 +217,38 @@ __global__ void __launch_bounds__(NW * 32)
 
     int consumed = 0;
     bool timed_out = false;
-    int s = 0;         // stage of block i: i % R
-    uint32_t ph = 0;   // its phase parity: (i / R) & 1
     for (int i = 0; i < nmine; ++i) {
+        const int s = i % ST;
         const uint32_t bar = bar_base + 8 * s;
-        bool ok = mbar_wait(bar, ph);
+        bool ok = mbar_wait(bar, (i / ST) & 1);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) {
             timed_out = true;
             break;
         }
-        const int j = blk_begin + gi + NG * i;
+        const int j = blk_begin + warp + NW * i;
         const int phys = __ldg(table + j);
         int valid = min(kBlockSize, ctx - j * kBlockSize);
         const int lo = j == first_blk ? j0 - j * kBlockSize : 0;
         if (static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_blocks)) {
             valid = 0;
-            if (lane == 0 && ti == 0 && p.status) atomicOr(p.status, kStatusBadBlockId);
+            if (lane == 0 && p.status) atomicOr(p.status, kStatusBadBlockId);
         }
         const uint32_t kb = stage_base + s * kStage;
         if constexpr (APPEND) {
             if (ctx_ok && j == nblocks - 1 && valid > 0) {
-                if (producer) {
-                    // The new row r of the last block: into the group's copy of the block (K and V,
-                    // 16 bytes per lane at the swizzled position) and, from one CTA per KV head, to the pool.
-                    const int r = (ctx - 1) & (kBlockSize - 1);
-                    const int box = (lane >> 3) & 1, ch = lane & 7;
-                    sts128(kb + (lane >> 4) * kTileBytes + box * kBoxBytes + r * 128 + ((ch ^ (r & 7)) << 4), app);
-                    if (hsl == 0) {
-                        void *pool = lane < 16 ? p.k_cache : p.v_cache;
-                        const size_t e = ((static_cast<size_t>(phys) * p.n_kv + g) * kBlockSize + r) * kHeadDim +
-                                         64 * box + 8 * ch;
-                        *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(pool) + e) = app;
-                    }
-                    if (T > 1) mbar_arrive(app_bar);  // every lane: its 16 bytes are in the stage
-                    __syncwarp();
-                } else {
-                    bool aok = mbar_wait(app_bar, 0);
-                    aok = __all_sync(0xffffffffu, aok);
-                    if (!aok) {
-                        timed_out = true;
-                        break;
-                    }
+                // The new row r of the last block: into this warp's copy of the block (K and V,
+                // 16 bytes per lane at the swizzled position) and, from one CTA per KV head, to the pool.
+                const int r = (ctx - 1) & (kBlockSize - 1);
+                const int box = (lane >> 3) & 1, ch = lane & 7;
+                sts128(kb + (lane >> 4) * kTileBytes + box * kBoxBytes + r * 128 + ((ch ^ (r & 7)) << 4), app);
+                if (hsl == 0) {
+                    void *pool = lane < 16 ? p.k_cache : p.v_cache;
+                    const size_t e = ((static_cast<size_t>(phys) * p.n_kv + g) * kBlockSize + r) * kHeadDim +
+                                     64 * box + 8 * ch;
+                    *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(pool) + e) = app;
                 }
+                __syncwarp();
             }
         }
         if constexpr (FP8 && VERIFY) {
@@ -309,32 +274,17 @@ __global__ void __launch_bounds__(NW * 32)
         consumed = i + 1;
 
         __syncwarp();
-        if (T > 1 && lane == 0) mbar_arrive(empty_base + 8 * s);  // this warp is done with stage s
-        if (producer && i + R < nmine) {
-            if (T > 1) {  // the group's other warps must be done with stage s before it is refilled
-                bool eok = mbar_wait(empty_base + 8 * s, ph);
-                eok = __all_sync(0xffffffffu, eok);
-                if (!eok) {
-                    timed_out = true;
-                    break;
-                }
-            }
-            if (lane < kIssueLanes) {
-                fence_proxy_async_smem();
-                issue(i + R, s);
-            }
-            ++issued;
-        }
-        if (++s == R) {
-            s = 0;
-            ph ^= 1u;
+        if (lane < kIssueLanes && i + ST < nmine) {
+            fence_proxy_async_smem();
+            issue(i + ST);
         }
     }
 
     if (timed_out) {
         if (lane == 0 && p.status) atomicOr(p.status, kStatusTimeout);
-        // Let the copies this warp issued that are still in flight land before the CTA exits.
-        for (int i = consumed; i < issued; ++i) mbar_wait(bar_base + 8 * (i % R), (i / R) & 1);
+        // Let this warp's copies still in flight land before the CTA exits.
+        const int issued = min(nmine, consumed + ST);
+        for (int i = consumed; i < issued; ++i) mbar_wait(bar_base + 8 * (i % ST), (i / ST) & 1);
     }
 
     if constexpr (FP8) fp8_finish(acc);
@@ -371,19 +321,18 @@ __global__ void __launch_bounds__(NW * 32)
     }
     __syncthreads();
 
-    // Column hh is column hh % kCols of tile hh / kCols, held by warp gg * T + hh / kCols of
-    // every group gg: slot (gg * T + hh / kCols) * kCols + hh % kCols = gg * T * kCols + hh.
     for (int idx = threadIdx.x; idx < ncols * kHeadDim; idx += NW * 32) {
         const int hh = idx >> 7, d = idx & 127;
         float M = -INFINITY;
-        for (int gg = 0; gg < NG; ++gg) M = fmaxf(M, red_m[gg * T * kCols + hh]);
+#pragma unroll
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, red_m[w * kCols + hh]);
         const float Mu = M == -INFINITY ? 0.f : M;
         float L = 0.f, O = 0.f;
-        for (int gg = 0; gg < NG; ++gg) {
-            const int slot = gg * T * kCols + hh;
-            const float f = fast_exp2(red_m[slot] - Mu);
-            L += f * red_l[slot];
-            O += f * red_o[slot * kHeadDim + d];
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            const float f = fast_exp2(red_m[w * kCols + hh] - Mu);
+            L += f * red_l[w * kCols + hh];
+            O += f * red_o[(w * kCols + hh) * kHeadDim + d];
         }
         const size_t row = col_row(hh);
         if (nparts == 1) {
@@ -516,9 +465,8 @@ constexpr int kFp8Warps = 4, kFp8Stages = 3;
 }  // namespace
 
 size_t decode_smem_bytes() {
-    // stage rings + full and empty mbarriers per stage + one append mbarrier per warp
-    // + 1 KB for aligning the base to the 1 KB swizzle period
-    return static_cast<size_t>(kWarps) * kStages * (kStageBytes + 16) + static_cast<size_t>(kWarps) * 8 + 1024;
+    // stage ring + mbarriers + 1 KB for aligning the base to the 1 KB swizzle period
+    return static_cast<size_t>(kWarps) * kStages * kStageBytes + static_cast<size_t>(kWarps) * kStages * 8 + 1024;
 }
 
 cudaError_t decode_prepare_device() {
@@ -537,8 +485,7 @@ cudaError_t decode_prepare_device() {
 }
 
 size_t decode_fp8_smem_bytes() {
-    return static_cast<size_t>(kFp8Warps) * kFp8Stages * (kStageBytes8 + kStageScaleBytes + 16) +
-           static_cast<size_t>(kFp8Warps) * 8 + 1024;
+    return static_cast<size_t>(kFp8Warps) * kFp8Stages * (kStageBytes8 + kStageScaleBytes + 8) + 1024;
 }
 
 cudaError_t decode_fp8_prepare_device() {

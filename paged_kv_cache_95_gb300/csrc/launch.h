@@ -58,9 +58,8 @@ struct DecodeParams {
     uint32_t *status;            // device status word
     int32_t num_seqs, n_q, n_kv;
     int32_t group;               // G = n_q / n_kv
-    int32_t heads_per_cta;       // query heads (MMA columns) per CTA: G <= 8: G; 16 or 32 for larger groups
+    int32_t heads_per_cta;       // min(G, 8)
     int32_t head_splits;         // G / heads_per_cta
-    int32_t col_tiles;           // T: 8-column tiles per CTA, one per warp of a block group (1, 2 or 4)
     int32_t max_blocks;          // block-table row length
     int32_t num_blocks;          // pool size
     int32_t part_blocks;         // blocks per partition
