@@ -28,6 +28,7 @@ constexpr int kMinPartBlocks = 16;      // automatic plans never go below 256 to
 constexpr int kDefaultPartBlocks = 64;  // 1024 tokens
 constexpr int kMaxAutoParts = 32;       // automatic bf16 decode plans: at most 32 partitions per sequence
 constexpr int kDecodeCtasPerSm = 3;     // resident decode CTAs per SM (64 KB of shared memory each)
+constexpr int kDecodeFp8CtasPerSm = 4;  // resident FP8 decode CTAs per SM (52 KB each, 128 registers)
 constexpr size_t kStatusBytes = 256;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -248,7 +249,22 @@ int32_t auto_part_blocks(int32_t num_seqs, int32_t n_kv, int32_t head_splits, in
     int32_t pb = std::max(kDefaultPartBlocks, floor_pb);
     const int64_t want = nsm * 2;  // (c)
     while (pb > floor_pb && units * ((max_blocks + pb - 1) / pb) < want) pb /= 2;
-    return std::max(pb, floor_pb);
+    pb = std::max(pb, floor_pb);
+    // (d) a grid a little over one wave of resident CTAs (its second wave a few
+    //     CTAs) takes instead the most partitions that fit in one wave, when those
+    //     still give every SM a CTA (MQA-shaped B=32 x 2048, 32 query heads over one
+    //     KV head, L2 flushed: 3 partitions of 688 tokens, 23.2 us, against 4 of 512,
+    //     29.3 us, and 4 of 768 or 1024, 25.2 us).
+    const int64_t slots = nsm * (fp8 ? kDecodeFp8CtasPerSm : kDecodeCtasPerSm);
+    const int64_t parts = (max_blocks + pb - 1) / pb;
+    if (units * parts > slots && units * parts < 2 * slots) {
+        const int64_t fit = slots / units;
+        if (fit >= 1 && units * fit >= nsm) {
+            const int32_t pb1 = static_cast<int32_t>((max_blocks + fit - 1) / fit);
+            if (pb1 >= floor_pb) pb = pb1;
+        }
+    }
+    return pb;
 }
 
 }  // namespace

@@ -80,7 +80,7 @@ def test_decode_parity(name):
     assert status_word(ws) == 0
 
 
-@pytest.mark.parametrize("part", [16, 48, 256, 512, 1024, 4096])
+@pytest.mark.parametrize("part", [16, 48, 256, 512, 688, 1024, 4096])
 def test_decode_partition_invariance(part):
     wl, _, _, _ = workload("llama3_8b_b64")
     d = DevWorkload(wl)
@@ -308,6 +308,11 @@ def test_auto_partitions_follow_the_measured_rules(built_library):
     if sms <= 32 * 8 <= 3 * sms:
         assert n(32, 32, 128) == 1      # B=32 x 2048, 8 KV heads: one wave unsplit
     assert n(2, 32, 2) == 1             # a context inside one partition is never split
+    if sms == 152:
+        # MQA-shaped B=32 x 2048 (one KV head, 4 CTAs of 8 heads each): 4 partitions
+        # of 512 tokens would be 1.12 waves of 3 CTAs per SM; 3 partitions fit one
+        c1 = P.CacheDesc(1000, 16, 1, 128, 0)
+        assert P.paged_attention_decode_partitions(32, 32, 128, 0, c1) == 3
     # FP8 cache: fewer, longer CTAs (half the bytes per CTA)
     c8 = P.CacheDesc(1000, 16, 8, 128, P.PKV_DTYPE_FP8_E4M3)
     n8 = lambda B, nq, mb: P.paged_attention_decode_partitions(B, nq, mb, 0, c8)  # noqa: E731
