@@ -207,7 +207,7 @@ DecodePlan plan_decode(int32_t num_seqs, int32_t n_q, int32_t max_blocks, int32_
 }
 
 int32_t auto_part_blocks(int32_t num_seqs, int32_t n_kv, int32_t head_splits, int32_t max_blocks, int sms,
-                         bool cap_parts, bool fp8 = false) {
+                         bool cap_parts, bool fp8 = false, bool window_span = false) {
     // Partitions of 1024 tokens (measured best on ragged 8B-shaped batches and
     // 70B-shaped B=8 long contexts) keep CTAs uniform and the merge small; a
     // context that fits one partition is not split.  Three refinements, each
@@ -225,6 +225,15 @@ int32_t auto_part_blocks(int32_t num_seqs, int32_t n_kv, int32_t head_splits, in
     //      256 tokens, nor below (b)'s floor) until the grid covers every SM twice.
     const int64_t units = static_cast<int64_t>(num_seqs) * n_kv * head_splits;
     const int64_t nsm = sms > 0 ? sms : 148;
+    // (e) a sliding window that bounds every long sequence's span (window_span: the
+    //     span, W / 16 + 1 blocks, is shorter than the table) gives CTAs of about
+    //     equal length, so splitting buys no balance, and the default partition
+    //     leaves a one-block tail partition (W = 1024: 64 + 1 blocks): spans up to 4
+    //     default partitions are not split when the units cover every SM (8B-shaped
+    //     B=64, back to back: W = 1024, 47.1 vs 52.1 us; W = 1536, 60.2 vs 62.1;
+    //     W = 2048, 69.6 vs 72.0; W = 3000, 84.3 vs 85.9; MHA B=32 x 2048: W = 1024,
+    //     79.1 vs 81.8; W = 1536, 115.5 vs 118.5).
+    if (window_span && units >= nsm && max_blocks <= 4 * kDefaultPartBlocks) return max_blocks;
     if (fp8) {
         // The FP8 decode moves half the bytes per CTA, so it prefers fewer, longer
         // CTAs (back-to-back decode calls, GB300): contexts of at most 2048 tokens
@@ -369,7 +378,8 @@ int32_t paged_attention_decode_partitions(int32_t num_seqs, int32_t num_q_heads,
         const int dev = current_device();
         if (dev < 0 || dev >= kMaxDevices) return PKV_ERR_CUDA;
         const bool fp8 = cache->dtype == PKV_DTYPE_FP8_E4M3;
-        pb = auto_part_blocks(num_seqs, cache->num_kv_heads, head_splits, span, sm_count(dev), !fp8, fp8);
+        pb = auto_part_blocks(num_seqs, cache->num_kv_heads, head_splits, span, sm_count(dev), !fp8, fp8,
+                              span < max_blocks_per_seq);
     }
     return plan_decode(num_seqs, num_q_heads, span, pb).max_parts;
 }
@@ -424,7 +434,8 @@ int decode_impl(void *out, int32_t out_dtype, const void *q, const void *k_cache
     const int sms = sm_count(dev);
 
     const int32_t pb = partition_size > 0 ? partition_size / kBlockSize
-                                          : auto_part_blocks(num_seqs, n_kv, head_splits, span_blocks, sms, !fp8, fp8);
+                                          : auto_part_blocks(num_seqs, n_kv, head_splits, span_blocks, sms, !fp8, fp8,
+                                                             span_blocks < max_blocks_per_seq);
     const DecodePlan pl = plan_decode(num_seqs, num_q_heads, span_blocks, pb);
     if (workspace_bytes < pl.total) return PKV_ERR_WORKSPACE_TOO_SMALL;  // cannot happen for auto plans
 
@@ -866,7 +877,8 @@ int verify_impl(void *out, int32_t out_dtype, const void *q, int32_t q_per_seq, 
                          max_blocks_per_seq, (static_cast<int64_t>(window) + q_per_seq - 1 + 15) / kBlockSize + 1))
                    : max_blocks_per_seq;
     const int32_t pb = partition_size > 0 ? partition_size / kBlockSize
-                                          : auto_part_blocks(num_seqs, n_kv, splits, span, sms, false);
+                                          : auto_part_blocks(num_seqs, n_kv, splits, span, sms, false, false,
+                                                             span < max_blocks_per_seq);
     const DecodePlan pl = plan_decode(num_seqs, num_q_heads, span, pb, q_per_seq);
     if (workspace_bytes < pl.total) return PKV_ERR_WORKSPACE_TOO_SMALL;
 

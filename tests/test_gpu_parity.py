@@ -308,6 +308,10 @@ def test_auto_partitions_follow_the_measured_rules(built_library):
     if sms <= 32 * 8 <= 3 * sms:
         assert n(32, 32, 128) == 1      # B=32 x 2048, 8 KV heads: one wave unsplit
     assert n(2, 32, 2) == 1             # a context inside one partition is never split
+    # a sliding window bounding every long sequence's span (W / 16 + 1 blocks): not split
+    assert P.paged_attention_decode_partitions(64, 32, 256, 0, c, window=1024) == 1
+    assert P.paged_attention_decode_partitions(64, 32, 256, 0, c, window=3000) == 1
+    assert P.paged_attention_decode_partitions(64, 32, 4096, 0, c, window=8192) > 1  # 513 blocks: split
     if sms == 152:
         # MQA-shaped B=32 x 2048 (one KV head, 4 CTAs of 8 heads each): 4 partitions
         # of 512 tokens would be 1.12 waves of 3 CTAs per SM; 3 partitions fit one
