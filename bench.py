@@ -392,7 +392,11 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     barrier(dist)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda._sleep(200000)  # the host enqueues the first steps while the GPU waits (outside the events)
+    # The host enqueues the first steps while the GPU waits (outside the events): a
+    # step's copies and events take the host about as long as the GPU takes to run
+    # it, so the head start is sized to the step count (≈ 145 µs of GPU spin per
+    # step, at most 200 steps) -- without it a short run measures the host's start.
+    torch.cuda._sleep(300000 * min(args.steps, 200))
     e0.record(stream)
     copy.wait_event(e0)
     e2e_run(args.steps)
