@@ -480,10 +480,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = wait(bar_q, 0);
             for (int kt = 0; ok && kt <= n_tiles; ++kt) {
                 const int st_k = kt % kStagesK, st_v = kt % kStagesV;
-                bool k_ready = false;  // K(kt) waited for (just before the first S that reads it)
+                // K(kt) waited for (just before the first S that reads it).  bf16: only K(0)
+                // here; for kt > 0 the P barrier of key tile kt - 1 that this thread waited
+                // for already covers K(kt), and a P barrier covers its key tile's V, since
+                // softmax warp 0 checks both before its pass (every wait here drains the
+                // tensor pipe for about 115 cycles).
+                bool k_ready = false;
                 auto need_k = [&]() -> bool {
                     if (!k_ready) {
-                        if (!wait(FP8 ? k_conv(st_k) : k_full(st_k), (kt / kStagesK) & 1)) return false;
+                        if ((FP8 || kt == 0) && !wait(FP8 ? k_conv(st_k) : k_full(st_k), (kt / kStagesK) & 1))
+                            return false;
                         tc_fence_after();
                         k_ready = true;
                     }
@@ -495,7 +501,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (kt >= 1 && kt - 1 < nt1) {  // tile 1's P V of the previous key tile
                     const int pk = kt - 1;
-                    if (!(ok = wait(p_full(1), pk & 1) && wait(FP8 ? v_conv(pk % kStagesV) : v_full(pk % kStagesV), (pk / kStagesV) & 1))) break;
+                    if (!(ok = wait(p_full(1), pk & 1) && (!FP8 || wait(v_conv(pk % kStagesV), (pk / kStagesV) & 1))))
+                        break;
                     tc_fence_after();
                     mma_pv(1, pk);
                     umma_commit(v_empty(pk % kStagesV));  // both tiles' P V of key tile pk are issued
@@ -506,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (kt < n_tiles) umma_commit(k_empty(st_k));  // both tiles' S of key tile kt are issued
                 if (kt < nt0) {
-                    if (!(ok = wait(p_full(0), kt & 1) && wait(FP8 ? v_conv(st_v) : v_full(st_v), (kt / kStagesV) & 1))) break;
+                    if (!(ok = wait(p_full(0), kt & 1) && (!FP8 || wait(v_conv(st_v), (kt / kStagesV) & 1)))) break;
                     tc_fence_after();
                     mma_pv(0, kt);
                     if (kt >= nt1) umma_commit(v_empty(st_v));  // tile 1 does not read this key tile
@@ -628,6 +635,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (t == 1 && kt + 1 < n_tiles) expand(false, kt + 1);
                 }
                 if (kt >= (t == 0 ? nt0 : nt1)) continue;  // (CTA-uniform)
+                // bf16: before its pass over S_t(kt) (while the MMAs still run), warp 0 checks that
+                // V(kt) and K(kt + 1) have landed, so that the P barrier it arrives on covers
+                // them and the MMA thread does not wait for copies itself.
+                if (!FP8 && warp == 0)
+                    alive = alive && warp_wait(v_full(kt % kStagesV), (kt / kStagesV) & 1) &&
+                            (kt + 1 >= n_tiles ||
+                             warp_wait(k_full((kt + 1) % kStagesK), ((kt + 1) / kStagesK) & 1));
                 alive = alive && warp_wait(s_full(t), kt & 1);
                 if (!alive) {
                     row_sync();
