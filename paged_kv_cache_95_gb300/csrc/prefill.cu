@@ -98,10 +98,10 @@ constexpr uint32_t kOffK = kOffQ + kRowTiles * kOpBytes;   // K ring: kStagesK x
 constexpr uint32_t kOffV = kOffK + kStagesK * kOpBytes;    // V ring: kStagesV x 32 KB
 constexpr uint32_t kOffBar = kOffV + kStagesV * kOpBytes;
 // q_full, k_full/k_empty[kStagesK], v_full/v_empty[kStagesV], then per tile s_full, p_full, o_done,
-// then (FP8 cache) k_conv[kStagesK], v_conv[kStagesV]
+// then (FP8 cache) k_conv[kStagesK] (a V stage's expansion is covered by the P barriers)
 constexpr int kBarTile = 1 + 2 * kStagesK + 2 * kStagesV;
 constexpr int kBarConv = kBarTile + 3 * kRowTiles;
-constexpr uint32_t kNumBars = kBarConv + kStagesK + kStagesV;
+constexpr uint32_t kNumBars = kBarConv + kStagesK;
 constexpr uint32_t kOffTmem = kOffBar + 8 * 24;
 constexpr uint32_t kOffAbort = kOffTmem + 8;
 constexpr uint32_t kXchBytes = 2 * 4 * 128 * 4;  // per tile: row maxima [key tile & 1][column quarter][128]
@@ -341,7 +341,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto p_full = [&](int t) { return sbase + kOffBar + 8 * (kBarTile + kRowTiles + t); };
     auto o_done = [&](int t) { return sbase + kOffBar + 8 * (kBarTile + 2 * kRowTiles + t); };
     auto k_conv = [&](int st) { return sbase + kOffBar + 8 * (kBarConv + st); };  // FP8: K stage in bf16
-    auto v_conv = [&](int st) { return sbase + kOffBar + 8 * (kBarConv + kStagesK + st); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffTmem);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + kOffAbort);
 
@@ -361,7 +360,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(o_done(t), 1);
         }
         for (int st = 0; st < kStagesK; ++st) mbar_init(k_conv(st), kSoftmaxWarps);
-        for (int st = 0; st < kStagesV; ++st) mbar_init(v_conv(st), kSoftmaxWarps);
         *abort_flag = 0u;
         fence_mbar_init();
     }
@@ -482,9 +480,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int st_k = kt % kStagesK, st_v = kt % kStagesV;
                 // K(kt) waited for (just before the first S that reads it).  bf16: only K(0)
                 // here; for kt > 0 the P barrier of key tile kt - 1 that this thread waited
-                // for already covers K(kt), and a P barrier covers its key tile's V, since
-                // softmax warp 0 checks both before its pass (every wait here drains the
-                // tensor pipe for about 115 cycles).
+                // for already covers K(kt), since softmax warp 0 checks it before its pass
+                // (every wait here drains the tensor pipe for about 115 cycles).  A P
+                // barrier also covers its key tile's V: bf16, by the same check; FP8,
+                // because every softmax warp expands its share of V(kt) (and fences it for
+                // the tensor core) before its pass over key tile kt.
                 bool k_ready = false;
                 auto need_k = [&]() -> bool {
                     if (!k_ready) {
@@ -501,8 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (kt >= 1 && kt - 1 < nt1) {  // tile 1's P V of the previous key tile
                     const int pk = kt - 1;
-                    if (!(ok = wait(p_full(1), pk & 1) && (!FP8 || wait(v_conv(pk % kStagesV), (pk / kStagesV) & 1))))
-                        break;
+                    if (!(ok = wait(p_full(1), pk & 1))) break;
                     tc_fence_after();
                     mma_pv(1, pk);
                     umma_commit(v_empty(pk % kStagesV));  // both tiles' P V of key tile pk are issued
@@ -513,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (kt < n_tiles) umma_commit(k_empty(st_k));  // both tiles' S of key tile kt are issued
                 if (kt < nt0) {
-                    if (!(ok = wait(p_full(0), kt & 1) && (!FP8 || wait(v_conv(st_v), (kt / kStagesV) & 1)))) break;
+                    if (!(ok = wait(p_full(0), kt & 1))) break;
                     tc_fence_after();
                     mma_pv(0, kt);
                     if (kt >= nt1) umma_commit(v_empty(st_v));  // tile 1 does not read this key tile
@@ -607,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             fence_proxy_async_smem();  // generic stores -> the tensor core (async proxy)
             __syncwarp();
-            if (ok && lane == 0) mbar_arrive(is_v ? v_conv(st) : k_conv(st));
+            if (ok && lane == 0 && !is_v) mbar_arrive(k_conv(st));
             alive = ok;
         };
         if constexpr (FP8) {
@@ -761,7 +760,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(p_full(t));
             }
-            // FP8: the next key tile's V (P0(kt+1) V waits for it).
+            // FP8: the next key tile's V (every warp's share is written before its P arrivals
+            // for key tile kt + 1, which the P V MMAs of that key tile wait for).
             if constexpr (FP8) {
                 if (kt + 1 < n_tiles) expand(true, kt + 1);
             }
