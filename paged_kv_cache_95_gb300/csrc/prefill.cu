@@ -223,6 +223,18 @@ __device__ __forceinline__ void stage_row(uint32_t stage, int32_t bf16, int r, i
 // bf16 operand layout (E4M3 values are exact in bf16) between two key tiles'
 // softmax passes; the K scale multiplies the scores and the V scale the weights
 // that enter P V (the row sums keep the unscaled weights).
+// OR of `pred` over the `nthreads` threads of named barrier `id` (a barrier as well).
+__device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t nthreads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %2, 0;\n\t"
+        "barrier.cta.red.or.pred q, %1, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(id), "r"(static_cast<uint32_t>(pred)), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+
 template <bool WINDOW, bool FP8, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_chunk_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
@@ -642,7 +654,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             (kt + 1 >= n_tiles ||
                              warp_wait(k_full((kt + 1) % kStagesK), ((kt + 1) / kStagesK) & 1));
                 alive = alive && warp_wait(s_full(t), kt & 1);
-                if (!alive) {
+                if (!alive) {  // (the exchange -- and for bf16 the vote before it -- of the other warps)
+                    if constexpr (!FP8 && !SPLIT && !WINDOW) bar_red_or(row_bar, 128, true);
                     row_sync();
                     continue;
                 }
@@ -652,70 +665,115 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float *xm = xch + ((t * 2 + (kt & 1)) * 4) * 128;
 
                 // This thread's 32 scores, masked by index (keys past the row's position or in a bad block).
+                auto load_scores = [&](uint32_t(&vv)[32]) {
+                    tmem_ld_32x32b_x32(t_s, vv);
+                    if constexpr (FP8) {  // scores times each key's K scale
+                        const uint32_t ks = sbase + kOffScale + (kt % kScaleSlotsK) * kScaleStage + 128 * cq;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const uint4 w = lds128(ks + 16 * i);
+                            const float2 a = fmul2(make_float2(__uint_as_float(vv[4 * i]), __uint_as_float(vv[4 * i + 1])),
+                                                   make_float2(__uint_as_float(w.x), __uint_as_float(w.y)));
+                            const float2 c = fmul2(make_float2(__uint_as_float(vv[4 * i + 2]), __uint_as_float(vv[4 * i + 3])),
+                                                   make_float2(__uint_as_float(w.z), __uint_as_float(w.w)));
+                            vv[4 * i] = __float_as_uint(a.x);
+                            vv[4 * i + 1] = __float_as_uint(a.y);
+                            vv[4 * i + 2] = __float_as_uint(c.x);
+                            vv[4 * i + 3] = __float_as_uint(c.y);
+                        }
+                    }
+                    if (!(kc + 31 <= limit[t] && (!WINDOW || kc >= first[t]) && !((bad >> (2 * cq)) & 3u))) {
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) {
+                            const bool ok = kc + k <= limit[t] && (!WINDOW || kc + k >= first[t]) &&
+                                            !((bad >> ((32 * cq + k) >> 4)) & 1u);
+                            if (!ok) vv[k] = __float_as_uint(-INFINITY);
+                        }
+                    }
+                };
                 uint32_t v[32];
-                tmem_ld_32x32b_x32(t_s, v);
-                if constexpr (FP8) {        // scores times each key's K scale
-                    const uint32_t ks = sbase + kOffScale + (kt % kScaleSlotsK) * kScaleStage + 128 * cq;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const uint4 w = lds128(ks + 16 * i);
-                        const float2 a = fmul2(make_float2(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1])),
-                                               make_float2(__uint_as_float(w.x), __uint_as_float(w.y)));
-                        const float2 c = fmul2(make_float2(__uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])),
-                                               make_float2(__uint_as_float(w.z), __uint_as_float(w.w)));
-                        v[4 * i] = __float_as_uint(a.x);
-                        v[4 * i + 1] = __float_as_uint(a.y);
-                        v[4 * i + 2] = __float_as_uint(c.x);
-                        v[4 * i + 3] = __float_as_uint(c.y);
-                    }
-                }
-                if (!(kc + 31 <= limit[t] && (!WINDOW || kc >= first[t]) && !((bad >> (2 * cq)) & 3u))) {
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                        const bool ok = kc + k <= limit[t] && (!WINDOW || kc + k >= first[t]) &&
-                                        !((bad >> ((32 * cq + k) >> 4)) & 1u);
-                        if (!ok) v[k] = __float_as_uint(-INFINITY);
-                    }
-                }
-                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-                for (int k = 0; k < 32; k += 2)
-                    mx[(k >> 1) & 3] = fmax3(mx[(k >> 1) & 3], __uint_as_float(v[k]), __uint_as_float(v[k + 1]));
-                xm[cq * 128 + r] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-                row_sync();
-                const float mraw = fmaxf(fmaxf(xm[r], xm[128 + r]), fmaxf(xm[256 + r], xm[384 + r]));
-                const float mt = mraw == -INFINITY ? -INFINITY : mraw * sl2;  // scale > 0 keeps the order
+                load_scores(v);
+                // The exponent reference m: raised to the exact row maximum (exchanged between
+                // the four warps of the row quarter; O and l rescaled) when that maximum passes
+                // it by more than 2^8 -- also at the first visible key (m_ref = -inf).
                 float alpha = 1.f;
-                if (mt > m_ref[t] + 8.f) {  // also taken at the first visible key (m_ref = -inf)
-                    alpha = fast_exp2(m_ref[t] - mt);  // 0 when m_ref = -inf
-                    m_ref[t] = mt;
-                }
-                const float mu = m_ref[t] == -INFINITY ? 0.f : m_ref[t];
-
-                // Rescale O: every earlier P V of this tile completed before S(kt) did.
-                if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                    uint32_t orow[32];
-                    tmem_ld_32x32b_x32(t_o, orow);
+                auto raise_reference = [&](const uint32_t(&vv)[32]) {
+                    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) orow[k] = __float_as_uint(__uint_as_float(orow[k]) * alpha);
-                    tmem_st_32x32b_x32(t_o, orow);
+                    for (int k = 0; k < 32; k += 2)
+                        mx[(k >> 1) & 3] = fmax3(mx[(k >> 1) & 3], __uint_as_float(vv[k]), __uint_as_float(vv[k + 1]));
+                    xm[cq * 128 + r] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+                    row_sync();
+                    const float mraw = fmaxf(fmaxf(xm[r], xm[128 + r]), fmaxf(xm[256 + r], xm[384 + r]));
+                    const float mt = mraw == -INFINITY ? -INFINITY : mraw * sl2;  // scale > 0 keeps the order
+                    if (mt > m_ref[t] + 8.f) {
+                        alpha = fast_exp2(m_ref[t] - mt);  // 0 when m_ref = -inf
+                        m_ref[t] = mt;
+                    }
+                    // Rescale O: every earlier P V of this tile completed before S(kt) did.
+                    if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                        uint32_t orow[32];
+                        tmem_ld_32x32b_x32(t_o, orow);
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) orow[k] = __float_as_uint(__uint_as_float(orow[k]) * alpha);
+                        tmem_st_32x32b_x32(t_o, orow);
+                    }
+                };
+                // P = 2^(s * scale * log2(e) - m) and this thread's share of the row sum.
+                const float2 sl2v = make_float2(sl2, sl2);
+                float2 pr2[16];
+                auto weights = [&](const uint32_t(&vv)[32]) -> float {
+                    const float mu = m_ref[t] == -INFINITY ? 0.f : m_ref[t];
+                    const float2 nmu = make_float2(-mu, -mu);
+                    float2 rs0 = make_float2(0.f, 0.f), rs1 = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float2 x =
+                            ffma2(make_float2(__uint_as_float(vv[2 * e]), __uint_as_float(vv[2 * e + 1])), sl2v, nmu);
+                        pr2[e] = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                        if (e & 1)
+                            rs1 = fadd2(rs1, pr2[e]);
+                        else
+                            rs0 = fadd2(rs0, pr2[e]);
+                    }
+                    const float2 rs = fadd2(rs0, rs1);
+                    return rs.x + rs.y;
+                };
+                float rsum;
+                // The vote (below) pays in the plain chunk only: the FP8, split and window
+                // instantiations take the exact maximum every pass (the split kernel spills
+                // with the vote's live weights, 294 -> 322 us on the 70B verify; under a window
+                // rows without a reference yet force the slow path, 43.7 -> 46.4 us at W=512).
+                if constexpr (FP8 || SPLIT || WINDOW) {
+                    raise_reference(v);
+                    rsum = weights(v);
+                } else {
+                    // Plain chunk: the weights against the current reference first; the maximum is
+                    // taken and exchanged only when a thread's 32 weights sum past 2^8 (then
+                    // some weight may exceed 2^8) or the row has no reference yet -- one vote
+                    // per pass instead of a maximum over every key and an exchange, which
+                    // leaves the integer pipe to the MMA thread (mixed chunk 68.8 -> 66.4 us).
+                    bool need = m_ref[t] == -INFINITY;
+                    rsum = 0.f;
+                    if (!need) {
+                        rsum = weights(v);
+                        need = !(rsum <= 256.f);
+                    }
+                    if (bar_red_or(row_bar, 128, need)) {
+                        uint32_t v2[32];  // S is still in tensor memory: reloaded, so v dies above
+                        load_scores(v2);
+                        raise_reference(v2);
+                        rsum = weights(v2);
+                    }
                 }
 
-                // P = 2^(s * scale * log2(e) - m), written back over the chunk's 32 columns as
-                // [16 columns bf16 head | 16 columns bf16 remainder] (two keys per column, the
-                // lower key in the low half); pairs of keys go through packed f32x2 arithmetic.
-                const float2 sl2v = make_float2(sl2, sl2), nmu = make_float2(-mu, -mu);
-                float2 rs0 = make_float2(0.f, 0.f), rs1 = make_float2(0.f, 0.f);
-                uint32_t hi[16], lo[16];
+                // P written back over the chunk's 32 columns as [16 columns bf16 head | 16
+                // columns bf16 remainder] (two keys per column, the lower key in the low
+                // half); pairs of keys go through packed f32x2 arithmetic.
+                uint32_t pk[32];  // [16 columns of heads | 16 columns of remainders], one store
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const float2 x =
-                        ffma2(make_float2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), sl2v, nmu);
-                    const float2 pr = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-                    if (e & 1)
-                        rs1 = fadd2(rs1, pr);
-                    else
-                        rs0 = fadd2(rs0, pr);
+                    const float2 pr = pr2[e];
                     // FP8: the weights entering P V carry each key's V scale (a masked key's
                     // scale was zeroed by the expansion); the row sums keep the plain weights.
                     float2 pw = pr;
@@ -727,16 +785,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // head: the upper 16 bits of each (bf16 truncation, exact in fp32);
                     // remainder: P - head >= 0 (exact in fp32), rounded to nearest bf16.
                     const uint32_t ua = __float_as_uint(pw.x), ub = __float_as_uint(pw.y);
-                    hi[e] = __byte_perm(ua, ub, 0x7632);
+                    pk[e] = __byte_perm(ua, ub, 0x7632);
                     const float2 rr =
                         fsub2(pw, make_float2(__uint_as_float(ua & 0xffff0000u), __uint_as_float(ub & 0xffff0000u)));
-                    lo[e] = pack_bf16x2(rr.x, rr.y);
+                    pk[16 + e] = pack_bf16x2(rr.x, rr.y);
                 }
-                tmem_st_32x32b_x16(t_s, hi);
-                tmem_st_32x32b_x16(t_s + 16, lo);
+                tmem_st_32x32b_x32(t_s, pk);  // (one store instead of two: 69.9 -> 69.0 us on the mixed chunk)
                 tmem_wait_st();
-                const float2 rs = fadd2(rs0, rs1);
-                l[t] = l[t] * alpha + (rs.x + rs.y);
+                l[t] = l[t] * alpha + rsum;
 
                 // Zero V rows of keys no row may see (past the context, of a bad block or
                 // of a block before the window), once per key tile, by the first tile that
