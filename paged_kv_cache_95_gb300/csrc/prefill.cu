@@ -824,14 +824,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 
         // ---- epilogue per tile: out = O / l (the four column quarters add their row sums) ----
-        // Both tiles' last P V first: then every MMA has completed and a full tile is
-        // staged in a free ring (tile 0: the V ring, tile 1: the K ring) for a TMA store.
+        // A full tile is staged in a free ring for a TMA store.  When both tiles end at the
+        // same key tile, tile 0's epilogue runs while tile 1's last P V is still in the
+        // pipe: tile 0 is staged in the K ring (free once tile 0's last P V completed,
+        // since every S was issued before it), tile 1 in the V ring after its own last P V.
+        // Otherwise both tiles' last P V first (tile 0: the V ring, tile 1: the K ring).
+        const bool early = nt0 == nt1;  // CTA-uniform
         bool done = alive;
-        if (nt0 > 0) done = done && warp_wait(o_done(0), (nt0 - 1) & 1);
-        if (nt1 > 0) done = done && warp_wait(o_done(1), (nt1 - 1) & 1);
+        if (!early) {
+            if (nt0 > 0) done = done && warp_wait(o_done(0), (nt0 - 1) & 1);
+            if (nt1 > 0) done = done && warp_wait(o_done(1), (nt1 - 1) & 1);
+        }
 #pragma unroll 1
         for (int t = 0; t < kRowTiles; ++t) {
             const int my_nt = t == 0 ? nt0 : nt1;
+            if (early && my_nt > 0) done = done && warp_wait(o_done(t), (my_nt - 1) & 1);
             const int i0 = tile_i0(t);
             const int rows_here = tile_rows(t);
             const bool row_valid = ii < rows_here;
@@ -839,7 +846,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             xch[cq * 128 + r] = l[t];
             row_sync();
             const bool staged = S == 1 && rows_here == rpt;  // CTA-uniform
-            const uint32_t stage = sbase + (t == 0 ? kOffV : kOffK);
+            const uint32_t stage = sbase + ((t == 0) != early ? kOffV : kOffK);
             // Split-KV: row (row0 + i0 + ii, head g G + r % G)'s partial of this split.
             auto part_index = [&]() {
                 return (static_cast<size_t>(row0 + i0 + ii) * p.n_q + static_cast<size_t>(g) * G + (r % G)) * S + split;
