@@ -831,6 +831,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Otherwise both tiles' last P V first (tile 0: the V ring, tile 1: the K ring).
         const bool early = nt0 == nt1;  // CTA-uniform
         bool done = alive;
+        // both tiles' row sums, added over the four column quarters through shared memory
+        row_sync();  // the last maxima have been read: the exchange area is free
+        xch[cq * 128 + r] = l[0];
+        xch[512 + cq * 128 + r] = l[1];
+        row_sync();
         if (!early) {
             if (nt0 > 0) done = done && warp_wait(o_done(0), (nt0 - 1) & 1);
             if (nt1 > 0) done = done && warp_wait(o_done(1), (nt1 - 1) & 1);
@@ -842,9 +847,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int i0 = tile_i0(t);
             const int rows_here = tile_rows(t);
             const bool row_valid = ii < rows_here;
-            row_sync();  // the last maxima have been read: the exchange area is free
-            xch[cq * 128 + r] = l[t];
-            row_sync();
             const bool staged = S == 1 && rows_here == rpt;  // CTA-uniform
             const uint32_t stage = sbase + ((t == 0) != early ? kOffV : kOffK);
             // Split-KV: row (row0 + i0 + ii, head g G + r % G)'s partial of this split.
@@ -863,7 +865,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (my_nt > 0 && done) {
                 tc_fence_after();
-                const float lt = (xch[r] + xch[128 + r]) + (xch[256 + r] + xch[384 + r]);
+                const float *xl = xch + 512 * t;
+                const float lt = (xl[r] + xl[128 + r]) + (xl[256 + r] + xl[384 + r]);
                 const float inv = lt > 0.f ? 1.f / lt : 0.f;
                 uint32_t orow[32];
                 tmem_ld_32x32b_x32(lane_base + kTmemO + 128 * t + 32 * cq, orow);
