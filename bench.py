@@ -410,8 +410,8 @@ def run_ours(args):
     # The host enqueues the first steps while the GPU waits (outside the events): a
     # step's copies and events take the host about as long as the GPU takes to run
     # it, so the head start is sized to the step count (≈ 145 µs of GPU spin per
-    # step, at most 200 steps) -- without it a short run measures the host's start.
-    torch.cuda._sleep(300000 * min(args.steps, 200))
+    # step, at most 20 steps) -- without it a short run measures the host's start.
+    torch.cuda._sleep(300000 * min(args.steps, 20))
     e0.record(stream)
     copy.wait_event(e0)
     e2e_run(args.steps)
@@ -526,14 +526,22 @@ class _L2Flush:
         self.torch.sum(self.rd, 0, out=self.sink)
 
 
+def _head_start_cycles(steps):
+    """GPU spin (cycles) that lets the host enqueue up to 20 steps before a timed region
+    (a longer spin slowed a 10000-step loop by 12%)."""
+    return 200000 + 150000 * min(steps, 20)
+
+
 def _timed_loop(torch, stream, fn, steps, flush=None):
     """Total ms of `steps` calls of fn().  Without `flush`: back to back between two
     events.  With it: L2 flushed before every call, outside per-call events."""
     if flush is None:
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         # Keep the GPU busy (outside the events) while the host enqueues the first steps,
-        # so the timed region starts with launches queued, not with host launch latency.
-        torch.cuda._sleep(200000)
+        # so the timed region starts with launches queued, not with host launch latency:
+        # ≈ 70 µs of spin per step, for up to 20 steps, covers the host's call overhead
+        # (a 20-step run otherwise measures the host's start as much as the GPU).
+        torch.cuda._sleep(_head_start_cycles(steps))
         a.record(stream)
         for _ in range(steps):
             fn()
@@ -710,7 +718,7 @@ def _time_events(torch, stream, fn, steps, warmup=3):
         fn()
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda._sleep(200000)
+    torch.cuda._sleep(_head_start_cycles(steps))
     a.record(stream)
     for _ in range(steps):
         fn()
