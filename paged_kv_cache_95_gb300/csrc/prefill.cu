@@ -820,9 +820,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
                         }
                     }
+                    fence_proxy_async_smem();  // zeroed V rows -> the tensor core (async proxy)
                 }
-
-                fence_proxy_async_smem();  // zeroed V rows -> the tensor core (async proxy)
+                // (P itself goes through tensor memory: the tcgen05 fence below orders it; the
+                // proxy fence costs 150-350 cycles per pass, so only passes that zeroed V rows
+                // pay it; FP8 fences its expansions where it writes them.)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(p_full(t));
