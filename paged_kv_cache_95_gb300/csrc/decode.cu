@@ -358,6 +358,13 @@ namespace {
 // Decoding; scores in the log2 domain).  8 warps fold the partitions
 // p = w, w + 8, ...; lane owns dims 4*lane .. 4*lane + 3.
 constexpr int kMergeWarps = 8;
+// Calls whose rows have at most this many partitions fold them with one warp per
+// (row, query head); more go to one CTA per (row, query head), whose warps fold the
+// partitions in parallel (measured, decode call back to back: 8B-shaped batch, 4
+// partitions, 91.7 -> 90.9 us with the warp fold; MQA sweep, 3, 23.6 -> 23.3; 70B
+// verify k = 16 on the split prefill, 7, 291.2 -> 284.1; mixed batch, 8, 159.3 ->
+// 159.9; 70B-shaped B=8 and B=1, 32, 165.0 -> 174.2 and 84.6 -> 91.9).
+constexpr int kMergeWarpMaxParts = 7;
 
 // Rows r = blockIdx.y, + gridDim.y, ... < rows.  fixed_parts > 0: every row has that
 // many partials (the prefill's key splits); 0: a row's partition count follows
@@ -430,9 +437,92 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
     griddep_launch_dependents();
 }
 
+// The same fold with one warp per (row, query head) and eight per CTA, for calls
+// with few partitions per row: lane i holds partition i's weight (32 at a time),
+// each partition's O row arrives as one float4 per lane, and no shared memory or
+// CTA barrier is involved (the one-CTA-per-row kernel spends most of a short fold
+// on its barriers and on CTA scheduling: 2048 CTAs for the 8B-shaped batch).
+constexpr int kMergeRowsPerCta = 8;
+__global__ void __launch_bounds__(kMergeRowsPerCta * 32)
+    lse_merge_warp_kernel(const DecodeParams p, int rows, int rows_per_seq, int fixed_parts) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    griddep_wait();  // the producing grid's partials
+    const int64_t total = static_cast<int64_t>(rows) * p.n_q;
+    for (int64_t idx = static_cast<int64_t>(blockIdx.x) * kMergeRowsPerCta + warp; idx < total;
+         idx += static_cast<int64_t>(gridDim.x) * kMergeRowsPerCta) {
+        const int r = static_cast<int>(idx / p.n_q), h = static_cast<int>(idx % p.n_q);
+        int nparts = fixed_parts;
+        if (nparts == 0) {  // as in lse_merge_kernel: the partitions of row r's sequence
+            const int b = r / rows_per_seq;
+            int ctx = __ldg(p.context_lens + b);
+            const int max_ctx = p.max_blocks * kBlockSize;
+            ctx = ctx < 1 ? 0 : (ctx > max_ctx ? max_ctx : ctx);
+            const int first_blk = (p.window > 0 ? max(0, ctx - rows_per_seq + 1 - p.window) : 0) / kBlockSize;
+            nparts = ((ctx + kBlockSize - 1) / kBlockSize - first_blk + p.part_blocks - 1) / p.part_blocks;
+        }
+        if (nparts <= 1) continue;  // written directly by the producing kernel (warp-uniform)
+        const size_t base = (static_cast<size_t>(r) * p.n_q + h) * p.max_parts;
+        float M = -INFINITY;
+        for (int i = lane; i < nparts; i += 32) M = fmaxf(M, __ldcg(p.part_m + base + i));
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        const float Mu = M == -INFINITY ? 0.f : M;
+        float L = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i0 = 0; i0 < nparts; i0 += 32) {
+            float f = 0.f;
+            if (i0 + lane < nparts) {
+                f = fast_exp2(__ldcg(p.part_m + base + i0 + lane) - Mu);
+                L += f * __ldcg(p.part_l + base + i0 + lane);
+            }
+            const int n = min(32, nparts - i0);
+            const float4 *po = reinterpret_cast<const float4 *>(p.part_o + (base + i0) * kHeadDim) + lane;
+#pragma unroll 4
+            for (int j = 0; j < n; ++j) {
+                const float fj = __shfl_sync(0xffffffffu, f, j);
+                const float4 v = __ldcg(po + static_cast<size_t>(j) * (kHeadDim / 4));
+                acc.x += fj * v.x;
+                acc.y += fj * v.y;
+                acc.z += fj * v.z;
+                acc.w += fj * v.w;
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+        if (L > 0.f) {
+            acc.x /= L;
+            acc.y /= L;
+            acc.z /= L;
+            acc.w /= L;
+        } else {
+            acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        // (4-byte stores: the output is only required to be 4-byte aligned)
+        const size_t o = (static_cast<size_t>(r) * p.n_q + h) * kHeadDim + 4 * lane;
+        if (p.out_bf16) {
+            __nv_bfloat162 *ob = reinterpret_cast<__nv_bfloat162 *>(static_cast<__nv_bfloat16 *>(p.out) + o);
+            ob[0] = __floats2bfloat162_rn(acc.x, acc.y);
+            ob[1] = __floats2bfloat162_rn(acc.z, acc.w);
+        } else {
+            float *of = static_cast<float *>(p.out) + o;
+            of[0] = acc.x;
+            of[1] = acc.y;
+            of[2] = acc.z;
+            of[3] = acc.w;
+        }
+    }
+    griddep_launch_dependents();  // (as lse_merge_kernel: the next grid launches as the merge ends)
+}
+
 }  // namespace
 
 cudaError_t launch_merge(const DecodeParams &p, int rows, int rows_per_seq, int fixed_parts, cudaStream_t stream) {
+    const int64_t pairs = static_cast<int64_t>(rows) * p.n_q;
+    if (p.max_parts <= kMergeWarpMaxParts) {
+        const int64_t ctas = (pairs + kMergeRowsPerCta - 1) / kMergeRowsPerCta;
+        return launch_pdl(lse_merge_warp_kernel, dim3(static_cast<unsigned>(ctas < 65535 * 16 ? ctas : 65535 * 16)),
+                          dim3(kMergeRowsPerCta * 32), 0, stream, p, rows, rows_per_seq, fixed_parts);
+    }
     return launch_pdl(lse_merge_kernel, dim3(p.n_q, rows < 65535 ? rows : 65535), dim3(kMergeWarps * 32), 0, stream, p,
                       rows, rows_per_seq, fixed_parts);
 }
