@@ -39,7 +39,10 @@
 //    of the P that the P V MMA issued just before it reads; MMAs of one thread
 //    execute in order, and the commit after S_t(k) completes only when every
 //    earlier MMA has, so when the softmax sees S_t(k) the previous P_t V is
-//    already in O_t.
+//    already in O_t.  The thread waits only for the P barriers (and K(0)):
+//    softmax warp 0 checks that V(k) and K(k+1) have landed before its pass
+//    over key tile k, so every P barrier also covers the copies the MMAs after
+//    it read (a wait on the issuing thread lets the tensor pipe run dry).
 //  * warps 0-15 (512 threads) work on tile 0's scores, then on tile 1's, for
 //    each key tile (the MMAs of one tile run while the other tile's softmax
 //    does): warps w, w+4, w+8, w+12 own tensor-memory lanes 32*(w%4) .. +31
@@ -47,20 +50,22 @@
 //    32 scores of one row in registers, applies the causal/length mask by
 //    index (skipped for fully visible chunks), and the four quarters exchange
 //    their row maxima through shared memory (a 128-thread named barrier per row
-//    quarter).  Each updates the running max and its quarter of the running
-//    sum (fp32, log2 domain, pairs of keys in packed f32x2 arithmetic) and
-//    writes P = 2^(s - m) back over its 32 columns as [16 columns bf16 head |
-//    16 columns bf16 remainder] (head = P truncated to bf16, remainder = the
-//    rest rounded to bf16; P V = P_hi V + P_lo V keeps the weights to ~2^-16
-//    relative).  The exponent reference is only raised when a row's max grows
-//    by more than 2^8, in which case the row's O is rescaled in tensor memory;
-//    P stays <= 256.
-//  * Epilogue per tile, after both tiles' last P V (every MMA has completed):
-//    O / l from tensor memory; a full tile is staged in a free ring (tile 0:
-//    the V ring, tile 1: the K ring) in the output tensor map's 128-byte-
-//    swizzled layout and leaves by TMA store; a ragged last tile by 16-byte
-//    stores of its valid rows only (a whole-box store would overwrite the next
-//    sequence).
+//    quarter) -- in the plain chunk only when a vote over those 128 threads
+//    says a weight against the current reference may pass 2^8.  Each updates
+//    its quarter of the running sum (fp32, log2 domain, pairs of keys in packed
+//    f32x2 arithmetic) and writes P = 2^(s - m) back over its 32 columns, in one
+//    store, as [16 columns bf16 head | 16 columns bf16 remainder] (head = P
+//    truncated to bf16, remainder = the rest, by mixed-precision FMAs, rounded to
+//    bf16; P V = P_hi V + P_lo V keeps the weights to ~2^-16 relative).  The
+//    exponent reference is only raised when a row's max grows by more than 2^8,
+//    in which case the row's O is rescaled in tensor memory; P stays <= 256.
+//  * Epilogue per tile after its last P V: O / l from tensor memory; a full
+//    tile is staged in a free ring in the output tensor map's 128-byte-swizzled
+//    layout and leaves by TMA store; a ragged last tile by 16-byte stores of its
+//    valid rows only (a whole-box store would overwrite the next sequence).
+//    When both tiles end at the same key tile, tile 0's epilogue (staged in the
+//    K ring) runs while tile 1's last P V is still in the pipe; otherwise both
+//    tiles' last P V first (tile 0: the V ring, tile 1: the K ring).
 //  * Keys at or past the context length and keys of blocks with an invalid id
 //    are masked by index and their V rows are zeroed in shared memory (once,
 //    before the first P V that reads them), so stale or NaN bytes cannot reach
