@@ -564,6 +564,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Per tile: the row's last visible key, running exponent reference and row-sum share.
         int limit[kRowTiles], first[kRowTiles];
         float m_ref[kRowTiles], l[kRowTiles];
+        // The vote (plain chunk and window, bf16, unsplit): up to key tile exact_until[t]
+        // some row of tile t has no reference yet, so those passes take the row maximum
+        // directly (CTA-uniform): the first key tile, or under a window the key tile
+        // where the tile's last row's window starts.
+        constexpr bool kVote = !FP8 && !SPLIT;
+        int exact_until[kRowTiles];
 #pragma unroll
         for (int t = 0; t < kRowTiles; ++t) {
             const int pos = c + tile_i0(t) + (ii < tile_rows(t) ? ii : 0);
@@ -571,6 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             first[t] = WINDOW ? max(0, pos + 1 - W) : 0;
             m_ref[t] = -INFINITY;
             l[t] = 0.f;
+            exact_until[t] = WINDOW ? max(0, c + tile_i0(t) + tile_rows(t) - W) / 128 - kt0 : 0;
         }
 
         // The four warps of a row quarter pass exactly one row barrier per (key tile,
@@ -669,9 +676,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     alive = alive && warp_wait(v_full(kt % kStagesV), (kt / kStagesV) & 1) &&
                             (kt + 1 >= n_tiles ||
                              warp_wait(k_full((kt + 1) % kStagesK), ((kt + 1) / kStagesK) & 1));
+                const bool exact = !kVote || kt <= exact_until[t];  // (CTA-uniform)
                 alive = alive && warp_wait(s_full(t), kt & 1);
-                if (!alive) {  // (the exchange -- and for bf16 the vote before it -- of the other warps)
-                    if constexpr (!FP8 && !SPLIT && !WINDOW) bar_red_or(row_bar, 128, true);
+                if (!alive) {  // (the exchange -- and the vote before it -- of the other warps)
+                    if (!exact) bar_red_or(row_bar, 128, true);
                     row_sync();
                     continue;
                 }
@@ -756,15 +764,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     return rs.x + rs.y;
                 };
                 float rsum;
-                // The vote (below) pays in the plain chunk only: the FP8, split and window
-                // instantiations take the exact maximum every pass (the split kernel spills
-                // with the vote's live weights, 294 -> 322 us on the 70B verify; under a window
-                // rows without a reference yet force the slow path, 43.7 -> 46.4 us at W=512).
-                if constexpr (FP8 || SPLIT || WINDOW) {
+                // The FP8 and split instantiations take the exact maximum every pass (the split
+                // kernel spills with the vote's live weights, 294 -> 322 us on the 70B verify;
+                // FP8 measured slower with the vote, 95.7 -> 97.8 us).
+                if (exact) {
                     raise_reference(v);
                     rsum = weights(v);
                 } else {
-                    // Plain chunk: the weights against the current reference first; the maximum is
+                    // The weights against the current reference first; the maximum is
                     // taken and exchanged only when a thread's 32 weights sum past 2^8 (then
                     // some weight may exceed 2^8) or the row has no reference yet -- one vote
                     // per pass instead of a maximum over every key and an exchange, which
