@@ -236,6 +236,46 @@ def test_prefill_ragged_chunks(n_q, n_kv):
     assert status_word(ws) == 0
 
 
+def _scaled_q(batch, factor):
+    """The batch with q scaled by `factor` (rounded to bf16 again)."""
+    q = W.bf16_bits_from_f32(W.f32_from_bf16_bits(batch.q) * np.float32(factor))
+    return W.Batch(q=q, cu_q_lens=batch.cu_q_lens, block_tables=batch.block_tables, context_lens=batch.context_lens)
+
+
+@pytest.mark.parametrize("n_q,n_kv,window", [(32, 8, 0), (32, 32, 0), (64, 8, 0), (32, 8, 700)])
+def test_prefill_large_score_range(n_q, n_kv, window):
+    """Scores with a wide range (q scaled by 12: score / ln 2 of spread ~17): a row's
+    running maximum passes the exponent reference by more than 2^8 again and again
+    along the keys, so the reference is raised -- and O and l rescaled in tensor
+    memory -- in the middle of a sequence, both on the first key tile's exact path and
+    after a vote; the weights of most keys underflow to zero."""
+    ctx = [1500, 900, 2000, 300]
+    q_lens = [300, 129, 64, 200]
+    wl, batch = W.make_custom(n_q, n_kv, ctx, q_lens=q_lens, seed=70 + n_q + n_kv + window,
+                              materialize_logical=False)
+    batch = _scaled_q(batch, 12.0)
+    d = DevWorkload(wl)
+    d.append()
+    out, ws = d.prefill(batch, window=window)
+    kc, vc = oracle_after_append(wl)
+    ref = oracle.paged_attention(batch.q, batch.cu_q_lens, kc, vc, batch.block_tables, batch.context_lens,
+                                 wl.scale, n_q=wl.n_q, window=window)
+    assert_close(out.cpu().numpy(), ref, what=f"G={n_q // n_kv} W={window}, q x12")
+    assert status_word(ws) == 0
+
+
+@pytest.mark.parametrize("part", [0, 256])
+def test_decode_large_score_range(part):
+    """The decode kernel's lazy reference under the same wide score range."""
+    wl, batch = W.make_custom(32, 8, [3000, 1700, 517, 4096], seed=77, materialize_logical=False)
+    batch = _scaled_q(batch, 12.0)
+    d = DevWorkload(wl)
+    d.append()
+    out, ws = d.decode(batch, partition_size=part)
+    assert_close(out.cpu().numpy(), oracle_attention(wl, batch), what=f"decode, q x12, partition {part}")
+    assert status_word(ws) == 0
+
+
 def test_prefill_bf16_output():
     t = torch()
     wl, batch = W.make_custom(32, 8, [700, 250], q_lens=[200, 250], seed=41, materialize_logical=False)
