@@ -245,6 +245,29 @@ def test_fp8_prefill_parity(n_q, n_kv):
         assert status_word(ws) == 0
 
 
+@pytest.mark.parametrize("n_q,n_kv", [(32, 8), (32, 32)])
+def test_fp8_prefill_and_decode_large_score_range(n_q, n_kv):
+    """q scaled by 12 over an FP8 cache: the exponent reference (and, in the decode,
+    the V exponent) is raised in the middle of sequences, O rescaled."""
+    ctx = [1500, 900, 2000, 300]
+    q_lens = [300, 129, 64, 200]
+    wl, batch = W.make_custom(n_q, n_kv, ctx, q_lens=q_lens, seed=430 + n_q + n_kv, materialize_logical=False)
+    q = W.bf16_bits_from_f32(W.f32_from_bf16_bits(batch.q) * np.float32(12.0))
+    batch = W.Batch(q=q, cu_q_lens=batch.cu_q_lens, block_tables=batch.block_tables, context_lens=batch.context_lens)
+    d = Fp8Dev(wl)
+    d.append()
+    for win in (0, 700):
+        out, ws = d.prefill(batch, window=win)
+        assert_close(out.cpu().numpy(), d.oracle(batch, window=win), what=f"fp8 prefill q x12 W={win}")
+        assert status_word(ws) == 0
+    last = batch.cu_q_lens[1:] - 1
+    dec_batch = W.Batch(q=batch.q[last], cu_q_lens=np.arange(len(ctx) + 1, dtype=np.int32),
+                        block_tables=batch.block_tables, context_lens=batch.context_lens)
+    out, ws = d.decode(dec_batch)
+    assert_close(out.cpu().numpy(), d.oracle(dec_batch), what="fp8 decode q x12")
+    assert status_word(ws) == 0
+
+
 def test_fp8_prefill_mixed_chunks_stale_entries_and_bf16_out():
     """The mixed workload's 512-row chunks over 1024 cached tokens on an FP8 pool:
     plain, and under a 300-token window with invalid ids in the table entries wholly

@@ -74,6 +74,24 @@ def test_prefill_split_long_contexts(n_q, n_kv):
     assert status_word(ws1) == 0
 
 
+def test_prefill_split_large_score_range():
+    """q scaled by 12 on the split plan: each key range raises its own exponent
+    reference in the middle of the range, and the merge folds partials whose
+    references differ by many powers of two."""
+    wl, batch = W.make_custom(32, 8, [16000, 9001], q_lens=[64, 33], seed=620, materialize_logical=False)
+    q = W.bf16_bits_from_f32(W.f32_from_bf16_bits(batch.q) * np.float32(12.0))
+    batch = W.Batch(q=q, cu_q_lens=batch.cu_q_lens, block_tables=batch.block_tables, context_lens=batch.context_lens)
+    d = DevWorkload(wl)
+    d.append()
+    ref = oracle.paged_attention(batch.q, batch.cu_q_lens, *oracle_after_append(wl), batch.block_tables,
+                                 batch.context_lens, wl.scale, n_q=wl.n_q)
+    nbytes = _split_bytes(wl, batch)
+    assert nbytes > 256
+    out, ws = _prefill(d, batch, nbytes)
+    assert_close(out.cpu().numpy(), ref, what="split, q x12")
+    assert status_word(ws) == 0
+
+
 @pytest.mark.parametrize("n_q,n_kv", [(32, 8), (64, 8), (32, 16)])
 def test_prefill_split_ragged_tiles_many_sequences(n_q, n_kv):
     """Several sequences whose chunks end inside a row tile (and one that is a
