@@ -314,6 +314,27 @@ def test_prefill_one_chunk_equals_two_chunks():
     assert_close(one.cpu().numpy(), two.astype(np.float64), abs_tol=2e-3, what="chunk split")
 
 
+def test_prefill_bad_block_is_masked_and_flagged():
+    """An invalid block id in the first and in a later key tile of one sequence's
+    table (unsplit chunk): its keys are masked, the status word flags it, the
+    outputs stay finite, and the other sequence matches the oracle."""
+    wl, batch = W.make_custom(32, 8, [1400, 1000], q_lens=[300, 200], seed=45, materialize_logical=False)
+    d = DevWorkload(wl)
+    d.append()
+    tables = batch.block_tables.copy()
+    tables[0, 2] = wl.k_cache.shape[0] + 5
+    tables[0, 40] = -3
+    t = torch()
+    ws0 = t.zeros(256, dtype=t.uint8, device="cuda")  # the status word alone: the unsplit kernel
+    out, ws = d.prefill(batch, tables=tables, workspace=ws0)
+    assert status_word(ws) & P.PKV_STATUS_BAD_BLOCK_ID
+    o = out.cpu().numpy()
+    assert np.all(np.isfinite(o))
+    sub = W.Batch(q=batch.q[300:], cu_q_lens=np.array([0, 200], np.int32), block_tables=batch.block_tables[1:],
+                  context_lens=batch.context_lens[1:])
+    assert_close(o[300:], oracle_attention(wl, sub), what="sequence beside the bad blocks")
+
+
 def test_prefill_flags_inconsistent_lengths():
     t = torch()
     wl, batch = W.make_custom(32, 8, [64, 64], q_lens=[16, 16], seed=44, materialize_logical=False)
