@@ -461,7 +461,12 @@ def run_ours(args):
 
     if rank == 0:
         peak, peak_src = measured_peaks()
-        achieved = kv_bytes / (decode_ms / 1e3) / 1e9
+        # The dominant kernel's launch time: a decode-only step is one call (the decode
+        # kernel with the append, then the merge), so the timed region itself gives it
+        # (events around the whole loop); with other kernels in the step (the mixed
+        # batch) the sampled pass with events around each call does.
+        roof_ms = ms_per_step if fused else decode_ms
+        achieved = kv_bytes / (roof_ms / 1e3) / 1e9
         cpu = None
         if world == 1:
             gbs, sps, sdesc, threads, reps, per_step = time_oracle(wl, budget_s=args.cpu_budget)
@@ -493,9 +498,12 @@ def run_ours(args):
                          "frac": round(achieved / peak, 4), "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                          if peak_src == "measured" else "fallback 6.8 TB/s",
                          "traffic": _profiled_traffic(args.workload),
-                         "bytes_per_launch": kv_bytes, "avg_launch_ms": round(decode_ms, 5),
+                         "bytes_per_launch": kv_bytes, "avg_launch_ms": round(roof_ms, 5),
                          "append_avg_ms": round(append_ms, 5),
-                         "timing": f"CUDA events around each call on {nsample} steps after the timed loop"},
+                         "timing": ("CUDA events around the timed loop / steps (one step = one call: the decode "
+                                    "kernel with the append, then the merge kernel)") if fused else
+                         f"CUDA events around each call on {nsample} steps after the timed loop",
+                         "avg_call_ms_events_each_call": round(decode_ms, 5)},
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": bi,
                     "d2h_bytes_per_step": bo, "ms_per_step": round(e2e_t / args.steps * 1e3, 5)},
